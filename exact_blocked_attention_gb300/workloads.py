@@ -1,0 +1,193 @@
+"""Seeded synthetic inputs for the attention workloads.
+
+This module only draws numbers: shapes, value distributions, cache lengths,
+logical positions and mask patterns.  It holds none of the attention
+arithmetic, and it is the one module that both the CUDA path's callers and the
+oracle's callers share.  Everything is generated on the CPU from fixed seeds
+(numpy PCG64, split into a fixed number of independent streams so that the
+result does not depend on the thread count), then cast to the workload dtype.
+
+Workloads (the problem statement of "Chapter 33: inference compute
+optimisation" §33.2: single-head Q [T_q, d_h], K [T_k, d_h], V [T_k, d_v], an
+additive bias M_j, grouped heads, and the cached-decoding positions of
+"Generation and Caching with the Same Model"):
+
+  tiny_fp32     1 seq, 1 head, d=64, T_q=1 at position T_k-1, T_k=1000, fp32
+  decode_gqa    batch 32, 32 query / 8 KV heads, d=128, T_q=1, cache lengths
+                uniform in [512, 8192], query at len-1, bf16
+  long_decode   batch 1, 32/8 heads, d=128, T_q=1, T_k=131072, 1% of key
+                positions scaled x3 (sharp maxima), bf16
+  spec_verify   batch 8, 64/8 heads, d=128, T_q=5 rows at L..L+4 (L uniform in
+                [1024, 32768], cache length L+5), a {0,-inf} bias that masks
+                random 128-key blocks of 10% of the sequences and every key of
+                1% of the (sequence, row) pairs, bf16
+  prefill       batch 2, 32 heads (MHA), d=128, T_q=T_k=8192, row i at i, bf16
+
+Each has a reduced twin (``small=True``) that the fp64 oracle finishes in
+seconds while still spanning several key tiles and a ragged tail.
+"""
+from __future__ import annotations
+
+import math
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field, replace
+
+import numpy as np
+import torch
+
+_STREAMS = 64  # independent generator streams per array (fixed, thread-count free)
+
+
+@dataclass(frozen=True)
+class Spec:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Tq: int
+    Tmax: int
+    d: int
+    dtype: str                   # "bf16" or "f32"
+    lens: tuple                  # ("fixed", n) | ("uniform", lo, hi) | ("verify", lo, hi)
+    pos: str                     # "last" | "verify" | "causal"
+    seed: int
+    sharp_frac: float = 0.0      # fraction of key positions whose K is scaled
+    sharp_gain: float = 1.0
+    bias: str = "none"           # "none" | "verify_blocks"
+    bias_seq_frac: float = 0.0
+    bias_block: int = 128
+    bias_block_frac: float = 0.0
+    masked_row_frac: float = 0.0
+    notes: str = field(default="", compare=False)
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+SPECS = {
+    "tiny_fp32": Spec("tiny_fp32", 1, 1, 1, 1, 1000, 64, "f32", ("fixed", 1000), "last", 0),
+    "decode_gqa": Spec("decode_gqa", 32, 32, 8, 1, 8192, 128, "bf16", ("uniform", 512, 8192), "last", 1),
+    "long_decode": Spec("long_decode", 1, 32, 8, 1, 131072, 128, "bf16", ("fixed", 131072), "last", 2,
+                        sharp_frac=0.01, sharp_gain=3.0),
+    "spec_verify": Spec("spec_verify", 8, 64, 8, 5, 32776, 128, "bf16", ("verify", 1024, 32768), "verify", 3,
+                        bias="verify_blocks", bias_seq_frac=0.10, bias_block=128, bias_block_frac=0.10,
+                        masked_row_frac=0.01),
+    "prefill": Spec("prefill", 2, 32, 32, 8192, 8192, 128, "bf16", ("fixed", 8192), "causal", 5),
+}
+
+# Reduced twins: same structure, sizes the fp64 oracle covers in seconds, still
+# several 64/128-key tiles per split and a ragged tail.
+SMALL = {
+    "tiny_fp32": SPECS["tiny_fp32"],
+    "decode_gqa": replace(SPECS["decode_gqa"], B=3, Hq=8, Hkv=2, Tmax=1000, lens=("uniform", 1, 1000)),
+    "long_decode": replace(SPECS["long_decode"], B=1, Hq=8, Hkv=2, Tmax=5003, lens=("fixed", 5003)),
+    "spec_verify": replace(SPECS["spec_verify"], B=3, Hq=16, Hkv=2, Tmax=1290,
+                           lens=("verify", 300, 1285), bias_seq_frac=0.34, masked_row_frac=0.07),
+    "prefill": replace(SPECS["prefill"], B=1, Hq=2, Hkv=2, Tq=333, Tmax=333, lens=("fixed", 333)),
+}
+
+
+def spec(name: str, small: bool = False) -> Spec:
+    return (SMALL if small else SPECS)[name]
+
+
+def _normal(shape, seed: int, tag: int) -> np.ndarray:
+    """Standard normal float32 array, deterministic for (seed, tag)."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.float32)
+    kids = np.random.SeedSequence([seed, tag]).spawn(_STREAMS)
+    bounds = np.linspace(0, n, _STREAMS + 1).astype(np.int64)
+
+    def fill(i):
+        g = np.random.Generator(np.random.PCG64(kids[i]))
+        g.standard_normal(out=out[bounds[i]:bounds[i + 1]], dtype=np.float32)
+
+    with ThreadPoolExecutor(8) as ex:
+        list(ex.map(fill, range(_STREAMS)))
+    return out.reshape(shape)
+
+
+def _cast(a: np.ndarray, dtype: str) -> torch.Tensor:
+    t = torch.from_numpy(a)
+    return t.to(torch.bfloat16) if dtype == "bf16" else t.clone()
+
+
+def generate(s: Spec, poison_padding: float | None = None) -> dict:
+    """Draw one batch of inputs for workload ``s`` on the CPU.
+
+    Returns q, k, v (torch, bf16 or f32), seqlens int32 [B], qpos int32 [B,T_q],
+    bias (float32 [B,1,T_q,T_max] or None), scale, and the spec.  Cache rows
+    at or beyond a sequence's length are drawn like the rest unless
+    ``poison_padding`` is given (e.g. float('nan')), in which case they hold it.
+    """
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([s.seed, 99])))
+    kind = s.lens[0]
+    if kind == "fixed":
+        lens = np.full(s.B, s.lens[1], dtype=np.int64)
+    elif kind == "uniform":
+        lens = rng.integers(s.lens[1], s.lens[2] + 1, size=s.B)
+    elif kind == "verify":
+        # history L uniform in [lo, hi]; the cache also holds the T_q new rows
+        L = rng.integers(s.lens[1], s.lens[2] + 1, size=s.B)
+        lens = L + s.Tq
+    else:
+        raise ValueError(kind)
+    lens = np.minimum(lens, s.Tmax)
+
+    if s.pos == "last":
+        qpos = (lens - 1)[:, None] + np.zeros((1, s.Tq), dtype=np.int64)
+    elif s.pos == "verify":
+        qpos = (lens - s.Tq)[:, None] + np.arange(s.Tq)[None, :]
+    elif s.pos == "causal":
+        qpos = np.broadcast_to(np.arange(s.Tq)[None, :], (s.B, s.Tq)).copy()
+    else:
+        raise ValueError(s.pos)
+
+    q = _normal((s.B, s.Hq, s.Tq, s.d), s.seed, 1)
+    k = _normal((s.B, s.Hkv, s.Tmax, s.d), s.seed, 2)
+    v = _normal((s.B, s.Hkv, s.Tmax, s.d), s.seed, 3)
+    if s.sharp_frac > 0:
+        n_sharp = int(round(s.sharp_frac * s.Tmax))
+        sharp = rng.choice(s.Tmax, size=n_sharp, replace=False)
+        k[:, :, sharp, :] *= s.sharp_gain
+    if poison_padding is not None:
+        for b in range(s.B):
+            k[b, :, lens[b]:, :] = poison_padding
+            v[b, :, lens[b]:, :] = poison_padding
+
+    bias = None
+    if s.bias == "verify_blocks":
+        bias = np.zeros((s.B, 1, s.Tq, s.Tmax), dtype=np.float32)
+        n_seq = max(1, math.ceil(s.bias_seq_frac * s.B))
+        for b in rng.choice(s.B, size=n_seq, replace=False):
+            n_blocks = math.ceil(lens[b] / s.bias_block)
+            n_mask = max(1, math.ceil(s.bias_block_frac * n_blocks))
+            for blk in rng.choice(n_blocks, size=n_mask, replace=False):
+                bias[b, 0, :, blk * s.bias_block:(blk + 1) * s.bias_block] = -np.inf
+        n_rows = max(1, math.ceil(s.masked_row_frac * s.B * s.Tq))
+        for flat in rng.choice(s.B * s.Tq, size=n_rows, replace=False):
+            bias[flat // s.Tq, 0, flat % s.Tq, :] = -np.inf
+
+    return {
+        "q": _cast(q, s.dtype),
+        "k": _cast(k, s.dtype),
+        "v": _cast(v, s.dtype),
+        "seqlens": torch.from_numpy(lens.astype(np.int32)),
+        "qpos": torch.from_numpy(qpos.astype(np.int32)),
+        "bias": None if bias is None else torch.from_numpy(bias),
+        "scale": s.scale,
+        "spec": s,
+    }
+
+
+def kv_bytes(s: Spec, seqlens) -> int:
+    """Algorithmic K+V bytes one call reads: the visible cache rows of every
+    (sequence, KV head), each read once."""
+    elt = 2 if s.dtype == "bf16" else 4
+    lens = np.minimum(np.asarray(seqlens, dtype=np.int64), s.Tmax)
+    return int(lens.sum()) * s.Hkv * s.d * elt * 2
