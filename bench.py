@@ -1,0 +1,434 @@
+"""Benchmark of the exact blocked attention path on GB300.
+
+Default (N=1): the batched GQA decode workload (batch 32, 32 query / 8 KV
+heads, d=128, T_q=1, cache lengths uniform in [512, 8192], bf16).  One step is
+one blkattn_fwd call over the whole batch (split-KV kernel + split-merge
+kernel).  ``value`` is KV-cache GB/s: the algorithmic K+V bytes of the visible
+cache rows (each (sequence, KV head) row read once) over the device time.
+
+The other workloads (tiny fp32, long-context decode, speculative verify,
+causal prefill) are measured in the same run and reported under
+``workloads`` with their own roofline figures.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_blocked_attention_gb300 import workloads  # noqa: E402
+
+HEADLINE = "decode_gqa"
+METRIC = "decode attn KV-cache GB/s (batched GQA decode, bf16)"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j["bf16_tflops"]),
+                "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def describe(s):
+    return (f"{s.name}: B={s.B} Hq={s.Hq} Hkv={s.Hkv} d={s.d} Tq={s.Tq} Tmax={s.Tmax} "
+            f"lens={s.lens} pos={s.pos} {s.dtype}" + (f" bias={s.bias}" if s.bias != "none" else ""))
+
+
+def algorithmic_bytes(s, inp):
+    """K+V of the visible cache rows (once per KV head) + Q + O (+ lse)."""
+    kv = workloads.kv_bytes(s, inp["seqlens"].numpy())
+    elt = 2 if s.dtype == "bf16" else 4
+    q = s.B * s.Hq * s.Tq * s.d * elt
+    o = s.B * s.Hq * s.Tq * (s.d * 4 + 4)  # fp32 out + lse
+    return kv, kv + q + o
+
+
+def causal_flops(s, inp):
+    """4 * d per (row, visible key): QK^T and PV, 2 flops per multiply-add."""
+    lens = inp["seqlens"].numpy().astype(np.int64)
+    pos = inp["qpos"].numpy().astype(np.int64)
+    vis = np.clip(np.minimum(lens[:, None], pos + 1), 0, None)  # [B, Tq]
+    return float(vis.sum()) * s.Hq * 4 * s.d
+
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        if shutil.which("nvidia-smi") is None:
+            return self
+        self.file = tempfile.TemporaryFile(mode="w+")
+        self.proc = subprocess.Popen(
+            ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+             "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.file is None:
+            return None
+        self.file.seek(0)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, flag in zip(names, parts[4:8]):
+                if flag.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+class Runner:
+    """Inputs resident on the device plus the call the user makes."""
+
+    def __init__(self, name, seed_offset=0):
+        from exact_blocked_attention_gb300 import blkattn
+        self.blkattn = blkattn
+        s = workloads.spec(name)
+        if seed_offset:
+            s = workloads.replace(s, seed=s.seed + 1000 * seed_offset)
+        self.s = s
+        self.cpu = workloads.generate(s)
+        self.dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in self.cpu.items()}
+        self.out = torch.empty(s.B, s.Hq, s.Tq, s.d, device="cuda")
+        self.lse = torch.empty(s.B, s.Hq, s.Tq, device="cuda")
+        self.plan = blkattn.debug_plan(s.B, s.Hq, s.Hkv, s.Tq, s.Tmax, s.d,
+                                       torch.bfloat16 if s.dtype == "bf16" else torch.float32,
+                                       torch.cuda.get_device_properties(0).multi_processor_count)
+
+    def launches_per_call(self):
+        return 1 + (1 if self.plan["n_splits"] > 1 else 0)
+
+    def call(self):
+        g = self.dev
+        self.blkattn.fwd(g["q"], g["k"], g["v"], g["seqlens"], g["qpos"], g["bias"], g["scale"],
+                         self.out, self.lse)
+
+    def free(self):
+        del self.dev, self.out, self.lse
+
+
+def time_steps(r: Runner, steps: int, warmup: int, world: int, flush: bool):
+    """Per-step device times (ms) of the whole call and of the main kernel."""
+    blk = r.blkattn
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") if flush else None
+    for _ in range(warmup):
+        r.call()
+    torch.cuda.synchronize()
+    split_ev = torch.cuda.Event(enable_timing=True)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(steps):
+        if flush_buf is not None:
+            flush_l2(flush_buf)
+        blk.set_split_event(mids[i])
+        starts[i].record()
+        r.call()
+        ends[i].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    blk.set_split_event(None)
+    total = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    main = [s.elapsed_time(m) for s, m in zip(starts, mids)]
+    return total, main, wall
+
+
+def time_e2e(r: Runner, steps: int, warmup: int):
+    """The user's call end to end: pinned host inputs -> device, fwd, result
+    -> pinned host, every step (device-timed with events)."""
+    g = r.dev
+    host = {k: r.cpu[k].pin_memory() for k in ("q", "k", "v", "seqlens", "qpos")}
+    if r.cpu["bias"] is not None:
+        host["bias"] = r.cpu["bias"].pin_memory()
+    out_h = torch.empty(r.out.shape, dtype=r.out.dtype).pin_memory()
+    lse_h = torch.empty(r.lse.shape, dtype=r.lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+    def step():
+        for k_, t in host.items():
+            g[k_].copy_(t, non_blocking=True)
+        r.call()
+        out_h.copy_(r.out, non_blocking=True)
+        lse_h.copy_(r.lse, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps, h2d, d2h
+
+
+def roofline_entry(r: Runner, main_ms, peaks, flops=None):
+    s = r.s
+    kv, total_bytes = algorithmic_bytes(s, r.cpu)
+    if s.name == "prefill":
+        achieved = flops / (main_ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "peak_note": f"dense bf16 burst, {peaks['source']}"}
+    achieved = total_bytes / (main_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+            "peak_note": f"HBM copy bandwidth, {peaks['source']}"}
+
+
+def oracle_rate(s, inp, budget_s: float, threads: int = 0):
+    """Time the fp64 oracle on a bounded row sample; return (seconds per full
+    workload, rows sampled, cores used)."""
+    import oracle
+    total_rows = s.B * s.Hq * s.Tq
+    rng = np.random.default_rng(0)
+    cores = oracle.max_threads() if threads <= 0 else threads
+    n = min(total_rows, 64)
+    spent, done = 0.0, 0
+    while True:
+        rows = rng.choice(total_rows, size=n, replace=False)
+        t0 = time.perf_counter()
+        oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"], inp["qpos"], inp["scale"],
+                         bias=inp["bias"], rows=rows, nthreads=threads)
+        spent += time.perf_counter() - t0
+        done += n
+        if spent >= budget_s or done >= total_rows:
+            break
+        n = min(total_rows, n * 2)
+    return spent / done * total_rows, done, cores
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the fp64 CPU oracle on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    s = workloads.spec(HEADLINE)
+    inp = workloads.generate(s)
+    kv, _ = algorithmic_bytes(s, inp)
+    budget = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    import oracle
+    for _ in range(args.warmup):
+        oracle_rate(s, inp, budget / 4)
+    per_step = []
+    rows_total = 0
+    cores = 1
+    for _ in range(args.steps):
+        sec, rows, cores = oracle_rate(s, inp, budget)
+        per_step.append(sec)
+        rows_total += rows
+    sec = statistics.mean(per_step)
+    value = kv / sec / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(s), "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows_total} random query rows over {args.steps} steps, "
+                                   f"scaled to all {s.B * s.Hq * s.Tq} rows"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=HEADLINE, choices=list(workloads.SPECS))
+    ap.add_argument("--no-others", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    rank, local, world = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    torch.cuda.set_device(local)
+    from exact_blocked_attention_gb300 import build as libbuild
+    if rank == 0:
+        libbuild.build()
+    barrier(world)
+    peaks = measured_peaks()
+
+    # ---- headline workload: every rank runs its own batch (weak scaling) ----
+    r = Runner(args.workload, seed_offset=rank)
+    s = r.s
+    kv, total_bytes = algorithmic_bytes(s, r.cpu)
+    in_bytes = sum(t.numel() * t.element_size() for k, t in r.dev.items() if torch.is_tensor(t))
+    flush = in_bytes < 2 * L2_BYTES
+    with ClockSampler(local) as clk:
+        total, main_ms, wall = time_steps(r, args.steps, args.warmup, world, flush)
+    clocks = clk.summary()
+    step_ms = max_over_ranks(sum(total) / len(total), world)
+    main_avg = max_over_ranks(sum(main_ms) / len(main_ms), world)
+    value = kv * world / (step_ms * 1e-3) / 1e9
+    if s.name == "prefill":
+        value = causal_flops(s, r.cpu) * world / (step_ms * 1e-3) / 1e12
+    e2e_ms, h2d, d2h = time_e2e(r, max(3, args.steps // 4), 2)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    e2e_value = kv * world / (e2e_ms * 1e-3) / 1e9
+    roof = roofline_entry(r, main_avg, peaks, causal_flops(s, r.cpu))
+    launches = r.launches_per_call() * args.steps
+    plan = r.plan
+    cpu_inp = r.cpu
+    r.free()
+    torch.cuda.empty_cache()
+
+    line = {
+        "metric": METRIC if s.name == HEADLINE else f"{s.name} throughput",
+        "value": value,
+        "unit": "GB/s" if s.name != "prefill" else "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": s.dtype,
+        "data": "synthetic",
+        "config": {"workload": describe(s), "kv_bytes_per_step": kv, "algorithmic_bytes_per_step": total_bytes,
+                   "l2": "flushed between steps" if flush else f"inputs ({in_bytes / 1e6:.0f} MB) larger than L2",
+                   "plan": plan, "parallelism": f"weak: {world} rank(s), own batch each"},
+        "us_per_call": step_ms * 1e3,
+        "main_kernel_us": main_avg * 1e3,
+        "frac_of_hbm_peak": (total_bytes / (step_ms * 1e-3) / 1e9) / peaks["hbm_gbs"],
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "wall_s_timed": wall,
+    }
+
+    # ---- the other workloads (rank 0 only), each with its own roofline ----
+    if rank == 0 and not args.no_others:
+        others = {}
+        for name in workloads.SPECS:
+            if name == s.name:
+                continue
+            ro = Runner(name)
+            fl = ro.s.name == "prefill"
+            steps_o = 10 if not fl else 5
+            tot, mn, _ = time_steps(ro, steps_o, 3, 1, flush=True)
+            t_ms = sum(tot) / len(tot)
+            m_ms = sum(mn) / len(mn)
+            kvo, tb = algorithmic_bytes(ro.s, ro.cpu)
+            entry = {"workload": describe(ro.s), "us_per_call": t_ms * 1e3, "main_kernel_us": m_ms * 1e3,
+                     "kv_gbs": kvo / (t_ms * 1e-3) / 1e9, "plan": ro.plan,
+                     "roofline": roofline_entry(ro, m_ms, peaks, causal_flops(ro.s, ro.cpu) if fl else None)}
+            if fl:
+                f = causal_flops(ro.s, ro.cpu)
+                entry["tflops"] = f / (t_ms * 1e-3) / 1e12
+                entry["frac_of_bf16_peak"] = entry["tflops"] / peaks["bf16_tflops"]
+                entry["frac_of_bf16_sustained"] = entry["tflops"] / peaks["bf16_tflops_sustained"]
+            else:
+                entry["frac_of_hbm_peak"] = (tb / (t_ms * 1e-3) / 1e9) / peaks["hbm_gbs"]
+            others[name] = entry
+            ro.free()
+            del ro
+            torch.cuda.empty_cache()
+        line["workloads"] = others
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1 only) ----
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sec, rows, cores = oracle_rate(s, cpu_inp, 15.0)
+        line["cpu_baseline"] = {"value": kv / sec / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{rows} random query rows of the same batch, fp64, "
+                                          f"scaled to all {s.B * s.Hq * s.Tq} rows"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,343 @@
+// Host side of libblkattn: the C ABI of include/blkattn.h.
+//
+// Every argument is validated before any CUDA call, so invalid requests fail
+// the same way with or without a GPU.  The split plan is pure integer host
+// arithmetic on sizes the host already knows (T_max, heads, rows, SM count);
+// cache lengths and logical positions are only ever read on the device, so a
+// call never synchronises with the GPU ("Chapter 33: inference compute
+// optimisation" §33.4: host reads of device values cut a capturable region).
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "blkattn.h"
+#include "kernels.h"
+
+namespace {
+
+using blkattn::DecodeConfig;
+using blkattn::Elt;
+using blkattn::FwdParams;
+
+__device__ int g_error_word;  // set by kernels whose bounded waits ran out
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int* err = nullptr;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+cudaEvent_t g_split_event = nullptr;  // measurement hook (blkattn_debug_set_split_event)
+
+// ------------------------------------------------------------ validation
+bool is_float_dtype(int32_t t) { return t == BLKATTN_BF16 || t == BLKATTN_F32; }
+int elt_bytes(int32_t t) { return t == BLKATTN_BF16 ? 2 : 4; }
+
+bool dims_ok(const blkattn_tensor* t, int ndim) {
+  if (t == nullptr || t->ndim != ndim) return false;
+  for (int i = 0; i < ndim; ++i)
+    if (t->sizes[i] < 0 || t->strides[i] < 0) return false;
+  return true;
+}
+
+
+// Integer plan shared by blkattn_fwd and blkattn_debug_plan.
+struct Plan {
+  DecodeConfig cfg;
+  int tile;
+  int64_t ctas;
+  int64_t ws_bytes;
+};
+
+int resident_ctas_per_sm(size_t smem_bytes) {
+  const size_t per_sm = 228 * 1024;
+  const size_t per_cta = smem_bytes + 1024;  // 1 KB the runtime reserves per CTA
+  int n = (int)(per_sm / per_cta);
+  return n < 1 ? 1 : n;
+}
+
+Plan make_plan(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tmax, int d, Elt elt,
+               int sms) {
+  Plan pl;
+  const int64_t rows = (Hq / Hkv) * Tq;
+  int R = 1;
+  while (R < rows && R < 8) R *= 2;
+  pl.cfg.rows_per_cta = R;
+  pl.cfg.row_groups = (int)((rows + R - 1) / R);
+  pl.cfg.warps = 4;
+  pl.cfg.stages = (elt == Elt::BF16) ? 3 : 2;
+  pl.tile = 16 * pl.cfg.warps;
+  const int64_t units = B * Hkv * pl.cfg.row_groups;
+  const int resident = resident_ctas_per_sm(blkattn::decode_smem_bytes(elt, d, pl.cfg));
+  const int64_t target = (int64_t)(sms > 0 ? sms : 148) * resident * 4;  // ~4 waves
+  int64_t chunk;
+  if (units >= target) {
+    chunk = Tmax;
+  } else {
+    chunk = (Tmax * units + target - 1) / target;
+    const int64_t min_chunk = 2 * pl.tile;
+    if (chunk < min_chunk) chunk = min_chunk;
+  }
+  if (const char* env = std::getenv("BLKATTN_CHUNK")) {  // tuning sweeps only
+    const long v = std::strtol(env, nullptr, 10);
+    if (v > 0) chunk = v;
+  }
+  chunk = (chunk + pl.tile - 1) / pl.tile * pl.tile;
+  if (chunk > Tmax) chunk = (Tmax + pl.tile - 1) / pl.tile * pl.tile;
+  if (chunk > 0x40000000) chunk = 0x40000000;
+  pl.cfg.chunk = (int)chunk;
+  pl.cfg.n_splits = (int)((Tmax + chunk - 1) / chunk);
+  pl.ctas = (int64_t)pl.cfg.n_splits * Hkv * B * pl.cfg.row_groups;
+  pl.ws_bytes = 0;
+  if (pl.cfg.n_splits > 1)
+    pl.ws_bytes = B * Hq * Tq * (int64_t)pl.cfg.n_splits * (d + 2) * 4 + 256 * 3;
+  return pl;
+}
+
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BLKATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return BLKATTN_ERR_UNSUPPORTED;
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    if (cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return BLKATTN_ERR_CUDA;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&s.err), g_error_word) != cudaSuccess)
+      return BLKATTN_ERR_CUDA;
+    s.ready = true;
+  }
+  *out = &s;
+  return BLKATTN_OK;
+}
+
+// Grow-only per-device scratch.  Growing while the stream is being captured
+// is refused (a capture may not allocate).
+int ensure_workspace(DeviceState* s, size_t bytes, cudaStream_t stream) {
+  if (bytes <= s->ws_bytes) return BLKATTN_OK;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return BLKATTN_ERR_CUDA;
+  if (cs != cudaStreamCaptureStatusNone) return BLKATTN_ERR_NO_WORKSPACE;
+  if (s->ws) {
+    if (cudaFree(s->ws) != cudaSuccess) return BLKATTN_ERR_CUDA;  // waits for users of the old one
+    s->ws = nullptr;
+    s->ws_bytes = 0;
+  }
+  if (cudaMalloc(&s->ws, bytes) != cudaSuccess) {
+    s->ws = nullptr;
+    return BLKATTN_ERR_CUDA;
+  }
+  s->ws_bytes = bytes;
+  return BLKATTN_OK;
+}
+
+struct Checked {
+  int64_t B, Hq, Hkv, Tq, Tmax, d;
+  Elt elt;
+};
+
+int validate_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
+                 const blkattn_tensor* sl, const blkattn_tensor* qp, const blkattn_tensor* bias,
+                 const blkattn_tensor* out, const blkattn_tensor* lse, Checked* c) {
+  if (!dims_ok(q, 4) || !dims_ok(k, 4) || !dims_ok(v, 4) || !dims_ok(sl, 1) ||
+      !dims_ok(qp, 2) || !dims_ok(out, 4) || !dims_ok(lse, 3))
+    return BLKATTN_ERR_INVALID_ARG;
+  if (bias && !dims_ok(bias, 4)) return BLKATTN_ERR_INVALID_ARG;
+  if (!is_float_dtype(q->dtype) || k->dtype != q->dtype || v->dtype != q->dtype)
+    return BLKATTN_ERR_INVALID_ARG;
+  if (sl->dtype != BLKATTN_I32 || qp->dtype != BLKATTN_I32) return BLKATTN_ERR_INVALID_ARG;
+  if (!is_float_dtype(out->dtype) || lse->dtype != BLKATTN_F32) return BLKATTN_ERR_INVALID_ARG;
+  if (bias && bias->dtype != BLKATTN_F32) return BLKATTN_ERR_INVALID_ARG;
+
+  c->B = q->sizes[0];
+  c->Hq = q->sizes[1];
+  c->Tq = q->sizes[2];
+  c->d = q->sizes[3];
+  c->Hkv = k->sizes[1];
+  c->Tmax = k->sizes[2];
+  const int64_t B = c->B, Hq = c->Hq, Tq = c->Tq, d = c->d, Hkv = c->Hkv, Tmax = c->Tmax;
+  if (k->sizes[0] != B || v->sizes[0] != B || sl->sizes[0] != B || qp->sizes[0] != B ||
+      out->sizes[0] != B || lse->sizes[0] != B)
+    return BLKATTN_ERR_INVALID_ARG;
+  if (out->sizes[1] != Hq || lse->sizes[1] != Hq || v->sizes[1] != Hkv)
+    return BLKATTN_ERR_INVALID_ARG;
+  if (Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0) return BLKATTN_ERR_INVALID_ARG;
+  if (qp->sizes[1] != Tq || out->sizes[2] != Tq || lse->sizes[2] != Tq)
+    return BLKATTN_ERR_INVALID_ARG;
+  if (Tmax < 1 || v->sizes[2] != Tmax) return BLKATTN_ERR_INVALID_ARG;
+  if (k->sizes[3] != d || v->sizes[3] != d || out->sizes[3] != d) return BLKATTN_ERR_INVALID_ARG;
+  if (bias && (bias->sizes[0] != B || bias->sizes[1] != Hq || bias->sizes[2] != Tq ||
+               bias->sizes[3] != Tmax))
+    return BLKATTN_ERR_INVALID_ARG;
+  // cache rows move with 16-byte bulk copies
+  const int eb = elt_bytes(q->dtype);
+  for (const blkattn_tensor* t : {k, v}) {
+    if (t->strides[3] != 1) return BLKATTN_ERR_INVALID_ARG;
+    for (int i = 0; i < 3; ++i)
+      if ((t->strides[i] * eb) % 16 != 0) return BLKATTN_ERR_INVALID_ARG;
+  }
+  const bool empty = (B == 0 || Tq == 0);
+  if (!empty) {
+    for (const blkattn_tensor* t : {q, k, v, sl, qp, out, lse})
+      if (t->data == nullptr) return BLKATTN_ERR_INVALID_ARG;
+    if (bias && bias->data == nullptr) return BLKATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(k->data) | reinterpret_cast<uintptr_t>(v->data)) % 16 != 0)
+      return BLKATTN_ERR_INVALID_ARG;
+  }
+  // 32-bit index ranges used on the device, grid limits
+  if (B > 0x7fffffff || Hq > 0xffff || Hkv > 0xffff || Tq > 0x7fffffff || Tmax > 0x7fffffff)
+    return BLKATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return BLKATTN_ERR_UNSUPPORTED;
+  c->elt = (q->dtype == BLKATTN_BF16) ? Elt::BF16 : Elt::F32;
+  return BLKATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* blkattn_status_string(int status) {
+  switch (status) {
+    case BLKATTN_OK: return "ok";
+    case BLKATTN_ERR_INVALID_ARG: return "invalid argument (shape, dtype, stride, alignment or head grouping)";
+    case BLKATTN_ERR_UNSUPPORTED: return "unsupported configuration (head dim, dtype or size)";
+    case BLKATTN_ERR_CUDA: return "CUDA runtime or launch error";
+    case BLKATTN_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait timed out";
+    case BLKATTN_ERR_NO_WORKSPACE: return "workspace would have to grow during stream capture";
+  }
+  return "unknown status";
+}
+
+int blkattn_debug_plan(int64_t B, int64_t H_q, int64_t H_kv, int64_t T_q, int64_t T_max,
+                       int64_t d, int32_t dtype, int32_t num_sms, blkattn_plan* plan) {
+  if (plan == nullptr || B < 0 || H_q <= 0 || H_kv <= 0 || H_q % H_kv != 0 || T_q < 0 ||
+      T_max < 1 || (d != 64 && d != 128) || !is_float_dtype(dtype) || num_sms <= 0)
+    return BLKATTN_ERR_INVALID_ARG;
+  const Plan pl = make_plan(B, H_q, H_kv, T_q, T_max, (int)d,
+                            dtype == BLKATTN_BF16 ? Elt::BF16 : Elt::F32, num_sms);
+  plan->kernel = 0;
+  plan->rows_per_cta = pl.cfg.rows_per_cta;
+  plan->row_groups = pl.cfg.row_groups;
+  plan->chunk_keys = pl.cfg.chunk;
+  plan->n_splits = pl.cfg.n_splits;
+  plan->tile_keys = pl.tile;
+  plan->ctas = pl.ctas;
+  plan->workspace_bytes = pl.ws_bytes;
+  return BLKATTN_OK;
+}
+
+int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
+                const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos,
+                const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out,
+                const blkattn_tensor* lse, blkattn_stream_t stream_) {
+  Checked c;
+  int st = validate_fwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, out, lse, &c);
+  if (st != BLKATTN_OK) return st;
+  if (c.B == 0 || c.Tq == 0) return BLKATTN_OK;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != BLKATTN_OK) return st;
+  const Plan pl = make_plan(c.B, c.Hq, c.Hkv, c.Tq, c.Tmax, (int)c.d, c.elt, ds->sms);
+  if (c.B * pl.cfg.row_groups > 65535) return BLKATTN_ERR_UNSUPPORTED;
+  if (pl.ws_bytes > 0) {
+    st = ensure_workspace(ds, (size_t)pl.ws_bytes, stream);
+    if (st != BLKATTN_OK) return st;
+  }
+
+  const int eb = elt_bytes(q->dtype);
+  FwdParams p;
+  std::memset(&p, 0, sizeof p);
+  p.q = q->data;
+  p.q_sb = q->strides[0]; p.q_sh = q->strides[1]; p.q_si = q->strides[2]; p.q_sd = q->strides[3];
+  p.k = static_cast<const char*>(k->data);
+  p.v = static_cast<const char*>(v->data);
+  p.k_sb = k->strides[0] * eb; p.k_sh = k->strides[1] * eb; p.k_st = k->strides[2] * eb;
+  p.v_sb = v->strides[0] * eb; p.v_sh = v->strides[1] * eb; p.v_st = v->strides[2] * eb;
+  p.seqlens = static_cast<const int32_t*>(seqlens_k->data);
+  p.sl_s = seqlens_k->strides[0];
+  p.qpos = static_cast<const int32_t*>(q_logical_pos->data);
+  p.qp_sb = q_logical_pos->strides[0]; p.qp_si = q_logical_pos->strides[1];
+  if (mask_bias) {
+    p.bias = static_cast<const float*>(mask_bias->data);
+    p.bi_sb = mask_bias->strides[0]; p.bi_sh = mask_bias->strides[1];
+    p.bi_si = mask_bias->strides[2]; p.bi_sj = mask_bias->strides[3];
+  }
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.out = out->data;
+  p.out_bf16 = out->dtype == BLKATTN_BF16;
+  p.o_sb = out->strides[0]; p.o_sh = out->strides[1]; p.o_si = out->strides[2]; p.o_sd = out->strides[3];
+  p.lse = static_cast<float*>(lse->data);
+  p.l_sb = lse->strides[0]; p.l_sh = lse->strides[1]; p.l_si = lse->strides[2];
+  p.B = (int)c.B; p.Hq = (int)c.Hq; p.Hkv = (int)c.Hkv; p.G = (int)(c.Hq / c.Hkv);
+  p.Tq = (int)c.Tq; p.Tmax = (int)c.Tmax;
+  p.rows_per_head = (int)(p.G * c.Tq);
+  p.row_groups = pl.cfg.row_groups;
+  p.chunk = pl.cfg.chunk;
+  p.n_splits = pl.cfg.n_splits;
+  if (pl.cfg.n_splits > 1) {
+    const int64_t n = c.B * c.Hq * c.Tq * (int64_t)pl.cfg.n_splits;
+    char* base = static_cast<char*>(ds->ws);
+    p.ws_m = reinterpret_cast<float*>(base);
+    p.ws_l = reinterpret_cast<float*>(base + ((n * 4 + 255) / 256) * 256);
+    p.ws_u = reinterpret_cast<float*>(base + 2 * ((n * 4 + 255) / 256) * 256);
+  }
+  p.err = ds->err;
+
+  if (blkattn::launch_decode_split(p, c.elt, (int)c.d, pl.cfg, stream) != cudaSuccess)
+    return BLKATTN_ERR_CUDA;
+  if (g_split_event != nullptr && cudaEventRecord(g_split_event, stream) != cudaSuccess)
+    return BLKATTN_ERR_CUDA;
+  if (pl.cfg.n_splits > 1 && blkattn::launch_split_merge(p, (int)c.d, stream) != cudaSuccess)
+    return BLKATTN_ERR_CUDA;
+  return BLKATTN_OK;
+}
+
+int blkattn_merge(const blkattn_states* a, const blkattn_states* b, const blkattn_states* out,
+                  blkattn_stream_t stream_) {
+  if (!a || !b || !out) return BLKATTN_ERR_INVALID_ARG;
+  if (a->rows != b->rows || a->rows != out->rows || a->d_v != b->d_v || a->d_v != out->d_v)
+    return BLKATTN_ERR_INVALID_ARG;
+  if (a->rows < 0 || a->d_v < 1 || a->d_v > 1024) return BLKATTN_ERR_INVALID_ARG;
+  for (const blkattn_states* s : {a, b, out})
+    if (s->u_row_stride < s->d_v) return BLKATTN_ERR_INVALID_ARG;
+  if (a->rows == 0) return BLKATTN_OK;
+  for (const blkattn_states* s : {a, b, out})
+    if (s->m == nullptr || s->u == nullptr) return BLKATTN_ERR_INVALID_ARG;
+  blkattn::MergeParams p;
+  p.am = a->m; p.al = a->l; p.au = a->u; p.a_us = a->u_row_stride;
+  p.bm = b->m; p.bl = b->l; p.bu = b->u; p.b_us = b->u_row_stride;
+  p.om = out->m; p.ol = out->l; p.ou = out->u; p.o_us = out->u_row_stride;
+  p.rows = a->rows;
+  p.d = a->d_v;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (blkattn::launch_state_merge(p, stream) != cudaSuccess) return BLKATTN_ERR_CUDA;
+  return BLKATTN_OK;
+}
+
+void blkattn_debug_set_split_event(void* ev) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_split_event = static_cast<cudaEvent_t>(ev);
+}
+
+int blkattn_check_device_error(blkattn_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return BLKATTN_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof word) != cudaSuccess) return BLKATTN_ERR_CUDA;
+  if (word != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof zero) != cudaSuccess) return BLKATTN_ERR_CUDA;
+    return BLKATTN_ERR_DEVICE_TIMEOUT;
+  }
+  return BLKATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,76 @@
+// Parameter blocks and launcher declarations shared by the host API and the
+// kernel translation units.  Internal to libblkattn (not part of the C ABI).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace blkattn {
+
+enum class Elt : int { BF16 = 1, F32 = 2 };
+
+// One blkattn_fwd call, after validation.  K/V strides are in BYTES, all the
+// others in elements.
+struct FwdParams {
+  // query rows
+  const void* q;
+  int64_t q_sb, q_sh, q_si, q_sd;
+  // cache (device pointers, 16-byte aligned rows)
+  const char* k;
+  const char* v;
+  int64_t k_sb, k_sh, k_st;
+  int64_t v_sb, v_sh, v_st;
+  // lengths and logical positions (device int32)
+  const int32_t* seqlens;
+  int64_t sl_s;
+  const int32_t* qpos;
+  int64_t qp_sb, qp_si;
+  // optional additive bias (device f32), 0-strides broadcast
+  const float* bias;
+  int64_t bi_sb, bi_sh, bi_si, bi_sj;
+  float scale_log2;  // scale * log2(e): scores are kept in base-2 units
+  // results
+  void* out;
+  int out_bf16;
+  int64_t o_sb, o_sh, o_si, o_sd;
+  float* lse;
+  int64_t l_sb, l_sh, l_si;
+  // sizes
+  int B, Hq, Hkv, G, Tq, Tmax;
+  int rows_per_head;  // G * Tq query rows read one KV head
+  int row_groups;     // CTAs along those rows
+  int chunk;          // keys per split
+  int n_splits;
+  // per-split partial states (only when n_splits > 1): index row*n_splits+s,
+  // row = (b*Hq + h)*Tq + i; m and l in base-2 units, u [.., d]
+  float* ws_m;
+  float* ws_l;
+  float* ws_u;
+  int* err;  // device error word
+};
+
+// Split-KV kernel configuration chosen by the planner.
+struct DecodeConfig {
+  int rows_per_cta;  // 1, 2, 4 or 8
+  int warps;         // consumer warps; keys per stage = 16 * warps
+  int stages;
+  int chunk;
+  int n_splits;
+  int row_groups;
+};
+
+cudaError_t launch_decode_split(const FwdParams& p, Elt elt, int d, const DecodeConfig& cfg,
+                                cudaStream_t stream);
+cudaError_t launch_split_merge(const FwdParams& p, int d, cudaStream_t stream);
+
+struct MergeParams {
+  const float* am; const float* al; const float* au; int64_t a_us;
+  const float* bm; const float* bl; const float* bu; int64_t b_us;
+  float* om; float* ol; float* ou; int64_t o_us;
+  int64_t rows;
+  int d;
+};
+cudaError_t launch_state_merge(const MergeParams& p, cudaStream_t stream);
+
+size_t decode_smem_bytes(Elt elt, int d, const DecodeConfig& cfg);
+
+}  // namespace blkattn

@@ -1,0 +1,189 @@
+/*
+ * libblkattn — exact blocked attention over a KV cache on GB300 (sm_103a).
+ *
+ * C ABI.  No torch types, no C++ types; every pointer in a descriptor is a
+ * DEVICE pointer on the current CUDA device unless stated otherwise.  The
+ * caller owns every buffer it passes.  No call reads device memory from the
+ * host (cache lengths and positions stay on the device), so a call can be
+ * captured in a CUDA graph once the library's workspace has been sized by an
+ * earlier uncaptured call of the same or a larger problem.
+ *
+ * What is computed ("Chapter 33: inference compute optimisation", §33.2,
+ * eq. 33.2): for every query row (b, h, i)
+ *
+ *     z_j = scale * (q[b,h,i,:] . k[b,hk,j,:]) + M[b,h,i,j]
+ *     out[b,h,i,:] = sum_j e^{z_j} v[b,hk,j,:] / sum_j e^{z_j}
+ *     lse[b,h,i]   = ln sum_j e^{z_j}
+ *
+ * over the VALID keys j, with hk = floor(h / (H_q / H_kv)) (grouped-query
+ * heads, contiguous groups; the head-grouping condition of §33.3 "interface,
+ * backend and correctness conditions").  Key j is valid for row (b, h, i) iff
+ *
+ *     j < min(seqlens_k[b], T_max)              (the key exists in the cache)
+ *     j <= q_logical_pos[b, i]                  (causal by LOGICAL position)
+ *     M[b,h,i,j] != -inf                        (additive mask, when given)
+ *
+ * Logical positions follow "Generation and Caching with the Same Model"
+ * (cache reuse: after a cache of length t the new queries sit at t, t+1, ...)
+ * and §33.3 of Chapter 33 (a decode row must not be aligned from zero).  A
+ * non-causal row is expressed with q_logical_pos >= seqlens_k[b] - 1.
+ *
+ * A row with no valid key gets out = 0 (all +0.0) and lse = -inf: the defined
+ * output that §33.2 asks an interface to fix for a fully masked row (the
+ * paragraph after eq. 33.5, and Exercise 33.3).  No NaN is produced for it.
+ *
+ * The result is computed with the sufficient statistics (m, l, u) of eq. 33.3
+ * and the merge rule of eqs. 33.4–33.5 (Algorithm 33.1): exact up to rounding
+ * order; the T_q x T_k score matrix is never written to memory.
+ */
+#ifndef BLKATTN_H_
+#define BLKATTN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle (cudaStream_t / CUstream); NULL = legacy stream. */
+typedef struct CUstream_st* blkattn_stream_t;
+
+/* ---------------------------------------------------------------- status */
+enum {
+  BLKATTN_OK = 0,
+  BLKATTN_ERR_INVALID_ARG = -1,   /* bad shape, dtype, stride, alignment, H_q % H_kv, NULL */
+  BLKATTN_ERR_UNSUPPORTED = -2,   /* a valid request this build has no kernel for (e.g. d not in {64,128}) */
+  BLKATTN_ERR_CUDA = -3,          /* a CUDA runtime call or kernel launch failed */
+  BLKATTN_ERR_DEVICE_TIMEOUT = -4,/* a kernel's bounded wait ran out (reported by blkattn_check_device_error) */
+  BLKATTN_ERR_NO_WORKSPACE = -5   /* the workspace must grow while the stream is being captured */
+};
+
+/* ---------------------------------------------------------------- tensors */
+enum {
+  BLKATTN_BF16 = 1,  /* bfloat16 */
+  BLKATTN_F32 = 2,   /* IEEE binary32 */
+  BLKATTN_I32 = 3    /* int32 */
+};
+
+/*
+ * A strided view.  sizes/strides are in ELEMENTS; a stride of 0 broadcasts.
+ * Only the first ndim entries are read.
+ */
+typedef struct {
+  void* data;
+  int32_t dtype;      /* BLKATTN_BF16 | BLKATTN_F32 | BLKATTN_I32 */
+  int32_t ndim;
+  int64_t sizes[4];
+  int64_t strides[4];
+} blkattn_tensor;
+
+/*
+ * blkattn_fwd — exact attention of T_q query rows per sequence over a KV cache.
+ *
+ * q             [B, H_q, T_q, d_h]   bf16 or f32.  Any strides.
+ * k             [B, H_kv, T_max, d_h] same dtype as q.  Last stride 1; the
+ *               other strides and the base address must be multiples of 16
+ *               bytes (rows are moved with bulk asynchronous copies).
+ * v             [B, H_kv, T_max, d_v] same dtype and rules as k; d_v == d_h.
+ * seqlens_k     [B] int32: valid cache length of each sequence (clamped to
+ *               [0, T_max] on the device).
+ * q_logical_pos [B, T_q] int32: logical position of each query row (the same
+ *               for every head of a sequence).  Negative: no key is visible.
+ * mask_bias     NULL, or f32 [B, H_q, T_q, T_max] view (0-strides broadcast)
+ *               holding the additive M_j of eq. 33.2: finite or -inf.  +inf or
+ *               NaN entries are out of contract (the result is then undefined).
+ * scale         multiplies q.k (eq. 33.2 uses 1/sqrt(d_h)).
+ * out           [B, H_q, T_q, d_v] bf16 or f32, any strides: written.
+ * lse           [B, H_q, T_q] f32, any strides: written (natural log).
+ * stream        the stream every kernel of the call is enqueued on.
+ *
+ * Supported: d_h = d_v in {64, 128}; q/k/v all bf16 or all f32.  H_q % H_kv
+ * must be 0.  B, T_q >= 0 (0 is a no-op), T_max >= 1.
+ * Returns BLKATTN_OK after enqueuing the work (asynchronous), or a negative
+ * status without enqueuing anything.  Library-owned scratch (per-split
+ * partial states) comes from a per-device, grow-only workspace; calls on
+ * different streams of one device must not overlap in time.
+ */
+int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k,
+                const blkattn_tensor* v, const blkattn_tensor* seqlens_k,
+                const blkattn_tensor* q_logical_pos,
+                const blkattn_tensor* mask_bias, float scale,
+                const blkattn_tensor* out, const blkattn_tensor* lse,
+                blkattn_stream_t stream);
+
+/*
+ * Attention states of rows, in the sufficient statistics of eq. 33.3:
+ *   m [rows]           f32, the maximum score (natural-log units); -inf = empty
+ *   l [rows]           f32, sum e^{z_j - m}; NULL means "normalised": l = 1 and
+ *                      u holds o = u / l (then m is the row's lse, so the
+ *                      (out, lse) pair blkattn_fwd writes IS a state)
+ *   u [rows, d_v]      f32, sum e^{z_j - m} v_j, row stride u_row_stride elements
+ * An empty state (no valid key) is m = -inf; its l and u are not read.
+ */
+typedef struct {
+  float* m;
+  float* l;
+  float* u;
+  int64_t rows;
+  int32_t d_v;
+  int64_t u_row_stride;
+} blkattn_states;
+
+/*
+ * blkattn_merge — row-wise merge of two disjoint-key states, eqs. 33.4–33.5
+ * (m = max(m_a, m_b); l and u rescaled by e^{m_x - m}), with the valid-flag
+ * rule: an empty side contributes nothing and -inf - (-inf) is never formed.
+ * out may alias a or b.  If out->l is NULL the result is written normalised
+ * (u <- u / l, m <- m + ln l); an empty result is then u = 0, m = -inf.
+ * rows and d_v must agree across a, b and out; d_v in [1, 1024].
+ * Asynchronous on stream; returns a status as blkattn_fwd does.
+ */
+int blkattn_merge(const blkattn_states* a, const blkattn_states* b,
+                  const blkattn_states* out, blkattn_stream_t stream);
+
+/* Human-readable text for a status code (static storage). */
+const char* blkattn_status_string(int status);
+
+/*
+ * Test hook: synchronises the stream, then reads and clears the library's
+ * device error word.  Returns BLKATTN_OK, BLKATTN_ERR_DEVICE_TIMEOUT when a
+ * kernel gave up a bounded wait, or BLKATTN_ERR_CUDA if the sync failed.
+ */
+int blkattn_check_device_error(blkattn_stream_t stream);
+
+/*
+ * Host-only view of the split plan blkattn_fwd would use (no CUDA call).
+ * Keys [0, T_max) are cut into n_splits consecutive chunks of chunk_keys
+ * (the last may be shorter); rows_per_cta query rows of one KV head share a
+ * CTA.  kernel: 0 = CUDA-core split-KV kernel, 1 = tensor-core kernel.
+ * Returns BLKATTN_OK or BLKATTN_ERR_INVALID_ARG.
+ */
+typedef struct {
+  int32_t kernel;
+  int32_t rows_per_cta;
+  int32_t row_groups;     /* CTAs along the query rows of one KV head */
+  int32_t chunk_keys;
+  int32_t n_splits;
+  int32_t tile_keys;      /* keys per pipeline stage */
+  int64_t ctas;           /* grid size */
+  int64_t workspace_bytes;
+} blkattn_plan;
+
+int blkattn_debug_plan(int64_t B, int64_t H_q, int64_t H_kv, int64_t T_q,
+                       int64_t T_max, int64_t d, int32_t dtype,
+                       int32_t num_sms, blkattn_plan* plan);
+
+/*
+ * Measurement hook: when ev is not NULL (a cudaEvent_t of the calling
+ * process), every later blkattn_fwd records it on its stream right after the
+ * main attention kernel and before the split-merge kernel, so a caller can
+ * time the two kernels separately with events on the launch stream.  NULL
+ * switches it off.  Process-wide; not for concurrent callers.
+ */
+void blkattn_debug_set_split_event(void* ev);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BLKATTN_H_ */

@@ -1,0 +1,192 @@
+"""Host-side checks of the C ABI: the library builds and loads, exports every
+function include/blkattn.h declares, rejects invalid requests before any CUDA
+call, and plans splits that partition the cache exactly once.  No GPU needed.
+"""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+import torch
+
+from exact_blocked_attention_gb300 import blkattn, workloads
+from exact_blocked_attention_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return blkattn.load()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "blkattn.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:int|void|const char\*)\s+(blkattn_\w+)\s*\(", text, re.M)))
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert set(blkattn.EXPORTED) <= set(names)
+    for name in names:
+        assert hasattr(lib, name), f"{name} not exported"
+
+
+def test_status_strings(lib):
+    for st in (0, -1, -2, -3, -4, -5):
+        assert blkattn.status_string(st)
+    assert blkattn.status_string(-99) == "unknown status"
+
+
+class FakeTensor:
+    """Descriptor with a fake (never dereferenced) device address."""
+
+    def __init__(self, shape, dtype, strides=None, addr=0x10000):
+        self.shape = tuple(shape)
+        self.dtype = dtype
+        if strides is None:
+            strides, acc = [], 1
+            for s in reversed(self.shape):
+                strides.insert(0, acc)
+                acc *= s
+        self.strides = tuple(strides)
+        self.addr = addr
+
+    def desc(self):
+        d = blkattn.Tensor()
+        d.data = self.addr
+        d.dtype = {torch.bfloat16: 1, torch.float32: 2, torch.int32: 3}[self.dtype]
+        d.ndim = len(self.shape)
+        for i, (s, st) in enumerate(zip(self.shape, self.strides)):
+            d.sizes[i] = s
+            d.strides[i] = st
+        return d
+
+
+def call_fwd(lib, q, k, v, sl, qp, bias, out, lse):
+    ds = [None if t is None else t.desc() for t in (q, k, v, sl, qp, bias, out, lse)]
+    ref = lambda d: None if d is None else ctypes.byref(d)
+    return lib.blkattn_fwd(ref(ds[0]), ref(ds[1]), ref(ds[2]), ref(ds[3]), ref(ds[4]), ref(ds[5]),
+                           ctypes.c_float(0.1), ref(ds[6]), ref(ds[7]), None)
+
+
+def good_args(B=2, Hq=8, Hkv=2, Tq=3, Tmax=100, d=128, dt=torch.bfloat16):
+    return dict(
+        q=FakeTensor((B, Hq, Tq, d), dt), k=FakeTensor((B, Hkv, Tmax, d), dt),
+        v=FakeTensor((B, Hkv, Tmax, d), dt), sl=FakeTensor((B,), torch.int32),
+        qp=FakeTensor((B, Tq), torch.int32), bias=None,
+        out=FakeTensor((B, Hq, Tq, d), torch.float32), lse=FakeTensor((B, Hq, Tq), torch.float32))
+
+
+@pytest.mark.parametrize("mutate,expect", [
+    (lambda a: a.update(q=FakeTensor((2, 8, 3, 128), torch.int32)), -1),
+    (lambda a: a.update(k=FakeTensor((2, 2, 100, 128), torch.float32)), -1),  # mixed q/k dtypes
+    (lambda a: a.update(k=FakeTensor((2, 3, 100, 128), torch.bfloat16),
+                        v=FakeTensor((2, 3, 100, 128), torch.bfloat16)), -1),  # 8 % 3 != 0
+    (lambda a: a.update(v=FakeTensor((2, 2, 99, 128), torch.bfloat16)), -1),
+    (lambda a: a.update(qp=FakeTensor((2, 4), torch.int32)), -1),
+    (lambda a: a.update(sl=FakeTensor((3,), torch.int32)), -1),
+    (lambda a: a.update(sl=FakeTensor((2,), torch.float32)), -1),
+    (lambda a: a.update(lse=FakeTensor((2, 8, 3), torch.bfloat16)), -1),
+    (lambda a: a.update(out=FakeTensor((2, 8, 3, 64), torch.float32)), -1),
+    (lambda a: a.update(k=FakeTensor((2, 2, 100, 128), torch.bfloat16, strides=(25600, 12800, 128, 2))), -1),
+    (lambda a: a.update(k=FakeTensor((2, 2, 100, 128), torch.bfloat16, strides=(25600, 12803, 128, 1))), -1),
+    (lambda a: a.update(k=FakeTensor((2, 2, 100, 128), torch.bfloat16, addr=0x10008)), -1),  # not 16-B aligned
+    (lambda a: a.update(bias=FakeTensor((2, 8, 3, 99), torch.float32)), -1),
+    (lambda a: a.update(bias=FakeTensor((2, 8, 3, 100), torch.bfloat16)), -1),
+    (lambda a: a.update(q=FakeTensor((2, 8, 3, 128), torch.bfloat16, addr=0)), -1),  # NULL data
+    (lambda a: a.update(**good_args(d=96)), -2),  # head dim without a kernel
+    (lambda a: a.update(q=None), -1),
+], ids=["q-int", "mixed-dtype", "hq-not-multiple", "v-len", "qpos-shape", "seqlens-shape",
+        "seqlens-dtype", "lse-dtype", "out-dim", "k-inner-stride", "k-row-misaligned",
+        "k-base-misaligned", "bias-shape", "bias-dtype", "null-data", "d96", "missing-q"])
+def test_invalid_requests_are_rejected_before_cuda(lib, mutate, expect):
+    a = good_args()
+    mutate(a)
+    assert call_fwd(lib, a["q"], a["k"], a["v"], a["sl"], a["qp"], a["bias"], a["out"], a["lse"]) == expect
+
+
+def test_empty_problem_is_a_no_op(lib):
+    a = good_args(B=0)
+    for t in a.values():
+        if t is not None:
+            t.addr = 0
+    assert call_fwd(lib, a["q"], a["k"], a["v"], a["sl"], a["qp"], None, a["out"], a["lse"]) == 0
+    a = good_args(Tq=0)
+    assert call_fwd(lib, a["q"], a["k"], a["v"], a["sl"], a["qp"], None, a["out"], a["lse"]) == 0
+
+
+def test_merge_rejects_mismatched_states(lib):
+    def st(rows, d, stride=None):
+        s = blkattn.States()
+        s.m, s.l, s.u = 0x1000, None, 0x2000
+        s.rows, s.d_v, s.u_row_stride = rows, d, stride or d
+        return s
+    a, b = st(4, 8), st(5, 8)
+    assert lib.blkattn_merge(ctypes.byref(a), ctypes.byref(b), ctypes.byref(a), None) == -1
+    a, b = st(4, 8), st(4, 8, stride=4)
+    assert lib.blkattn_merge(ctypes.byref(a), ctypes.byref(b), ctypes.byref(a), None) == -1
+    z = st(0, 8)
+    assert lib.blkattn_merge(ctypes.byref(z), ctypes.byref(z), ctypes.byref(z), None) == 0
+
+
+def _check_partition(p, Tmax):
+    chunk, n = p["chunk_keys"], p["n_splits"]
+    assert chunk % p["tile_keys"] == 0 and chunk > 0
+    # consecutive chunks [s*chunk, min((s+1)*chunk, Tmax)) cover [0, Tmax) exactly once
+    covered = []
+    for s in range(n):
+        lo, hi = s * chunk, min((s + 1) * chunk, Tmax)
+        assert lo < hi
+        covered.extend(range(lo, hi))
+    assert covered == list(range(Tmax))
+
+
+@pytest.mark.parametrize("name", list(workloads.SPECS))
+def test_plan_partitions_every_workload(lib, name):
+    for small in (False, True):
+        s = workloads.spec(name, small)
+        p = blkattn.debug_plan(s.B, s.Hq, s.Hkv, s.Tq, s.Tmax, s.d,
+                               torch.bfloat16 if s.dtype == "bf16" else torch.float32, 152)
+        _check_partition(p, s.Tmax)
+        rows = s.G * s.Tq
+        assert p["rows_per_cta"] in (1, 2, 4, 8)
+        assert p["row_groups"] == math.ceil(rows / p["rows_per_cta"])
+        assert p["ctas"] == p["n_splits"] * s.Hkv * s.B * p["row_groups"]
+        if p["n_splits"] > 1:
+            assert p["workspace_bytes"] >= s.B * s.Hq * s.Tq * p["n_splits"] * (s.d + 2) * 4
+        else:
+            assert p["workspace_bytes"] == 0
+
+
+def test_plan_random_shapes(lib):
+    g = torch.Generator().manual_seed(0)
+    for _ in range(300):
+        B = int(torch.randint(1, 40, (1,), generator=g))
+        Hkv = int(torch.randint(1, 9, (1,), generator=g))
+        G = int(torch.randint(1, 9, (1,), generator=g))
+        Tq = int(torch.randint(1, 20, (1,), generator=g))
+        Tmax = int(torch.randint(1, 300000, (1,), generator=g))
+        sms = int(torch.randint(1, 200, (1,), generator=g))
+        p = blkattn.debug_plan(B, Hkv * G, Hkv, Tq, Tmax, 128, torch.bfloat16, sms)
+        _check_partition(p, Tmax)
+
+
+def test_plan_rejects_bad_shapes(lib):
+    with pytest.raises(ValueError):
+        blkattn.debug_plan(1, 6, 4, 1, 100, 128)
+    with pytest.raises(ValueError):
+        blkattn.debug_plan(1, 4, 4, 1, 0, 128)
+
+
+def test_product_path_does_not_touch_the_oracle():
+    pkg = os.path.join(ROOT, "exact_blocked_attention_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle", text, re.M), f
+                assert "attention_oracle" not in text, f

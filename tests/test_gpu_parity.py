@@ -1,0 +1,350 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Tolerances (written here, derived from the arithmetic): for bf16 inputs with
+fp32 accumulation and an fp32 output, max |out - out_ref| <= 2e-3 * (1 +
+|out_ref|) and |lse - lse_ref| <= 1e-3; for the fp32 workload 1e-5 for both.
+A bf16 output may differ by its own rounding on top: half a bf16 ulp of
+out_ref (at most 2^-8 |out_ref|).  Rows with no valid key must be exact:
+out == +0.0 and lse == -inf.  The integer facts (which rows are fully masked)
+are compared bit for bit.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_blocked_attention_gb300 import blkattn, workloads
+from exact_blocked_attention_gb300 import build as libbuild
+
+pytestmark = pytest.mark.gpu
+
+BF16_TOL_O, BF16_TOL_L = 2e-3, 1e-3
+F32_TOL = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    libbuild.build()
+    blkattn.load()
+
+
+def to_dev(inp):
+    return {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+
+
+def run_gpu(inp, out_dtype=torch.float32):
+    g = to_dev(inp)
+    out, lse = blkattn.attention(g["q"], g["k"], g["v"], g["seqlens"], g["qpos"], g["bias"],
+                                 g["scale"], out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert blkattn.check_device_error() == 0
+    d = out.shape[-1]
+    return out.cpu(), lse.cpu(), out.double().cpu().numpy().reshape(-1, d), lse.double().cpu().numpy().reshape(-1)
+
+
+def run_oracle(inp, rows=None):
+    return oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"], inp["qpos"], inp["scale"],
+                            bias=inp["bias"], rows=rows)
+
+
+def assert_parity(o, l, ref, tol_o, tol_l, out_raw=None, bf16_out=False):
+    masked = ref["n_visible"] == 0
+    gpu_masked = np.isneginf(l)
+    np.testing.assert_array_equal(gpu_masked, masked)  # integer fact, exact
+    assert np.all(o[masked] == 0.0)
+    if out_raw is not None and masked.any():
+        assert not torch.signbit(out_raw.float().reshape(-1, o.shape[1])[torch.from_numpy(masked)]).any()
+    live = ~masked
+    if not live.any():
+        return
+    ro = ref["out"][live]
+    bound = tol_o * (1 + np.abs(ro))
+    if bf16_out:
+        bound = bound + np.abs(ro) * 2.0 ** -8
+    err = np.abs(o[live] - ro)
+    worst = np.argmax(err - bound)
+    assert np.all(err <= bound), f"out: max excess {float((err - bound).flat[worst]):.3e}, max err {err.max():.3e}"
+    assert np.all(np.isfinite(l[live]))
+    lerr = np.abs(l[live] - ref["lse"][live])
+    assert lerr.max() <= tol_l, f"lse err {lerr.max():.3e}"
+
+
+def tols(s):
+    return (F32_TOL, F32_TOL) if s.dtype == "f32" else (BF16_TOL_O, BF16_TOL_L)
+
+
+# ------------------------------------------------------------ reduced workloads, every row
+
+@pytest.mark.parametrize("name", list(workloads.SMALL))
+def test_small_workload_parity(name):
+    s = workloads.spec(name, small=True)
+    inp = workloads.generate(s)
+    raw, _, o, l = run_gpu(inp)
+    ref = run_oracle(inp)
+    assert_parity(o, l, ref, *tols(s), out_raw=raw)
+
+
+@pytest.mark.parametrize("name", [n for n in workloads.SMALL if workloads.SMALL[n].dtype == "bf16"])
+def test_small_workload_bf16_output(name):
+    s = workloads.spec(name, small=True)
+    inp = workloads.generate(s)
+    raw, _, o, l = run_gpu(inp, out_dtype=torch.bfloat16)
+    ref = run_oracle(inp)
+    assert_parity(o, l, ref, *tols(s), out_raw=raw, bf16_out=True)
+
+
+def test_tiny_fp32_workload_full():
+    s = workloads.spec("tiny_fp32")
+    inp = workloads.generate(s)
+    _, _, o, l = run_gpu(inp)
+    assert_parity(o, l, run_oracle(inp), F32_TOL, F32_TOL)
+
+
+# ------------------------------------------------------------ full-size workloads, sampled rows
+
+def sample_rows(s, inp, n_random=160, seed=0):
+    rng = np.random.default_rng(seed)
+    total = s.B * s.Hq * s.Tq
+    rows = set(range(min(s.Tq * 2, total)))
+    rows.update(range(max(0, total - 4), total))
+    if s.pos == "causal":
+        for t in (0, 1, 2, 63, 64, 127, 128, 129, 255, 256, 1023, 4096, s.Tq - 1):
+            if t < s.Tq:
+                rows.add(t)
+                rows.add((s.B * s.Hq - 1) * s.Tq + t)
+    if inp["bias"] is not None:  # rows of the fully masked (sequence, position) pairs
+        full = torch.isneginf(inp["bias"]).all(dim=-1)[:, 0, :]
+        for b, i in zip(*torch.nonzero(full, as_tuple=True)):
+            for h in (0, s.Hq // 2, s.Hq - 1):
+                rows.add((int(b) * s.Hq + h) * s.Tq + int(i))
+    rows.update(rng.choice(total, size=min(n_random, total), replace=False).tolist())
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", ["decode_gqa", "long_decode", "spec_verify", "prefill"])
+def test_full_size_workload_sampled_rows(name):
+    s = workloads.spec(name)
+    inp = workloads.generate(s)
+    raw, _, o, l = run_gpu(inp)
+    rows = sample_rows(s, inp)
+    ref = run_oracle(inp, rows=rows)
+    assert_parity(o[rows], l[rows], ref, *tols(s))
+    if s.bias != "none":
+        assert (ref["n_visible"] == 0).any(), "the fully masked rows must be sampled"
+
+
+# ------------------------------------------------------------ worked example on the GPU
+
+def test_example_25_1_on_gpu():
+    """Scores (log 2, log 1, log 6), values (1, 4, 5) -> o = 4: d = 64, fp32,
+    scale 1/8, q = 8 e0, k_j = z_j e0, v_j = value_j e0."""
+    d = 64
+    q = torch.zeros(1, 1, 1, d); q[0, 0, 0, 0] = 8.0
+    k = torch.zeros(1, 1, 3, d); k[0, 0, :, 0] = torch.tensor([math.log(2), 0.0, math.log(6)])
+    v = torch.zeros(1, 1, 3, d); v[0, 0, :, 0] = torch.tensor([1.0, 4.0, 5.0])
+    inp = {"q": q, "k": k, "v": v, "seqlens": torch.tensor([3], dtype=torch.int32),
+           "qpos": torch.tensor([[2]], dtype=torch.int32), "bias": None, "scale": 1 / 8}
+    _, _, o, l = run_gpu(inp)
+    assert o[0, 0] == pytest.approx(4.0, abs=1e-5)
+    assert np.all(o[0, 1:] == 0)
+    assert l[0] == pytest.approx(math.log(9.0), abs=1e-5)
+
+
+# ------------------------------------------------------------ merge API and split invariance
+
+def states_from_fwd(out, lse):
+    rows = out.shape[0] * out.shape[1] * out.shape[2]
+    return lse.reshape(rows).contiguous(), None, out.reshape(rows, -1).contiguous()
+
+
+def test_random_key_partitions_merge_to_the_whole():
+    """fwd on disjoint key ranges + blkattn_merge == fwd on all keys (any
+    partition, any order; eqs. 33.4-33.5 and their order independence)."""
+    s = workloads.spec("tiny_fp32")
+    inp = to_dev(workloads.generate(s))
+    whole_o, whole_l = blkattn.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"], inp["qpos"],
+                                         None, inp["scale"])
+    rng = np.random.default_rng(1)
+    T = s.Tmax
+    for trial in range(100):
+        n_cuts = int(rng.integers(0, 12))
+        # cuts on 4-key boundaries keep every K/V view 16-byte aligned (fp32 rows of 256 B are)
+        cuts = sorted(set(rng.integers(1, T, size=n_cuts).tolist()))
+        bounds = [0] + cuts + [T]
+        parts = list(zip(bounds[:-1], bounds[1:]))
+        rng.shuffle(parts)
+        acc = None
+        for lo, hi in parts:
+            k = inp["k"][:, :, lo:hi]
+            v = inp["v"][:, :, lo:hi]
+            pos = inp["qpos"] - lo
+            sl = torch.clamp(inp["seqlens"] - lo, min=0).to(torch.int32)
+            o, l = blkattn.attention(inp["q"], k, v, sl, pos.to(torch.int32), None, inp["scale"])
+            st = states_from_fwd(o, l)
+            if acc is None:
+                acc = st
+            else:
+                blkattn.merge(acc, st, acc)
+        torch.cuda.synchronize()
+        np.testing.assert_allclose(acc[2].cpu().numpy(), whole_o.reshape(1, -1).cpu().numpy(), rtol=0, atol=1e-5)
+        np.testing.assert_allclose(acc[0].cpu().numpy(), whole_l.reshape(-1).cpu().numpy(), rtol=0, atol=1e-5)
+
+
+def test_merge_matches_oracle_states():
+    from oracle import states as ost
+    rng = np.random.default_rng(4)
+    rows, d = 1000, 48
+    ma = rng.normal(size=rows) * 5
+    mb = rng.normal(size=rows) * 5
+    ma[::7] = -np.inf
+    mb[::11] = -np.inf
+    la = rng.uniform(0.5, 20, rows); lb = rng.uniform(0.5, 20, rows)
+    ua = rng.normal(size=(rows, d)); ub = rng.normal(size=(rows, d))
+    f = lambda x: torch.tensor(x, dtype=torch.float32, device="cuda")
+    A = (f(ma), f(la), f(ua)); Bs = (f(mb), f(lb), f(ub))
+    out = (torch.empty(rows, device="cuda"), torch.empty(rows, device="cuda"), torch.empty(rows, d, device="cuda"))
+    blkattn.merge(A, Bs, out)
+    norm = (torch.empty(rows, device="cuda"), None, torch.empty(rows, d, device="cuda"))
+    blkattn.merge(A, Bs, norm)
+    # aliasing: out = a
+    Ac = tuple(t.clone() for t in A)
+    blkattn.merge(Ac, Bs, Ac)
+    torch.cuda.synchronize()
+    a32 = lambda x: np.asarray(x, np.float32).astype(np.float64)
+    for r in range(rows):
+        sa = None if ma[r] == -np.inf else (a32(ma[r]), a32(la[r]), a32(ua[r]))
+        sb = None if mb[r] == -np.inf else (a32(mb[r]), a32(lb[r]), a32(ub[r]))
+        st = ost.merge(sa, sb)
+        if st is None:
+            assert out[0][r].item() == -math.inf and norm[0][r].item() == -math.inf
+            assert torch.all(norm[2][r] == 0)
+            continue
+        m, l, u = st
+        assert out[0][r].item() == pytest.approx(m, abs=1e-6)
+        assert out[1][r].item() == pytest.approx(l, rel=1e-5)
+        np.testing.assert_allclose(out[2][r].cpu().numpy(), u, rtol=1e-5, atol=1e-5)
+        o, lse = ost.finish(st, d)
+        np.testing.assert_allclose(norm[2][r].cpu().numpy(), o, rtol=1e-5, atol=1e-5)
+        assert norm[0][r].item() == pytest.approx(lse, abs=1e-5)
+    for t_ref, t in zip(out, Ac):
+        torch.testing.assert_close(t, t_ref, rtol=0, atol=0)
+
+
+def test_merge_example_25_1_states():
+    """The printed states of Example 25.1 through blkattn_merge."""
+    f = lambda x: torch.tensor(x, dtype=torch.float32, device="cuda")
+    A = (f([math.log(2)]), f([1.5]), f([[3.0]]))
+    Bs = (f([math.log(6)]), f([1.0]), f([[5.0]]))
+    out = (f([0.0]), f([0.0]), f([[0.0]]))
+    blkattn.merge(A, Bs, out)
+    torch.cuda.synchronize()
+    assert out[1].item() == pytest.approx(1.5, abs=1e-6)
+    assert out[2].item() == pytest.approx(6.0, abs=1e-5)
+    assert out[2].item() / out[1].item() == pytest.approx(4.0, abs=1e-5)
+
+
+# ------------------------------------------------------------ padding, masks and edge cases
+
+@pytest.mark.parametrize("name", ["decode_gqa", "spec_verify"])
+def test_poisoned_padding_is_never_read(name):
+    s = workloads.spec(name, small=True)
+    clean = workloads.generate(s)
+    for poison in (float("nan"), float("inf")):
+        dirty = workloads.generate(s, poison_padding=poison)
+        _, _, o1, l1 = run_gpu(clean)
+        _, _, o2, l2 = run_gpu(dirty)
+        np.testing.assert_array_equal(o1, o2)
+        np.testing.assert_array_equal(l1, l2)
+
+
+def make_case(B, Hq, Hkv, Tq, Tmax, d, dtype, seqlens, qpos, bias=None, seed=0):
+    g = torch.Generator().manual_seed(seed)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    return {"q": torch.randn(B, Hq, Tq, d, generator=g).to(dt),
+            "k": torch.randn(B, Hkv, Tmax, d, generator=g).to(dt),
+            "v": torch.randn(B, Hkv, Tmax, d, generator=g).to(dt),
+            "seqlens": torch.tensor(seqlens, dtype=torch.int32),
+            "qpos": torch.tensor(qpos, dtype=torch.int32), "bias": bias, "scale": d ** -0.5}
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("bf16", 64), ("f32", 128), ("f32", 64)])
+def test_edge_positions_and_lengths(dtype, d):
+    """pos < 0, len 0, len > T_max, pos beyond len, one key, ragged tails."""
+    B, Hq, Hkv, Tq, Tmax = 5, 6, 3, 3, 333
+    seqlens = [0, 1, 333, 500, 130]
+    qpos = [[5, -1, 0], [0, 0, 7], [332, 100, -5], [1000, 64, 63], [129, 128, 127]]
+    inp = make_case(B, Hq, Hkv, Tq, Tmax, d, dtype, seqlens, qpos)
+    _, _, o, l = run_gpu(inp)
+    ref = run_oracle(inp)
+    assert ref["n_visible"].min() == 0 and ref["n_visible"].max() == 333
+    tol = (F32_TOL, F32_TOL) if dtype == "f32" else (BF16_TOL_O, BF16_TOL_L)
+    assert_parity(o, l, ref, *tol)
+
+
+def test_dense_per_head_bias_with_masked_rows():
+    B, Hq, Hkv, Tq, Tmax, d = 2, 8, 2, 4, 300, 128
+    g = torch.Generator().manual_seed(3)
+    bias = torch.randn(B, Hq, Tq, Tmax, generator=g) * 2
+    bias[torch.rand(B, Hq, Tq, Tmax, generator=g) < 0.3] = -math.inf
+    bias[0, 3, 1, :] = -math.inf  # one fully masked (b, h, i) row
+    bias[1, :, 2, 100:] = -math.inf
+    inp = make_case(B, Hq, Hkv, Tq, Tmax, d, "bf16", [300, 257], [[299, 100, 50, 299], [0, 256, 256, 300]], bias)
+    _, _, o, l = run_gpu(inp)
+    ref = run_oracle(inp)
+    assert (ref["n_visible"] == 0).sum() >= 1
+    assert_parity(o, l, ref, BF16_TOL_O, BF16_TOL_L)
+
+
+def test_one_hot_values_pin_visibility():
+    """V = I over T_max <= d: out[i, j] is the probability of key j, and every
+    invisible key gives exactly 0.0 (visibility checked bit-exactly)."""
+    B, Hq, Hkv, Tq, Tmax, d = 2, 4, 2, 5, 128, 128
+    inp = make_case(B, Hq, Hkv, Tq, Tmax, d, "f32", [128, 77], [[0, 5, 64, 127, 200], [-1, 10, 76, 77, 3]])
+    inp["v"] = torch.eye(Tmax, d).expand(B, Hkv, Tmax, d).contiguous()
+    _, _, o, l = run_gpu(inp)
+    ref = run_oracle(inp)
+    for r in range(o.shape[0]):
+        n = ref["n_visible"][r]
+        last = ref["last"][r]
+        assert np.all(o[r, last + 1:] == 0.0)
+        if n:
+            assert np.all(o[r, :last + 1] > 0.0)
+    assert_parity(o, l, ref, F32_TOL, F32_TOL)
+
+
+def test_strided_views():
+    """Non-contiguous q / out / lse and K/V that are views into a larger cache."""
+    B, Hq, Hkv, Tq, d = 3, 8, 4, 2, 128
+    g = torch.Generator().manual_seed(5)
+    big_k = torch.randn(B, Hkv, 700, d, generator=g).to(torch.bfloat16).cuda()
+    big_v = torch.randn(B, Hkv, 700, d, generator=g).to(torch.bfloat16).cuda()
+    k = big_k[:, :, 64:600]  # row-aligned view
+    v = big_v[:, :, 64:600]
+    qt = torch.randn(B, Tq, Hq, d, generator=g).to(torch.bfloat16).cuda()
+    q = qt.transpose(1, 2)  # [B, Hq, Tq, d] with a permuted layout
+    sl = torch.tensor([536, 300, 17], dtype=torch.int32).cuda()
+    qp = torch.tensor([[535, 534], [299, 400], [16, 3]], dtype=torch.int32).cuda()
+    out_store = torch.empty(B, Tq, Hq, d, device="cuda")
+    out = out_store.transpose(1, 2)
+    lse_store = torch.empty(B, Tq, Hq, device="cuda")
+    lse = lse_store.transpose(1, 2)
+    blkattn.fwd(q, k, v, sl, qp, None, d ** -0.5, out, lse)
+    torch.cuda.synchronize()
+    ref = oracle.attention(q.cpu().contiguous(), k.cpu().contiguous(), v.cpu().contiguous(), sl.cpu(),
+                           qp.cpu(), d ** -0.5)
+    assert_parity(out.double().cpu().numpy().reshape(-1, d), lse.double().cpu().numpy().reshape(-1), ref,
+                  BF16_TOL_O, BF16_TOL_L)
+
+
+def test_empty_calls_are_no_ops():
+    inp = to_dev(make_case(1, 2, 1, 1, 16, 64, "bf16", [16], [[15]]))
+    out = torch.full((0, 2, 1, 64), 7.0, device="cuda")
+    lse = torch.full((0, 2, 1), 7.0, device="cuda")
+    z = lambda t: t[:0]
+    blkattn.fwd(z(inp["q"]), z(inp["k"]), z(inp["v"]), z(inp["seqlens"]), z(inp["qpos"]), None, 0.1, out, lse)
+    torch.cuda.synchronize()
+    assert blkattn.check_device_error() == 0
