@@ -320,6 +320,28 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def measure_other(name, peaks):
+    ro = Runner(name)
+    fl = ro.s.name == "prefill"
+    steps_o = 10 if not fl else 5
+    tot, mn, _ = time_steps(ro, steps_o, 3, 1, flush=True)
+    t_ms = sum(tot) / len(tot)
+    m_ms = sum(mn) / len(mn)
+    kvo, tb = algorithmic_bytes(ro.s, ro.cpu)
+    entry = {"workload": describe(ro.s), "us_per_call": t_ms * 1e3, "main_kernel_us": m_ms * 1e3,
+             "kv_gbs": kvo / (t_ms * 1e-3) / 1e9, "plan": ro.plan,
+             "roofline": roofline_entry(ro, m_ms, peaks, causal_flops(ro.s, ro.cpu) if fl else None)}
+    if fl:
+        f = causal_flops(ro.s, ro.cpu)
+        entry["tflops"] = f / (t_ms * 1e-3) / 1e12
+        entry["frac_of_bf16_peak"] = entry["tflops"] / peaks["bf16_tflops"]
+        entry["frac_of_bf16_sustained"] = entry["tflops"] / peaks["bf16_tflops_sustained"]
+    else:
+        entry["frac_of_hbm_peak"] = (tb / (t_ms * 1e-3) / 1e9) / peaks["hbm_gbs"]
+    ro.free()
+    return entry
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -394,26 +416,10 @@ def main():
         for name in workloads.SPECS:
             if name == s.name:
                 continue
-            ro = Runner(name)
-            fl = ro.s.name == "prefill"
-            steps_o = 10 if not fl else 5
-            tot, mn, _ = time_steps(ro, steps_o, 3, 1, flush=True)
-            t_ms = sum(tot) / len(tot)
-            m_ms = sum(mn) / len(mn)
-            kvo, tb = algorithmic_bytes(ro.s, ro.cpu)
-            entry = {"workload": describe(ro.s), "us_per_call": t_ms * 1e3, "main_kernel_us": m_ms * 1e3,
-                     "kv_gbs": kvo / (t_ms * 1e-3) / 1e9, "plan": ro.plan,
-                     "roofline": roofline_entry(ro, m_ms, peaks, causal_flops(ro.s, ro.cpu) if fl else None)}
-            if fl:
-                f = causal_flops(ro.s, ro.cpu)
-                entry["tflops"] = f / (t_ms * 1e-3) / 1e12
-                entry["frac_of_bf16_peak"] = entry["tflops"] / peaks["bf16_tflops"]
-                entry["frac_of_bf16_sustained"] = entry["tflops"] / peaks["bf16_tflops_sustained"]
-            else:
-                entry["frac_of_hbm_peak"] = (tb / (t_ms * 1e-3) / 1e9) / peaks["hbm_gbs"]
-            others[name] = entry
-            ro.free()
-            del ro
+            try:
+                others[name] = measure_other(name, peaks)
+            except Exception as exc:  # report, keep the headline line
+                others[name] = {"error": f"{type(exc).__name__}: {exc}"}
             torch.cuda.empty_cache()
         line["workloads"] = others
 

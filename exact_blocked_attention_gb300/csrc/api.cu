@@ -171,9 +171,11 @@ int validate_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn
     return BLKATTN_ERR_INVALID_ARG;
   if (Tmax < 1 || v->sizes[2] != Tmax) return BLKATTN_ERR_INVALID_ARG;
   if (k->sizes[3] != d || v->sizes[3] != d || out->sizes[3] != d) return BLKATTN_ERR_INVALID_ARG;
-  if (bias && (bias->sizes[0] != B || bias->sizes[1] != Hq || bias->sizes[2] != Tq ||
-               bias->sizes[3] != Tmax))
-    return BLKATTN_ERR_INVALID_ARG;
+  if (bias) {  // each dim is full-size or 1 (a size-1 dim broadcasts)
+    const int64_t full[4] = {B, Hq, Tq, Tmax};
+    for (int i = 0; i < 4; ++i)
+      if (bias->sizes[i] != full[i] && bias->sizes[i] != 1) return BLKATTN_ERR_INVALID_ARG;
+  }
   // cache rows move with 16-byte bulk copies
   const int eb = elt_bytes(q->dtype);
   for (const blkattn_tensor* t : {k, v}) {
@@ -267,8 +269,9 @@ int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_
   p.qp_sb = q_logical_pos->strides[0]; p.qp_si = q_logical_pos->strides[1];
   if (mask_bias) {
     p.bias = static_cast<const float*>(mask_bias->data);
-    p.bi_sb = mask_bias->strides[0]; p.bi_sh = mask_bias->strides[1];
-    p.bi_si = mask_bias->strides[2]; p.bi_sj = mask_bias->strides[3];
+    int64_t bs[4];
+    for (int i = 0; i < 4; ++i) bs[i] = mask_bias->sizes[i] == 1 ? 0 : mask_bias->strides[i];
+    p.bi_sb = bs[0]; p.bi_sh = bs[1]; p.bi_si = bs[2]; p.bi_sj = bs[3];
   }
   p.scale_log2 = scale * 1.4426950408889634f;
   p.out = out->data;

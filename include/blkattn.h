@@ -89,7 +89,8 @@ typedef struct {
  *               [0, T_max] on the device).
  * q_logical_pos [B, T_q] int32: logical position of each query row (the same
  *               for every head of a sequence).  Negative: no key is visible.
- * mask_bias     NULL, or f32 [B, H_q, T_q, T_max] view (0-strides broadcast)
+ * mask_bias     NULL, or f32 [B, H_q, T_q, T_max] view; a dim of size 1 or
+ *               stride 0 broadcasts (e.g. [B, 1, T_q, T_max] for all heads)
  *               holding the additive M_j of eq. 33.2: finite or -inf.  +inf or
  *               NaN entries are out of contract (the result is then undefined).
  * scale         multiplies q.k (eq. 33.2 uses 1/sqrt(d_h)).

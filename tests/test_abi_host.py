@@ -96,13 +96,14 @@ def good_args(B=2, Hq=8, Hkv=2, Tq=3, Tmax=100, d=128, dt=torch.bfloat16):
     (lambda a: a.update(k=FakeTensor((2, 2, 100, 128), torch.bfloat16, strides=(25600, 12803, 128, 1))), -1),
     (lambda a: a.update(k=FakeTensor((2, 2, 100, 128), torch.bfloat16, addr=0x10008)), -1),  # not 16-B aligned
     (lambda a: a.update(bias=FakeTensor((2, 8, 3, 99), torch.float32)), -1),
+    (lambda a: a.update(bias=FakeTensor((2, 2, 3, 100), torch.float32)), -1),
     (lambda a: a.update(bias=FakeTensor((2, 8, 3, 100), torch.bfloat16)), -1),
     (lambda a: a.update(q=FakeTensor((2, 8, 3, 128), torch.bfloat16, addr=0)), -1),  # NULL data
     (lambda a: a.update(**good_args(d=96)), -2),  # head dim without a kernel
     (lambda a: a.update(q=None), -1),
 ], ids=["q-int", "mixed-dtype", "hq-not-multiple", "v-len", "qpos-shape", "seqlens-shape",
         "seqlens-dtype", "lse-dtype", "out-dim", "k-inner-stride", "k-row-misaligned",
-        "k-base-misaligned", "bias-shape", "bias-dtype", "null-data", "d96", "missing-q"])
+        "k-base-misaligned", "bias-shape", "bias-heads", "bias-dtype", "null-data", "d96", "missing-q"])
 def test_invalid_requests_are_rejected_before_cuda(lib, mutate, expect):
     a = good_args()
     mutate(a)
