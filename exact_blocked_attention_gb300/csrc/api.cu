@@ -6,6 +6,8 @@
 // cache lengths and logical positions are only ever read on the device, so a
 // call never synchronises with the GPU ("Chapter 33: inference compute
 // optimisation" §33.4: host reads of device values cut a capturable region).
+#include <cudaTypedefs.h>
+
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -65,16 +67,34 @@ int resident_ctas_per_sm(size_t smem_bytes) {
 Plan make_plan(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tmax, int d, Elt elt,
                int sms) {
   Plan pl;
-  const int64_t rows = (Hq / Hkv) * Tq;
-  int R = 1;
-  while (R < rows && R < 8) R *= 2;
-  pl.cfg.rows_per_cta = R;
-  pl.cfg.row_groups = (int)((rows + R - 1) / R);
-  pl.cfg.warps = 4;
-  pl.cfg.stages = (elt == Elt::BF16) ? 3 : 2;
-  pl.tile = 16 * pl.cfg.warps;
+  const int64_t rows = (Hq / Hkv) * Tq;  // query rows that read one KV head
+  size_t smem;
+  bool tensor = (elt == Elt::BF16);
+  if (const char* env = std::getenv("BLKATTN_KERNEL"))  // comparison runs only
+    if (std::strcmp(env, "cudacore") == 0) tensor = false;
+  if (tensor) {
+    // bf16: warp-level tensor cores, 16-row m-tiles (up to 3 per CTA)
+    int64_t mt = (rows + 15) / 16;
+    if (mt > 3) mt = 3;
+    pl.cfg.kernel = blkattn::Kernel::TensorCore;
+    pl.cfg.rows_per_cta = (int)(16 * mt);
+    pl.cfg.warps = (int)(4 * mt);
+    pl.cfg.stages = 3;
+    pl.tile = 64;
+    smem = blkattn::decode_mma_smem_bytes(d, (int)mt);
+  } else {
+    int R = 1;
+    while (R < rows && R < 8) R *= 2;
+    pl.cfg.kernel = blkattn::Kernel::CudaCore;
+    pl.cfg.rows_per_cta = R;
+    pl.cfg.warps = 4;
+    pl.cfg.stages = (elt == Elt::BF16) ? 3 : 2;
+    pl.tile = 16 * pl.cfg.warps;
+    smem = blkattn::decode_smem_bytes(elt, d, pl.cfg);
+  }
+  pl.cfg.row_groups = (int)((rows + pl.cfg.rows_per_cta - 1) / pl.cfg.rows_per_cta);
   const int64_t units = B * Hkv * pl.cfg.row_groups;
-  const int resident = resident_ctas_per_sm(blkattn::decode_smem_bytes(elt, d, pl.cfg));
+  const int resident = resident_ctas_per_sm(smem);
   const int64_t target = (int64_t)(sms > 0 ? sms : 148) * resident * 4;  // ~4 waves
   int64_t chunk;
   if (units >= target) {
@@ -113,6 +133,77 @@ int device_state(DeviceState** out) {
     s.ready = true;
   }
   *out = &s;
+  return BLKATTN_OK;
+}
+
+// ---- tiled-TMA tensor maps for the K/V cache ----
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_encoder() {
+  if (g_encode) return BLKATTN_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return BLKATTN_ERR_CUDA;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return BLKATTN_OK;
+}
+
+struct MapKey {
+  int dev;
+  const void* ptr;
+  int64_t sizes[4];
+  int64_t strides[3];
+  bool operator==(const MapKey& o) const {
+    return dev == o.dev && ptr == o.ptr && std::memcmp(sizes, o.sizes, sizeof sizes) == 0 &&
+           std::memcmp(strides, o.strides, sizeof strides) == 0;
+  }
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  bool used = false;
+};
+constexpr int kMapCache = 32;
+MapEntry g_maps[kMapCache];
+int g_map_next = 0;
+
+// 4-D map over a bf16 cache view [B, H, T, d] (element strides, last = 1):
+// dims {d, T, H, B}, box {64, 64, 1, 1}, 128-byte swizzle, zero fill past T.
+int kv_tensor_map(int dev, const blkattn_tensor* t, const CUtensorMap** out) {
+  MapKey key;
+  std::memset(&key, 0, sizeof key);
+  key.dev = dev;
+  key.ptr = t->data;
+  for (int i = 0; i < 4; ++i) key.sizes[i] = t->sizes[i];
+  for (int i = 0; i < 3; ++i) key.strides[i] = t->strides[i];
+  for (int i = 0; i < kMapCache; ++i)
+    if (g_maps[i].used && g_maps[i].key == key) {
+      *out = &g_maps[i].map;
+      return BLKATTN_OK;
+    }
+  int st = get_encoder();
+  if (st != BLKATTN_OK) return st;
+  MapEntry& e = g_maps[g_map_next];
+  g_map_next = (g_map_next + 1) % kMapCache;
+  const cuuint64_t dims[4] = {(cuuint64_t)t->sizes[3], (cuuint64_t)t->sizes[2], (cuuint64_t)t->sizes[1],
+                              (cuuint64_t)t->sizes[0]};
+  const cuuint64_t strides[3] = {(cuuint64_t)t->strides[2] * 2, (cuuint64_t)t->strides[1] * 2,
+                                 (cuuint64_t)t->strides[0] * 2};
+  const cuuint32_t box[4] = {64, 64, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(&e.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    e.used = false;
+    return BLKATTN_ERR_CUDA;
+  }
+  e.key = key;
+  e.used = true;
+  *out = &e.map;
   return BLKATTN_OK;
 }
 
@@ -222,7 +313,7 @@ int blkattn_debug_plan(int64_t B, int64_t H_q, int64_t H_kv, int64_t T_q, int64_
     return BLKATTN_ERR_INVALID_ARG;
   const Plan pl = make_plan(B, H_q, H_kv, T_q, T_max, (int)d,
                             dtype == BLKATTN_BF16 ? Elt::BF16 : Elt::F32, num_sms);
-  plan->kernel = 0;
+  plan->kernel = (int32_t)pl.cfg.kernel;
   plan->rows_per_cta = pl.cfg.rows_per_cta;
   plan->row_groups = pl.cfg.row_groups;
   plan->chunk_keys = pl.cfg.chunk;
@@ -294,8 +385,21 @@ int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_
   }
   p.err = ds->err;
 
-  if (blkattn::launch_decode_split(p, c.elt, (int)c.d, pl.cfg, stream) != cudaSuccess)
-    return BLKATTN_ERR_CUDA;
+  cudaError_t le;
+  if (pl.cfg.kernel == blkattn::Kernel::TensorCore) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BLKATTN_ERR_CUDA;
+    const CUtensorMap* mk = nullptr;
+    const CUtensorMap* mv = nullptr;
+    st = kv_tensor_map(dev, k, &mk);
+    if (st != BLKATTN_OK) return st;
+    st = kv_tensor_map(dev, v, &mv);
+    if (st != BLKATTN_OK) return st;
+    le = blkattn::launch_decode_mma(p, (int)c.d, pl.cfg, *mk, *mv, stream);
+  } else {
+    le = blkattn::launch_decode_split(p, c.elt, (int)c.d, pl.cfg, stream);
+  }
+  if (le != cudaSuccess) return BLKATTN_ERR_CUDA;
   if (g_split_event != nullptr && cudaEventRecord(g_split_event, stream) != cudaSuccess)
     return BLKATTN_ERR_CUDA;
   if (pl.cfg.n_splits > 1 && blkattn::launch_split_merge(p, (int)c.d, stream) != cudaSuccess)

@@ -1,8 +1,10 @@
 // Parameter blocks and launcher declarations shared by the host API and the
 // kernel translation units.  Internal to libblkattn (not part of the C ABI).
 #pragma once
-#include <cstdint>
+#include <cuda.h>  // CUtensorMap (type only; the encoder is fetched at run time)
 #include <cuda_runtime.h>
+
+#include <cstdint>
 
 namespace blkattn {
 
@@ -49,8 +51,10 @@ struct FwdParams {
 };
 
 // Split-KV kernel configuration chosen by the planner.
+enum class Kernel : int { CudaCore = 0, TensorCore = 1 };
 struct DecodeConfig {
-  int rows_per_cta;  // 1, 2, 4 or 8
+  Kernel kernel;
+  int rows_per_cta;  // CUDA-core: 1, 2, 4 or 8; tensor-core: 16, 32 or 48
   int warps;         // consumer warps; keys per stage = 16 * warps
   int stages;
   int chunk;
@@ -72,5 +76,12 @@ struct MergeParams {
 cudaError_t launch_state_merge(const MergeParams& p, cudaStream_t stream);
 
 size_t decode_smem_bytes(Elt elt, int d, const DecodeConfig& cfg);
+
+// Tensor-core (mma.sync, bf16) split-KV kernel: 16 * mt query rows per CTA.
+// K and V tiles arrive by tiled TMA through these maps: 4-D {d, T_max, H_kv,
+// B}, box {64, 64, 1, 1}, bf16, 128-byte swizzle.
+cudaError_t launch_decode_mma(const FwdParams& p, int d, const DecodeConfig& cfg,
+                              const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, cudaStream_t stream);
+size_t decode_mma_smem_bytes(int d, int mt);
 
 }  // namespace blkattn

@@ -156,7 +156,8 @@ int blkattn_check_device_error(blkattn_stream_t stream);
  * Host-only view of the split plan blkattn_fwd would use (no CUDA call).
  * Keys [0, T_max) are cut into n_splits consecutive chunks of chunk_keys
  * (the last may be shorter); rows_per_cta query rows of one KV head share a
- * CTA.  kernel: 0 = CUDA-core split-KV kernel, 1 = tensor-core kernel.
+ * CTA.  kernel: 0 = CUDA-core split-KV kernel (f32 inputs), 1 = warp-level
+ * tensor-core split-KV kernel (bf16 inputs).
  * Returns BLKATTN_OK or BLKATTN_ERR_INVALID_ARG.
  */
 typedef struct {

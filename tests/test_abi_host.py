@@ -154,7 +154,10 @@ def test_plan_partitions_every_workload(lib, name):
                                torch.bfloat16 if s.dtype == "bf16" else torch.float32, 152)
         _check_partition(p, s.Tmax)
         rows = s.G * s.Tq
-        assert p["rows_per_cta"] in (1, 2, 4, 8)
+        if s.dtype == "bf16":
+            assert p["kernel"] == 1 and p["rows_per_cta"] in (16, 32, 48)
+        else:
+            assert p["kernel"] == 0 and p["rows_per_cta"] in (1, 2, 4, 8)
         assert p["row_groups"] == math.ceil(rows / p["rows_per_cta"])
         assert p["ctas"] == p["n_splits"] * s.Hkv * s.B * p["row_groups"]
         if p["n_splits"] > 1:
