@@ -22,12 +22,15 @@ ERR_UNSUPPORTED = -2
 ERR_CUDA = -3
 ERR_DEVICE_TIMEOUT = -4
 ERR_NO_WORKSPACE = -5
+ERR_SCRATCH_LIMIT = -6
+STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 BF16, F32, I32 = 1, 2, 3
 _DTYPES = {torch.bfloat16: BF16, torch.float32: F32, torch.int32: I32}
 
 EXPORTED = ("blkattn_fwd", "blkattn_merge", "blkattn_status_string",
-            "blkattn_check_device_error", "blkattn_debug_plan", "blkattn_debug_set_split_event")
+            "blkattn_check_device_error", "blkattn_debug_plan", "blkattn_debug_set_split_event",
+            "blkattn_fwd_static_scratch")
 
 
 class Tensor(ctypes.Structure):
@@ -71,6 +74,8 @@ def load(path: str = LIB_PATH):
             P = ctypes.c_void_p
             lib.blkattn_fwd.restype = ctypes.c_int
             lib.blkattn_fwd.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P]
+            lib.blkattn_fwd_static_scratch.restype = ctypes.c_int
+            lib.blkattn_fwd_static_scratch.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P]
             lib.blkattn_merge.restype = ctypes.c_int
             lib.blkattn_merge.argtypes = [P, P, P, P]
             lib.blkattn_status_string.restype = ctypes.c_char_p
@@ -133,6 +138,23 @@ def fwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale: float, out, lse, st
     st = lib.blkattn_fwd(_ref(descs[0]), _ref(descs[1]), _ref(descs[2]), _ref(descs[3]),
                          _ref(descs[4]), _ref(descs[5]), ctypes.c_float(scale),
                          _ref(descs[6]), _ref(descs[7]), _stream_handle(stream) if q.is_cuda else None)
+    _check(st)
+    return out, lse
+
+
+def fwd_static_scratch(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale: float, out, lse,
+                       stream=None):
+    """blkattn_fwd_static_scratch: the same call as fwd, for callers that must
+    not allocate device memory at call time; the per-split scratch is a fixed
+    16 MiB array inside the library (shared by all calls on a device, so calls
+    must not overlap on the GPU).  Raises BlkattnError with ERR_SCRATCH_LIMIT
+    when the problem needs more scratch than that."""
+    lib = load()
+    descs = [describe(t) for t in (q, k, v, seqlens_k, q_logical_pos, mask_bias, out, lse)]
+    st = lib.blkattn_fwd_static_scratch(_ref(descs[0]), _ref(descs[1]), _ref(descs[2]), _ref(descs[3]),
+                                        _ref(descs[4]), _ref(descs[5]), ctypes.c_float(scale),
+                                        _ref(descs[6]), _ref(descs[7]),
+                                        _stream_handle(stream) if q.is_cuda else None)
     _check(st)
     return out, lse
 

@@ -290,7 +290,116 @@ int validate_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn
   return BLKATTN_OK;
 }
 
+// Kernel parameters of one call; `ws` holds the per-split partial states
+// when the plan has more than one split (m, l, u in 256-byte aligned parts).
+FwdParams fill_params(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
+                      const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos,
+                      const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out,
+                      const blkattn_tensor* lse, const Checked& c, const Plan& pl, void* ws, int* err) {
+  const int eb = elt_bytes(q->dtype);
+  FwdParams p;
+  std::memset(&p, 0, sizeof p);
+  p.q = q->data;
+  p.q_sb = q->strides[0]; p.q_sh = q->strides[1]; p.q_si = q->strides[2]; p.q_sd = q->strides[3];
+  p.k = static_cast<const char*>(k->data);
+  p.v = static_cast<const char*>(v->data);
+  p.k_sb = k->strides[0] * eb; p.k_sh = k->strides[1] * eb; p.k_st = k->strides[2] * eb;
+  p.v_sb = v->strides[0] * eb; p.v_sh = v->strides[1] * eb; p.v_st = v->strides[2] * eb;
+  p.seqlens = static_cast<const int32_t*>(seqlens_k->data);
+  p.sl_s = seqlens_k->strides[0];
+  p.qpos = static_cast<const int32_t*>(q_logical_pos->data);
+  p.qp_sb = q_logical_pos->strides[0]; p.qp_si = q_logical_pos->strides[1];
+  if (mask_bias) {
+    p.bias = static_cast<const float*>(mask_bias->data);
+    int64_t bs[4];
+    for (int i = 0; i < 4; ++i) bs[i] = mask_bias->sizes[i] == 1 ? 0 : mask_bias->strides[i];
+    p.bi_sb = bs[0]; p.bi_sh = bs[1]; p.bi_si = bs[2]; p.bi_sj = bs[3];
+  }
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.out = out->data;
+  p.out_bf16 = out->dtype == BLKATTN_BF16;
+  p.o_sb = out->strides[0]; p.o_sh = out->strides[1]; p.o_si = out->strides[2]; p.o_sd = out->strides[3];
+  p.lse = static_cast<float*>(lse->data);
+  p.l_sb = lse->strides[0]; p.l_sh = lse->strides[1]; p.l_si = lse->strides[2];
+  p.B = (int)c.B; p.Hq = (int)c.Hq; p.Hkv = (int)c.Hkv; p.G = (int)(c.Hq / c.Hkv);
+  p.Tq = (int)c.Tq; p.Tmax = (int)c.Tmax;
+  p.rows_per_head = (int)(p.G * c.Tq);
+  p.row_groups = pl.cfg.row_groups;
+  p.chunk = pl.cfg.chunk;
+  p.n_splits = pl.cfg.n_splits;
+  if (pl.cfg.n_splits > 1) {
+    const int64_t n = c.B * c.Hq * c.Tq * (int64_t)pl.cfg.n_splits;
+    char* base = static_cast<char*>(ws);
+    p.ws_m = reinterpret_cast<float*>(base);
+    p.ws_l = reinterpret_cast<float*>(base + ((n * 4 + 255) / 256) * 256);
+    p.ws_u = reinterpret_cast<float*>(base + 2 * ((n * 4 + 255) / 256) * 256);
+  }
+  p.err = err;
+  return p;
+}
+
+// Enqueue the split-KV kernel and, with more than one split, the merge.
+int launch_fwd(const FwdParams& p, const Checked& c, const Plan& pl, const blkattn_tensor* k,
+               const blkattn_tensor* v, cudaStream_t stream) {
+  cudaError_t le;
+  if (pl.cfg.kernel == blkattn::Kernel::TensorCore) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BLKATTN_ERR_CUDA;
+    const CUtensorMap* mk = nullptr;
+    const CUtensorMap* mv = nullptr;
+    int st = kv_tensor_map(dev, k, &mk);
+    if (st != BLKATTN_OK) return st;
+    st = kv_tensor_map(dev, v, &mv);
+    if (st != BLKATTN_OK) return st;
+    le = blkattn::launch_decode_mma(p, (int)c.d, pl.cfg, *mk, *mv, stream);
+  } else {
+    le = blkattn::launch_decode_split(p, c.elt, (int)c.d, pl.cfg, stream);
+  }
+  if (le != cudaSuccess) return BLKATTN_ERR_CUDA;
+  if (g_split_event != nullptr && cudaEventRecord(g_split_event, stream) != cudaSuccess)
+    return BLKATTN_ERR_CUDA;
+  if (pl.cfg.n_splits > 1 && blkattn::launch_split_merge(p, (int)c.d, stream) != cudaSuccess)
+    return BLKATTN_ERR_CUDA;
+  return BLKATTN_OK;
+}
+
 }  // namespace
+
+namespace blkattn {
+
+int validate_fwd_args(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
+                      const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos,
+                      const blkattn_tensor* mask_bias, const blkattn_tensor* out,
+                      const blkattn_tensor* lse) {
+  Checked c;
+  return validate_fwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, out, lse, &c);
+}
+
+// blkattn_fwd with caller-provided scratch for the per-split states instead
+// of the library's grow-only workspace.  Never allocates device memory.
+int fwd_with_scratch(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
+                     const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos,
+                     const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out,
+                     const blkattn_tensor* lse, blkattn_stream_t stream_, void* scratch,
+                     size_t scratch_bytes) {
+  Checked c;
+  int st = validate_fwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, out, lse, &c);
+  if (st != BLKATTN_OK) return st;
+  if (c.B == 0 || c.Tq == 0) return BLKATTN_OK;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != BLKATTN_OK) return st;
+  const Plan pl = make_plan(c.B, c.Hq, c.Hkv, c.Tq, c.Tmax, (int)c.d, c.elt, ds->sms);
+  if (c.B * pl.cfg.row_groups > 65535) return BLKATTN_ERR_UNSUPPORTED;
+  if ((size_t)pl.ws_bytes > scratch_bytes) return BLKATTN_ERR_SCRATCH_LIMIT;
+  const FwdParams p = fill_params(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, c, pl,
+                                  scratch, ds->err);
+  return launch_fwd(p, c, pl, k, v, stream);
+}
+
+}  // namespace blkattn
 
 extern "C" {
 
@@ -302,6 +411,7 @@ const char* blkattn_status_string(int status) {
     case BLKATTN_ERR_CUDA: return "CUDA runtime or launch error";
     case BLKATTN_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait timed out";
     case BLKATTN_ERR_NO_WORKSPACE: return "workspace would have to grow during stream capture";
+    case BLKATTN_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the fixed static maximum";
   }
   return "unknown status";
 }
@@ -344,67 +454,9 @@ int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_
     st = ensure_workspace(ds, (size_t)pl.ws_bytes, stream);
     if (st != BLKATTN_OK) return st;
   }
-
-  const int eb = elt_bytes(q->dtype);
-  FwdParams p;
-  std::memset(&p, 0, sizeof p);
-  p.q = q->data;
-  p.q_sb = q->strides[0]; p.q_sh = q->strides[1]; p.q_si = q->strides[2]; p.q_sd = q->strides[3];
-  p.k = static_cast<const char*>(k->data);
-  p.v = static_cast<const char*>(v->data);
-  p.k_sb = k->strides[0] * eb; p.k_sh = k->strides[1] * eb; p.k_st = k->strides[2] * eb;
-  p.v_sb = v->strides[0] * eb; p.v_sh = v->strides[1] * eb; p.v_st = v->strides[2] * eb;
-  p.seqlens = static_cast<const int32_t*>(seqlens_k->data);
-  p.sl_s = seqlens_k->strides[0];
-  p.qpos = static_cast<const int32_t*>(q_logical_pos->data);
-  p.qp_sb = q_logical_pos->strides[0]; p.qp_si = q_logical_pos->strides[1];
-  if (mask_bias) {
-    p.bias = static_cast<const float*>(mask_bias->data);
-    int64_t bs[4];
-    for (int i = 0; i < 4; ++i) bs[i] = mask_bias->sizes[i] == 1 ? 0 : mask_bias->strides[i];
-    p.bi_sb = bs[0]; p.bi_sh = bs[1]; p.bi_si = bs[2]; p.bi_sj = bs[3];
-  }
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.out = out->data;
-  p.out_bf16 = out->dtype == BLKATTN_BF16;
-  p.o_sb = out->strides[0]; p.o_sh = out->strides[1]; p.o_si = out->strides[2]; p.o_sd = out->strides[3];
-  p.lse = static_cast<float*>(lse->data);
-  p.l_sb = lse->strides[0]; p.l_sh = lse->strides[1]; p.l_si = lse->strides[2];
-  p.B = (int)c.B; p.Hq = (int)c.Hq; p.Hkv = (int)c.Hkv; p.G = (int)(c.Hq / c.Hkv);
-  p.Tq = (int)c.Tq; p.Tmax = (int)c.Tmax;
-  p.rows_per_head = (int)(p.G * c.Tq);
-  p.row_groups = pl.cfg.row_groups;
-  p.chunk = pl.cfg.chunk;
-  p.n_splits = pl.cfg.n_splits;
-  if (pl.cfg.n_splits > 1) {
-    const int64_t n = c.B * c.Hq * c.Tq * (int64_t)pl.cfg.n_splits;
-    char* base = static_cast<char*>(ds->ws);
-    p.ws_m = reinterpret_cast<float*>(base);
-    p.ws_l = reinterpret_cast<float*>(base + ((n * 4 + 255) / 256) * 256);
-    p.ws_u = reinterpret_cast<float*>(base + 2 * ((n * 4 + 255) / 256) * 256);
-  }
-  p.err = ds->err;
-
-  cudaError_t le;
-  if (pl.cfg.kernel == blkattn::Kernel::TensorCore) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return BLKATTN_ERR_CUDA;
-    const CUtensorMap* mk = nullptr;
-    const CUtensorMap* mv = nullptr;
-    st = kv_tensor_map(dev, k, &mk);
-    if (st != BLKATTN_OK) return st;
-    st = kv_tensor_map(dev, v, &mv);
-    if (st != BLKATTN_OK) return st;
-    le = blkattn::launch_decode_mma(p, (int)c.d, pl.cfg, *mk, *mv, stream);
-  } else {
-    le = blkattn::launch_decode_split(p, c.elt, (int)c.d, pl.cfg, stream);
-  }
-  if (le != cudaSuccess) return BLKATTN_ERR_CUDA;
-  if (g_split_event != nullptr && cudaEventRecord(g_split_event, stream) != cudaSuccess)
-    return BLKATTN_ERR_CUDA;
-  if (pl.cfg.n_splits > 1 && blkattn::launch_split_merge(p, (int)c.d, stream) != cudaSuccess)
-    return BLKATTN_ERR_CUDA;
-  return BLKATTN_OK;
+  const FwdParams p = fill_params(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, c, pl,
+                                  ds->ws, ds->err);
+  return launch_fwd(p, c, pl, k, v, stream);
 }
 
 int blkattn_merge(const blkattn_states* a, const blkattn_states* b, const blkattn_states* out,

@@ -4,7 +4,10 @@
 #include <cuda.h>  // CUtensorMap (type only; the encoder is fetched at run time)
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
+
+#include "blkattn.h"
 
 namespace blkattn {
 
@@ -83,5 +86,18 @@ size_t decode_smem_bytes(Elt elt, int d, const DecodeConfig& cfg);
 cudaError_t launch_decode_mma(const FwdParams& p, int d, const DecodeConfig& cfg,
                               const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, cudaStream_t stream);
 size_t decode_mma_smem_bytes(int d, int mt);
+
+// Validation only (no CUDA call), and blkattn_fwd with caller-given scratch
+// for the per-split states (no allocation; BLKATTN_ERR_SCRATCH_LIMIT when the
+// plan needs more than scratch_bytes).  Both live in api.cu.
+int validate_fwd_args(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
+                      const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos,
+                      const blkattn_tensor* mask_bias, const blkattn_tensor* out,
+                      const blkattn_tensor* lse);
+int fwd_with_scratch(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
+                     const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos,
+                     const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out,
+                     const blkattn_tensor* lse, blkattn_stream_t stream, void* scratch,
+                     size_t scratch_bytes);
 
 }  // namespace blkattn

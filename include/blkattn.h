@@ -55,7 +55,8 @@ enum {
   BLKATTN_ERR_UNSUPPORTED = -2,   /* a valid request this build has no kernel for (e.g. d not in {64,128}) */
   BLKATTN_ERR_CUDA = -3,          /* a CUDA runtime call or kernel launch failed */
   BLKATTN_ERR_DEVICE_TIMEOUT = -4,/* a kernel's bounded wait ran out (reported by blkattn_check_device_error) */
-  BLKATTN_ERR_NO_WORKSPACE = -5   /* the workspace must grow while the stream is being captured */
+  BLKATTN_ERR_NO_WORKSPACE = -5,  /* the workspace must grow while the stream is being captured */
+  BLKATTN_ERR_SCRATCH_LIMIT = -6  /* blkattn_fwd_static_scratch: more scratch needed than it has */
 };
 
 /* ---------------------------------------------------------------- tensors */
@@ -111,6 +112,41 @@ int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k,
                 const blkattn_tensor* mask_bias, float scale,
                 const blkattn_tensor* out, const blkattn_tensor* lse,
                 blkattn_stream_t stream);
+
+/*
+ * blkattn_fwd_static_scratch — blkattn_fwd that allocates no device memory.
+ *
+ * No counterpart on the pages: this is a deployment variant of blkattn_fwd.
+ * It is for callers that must not allocate device memory at call time: a
+ * host framework that owns every byte of device memory through its own pool
+ * or budget, a latency-critical loop that cannot afford the device-wide
+ * synchronisation cudaMalloc/cudaFree may bring, or a runtime that forbids
+ * dynamic device allocation after start-up.
+ *
+ * Same arguments, layouts, semantics and results as blkattn_fwd.  The
+ * per-split partial states live in one fixed array compiled into the library
+ * (BLKATTN_STATIC_SCRATCH_BYTES, 16 MiB, held on every device that loads the
+ * library until the process exits) instead of the grow-only workspace; the
+ * call makes no cudaMalloc, cudaFree or other allocating call.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - A problem whose split plan needs more than BLKATTN_STATIC_SCRATCH_BYTES
+ *     (about rows * n_splits * (d + 2) * 4 bytes, see blkattn_debug_plan's
+ *     workspace_bytes) is rejected with BLKATTN_ERR_SCRATCH_LIMIT before
+ *     anything is enqueued.
+ *   - Every call shares the one array and leaves its contents behind.  No
+ *     part of it has to start at zero: each call writes every partial state
+ *     it later reads.  Calls whose kernels overlap on the GPU (concurrent
+ *     streams, several host threads) race on the array: serialise them.
+ */
+#define BLKATTN_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int blkattn_fwd_static_scratch(const blkattn_tensor* q, const blkattn_tensor* k,
+                               const blkattn_tensor* v, const blkattn_tensor* seqlens_k,
+                               const blkattn_tensor* q_logical_pos,
+                               const blkattn_tensor* mask_bias, float scale,
+                               const blkattn_tensor* out, const blkattn_tensor* lse,
+                               blkattn_stream_t stream);
 
 /*
  * Attention states of rows, in the sufficient statistics of eq. 33.3:

@@ -36,7 +36,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_status_strings(lib):
-    for st in (0, -1, -2, -3, -4, -5):
+    for st in (0, -1, -2, -3, -4, -5, -6):
         assert blkattn.status_string(st)
     assert blkattn.status_string(-99) == "unknown status"
 
