@@ -63,8 +63,15 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return (uint32_t)((c >> 3) * (64 * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
+// Register cap so that two CTAs (2 x 5 warps) share an SM at MT = 1: the
+// register file is split per sub-partition, 3 warps x 168 x 32 fit one.
+template <int MT, int NWK>
+constexpr int mma_max_regs() {
+  return (MT * NWK + 1) <= 5 ? 168 : ((MT * NWK + 1) <= 9 ? 168 : 128);
+}
+
 template <int D, int MT, int NWK, int STAGES>
-__global__ void __launch_bounds__((MT * NWK + 1) * 32, 1)
+__global__ void __maxnreg__((mma_max_regs<MT, NWK>()))
     decode_mma_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv) {
   using L = MmaLayout<D, MT, NWK, STAGES>;
@@ -332,6 +339,10 @@ __global__ void __launch_bounds__((MT * NWK + 1) * 32, 1)
     }
   }
 
+  // the split-merge grid may start launching now (it waits for this grid's
+  // completion before reading anything)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   // ---- drain every issued copy before the ring is reused ----
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -421,6 +432,9 @@ cudaError_t launch_mt(const FwdParams& p, const DecodeConfig& cfg, const CUtenso
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    if (e != cudaSuccess) return e;
+    // all of the unified L1/shared storage as shared memory: two ~100 KB CTAs per SM
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }

@@ -345,6 +345,10 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     }
   }
 
+  // the split-merge grid may start launching now (it waits for this grid's
+  // completion before reading anything)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   // ---- drain: every issued copy must have landed before the ring is reused ----
   __syncthreads();
   if (threadIdx.x == 0) {
