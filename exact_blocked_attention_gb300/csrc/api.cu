@@ -64,10 +64,26 @@ int resident_ctas_per_sm(size_t smem_bytes) {
   return n < 1 ? 1 : n;
 }
 
+// prefill_ok: the request qualifies for the tcgen05 prefill kernel (bf16,
+// d = 128, no bias, 16-byte aligned query rows) if it also has T_q >= 64.
 Plan make_plan(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tmax, int d, Elt elt,
-               int sms) {
+               int sms, bool prefill_ok) {
   Plan pl;
   const int64_t rows = (Hq / Hkv) * Tq;  // query rows that read one KV head
+  if (prefill_ok && elt == Elt::BF16 && d == 128 && Tq >= 64 && B <= 65535) {
+    // many query rows per head: 128-row query tiles on tcgen05, no splits
+    pl.cfg.kernel = blkattn::Kernel::Prefill;
+    pl.cfg.rows_per_cta = 128;
+    pl.cfg.row_groups = (int)((Tq + 127) / 128);
+    pl.cfg.warps = 4;
+    pl.cfg.stages = 2;
+    pl.tile = 64;
+    pl.cfg.chunk = (int)((Tmax + 63) / 64 * 64);
+    pl.cfg.n_splits = 1;
+    pl.ctas = (int64_t)pl.cfg.row_groups * Hq * B;
+    pl.ws_bytes = 0;
+    return pl;
+  }
   size_t smem;
   bool tensor = (elt == Elt::BF16);
   if (const char* env = std::getenv("BLKATTN_KERNEL"))  // comparison runs only
@@ -153,11 +169,12 @@ int get_encoder() {
 
 struct MapKey {
   int dev;
+  int box_rows;
   const void* ptr;
   int64_t sizes[4];
   int64_t strides[3];
   bool operator==(const MapKey& o) const {
-    return dev == o.dev && ptr == o.ptr && std::memcmp(sizes, o.sizes, sizeof sizes) == 0 &&
+    return dev == o.dev && box_rows == o.box_rows && ptr == o.ptr && std::memcmp(sizes, o.sizes, sizeof sizes) == 0 &&
            std::memcmp(strides, o.strides, sizeof strides) == 0;
   }
 };
@@ -170,12 +187,14 @@ constexpr int kMapCache = 32;
 MapEntry g_maps[kMapCache];
 int g_map_next = 0;
 
-// 4-D map over a bf16 cache view [B, H, T, d] (element strides, last = 1):
-// dims {d, T, H, B}, box {64, 64, 1, 1}, 128-byte swizzle, zero fill past T.
-int kv_tensor_map(int dev, const blkattn_tensor* t, const CUtensorMap** out) {
+// 4-D map over a bf16 view [B, H, T, d] (element strides, last = 1):
+// dims {d, T, H, B}, box {64, box_rows, 1, 1}, 128-byte swizzle, zero fill
+// past T.  Used for the K/V cache (64-row boxes) and for Q (128-row boxes).
+int kv_tensor_map(int dev, const blkattn_tensor* t, int box_rows, const CUtensorMap** out) {
   MapKey key;
   std::memset(&key, 0, sizeof key);
   key.dev = dev;
+  key.box_rows = box_rows;
   key.ptr = t->data;
   for (int i = 0; i < 4; ++i) key.sizes[i] = t->sizes[i];
   for (int i = 0; i < 3; ++i) key.strides[i] = t->strides[i];
@@ -192,7 +211,7 @@ int kv_tensor_map(int dev, const blkattn_tensor* t, const CUtensorMap** out) {
                               (cuuint64_t)t->sizes[0]};
   const cuuint64_t strides[3] = {(cuuint64_t)t->strides[2] * 2, (cuuint64_t)t->strides[1] * 2,
                                  (cuuint64_t)t->strides[0] * 2};
-  const cuuint32_t box[4] = {64, 64, 1, 1};
+  const cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = g_encode(&e.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, estr,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -230,6 +249,7 @@ int ensure_workspace(DeviceState* s, size_t bytes, cudaStream_t stream) {
 struct Checked {
   int64_t B, Hq, Hkv, Tq, Tmax, d;
   Elt elt;
+  bool prefill_ok;  // no bias and q rows movable by TMA (see make_plan)
 };
 
 int validate_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
@@ -287,6 +307,10 @@ int validate_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn
     return BLKATTN_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return BLKATTN_ERR_UNSUPPORTED;
   c->elt = (q->dtype == BLKATTN_BF16) ? Elt::BF16 : Elt::F32;
+  c->prefill_ok = bias == nullptr && q->strides[3] == 1 &&
+                  (reinterpret_cast<uintptr_t>(q->data) % 16) == 0 &&
+                  (q->strides[0] * 2) % 16 == 0 && (q->strides[1] * 2) % 16 == 0 &&
+                  (q->strides[2] * 2) % 16 == 0;
   return BLKATTN_OK;
 }
 
@@ -339,19 +363,26 @@ FwdParams fill_params(const blkattn_tensor* q, const blkattn_tensor* k, const bl
 }
 
 // Enqueue the split-KV kernel and, with more than one split, the merge.
-int launch_fwd(const FwdParams& p, const Checked& c, const Plan& pl, const blkattn_tensor* k,
-               const blkattn_tensor* v, cudaStream_t stream) {
+int launch_fwd(const FwdParams& p, const Checked& c, const Plan& pl, const blkattn_tensor* q,
+               const blkattn_tensor* k, const blkattn_tensor* v, cudaStream_t stream) {
   cudaError_t le;
-  if (pl.cfg.kernel == blkattn::Kernel::TensorCore) {
+  if (pl.cfg.kernel == blkattn::Kernel::TensorCore || pl.cfg.kernel == blkattn::Kernel::Prefill) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return BLKATTN_ERR_CUDA;
     const CUtensorMap* mk = nullptr;
     const CUtensorMap* mv = nullptr;
-    int st = kv_tensor_map(dev, k, &mk);
+    int st = kv_tensor_map(dev, k, 64, &mk);
     if (st != BLKATTN_OK) return st;
-    st = kv_tensor_map(dev, v, &mv);
+    st = kv_tensor_map(dev, v, 64, &mv);
     if (st != BLKATTN_OK) return st;
-    le = blkattn::launch_decode_mma(p, (int)c.d, pl.cfg, *mk, *mv, stream);
+    if (pl.cfg.kernel == blkattn::Kernel::Prefill) {
+      const CUtensorMap* mq = nullptr;
+      st = kv_tensor_map(dev, q, 128, &mq);
+      if (st != BLKATTN_OK) return st;
+      le = blkattn::launch_prefill_tc(p, pl.cfg.row_groups, *mq, *mk, *mv, stream);
+    } else {
+      le = blkattn::launch_decode_mma(p, (int)c.d, pl.cfg, *mk, *mv, stream);
+    }
   } else {
     le = blkattn::launch_decode_split(p, c.elt, (int)c.d, pl.cfg, stream);
   }
@@ -391,12 +422,12 @@ int fwd_with_scratch(const blkattn_tensor* q, const blkattn_tensor* k, const blk
   DeviceState* ds = nullptr;
   st = device_state(&ds);
   if (st != BLKATTN_OK) return st;
-  const Plan pl = make_plan(c.B, c.Hq, c.Hkv, c.Tq, c.Tmax, (int)c.d, c.elt, ds->sms);
+  const Plan pl = make_plan(c.B, c.Hq, c.Hkv, c.Tq, c.Tmax, (int)c.d, c.elt, ds->sms, c.prefill_ok);
   if (c.B * pl.cfg.row_groups > 65535) return BLKATTN_ERR_UNSUPPORTED;
   if ((size_t)pl.ws_bytes > scratch_bytes) return BLKATTN_ERR_SCRATCH_LIMIT;
   const FwdParams p = fill_params(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, c, pl,
                                   scratch, ds->err);
-  return launch_fwd(p, c, pl, k, v, stream);
+  return launch_fwd(p, c, pl, q, k, v, stream);
 }
 
 }  // namespace blkattn
@@ -422,7 +453,7 @@ int blkattn_debug_plan(int64_t B, int64_t H_q, int64_t H_kv, int64_t T_q, int64_
       T_max < 1 || (d != 64 && d != 128) || !is_float_dtype(dtype) || num_sms <= 0)
     return BLKATTN_ERR_INVALID_ARG;
   const Plan pl = make_plan(B, H_q, H_kv, T_q, T_max, (int)d,
-                            dtype == BLKATTN_BF16 ? Elt::BF16 : Elt::F32, num_sms);
+                            dtype == BLKATTN_BF16 ? Elt::BF16 : Elt::F32, num_sms, true);
   plan->kernel = (int32_t)pl.cfg.kernel;
   plan->rows_per_cta = pl.cfg.rows_per_cta;
   plan->row_groups = pl.cfg.row_groups;
@@ -448,7 +479,7 @@ int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_
   DeviceState* ds = nullptr;
   st = device_state(&ds);
   if (st != BLKATTN_OK) return st;
-  const Plan pl = make_plan(c.B, c.Hq, c.Hkv, c.Tq, c.Tmax, (int)c.d, c.elt, ds->sms);
+  const Plan pl = make_plan(c.B, c.Hq, c.Hkv, c.Tq, c.Tmax, (int)c.d, c.elt, ds->sms, c.prefill_ok);
   if (c.B * pl.cfg.row_groups > 65535) return BLKATTN_ERR_UNSUPPORTED;
   if (pl.ws_bytes > 0) {
     st = ensure_workspace(ds, (size_t)pl.ws_bytes, stream);
@@ -456,7 +487,7 @@ int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_
   }
   const FwdParams p = fill_params(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, c, pl,
                                   ds->ws, ds->err);
-  return launch_fwd(p, c, pl, k, v, stream);
+  return launch_fwd(p, c, pl, q, k, v, stream);
 }
 
 int blkattn_merge(const blkattn_states* a, const blkattn_states* b, const blkattn_states* out,

@@ -54,7 +54,7 @@ struct FwdParams {
 };
 
 // Split-KV kernel configuration chosen by the planner.
-enum class Kernel : int { CudaCore = 0, TensorCore = 1 };
+enum class Kernel : int { CudaCore = 0, TensorCore = 1, Prefill = 2 };
 struct DecodeConfig {
   Kernel kernel;
   int rows_per_cta;  // CUDA-core: 1, 2, 4 or 8; tensor-core: 16, 32 or 48
@@ -86,6 +86,12 @@ size_t decode_smem_bytes(Elt elt, int d, const DecodeConfig& cfg);
 cudaError_t launch_decode_mma(const FwdParams& p, int d, const DecodeConfig& cfg,
                               const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, cudaStream_t stream);
 size_t decode_mma_smem_bytes(int d, int mt);
+
+// Causal prefill on tcgen05 (bf16, d = 128, no bias): one CTA per 128 query
+// rows of one head; maps: Q box {64, 128}, K/V box {64, 64}, all 128-byte swizzle.
+cudaError_t launch_prefill_tc(const FwdParams& p, int n_qtiles, const CUtensorMap& tmq, const CUtensorMap& tmk,
+                              const CUtensorMap& tmv, cudaStream_t stream);
+int prefill_tc_smem_bytes();
 
 // Validation only (no CUDA call), and blkattn_fwd with caller-given scratch
 // for the per-split states (no allocation; BLKATTN_ERR_SCRATCH_LIMIT when the

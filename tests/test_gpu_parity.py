@@ -348,3 +348,73 @@ def test_empty_calls_are_no_ops():
     blkattn.fwd(z(inp["q"]), z(inp["k"]), z(inp["v"]), z(inp["seqlens"]), z(inp["qpos"]), None, 0.1, out, lse)
     torch.cuda.synchronize()
     assert blkattn.check_device_error() == 0
+
+
+# ------------------------------------------------------------ tcgen05 prefill kernel
+
+def plan_of(inp):
+    s_q = inp["q"]
+    B, Hq, Tq, d = s_q.shape
+    Hkv, Tmax = inp["k"].shape[1], inp["k"].shape[2]
+    dt = torch.bfloat16 if s_q.dtype == torch.bfloat16 else torch.float32
+    return blkattn.debug_plan(B, Hq, Hkv, Tq, Tmax, d, dt, torch.cuda.get_device_properties(0).multi_processor_count)
+
+
+@pytest.mark.parametrize("case", ["causal", "gqa_cache", "noncausal", "neg_pos", "short_len", "tail"])
+def test_prefill_kernel_cases(case):
+    seed = ["causal", "gqa_cache", "noncausal", "neg_pos", "short_len", "tail"].index(case)
+    if case == "causal":
+        B, Hq, Hkv, Tq, Tmax = 2, 2, 2, 300, 300
+        seqlens = [300, 300]
+        qpos = [list(range(Tq))] * B
+    elif case == "gqa_cache":  # new rows after a cache: positions L..L+Tq-1
+        B, Hq, Hkv, Tq, Tmax = 2, 4, 2, 130, 700
+        seqlens = [650, 700]
+        qpos = [list(range(520, 650)), list(range(570, 700))]
+    elif case == "noncausal":
+        B, Hq, Hkv, Tq, Tmax = 1, 2, 1, 200, 333
+        seqlens = [333]
+        qpos = [[332] * Tq]
+    elif case == "neg_pos":  # some rows see nothing, one tile sees nothing at all
+        B, Hq, Hkv, Tq, Tmax = 1, 2, 2, 256, 256
+        seqlens = [256]
+        qpos = [[-1] * 128 + list(range(-60, 68))]
+    elif case == "short_len":  # cache shorter than the positions
+        B, Hq, Hkv, Tq, Tmax = 2, 2, 1, 192, 500
+        seqlens = [100, 0]
+        qpos = [list(range(192)), list(range(192))]
+    else:  # T_q not a multiple of 128, T_max not a multiple of 64
+        B, Hq, Hkv, Tq, Tmax = 1, 3, 1, 129, 129
+        seqlens = [129]
+        qpos = [list(range(129))]
+    inp = make_case(B, Hq, Hkv, Tq, Tmax, 128, "bf16", seqlens, qpos, seed=seed)
+    assert plan_of(inp)["kernel"] == 2
+    _, _, o, l = run_gpu(inp)
+    ref = run_oracle(inp)
+    assert_parity(o, l, ref, BF16_TOL_O, BF16_TOL_L)
+    raw, _, ob, lb = run_gpu(inp, out_dtype=torch.bfloat16)
+    assert_parity(ob, lb, ref, BF16_TOL_O, BF16_TOL_L, out_raw=raw, bf16_out=True)
+
+
+def test_prefill_kernel_poisoned_padding():
+    B, Hq, Hkv, Tq, Tmax = 1, 2, 2, 200, 512
+    qpos = [list(range(100, 300))]
+    clean = make_case(B, Hq, Hkv, Tq, Tmax, 128, "bf16", [300], qpos)
+    dirty = {k: (v.clone() if torch.is_tensor(v) else v) for k, v in clean.items()}
+    dirty["k"][:, :, 300:] = float("nan")
+    dirty["v"][:, :, 300:] = float("inf")
+    assert plan_of(clean)["kernel"] == 2
+    _, _, o1, l1 = run_gpu(clean)
+    _, _, o2, l2 = run_gpu(dirty)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+    assert_parity(o1, l1, run_oracle(clean), BF16_TOL_O, BF16_TOL_L)
+
+
+def test_prefill_shape_with_bias_uses_the_split_kernel():
+    B, Hq, Hkv, Tq, Tmax = 1, 2, 1, 160, 160
+    bias = torch.zeros(B, 1, Tq, Tmax)
+    bias[0, 0, :, 5:37] = -math.inf
+    inp = make_case(B, Hq, Hkv, Tq, Tmax, 128, "bf16", [160], [list(range(Tq))], bias)
+    _, _, o, l = run_gpu(inp)
+    assert_parity(o, l, run_oracle(inp), BF16_TOL_O, BF16_TOL_L)
