@@ -69,17 +69,17 @@ def test_static_scratch_matches_blkattn_fwd_on_consecutive_calls():
 
 
 def test_static_scratch_refuses_problems_beyond_its_size():
-    # many grouped query heads on one KV head, few rows each: the split-KV
-    # plan (T_q < 64) with a large per-split state
+    # 32 packed query rows per KV head (8 grouped heads x 4 rows) over a long
+    # cache: a split plan whose per-split states outgrow the static array
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    B, Hkv, Tq, Tmax, d = 1, 1, 30, 4096, 128
-    Hq = 64
+    B, Hq, Hkv, Tq, d = 1, 64, 8, 4, 128
+    Tmax = 16384
     while True:
         plan = blkattn.debug_plan(B, Hq, Hkv, Tq, Tmax, d, torch.bfloat16, sms)
         if plan["n_splits"] > 1 and plan["workspace_bytes"] > blkattn.STATIC_SCRATCH_BYTES:
             break
-        Hq *= 2
-        assert Hq <= 4096, "no over-limit split plan found"
+        Tmax *= 2
+        assert Tmax <= 262144, "no over-limit split plan found"
     g = torch.Generator().manual_seed(0)
     q = torch.randn(B, Hq, Tq, d, generator=g).to(torch.bfloat16).cuda()
     k = torch.randn(B, Hkv, Tmax, d, generator=g).to(torch.bfloat16).cuda()
