@@ -71,14 +71,15 @@ Plan make_plan(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tmax, int
   Plan pl;
   const int64_t rows = (Hq / Hkv) * Tq;  // query rows that read one KV head
   if (prefill_ok && elt == Elt::BF16 && d == 128 && Tq >= 64 && B <= 65535) {
-    // many query rows per head: 128-row query tiles on tcgen05, no splits
+    // many query rows per head: two 128-row query tiles per CTA on tcgen05,
+    // no splits
     pl.cfg.kernel = blkattn::Kernel::Prefill;
-    pl.cfg.rows_per_cta = 128;
-    pl.cfg.row_groups = (int)((Tq + 127) / 128);
+    pl.cfg.rows_per_cta = 256;
+    pl.cfg.row_groups = (int)((Tq + 255) / 256);
     pl.cfg.warps = 4;
     pl.cfg.stages = 2;
-    pl.tile = 64;
-    pl.cfg.chunk = (int)((Tmax + 63) / 64 * 64);
+    pl.tile = 128;
+    pl.cfg.chunk = (int)((Tmax + 127) / 128 * 128);
     pl.cfg.n_splits = 1;
     pl.ctas = (int64_t)pl.cfg.row_groups * Hq * B;
     pl.ws_bytes = 0;
@@ -371,9 +372,11 @@ int launch_fwd(const FwdParams& p, const Checked& c, const Plan& pl, const blkat
     if (cudaGetDevice(&dev) != cudaSuccess) return BLKATTN_ERR_CUDA;
     const CUtensorMap* mk = nullptr;
     const CUtensorMap* mv = nullptr;
-    int st = kv_tensor_map(dev, k, 64, &mk);
+    // K/V boxes: 64 keys for the split-KV kernel, 128 for the prefill kernel
+    const int kv_rows = (pl.cfg.kernel == blkattn::Kernel::Prefill) ? 128 : 64;
+    int st = kv_tensor_map(dev, k, kv_rows, &mk);
     if (st != BLKATTN_OK) return st;
-    st = kv_tensor_map(dev, v, 64, &mv);
+    st = kv_tensor_map(dev, v, kv_rows, &mv);
     if (st != BLKATTN_OK) return st;
     if (pl.cfg.kernel == blkattn::Kernel::Prefill) {
       const CUtensorMap* mq = nullptr;
@@ -422,7 +425,8 @@ int fwd_with_scratch(const blkattn_tensor* q, const blkattn_tensor* k, const blk
   DeviceState* ds = nullptr;
   st = device_state(&ds);
   if (st != BLKATTN_OK) return st;
-  const Plan pl = make_plan(c.B, c.Hq, c.Hkv, c.Tq, c.Tmax, (int)c.d, c.elt, ds->sms, c.prefill_ok);
+  const Plan pl = make_plan(c.B, c.Hq, c.Hkv, c.Tq, c.Tmax, (int)c.d, c.elt, ds->sms,
+                            c.prefill_ok && scale > 0.f);
   if (c.B * pl.cfg.row_groups > 65535) return BLKATTN_ERR_UNSUPPORTED;
   if ((size_t)pl.ws_bytes > scratch_bytes) return BLKATTN_ERR_SCRATCH_LIMIT;
   const FwdParams p = fill_params(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, c, pl,
@@ -479,7 +483,8 @@ int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_
   DeviceState* ds = nullptr;
   st = device_state(&ds);
   if (st != BLKATTN_OK) return st;
-  const Plan pl = make_plan(c.B, c.Hq, c.Hkv, c.Tq, c.Tmax, (int)c.d, c.elt, ds->sms, c.prefill_ok);
+  const Plan pl = make_plan(c.B, c.Hq, c.Hkv, c.Tq, c.Tmax, (int)c.d, c.elt, ds->sms,
+                            c.prefill_ok && scale > 0.f);
   if (c.B * pl.cfg.row_groups > 65535) return BLKATTN_ERR_UNSUPPORTED;
   if (pl.ws_bytes > 0) {
     st = ensure_workspace(ds, (size_t)pl.ws_bytes, stream);

@@ -87,9 +87,10 @@ cudaError_t launch_decode_mma(const FwdParams& p, int d, const DecodeConfig& cfg
                               const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, cudaStream_t stream);
 size_t decode_mma_smem_bytes(int d, int mt);
 
-// Causal prefill on tcgen05 (bf16, d = 128, no bias): one CTA per 128 query
-// rows of one head; maps: Q box {64, 128}, K/V box {64, 64}, all 128-byte swizzle.
-cudaError_t launch_prefill_tc(const FwdParams& p, int n_qtiles, const CUtensorMap& tmq, const CUtensorMap& tmk,
+// Causal prefill on tcgen05 (bf16, d = 128, no bias): one CTA per 256 query
+// rows of one head (two 128-row query tiles); maps: Q and K/V boxes {64, 128},
+// all 128-byte swizzle.
+cudaError_t launch_prefill_tc(const FwdParams& p, int n_pairs, const CUtensorMap& tmq, const CUtensorMap& tmk,
                               const CUtensorMap& tmv, cudaStream_t stream);
 int prefill_tc_smem_bytes();
 

@@ -2,27 +2,32 @@
 //
 // Exact blocked attention ("Chapter 33: inference compute optimisation"
 // §33.2, Algorithm 33.1; §33.3 for the on-chip tiling and the skipping of
-// fully invisible blocks): one CTA owns 128 consecutive query rows of one
-// head and walks the key tiles of 64 keys that hold any key visible to them,
-// keeping per row the statistics (m, l, u) of eq. 33.3 with u in tensor
-// memory.  Key tiles beyond the CTA's last visible key are never loaded.
+// fully invisible blocks): a CTA owns TWO query tiles of 128 consecutive rows
+// of one head (rows [i0, i0 + 256)) and walks the key tiles of 128 keys that
+// hold any key visible to them, keeping per row the statistics (m, l, u) of
+// eq. 33.3 with u in tensor memory.  Both query tiles share every K/V tile
+// the CTA loads; key tiles beyond the CTA's last visible key are never loaded.
 //
-//   S_j  = Q K_j^T         tcgen05.mma M=128 N=64  K=16 x 8   (smem x smem -> TMEM)
-//   U   += P_j V_j         tcgen05.mma M=128 N=128 K=16 x 4 x 2 (P from TMEM, V smem)
+//   S_j  = Q K_j^T     tcgen05.mma M=128 N=128 K=16 x 8      (smem x smem -> TMEM)
+//   U   += P_j V_j     tcgen05.mma M=128 N=128 K=16 x 8 x 2  (P from TMEM, V smem)
 //
-// Roles (192 threads): warps 0-3 = one thread per query row (TMEM lane):
-// scores, mask by select, online statistics, P; warp 4 = TMA producer (Q
-// once, K/V tiles into a 2-stage ring); warp 5 = TMEM allocation and the
-// single thread that issues every MMA.  Two S buffers let S_{j+1} be formed
-// while the rows work on S_j; P_j is written back over S_j's columns as
-// bf16 P_hi and P_lo (P = P_hi + P_lo to ~16 bits, so the PV product keeps
-// ~2^-17 relative accuracy although P is not an input).
+// Roles (320 threads): warps 0-3 and 4-7 = one thread per query row of the
+// first / second query tile (a TMEM lane each): scores, mask by select,
+// online statistics, P; warp 8 = TMA producer (both Q tiles once, K and V
+// tiles into 2-stage rings released separately); warp 9 = TMEM allocation
+// and the single thread that issues every MMA.  Each query tile has one S
+// buffer in TMEM; P_j is written over it as bf16 P_hi and P_lo (P = P_hi +
+// P_lo to ~16 bits, so the PV product keeps ~2^-17 relative accuracy
+// although P is not an input), and S_{j+1} is issued right after U += P_j V_j
+// (products execute in issue order).  The two query tiles ping-pong: while
+// one tile's rows compute P, the tensor core runs the other tile's products.
 //
 // Online rescaling is lazy: a row keeps its reference maximum m until a tile
 // raises the row maximum by more than 8 (base-2 units); only then is its U
-// row rescaled in TMEM (after the previous PV product has completed).  With
-// any reference m >= (true max - 8) the state (m, l, u) still represents the
-// same set (eqs. 33.4-33.5 hold for any common reference), and P <= 2^8.
+// row rescaled in TMEM.  S_j ready implies U += P_{j-1} V_{j-1} completed, so
+// the rescale needs no extra wait.  With any reference m >= (true max - 8)
+// the state (m, l, u) still represents the same set (eqs. 33.4-33.5 hold for
+// any common reference), and P <= 2^8.
 //
 // Rows with no visible key keep the empty state and get out = 0,
 // lse = -inf.  V rows of the last tile past the CTA's last visible key (cache
@@ -41,26 +46,29 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kLazyRescale = 8.f;  // base-2 units: rescale only when max grows by > 2^8
 
-constexpr int BM = 128;  // query rows per CTA (TMEM lanes)
-constexpr int BN = 64;   // keys per tile
+constexpr int BM = 128;  // query rows per query tile (TMEM lanes)
+constexpr int QT = 2;    // query tiles per CTA
+constexpr int BN = 128;  // keys per tile
 constexpr int D = 128;   // head dim
 constexpr int STAGES = 2;
-constexpr int kQBox = BM * 128;    // one 64-dim (128-byte) box of Q: 16 KB
-constexpr int kKVBox = BN * 128;   // one 64-dim box of a K or V tile: 8 KB
-constexpr int kQBytes = 2 * kQBox;
-constexpr int kKVTile = 2 * kKVBox;
+constexpr int kBox = 128 * 128;       // one 64-dim (128-byte) box of 128 rows: 16 KB
+constexpr int kTileBytes = 2 * kBox;  // one Q, K or V tile of 128 rows x 128 dims
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kQBytes;
-constexpr int kOffV = kOffK + STAGES * kKVTile;
-constexpr int kOffBar = kOffV + STAGES * kKVTile;
-// q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_done, drain
-constexpr int kNumBars = 1 + 3 * STAGES + 6;
+constexpr int kOffK = kOffQ + QT * kTileBytes;
+constexpr int kOffV = kOffK + STAGES * kTileBytes;
+constexpr int kOffBar = kOffV + STAGES * kTileBytes;
+// q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[QT], p_full[QT], drain
+constexpr int kNumBars = 1 + 4 * STAGES + QT + QT + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align to 1024
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0;    // S buffers at [0, 64) and [64, 128); P_b over S_b
-constexpr uint32_t kColO = 128;  // U (the unnormalised output) at [128, 256)
-constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTileCols = 256;  // per query tile: S / P at [0, 128), U at [128, 256)
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColPlo = 64;     // P_hi at [0, 64), P_lo at [64, 128) (bf16 pairs)
+constexpr uint32_t kColO = 128;
+constexpr int kThreads = 320;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr uint32_t kIdescQK = tc::idesc_bf16(BM, BN, 0, 0);  // Q, K both K-major
 constexpr uint32_t kIdescPV = tc::idesc_bf16(BM, D, 0, 1);   // P (TMEM), V MN-major
 
@@ -70,67 +78,70 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return pol;
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmq,
                       const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
+  uint64_t* k_full = q_full + 1;
   uint64_t* v_full = k_full + STAGES;
-  uint64_t* kv_empty = v_full + STAGES;
-  uint64_t* s_full = kv_empty + STAGES;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 2;
-  uint64_t* drain = o_done + 1;
-  int* misc = reinterpret_cast<int*>(sm + kOffMisc);  // tmem base, cta_end, cta_min, timeout
+  uint64_t* k_empty = v_full + STAGES;
+  uint64_t* v_empty = k_empty + STAGES;
+  uint64_t* s_full = v_empty + STAGES;  // [QT]
+  uint64_t* p_full = s_full + QT;       // [QT]
+  uint64_t* drain = p_full + QT;
+  // misc: [0] tmem base, [1 + 2x] end of query tile x, [2 + 2x] min end of x, [5] timeout
+  int* misc = reinterpret_cast<int*>(sm + kOffMisc);
 
-  const int qt = gridDim.x - 1 - blockIdx.x;  // the longest (latest) query tiles first
+  const int pair = gridDim.x - 1 - blockIdx.x;  // the longest (latest) query tiles first
   const int h = blockIdx.y;
   const int b = blockIdx.z;
   const int hk = h / p.G;
-  const int i0 = qt * BM;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int x = warp >> 2;  // query tile of a row warp (0 or 1)
+  const int i0 = (2 * pair + (warp < 8 ? x : 0)) * BM;
 
-  // ---- visibility of this CTA's rows (integers) ----
+  // ---- visibility of the rows (integers) ----
   int len = p.seqlens[b * p.sl_s];
   len = len < 0 ? 0 : (len > p.Tmax ? p.Tmax : len);
   if (threadIdx.x == 0) {
-    misc[1] = 0;
-    misc[2] = 0x7fffffff;
-    misc[3] = 0;
+    misc[1] = 0; misc[2] = 0x7fffffff;
+    misc[3] = 0; misc[4] = 0x7fffffff;
+    misc[5] = 0;
   }
   __syncthreads();
   int my_end = 0;
   bool my_row = false;
-  if (warp < 4) {
-    const int i = i0 + (int)threadIdx.x;
-    if (i < p.Tq) {
-      const int pos = p.qpos[b * p.qp_sb + i * p.qp_si];
-      my_end = pos < 0 ? 0 : (pos >= len ? len : pos + 1);
-      my_row = true;
-      atomicMax(&misc[1], my_end);
-      atomicMin(&misc[2], my_end);
-    }
+  const int row_i = i0 + (int)(threadIdx.x & 127);
+  if (warp < 8 && row_i < p.Tq) {
+    const int pos = p.qpos[b * p.qp_sb + row_i * p.qp_si];
+    my_end = pos < 0 ? 0 : (pos >= len ? len : pos + 1);
+    my_row = true;
+    atomicMax(&misc[1 + 2 * x], my_end);
+    atomicMin(&misc[2 + 2 * x], my_end);
   }
   __syncthreads();
-  const int cta_end = misc[1];
-  const int cta_min = misc[2];
-  const int n_tiles = (cta_end + BN - 1) / BN;
-  const int64_t out_row = (int64_t)b * p.o_sb + (int64_t)h * p.o_sh + (int64_t)(i0 + (int)threadIdx.x) * p.o_si;
-  const int64_t lse_idx = (int64_t)b * p.l_sb + (int64_t)h * p.l_sh + (int64_t)(i0 + (int)threadIdx.x) * p.l_si;
-  if (n_tiles == 0) {  // no row of this tile sees any key: the defined output
-    if (my_row) {
-      for (int d = 0; d < D; ++d) {
-        if (p.out_bf16)
-          static_cast<__nv_bfloat16*>(p.out)[out_row + (int64_t)d * p.o_sd] = __float2bfloat16_rn(0.f);
-        else
-          static_cast<float*>(p.out)[out_row + (int64_t)d * p.o_sd] = 0.f;
-      }
-      p.lse[lse_idx] = kNegInf;
+  const int n_t0 = (misc[1] + BN - 1) / BN;
+  const int n_t1 = (misc[3] + BN - 1) / BN;
+  const int n_max = max(n_t0, n_t1);
+  const int cta_end = max(misc[1], misc[3]);
+  const int64_t out_row = (int64_t)b * p.o_sb + (int64_t)h * p.o_sh + (int64_t)row_i * p.o_si;
+  const int64_t lse_idx = (int64_t)b * p.l_sb + (int64_t)h * p.l_sh + (int64_t)row_i * p.l_si;
+
+  auto write_empty_row = [&]() {  // the defined output of a row with no visible key
+    for (int d = 0; d < D; ++d) {
+      if (p.out_bf16)
+        static_cast<__nv_bfloat16*>(p.out)[out_row + (int64_t)d * p.o_sd] = __float2bfloat16_rn(0.f);
+      else
+        static_cast<float*>(p.out)[out_row + (int64_t)d * p.o_sd] = 0.f;
     }
+    p.lse[lse_idx] = kNegInf;
+  };
+  if (n_max == 0) {
+    if (my_row) write_empty_row();
     return;
   }
 
@@ -139,17 +150,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 4);  // one arrival per row warp
+    for (int t = 0; t < QT; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 4);  // one arrival per row warp of the query tile
     }
-    mbar_init(o_done, 1);
     mbar_init(drain, 1);
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc::alloc(reinterpret_cast<uint32_t*>(&misc[0]), kTmemCols);
     tc::relinquish();
   }
@@ -161,230 +172,308 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t sK = smem_u32(sm + kOffK);
   const uint32_t sV = smem_u32(sm + kOffV);
 
-  if (warp == 4) {
+  if (warp == kTmaWarp) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();  // K/V tiles are re-read by the other query tiles
-      mbar_arrive_expect_tx(q_full, kQBytes);
-      tma_load_4d(sm + kOffQ, &tmq, 0, i0, h, b, q_full, pol_q);
-      tma_load_4d(sm + kOffQ + kQBox, &tmq, 64, i0, h, b, q_full, pol_q);
-      int issued = 0;
-      for (int j = 0; j < n_tiles; ++j) {
+      const int q0 = 2 * pair * BM;
+      mbar_arrive_expect_tx(q_full, QT * kTileBytes);
+      for (int t = 0; t < QT; ++t) {
+        tma_load_4d(sm + kOffQ + t * kTileBytes, &tmq, 0, q0 + t * BM, h, b, q_full, pol_q);
+        tma_load_4d(sm + kOffQ + t * kTileBytes + kBox, &tmq, 64, q0 + t * BM, h, b, q_full, pol_q);
+      }
+      int k_issued = 0, v_issued = 0;
+      bool ok = true;
+      for (int j = 0; j < n_max && ok; ++j) {
         const int s = j % STAGES;
-        if (j >= STAGES && !mbar_wait(&kv_empty[s], ((j / STAGES) - 1) & 1)) {
-          record_error(p.err, kErrTimeout);
-          misc[3] = 1;
-          break;
-        }
         const int key0 = j * BN;
-        unsigned char* kd = sm + kOffK + s * kKVTile;
-        unsigned char* vd = sm + kOffV + s * kKVTile;
-        mbar_arrive_expect_tx(&k_full[s], kKVTile);
+        if (j >= STAGES && !mbar_wait(&k_empty[s], ((j / STAGES) - 1) & 1)) { ok = false; break; }
+        unsigned char* kd = sm + kOffK + s * kTileBytes;
+        mbar_arrive_expect_tx(&k_full[s], kTileBytes);
         tma_load_4d(kd, &tmk, 0, key0, hk, b, &k_full[s], pol_kv);
-        tma_load_4d(kd + kKVBox, &tmk, 64, key0, hk, b, &k_full[s], pol_kv);
-        mbar_arrive_expect_tx(&v_full[s], kKVTile);
+        tma_load_4d(kd + kBox, &tmk, 64, key0, hk, b, &k_full[s], pol_kv);
+        k_issued = j + 1;
+        if (j >= STAGES && !mbar_wait(&v_empty[s], ((j / STAGES) - 1) & 1)) { ok = false; break; }
+        unsigned char* vd = sm + kOffV + s * kTileBytes;
+        mbar_arrive_expect_tx(&v_full[s], kTileBytes);
         tma_load_4d(vd, &tmv, 0, key0, hk, b, &v_full[s], pol_kv);
-        tma_load_4d(vd + kKVBox, &tmv, 64, key0, hk, b, &v_full[s], pol_kv);
-        issued = j + 1;
+        tma_load_4d(vd + kBox, &tmv, 64, key0, hk, b, &v_full[s], pol_kv);
+        v_issued = j + 1;
       }
       // every issued copy must land before the CTA can exit
-      if (!mbar_wait(q_full, 0)) misc[3] = 1;
-      for (int j = issued - STAGES < 0 ? 0 : issued - STAGES; j < issued; ++j) {
-        const int s = j % STAGES;
-        if (!mbar_wait(&k_full[s], (j / STAGES) & 1) || !mbar_wait(&v_full[s], (j / STAGES) & 1)) {
-          record_error(p.err, kErrTimeout);
-          misc[3] = 1;
-        }
+      if (!mbar_wait(q_full, 0)) ok = false;
+      for (int j = k_issued - STAGES < 0 ? 0 : k_issued - STAGES; j < k_issued; ++j)
+        if (!mbar_wait(&k_full[j % STAGES], (j / STAGES) & 1)) ok = false;
+      for (int j = v_issued - STAGES < 0 ? 0 : v_issued - STAGES; j < v_issued; ++j)
+        if (!mbar_wait(&v_full[j % STAGES], (j / STAGES) & 1)) ok = false;
+      if (!ok) {
+        record_error(p.err, kErrTimeout);
+        misc[5] = 1;
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ---------------- MMA issue (one thread) ----------------
     if (lane == 0) {
       bool ok = mbar_wait(q_full, 0);
-      auto issue_pv = [&](int jj) -> bool {
-        const int bb = jj & 1;
-        const int ss = jj % STAGES;
-        if (!mbar_wait(&v_full[ss], (jj / STAGES) & 1)) return false;
-        if (!mbar_wait(&p_full[bb], (jj >> 1) & 1)) return false;
-        tc::fence_after();
-        const uint32_t vbase = sV + ss * kKVTile;
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {  // P_hi, then P_lo
-#pragma unroll
-          for (int ks = 0; ks < BN / 16; ++ks) {
-            // B = V rows [16ks, 16ks+16) (keys, K) x 128 dims (N, two 64-dim boxes 8 KB apart)
-            const uint64_t bdesc = tc::smem_desc(vbase + ks * 16 * 128, kKVBox, 1024);
-            const uint32_t acol = tb + kColS + 64 * bb + 32 * part + 8 * ks;
-            tc::mma_ts(tb + kColO, acol, bdesc, kIdescPV, (jj > 0 || part > 0 || ks > 0) ? 1u : 0u);
-          }
-        }
-        tc::commit(o_done);
-        tc::commit(&kv_empty[ss]);
-        return true;
-      };
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int bb = j & 1;
-        const int s = j % STAGES;
-        if (!mbar_wait(&k_full[s], (j / STAGES) & 1)) { ok = false; break; }
-        tc::fence_after();
-        const uint32_t kbase = sK + s * kKVTile;
+      // S_jj = Q_t K_jj^T into query tile t's S buffer
+      auto issue_qk = [&](int t, int jj) {
+        const uint32_t kbase = sK + (jj % STAGES) * kTileBytes;
+        const uint32_t qbase = sQ + t * kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t adesc = tc::smem_desc(sQ + (ks >> 2) * kQBox + (ks & 3) * 32, 16, 1024);
-          const uint64_t bdesc = tc::smem_desc(kbase + (ks >> 2) * kKVBox + (ks & 3) * 32, 16, 1024);
-          tc::mma_ss(tb + kColS + 64 * bb, adesc, bdesc, kIdescQK, ks > 0 ? 1u : 0u);
+          const uint64_t adesc = tc::smem_desc(qbase + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024);
+          const uint64_t bdesc = tc::smem_desc(kbase + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024);
+          tc::mma_ss(tb + t * kTileCols + kColS, adesc, bdesc, kIdescQK, ks > 0 ? 1u : 0u);
         }
-        tc::commit(&s_full[bb]);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        tc::commit(&s_full[t]);
+      };
+      // U_t += P_jj V_jj (P_hi, then P_lo)
+      auto issue_pv = [&](int t, int jj) {
+        const uint32_t vbase = sV + (jj % STAGES) * kTileBytes;
+        const uint32_t tcol = tb + t * kTileCols;
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+#pragma unroll
+          for (int ks = 0; ks < BN / 16; ++ks) {
+            // B = V rows [16ks, 16ks+16) (keys, K) x 128 dims (N, two 64-dim boxes 16 KB apart)
+            const uint64_t bdesc = tc::smem_desc(vbase + ks * 16 * 128, kBox, 1024);
+            const uint32_t acol = tcol + kColS + part * kColPlo + 8 * ks;
+            tc::mma_ts(tcol + kColO, acol, bdesc, kIdescPV, (jj > 0 || part > 0 || ks > 0) ? 1u : 0u);
+          }
+        }
+      };
+      // prologue: S_0 for both query tiles
+      if (ok && !mbar_wait(&k_full[0], 0)) ok = false;
+      if (ok) {
+        tc::fence_after();
+        if (n_t0 > 0) issue_qk(0, 0);
+        if (n_t1 > 0) issue_qk(1, 0);
+        tc::commit(&k_empty[0]);
       }
-      if (ok && !issue_pv(n_tiles - 1)) ok = false;
+      for (int j = 0; ok && j < n_max; ++j) {
+        const int s = j % STAGES;
+        const bool next = j + 1 < n_max;
+        if (!mbar_wait(&v_full[s], (j / STAGES) & 1)) { ok = false; break; }
+        if (next && !mbar_wait(&k_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1)) { ok = false; break; }
+        for (int t = 0; t < QT && ok; ++t) {
+          const int nt = t == 0 ? n_t0 : n_t1;
+          if (j >= nt) continue;
+          // U += P_j V_j as soon as this query tile's P_j is ready, then
+          // S_{j+1} into the same TMEM columns (issue order = execution order)
+          if (!mbar_wait(&p_full[t], j & 1)) { ok = false; break; }
+          tc::fence_after();
+          issue_pv(t, j);
+          if (j + 1 < nt) issue_qk(t, j + 1);
+        }
+        if (!ok) break;
+        tc::commit(&v_empty[s]);                           // V_j free once these products complete
+        if (next) tc::commit(&k_empty[(j + 1) % STAGES]);  // K_{j+1} likewise
+      }
       if (!ok) {
         record_error(p.err, kErrTimeout);
-        misc[3] = 1;
+        misc[5] = 1;
       }
       // every MMA issued must complete before TMEM is released
       tc::commit(drain);
       if (!mbar_wait(drain, 0)) {
         record_error(p.err, kErrTimeout);
-        misc[3] = 1;
+        misc[5] = 1;
       }
     }
   } else {
-    // ---------------- rows: online softmax statistics ----------------
-    const uint32_t tl = tb + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lane quarter
-    float m_ref = kNegInf;  // reference maximum (base-2 units), -inf = no valid key yet
-    float l = 0.f;
-    bool ok = true;
-    // waits are made warp-uniform: the tensor-memory accesses that follow
-    // are warp-collective
-    auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity));
-    };
-    for (int j = 0; j < n_tiles; ++j) {
-      const int bb = j & 1;
-      if (!wait_all(&s_full[bb], (j >> 1) & 1)) { ok = false; break; }
-      tc::fence_after();
-      uint32_t sa[32], sb2[32];
-      tc::ld32(tl + kColS + 64 * bb, sa);
-      tc::ld32(tl + kColS + 64 * bb + 32, sb2);
-      tc::wait_ld();
-      const int key0 = j * BN;
-      const bool need_mask = key0 + BN > cta_min;
-      float x[64];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        x[c] = __uint_as_float(sa[c]) * p.scale_log2;
-        x[32 + c] = __uint_as_float(sb2[c]) * p.scale_log2;
-      }
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) x[c] = (key0 + c < my_end) ? x[c] : kNegInf;
-      }
-      float mt = x[0];
-#pragma unroll
-      for (int c = 1; c < 64; ++c) mt = fmaxf(mt, x[c]);
-      float alpha = 1.f;
-      bool resc = false;
-      if (mt != kNegInf) {
-        if (m_ref == kNegInf) {
-          m_ref = mt;  // first block with a valid key initialises the state
-        } else if (mt > m_ref + kLazyRescale) {
-          alpha = fast_exp2(m_ref - mt);
-          m_ref = mt;
-          l *= alpha;
-          resc = true;
-        }
-      }
-      if (__any_sync(0xffffffffu, resc)) {
-        // U rows change reference: wait for the previous PV product, rescale.
-        // (S_j being ready implies PV_{j-2} completed, so o_done is at phase
-        // j-1 or j and the parity wait is unambiguous.)
-        if (!wait_all(o_done, (j - 1) & 1)) { ok = false; break; }
+    // ---------------- rows: online softmax statistics (query tile x) ----------------
+    const int n_mine = x == 0 ? n_t0 : n_t1;
+    const int my_min = misc[2 + 2 * x];
+    if (n_mine == 0) {
+      if (my_row) write_empty_row();
+    } else {
+      const uint32_t tl = tb + x * kTileCols + ((uint32_t)(32 * (warp & 3)) << 16);  // lane quarter
+      float m_ref = kNegInf;  // reference maximum (base-2 units), -inf = no valid key yet
+      float l = 0.f;
+      bool ok = true;
+      // waits are made warp-uniform: the tensor-memory accesses that follow
+      // are warp-collective
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+      };
+      for (int j = 0; j < n_mine; ++j) {
+        if (!wait_all(&s_full[x], j & 1)) { ok = false; break; }
         tc::fence_after();
+        float xs[128];
+        {
+          uint32_t r[32];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            tc::ld32(tl + kColS + 32 * q4, r);
+            tc::wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) xs[32 * q4 + c] = __uint_as_float(r[c]);
+          }
+        }
+        const int key0 = j * BN;
+        // the mask (select, diagonal tiles only) before any arithmetic
+        if (key0 + BN > my_min) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) xs[c] = (key0 + c < my_end) ? xs[c] : kNegInf;
+        }
+        // block maximum on the raw scores (scale > 0), a tree of short chains
+        float mx8[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) mx8[c] = xs[c];
+#pragma unroll
+        for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], xs[c]);
+        const float mraw = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        const float mt = (mraw == kNegInf) ? kNegInf : mraw * p.scale_log2;
+        float alpha = 1.f;
+        bool resc = false;
+        if (mt != kNegInf) {
+          if (m_ref == kNegInf) {
+            m_ref = mt;  // first block with a valid key initialises the state
+          } else if (mt > m_ref + kLazyRescale) {
+            alpha = fast_exp2(m_ref - mt);
+            m_ref = mt;
+            l *= alpha;
+            resc = true;
+          }
+        }
+        if (__any_sync(0xffffffffu, resc)) {
+          // U rows change reference (U += P_{j-1} V_{j-1} has completed: S_j
+          // was issued after it)
+#pragma unroll 1
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t r[32];
+            tc::ld32(tl + kColO + 32 * q4, r);
+            tc::wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+            tc::st32(tl + kColO + 32 * q4, r);
+          }
+        }
+        // p = 2^(s * scale_log2 - m): masked entries are -inf and give exactly 0;
+        // a row with no valid key yet has only masked entries in this tile
+        const float m_use = (m_ref == kNegInf) ? 0.f : m_ref;
+        const uint64_t sc2 = f2(p.scale_log2, p.scale_log2);
+        const uint64_t nm2 = f2(-m_use, -m_use);
+        uint64_t lsum[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {  // 32 keys -> 16 columns of P_hi and of P_lo
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int k2 = 32 * q4 + 2 * c;
+            float e0, e1;
+            f2_split(ffma2(f2(xs[k2], xs[k2 + 1]), sc2, nm2), e0, e1);
+            const float p0 = fast_exp2(e0);
+            const float p1 = fast_exp2(e1);
+            lsum[c & 3] = fadd2(lsum[c & 3], f2(p0, p1));
+            split_bf16_trunc(p0, p1, hi[c], lo[c]);
+          }
+          tc::st16(tl + kColS + 16 * q4, hi);
+          tc::st16(tl + kColPlo + 16 * q4, lo);
+        }
+        {
+          float l0, l1, l2, l3, l4, l5, l6, l7;
+          f2_split(lsum[0], l0, l1);
+          f2_split(lsum[1], l2, l3);
+          f2_split(lsum[2], l4, l5);
+          f2_split(lsum[3], l6, l7);
+          l += ((l0 + l1) + (l2 + l3)) + ((l4 + l5) + (l6 + l7));
+        }
+        if (key0 + BN > cta_end) {
+          // last tile of the CTA: zero the V rows past every visible key of
+          // both query tiles (both may do it; the values are the same)
+          const int s = j % STAGES;
+          if (!wait_all(&v_full[s], (j / STAGES) & 1)) { ok = false; break; }
+          unsigned char* vt = sm + kOffV + s * kTileBytes;
+          const int z0 = cta_end - key0;
+          for (int idx = (int)(threadIdx.x & 127); idx < (BN - z0) * 16; idx += 128) {
+            const int r = z0 + (idx >> 4);
+            const int c = idx & 15;  // 16-byte chunk over the 128 dims (two boxes)
+            *reinterpret_cast<uint4*>(vt + (c >> 3) * kBox + r * 128 + (((c & 7) ^ (r & 7)) << 4)) =
+                make_uint4(0, 0, 0, 0);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        tc::wait_st();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[x]);
+      }
+      // ---- epilogue: o = u / l, lse = m + ln l ----
+      // `drain` completes once every MMA of the CTA has (single phase)
+      if (ok && !wait_all(drain, 0)) ok = false;
+      if (!ok) {
+        if (lane == 0) {
+          record_error(p.err, kErrTimeout);
+          misc[5] = 1;
+        }
+      } else {
+        tc::fence_after();
+        const float inv = (m_ref == kNegInf) ? 0.f : 1.f / l;
+        // Every MMA has completed (drain), so the K (query tile 0) or V
+        // (query tile 1) ring is free: stage the 128 x 128 fp32 rows there and
+        // store whole rows with coalesced 16-byte writes.  Row r's 16-byte
+        // chunk c sits at chunk c ^ (r mod 32) (conflict-free both ways).
+        const bool staged = p.o_sd == 1 && !p.out_bf16 && (p.o_si % 4) == 0 &&
+                            (reinterpret_cast<uintptr_t>(p.out) % 16) == 0 && (p.o_sb % 4) == 0 &&
+                            (p.o_sh % 4) == 0;
+        float4* stage = reinterpret_cast<float4*>(sm + (x == 0 ? kOffK : kOffV));
+        const int rr = (int)(threadIdx.x & 127);
 #pragma unroll 1
         for (int q4 = 0; q4 < 4; ++q4) {
           uint32_t r[32];
           tc::ld32(tl + kColO + 32 * q4, r);
           tc::wait_ld();
+          if (staged) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
-          tc::st32(tl + kColO + 32 * q4, r);
-        }
-        tc::wait_st();
-      }
-      uint32_t hi[32], lo[32];
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const int c = q4 * 8 + c4;
+              stage[rr * 32 + (c ^ (rr & 31))] =
+                  make_float4(__uint_as_float(r[4 * c4]) * inv, __uint_as_float(r[4 * c4 + 1]) * inv,
+                              __uint_as_float(r[4 * c4 + 2]) * inv, __uint_as_float(r[4 * c4 + 3]) * inv);
+            }
+          } else if (my_row) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p0 = (x[2 * c] == kNegInf) ? 0.f : fast_exp2(x[2 * c] - m_ref);
-        const float p1 = (x[2 * c + 1] == kNegInf) ? 0.f : fast_exp2(x[2 * c + 1] - m_ref);
-        l += p0 + p1;
-        split_bf16(p0, p1, hi[c], lo[c]);
-      }
-      tc::st32(tl + kColS + 64 * bb, hi);
-      tc::st32(tl + kColS + 64 * bb + 32, lo);
-      if (key0 + BN > cta_end) {
-        // last tile: zero the V rows past the CTA's last visible key
-        const int s = j % STAGES;
-        if (!wait_all(&v_full[s], (j / STAGES) & 1)) { ok = false; break; }
-        unsigned char* vt = sm + kOffV + s * kKVTile;
-        const int z0 = cta_end - key0;
-        for (int idx = threadIdx.x; idx < (BN - z0) * 16; idx += 128) {
-          const int r = z0 + (idx >> 4);
-          const int c = idx & 15;  // 16-byte chunk over the 128 dims (two boxes)
-          *reinterpret_cast<uint4*>(vt + (c >> 3) * kKVBox + r * 128 + (((c & 7) ^ (r & 7)) << 4)) =
-              make_uint4(0, 0, 0, 0);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      }
-      tc::wait_st();
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[bb]);
-    }
-    // ---- epilogue: o = u / l, lse = m + ln l ----
-    // `drain` completes once every MMA of the CTA has (single phase)
-    if (ok && !wait_all(drain, 0)) ok = false;
-    if (!ok) {
-      if (lane == 0) {
-        record_error(p.err, kErrTimeout);
-        misc[3] = 1;
-      }
-    } else {
-      tc::fence_after();
-      const float inv = (m_ref == kNegInf) ? 0.f : 1.f / l;
-#pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t r[32];
-        tc::ld32(tl + kColO + 32 * q4, r);
-        tc::wait_ld();
-        if (my_row) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float o = __uint_as_float(r[c]) * inv;
-            const int64_t oi = out_row + (int64_t)(32 * q4 + c) * p.o_sd;
-            if (p.out_bf16)
-              static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
-            else
-              static_cast<float*>(p.out)[oi] = o;
+            for (int c = 0; c < 32; ++c) {
+              const float o = __uint_as_float(r[c]) * inv;
+              const int64_t oi = out_row + (int64_t)(32 * q4 + c) * p.o_sd;
+              if (p.out_bf16)
+                static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+              else
+                static_cast<float*>(p.out)[oi] = o;
+            }
           }
         }
+        if (staged) {
+          asm volatile("bar.sync %0, 128;" ::"r"(1 + x) : "memory");  // this query tile's 4 warps
+          const int w4 = warp & 3;
+          const int row0 = (2 * pair + x) * BM;
+          for (int r2 = w4; r2 < BM; r2 += 4) {
+            if (row0 + r2 >= p.Tq) break;
+            const float4 v4 = stage[r2 * 32 + (lane ^ (r2 & 31))];
+            float* dst = static_cast<float*>(p.out) + (int64_t)b * p.o_sb + (int64_t)h * p.o_sh +
+                         (int64_t)(row0 + r2) * p.o_si;
+            reinterpret_cast<float4*>(dst)[lane] = v4;
+          }
+        }
+        if (my_row) p.lse[lse_idx] = (m_ref == kNegInf) ? kNegInf : (m_ref + __log2f(l)) * kLn2;
       }
-      if (my_row) p.lse[lse_idx] = (m_ref == kNegInf) ? kNegInf : (m_ref + __log2f(l)) * kLn2;
     }
   }
 
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  if (warp == 5) tc::dealloc(tb, kTmemCols);
+  if (warp == kMmaWarp) tc::dealloc(tb, kTmemCols);
 }
 
 }  // namespace
 
 int prefill_tc_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_prefill_tc(const FwdParams& p, int n_qtiles, const CUtensorMap& tmq, const CUtensorMap& tmk,
+cudaError_t launch_prefill_tc(const FwdParams& p, int n_pairs, const CUtensorMap& tmq, const CUtensorMap& tmk,
                               const CUtensorMap& tmv, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
@@ -394,7 +483,7 @@ cudaError_t launch_prefill_tc(const FwdParams& p, int n_qtiles, const CUtensorMa
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(n_qtiles, p.Hq, p.B);
+  dim3 grid(n_pairs, p.Hq, p.B);
   prefill_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, tmq, tmk, tmv);
   return cudaGetLastError();
 }

@@ -147,6 +147,43 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return d;
 }
 
+// ---- packed fp32 pairs (one 64-bit register, .f32x2 arithmetic) ----
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fsub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// p = hi + lo, hi = p truncated to bf16 (exact upper half), lo = bf16(p - hi)
+// (p - hi is exact in fp32 and below 2^-7 p, so hi + lo keeps ~16 bits).
+// Two values at a time: hi/lo are packed bf16x2, first value in the low half.
+__device__ __forceinline__ void split_bf16_trunc(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+  asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(__float_as_uint(p0)), "r"(__float_as_uint(p1)));
+  const uint64_t t = f2(__uint_as_float(__float_as_uint(p0) & 0xffff0000u),
+                        __uint_as_float(__float_as_uint(p1) & 0xffff0000u));
+  float r0, r1;
+  f2_split(fsub2(f2(p0, p1), t), r0, r1);
+  lo = pack_bf16(r0, r1);
+}
+
 // p = hi + lo with hi = bf16(p) and lo = bf16(p - hi): ~16 significant bits.
 __device__ __forceinline__ void split_bf16(float p0, float p1, uint32_t& hi, uint32_t& lo) {
   hi = pack_bf16(p0, p1);

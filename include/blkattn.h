@@ -194,8 +194,8 @@ int blkattn_check_device_error(blkattn_stream_t stream);
  * (the last may be shorter); rows_per_cta query rows of one KV head share a
  * CTA.  kernel: 0 = CUDA-core split-KV kernel (f32 inputs), 1 = warp-level
  * tensor-core split-KV kernel (bf16 inputs), 2 = tcgen05 prefill kernel
- * (bf16, d = 128, T_q >= 64, no bias; the plan shown assumes no bias and
- * 16-byte aligned query rows).
+ * (bf16, d = 128, T_q >= 64, no bias, scale > 0; the plan shown assumes no
+ * bias, a positive scale and 16-byte aligned query rows).
  * Returns BLKATTN_OK or BLKATTN_ERR_INVALID_ARG.
  */
 typedef struct {

@@ -155,8 +155,8 @@ def test_plan_partitions_every_workload(lib, name):
         _check_partition(p, s.Tmax)
         rows = s.G * s.Tq
         if s.dtype == "bf16" and s.Tq >= 64 and s.d == 128:
-            assert p["kernel"] == 2 and p["rows_per_cta"] == 128 and p["n_splits"] == 1
-            assert p["row_groups"] == math.ceil(s.Tq / 128)
+            assert p["kernel"] == 2 and p["rows_per_cta"] == 256 and p["n_splits"] == 1
+            assert p["row_groups"] == math.ceil(s.Tq / 256)
             assert p["ctas"] == p["row_groups"] * s.Hq * s.B
             continue
         if s.dtype == "bf16":

@@ -418,3 +418,12 @@ def test_prefill_shape_with_bias_uses_the_split_kernel():
     inp = make_case(B, Hq, Hkv, Tq, Tmax, 128, "bf16", [160], [list(range(Tq))], bias)
     _, _, o, l = run_gpu(inp)
     assert_parity(o, l, run_oracle(inp), BF16_TOL_O, BF16_TOL_L)
+
+
+def test_prefill_shape_with_negative_scale():
+    """A non-positive scale is valid input; it is served by the split kernel."""
+    B, Hq, Hkv, Tq, Tmax = 1, 2, 1, 96, 96
+    inp = make_case(B, Hq, Hkv, Tq, Tmax, 128, "bf16", [96], [list(range(Tq))])
+    inp["scale"] = -0.05
+    _, _, o, l = run_gpu(inp)
+    assert_parity(o, l, run_oracle(inp), BF16_TOL_O, BF16_TOL_L)
