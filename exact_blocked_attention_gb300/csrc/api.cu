@@ -70,7 +70,7 @@ Plan make_plan(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tmax, int
                int sms, bool prefill_ok) {
   Plan pl;
   const int64_t rows = (Hq / Hkv) * Tq;  // query rows that read one KV head
-  if (prefill_ok && elt == Elt::BF16 && d == 128 && Tq >= 64 && B <= 65535) {
+  if (prefill_ok && elt == Elt::BF16 && d == 128 && Tq >= 64 && (Tq + 255) / 256 <= 65535) {
     // many query rows per head: two 128-row query tiles per CTA on tcgen05,
     // no splits
     pl.cfg.kernel = blkattn::Kernel::Prefill;
@@ -427,7 +427,8 @@ int fwd_with_scratch(const blkattn_tensor* q, const blkattn_tensor* k, const blk
   if (st != BLKATTN_OK) return st;
   const Plan pl = make_plan(c.B, c.Hq, c.Hkv, c.Tq, c.Tmax, (int)c.d, c.elt, ds->sms,
                             c.prefill_ok && scale > 0.f);
-  if (c.B * pl.cfg.row_groups > 65535) return BLKATTN_ERR_UNSUPPORTED;
+  if (pl.cfg.kernel != blkattn::Kernel::Prefill && c.B * pl.cfg.row_groups > 65535)
+    return BLKATTN_ERR_UNSUPPORTED;  // grid z of the split-KV kernels
   if ((size_t)pl.ws_bytes > scratch_bytes) return BLKATTN_ERR_SCRATCH_LIMIT;
   const FwdParams p = fill_params(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, c, pl,
                                   scratch, ds->err);
@@ -485,7 +486,8 @@ int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_
   if (st != BLKATTN_OK) return st;
   const Plan pl = make_plan(c.B, c.Hq, c.Hkv, c.Tq, c.Tmax, (int)c.d, c.elt, ds->sms,
                             c.prefill_ok && scale > 0.f);
-  if (c.B * pl.cfg.row_groups > 65535) return BLKATTN_ERR_UNSUPPORTED;
+  if (pl.cfg.kernel != blkattn::Kernel::Prefill && c.B * pl.cfg.row_groups > 65535)
+    return BLKATTN_ERR_UNSUPPORTED;  // grid z of the split-KV kernels
   if (pl.ws_bytes > 0) {
     st = ensure_workspace(ds, (size_t)pl.ws_bytes, stream);
     if (st != BLKATTN_OK) return st;

@@ -95,9 +95,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // misc: [0] tmem base, [1 + 2x] end of query tile x, [2 + 2x] min end of x, [5] timeout
   int* misc = reinterpret_cast<int*>(sm + kOffMisc);
 
-  const int pair = gridDim.x - 1 - blockIdx.x;  // the longest (latest) query tiles first
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
+  // Grid (heads x batch, pairs): blocks are dispatched x-fastest, so every
+  // head's longest (latest) query-tile pair goes before any shorter pair.
+  const int pair = gridDim.y - 1 - blockIdx.y;
+  const int h = blockIdx.x % p.Hq;
+  const int b = blockIdx.x / p.Hq;
   const int hk = h / p.G;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -302,13 +304,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after();
         float xs[128];
         {
-          uint32_t r[32];
+          // all four 32-column loads in flight, one wait
+          uint32_t r0[32], r1[32], r2[32], r3[32];
+          tc::ld32(tl + kColS, r0);
+          tc::ld32(tl + kColS + 32, r1);
+          tc::ld32(tl + kColS + 64, r2);
+          tc::ld32(tl + kColS + 96, r3);
+          tc::wait_ld();
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            tc::ld32(tl + kColS + 32 * q4, r);
-            tc::wait_ld();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) xs[32 * q4 + c] = __uint_as_float(r[c]);
+          for (int c = 0; c < 32; ++c) {
+            xs[c] = __uint_as_float(r0[c]);
+            xs[32 + c] = __uint_as_float(r1[c]);
+            xs[64 + c] = __uint_as_float(r2[c]);
+            xs[96 + c] = __uint_as_float(r3[c]);
           }
         }
         const int key0 = j * BN;
@@ -352,34 +360,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // p = 2^(s * scale_log2 - m): masked entries are -inf and give exactly 0;
-        // a row with no valid key yet has only masked entries in this tile
+        // a row with no valid key yet has only masked entries in this tile.
+        // Pairs of keys in float2 registers (packed fp32 arithmetic).
         const float m_use = (m_ref == kNegInf) ? 0.f : m_ref;
-        const uint64_t sc2 = f2(p.scale_log2, p.scale_log2);
-        const uint64_t nm2 = f2(-m_use, -m_use);
-        uint64_t lsum[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+        const float2 nm2 = make_float2(-m_use, -m_use);
+        const float2 neg1 = make_float2(-1.f, -1.f);
+        float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {  // 32 keys -> 16 columns of P_hi and of P_lo
           uint32_t hi[16], lo[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const int k2 = 32 * q4 + 2 * c;
-            float e0, e1;
-            f2_split(ffma2(f2(xs[k2], xs[k2 + 1]), sc2, nm2), e0, e1);
-            const float p0 = fast_exp2(e0);
-            const float p1 = fast_exp2(e1);
-            lsum[c & 3] = fadd2(lsum[c & 3], f2(p0, p1));
-            split_bf16_trunc(p0, p1, hi[c], lo[c]);
+            const float2 e = __ffma2_rn(make_float2(xs[k2], xs[k2 + 1]), sc2, nm2);
+            const float2 pp = make_float2(fast_exp2(e.x), fast_exp2(e.y));
+            ls[c & 3] = __fadd2_rn(ls[c & 3], pp);
+            // P = P_hi + P_lo: P_hi = the upper halves (truncation, exact),
+            // P_lo = bf16(P - P_hi) (P - P_hi exact in fp32, below 2^-7 P)
+            asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi[c]) : "r"(__float_as_uint(pp.x)), "r"(__float_as_uint(pp.y)));
+            const float2 th = make_float2(__uint_as_float(__float_as_uint(pp.x) & 0xffff0000u),
+                                          __uint_as_float(__float_as_uint(pp.y) & 0xffff0000u));
+            const float2 rem = __ffma2_rn(th, neg1, pp);
+            lo[c] = pack_bf16(rem.x, rem.y);
           }
           tc::st16(tl + kColS + 16 * q4, hi);
           tc::st16(tl + kColPlo + 16 * q4, lo);
         }
         {
-          float l0, l1, l2, l3, l4, l5, l6, l7;
-          f2_split(lsum[0], l0, l1);
-          f2_split(lsum[1], l2, l3);
-          f2_split(lsum[2], l4, l5);
-          f2_split(lsum[3], l6, l7);
-          l += ((l0 + l1) + (l2 + l3)) + ((l4 + l5) + (l6 + l7));
+          const float2 a = __fadd2_rn(ls[0], ls[1]);
+          const float2 c2 = __fadd2_rn(ls[2], ls[3]);
+          const float2 t2 = __fadd2_rn(a, c2);
+          l += t2.x + t2.y;
         }
         if (key0 + BN > cta_end) {
           // last tile of the CTA: zero the V rows past every visible key of
@@ -483,7 +496,9 @@ cudaError_t launch_prefill_tc(const FwdParams& p, int n_pairs, const CUtensorMap
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(n_pairs, p.Hq, p.B);
+  const int64_t heads = (int64_t)p.Hq * p.B;
+  if (heads > 0x7fffffff || n_pairs > 65535) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)heads, n_pairs, 1);
   prefill_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, tmq, tmk, tmv);
   return cudaGetLastError();
 }

@@ -96,6 +96,21 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const void* map, int c0, 
       : "memory");
 }
 
+// Named barrier `id` over `count` threads that also ANDs a predicate across
+// them: every thread gets the same answer.
+__device__ __forceinline__ bool bar_and(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void record_error(int* err, int code) {
   if (err) atomicExch(err, code);
 }
