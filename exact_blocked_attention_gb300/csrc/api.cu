@@ -360,6 +360,24 @@ FwdParams fill_params(const blkattn_tensor* q, const blkattn_tensor* k, const bl
     p.ws_u = reinterpret_cast<float*>(base + 2 * ((n * 4 + 255) / 256) * 256);
   }
   p.err = err;
+  // prefill dispatch groups: (sequence, head) pairs whose K and V take about
+  // half of the L2 cache together (129 MB on GB300; queried once per device)
+  {
+    static int l2_bytes = 0;
+    if (l2_bytes == 0) {
+      int dev = 0, v = 0;
+      if (cudaGetDevice(&dev) == cudaSuccess &&
+          cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) == cudaSuccess && v > 0)
+        l2_bytes = v;
+      else
+        l2_bytes = 64 << 20;
+    }
+    const int64_t kv_per_head = 2 * c.Tmax * c.d * elt_bytes(q->dtype);
+    int64_t hg = (l2_bytes / 2) / (kv_per_head > 0 ? kv_per_head : 1);
+    const int64_t heads = c.B * c.Hq;
+    hg = hg < 1 ? 1 : (hg > heads ? heads : hg);
+    p.head_group = (int)hg;
+  }
   return p;
 }
 

@@ -51,6 +51,7 @@ struct FwdParams {
   float* ws_l;
   float* ws_u;
   int* err;  // device error word
+  int head_group;  // prefill: (sequence, head) pairs dispatched together (L2 reuse of K/V)
 };
 
 // Split-KV kernel configuration chosen by the planner.

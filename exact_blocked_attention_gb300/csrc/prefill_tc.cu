@@ -95,11 +95,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   // misc: [0] tmem base, [1 + 2x] end of query tile x, [2 + 2x] min end of x, [5] timeout
   int* misc = reinterpret_cast<int*>(sm + kOffMisc);
 
-  // Grid (heads x batch, pairs): blocks are dispatched x-fastest, so every
-  // head's longest (latest) query-tile pair goes before any shorter pair.
-  const int pair = gridDim.y - 1 - blockIdx.y;
-  const int h = blockIdx.x % p.Hq;
-  const int b = blockIdx.x / p.Hq;
+  // Linear grid in dispatch order: groups of p.head_group (sequence, head)
+  // pairs whose K/V fit in L2 together; within a group every head's longest
+  // (latest) query-tile pair goes before any shorter one.  The next group's
+  // long pairs start while the previous group's short ones finish.
+  const int n_pairs = (p.Tq + 2 * BM - 1) / (2 * BM);
+  const int hg = p.head_group;
+  const int per_group = n_pairs * hg;
+  const int group = blockIdx.x / per_group;
+  const int r_in = blockIdx.x % per_group;
+  const int pair = n_pairs - 1 - r_in / hg;
+  const int bh = group * hg + r_in % hg;
+  if (bh >= p.Hq * p.B) return;  // padding of the last group
+  const int h = bh % p.Hq;
+  const int b = bh / p.Hq;
   const int hk = h / p.G;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -497,9 +506,11 @@ cudaError_t launch_prefill_tc(const FwdParams& p, int n_pairs, const CUtensorMap
     attr_set = true;
   }
   const int64_t heads = (int64_t)p.Hq * p.B;
-  if (heads > 0x7fffffff || n_pairs > 65535) return cudaErrorInvalidValue;
-  dim3 grid((unsigned)heads, n_pairs, 1);
-  prefill_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, tmq, tmk, tmv);
+  if (p.head_group < 1) return cudaErrorInvalidValue;
+  const int64_t groups = (heads + p.head_group - 1) / p.head_group;
+  const int64_t blocks = groups * p.head_group * n_pairs;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  prefill_tc_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmk, tmv);
   return cudaGetLastError();
 }
 
