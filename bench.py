@@ -53,6 +53,26 @@ def measured_peaks():
                 "source": "fallback"}
 
 
+def measured_traffic(workload):
+    """DRAM bytes per launch of the workload's main kernel from the committed
+    ncu capture (profiles/traffic.json), or None when the kernel's sources
+    changed since that capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            entry = json.load(f)["workloads"][workload]
+        m = hashlib.sha256()
+        for src in entry["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                m.update(f.read())
+        if m.hexdigest()[:16] != entry["sources_sha256_16"]:
+            return None
+        return entry["dram_bytes_per_launch"]
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def describe(s):
     return (f"{s.name}: B={s.B} Hq={s.Hq} Hkv={s.Hkv} d={s.d} Tq={s.Tq} Tmax={s.Tmax} "
             f"lens={s.lens} pos={s.pos} {s.dtype}" + (f" bias={s.bias}" if s.bias != "none" else ""))
@@ -267,12 +287,12 @@ def roofline_entry(r: Runner, main_ms, peaks, flops=None):
     if s.name == "prefill":
         achieved = flops / (main_ms * 1e-3) / 1e12
         return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"], "traffic": None,
-                "peak_note": f"dense bf16 burst, {peaks['source']}"}
+                "frac": achieved / peaks["bf16_tflops"], "traffic": measured_traffic(s.name),
+                "algorithmic_bytes": total_bytes, "peak_note": f"dense bf16 burst, {peaks['source']}"}
     achieved = total_bytes / (main_ms * 1e-3) / 1e9
     return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"], "traffic": None,
-            "peak_note": f"HBM copy bandwidth, {peaks['source']}"}
+            "frac": achieved / peaks["hbm_gbs"], "traffic": measured_traffic(s.name),
+            "algorithmic_bytes": total_bytes, "peak_note": f"HBM copy bandwidth, {peaks['source']}"}
 
 
 def oracle_rate(s, inp, budget_s: float, threads: int = 0):
