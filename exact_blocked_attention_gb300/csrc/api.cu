@@ -66,10 +66,15 @@ int resident_ctas_per_sm(size_t smem_bytes) {
 
 // prefill_ok: the request qualifies for the tcgen05 prefill kernel (bf16,
 // d = 128, no bias, 16-byte aligned query rows) if it also has T_q >= 64.
+// q_vec_ok: the query rows are contiguous and 16-byte aligned (the tcgen05
+// decode kernel loads them with 16-byte vector loads).
 Plan make_plan(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tmax, int d, Elt elt,
-               int sms, bool prefill_ok) {
+               int sms, bool prefill_ok, bool q_vec_ok) {
   Plan pl;
   const int64_t rows = (Hq / Hkv) * Tq;  // query rows that read one KV head
+  const char* force = std::getenv("BLKATTN_KERNEL");  // comparison runs only
+  const bool force_mma = force && std::strcmp(force, "mma") == 0;
+  const bool force_cudacore = force && std::strcmp(force, "cudacore") == 0;
   if (prefill_ok && elt == Elt::BF16 && d == 128 && Tq >= 64 && (Tq + 255) / 256 <= 65535) {
     // many query rows per head: two 128-row query tiles per CTA on tcgen05,
     // no splits
@@ -85,10 +90,32 @@ Plan make_plan(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tmax, int
     pl.ws_bytes = 0;
     return pl;
   }
+  {
+    // few rows per KV head: tcgen05 with the keys on the TMEM lanes, one
+    // persistent CTA per SM sharing the key tiles of all units equally
+    const int64_t rg = (rows + 47) / 48;
+    const int64_t R = (rows + rg - 1) / rg;
+    if (q_vec_ok && elt == Elt::BF16 && d == 128 && !force_mma && !force_cudacore && rows >= 1 &&
+        B * rg <= blkattn::kDecodeTcMaxEntries && Tmax <= 65535LL * 128) {
+      const int64_t P = sms > 0 ? sms : 148;
+      const int64_t U = B * Hkv * rg;
+      const int64_t slots = P + U;
+      pl.cfg.kernel = blkattn::Kernel::DecodeTc;
+      pl.cfg.rows_per_cta = (int)R;
+      pl.cfg.row_groups = (int)rg;
+      pl.cfg.warps = 4;
+      pl.cfg.stages = 5;
+      pl.cfg.chunk = 0;  // the key ranges follow the device-resident lengths
+      pl.cfg.n_splits = (int)slots;
+      pl.tile = 128;
+      pl.ctas = P;
+      auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
+      pl.ws_bytes = 2 * al(slots * R * 4) + al(slots * R * d * 4) + al(U * 8);
+      return pl;
+    }
+  }
   size_t smem;
-  bool tensor = (elt == Elt::BF16);
-  if (const char* env = std::getenv("BLKATTN_KERNEL"))  // comparison runs only
-    if (std::strcmp(env, "cudacore") == 0) tensor = false;
+  bool tensor = (elt == Elt::BF16) && !force_cudacore;
   if (tensor) {
     // bf16: warp-level tensor cores, 16-row m-tiles (up to 3 per CTA)
     int64_t mt = (rows + 15) / 16;
@@ -251,6 +278,7 @@ struct Checked {
   int64_t B, Hq, Hkv, Tq, Tmax, d;
   Elt elt;
   bool prefill_ok;  // no bias and q rows movable by TMA (see make_plan)
+  bool q_vec_ok;    // query rows contiguous and 16-byte aligned
 };
 
 int validate_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
@@ -308,10 +336,10 @@ int validate_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn
     return BLKATTN_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return BLKATTN_ERR_UNSUPPORTED;
   c->elt = (q->dtype == BLKATTN_BF16) ? Elt::BF16 : Elt::F32;
-  c->prefill_ok = bias == nullptr && q->strides[3] == 1 &&
-                  (reinterpret_cast<uintptr_t>(q->data) % 16) == 0 &&
-                  (q->strides[0] * 2) % 16 == 0 && (q->strides[1] * 2) % 16 == 0 &&
-                  (q->strides[2] * 2) % 16 == 0;
+  c->q_vec_ok = q->strides[3] == 1 && (reinterpret_cast<uintptr_t>(q->data) % 16) == 0 &&
+                (q->strides[0] * 2) % 16 == 0 && (q->strides[1] * 2) % 16 == 0 &&
+                (q->strides[2] * 2) % 16 == 0;
+  c->prefill_ok = bias == nullptr && c->q_vec_ok;
   return BLKATTN_OK;
 }
 
@@ -352,7 +380,18 @@ FwdParams fill_params(const blkattn_tensor* q, const blkattn_tensor* k, const bl
   p.row_groups = pl.cfg.row_groups;
   p.chunk = pl.cfg.chunk;
   p.n_splits = pl.cfg.n_splits;
-  if (pl.cfg.n_splits > 1) {
+  p.rows_cta = pl.cfg.rows_per_cta;
+  if (pl.cfg.kernel == blkattn::Kernel::DecodeTc) {
+    // per-CTA partial states: [slots][rows_cta] (m, l), [slots][rows_cta][d] (u),
+    // then {first slot, count} per unit
+    auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
+    const int64_t n = (int64_t)pl.cfg.n_splits * pl.cfg.rows_per_cta;
+    char* base = static_cast<char*>(ws);
+    p.ws_m = reinterpret_cast<float*>(base);
+    p.ws_l = reinterpret_cast<float*>(base + al(n * 4));
+    p.ws_u = reinterpret_cast<float*>(base + 2 * al(n * 4));
+    p.unit_info = reinterpret_cast<int2*>(base + 2 * al(n * 4) + al(n * c.d * 4));
+  } else if (pl.cfg.n_splits > 1) {
     const int64_t n = c.B * c.Hq * c.Tq * (int64_t)pl.cfg.n_splits;
     char* base = static_cast<char*>(ws);
     p.ws_m = reinterpret_cast<float*>(base);
@@ -385,7 +424,17 @@ FwdParams fill_params(const blkattn_tensor* q, const blkattn_tensor* k, const bl
 int launch_fwd(const FwdParams& p, const Checked& c, const Plan& pl, const blkattn_tensor* q,
                const blkattn_tensor* k, const blkattn_tensor* v, cudaStream_t stream) {
   cudaError_t le;
-  if (pl.cfg.kernel == blkattn::Kernel::TensorCore || pl.cfg.kernel == blkattn::Kernel::Prefill) {
+  if (pl.cfg.kernel == blkattn::Kernel::DecodeTc) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BLKATTN_ERR_CUDA;
+    const CUtensorMap* mk = nullptr;
+    const CUtensorMap* mv = nullptr;
+    int st = kv_tensor_map(dev, k, 128, &mk);
+    if (st != BLKATTN_OK) return st;
+    st = kv_tensor_map(dev, v, 128, &mv);
+    if (st != BLKATTN_OK) return st;
+    le = blkattn::launch_decode_tc(p, (int)pl.ctas, *mk, *mv, stream);
+  } else if (pl.cfg.kernel == blkattn::Kernel::TensorCore || pl.cfg.kernel == blkattn::Kernel::Prefill) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return BLKATTN_ERR_CUDA;
     const CUtensorMap* mk = nullptr;
@@ -410,6 +459,7 @@ int launch_fwd(const FwdParams& p, const Checked& c, const Plan& pl, const blkat
   if (le != cudaSuccess) return BLKATTN_ERR_CUDA;
   if (g_split_event != nullptr && cudaEventRecord(g_split_event, stream) != cudaSuccess)
     return BLKATTN_ERR_CUDA;
+  // the tcgen05 decode kernel decides on the device which units need merging
   if (pl.cfg.n_splits > 1 && blkattn::launch_split_merge(p, (int)c.d, stream) != cudaSuccess)
     return BLKATTN_ERR_CUDA;
   return BLKATTN_OK;
@@ -444,8 +494,9 @@ int fwd_with_scratch(const blkattn_tensor* q, const blkattn_tensor* k, const blk
   st = device_state(&ds);
   if (st != BLKATTN_OK) return st;
   const Plan pl = make_plan(c.B, c.Hq, c.Hkv, c.Tq, c.Tmax, (int)c.d, c.elt, ds->sms,
-                            c.prefill_ok && scale > 0.f);
-  if (pl.cfg.kernel != blkattn::Kernel::Prefill && c.B * pl.cfg.row_groups > 65535)
+                            c.prefill_ok && scale > 0.f, c.q_vec_ok);
+  if ((pl.cfg.kernel == blkattn::Kernel::TensorCore || pl.cfg.kernel == blkattn::Kernel::CudaCore) &&
+      c.B * pl.cfg.row_groups > 65535)
     return BLKATTN_ERR_UNSUPPORTED;  // grid z of the split-KV kernels
   if ((size_t)pl.ws_bytes > scratch_bytes) return BLKATTN_ERR_SCRATCH_LIMIT;
   const FwdParams p = fill_params(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, c, pl,
@@ -476,7 +527,7 @@ int blkattn_debug_plan(int64_t B, int64_t H_q, int64_t H_kv, int64_t T_q, int64_
       T_max < 1 || (d != 64 && d != 128) || !is_float_dtype(dtype) || num_sms <= 0)
     return BLKATTN_ERR_INVALID_ARG;
   const Plan pl = make_plan(B, H_q, H_kv, T_q, T_max, (int)d,
-                            dtype == BLKATTN_BF16 ? Elt::BF16 : Elt::F32, num_sms, true);
+                            dtype == BLKATTN_BF16 ? Elt::BF16 : Elt::F32, num_sms, true, true);
   plan->kernel = (int32_t)pl.cfg.kernel;
   plan->rows_per_cta = pl.cfg.rows_per_cta;
   plan->row_groups = pl.cfg.row_groups;
@@ -503,8 +554,9 @@ int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_
   st = device_state(&ds);
   if (st != BLKATTN_OK) return st;
   const Plan pl = make_plan(c.B, c.Hq, c.Hkv, c.Tq, c.Tmax, (int)c.d, c.elt, ds->sms,
-                            c.prefill_ok && scale > 0.f);
-  if (pl.cfg.kernel != blkattn::Kernel::Prefill && c.B * pl.cfg.row_groups > 65535)
+                            c.prefill_ok && scale > 0.f, c.q_vec_ok);
+  if ((pl.cfg.kernel == blkattn::Kernel::TensorCore || pl.cfg.kernel == blkattn::Kernel::CudaCore) &&
+      c.B * pl.cfg.row_groups > 65535)
     return BLKATTN_ERR_UNSUPPORTED;  // grid z of the split-KV kernels
   if (pl.ws_bytes > 0) {
     st = ensure_workspace(ds, (size_t)pl.ws_bytes, stream);

@@ -1,0 +1,816 @@
+// Decode / verify kernel on the 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// Exact blocked attention of a few query rows per KV head over a long cache
+// ("Chapter 33: inference compute optimisation" §33.2, Algorithm 33.1 with
+// the statistics (m, l, u) of eq. 33.3 and the merge rule of eqs.
+// 33.4-33.5).  The G x T_q query rows that read one KV head form a "unit"
+// (at most 48 rows; more rows make several row groups).  The unit's rows are
+// the N dimension of the MMA and the keys sit on the 128 TMEM lanes:
+//
+//   S^T_j  = K_j Q^T       M = 128 keys, N = NR rows, K = 16 x 8
+//                          (A = K tile, B = Q rows; both K-major in smem)
+//   U^T   += V_j^T P_j^T   M = 128 value dims, N = 64 + NR, K = 16 x 8
+//                          (A = the V tile read MN-major, B = P^T in smem)
+//
+// so a tile of 128 keys costs 16 MMAs whatever the row count.  P is not an
+// input: each P^T row is written as bf16 P_hi (columns [0, NR) of the first
+// 64-column atom) and P_lo = bf16(P - P_hi) (the same columns of a second
+// atom), P_hi the truncated upper half of P; one product with N = 64 + NR
+// gives U_hi and U_lo side by side and U = U_hi + U_lo keeps ~2^-17 relative
+// accuracy of P while V stays bf16 and is read once.
+//
+// Work split: the key tiles of all units, in the order (sequence, KV head,
+// row group, tile), are cut into P = min(gridDim.x, tiles) equal contiguous
+// non-empty ranges, one per CTA (one CTA per SM).  A unit whose tiles lie in one CTA is finished in
+// place; otherwise each CTA leaves its partial state of the unit in the
+// workspace slot (CTA index + unit index) and the merge kernel folds them.
+// The tile counts come from the device-resident lengths and positions, so
+// every CTA streams the same number of tiles whatever the length mix, and no
+// SM idles at the end.
+//
+// Roles (192 threads):
+//  * warps 0-3: thread k owns key k of the current tile (TMEM lane k).  It
+//    reads the NR scores of its key, applies the mask by select (cache
+//    length, logical position, additive bias with -inf = masked), and
+//    writes its P^T row; per unit it then owns value dim k for the epilogue.
+//  * warp 4: producer.  Per unit, the query rows (16-byte loads into the
+//    128-byte swizzled K-major layout) and the rows' integer facts, into one
+//    of two buffers; K and V tiles of 128 keys x 128 dims by tiled TMA into a
+//    ring of 4 slots of 32 KB (K_j and V_j alternate).
+//  * warp 5: TMEM allocation and the one thread that issues every MMA, in
+//    the order S_0, S_1, U += P_0 V_0, S_2, U += P_1 V_1, ...: the scores of
+//    tile j + 1 are computed while the key threads work on tile j.  S^T and
+//    P^T have two buffers each (by tile parity).  A tcgen05.commit fires
+//    once every earlier MMA of the thread has completed, so S_j ready
+//    implies the product with P_{j-2} is done and P^T buffer (j mod 2) is
+//    free; a rescale of U^T at tile j first waits for the product with
+//    P_{j-1} (one more barrier, rarely needed).
+//
+// Statistics: every thread keeps its own partial sums l over its keys for
+// all NR rows; the reference maxima m (base-2 units) live in shared memory.
+// Per tile the 128 key threads vote (bar.red.or) whether any score exceeds
+// its row's m by more than 8.  Only then (always on a unit's first tile)
+// are the tile's row maxima reduced across the keys, m raised and l and U^T
+// rescaled: with any common reference m >= (max - 8) the state represents
+// the same set and every P <= 2^8.  Rows with no visible key keep the empty
+// state (out = 0, lse = -inf).  V rows past the unit's last visible key in
+// its last tile (cache padding, possibly NaN) are zero-filled before the
+// product so that 0 * garbage never reaches U.
+//
+// Every wait is bounded (%globaltimer); on a timeout the CTA records the
+// error word, stops issuing work, lets its own copies and products drain
+// and frees its tensor memory.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tc.cuh"
+
+namespace blkattn {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kLazyRescale = 8.f;
+
+constexpr int BK = 128;               // keys per tile (TMEM lanes of S^T)
+constexpr int D = 128;                // head dim (TMEM lanes of U^T)
+constexpr int kSlots = 4;             // ring slots of one K or V tile
+constexpr int kBox = BK * 128;        // 128 rows x 64 dims, bf16: 16 KB
+constexpr int kSlotBytes = 2 * kBox;  // 128 rows x 128 dims
+constexpr int kThreads = 192;
+constexpr int kTmaWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kBarRows = 1;  // named barrier of the 128 key threads
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;    // S^T of tiles with even / odd index: +0 / +64
+constexpr uint32_t kColU = 128;  // U^T of units with even / odd index: +0 / +128;
+                                 // the P_hi part in columns [0, NR), P_lo in [64, 64 + NR)
+constexpr int kPBytes = 2 * kBox;  // one P^T buffer: P_hi box, then P_lo box
+
+// Integer facts of the rows of one unit (written by the producer).
+template <int NR>
+struct RowFacts {
+  int64_t boff[NR];  // bias row offsets (elements)
+  int64_t ooff[NR];  // output row offsets
+  int64_t loff[NR];  // lse offsets
+  int end[NR];       // visible keys are [0, end): min(len, pos + 1), 0 for padding rows
+  int unit_end;      // max over the rows
+  int min_end;       // min over the real rows
+  int pad[2];
+};
+
+template <int NR>
+struct TcLayout {
+  static constexpr int kQBox = NR * 128;  // NR rows x 64 dims
+  static constexpr int kQBytes = 2 * kQBox;
+  static constexpr int kOffRing = 0;
+  static constexpr int kOffQ = kSlots * kSlotBytes;              // two query buffers
+  static constexpr int kOffP = kOffQ + 2 * kQBytes;              // two P^T buffers
+  static constexpr int kOffRows = kOffP + 2 * kPBytes;           // RowFacts[2]
+  static constexpr int kRowsBytes = (int)((sizeof(RowFacts<NR>) + 15) / 16 * 16);
+  static constexpr int kOffNTab = kOffRows + 2 * kRowsBytes;     // uint16 tiles per (sequence, row group)
+  static constexpr int kOffRed = kOffNTab + kDecodeTcMaxEntries * 2;  // float [4][NR]
+  static constexpr int kOffStat = kOffRed + 4 * NR * 4;          // float m, m_use, thr, alpha, l [NR]
+  static constexpr int kOffBar = kOffStat + 5 * NR * 4;
+  // full[kSlots], empty[kSlots], q_full[2], q_empty[2], s_full[2], p_full[2], u_full[2],
+  // pv_done, drain
+  static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 2 + 1 + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 128 + 1024;  // + slack to align to 1024
+  static_assert(kOffQ % 1024 == 0 && kQBox % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms");
+  static_assert(kOffBar % 8 == 0 && kOffStat % 16 == 0, "alignment");
+  static_assert(kBytes <= 232448, "shared memory per block");
+};
+
+// The CTA's start in the tile order (written once by warp 0).
+struct Start {
+  long long t0, t1, W, P, su;
+  int b, kvh, rg, j;
+};
+
+// Position in the tile order: global tile t of unit (b, kvh, rg), local tile
+// j of n, the unit's first global tile su.
+struct Cursor {
+  int64_t t, su;
+  int b, kvh, rg, j, n;
+  __device__ __forceinline__ void next(const uint16_t* ntab, int RG, int Hkv, int B) {
+    ++t;
+    if (++j == n) {
+      su += n;
+      j = 0;
+      if (++rg == RG) {
+        rg = 0;
+        if (++kvh == Hkv) {
+          kvh = 0;
+          ++b;
+        }
+      }
+      n = (b < B) ? (int)ntab[b * RG + rg] : 1;
+    }
+  }
+};
+
+// CTA whose range [c W / P, (c + 1) W / P) holds global tile t.
+__device__ __forceinline__ int64_t cta_of(int64_t t, int64_t W, int64_t P) {
+  return ((t + 1) * P + W - 1) / W - 1;
+}
+
+__device__ __forceinline__ int row_end_of(const FwdParams& p, int b, int i, int len) {
+  const int pos = p.qpos[b * p.qp_sb + i * p.qp_si];
+  return pos < 0 ? 0 : (pos >= len ? len : pos + 1);
+}
+
+// NR consecutive TMEM columns of this thread's lane -> floats.
+template <int NR>
+__device__ __forceinline__ void ld_cols(uint32_t taddr, float (&x)[NR]) {
+  uint32_t r[NR];
+  if constexpr (NR == 16) {
+    tc::ld16(taddr, &r[0]);
+  } else {
+    tc::ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+    if constexpr (NR == 48) tc::ld16(taddr + 32, &r[32]);
+  }
+  tc::wait_ld();
+#pragma unroll
+  for (int c = 0; c < NR; ++c) x[c] = __uint_as_float(r[c]);
+}
+
+template <int NR>
+__device__ __forceinline__ void st_cols(uint32_t taddr, const float (&x)[NR]) {
+  uint32_t r[NR];
+#pragma unroll
+  for (int c = 0; c < NR; ++c) r[c] = __float_as_uint(x[c]);
+  if constexpr (NR == 16) {
+    tc::st16(taddr, &r[0]);
+  } else {
+    tc::st32(taddr, *reinterpret_cast<const uint32_t(*)[32]>(&r[0]));
+    if constexpr (NR == 48) tc::st16(taddr + 32, &r[32]);
+  }
+}
+
+template <int NR>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmk,
+                     const __grid_constant__ CUtensorMap tmv) {
+  using L = TcLayout<NR>;
+  constexpr uint32_t kIdescQK = tc::idesc_bf16(128, NR, 0, 0);  // K, Q both K-major
+  // V^T, P^T both MN-major; N spans the P_hi atom (NR used of 64) and the P_lo atom
+  constexpr uint32_t kIdescPV = tc::idesc_bf16(128, 64 + NR, 1, 1);
+
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  RowFacts<NR>* facts0 = reinterpret_cast<RowFacts<NR>*>(sm + L::kOffRows);
+  uint16_t* ntab = reinterpret_cast<uint16_t*>(sm + L::kOffNTab);
+  float* red = reinterpret_cast<float*>(sm + L::kOffRed);
+  float* s_m = reinterpret_cast<float*>(sm + L::kOffStat);  // reference maximum, -inf = none yet
+  float* s_muse = s_m + NR;                                  // m, or 0 when none yet
+  float* s_thr = s_m + 2 * NR;                               // m + 8, -inf when none yet
+  float* s_alpha = s_m + 3 * NR;
+  float* s_l = s_m + 4 * NR;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kOffBar);
+  uint64_t* full = bars;
+  uint64_t* empty = full + kSlots;
+  uint64_t* q_full = empty + kSlots;  // [2]
+  uint64_t* q_empty = q_full + 2;     // [2]
+  uint64_t* s_full = q_empty + 2;     // [2] by tile parity
+  uint64_t* p_full = s_full + 2;      // [2] by tile parity
+  uint64_t* u_full = p_full + 2;      // [2] by unit parity
+  uint64_t* pv_done = u_full + 2;     // once per U += P V product
+  uint64_t* drain = pv_done + 1;
+  // misc: [0] tmem base, [1] error seen by the producer / MMA thread,
+  // [2] abort of the key threads (written before a barrier, read after it)
+  int* misc = reinterpret_cast<int*>(sm + L::kOffMisc);
+  Start* start = reinterpret_cast<Start*>(sm + L::kOffMisc + 64);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int RG = p.row_groups;
+  const int R = p.rows_cta;
+  const int B = p.B;
+  const int Hkv = p.Hkv;
+
+  // ---------------- schedule: tiles per (sequence, row group) ----------------
+  {
+    int* nb = reinterpret_cast<int*>(sm + L::kOffP);  // per-sequence totals (P^T area, start-up only)
+    const int E = B * RG;
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+      const int b = e / RG;
+      const int rg = e - b * RG;
+      int len = p.seqlens[b * p.sl_s];
+      len = len < 0 ? 0 : (len > p.Tmax ? p.Tmax : len);
+      const int pk0 = rg * R;
+      const int pk1 = min(pk0 + R, p.rows_per_head);
+      int uend = 0;
+      if (pk1 - pk0 >= p.Tq) {
+        for (int i = 0; i < p.Tq; ++i) uend = max(uend, row_end_of(p, b, i, len));
+      } else {
+        for (int pk = pk0; pk < pk1; ++pk) uend = max(uend, row_end_of(p, b, pk % p.Tq, len));
+      }
+      const int n = (uend + BK - 1) / BK;
+      ntab[e] = (uint16_t)(n < 1 ? 1 : n);  // an all-empty unit still takes one (masked) tile
+    }
+    if (threadIdx.x == 0) {
+      misc[1] = 0;
+      misc[2] = 0;
+      for (int s = 0; s < kSlots; ++s) {
+        mbar_init(&full[s], 1);
+        mbar_init(&empty[s], 1);
+      }
+      for (int x = 0; x < 2; ++x) {
+        mbar_init(&q_full[x], 1);
+        // query buffer x is free once the unit's last S product completed
+        // (MMA commit) and its row facts are no longer read (key threads)
+        mbar_init(&q_empty[x], 2);
+        mbar_init(&u_full[x], 1);
+      }
+      for (int x = 0; x < 2; ++x) {
+        mbar_init(&s_full[x], 1);
+        mbar_init(&p_full[x], 4);  // one arrival per key warp
+      }
+      mbar_init(pv_done, 1);
+      mbar_init(drain, 1);
+      fence_barrier_init();
+    }
+    if (threadIdx.x < NR) {
+      s_m[threadIdx.x] = kNegInf;
+      s_muse[threadIdx.x] = 0.f;
+      s_thr[threadIdx.x] = kNegInf;
+    }
+    if (warp == kMmaWarp) {
+      tc::alloc(reinterpret_cast<uint32_t*>(&misc[0]), kTmemCols);
+      tc::relinquish();
+    }
+    __syncthreads();
+    for (int b = threadIdx.x; b < B; b += kThreads) {
+      int s = 0;
+      for (int rg = 0; rg < RG; ++rg) s += ntab[b * RG + rg];
+      nb[b] = s;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // tiles of sequence b: Hkv * nb[b]; lane l sums a contiguous run of sequences
+      const int per = (B + 31) / 32;
+      const int b0 = min(lane * per, B);
+      const int b1 = min(b0 + per, B);
+      long long s = 0;
+      for (int b = b0; b < b1; ++b) s += (long long)nb[b] * Hkv;
+      long long incl = s;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const long long v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      const long long W = __shfl_sync(0xffffffffu, incl, 31);
+      // with fewer tiles than CTAs the last CTAs stay idle, so that every
+      // working CTA has a tile and the CTAs holding one unit are consecutive
+      const long long P = W < (long long)gridDim.x ? W : (long long)gridDim.x;
+      const bool works = (long long)blockIdx.x < P;
+      const long long t0 = works ? (long long)blockIdx.x * W / P : W;
+      const long long t1 = works ? ((long long)blockIdx.x + 1) * W / P : W;
+      const long long excl = incl - s;
+      const unsigned own = __ballot_sync(0xffffffffu, t0 < t1 && excl <= t0 && t0 < incl);
+      if (lane == 0) {
+        start->t0 = t0;
+        start->t1 = t1;
+        start->W = W;
+        start->P = P;
+      }
+      if (own != 0 && lane == __ffs(own) - 1) {
+        long long pre = excl;
+        int b = b0;
+        while (pre + (long long)nb[b] * Hkv <= t0) {
+          pre += (long long)nb[b] * Hkv;
+          ++b;
+        }
+        const long long o = t0 - pre;
+        const int kvh = (int)(o / nb[b]);
+        long long o2 = o - (long long)kvh * nb[b];
+        long long su = pre + (long long)kvh * nb[b];
+        int rg = 0;
+        while (o2 >= ntab[b * RG + rg]) {
+          o2 -= ntab[b * RG + rg];
+          su += ntab[b * RG + rg];
+          ++rg;
+        }
+        start->b = b;
+        start->kvh = kvh;
+        start->rg = rg;
+        start->j = (int)o2;
+        start->su = su;
+      }
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+  }
+  const int64_t t0 = start->t0;
+  const int64_t t1 = start->t1;
+  const int64_t W = start->W;
+  const int64_t P_work = start->P;  // CTAs that hold tiles: [0, P_work)
+  const uint32_t tb = static_cast<uint32_t>(misc[0]);
+  const uint32_t sRing = smem_u32(sm + L::kOffRing);
+  const uint32_t sQ = smem_u32(sm + L::kOffQ);
+  const uint32_t sP = smem_u32(sm + L::kOffP);
+  Cursor cur;
+  cur.t = t0;
+  cur.su = start->su;
+  cur.b = start->b;
+  cur.kvh = start->kvh;
+  cur.rg = start->rg;
+  cur.j = start->j;
+  cur.n = (t0 < t1) ? (int)ntab[cur.b * RG + cur.rg] : 1;
+
+  if (warp == kTmaWarp) {
+    // ---------------- producer ----------------
+    const uint64_t pol = policy_evict_first();
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+    }
+    int uidx = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    for (; cur.t < t1; cur.next(ntab, RG, Hkv, B)) {
+      const bool first = cur.t == t0 || cur.j == 0;
+      const bool last = cur.t == t1 - 1 || cur.j == cur.n - 1;
+      if (first) {
+        const int qb = uidx & 1;
+        if (uidx >= 2) {
+          bool w = true;
+          if (lane == 0) w = mbar_wait(&q_empty[qb], ((uidx >> 1) - 1) & 1);
+          if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+        }
+        // query rows of the unit, 128-byte swizzled K-major (rows of 64 dims)
+        unsigned char* qs = sm + L::kOffQ + qb * L::kQBytes;
+        const int b = cur.b;
+        int len = p.seqlens[b * p.sl_s];
+        len = len < 0 ? 0 : (len > p.Tmax ? p.Tmax : len);
+        uint4 val[NR / 2];
+#pragma unroll
+        for (int it = 0; it < NR / 2; ++it) {
+          const int idx = lane + 32 * it;
+          const int r = idx >> 4;
+          const int c = idx & 15;
+          const int pk = cur.rg * R + r;
+          val[it] = make_uint4(0, 0, 0, 0);
+          if (r < R && pk < p.rows_per_head) {
+            const int g = pk / p.Tq;
+            const int i = pk - g * p.Tq;
+            const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) + (int64_t)b * p.q_sb +
+                                        (int64_t)(cur.kvh * p.G + g) * p.q_sh + (int64_t)i * p.q_si;
+            val[it] = __ldg(reinterpret_cast<const uint4*>(qrow) + c);
+          }
+        }
+#pragma unroll
+        for (int it = 0; it < NR / 2; ++it) {
+          const int idx = lane + 32 * it;
+          const int r = idx >> 4;
+          const int c = idx & 15;
+          *reinterpret_cast<uint4*>(qs + (c >> 3) * L::kQBox + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = val[it];
+        }
+        // integer facts of the rows
+        RowFacts<NR>& rf = facts0[qb];
+        int umax = 0, umin = 0x7fffffff;
+        for (int r = lane; r < NR; r += 32) {
+          const int pk = cur.rg * R + r;
+          int e = 0;
+          int64_t bo = 0, oo = 0, lo = 0;
+          if (r < R && pk < p.rows_per_head) {
+            const int g = pk / p.Tq;
+            const int i = pk - g * p.Tq;
+            const int h = cur.kvh * p.G + g;
+            e = row_end_of(p, b, i, len);
+            bo = (int64_t)b * p.bi_sb + (int64_t)h * p.bi_sh + (int64_t)i * p.bi_si;
+            oo = (int64_t)b * p.o_sb + (int64_t)h * p.o_sh + (int64_t)i * p.o_si;
+            lo = (int64_t)b * p.l_sb + (int64_t)h * p.l_sh + (int64_t)i * p.l_si;
+            umin = min(umin, e);
+          }
+          umax = max(umax, e);
+          rf.end[r] = e;
+          rf.boff[r] = bo;
+          rf.ooff[r] = oo;
+          rf.loff[r] = lo;
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+          umax = max(umax, __shfl_xor_sync(0xffffffffu, umax, off));
+          umin = min(umin, __shfl_xor_sync(0xffffffffu, umin, off));
+        }
+        if (lane == 0) {
+          rf.unit_end = umax;
+          rf.min_end = umin;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q rows -> tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_full[qb]);
+      }
+      if (lane == 0) {
+        const int64_t g = cur.t - t0;
+#pragma unroll
+        for (int kv = 0; kv < 2 && ok; ++kv) {
+          const int64_t seq = 2 * g + kv;
+          const int s = (int)(seq % kSlots);
+          if (seq >= kSlots && !mbar_wait(&empty[s], (uint32_t)(((seq / kSlots) - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          unsigned char* dst = sm + L::kOffRing + s * kSlotBytes;
+          const void* map = kv ? static_cast<const void*>(&tmv) : static_cast<const void*>(&tmk);
+          mbar_arrive_expect_tx(&full[s], kSlotBytes);
+          tma_load_4d(dst, map, 0, cur.j * BK, cur.kvh, cur.b, &full[s], pol);
+          tma_load_4d(dst + kBox, map, 64, cur.j * BK, cur.kvh, cur.b, &full[s], pol);
+          issued = seq + 1;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (last) ++uidx;
+    }
+    if (lane == 0) {
+      // every issued copy must land before the CTA exits
+      for (int64_t seq = issued - kSlots < 0 ? 0 : issued - kSlots; seq < issued; ++seq)
+        if (!mbar_wait(&full[seq % kSlots], (uint32_t)((seq / kSlots) & 1))) ok = false;
+      if (!ok) {
+        record_error(p.err, kErrTimeout);
+        misc[1] = 1;
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issue (one thread) ----------------
+    // Order S_0, S_1, U += P_0 V_0, S_2, U += P_1 V_1, ...: the products of
+    // the next tile's scores run while the key threads work on this tile.
+    if (lane == 0) {
+      const int64_t n_t = t1 - t0;
+      Cursor cq = cur;  // tile of the next S product
+      int uq = 0, up = 0;  // unit counters of the S and the U sides
+      auto issue_qk = [&](int64_t gq) -> bool {
+        const bool first = cq.t == t0 || cq.j == 0;
+        const bool last = cq.t == t1 - 1 || cq.j == cq.n - 1;
+        const int qb = uq & 1;
+        if (first && !mbar_wait(&q_full[qb], (uint32_t)((uq >> 1) & 1))) return false;
+        const int64_t sk = 2 * gq;
+        if (!mbar_wait(&full[sk % kSlots], (uint32_t)((sk / kSlots) & 1))) return false;
+        tc::fence_after();
+        // S^T = K_j Q^T into the S buffer of the tile's parity
+        const uint32_t kb = sRing + (uint32_t)(sk % kSlots) * kSlotBytes;
+        const uint32_t qbase = sQ + qb * L::kQBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t adesc = tc::smem_desc(kb + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024);
+          const uint64_t bdesc = tc::smem_desc(qbase + (ks >> 2) * L::kQBox + (ks & 3) * 32, 16, 1024);
+          tc::mma_ss(tb + kColS + 64u * (uint32_t)(gq & 1), adesc, bdesc, kIdescQK, ks > 0 ? 1u : 0u);
+        }
+        tc::commit(&s_full[gq & 1]);
+        tc::commit(&empty[sk % kSlots]);
+        if (last) {
+          tc::commit(&q_empty[qb]);
+          ++uq;
+        }
+        cq.next(ntab, RG, Hkv, B);
+        return true;
+      };
+      bool ok = n_t == 0 || issue_qk(0);
+      for (int64_t g = 0; ok && g < n_t; cur.next(ntab, RG, Hkv, B), ++g) {
+        const bool first = cur.t == t0 || cur.j == 0;
+        const bool last = cur.t == t1 - 1 || cur.j == cur.n - 1;
+        if (g + 1 < n_t && !issue_qk(g + 1)) { ok = false; break; }
+        // U^T += V_j^T [P_hi | P_lo]^T once the key threads wrote P^T
+        const int64_t sv = 2 * g + 1;
+        if (!mbar_wait(&p_full[g & 1], (uint32_t)((g >> 1) & 1))) { ok = false; break; }
+        if (!mbar_wait(&full[sv % kSlots], (uint32_t)((sv / kSlots) & 1))) { ok = false; break; }
+        tc::fence_after();
+        const uint32_t vb = sRing + (uint32_t)(sv % kSlots) * kSlotBytes;
+        const uint32_t pb = sP + (uint32_t)(g & 1) * kPBytes;
+        const uint32_t ucol = tb + kColU + 128u * (uint32_t)(up & 1);
+#pragma unroll
+        for (int ks = 0; ks < BK / 16; ++ks) {
+          // A = V^T: 128 dims (two 64-dim boxes 16 KB apart) x keys [16 ks, 16 ks + 16)
+          const uint64_t adesc = tc::smem_desc(vb + ks * 2048, kBox, 1024);
+          // B = P^T: keys [16 ks, +16) x (P_hi atom, P_lo atom 16 KB further)
+          const uint64_t bdesc = tc::smem_desc(pb + ks * 2048, kBox, 1024);
+          tc::mma_ss(ucol, adesc, bdesc, kIdescPV, (!first || ks > 0) ? 1u : 0u);
+        }
+        tc::commit(&empty[sv % kSlots]);
+        tc::commit(pv_done);
+        if (last) {
+          tc::commit(&u_full[up & 1]);
+          ++up;
+        }
+      }
+      if (!ok) {
+        record_error(p.err, kErrTimeout);
+        misc[1] = 1;
+      }
+      // every MMA issued must complete before TMEM is released
+      tc::commit(drain);
+      if (!mbar_wait(drain, 0)) {
+        record_error(p.err, kErrTimeout);
+        misc[1] = 1;
+      }
+    }
+  } else {
+    // ---------------- key threads ----------------
+    const int k = threadIdx.x;  // key of the tile / value dim in the epilogue
+    const uint32_t tl = tb + ((uint32_t)(32 * warp) << 16);
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+    };
+    const bool has_bias = p.bias != nullptr;
+    float lp[NR];  // this key thread's partial sums of P
+#pragma unroll
+    for (int r = 0; r < NR; ++r) lp[r] = 0.f;
+    int uidx = 0;
+    bool ok = true;
+    for (; cur.t < t1; cur.next(ntab, RG, Hkv, B)) {
+      const bool first = cur.t == t0 || cur.j == 0;
+      const bool last = cur.t == t1 - 1 || cur.j == cur.n - 1;
+      const int ub = uidx & 1;
+      const int64_t g = cur.t - t0;
+      const RowFacts<NR>& rf = facts0[ub];
+      if (first) {
+        // the row facts come with the query rows
+        const bool w = bar_and(kBarRows, 128, wait_all(&q_full[ub], (uint32_t)((uidx >> 1) & 1)));
+        if (!w) { ok = false; break; }
+      }
+      const int key0 = cur.j * BK;
+      const int key = key0 + k;
+      float x[NR];
+      if (has_bias) {  // issued before the wait: the loads overlap the products
+        const bool kin = key < p.Tmax;
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+          x[r] = kin ? __ldg(p.bias + rf.boff[r] + (int64_t)key * p.bi_sj) : 0.f;
+      }
+      const bool sok = wait_all(&s_full[g & 1], (uint32_t)((g >> 1) & 1));
+      bool trig = !sok;
+      if (sok) {
+        tc::fence_after();
+        float s[NR];
+        ld_cols<NR>(tl + kColS + 64u * (uint32_t)(g & 1), s);
+        const bool tail = key0 + BK > rf.min_end;
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          float v = has_bias ? fmaf(s[r], p.scale_log2, x[r] * kLog2e) : s[r] * p.scale_log2;
+          if (tail && key >= rf.end[r]) v = kNegInf;
+          x[r] = v;
+        }
+#pragma unroll
+        for (int r4 = 0; r4 < NR / 4; ++r4) {
+          const float4 t4 = reinterpret_cast<const float4*>(s_thr)[r4];
+          trig |= (x[4 * r4] > t4.x) | (x[4 * r4 + 1] > t4.y) | (x[4 * r4 + 2] > t4.z) | (x[4 * r4 + 3] > t4.w);
+        }
+      } else if (lane == 0) {
+        misc[2] = 1;
+      }
+      bool resc = false;
+      if (bar_or(kBarRows, 128, trig)) {
+        if (misc[2] != 0) { ok = false; break; }  // read after the barrier: same answer everywhere
+        // ---- raise the reference maxima: tile maxima over the 128 keys ----
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          float v = x[r];
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+          if (lane == (r & 31)) red[warp * NR + r] = v;
+        }
+        bar_sync(kBarRows, 128);
+        if (k < NR) {
+          const float tmax = fmaxf(fmaxf(red[k], red[NR + k]), fmaxf(red[2 * NR + k], red[3 * NR + k]));
+          const float mo = s_m[k];
+          float a = 1.f;
+          if (tmax > s_thr[k]) {
+            a = (mo == kNegInf) ? 1.f : fast_exp2(mo - tmax);  // a row with no key yet has l = u = 0
+            s_m[k] = tmax;
+            s_muse[k] = tmax;
+            s_thr[k] = tmax + kLazyRescale;
+          }
+          s_alpha[k] = a;
+        }
+        bar_sync(kBarRows, 128);
+#pragma unroll
+        for (int r4 = 0; r4 < NR / 4; ++r4) {
+          const float4 a4 = reinterpret_cast<const float4*>(s_alpha)[r4];
+          lp[4 * r4] *= a4.x;
+          lp[4 * r4 + 1] *= a4.y;
+          lp[4 * r4 + 2] *= a4.z;
+          lp[4 * r4 + 3] *= a4.w;
+        }
+        if (!first) {
+          // U^T lane k = value dim k, both parts; the product with P_{j-1}
+          // must have completed (U += P_j V_j waits for this tile's P)
+          const bool pv = bar_and(kBarRows, 128, wait_all(pv_done, (uint32_t)((g - 1) & 1)));
+          if (!pv) { ok = false; break; }
+          tc::fence_after();
+          const uint32_t ua = tl + kColU + 128u * (uint32_t)ub;
+#pragma unroll 1
+          for (int part = 0; part < 2; ++part) {
+            float u[NR];
+            ld_cols<NR>(ua + 64u * part, u);
+#pragma unroll
+            for (int r = 0; r < NR; ++r) u[r] *= s_alpha[r];
+            st_cols<NR>(ua + 64u * part, u);
+          }
+          resc = true;
+        }
+      }
+      // ---- P^T row of key k: 2^(x - m), as bf16 P_hi + P_lo ----
+      {
+        unsigned char* ph = sm + L::kOffP + (int)(g & 1) * kPBytes + k * 128;
+#pragma unroll
+        for (int c8 = 0; c8 < NR / 8; ++c8) {
+          const float4 m0 = reinterpret_cast<const float4*>(s_muse)[2 * c8];
+          const float4 m1 = reinterpret_cast<const float4*>(s_muse)[2 * c8 + 1];
+          const float mu[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const int r = 8 * c8 + 2 * e2;
+            const float pa = fast_exp2(x[r] - mu[2 * e2]);  // masked: 2^-inf = 0
+            const float pb = fast_exp2(x[r + 1] - mu[2 * e2 + 1]);
+            lp[r] += pa;
+            lp[r + 1] += pb;
+            asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi[e2]) : "r"(__float_as_uint(pa)), "r"(__float_as_uint(pb)));
+            const float ra = pa - __uint_as_float(__float_as_uint(pa) & 0xffff0000u);
+            const float rb = pb - __uint_as_float(__float_as_uint(pb) & 0xffff0000u);
+            lo[e2] = pack_bf16(ra, rb);
+          }
+          const int off = ((c8 ^ (k & 7)) << 4);
+          *reinterpret_cast<uint4*>(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(ph + kBox + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
+      if (cur.j == cur.n - 1 && key0 + BK > rf.unit_end) {
+        // the unit's last tile: zero the V rows past every visible key
+        const int64_t sv = 2 * g + 1;
+        const bool vok = bar_and(kBarRows, 128, wait_all(&full[sv % kSlots], (uint32_t)((sv / kSlots) & 1)));
+        if (!vok) { ok = false; break; }
+        if (key >= rf.unit_end) {
+          unsigned char* vr = sm + L::kOffRing + (int)(sv % kSlots) * kSlotBytes + k * 128;
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            *reinterpret_cast<uint4*>(vr + (c >> 3) * kBox + (((c & 7) ^ (k & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P^T, V rows -> tensor core
+      if (resc) tc::wait_st();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[g & 1]);
+
+      if (last) {
+        // ---- epilogue of the unit (or of this CTA's part of it) ----
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          float v = lp[r];
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+          if (lane == (r & 31)) red[warp * NR + r] = v;
+          lp[r] = 0.f;
+        }
+        bar_sync(kBarRows, 128);
+        if (k < NR) s_l[k] = (red[k] + red[NR + k]) + (red[2 * NR + k] + red[3 * NR + k]);
+        const bool uok = bar_and(kBarRows, 128, wait_all(&u_full[ub], (uint32_t)((uidx >> 1) & 1)));
+        if (!uok) { ok = false; break; }
+        tc::fence_after();
+        float u[NR];
+        {
+          float ulo[NR];
+          ld_cols<NR>(tl + kColU + 128u * (uint32_t)ub, u);
+          ld_cols<NR>(tl + kColU + 128u * (uint32_t)ub + 64u, ulo);
+#pragma unroll
+          for (int r = 0; r < NR; ++r) u[r] += ulo[r];  // U = P_hi V + P_lo V
+        }
+        const int64_t unit = ((int64_t)cur.b * Hkv + cur.kvh) * RG + cur.rg;
+        const int64_t cf = cta_of(cur.su, W, P_work);
+        const int64_t cl = cta_of(cur.su + cur.n - 1, W, P_work);
+        const int nparts = (int)(cl - cf + 1);
+        const int rr = min(R, p.rows_per_head - cur.rg * R);  // real rows of the unit
+        if (nparts == 1) {
+#pragma unroll
+          for (int r = 0; r < NR; ++r) {
+            if (r >= rr) break;
+            const float m = s_m[r];
+            const float o = (m == kNegInf) ? 0.f : u[r] / s_l[r];
+            const int64_t oi = rf.ooff[r] + (int64_t)k * p.o_sd;
+            if (p.out_bf16)
+              static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+            else
+              static_cast<float*>(p.out)[oi] = o;
+          }
+          if (k < rr) {
+            const float m = s_m[k];
+            p.lse[rf.loff[k]] = (m == kNegInf) ? kNegInf : (m + __log2f(s_l[k])) * kLn2;
+          }
+        } else {
+          const int64_t slot = (int64_t)blockIdx.x + unit;
+#pragma unroll
+          for (int r = 0; r < NR; ++r) {
+            if (r >= rr) break;
+            p.ws_u[((slot * R + r) * D) + k] = u[r];
+          }
+          if (k < rr) {
+            p.ws_m[slot * R + k] = s_m[k];
+            p.ws_l[slot * R + k] = s_l[k];
+          }
+        }
+        if (k == 0 && blockIdx.x == cf) p.unit_info[unit] = make_int2((int)(cf + unit), nparts);
+        // fresh statistics for the next unit; the row facts are released
+        bar_sync(kBarRows, 128);
+        if (k < NR) {
+          s_m[k] = kNegInf;
+          s_muse[k] = 0.f;
+          s_thr[k] = kNegInf;
+        }
+        if (k == 0) mbar_arrive(&q_empty[ub]);
+        bar_sync(kBarRows, 128);
+        ++uidx;
+      }
+    }
+    if (!ok && lane == 0) record_error(p.err, kErrTimeout);
+  }
+
+  // the merge grid may start launching (it waits for this grid's completion
+  // before reading anything)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  if (warp == kMmaWarp) tc::dealloc(tb, kTmemCols);
+}
+
+template <int NR>
+cudaError_t launch_nr(const FwdParams& p, int ctas, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                      cudaStream_t stream) {
+  using L = TcLayout<NR>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(decode_tc_kernel<NR>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  decode_tc_kernel<NR><<<ctas, kThreads, L::kBytes, stream>>>(p, tmk, tmv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t decode_tc_smem_bytes(int nr) {
+  if (nr <= 16) return TcLayout<16>::kBytes;
+  if (nr <= 32) return TcLayout<32>::kBytes;
+  return TcLayout<48>::kBytes;
+}
+
+cudaError_t launch_decode_tc(const FwdParams& p, int ctas, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                             cudaStream_t stream) {
+  if (p.rows_cta < 1 || p.rows_cta > 48 || ctas < 1 || p.B * p.row_groups > kDecodeTcMaxEntries)
+    return cudaErrorInvalidValue;
+  if (p.rows_cta <= 16) return launch_nr<16>(p, ctas, tmk, tmv, stream);
+  if (p.rows_cta <= 32) return launch_nr<32>(p, ctas, tmk, tmv, stream);
+  return launch_nr<48>(p, ctas, tmk, tmv, stream);
+}
+
+}  // namespace blkattn

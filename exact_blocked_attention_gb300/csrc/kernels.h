@@ -52,10 +52,15 @@ struct FwdParams {
   float* ws_u;
   int* err;  // device error word
   int head_group;  // prefill: (sequence, head) pairs dispatched together (L2 reuse of K/V)
+  // tcgen05 decode kernel: query rows per unit (one row group of one KV head),
+  // and per unit {first workspace slot, number of partial states}; the partial
+  // state of unit row r in slot s sits at index s * rows_cta + r
+  int rows_cta;
+  int2* unit_info;
 };
 
 // Split-KV kernel configuration chosen by the planner.
-enum class Kernel : int { CudaCore = 0, TensorCore = 1, Prefill = 2 };
+enum class Kernel : int { CudaCore = 0, TensorCore = 1, Prefill = 2, DecodeTc = 3 };
 struct DecodeConfig {
   Kernel kernel;
   int rows_per_cta;  // CUDA-core: 1, 2, 4 or 8; tensor-core: 16, 32 or 48
@@ -94,6 +99,16 @@ size_t decode_mma_smem_bytes(int d, int mt);
 cudaError_t launch_prefill_tc(const FwdParams& p, int n_pairs, const CUtensorMap& tmq, const CUtensorMap& tmk,
                               const CUtensorMap& tmv, cudaStream_t stream);
 int prefill_tc_smem_bytes();
+
+// Decode / verify on tcgen05 (bf16, d = 128, 16-byte aligned query rows, at
+// most 48 query rows per unit): `ctas` persistent CTAs share the key tiles of
+// all units equally; maps as for the prefill kernel (K/V boxes {64, 128}).
+// The (sequence, row group) table lives in shared memory: B * row_groups
+// must not exceed kDecodeTcMaxEntries.
+constexpr int kDecodeTcMaxEntries = 1024;
+cudaError_t launch_decode_tc(const FwdParams& p, int ctas, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                             cudaStream_t stream);
+size_t decode_tc_smem_bytes(int rows_cta);
 
 // Validation only (no CUDA call), and blkattn_fwd with caller-given scratch
 // for the per-split states (no allocation; BLKATTN_ERR_SCRATCH_LIMIT when the

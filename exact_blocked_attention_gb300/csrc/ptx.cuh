@@ -111,6 +111,26 @@ __device__ __forceinline__ bool bar_and(int id, int count, bool pred) {
   return r != 0;
 }
 
+// Named barrier `id` over `count` threads that ORs a predicate across them.
+__device__ __forceinline__ bool bar_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+// Named barrier `id` over `count` threads (shared-memory writes before it are
+// visible to the participating threads after it).
+__device__ __forceinline__ void bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void record_error(int* err, int code) {
   if (err) atomicExch(err, code);
 }

@@ -146,19 +146,35 @@ def _check_partition(p, Tmax):
     assert covered == list(range(Tmax))
 
 
+def _check_tc_decode_plan(p, B, Hq, Hkv, Tq, d, sms):
+    rows = (Hq // Hkv) * Tq
+    rg = math.ceil(rows / 48)
+    R = math.ceil(rows / rg)
+    assert p["kernel"] == 3 and p["tile_keys"] == 128 and p["chunk_keys"] == 0
+    assert p["row_groups"] == rg and p["rows_per_cta"] == R <= 48
+    assert p["ctas"] == sms  # one persistent CTA per SM
+    units = B * Hkv * rg
+    assert p["n_splits"] == sms + units  # workspace slots: CTA index + unit index
+    slots = p["n_splits"]
+    assert p["workspace_bytes"] >= slots * R * (d + 2) * 4 + units * 8
+
+
 @pytest.mark.parametrize("name", list(workloads.SPECS))
 def test_plan_partitions_every_workload(lib, name):
     for small in (False, True):
         s = workloads.spec(name, small)
         p = blkattn.debug_plan(s.B, s.Hq, s.Hkv, s.Tq, s.Tmax, s.d,
                                torch.bfloat16 if s.dtype == "bf16" else torch.float32, 152)
-        _check_partition(p, s.Tmax)
         rows = s.G * s.Tq
         if s.dtype == "bf16" and s.Tq >= 64 and s.d == 128:
             assert p["kernel"] == 2 and p["rows_per_cta"] == 256 and p["n_splits"] == 1
             assert p["row_groups"] == math.ceil(s.Tq / 256)
             assert p["ctas"] == p["row_groups"] * s.Hq * s.B
             continue
+        if s.dtype == "bf16" and s.d == 128:
+            _check_tc_decode_plan(p, s.B, s.Hq, s.Hkv, s.Tq, s.d, 152)
+            continue
+        _check_partition(p, s.Tmax)
         if s.dtype == "bf16":
             assert p["kernel"] == 1 and p["rows_per_cta"] in (16, 32, 48)
         else:
@@ -180,8 +196,22 @@ def test_plan_random_shapes(lib):
         Tq = int(torch.randint(1, 20, (1,), generator=g))
         Tmax = int(torch.randint(1, 300000, (1,), generator=g))
         sms = int(torch.randint(1, 200, (1,), generator=g))
-        p = blkattn.debug_plan(B, Hkv * G, Hkv, Tq, Tmax, 128, torch.bfloat16, sms)
-        _check_partition(p, Tmax)
+        d = 64 if int(torch.randint(0, 2, (1,), generator=g)) else 128
+        p = blkattn.debug_plan(B, Hkv * G, Hkv, Tq, Tmax, d, torch.bfloat16, sms)
+        if d == 128:
+            _check_tc_decode_plan(p, B, Hkv * G, Hkv, Tq, d, sms)
+        else:
+            assert p["kernel"] == 1
+            _check_partition(p, Tmax)
+
+
+def test_plan_large_batches_leave_the_tc_decode_kernel(lib):
+    # the (sequence, row group) table of the tcgen05 decode kernel holds 1024 entries
+    assert blkattn.debug_plan(1024, 8, 8, 1, 4096, 128, torch.bfloat16, 152)["kernel"] == 3
+    assert blkattn.debug_plan(1025, 8, 8, 1, 4096, 128, torch.bfloat16, 152)["kernel"] == 1
+    assert blkattn.debug_plan(512, 64, 1, 1, 4096, 128, torch.bfloat16, 152)["kernel"] == 3  # 2 row groups
+    assert blkattn.debug_plan(513, 64, 1, 1, 4096, 128, torch.bfloat16, 152)["kernel"] == 1
+    assert blkattn.debug_plan(1, 8, 8, 1, 65535 * 128 + 1, 128, torch.bfloat16, 152)["kernel"] == 1
 
 
 def test_plan_rejects_bad_shapes(lib):

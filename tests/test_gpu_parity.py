@@ -427,3 +427,98 @@ def test_prefill_shape_with_negative_scale():
     inp["scale"] = -0.05
     _, _, o, l = run_gpu(inp)
     assert_parity(o, l, run_oracle(inp), BF16_TOL_O, BF16_TOL_L)
+
+
+# ------------------------------------------------------------ tcgen05 decode kernel
+# One persistent CTA per SM shares the key tiles of all (sequence, KV head,
+# row group) units equally; units spanning several CTAs are merged.  The
+# cases below cover the shapes of that schedule: fewer tiles than CTAs, many
+# units per CTA, units over many CTAs, two row groups, each row count class
+# (16 / 32 / 48 columns), rescaling in the middle of a CTA's range, and rows
+# whose first visible key comes late.
+
+def tc_case(name):
+    rng = np.random.default_rng(11)
+    if name == "fewer_tiles_than_ctas":
+        return make_case(2, 4, 1, 1, 300, 128, "bf16", [100, 0], [[99], [0]])
+    if name == "many_units":
+        B = 300
+        lens = rng.integers(0, 257, B)
+        lens[:3] = [0, 1, 256]
+        pos = (lens - 1)[:, None]
+        return make_case(B, 8, 2, 1, 256, 128, "bf16", lens.tolist(), pos.tolist(), seed=1)
+    if name == "units_over_many_ctas":
+        return make_case(1, 8, 2, 2, 20000, 128, "bf16", [19999], [[19997, 19998]], seed=2)
+    if name == "two_row_groups":
+        B, Hq, Hkv, Tq, Tmax = 3, 32, 2, 4, 1500
+        g = torch.Generator().manual_seed(4)
+        bias = torch.randn(B, Hq, Tq, Tmax, generator=g)
+        bias[torch.rand(B, Hq, Tq, Tmax, generator=g) < 0.2] = -math.inf
+        return make_case(B, Hq, Hkv, Tq, Tmax, 128, "bf16", [1500, 700, 1],
+                         [[1496, 1497, 1498, 1499], [10, 699, 300, -1], [0, 0, 5, 0]], bias, seed=3)
+    if name == "rows32":
+        return make_case(4, 16, 2, 4, 3000, 128, "bf16", [3000, 2999, 1200, 64],
+                         [[2996, 2997, 2998, 2999], [2995, 2996, 2997, 2998], [1196, 1197, 1198, 1199],
+                          [60, 61, 62, 63]], seed=5)
+    if name == "rising_scores":
+        inp = make_case(8, 8, 8, 1, 8192, 128, "bf16", [8192] * 8, [[8191]] * 8, seed=6)
+        # scores grow along the cache: the reference maximum must be raised
+        # (and U^T rescaled) in the middle of a CTA's key range
+        ramp = torch.linspace(0.2, 3.0, 8192)[None, None, :, None]
+        inp["k"] = (inp["k"].float() * ramp).to(torch.bfloat16)
+        return inp
+    if name == "late_first_key":
+        B, Hq, Hkv, Tq, Tmax = 2, 8, 2, 3, 2000
+        bias = torch.zeros(B, 1, Tq, Tmax)
+        bias[0, 0, 0, :1500] = -math.inf  # first visible key in a late tile
+        bias[1, 0, 1, :1999] = -math.inf  # exactly one visible key
+        bias[1, 0, 2, :] = -math.inf      # none
+        return make_case(B, Hq, Hkv, Tq, Tmax, 128, "bf16", [2000, 2000],
+                         [[1997, 1998, 1999], [1997, 1998, 1999]], bias, seed=7)
+    raise KeyError(name)
+
+
+TC_CASES = ["fewer_tiles_than_ctas", "many_units", "units_over_many_ctas", "two_row_groups", "rows32",
+            "rising_scores", "late_first_key"]
+
+
+@pytest.mark.parametrize("case", TC_CASES)
+def test_tc_decode_kernel_cases(case):
+    inp = tc_case(case)
+    assert plan_of(inp)["kernel"] == 3
+    raw, _, o, l = run_gpu(inp)
+    ref = run_oracle(inp)
+    assert_parity(o, l, ref, BF16_TOL_O, BF16_TOL_L, out_raw=raw)
+
+
+@pytest.mark.parametrize("name", ["decode_gqa", "long_decode", "spec_verify"])
+def test_tc_decode_kernel_serves_the_decode_workloads(name):
+    s = workloads.spec(name)
+    p = blkattn.debug_plan(s.B, s.Hq, s.Hkv, s.Tq, s.Tmax, s.d, torch.bfloat16,
+                           torch.cuda.get_device_properties(0).multi_processor_count)
+    assert p["kernel"] == 3
+
+
+@pytest.fixture
+def force_split_mma(monkeypatch):
+    monkeypatch.setenv("BLKATTN_KERNEL", "mma")
+    yield
+
+
+@pytest.mark.parametrize("name", ["decode_gqa", "long_decode", "spec_verify"])
+def test_split_mma_kernel_small_workloads(force_split_mma, name):
+    """The mma.sync split-KV kernel stays correct (it serves d = 64 and
+    non-contiguous query rows)."""
+    s = workloads.spec(name, small=True)
+    inp = workloads.generate(s)
+    assert plan_of(inp)["kernel"] == 1
+    raw, _, o, l = run_gpu(inp)
+    assert_parity(o, l, run_oracle(inp), *tols(s), out_raw=raw)
+
+
+@pytest.mark.parametrize("case", ["many_units", "two_row_groups", "late_first_key"])
+def test_split_mma_kernel_cases(force_split_mma, case):
+    inp = tc_case(case)
+    assert plan_of(inp)["kernel"] == 1
+    raw, _, o, l = run_gpu(inp)
+    assert_parity(o, l, run_oracle(inp), BF16_TOL_O, BF16_TOL_L, out_raw=raw)

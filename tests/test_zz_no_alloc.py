@@ -69,22 +69,22 @@ def test_static_scratch_matches_blkattn_fwd_on_consecutive_calls():
 
 
 def test_static_scratch_refuses_problems_beyond_its_size():
-    # 32 packed query rows per KV head (8 grouped heads x 4 rows) over a long
-    # cache: a split plan whose per-split states outgrow the static array
+    # 32 packed query rows per KV head (8 grouped heads x 4 rows) for a batch
+    # large enough that the per-CTA / per-unit states outgrow the static array
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    B, Hq, Hkv, Tq, d = 1, 64, 8, 4, 128
-    Tmax = 16384
+    Hq, Hkv, Tq, d, Tmax = 64, 8, 4, 128, 256
+    B = 16
     while True:
         plan = blkattn.debug_plan(B, Hq, Hkv, Tq, Tmax, d, torch.bfloat16, sms)
         if plan["n_splits"] > 1 and plan["workspace_bytes"] > blkattn.STATIC_SCRATCH_BYTES:
             break
-        Tmax *= 2
-        assert Tmax <= 262144, "no over-limit split plan found"
+        B *= 2
+        assert B <= 1024, "no over-limit split plan found"
     g = torch.Generator().manual_seed(0)
     q = torch.randn(B, Hq, Tq, d, generator=g).to(torch.bfloat16).cuda()
     k = torch.randn(B, Hkv, Tmax, d, generator=g).to(torch.bfloat16).cuda()
     v = torch.randn(B, Hkv, Tmax, d, generator=g).to(torch.bfloat16).cuda()
-    sl = torch.tensor([Tmax], dtype=torch.int32).cuda()
+    sl = torch.full((B,), Tmax, dtype=torch.int32).cuda()
     qp = torch.full((B, Tq), Tmax - 1, dtype=torch.int32).cuda()
     out = torch.full((B, Hq, Tq, d), 7.0, device="cuda")
     lse = torch.full((B, Hq, Tq), 7.0, device="cuda")
