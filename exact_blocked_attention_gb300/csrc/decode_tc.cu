@@ -28,16 +28,19 @@
 // every CTA streams the same number of tiles whatever the length mix, and no
 // SM idles at the end.
 //
-// Roles (192 threads):
-//  * warps 0-3: thread k owns key k of the current tile (TMEM lane k).  It
-//    reads the NR scores of its key, applies the mask by select (cache
-//    length, logical position, additive bias with -inf = masked), and
-//    writes its P^T row; per unit it then owns value dim k for the epilogue.
-//  * warp 4: producer.  Per unit, the query rows (16-byte loads into the
+// Roles (352 threads):
+//  * warps 0-7: key threads.  Thread k of lane quarter k / 32 owns key k of
+//    the current tile (TMEM lane k); the two warps of a quarter split the NR
+//    rows in halves.  A thread reads the scores of its key for its rows,
+//    applies the mask by select (cache length, logical position, additive
+//    bias with -inf = masked), and writes its part of the P^T row; per unit
+//    it then owns value dim k of its rows for the epilogue.
+//  * warp 8: producer: K and V tiles of 128 keys x 128 dims by tiled TMA
+//    into a ring of 4 slots of 32 KB (K_j and V_j alternate).
+//  * warp 10: unit loader: per unit, the query rows (16-byte loads into the
 //    128-byte swizzled K-major layout) and the rows' integer facts, into one
-//    of two buffers; K and V tiles of 128 keys x 128 dims by tiled TMA into a
-//    ring of 4 slots of 32 KB (K_j and V_j alternate).
-//  * warp 5: TMEM allocation and the one thread that issues every MMA, in
+//    of two buffers, ahead of the unit's first product.
+//  * warp 9: TMEM allocation and the one thread that issues every MMA, in
 //    the order S_0, S_1, U += P_0 V_0, S_2, U += P_1 V_1, ...: the scores of
 //    tile j + 1 are computed while the key threads work on tile j.  S^T and
 //    P^T have two buffers each (by tile parity).  A tcgen05.commit fires
@@ -46,9 +49,9 @@
 //    free; a rescale of U^T at tile j first waits for the product with
 //    P_{j-1} (one more barrier, rarely needed).
 //
-// Statistics: every thread keeps its own partial sums l over its keys for
-// all NR rows; the reference maxima m (base-2 units) live in shared memory.
-// Per tile the 128 key threads vote (bar.red.or) whether any score exceeds
+// Statistics: every key thread keeps its own partial sums l over its keys
+// for its rows; the reference maxima m (base-2 units) live in shared memory.
+// Per tile the key threads vote (bar.red.or) whether any score exceeds
 // its row's m by more than 8.  Only then (always on a unit's first tile)
 // are the tile's row maxima reduced across the keys, m raised and l and U^T
 // rescaled: with any common reference m >= (max - 8) the state represents
@@ -79,10 +82,13 @@ constexpr int D = 128;                // head dim (TMEM lanes of U^T)
 constexpr int kSlots = 4;             // ring slots of one K or V tile
 constexpr int kBox = BK * 128;        // 128 rows x 64 dims, bf16: 16 KB
 constexpr int kSlotBytes = 2 * kBox;  // 128 rows x 128 dims
-constexpr int kThreads = 192;
-constexpr int kTmaWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kBarRows = 1;  // named barrier of the 128 key threads
+constexpr int kKeyWarps = 8;   // two warps per TMEM lane quarter, each with half of the rows
+constexpr int kKeyThreads = 32 * kKeyWarps;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kLoadWarp = 10;
+constexpr int kThreads = 32 * 11;
+constexpr int kBarRows = 1;  // named barrier of the key threads
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // S^T of tiles with even / odd index: +0 / +64
 constexpr uint32_t kColU = 128;  // U^T of units with even / odd index: +0 / +128;
@@ -135,19 +141,26 @@ struct Start {
 struct Cursor {
   int64_t t, su;
   int b, kvh, rg, j, n;
-  __device__ __forceinline__ void next(const uint16_t* ntab, int RG, int Hkv, int B) {
-    ++t;
-    if (++j == n) {
-      su += n;
-      j = 0;
-      if (++rg == RG) {
-        rg = 0;
-        if (++kvh == Hkv) {
-          kvh = 0;
-          ++b;
-        }
+  // to the first tile of the next unit
+  __device__ __forceinline__ void step_unit(const uint16_t* ntab, int RG, int Hkv, int B) {
+    su += n;
+    t = su;
+    j = 0;
+    if (++rg == RG) {
+      rg = 0;
+      if (++kvh == Hkv) {
+        kvh = 0;
+        ++b;
       }
-      n = (b < B) ? (int)ntab[b * RG + rg] : 1;
+    }
+    n = (b < B) ? (int)ntab[b * RG + rg] : 1;
+  }
+  __device__ __forceinline__ void next(const uint16_t* ntab, int RG, int Hkv, int B) {
+    if (j + 1 == n) {
+      step_unit(ntab, RG, Hkv, B);
+    } else {
+      ++t;
+      ++j;
     }
   }
 };
@@ -162,31 +175,32 @@ __device__ __forceinline__ int row_end_of(const FwdParams& p, int b, int i, int 
   return pos < 0 ? 0 : (pos >= len ? len : pos + 1);
 }
 
-// NR consecutive TMEM columns of this thread's lane -> floats.
-template <int NR>
-__device__ __forceinline__ void ld_cols(uint32_t taddr, float (&x)[NR]) {
-  uint32_t r[NR];
-  if constexpr (NR == 16) {
+// N consecutive TMEM columns of this thread's lane (N = 8, 16 or 24; the
+// column offset is a multiple of 8, of 16 for N = 16) -> floats.
+template <int N>
+__device__ __forceinline__ void ld_cols(uint32_t taddr, float (&x)[N]) {
+  uint32_t r[N];
+  if constexpr (N == 16) {
     tc::ld16(taddr, &r[0]);
   } else {
-    tc::ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-    if constexpr (NR == 48) tc::ld16(taddr + 32, &r[32]);
+#pragma unroll
+    for (int c = 0; c < N; c += 8) tc::ld8(taddr + c, &r[c]);
   }
   tc::wait_ld();
 #pragma unroll
-  for (int c = 0; c < NR; ++c) x[c] = __uint_as_float(r[c]);
+  for (int c = 0; c < N; ++c) x[c] = __uint_as_float(r[c]);
 }
 
-template <int NR>
-__device__ __forceinline__ void st_cols(uint32_t taddr, const float (&x)[NR]) {
-  uint32_t r[NR];
+template <int N>
+__device__ __forceinline__ void st_cols(uint32_t taddr, const float (&x)[N]) {
+  uint32_t r[N];
 #pragma unroll
-  for (int c = 0; c < NR; ++c) r[c] = __float_as_uint(x[c]);
-  if constexpr (NR == 16) {
+  for (int c = 0; c < N; ++c) r[c] = __float_as_uint(x[c]);
+  if constexpr (N == 16) {
     tc::st16(taddr, &r[0]);
   } else {
-    tc::st32(taddr, *reinterpret_cast<const uint32_t(*)[32]>(&r[0]));
-    if constexpr (NR == 48) tc::st16(taddr + 32, &r[32]);
+#pragma unroll
+    for (int c = 0; c < N; c += 8) tc::st8(taddr + c, &r[c]);
   }
 }
 
@@ -267,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int x = 0; x < 2; ++x) {
         mbar_init(&s_full[x], 1);
-        mbar_init(&p_full[x], 4);  // one arrival per key warp
+        mbar_init(&p_full[x], kKeyWarps);  // one arrival per key warp
       }
       mbar_init(pv_done, 1);
       mbar_init(drain, 1);
@@ -363,93 +377,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   cur.n = (t0 < t1) ? (int)ntab[cur.b * RG + cur.rg] : 1;
 
   if (warp == kTmaWarp) {
-    // ---------------- producer ----------------
+    // ---------------- producer: K and V tiles ----------------
     const uint64_t pol = policy_evict_first();
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
-    }
-    int uidx = 0;
-    int64_t issued = 0;
-    bool ok = true;
-    for (; cur.t < t1; cur.next(ntab, RG, Hkv, B)) {
-      const bool first = cur.t == t0 || cur.j == 0;
-      const bool last = cur.t == t1 - 1 || cur.j == cur.n - 1;
-      if (first) {
-        const int qb = uidx & 1;
-        if (uidx >= 2) {
-          bool w = true;
-          if (lane == 0) w = mbar_wait(&q_empty[qb], ((uidx >> 1) - 1) & 1);
-          if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-        }
-        // query rows of the unit, 128-byte swizzled K-major (rows of 64 dims)
-        unsigned char* qs = sm + L::kOffQ + qb * L::kQBytes;
-        const int b = cur.b;
-        int len = p.seqlens[b * p.sl_s];
-        len = len < 0 ? 0 : (len > p.Tmax ? p.Tmax : len);
-        uint4 val[NR / 2];
-#pragma unroll
-        for (int it = 0; it < NR / 2; ++it) {
-          const int idx = lane + 32 * it;
-          const int r = idx >> 4;
-          const int c = idx & 15;
-          const int pk = cur.rg * R + r;
-          val[it] = make_uint4(0, 0, 0, 0);
-          if (r < R && pk < p.rows_per_head) {
-            const int g = pk / p.Tq;
-            const int i = pk - g * p.Tq;
-            const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) + (int64_t)b * p.q_sb +
-                                        (int64_t)(cur.kvh * p.G + g) * p.q_sh + (int64_t)i * p.q_si;
-            val[it] = __ldg(reinterpret_cast<const uint4*>(qrow) + c);
-          }
-        }
-#pragma unroll
-        for (int it = 0; it < NR / 2; ++it) {
-          const int idx = lane + 32 * it;
-          const int r = idx >> 4;
-          const int c = idx & 15;
-          *reinterpret_cast<uint4*>(qs + (c >> 3) * L::kQBox + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = val[it];
-        }
-        // integer facts of the rows
-        RowFacts<NR>& rf = facts0[qb];
-        int umax = 0, umin = 0x7fffffff;
-        for (int r = lane; r < NR; r += 32) {
-          const int pk = cur.rg * R + r;
-          int e = 0;
-          int64_t bo = 0, oo = 0, lo = 0;
-          if (r < R && pk < p.rows_per_head) {
-            const int g = pk / p.Tq;
-            const int i = pk - g * p.Tq;
-            const int h = cur.kvh * p.G + g;
-            e = row_end_of(p, b, i, len);
-            bo = (int64_t)b * p.bi_sb + (int64_t)h * p.bi_sh + (int64_t)i * p.bi_si;
-            oo = (int64_t)b * p.o_sb + (int64_t)h * p.o_sh + (int64_t)i * p.o_si;
-            lo = (int64_t)b * p.l_sb + (int64_t)h * p.l_sh + (int64_t)i * p.l_si;
-            umin = min(umin, e);
-          }
-          umax = max(umax, e);
-          rf.end[r] = e;
-          rf.boff[r] = bo;
-          rf.ooff[r] = oo;
-          rf.loff[r] = lo;
-        }
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-          umax = max(umax, __shfl_xor_sync(0xffffffffu, umax, off));
-          umin = min(umin, __shfl_xor_sync(0xffffffffu, umin, off));
-        }
-        if (lane == 0) {
-          rf.unit_end = umax;
-          rf.min_end = umin;
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q rows -> tensor core
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&q_full[qb]);
-      }
-      if (lane == 0) {
+      int64_t issued = 0;
+      bool ok = true;
+      for (; ok && cur.t < t1; cur.next(ntab, RG, Hkv, B)) {
         const int64_t g = cur.t - t0;
 #pragma unroll
-        for (int kv = 0; kv < 2 && ok; ++kv) {
+        for (int kv = 0; kv < 2; ++kv) {
           const int64_t seq = 2 * g + kv;
           const int s = (int)(seq % kSlots);
           if (seq >= kSlots && !mbar_wait(&empty[s], (uint32_t)(((seq / kSlots) - 1) & 1))) {
@@ -464,11 +402,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           issued = seq + 1;
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (last) ++uidx;
-    }
-    if (lane == 0) {
       // every issued copy must land before the CTA exits
       for (int64_t seq = issued - kSlots < 0 ? 0 : issued - kSlots; seq < issued; ++seq)
         if (!mbar_wait(&full[seq % kSlots], (uint32_t)((seq / kSlots) & 1))) ok = false;
@@ -476,6 +409,85 @@ __global__ void __launch_bounds__(kThreads, 1)
         record_error(p.err, kErrTimeout);
         misc[1] = 1;
       }
+    }
+  } else if (warp == kLoadWarp) {
+    // ---------------- unit loader: query rows and row facts ----------------
+    int uidx = 0;
+    bool ok = true;
+    for (; t0 < t1 && cur.su < t1; cur.step_unit(ntab, RG, Hkv, B), ++uidx) {
+      const int qb = uidx & 1;
+      if (uidx >= 2) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(&q_empty[qb], (uint32_t)(((uidx >> 1) - 1) & 1));
+        if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+      }
+      // query rows of the unit, 128-byte swizzled K-major (rows of 64 dims)
+      unsigned char* qs = sm + L::kOffQ + qb * L::kQBytes;
+      const int b = cur.b;
+      int len = p.seqlens[b * p.sl_s];
+      len = len < 0 ? 0 : (len > p.Tmax ? p.Tmax : len);
+      uint4 val[NR / 2];
+#pragma unroll
+      for (int it = 0; it < NR / 2; ++it) {
+        const int idx = lane + 32 * it;
+        const int r = idx >> 4;
+        const int c = idx & 15;
+        const int pk = cur.rg * R + r;
+        val[it] = make_uint4(0, 0, 0, 0);
+        if (r < R && pk < p.rows_per_head) {
+          const int g = pk / p.Tq;
+          const int i = pk - g * p.Tq;
+          const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) + (int64_t)b * p.q_sb +
+                                      (int64_t)(cur.kvh * p.G + g) * p.q_sh + (int64_t)i * p.q_si;
+          val[it] = __ldg(reinterpret_cast<const uint4*>(qrow) + c);
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < NR / 2; ++it) {
+        const int idx = lane + 32 * it;
+        const int r = idx >> 4;
+        const int c = idx & 15;
+        *reinterpret_cast<uint4*>(qs + (c >> 3) * L::kQBox + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = val[it];
+      }
+      // integer facts of the rows
+      RowFacts<NR>& rf = facts0[qb];
+      int umax = 0, umin = 0x7fffffff;
+      for (int r = lane; r < NR; r += 32) {
+        const int pk = cur.rg * R + r;
+        int e = 0;
+        int64_t bo = 0, oo = 0, lo = 0;
+        if (r < R && pk < p.rows_per_head) {
+          const int g = pk / p.Tq;
+          const int i = pk - g * p.Tq;
+          const int h = cur.kvh * p.G + g;
+          e = row_end_of(p, b, i, len);
+          bo = (int64_t)b * p.bi_sb + (int64_t)h * p.bi_sh + (int64_t)i * p.bi_si;
+          oo = (int64_t)b * p.o_sb + (int64_t)h * p.o_sh + (int64_t)i * p.o_si;
+          lo = (int64_t)b * p.l_sb + (int64_t)h * p.l_sh + (int64_t)i * p.l_si;
+          umin = min(umin, e);
+        }
+        umax = max(umax, e);
+        rf.end[r] = e;
+        rf.boff[r] = bo;
+        rf.ooff[r] = oo;
+        rf.loff[r] = lo;
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        umax = max(umax, __shfl_xor_sync(0xffffffffu, umax, off));
+        umin = min(umin, __shfl_xor_sync(0xffffffffu, umin, off));
+      }
+      if (lane == 0) {
+        rf.unit_end = umax;
+        rf.min_end = umin;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q rows -> tensor core
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_full[qb]);
+    }
+    if (!ok && lane == 0) {
+      record_error(p.err, kErrTimeout);
+      misc[1] = 1;
     }
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issue (one thread) ----------------
@@ -552,15 +564,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- key threads ----------------
-    const int k = threadIdx.x;  // key of the tile / value dim in the epilogue
-    const uint32_t tl = tb + ((uint32_t)(32 * warp) << 16);
+    // warp w: TMEM lane quarter (w mod 4), row half (w / 4): thread = key k
+    // of the tile (value dim k in the epilogue), rows [c0, c0 + NH)
+    constexpr int NH = NR / 2;
+    const int quarter = warp & 3;
+    const int half = warp >> 2;
+    const int k = 32 * quarter + lane;
+    const int c0 = half * NH;
+    const uint32_t tl = tb + ((uint32_t)(32 * quarter) << 16);
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity));
     };
     const bool has_bias = p.bias != nullptr;
-    float lp[NR];  // this key thread's partial sums of P
+    float lp[NH];  // this thread's partial sums of P over its keys
 #pragma unroll
-    for (int r = 0; r < NR; ++r) lp[r] = 0.f;
+    for (int r = 0; r < NH; ++r) lp[r] = 0.f;
     int uidx = 0;
     bool ok = true;
     for (; cur.t < t1; cur.next(ntab, RG, Hkv, B)) {
@@ -571,52 +589,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       const RowFacts<NR>& rf = facts0[ub];
       if (first) {
         // the row facts come with the query rows
-        const bool w = bar_and(kBarRows, 128, wait_all(&q_full[ub], (uint32_t)((uidx >> 1) & 1)));
+        const bool w = bar_and(kBarRows, kKeyThreads, wait_all(&q_full[ub], (uint32_t)((uidx >> 1) & 1)));
         if (!w) { ok = false; break; }
       }
       const int key0 = cur.j * BK;
       const int key = key0 + k;
-      float x[NR];
+      float x[NH];
       if (has_bias) {  // issued before the wait: the loads overlap the products
         const bool kin = key < p.Tmax;
 #pragma unroll
-        for (int r = 0; r < NR; ++r)
-          x[r] = kin ? __ldg(p.bias + rf.boff[r] + (int64_t)key * p.bi_sj) : 0.f;
+        for (int r = 0; r < NH; ++r)
+          x[r] = kin ? __ldg(p.bias + rf.boff[c0 + r] + (int64_t)key * p.bi_sj) : 0.f;
       }
       const bool sok = wait_all(&s_full[g & 1], (uint32_t)((g >> 1) & 1));
       bool trig = !sok;
       if (sok) {
         tc::fence_after();
-        float s[NR];
-        ld_cols<NR>(tl + kColS + 64u * (uint32_t)(g & 1), s);
+        float sc[NH];
+        ld_cols<NH>(tl + kColS + 64u * (uint32_t)(g & 1) + c0, sc);
         const bool tail = key0 + BK > rf.min_end;
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          float v = has_bias ? fmaf(s[r], p.scale_log2, x[r] * kLog2e) : s[r] * p.scale_log2;
-          if (tail && key >= rf.end[r]) v = kNegInf;
+        for (int r = 0; r < NH; ++r) {
+          float v = has_bias ? fmaf(sc[r], p.scale_log2, x[r] * kLog2e) : sc[r] * p.scale_log2;
+          if (tail && key >= rf.end[c0 + r]) v = kNegInf;
           x[r] = v;
         }
 #pragma unroll
-        for (int r4 = 0; r4 < NR / 4; ++r4) {
-          const float4 t4 = reinterpret_cast<const float4*>(s_thr)[r4];
+        for (int r4 = 0; r4 < NH / 4; ++r4) {
+          const float4 t4 = reinterpret_cast<const float4*>(s_thr + c0)[r4];
           trig |= (x[4 * r4] > t4.x) | (x[4 * r4 + 1] > t4.y) | (x[4 * r4 + 2] > t4.z) | (x[4 * r4 + 3] > t4.w);
         }
       } else if (lane == 0) {
         misc[2] = 1;
       }
       bool resc = false;
-      if (bar_or(kBarRows, 128, trig)) {
+      if (bar_or(kBarRows, kKeyThreads, trig)) {
         if (misc[2] != 0) { ok = false; break; }  // read after the barrier: same answer everywhere
         // ---- raise the reference maxima: tile maxima over the 128 keys ----
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
+        for (int r = 0; r < NH; ++r) {
           float v = x[r];
 #pragma unroll
           for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-          if (lane == (r & 31)) red[warp * NR + r] = v;
+          if (lane == (r & 31)) red[quarter * NR + c0 + r] = v;
         }
-        bar_sync(kBarRows, 128);
-        if (k < NR) {
+        bar_sync(kBarRows, kKeyThreads);
+        if (half == 0 && k < NR) {
           const float tmax = fmaxf(fmaxf(red[k], red[NR + k]), fmaxf(red[2 * NR + k], red[3 * NR + k]));
           const float mo = s_m[k];
           float a = 1.f;
@@ -628,40 +646,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           s_alpha[k] = a;
         }
-        bar_sync(kBarRows, 128);
+        bar_sync(kBarRows, kKeyThreads);
 #pragma unroll
-        for (int r4 = 0; r4 < NR / 4; ++r4) {
-          const float4 a4 = reinterpret_cast<const float4*>(s_alpha)[r4];
+        for (int r4 = 0; r4 < NH / 4; ++r4) {
+          const float4 a4 = reinterpret_cast<const float4*>(s_alpha + c0)[r4];
           lp[4 * r4] *= a4.x;
           lp[4 * r4 + 1] *= a4.y;
           lp[4 * r4 + 2] *= a4.z;
           lp[4 * r4 + 3] *= a4.w;
         }
         if (!first) {
-          // U^T lane k = value dim k, both parts; the product with P_{j-1}
-          // must have completed (U += P_j V_j waits for this tile's P)
-          const bool pv = bar_and(kBarRows, 128, wait_all(pv_done, (uint32_t)((g - 1) & 1)));
+          // U^T lane k = value dim k, this half's columns of both parts; the
+          // product with P_{j-1} must have completed (U += P_j V_j waits for
+          // this tile's P)
+          const bool pv = bar_and(kBarRows, kKeyThreads, wait_all(pv_done, (uint32_t)((g - 1) & 1)));
           if (!pv) { ok = false; break; }
           tc::fence_after();
-          const uint32_t ua = tl + kColU + 128u * (uint32_t)ub;
+          const uint32_t ua = tl + kColU + 128u * (uint32_t)ub + c0;
 #pragma unroll 1
           for (int part = 0; part < 2; ++part) {
-            float u[NR];
-            ld_cols<NR>(ua + 64u * part, u);
+            float u[NH];
+            ld_cols<NH>(ua + 64u * part, u);
 #pragma unroll
-            for (int r = 0; r < NR; ++r) u[r] *= s_alpha[r];
-            st_cols<NR>(ua + 64u * part, u);
+            for (int r = 0; r < NH; ++r) u[r] *= s_alpha[c0 + r];
+            st_cols<NH>(ua + 64u * part, u);
           }
           resc = true;
         }
       }
-      // ---- P^T row of key k: 2^(x - m), as bf16 P_hi + P_lo ----
+      // ---- P^T row of key k, this half's rows: 2^(x - m) as bf16 P_hi + P_lo ----
       {
         unsigned char* ph = sm + L::kOffP + (int)(g & 1) * kPBytes + k * 128;
 #pragma unroll
-        for (int c8 = 0; c8 < NR / 8; ++c8) {
-          const float4 m0 = reinterpret_cast<const float4*>(s_muse)[2 * c8];
-          const float4 m1 = reinterpret_cast<const float4*>(s_muse)[2 * c8 + 1];
+        for (int c8 = 0; c8 < NH / 8; ++c8) {
+          const float4 m0 = reinterpret_cast<const float4*>(s_muse + c0)[2 * c8];
+          const float4 m1 = reinterpret_cast<const float4*>(s_muse + c0)[2 * c8 + 1];
           const float mu[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
           uint32_t hi[4], lo[4];
 #pragma unroll
@@ -676,21 +695,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float rb = pb - __uint_as_float(__float_as_uint(pb) & 0xffff0000u);
             lo[e2] = pack_bf16(ra, rb);
           }
-          const int off = ((c8 ^ (k & 7)) << 4);
+          const int off = (((c0 / 8 + c8) ^ (k & 7)) << 4);
           *reinterpret_cast<uint4*>(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           *reinterpret_cast<uint4*>(ph + kBox + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
       if (cur.j == cur.n - 1 && key0 + BK > rf.unit_end) {
-        // the unit's last tile: zero the V rows past every visible key
+        // the unit's last tile: zero the V rows past every visible key (each
+        // half of the warps one 64-dim box)
         const int64_t sv = 2 * g + 1;
-        const bool vok = bar_and(kBarRows, 128, wait_all(&full[sv % kSlots], (uint32_t)((sv / kSlots) & 1)));
+        const bool vok = bar_and(kBarRows, kKeyThreads, wait_all(&full[sv % kSlots], (uint32_t)((sv / kSlots) & 1)));
         if (!vok) { ok = false; break; }
         if (key >= rf.unit_end) {
-          unsigned char* vr = sm + L::kOffRing + (int)(sv % kSlots) * kSlotBytes + k * 128;
+          unsigned char* vr = sm + L::kOffRing + (int)(sv % kSlots) * kSlotBytes + half * kBox + k * 128;
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            *reinterpret_cast<uint4*>(vr + (c >> 3) * kBox + (((c & 7) ^ (k & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vr + ((c ^ (k & 7)) << 4)) = make_uint4(0, 0, 0, 0);
         }
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P^T, V rows -> tensor core
@@ -702,25 +721,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (last) {
         // ---- epilogue of the unit (or of this CTA's part of it) ----
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
+        for (int r = 0; r < NH; ++r) {
           float v = lp[r];
 #pragma unroll
           for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-          if (lane == (r & 31)) red[warp * NR + r] = v;
+          if (lane == (r & 31)) red[quarter * NR + c0 + r] = v;
           lp[r] = 0.f;
         }
-        bar_sync(kBarRows, 128);
-        if (k < NR) s_l[k] = (red[k] + red[NR + k]) + (red[2 * NR + k] + red[3 * NR + k]);
-        const bool uok = bar_and(kBarRows, 128, wait_all(&u_full[ub], (uint32_t)((uidx >> 1) & 1)));
+        bar_sync(kBarRows, kKeyThreads);
+        if (half == 0 && k < NR) s_l[k] = (red[k] + red[NR + k]) + (red[2 * NR + k] + red[3 * NR + k]);
+        const bool uok = bar_and(kBarRows, kKeyThreads, wait_all(&u_full[ub], (uint32_t)((uidx >> 1) & 1)));
         if (!uok) { ok = false; break; }
         tc::fence_after();
-        float u[NR];
+        float u[NH];
         {
-          float ulo[NR];
-          ld_cols<NR>(tl + kColU + 128u * (uint32_t)ub, u);
-          ld_cols<NR>(tl + kColU + 128u * (uint32_t)ub + 64u, ulo);
+          float ulo[NH];
+          const uint32_t ua = tl + kColU + 128u * (uint32_t)ub + c0;
+          ld_cols<NH>(ua, u);
+          ld_cols<NH>(ua + 64u, ulo);
 #pragma unroll
-          for (int r = 0; r < NR; ++r) u[r] += ulo[r];  // U = P_hi V + P_lo V
+          for (int r = 0; r < NH; ++r) u[r] += ulo[r];  // U = P_hi V + P_lo V
         }
         const int64_t unit = ((int64_t)cur.b * Hkv + cur.kvh) * RG + cur.rg;
         const int64_t cf = cta_of(cur.su, W, P_work);
@@ -729,42 +749,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rr = min(R, p.rows_per_head - cur.rg * R);  // real rows of the unit
         if (nparts == 1) {
 #pragma unroll
-          for (int r = 0; r < NR; ++r) {
-            if (r >= rr) break;
-            const float m = s_m[r];
-            const float o = (m == kNegInf) ? 0.f : u[r] / s_l[r];
-            const int64_t oi = rf.ooff[r] + (int64_t)k * p.o_sd;
+          for (int r = 0; r < NH; ++r) {
+            const int row = c0 + r;
+            if (row >= rr) break;
+            const float m = s_m[row];
+            const float o = (m == kNegInf) ? 0.f : u[r] / s_l[row];
+            const int64_t oi = rf.ooff[row] + (int64_t)k * p.o_sd;
             if (p.out_bf16)
               static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
             else
               static_cast<float*>(p.out)[oi] = o;
           }
-          if (k < rr) {
+          if (half == 0 && k < rr) {
             const float m = s_m[k];
             p.lse[rf.loff[k]] = (m == kNegInf) ? kNegInf : (m + __log2f(s_l[k])) * kLn2;
           }
         } else {
           const int64_t slot = (int64_t)blockIdx.x + unit;
 #pragma unroll
-          for (int r = 0; r < NR; ++r) {
-            if (r >= rr) break;
-            p.ws_u[((slot * R + r) * D) + k] = u[r];
+          for (int r = 0; r < NH; ++r) {
+            const int row = c0 + r;
+            if (row >= rr) break;
+            p.ws_u[((slot * R + row) * D) + k] = u[r];
           }
-          if (k < rr) {
+          if (half == 0 && k < rr) {
             p.ws_m[slot * R + k] = s_m[k];
             p.ws_l[slot * R + k] = s_l[k];
           }
         }
-        if (k == 0 && blockIdx.x == cf) p.unit_info[unit] = make_int2((int)(cf + unit), nparts);
+        if (threadIdx.x == 0 && blockIdx.x == cf) p.unit_info[unit] = make_int2((int)(cf + unit), nparts);
         // fresh statistics for the next unit; the row facts are released
-        bar_sync(kBarRows, 128);
-        if (k < NR) {
+        bar_sync(kBarRows, kKeyThreads);
+        if (half == 0 && k < NR) {
           s_m[k] = kNegInf;
           s_muse[k] = 0.f;
           s_thr[k] = kNegInf;
         }
-        if (k == 0) mbar_arrive(&q_empty[ub]);
-        bar_sync(kBarRows, 128);
+        if (threadIdx.x == 0) mbar_arrive(&q_empty[ub]);
+        bar_sync(kBarRows, kKeyThreads);
         ++uidx;
       }
     }
