@@ -118,8 +118,10 @@ struct TcLayout {
   static constexpr int kRowsBytes = (int)((sizeof(RowFacts<NR>) + 15) / 16 * 16);
   static constexpr int kOffNTab = kOffRows + 2 * kRowsBytes;     // uint16 tiles per (sequence, row group)
   static constexpr int kOffRed = kOffNTab + kDecodeTcMaxEntries * 2;  // float [4][NR]
-  static constexpr int kOffStat = kOffRed + 4 * NR * 4;          // float m, m_use, thr, alpha, l [NR]
-  static constexpr int kOffBar = kOffStat + 5 * NR * 4;
+  // float [NR] each: m, m_use, thr, alpha of the current unit; m, l, 1 / l
+  // of the finished unit whose U readout is pending
+  static constexpr int kOffStat = kOffRed + 4 * NR * 4;
+  static constexpr int kOffBar = kOffStat + 7 * NR * 4;
   // full[kSlots], empty[kSlots], q_full[2], q_empty[2], s_full[2], p_full[2], u_full[2],
   // pv_done, drain
   static constexpr int kNumBars = 2 * kSlots + 2 + 2 + 2 + 2 + 2 + 1 + 1;
@@ -170,11 +172,6 @@ __device__ __forceinline__ int64_t cta_of(int64_t t, int64_t W, int64_t P) {
   return ((t + 1) * P + W - 1) / W - 1;
 }
 
-__device__ __forceinline__ int row_end_of(const FwdParams& p, int b, int i, int len) {
-  const int pos = p.qpos[b * p.qp_sb + i * p.qp_si];
-  return pos < 0 ? 0 : (pos >= len ? len : pos + 1);
-}
-
 // N consecutive TMEM columns of this thread's lane (N = 8, 16 or 24; the
 // column offset is a multiple of 8, of 16 for N = 16) -> floats.
 template <int N>
@@ -222,7 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* s_muse = s_m + NR;                                  // m, or 0 when none yet
   float* s_thr = s_m + 2 * NR;                               // m + 8, -inf when none yet
   float* s_alpha = s_m + 3 * NR;
-  float* s_l = s_m + 4 * NR;
+  float* s_mfin = s_m + 4 * NR;
+  float* s_lfin = s_m + 5 * NR;
+  float* s_inv = s_m + 6 * NR;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kOffBar);
   uint64_t* full = bars;
   uint64_t* empty = full + kSlots;
@@ -252,16 +251,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int e = threadIdx.x; e < E; e += kThreads) {
       const int b = e / RG;
       const int rg = e - b * RG;
-      int len = p.seqlens[b * p.sl_s];
-      len = len < 0 ? 0 : (len > p.Tmax ? p.Tmax : len);
+      // the row end min(len, pos + 1) (0 for pos < 0) grows with pos, so the
+      // unit's end follows from the largest position of its rows; all loads
+      // are independent (one round trip)
+      const int len_raw = p.seqlens[b * p.sl_s];
       const int pk0 = rg * R;
       const int pk1 = min(pk0 + R, p.rows_per_head);
-      int uend = 0;
+      int maxpos = -1;
       if (pk1 - pk0 >= p.Tq) {
-        for (int i = 0; i < p.Tq; ++i) uend = max(uend, row_end_of(p, b, i, len));
+#pragma unroll 4
+        for (int i = 0; i < p.Tq; ++i) maxpos = max(maxpos, p.qpos[b * p.qp_sb + i * p.qp_si]);
       } else {
-        for (int pk = pk0; pk < pk1; ++pk) uend = max(uend, row_end_of(p, b, pk % p.Tq, len));
+#pragma unroll 4
+        for (int pk = pk0; pk < pk1; ++pk) maxpos = max(maxpos, p.qpos[b * p.qp_sb + (pk % p.Tq) * p.qp_si]);
       }
+      const int len = len_raw < 0 ? 0 : (len_raw > p.Tmax ? p.Tmax : len_raw);
+      const int uend = maxpos < 0 ? 0 : min(maxpos + 1, len);
       const int n = (uend + BK - 1) / BK;
       ntab[e] = (uint16_t)(n < 1 ? 1 : n);  // an all-empty unit still takes one (masked) tile
     }
@@ -421,11 +426,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) w = mbar_wait(&q_empty[qb], (uint32_t)(((uidx >> 1) - 1) & 1));
         if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
       }
-      // query rows of the unit, 128-byte swizzled K-major (rows of 64 dims)
+      // every global load of the unit first (one round trip): cache length,
+      // positions of this lane's rows, query rows
       unsigned char* qs = sm + L::kOffQ + qb * L::kQBytes;
       const int b = cur.b;
-      int len = p.seqlens[b * p.sl_s];
-      len = len < 0 ? 0 : (len > p.Tmax ? p.Tmax : len);
+      const int len_raw = p.seqlens[b * p.sl_s];
+      int pos[2] = {-1, -1};
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int r = lane + 32 * h2;
+        const int pk = cur.rg * R + r;
+        if (r < NR && r < R && pk < p.rows_per_head) pos[h2] = p.qpos[b * p.qp_sb + (pk % p.Tq) * p.qp_si];
+      }
       uint4 val[NR / 2];
 #pragma unroll
       for (int it = 0; it < NR / 2; ++it) {
@@ -442,6 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           val[it] = __ldg(reinterpret_cast<const uint4*>(qrow) + c);
         }
       }
+      // query rows, 128-byte swizzled K-major (rows of 64 dims)
 #pragma unroll
       for (int it = 0; it < NR / 2; ++it) {
         const int idx = lane + 32 * it;
@@ -450,9 +463,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4*>(qs + (c >> 3) * L::kQBox + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = val[it];
       }
       // integer facts of the rows
+      const int len = len_raw < 0 ? 0 : (len_raw > p.Tmax ? p.Tmax : len_raw);
       RowFacts<NR>& rf = facts0[qb];
       int umax = 0, umin = 0x7fffffff;
-      for (int r = lane; r < NR; r += 32) {
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int r = lane + 32 * h2;
+        if (r >= NR) break;
         const int pk = cur.rg * R + r;
         int e = 0;
         int64_t bo = 0, oo = 0, lo = 0;
@@ -460,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int g = pk / p.Tq;
           const int i = pk - g * p.Tq;
           const int h = cur.kvh * p.G + g;
-          e = row_end_of(p, b, i, len);
+          e = pos[h2] < 0 ? 0 : min(pos[h2] + 1, len);
           bo = (int64_t)b * p.bi_sb + (int64_t)h * p.bi_sh + (int64_t)i * p.bi_si;
           oo = (int64_t)b * p.o_sb + (int64_t)h * p.o_sh + (int64_t)i * p.o_si;
           lo = (int64_t)b * p.l_sb + (int64_t)h * p.l_sh + (int64_t)i * p.l_si;
@@ -581,6 +598,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; r < NH; ++r) lp[r] = 0.f;
     int uidx = 0;
     bool ok = true;
+    // A finished unit's U is read one tile later, after the next tile's P:
+    // by then its last product has completed and the readout does not stall
+    // the pipeline.  Its m, l and 1 / l wait in s_mfin / s_lfin / s_inv, its
+    // row facts stay in their buffer until the readout releases them.
+    bool pend = false;
+    int pend_uidx = 0, pend_b = 0, pend_kvh = 0, pend_rg = 0, pend_n = 1;
+    int64_t pend_su = 0;
+    auto flush = [&]() -> bool {
+      const int pb = pend_uidx & 1;
+      const RowFacts<NR>& pf = facts0[pb];
+      if (!bar_and(kBarRows, kKeyThreads, wait_all(&u_full[pb], (uint32_t)((pend_uidx >> 1) & 1)))) return false;
+      tc::fence_after();
+      float u[NH];
+      {
+        float ulo[NH];
+        const uint32_t ua = tl + kColU + 128u * (uint32_t)pb + c0;
+        ld_cols<NH>(ua, u);
+        ld_cols<NH>(ua + 64u, ulo);
+#pragma unroll
+        for (int r = 0; r < NH; ++r) u[r] += ulo[r];  // U = P_hi V + P_lo V
+      }
+      const int64_t unit = ((int64_t)pend_b * Hkv + pend_kvh) * RG + pend_rg;
+      const int64_t cf = cta_of(pend_su, W, P_work);
+      const int64_t cl = cta_of(pend_su + pend_n - 1, W, P_work);
+      const int nparts = (int)(cl - cf + 1);
+      const int rr = min(R, p.rows_per_head - pend_rg * R);  // real rows of the unit
+      if (nparts == 1) {
+#pragma unroll
+        for (int r = 0; r < NH; ++r) {
+          const int row = c0 + r;
+          if (row >= rr) break;
+          const float o = (s_mfin[row] == kNegInf) ? 0.f : u[r] * s_inv[row];
+          const int64_t oi = pf.ooff[row] + (int64_t)k * p.o_sd;
+          if (p.out_bf16)
+            static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+          else
+            static_cast<float*>(p.out)[oi] = o;
+        }
+        if (half == 0 && k < rr) {
+          const float m = s_mfin[k];
+          p.lse[pf.loff[k]] = (m == kNegInf) ? kNegInf : (m + __log2f(s_lfin[k])) * kLn2;
+        }
+      } else {
+        const int64_t slot = (int64_t)blockIdx.x + unit;
+#pragma unroll
+        for (int r = 0; r < NH; ++r) {
+          const int row = c0 + r;
+          if (row >= rr) break;
+          p.ws_u[((slot * R + row) * D) + k] = u[r];
+        }
+        if (half == 0 && k < rr) {
+          p.ws_m[slot * R + k] = s_mfin[k];
+          p.ws_l[slot * R + k] = s_lfin[k];
+        }
+      }
+      if (threadIdx.x == 0 && blockIdx.x == cf) p.unit_info[unit] = make_int2((int)(cf + unit), nparts);
+      bar_sync(kBarRows, kKeyThreads);  // the finished unit's statistics and row facts are read
+      if (threadIdx.x == 0) mbar_arrive(&q_empty[pb]);
+      return true;
+    };
     for (; cur.t < t1; cur.next(ntab, RG, Hkv, B)) {
       const bool first = cur.t == t0 || cur.j == 0;
       const bool last = cur.t == t1 - 1 || cur.j == cur.n - 1;
@@ -718,8 +795,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[g & 1]);
 
+      // the U readout of the previous unit (its last product has long
+      // completed by now)
+      if (pend) {
+        if (!flush()) { ok = false; break; }
+        pend = false;
+      }
       if (last) {
-        // ---- epilogue of the unit (or of this CTA's part of it) ----
+        // ---- close the unit (or this CTA's part of it): l over the keys ----
 #pragma unroll
         for (int r = 0; r < NH; ++r) {
           float v = lp[r];
@@ -729,67 +812,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           lp[r] = 0.f;
         }
         bar_sync(kBarRows, kKeyThreads);
-        if (half == 0 && k < NR) s_l[k] = (red[k] + red[NR + k]) + (red[2 * NR + k] + red[3 * NR + k]);
-        const bool uok = bar_and(kBarRows, kKeyThreads, wait_all(&u_full[ub], (uint32_t)((uidx >> 1) & 1)));
-        if (!uok) { ok = false; break; }
-        tc::fence_after();
-        float u[NH];
-        {
-          float ulo[NH];
-          const uint32_t ua = tl + kColU + 128u * (uint32_t)ub + c0;
-          ld_cols<NH>(ua, u);
-          ld_cols<NH>(ua + 64u, ulo);
-#pragma unroll
-          for (int r = 0; r < NH; ++r) u[r] += ulo[r];  // U = P_hi V + P_lo V
-        }
-        const int64_t unit = ((int64_t)cur.b * Hkv + cur.kvh) * RG + cur.rg;
-        const int64_t cf = cta_of(cur.su, W, P_work);
-        const int64_t cl = cta_of(cur.su + cur.n - 1, W, P_work);
-        const int nparts = (int)(cl - cf + 1);
-        const int rr = min(R, p.rows_per_head - cur.rg * R);  // real rows of the unit
-        if (nparts == 1) {
-#pragma unroll
-          for (int r = 0; r < NH; ++r) {
-            const int row = c0 + r;
-            if (row >= rr) break;
-            const float m = s_m[row];
-            const float o = (m == kNegInf) ? 0.f : u[r] / s_l[row];
-            const int64_t oi = rf.ooff[row] + (int64_t)k * p.o_sd;
-            if (p.out_bf16)
-              static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
-            else
-              static_cast<float*>(p.out)[oi] = o;
-          }
-          if (half == 0 && k < rr) {
-            const float m = s_m[k];
-            p.lse[rf.loff[k]] = (m == kNegInf) ? kNegInf : (m + __log2f(s_l[k])) * kLn2;
-          }
-        } else {
-          const int64_t slot = (int64_t)blockIdx.x + unit;
-#pragma unroll
-          for (int r = 0; r < NH; ++r) {
-            const int row = c0 + r;
-            if (row >= rr) break;
-            p.ws_u[((slot * R + row) * D) + k] = u[r];
-          }
-          if (half == 0 && k < rr) {
-            p.ws_m[slot * R + k] = s_m[k];
-            p.ws_l[slot * R + k] = s_l[k];
-          }
-        }
-        if (threadIdx.x == 0 && blockIdx.x == cf) p.unit_info[unit] = make_int2((int)(cf + unit), nparts);
-        // fresh statistics for the next unit; the row facts are released
-        bar_sync(kBarRows, kKeyThreads);
         if (half == 0 && k < NR) {
+          const float l = (red[k] + red[NR + k]) + (red[2 * NR + k] + red[3 * NR + k]);
+          const float m = s_m[k];
+          s_mfin[k] = m;
+          s_lfin[k] = l;
+          s_inv[k] = (m == kNegInf) ? 0.f : 1.f / l;
+          // fresh statistics for the next unit
           s_m[k] = kNegInf;
           s_muse[k] = 0.f;
           s_thr[k] = kNegInf;
         }
-        if (threadIdx.x == 0) mbar_arrive(&q_empty[ub]);
         bar_sync(kBarRows, kKeyThreads);
+        pend = true;
+        pend_uidx = uidx;
+        pend_su = cur.su;
+        pend_b = cur.b;
+        pend_kvh = cur.kvh;
+        pend_rg = cur.rg;
+        pend_n = cur.n;
         ++uidx;
       }
     }
+    if (ok && pend && !flush()) ok = false;
     if (!ok && lane == 0) record_error(p.err, kErrTimeout);
   }
 
