@@ -406,6 +406,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(dst + kBox, map, 64, cur.j * BK, cur.kvh, cur.b, &full[s], pol);
           issued = seq + 1;
         }
+        // after the first tile, let the first unit's query rows land before
+        // the stream fills the memory queues (they gate the first product)
+        if (ok && g == 0 && !mbar_wait(&q_full[0], 0)) ok = false;
       }
       // every issued copy must land before the CTA exits
       for (int64_t seq = issued - kSlots < 0 ? 0 : issued - kSlots; seq < issued; ++seq)
@@ -426,40 +429,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) w = mbar_wait(&q_empty[qb], (uint32_t)(((uidx >> 1) - 1) & 1));
         if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
       }
-      // every global load of the unit first (one round trip): cache length,
-      // positions of this lane's rows, query rows
+      // lane l describes rows l and l + 32 (one division each), then every
+      // global load of the unit is issued before any is used (one round
+      // trip): cache length, positions, query rows
       unsigned char* qs = sm + L::kOffQ + qb * L::kQBytes;
       const int b = cur.b;
       const int len_raw = p.seqlens[b * p.sl_s];
-      int pos[2] = {-1, -1};
+      bool real[2];
+      int hrow[2], irow[2], pos[2] = {-1, -1};
+      const __nv_bfloat16* qrow[2];
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         const int r = lane + 32 * h2;
         const int pk = cur.rg * R + r;
-        if (r < NR && r < R && pk < p.rows_per_head) pos[h2] = p.qpos[b * p.qp_sb + (pk % p.Tq) * p.qp_si];
+        real[h2] = r < NR && r < R && pk < p.rows_per_head;
+        const int g = real[h2] ? pk / p.Tq : 0;
+        irow[h2] = real[h2] ? pk - g * p.Tq : 0;
+        hrow[h2] = cur.kvh * p.G + g;
+        qrow[h2] = static_cast<const __nv_bfloat16*>(p.q) + (int64_t)b * p.q_sb + (int64_t)hrow[h2] * p.q_sh +
+                   (int64_t)irow[h2] * p.q_si;
+        if (real[h2]) pos[h2] = p.qpos[b * p.qp_sb + irow[h2] * p.qp_si];
       }
       uint4 val[NR / 2];
 #pragma unroll
       for (int it = 0; it < NR / 2; ++it) {
-        const int idx = lane + 32 * it;
-        const int r = idx >> 4;
-        const int c = idx & 15;
-        const int pk = cur.rg * R + r;
-        val[it] = make_uint4(0, 0, 0, 0);
-        if (r < R && pk < p.rows_per_head) {
-          const int g = pk / p.Tq;
-          const int i = pk - g * p.Tq;
-          const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) + (int64_t)b * p.q_sb +
-                                      (int64_t)(cur.kvh * p.G + g) * p.q_sh + (int64_t)i * p.q_si;
-          val[it] = __ldg(reinterpret_cast<const uint4*>(qrow) + c);
-        }
+        // chunk (lane & 15) of row 2 it + (lane >> 4), described by lane (row & 31)
+        const int r = 2 * it + (lane >> 4);
+        const int set = (2 * it) >> 5;  // rows of this iteration are all < 32 or all >= 32
+        const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(qrow[set]), r & 31));
+        const bool rr = __shfl_sync(0xffffffffu, real[set], r & 31);
+        val[it] = rr ? __ldg(reinterpret_cast<const uint4*>(src) + (lane & 15)) : make_uint4(0, 0, 0, 0);
       }
       // query rows, 128-byte swizzled K-major (rows of 64 dims)
 #pragma unroll
       for (int it = 0; it < NR / 2; ++it) {
-        const int idx = lane + 32 * it;
-        const int r = idx >> 4;
-        const int c = idx & 15;
+        const int r = 2 * it + (lane >> 4);
+        const int c = lane & 15;
         *reinterpret_cast<uint4*>(qs + (c >> 3) * L::kQBox + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = val[it];
       }
       // integer facts of the rows
@@ -470,18 +476,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int h2 = 0; h2 < 2; ++h2) {
         const int r = lane + 32 * h2;
         if (r >= NR) break;
-        const int pk = cur.rg * R + r;
         int e = 0;
         int64_t bo = 0, oo = 0, lo = 0;
-        if (r < R && pk < p.rows_per_head) {
-          const int g = pk / p.Tq;
-          const int i = pk - g * p.Tq;
-          const int h = cur.kvh * p.G + g;
+        if (real[h2]) {
+          const int h = hrow[h2], i = irow[h2];
           e = pos[h2] < 0 ? 0 : min(pos[h2] + 1, len);
           bo = (int64_t)b * p.bi_sb + (int64_t)h * p.bi_sh + (int64_t)i * p.bi_si;
           oo = (int64_t)b * p.o_sb + (int64_t)h * p.o_sh + (int64_t)i * p.o_si;
           lo = (int64_t)b * p.l_sb + (int64_t)h * p.l_sh + (int64_t)i * p.l_si;
           umin = min(umin, e);
+          if (p.bias != nullptr) {
+            // the bias of the unit's first tile here into L2 (new rows miss)
+            const int j0 = cur.j * BK;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int key = j0 + 32 * q4;
+              if (key < p.Tmax)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(p.bias + bo + (int64_t)key * p.bi_sj));
+            }
+          }
         }
         umax = max(umax, e);
         rf.end[r] = e;
@@ -672,11 +685,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int key0 = cur.j * BK;
       const int key = key0 + k;
       float x[NH];
-      if (has_bias) {  // issued before the wait: the loads overlap the products
+      if (has_bias) {
+        // this tile's bias (prefetched into L1 one tile ahead), then the
+        // next tile's of the same unit into L1
         const bool kin = key < p.Tmax;
+        const bool kin2 = cur.j + 1 < cur.n && key + BK < p.Tmax;
 #pragma unroll
-        for (int r = 0; r < NH; ++r)
-          x[r] = kin ? __ldg(p.bias + rf.boff[c0 + r] + (int64_t)key * p.bi_sj) : 0.f;
+        for (int r = 0; r < NH; ++r) {
+          const float* bp = p.bias + rf.boff[c0 + r] + (int64_t)key * p.bi_sj;
+          x[r] = kin ? __ldg(bp) : 0.f;
+          if (kin2) asm volatile("prefetch.global.L1 [%0];" ::"l"(bp + (int64_t)BK * p.bi_sj));
+        }
       }
       const bool sok = wait_all(&s_full[g & 1], (uint32_t)((g >> 1) & 1));
       bool trig = !sok;
