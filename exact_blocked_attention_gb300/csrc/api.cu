@@ -31,6 +31,10 @@ struct DeviceState {
   int* err = nullptr;
   void* ws = nullptr;
   size_t ws_bytes = 0;
+  // per-unit counters of the tcgen05 decode kernel: zeroed when allocated,
+  // left zero by every launch
+  unsigned* cnt = nullptr;
+  size_t cnt_n = 0;
 };
 
 std::mutex g_mu;
@@ -55,6 +59,7 @@ struct Plan {
   int tile;
   int64_t ctas;
   int64_t ws_bytes;
+  int64_t units = 0;  // tcgen05 decode kernel: per-unit counters needed
 };
 
 int resident_ctas_per_sm(size_t smem_bytes) {
@@ -110,7 +115,8 @@ Plan make_plan(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tmax, int
       pl.tile = 128;
       pl.ctas = P;
       auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
-      pl.ws_bytes = 2 * al(slots * R * 4) + al(slots * R * d * 4) + al(U * 8);
+      pl.ws_bytes = 2 * al(slots * R * 4) + al(slots * R * d * 4);
+      pl.units = U;
       return pl;
     }
   }
@@ -274,6 +280,28 @@ int ensure_workspace(DeviceState* s, size_t bytes, cudaStream_t stream) {
   return BLKATTN_OK;
 }
 
+// Grow-only per-device counters (zeroed on allocation, on the call's stream;
+// the kernel leaves them zero).  Growing while the stream is being captured
+// is refused.
+int ensure_counters(DeviceState* s, int64_t n, cudaStream_t stream) {
+  if ((size_t)n <= s->cnt_n) return BLKATTN_OK;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return BLKATTN_ERR_CUDA;
+  if (cs != cudaStreamCaptureStatusNone) return BLKATTN_ERR_NO_WORKSPACE;
+  if (s->cnt) {
+    if (cudaFree(s->cnt) != cudaSuccess) return BLKATTN_ERR_CUDA;
+    s->cnt = nullptr;
+    s->cnt_n = 0;
+  }
+  if (cudaMalloc(&s->cnt, (size_t)n * sizeof(unsigned)) != cudaSuccess) {
+    s->cnt = nullptr;
+    return BLKATTN_ERR_CUDA;
+  }
+  if (cudaMemsetAsync(s->cnt, 0, (size_t)n * sizeof(unsigned), stream) != cudaSuccess) return BLKATTN_ERR_CUDA;
+  s->cnt_n = (size_t)n;
+  return BLKATTN_OK;
+}
+
 struct Checked {
   int64_t B, Hq, Hkv, Tq, Tmax, d;
   Elt elt;
@@ -348,7 +376,8 @@ int validate_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn
 FwdParams fill_params(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
                       const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos,
                       const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out,
-                      const blkattn_tensor* lse, const Checked& c, const Plan& pl, void* ws, int* err) {
+                      const blkattn_tensor* lse, const Checked& c, const Plan& pl, void* ws, int* err,
+                      unsigned* counters) {
   const int eb = elt_bytes(q->dtype);
   FwdParams p;
   std::memset(&p, 0, sizeof p);
@@ -381,16 +410,15 @@ FwdParams fill_params(const blkattn_tensor* q, const blkattn_tensor* k, const bl
   p.chunk = pl.cfg.chunk;
   p.n_splits = pl.cfg.n_splits;
   p.rows_cta = pl.cfg.rows_per_cta;
+  p.unit_cnt = counters;
   if (pl.cfg.kernel == blkattn::Kernel::DecodeTc) {
-    // per-CTA partial states: [slots][rows_cta] (m, l), [slots][rows_cta][d] (u),
-    // then {first slot, count} per unit
+    // per-CTA partial states: [slots][rows_cta] (m, l), [slots][rows_cta][d] (u)
     auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
     const int64_t n = (int64_t)pl.cfg.n_splits * pl.cfg.rows_per_cta;
     char* base = static_cast<char*>(ws);
     p.ws_m = reinterpret_cast<float*>(base);
     p.ws_l = reinterpret_cast<float*>(base + al(n * 4));
     p.ws_u = reinterpret_cast<float*>(base + 2 * al(n * 4));
-    p.unit_info = reinterpret_cast<int2*>(base + 2 * al(n * 4) + al(n * c.d * 4));
   } else if (pl.cfg.n_splits > 1) {
     const int64_t n = c.B * c.Hq * c.Tq * (int64_t)pl.cfg.n_splits;
     char* base = static_cast<char*>(ws);
@@ -459,8 +487,9 @@ int launch_fwd(const FwdParams& p, const Checked& c, const Plan& pl, const blkat
   if (le != cudaSuccess) return BLKATTN_ERR_CUDA;
   if (g_split_event != nullptr && cudaEventRecord(g_split_event, stream) != cudaSuccess)
     return BLKATTN_ERR_CUDA;
-  // the tcgen05 decode kernel decides on the device which units need merging
-  if (pl.cfg.n_splits > 1 && blkattn::launch_split_merge(p, (int)c.d, stream) != cudaSuccess)
+  // the tcgen05 decode kernel folds its split units itself
+  if (pl.cfg.kernel != blkattn::Kernel::DecodeTc && pl.cfg.n_splits > 1 &&
+      blkattn::launch_split_merge(p, (int)c.d, stream) != cudaSuccess)
     return BLKATTN_ERR_CUDA;
   return BLKATTN_OK;
 }
@@ -498,9 +527,15 @@ int fwd_with_scratch(const blkattn_tensor* q, const blkattn_tensor* k, const blk
   if ((pl.cfg.kernel == blkattn::Kernel::TensorCore || pl.cfg.kernel == blkattn::Kernel::CudaCore) &&
       c.B * pl.cfg.row_groups > 65535)
     return BLKATTN_ERR_UNSUPPORTED;  // grid z of the split-KV kernels
-  if ((size_t)pl.ws_bytes > scratch_bytes) return BLKATTN_ERR_SCRATCH_LIMIT;
+  // the last kStaticCounterBytes hold the per-unit counters (zero initially,
+  // left zero by every call); plans get the rest
+  if (scratch_bytes < blkattn::kStaticCounterBytes) return BLKATTN_ERR_SCRATCH_LIMIT;
+  const size_t usable = scratch_bytes - blkattn::kStaticCounterBytes;
+  if ((size_t)pl.ws_bytes > usable) return BLKATTN_ERR_SCRATCH_LIMIT;
+  if ((size_t)pl.units * sizeof(unsigned) > blkattn::kStaticCounterBytes) return BLKATTN_ERR_SCRATCH_LIMIT;
+  unsigned* counters = reinterpret_cast<unsigned*>(static_cast<char*>(scratch) + usable);
   const FwdParams p = fill_params(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, c, pl,
-                                  scratch, ds->err);
+                                  scratch, ds->err, counters);
   return launch_fwd(p, c, pl, q, k, v, stream);
 }
 
@@ -562,8 +597,12 @@ int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_
     st = ensure_workspace(ds, (size_t)pl.ws_bytes, stream);
     if (st != BLKATTN_OK) return st;
   }
+  if (pl.units > 0) {
+    st = ensure_counters(ds, pl.units, stream);
+    if (st != BLKATTN_OK) return st;
+  }
   const FwdParams p = fill_params(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, c, pl,
-                                  ds->ws, ds->err);
+                                  ds->ws, ds->err, ds->cnt);
   return launch_fwd(p, c, pl, q, k, v, stream);
 }
 
@@ -602,6 +641,14 @@ int blkattn_check_device_error(blkattn_stream_t stream_) {
   if (word != 0) {
     const int zero = 0;
     if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof zero) != cudaSuccess) return BLKATTN_ERR_CUDA;
+    // a kernel that gave up may have left unit counters behind: restart them
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+      std::lock_guard<std::mutex> lock(g_mu);
+      DeviceState& ds = g_dev[dev];
+      if (ds.cnt && cudaMemset(ds.cnt, 0, ds.cnt_n * sizeof(unsigned)) != cudaSuccess) return BLKATTN_ERR_CUDA;
+    }
+    blkattn::clear_static_counters();
     return BLKATTN_ERR_DEVICE_TIMEOUT;
   }
   return BLKATTN_OK;

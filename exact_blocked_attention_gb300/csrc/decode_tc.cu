@@ -21,9 +21,11 @@
 //
 // Work split: the key tiles of all units, in the order (sequence, KV head,
 // row group, tile), are cut into P = min(gridDim.x, tiles) equal contiguous
-// non-empty ranges, one per CTA (one CTA per SM).  A unit whose tiles lie in one CTA is finished in
-// place; otherwise each CTA leaves its partial state of the unit in the
-// workspace slot (CTA index + unit index) and the merge kernel folds them.
+// non-empty ranges, one per CTA (one CTA per SM).  A unit whose tiles lie in
+// one CTA is finished in place; otherwise each CTA writes its partial state
+// of the unit to workspace slot (CTA index + unit index), counts itself in
+// the unit's counter, and the last CTA to arrive folds the unit's partial
+// states (no second kernel, no CTA ever waits for another).
 // The tile counts come from the device-resident lengths and positions, so
 // every CTA streams the same number of tiles whatever the length mix, and no
 // SM idles at the end.
@@ -233,7 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pv_done = u_full + 2;     // once per U += P V product
   uint64_t* drain = pv_done + 1;
   // misc: [0] tmem base, [1] error seen by the producer / MMA thread,
-  // [2] abort of the key threads (written before a barrier, read after it)
+  // [2] abort of the key threads, [3] "this CTA folds the unit" (both
+  // written before a barrier of the key threads, read after it)
   int* misc = reinterpret_cast<int*>(sm + L::kOffMisc);
   Start* start = reinterpret_cast<Start*>(sm + L::kOffMisc + 64);
 
@@ -654,6 +657,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.lse[pf.loff[k]] = (m == kNegInf) ? kNegInf : (m + __log2f(s_lfin[k])) * kLn2;
         }
       } else {
+        // this CTA's partial state of the unit, then the last of the unit's
+        // CTAs to get here folds all of them (eqs. 33.4-33.5, in CTA order)
         const int64_t slot = (int64_t)blockIdx.x + unit;
 #pragma unroll
         for (int r = 0; r < NH; ++r) {
@@ -665,8 +670,85 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.ws_m[slot * R + k] = s_mfin[k];
           p.ws_l[slot * R + k] = s_lfin[k];
         }
+        __threadfence();  // the partial state is visible before the count says so
+        bar_sync(kBarRows, kKeyThreads);
+        if (threadIdx.x == 0)
+          misc[3] = (atomicAdd(&p.unit_cnt[unit], 1u) == (unsigned)(nparts - 1)) ? 1 : 0;
+        bar_sync(kBarRows, kKeyThreads);
+        if (misc[3] != 0) {
+          __threadfence();
+          if (threadIdx.x == 0) p.unit_cnt[unit] = 0u;  // ready for the next launch
+          const int64_t fs = cf + unit;  // the unit's first slot; its parts are consecutive
+          // items (row, 4 value dims) over the key threads, two items at a
+          // time, the parts in batches of 4: all loads of a step in flight
+          const int n_items = rr * (D / 4);
+          for (int it0 = threadIdx.x; it0 < n_items; it0 += 2 * kKeyThreads) {
+            int row[2], d4[2];
+            bool live[2];
+            float M[2] = {kNegInf, kNegInf}, Ls[2] = {0.f, 0.f};
+            float4 Us[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+#pragma unroll
+            for (int x2 = 0; x2 < 2; ++x2) {
+              const int item = it0 + x2 * kKeyThreads;
+              live[x2] = item < n_items;
+              row[x2] = live[x2] ? item / (D / 4) : 0;
+              d4[x2] = live[x2] ? item - row[x2] * (D / 4) : 0;
+            }
+            for (int s0 = 0; s0 < nparts; s0 += 4) {
+              float ms[2][4], ls[2][4];
+              float4 us[2][4];
+#pragma unroll
+              for (int x2 = 0; x2 < 2; ++x2)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  ms[x2][e] = kNegInf;
+                  if (live[x2] && s0 + e < nparts) {
+                    const int64_t idx = (fs + s0 + e) * R + row[x2];
+                    ms[x2][e] = __ldcg(p.ws_m + idx);
+                    ls[x2][e] = __ldcg(p.ws_l + idx);
+                    us[x2][e] = __ldcg(reinterpret_cast<const float4*>(p.ws_u + idx * D) + d4[x2]);
+                  }
+                }
+#pragma unroll
+              for (int x2 = 0; x2 < 2; ++x2)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  if (ms[x2][e] == kNegInf) continue;  // an empty part contributes nothing
+                  float ca, cb;                        // scale of the running sum, of part e
+                  if (ms[x2][e] > M[x2]) {
+                    ca = (M[x2] == kNegInf) ? 0.f : fast_exp2(M[x2] - ms[x2][e]);
+                    cb = 1.f;
+                    M[x2] = ms[x2][e];
+                  } else {
+                    ca = 1.f;
+                    cb = fast_exp2(ms[x2][e] - M[x2]);
+                  }
+                  Ls[x2] = fmaf(Ls[x2], ca, cb * ls[x2][e]);
+                  Us[x2].x = fmaf(Us[x2].x, ca, cb * us[x2][e].x);
+                  Us[x2].y = fmaf(Us[x2].y, ca, cb * us[x2][e].y);
+                  Us[x2].z = fmaf(Us[x2].z, ca, cb * us[x2][e].z);
+                  Us[x2].w = fmaf(Us[x2].w, ca, cb * us[x2][e].w);
+                }
+            }
+#pragma unroll
+            for (int x2 = 0; x2 < 2; ++x2) {
+              if (!live[x2]) continue;
+              const float inv = (M[x2] == kNegInf) ? 0.f : 1.f / Ls[x2];
+              const float o4[4] = {Us[x2].x * inv, Us[x2].y * inv, Us[x2].z * inv, Us[x2].w * inv};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int64_t oi = pf.ooff[row[x2]] + (int64_t)(4 * d4[x2] + e) * p.o_sd;
+                if (p.out_bf16)
+                  static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o4[e]);
+                else
+                  static_cast<float*>(p.out)[oi] = o4[e];
+              }
+              if (d4[x2] == 0)
+                p.lse[pf.loff[row[x2]]] = (M[x2] == kNegInf) ? kNegInf : (M[x2] + __log2f(Ls[x2])) * kLn2;
+            }
+          }
+        }
       }
-      if (threadIdx.x == 0 && blockIdx.x == cf) p.unit_info[unit] = make_int2((int)(cf + unit), nparts);
       bar_sync(kBarRows, kKeyThreads);  // the finished unit's statistics and row facts are read
       if (threadIdx.x == 0) mbar_arrive(&q_empty[pb]);
       return true;

@@ -3,11 +3,13 @@
 // its own pool, a latency-critical loop that cannot take cudaMalloc's
 // synchronisation, a runtime that forbids allocation after start-up).
 //
-// The split-KV kernel's per-split partial states go to one fixed array that
-// is part of the library image, so the call allocates nothing.  The array is
-// shared by every call on a device and keeps the last call's contents; no
-// part of it must start at zero (each call writes every state it reads back),
-// but calls that overlap on the GPU race on it.
+// The split kernels' partial states go to one fixed array that is part of
+// the library image, so the call allocates nothing.  The array is shared by
+// every call on a device and keeps the last call's contents.  Its last
+// kStaticCounterBytes hold the tcgen05 decode kernel's per-unit counters:
+// zero when the library loads and left zero by every call; the rest never
+// has to start at zero (each call writes every state it reads back).  Calls
+// that overlap on the GPU race on it.
 #include <mutex>
 
 #include "blkattn.h"
@@ -44,6 +46,19 @@ int scratch_address(void** out) {
 }
 
 }  // namespace
+
+namespace blkattn {
+// After a kernel gave up a bounded wait: zero the counters region of the
+// array on the current device (if this device ever used it).
+void clear_static_counters() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_dev_addr[dev] != nullptr)
+    cudaMemset(static_cast<char*>(g_scratch_dev_addr[dev]) + kScratchBytes - kStaticCounterBytes, 0,
+               kStaticCounterBytes);
+}
+}  // namespace blkattn
 
 extern "C" int blkattn_fwd_static_scratch(const blkattn_tensor* q, const blkattn_tensor* k,
                                           const blkattn_tensor* v, const blkattn_tensor* seqlens_k,

@@ -52,11 +52,12 @@ struct FwdParams {
   float* ws_u;
   int* err;  // device error word
   int head_group;  // prefill: (sequence, head) pairs dispatched together (L2 reuse of K/V)
-  // tcgen05 decode kernel: query rows per unit (one row group of one KV head),
-  // and per unit {first workspace slot, number of partial states}; the partial
-  // state of unit row r in slot s sits at index s * rows_cta + r
+  // tcgen05 decode kernel: query rows per unit (one row group of one KV head);
+  // the partial state of unit row r from CTA c sits in slot c + unit, at
+  // index slot * rows_cta + r; unit_cnt counts the CTAs of each unit that
+  // wrote theirs (zero before the launch, left zero after it)
   int rows_cta;
-  int2* unit_info;
+  unsigned* unit_cnt;
 };
 
 // Split-KV kernel configuration chosen by the planner.
@@ -106,6 +107,11 @@ int prefill_tc_smem_bytes();
 // The (sequence, row group) table lives in shared memory: B * row_groups
 // must not exceed kDecodeTcMaxEntries.
 constexpr int kDecodeTcMaxEntries = 1024;
+// blkattn_fwd_static_scratch keeps the tcgen05 decode kernel's per-unit
+// counters in the last kStaticCounterBytes of its array (one 32-bit counter
+// per unit), outside every plan's workspace.
+constexpr size_t kStaticCounterBytes = 256 * 1024;
+void clear_static_counters();
 cudaError_t launch_decode_tc(const FwdParams& p, int ctas, const CUtensorMap& tmk, const CUtensorMap& tmv,
                              cudaStream_t stream);
 size_t decode_tc_smem_bytes(int rows_cta);

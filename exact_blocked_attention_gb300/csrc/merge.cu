@@ -1,15 +1,13 @@
 // Merge kernels: eqs. 33.4–33.5 of "Chapter 33: inference compute
 // optimisation" §33.2, in fp32, with the valid-flag rule for empty states.
 //
-//  * split_merge_kernel: one CTA per query row folds the row's partial
-//    states (per split of the split-KV kernels, or per CTA of the tcgen05
-//    decode kernel) in a fixed order per warp and a fixed warp order
-//    (deterministic, no atomics), then finishes with o = u / l and
-//    lse = m + ln l.  Rows finished in place by the producing kernel are
-//    skipped: for the split-KV kernels the row's split count is recomputed
-//    on the device from the same integers (cache length, logical position,
-//    chunk); the tcgen05 kernel records it per unit.  No value crosses to
-//    the host.
+//  * split_merge_kernel: one CTA per query row folds the per-split partial
+//    states of the split-KV kernels (fixed order per warp, fixed warp order:
+//    deterministic, no atomics), then finishes with o = u / l and
+//    lse = m + ln l.  Rows whose visible keys lie in a single split were
+//    finished by the split kernel and are skipped here; the row's split count
+//    is recomputed on the device from the same integers (cache length,
+//    logical position, chunk), so no value crosses to the host.
 //  * state_merge_kernel: the public two-state merge (blkattn_merge).
 #include <cuda_bf16.h>
 
@@ -26,16 +24,11 @@ constexpr int kWarpsPerBlock = 8;
 
 constexpr int kMergeWarps = 4;
 
-// One CTA per query row; its warps share the row's partial states.  Pass 1
-// takes the maximum m over the non-empty states, pass 2 sums e^{m_s - m} l_s
-// and e^{m_s - m} u_s (independent terms, so the loads of many states are in
+// One CTA per query row; its warps share the row's splits.  Pass 1 takes the
+// maximum m over the non-empty splits, pass 2 sums e^{m_s - m} l_s and
+// e^{m_s - m} u_s (independent terms, so the loads of many splits are in
 // flight at once), then the warps' partial sums are added.
-//
-// Two workspace layouts: the split-KV kernels keep the states of row `row`
-// at row * n_splits + s (s < the row's active splits); the tcgen05 decode
-// kernel keeps those of unit row r at (first + s) * rows_cta + r, s < n,
-// with {first, n} per unit in unit_info.
-template <int D, bool kUnits>
+template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) split_merge_kernel(const FwdParams p) {
   constexpr int DPL = D / 32;
   // launched as a programmatic dependent of the split kernel: wait for its
@@ -47,38 +40,21 @@ __global__ void __launch_bounds__(kMergeWarps * 32) split_merge_kernel(const Fwd
   const int i = (int)(row % p.Tq);
   const int h = (int)((row / p.Tq) % p.Hq);
   const int b = (int)(row / ((int64_t)p.Tq * p.Hq));
-  int n_active;
-  int64_t base, stride;
-  if constexpr (kUnits) {
-    const int kvh = h / p.G;
-    const int pk = (h - kvh * p.G) * p.Tq + i;
-    const int rg = pk / p.rows_cta;
-    const int64_t unit = ((int64_t)b * p.Hkv + kvh) * p.row_groups + rg;
-    const int2 info = p.unit_info[unit];
-    n_active = info.y;
-    if (n_active <= 1) return;  // finished by the decode kernel
-    base = (int64_t)info.x * p.rows_cta + (pk - rg * p.rows_cta);
-    stride = p.rows_cta;
-  } else {
-    int len = p.seqlens[b * p.sl_s];
-    len = len < 0 ? 0 : (len > p.Tmax ? p.Tmax : len);
-    const int pos = p.qpos[b * p.qp_sb + i * p.qp_si];
-    const int end = pos < 0 ? 0 : (pos >= len ? len : pos + 1);
-    n_active = (end + p.chunk - 1) / p.chunk;
-    if (n_active <= 1) return;  // finished by the split kernel
-    base = row * p.n_splits;
-    stride = 1;
-  }
-
+  int len = p.seqlens[b * p.sl_s];
+  len = len < 0 ? 0 : (len > p.Tmax ? p.Tmax : len);
+  const int pos = p.qpos[b * p.qp_sb + i * p.qp_si];
+  const int end = pos < 0 ? 0 : (pos >= len ? len : pos + 1);
+  const int n_active = (end + p.chunk - 1) / p.chunk;
+  if (n_active <= 1) return;  // finished by the split kernel
   __shared__ float red_m[kMergeWarps];
   __shared__ float red_l[kMergeWarps];
   __shared__ float red_u[kMergeWarps][D];
-  const float* wm = p.ws_m + base;
-  const float* wl = p.ws_l + base;
-  const float* wu = p.ws_u + base * D;
+  const float* wm = p.ws_m + row * p.n_splits;
+  const float* wl = p.ws_l + row * p.n_splits;
+  const float* wu = p.ws_u + row * p.n_splits * D;
 
   float M = kNegInf;
-  for (int s = threadIdx.x; s < n_active; s += kMergeWarps * 32) M = fmaxf(M, wm[s * stride]);
+  for (int s = threadIdx.x; s < n_active; s += kMergeWarps * 32) M = fmaxf(M, wm[s]);
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   if (lane == 0) red_m[warp] = M;
@@ -94,11 +70,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32) split_merge_kernel(const Fwd
   if (M != kNegInf) {
 #pragma unroll 4
     for (int s = warp; s < n_active; s += kMergeWarps) {
-      const float ms = wm[s * stride];
+      const float ms = wm[s];
       if (ms == kNegInf) continue;  // an empty state contributes nothing
       const float c = fast_exp2(ms - M);
-      Ls = fmaf(c, wl[s * stride], Ls);
-      const float* us = wu + (int64_t)s * stride * D + lane * DPL;
+      Ls = fmaf(c, wl[s], Ls);
+      const float* us = wu + (int64_t)s * D + lane * DPL;
       if constexpr (DPL == 4) {
         const float4 u4 = *reinterpret_cast<const float4*>(us);
         U[0] = fmaf(c, u4.x, U[0]); U[1] = fmaf(c, u4.y, U[1]);
@@ -200,12 +176,8 @@ cudaError_t launch_split_merge(const FwdParams& p, int d, cudaStream_t stream) {
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  if (p.unit_info != nullptr) {
-    if (d == 128) return cudaLaunchKernelEx(&cfg, split_merge_kernel<128, true>, p);
-    return cudaErrorInvalidValue;
-  }
-  if (d == 128) return cudaLaunchKernelEx(&cfg, split_merge_kernel<128, false>, p);
-  if (d == 64) return cudaLaunchKernelEx(&cfg, split_merge_kernel<64, false>, p);
+  if (d == 128) return cudaLaunchKernelEx(&cfg, split_merge_kernel<128>, p);
+  if (d == 64) return cudaLaunchKernelEx(&cfg, split_merge_kernel<64>, p);
   return cudaErrorInvalidValue;
 }
 

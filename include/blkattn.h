@@ -103,8 +103,10 @@ typedef struct {
  * must be 0.  B, T_q >= 0 (0 is a no-op), T_max >= 1.
  * Returns BLKATTN_OK after enqueuing the work (asynchronous), or a negative
  * status without enqueuing anything.  Library-owned scratch (per-split
- * partial states) comes from a per-device, grow-only workspace; calls on
- * different streams of one device must not overlap in time.
+ * partial states, and per-unit counters that every call leaves at zero)
+ * comes from per-device, grow-only buffers, allocated (counters zeroed on
+ * the stream) before the first call that needs them; calls on different
+ * streams of one device must not overlap in time.
  */
 int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k,
                 const blkattn_tensor* v, const blkattn_tensor* seqlens_k,
@@ -131,14 +133,17 @@ int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k,
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress with that device current) and caches it; make
  *     that first call before any stream capture.
- *   - A problem whose split plan needs more than BLKATTN_STATIC_SCRATCH_BYTES
- *     (about rows * n_splits * (d + 2) * 4 bytes, see blkattn_debug_plan's
- *     workspace_bytes) is rejected with BLKATTN_ERR_SCRATCH_LIMIT before
- *     anything is enqueued.
- *   - Every call shares the one array and leaves its contents behind.  No
- *     part of it has to start at zero: each call writes every partial state
- *     it later reads.  Calls whose kernels overlap on the GPU (concurrent
- *     streams, several host threads) race on the array: serialise them.
+ *   - The last 256 KiB of the array hold 32-bit per-unit counters of the
+ *     tcgen05 decode kernel (one per sequence x KV head x row group); they
+ *     are zero when the library loads and every call leaves them zero.  A
+ *     problem whose plan needs more than the remaining 15.75 MiB
+ *     (blkattn_debug_plan's workspace_bytes) or more than 65536 units is
+ *     rejected with BLKATTN_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *   - Every call shares the one array and leaves its contents behind.  Apart
+ *     from the counters nothing has to start at zero: each call writes every
+ *     partial state it later reads.  Calls whose kernels overlap on the GPU
+ *     (concurrent streams, several host threads) race on the array:
+ *     serialise them.
  */
 #define BLKATTN_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
 int blkattn_fwd_static_scratch(const blkattn_tensor* q, const blkattn_tensor* k,
@@ -184,7 +189,9 @@ const char* blkattn_status_string(int status);
 /*
  * Test hook: synchronises the stream, then reads and clears the library's
  * device error word.  Returns BLKATTN_OK, BLKATTN_ERR_DEVICE_TIMEOUT when a
- * kernel gave up a bounded wait, or BLKATTN_ERR_CUDA if the sync failed.
+ * kernel gave up a bounded wait (the per-unit counters of the current device
+ * are then reset to zero, since the kernel that gave up may have left some
+ * behind), or BLKATTN_ERR_CUDA if the sync failed.
  */
 int blkattn_check_device_error(blkattn_stream_t stream);
 

@@ -522,3 +522,16 @@ def test_split_mma_kernel_cases(force_split_mma, case):
     assert plan_of(inp)["kernel"] == 1
     raw, _, o, l = run_gpu(inp)
     assert_parity(o, l, run_oracle(inp), BF16_TOL_O, BF16_TOL_L, out_raw=raw)
+
+
+def test_tc_decode_counters_are_left_clean_between_shapes():
+    """Units spanning several CTAs are folded by the last CTA to arrive (a
+    per-unit counter that every launch must leave at zero): interleaved shapes
+    with different unit counts give the same results as when run alone."""
+    cases = [tc_case("units_over_many_ctas"), tc_case("rows32"), tc_case("many_units")]
+    first = [run_gpu(c)[2:] for c in cases]
+    for _ in range(2):
+        for c, (o0, l0) in zip(reversed(cases), reversed(first)):
+            _, _, o, l = run_gpu(c)
+            np.testing.assert_array_equal(o, o0)
+            np.testing.assert_array_equal(l, l0)
