@@ -206,6 +206,10 @@ class Runner:
                                        torch.cuda.get_device_properties(0).multi_processor_count)
 
     def launches_per_call(self):
+        # the tcgen05 decode kernel (kernel 3) folds its split units itself;
+        # the split-KV kernels are followed by the merge kernel when split
+        if self.plan["kernel"] == 3:
+            return 1
         return 1 + (1 if self.plan["n_splits"] > 1 else 0)
 
     def call(self):
