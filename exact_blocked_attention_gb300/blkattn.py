@@ -30,7 +30,7 @@ _DTYPES = {torch.bfloat16: BF16, torch.float32: F32, torch.int32: I32}
 
 EXPORTED = ("blkattn_fwd", "blkattn_merge", "blkattn_status_string",
             "blkattn_check_device_error", "blkattn_debug_plan", "blkattn_debug_set_split_event",
-            "blkattn_fwd_static_scratch")
+            "blkattn_fwd_static_scratch", "blkattn_last_cuda_error")
 
 
 class Tensor(ctypes.Structure):
@@ -86,6 +86,8 @@ def load(path: str = LIB_PATH):
             lib.blkattn_debug_plan.argtypes = [ctypes.c_int64] * 6 + [ctypes.c_int32, ctypes.c_int32, P]
             lib.blkattn_debug_set_split_event.restype = None
             lib.blkattn_debug_set_split_event.argtypes = [P]
+            lib.blkattn_last_cuda_error.restype = ctypes.c_char_p
+            lib.blkattn_last_cuda_error.argtypes = []
             _lib = lib
     return _lib
 
@@ -100,6 +102,8 @@ def _check(status: int):
     text = status_string(status)
     if status == ERR_INVALID_ARG:
         raise ValueError(f"blkattn: {text}")
+    if status == ERR_CUDA:
+        text += f" ({load().blkattn_last_cuda_error().decode()})"
     raise BlkattnError(status, text)
 
 

@@ -41,6 +41,13 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 cudaEvent_t g_split_event = nullptr;  // measurement hook (blkattn_debug_set_split_event)
 
+// The CUDA error behind the last BLKATTN_ERR_CUDA (blkattn_last_cuda_error).
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = e;
+  return BLKATTN_ERR_CUDA;
+}
+
 // ------------------------------------------------------------ validation
 bool is_float_dtype(int32_t t) { return t == BLKATTN_BF16 || t == BLKATTN_F32; }
 int elt_bytes(int32_t t) { return t == BLKATTN_BF16 ? 2 : 4; }
@@ -104,7 +111,7 @@ Plan make_plan(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tmax, int
         B * rg <= blkattn::kDecodeTcMaxEntries && Tmax <= 65535LL * 128) {
       const int64_t P = sms > 0 ? sms : 148;
       const int64_t U = B * Hkv * rg;
-      const int64_t slots = P + U;
+      const int64_t slots = P + U;  // partial-state slots: CTA index + unit index
       pl.cfg.kernel = blkattn::Kernel::DecodeTc;
       pl.cfg.rows_per_cta = (int)R;
       pl.cfg.row_groups = (int)rg;
@@ -116,7 +123,7 @@ Plan make_plan(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tmax, int
       pl.ctas = P;
       auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
       pl.ws_bytes = 2 * al(slots * R * 4) + al(slots * R * d * 4);
-      pl.units = U;
+      pl.units = U;  // per-unit arrival counters
       return pl;
     }
   }
@@ -172,14 +179,14 @@ Plan make_plan(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tmax, int
 
 int device_state(DeviceState** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return BLKATTN_ERR_CUDA;
+  if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return cuda_fail(e);
   if (dev < 0 || dev >= kMaxDevices) return BLKATTN_ERR_UNSUPPORTED;
   DeviceState& s = g_dev[dev];
   if (!s.ready) {
-    if (cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return BLKATTN_ERR_CUDA;
-    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&s.err), g_error_word) != cudaSuccess)
-      return BLKATTN_ERR_CUDA;
+    if (cudaError_t e = cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev); e != cudaSuccess)
+      return cuda_fail(e);
+    if (cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&s.err), g_error_word); e != cudaSuccess)
+      return cuda_fail(e);
     s.ready = true;
   }
   *out = &s;
@@ -193,10 +200,9 @@ int get_encoder() {
   if (g_encode) return BLKATTN_OK;
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
-  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-          cudaSuccess ||
-      q != cudaDriverEntryPointSuccess || fn == nullptr)
-    return BLKATTN_ERR_CUDA;
+  if (cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return cuda_fail(e != cudaSuccess ? e : cudaErrorNotSupported);
   g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   return BLKATTN_OK;
 }
@@ -252,7 +258,7 @@ int kv_tensor_map(int dev, const blkattn_tensor* t, int box_rows, const CUtensor
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     e.used = false;
-    return BLKATTN_ERR_CUDA;
+    return cuda_fail(cudaErrorInvalidValue);  // the tensor map was refused
   }
   e.key = key;
   e.used = true;
@@ -265,16 +271,16 @@ int kv_tensor_map(int dev, const blkattn_tensor* t, int box_rows, const CUtensor
 int ensure_workspace(DeviceState* s, size_t bytes, cudaStream_t stream) {
   if (bytes <= s->ws_bytes) return BLKATTN_OK;
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return BLKATTN_ERR_CUDA;
+  if (cudaError_t e = cudaStreamIsCapturing(stream, &cs); e != cudaSuccess) return cuda_fail(e);
   if (cs != cudaStreamCaptureStatusNone) return BLKATTN_ERR_NO_WORKSPACE;
   if (s->ws) {
-    if (cudaFree(s->ws) != cudaSuccess) return BLKATTN_ERR_CUDA;  // waits for users of the old one
+    if (cudaError_t e = cudaFree(s->ws); e != cudaSuccess) return cuda_fail(e);  // waits for users of the old one
     s->ws = nullptr;
     s->ws_bytes = 0;
   }
-  if (cudaMalloc(&s->ws, bytes) != cudaSuccess) {
+  if (cudaError_t e = cudaMalloc(&s->ws, bytes); e != cudaSuccess) {
     s->ws = nullptr;
-    return BLKATTN_ERR_CUDA;
+    return cuda_fail(e);
   }
   s->ws_bytes = bytes;
   return BLKATTN_OK;
@@ -286,18 +292,18 @@ int ensure_workspace(DeviceState* s, size_t bytes, cudaStream_t stream) {
 int ensure_counters(DeviceState* s, int64_t n, cudaStream_t stream) {
   if ((size_t)n <= s->cnt_n) return BLKATTN_OK;
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return BLKATTN_ERR_CUDA;
+  if (cudaError_t e = cudaStreamIsCapturing(stream, &cs); e != cudaSuccess) return cuda_fail(e);
   if (cs != cudaStreamCaptureStatusNone) return BLKATTN_ERR_NO_WORKSPACE;
   if (s->cnt) {
-    if (cudaFree(s->cnt) != cudaSuccess) return BLKATTN_ERR_CUDA;
+    if (cudaError_t e = cudaFree(s->cnt); e != cudaSuccess) return cuda_fail(e);
     s->cnt = nullptr;
     s->cnt_n = 0;
   }
-  if (cudaMalloc(&s->cnt, (size_t)n * sizeof(unsigned)) != cudaSuccess) {
+  if (cudaError_t e = cudaMalloc(&s->cnt, (size_t)n * sizeof(unsigned)); e != cudaSuccess) {
     s->cnt = nullptr;
-    return BLKATTN_ERR_CUDA;
+    return cuda_fail(e);
   }
-  if (cudaMemsetAsync(s->cnt, 0, (size_t)n * sizeof(unsigned), stream) != cudaSuccess) return BLKATTN_ERR_CUDA;
+  if (cudaError_t e = cudaMemsetAsync(s->cnt, 0, (size_t)n * sizeof(unsigned), stream); e != cudaSuccess) return cuda_fail(e);
   s->cnt_n = (size_t)n;
   return BLKATTN_OK;
 }
@@ -454,7 +460,7 @@ int launch_fwd(const FwdParams& p, const Checked& c, const Plan& pl, const blkat
   cudaError_t le;
   if (pl.cfg.kernel == blkattn::Kernel::DecodeTc) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return BLKATTN_ERR_CUDA;
+    if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return cuda_fail(e);
     const CUtensorMap* mk = nullptr;
     const CUtensorMap* mv = nullptr;
     int st = kv_tensor_map(dev, k, 128, &mk);
@@ -464,7 +470,7 @@ int launch_fwd(const FwdParams& p, const Checked& c, const Plan& pl, const blkat
     le = blkattn::launch_decode_tc(p, (int)pl.ctas, *mk, *mv, stream);
   } else if (pl.cfg.kernel == blkattn::Kernel::TensorCore || pl.cfg.kernel == blkattn::Kernel::Prefill) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return BLKATTN_ERR_CUDA;
+    if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return cuda_fail(e);
     const CUtensorMap* mk = nullptr;
     const CUtensorMap* mv = nullptr;
     // K/V boxes: 64 keys for the split-KV kernel, 128 for the prefill kernel
@@ -484,13 +490,12 @@ int launch_fwd(const FwdParams& p, const Checked& c, const Plan& pl, const blkat
   } else {
     le = blkattn::launch_decode_split(p, c.elt, (int)c.d, pl.cfg, stream);
   }
-  if (le != cudaSuccess) return BLKATTN_ERR_CUDA;
-  if (g_split_event != nullptr && cudaEventRecord(g_split_event, stream) != cudaSuccess)
-    return BLKATTN_ERR_CUDA;
+  if (le != cudaSuccess) return cuda_fail(le);
+  if (g_split_event != nullptr)
+    if (cudaError_t e = cudaEventRecord(g_split_event, stream); e != cudaSuccess) return cuda_fail(e);
   // the tcgen05 decode kernel folds its split units itself
-  if (pl.cfg.kernel != blkattn::Kernel::DecodeTc && pl.cfg.n_splits > 1 &&
-      blkattn::launch_split_merge(p, (int)c.d, stream) != cudaSuccess)
-    return BLKATTN_ERR_CUDA;
+  if (pl.cfg.kernel != blkattn::Kernel::DecodeTc && pl.cfg.n_splits > 1)
+    if (cudaError_t e = blkattn::launch_split_merge(p, (int)c.d, stream); e != cudaSuccess) return cuda_fail(e);
   return BLKATTN_OK;
 }
 
@@ -624,7 +629,7 @@ int blkattn_merge(const blkattn_states* a, const blkattn_states* b, const blkatt
   p.rows = a->rows;
   p.d = a->d_v;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  if (blkattn::launch_state_merge(p, stream) != cudaSuccess) return BLKATTN_ERR_CUDA;
+  if (cudaError_t e = blkattn::launch_state_merge(p, stream); e != cudaSuccess) return cuda_fail(e);
   return BLKATTN_OK;
 }
 
@@ -633,20 +638,25 @@ void blkattn_debug_set_split_event(void* ev) {
   g_split_event = static_cast<cudaEvent_t>(ev);
 }
 
+const char* blkattn_last_cuda_error(void) {
+  return g_last_cuda_error == cudaSuccess ? "no CUDA error recorded" : cudaGetErrorString(g_last_cuda_error);
+}
+
 int blkattn_check_device_error(blkattn_stream_t stream_) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return BLKATTN_ERR_CUDA;
+  if (cudaError_t e = cudaStreamSynchronize(stream); e != cudaSuccess) return cuda_fail(e);
   int word = 0;
-  if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof word) != cudaSuccess) return BLKATTN_ERR_CUDA;
+  if (cudaError_t e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof word); e != cudaSuccess) return cuda_fail(e);
   if (word != 0) {
     const int zero = 0;
-    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof zero) != cudaSuccess) return BLKATTN_ERR_CUDA;
+    if (cudaError_t e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof zero); e != cudaSuccess) return cuda_fail(e);
     // a kernel that gave up may have left unit counters behind: restart them
     int dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
       std::lock_guard<std::mutex> lock(g_mu);
       DeviceState& ds = g_dev[dev];
-      if (ds.cnt && cudaMemset(ds.cnt, 0, ds.cnt_n * sizeof(unsigned)) != cudaSuccess) return BLKATTN_ERR_CUDA;
+      if (ds.cnt)
+        if (cudaError_t e = cudaMemset(ds.cnt, 0, ds.cnt_n * sizeof(unsigned)); e != cudaSuccess) return cuda_fail(e);
     }
     blkattn::clear_static_counters();
     return BLKATTN_ERR_DEVICE_TIMEOUT;

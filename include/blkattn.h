@@ -187,6 +187,12 @@ int blkattn_merge(const blkattn_states* a, const blkattn_states* b,
 const char* blkattn_status_string(int status);
 
 /*
+ * The CUDA runtime's text for the error behind the calling thread's last
+ * BLKATTN_ERR_CUDA (static storage; "no CUDA error recorded" before any).
+ */
+const char* blkattn_last_cuda_error(void);
+
+/*
  * Test hook: synchronises the stream, then reads and clears the library's
  * device error word.  Returns BLKATTN_OK, BLKATTN_ERR_DEVICE_TIMEOUT when a
  * kernel gave up a bounded wait (the per-unit counters of the current device

@@ -467,6 +467,14 @@ def tc_case(name):
         ramp = torch.linspace(0.2, 3.0, 8192)[None, None, :, None]
         inp["k"] = (inp["k"].float() * ramp).to(torch.bfloat16)
         return inp
+    if name == "many_tiles_long":
+        # more than 32 key tiles per CTA over a few long units
+        return make_case(2, 8, 8, 1, 40000, 128, "bf16", [40000, 39001], [[39999], [39000]], seed=8)
+    if name == "many_tiles_many_units":
+        B = 600
+        lens = rng.integers(1000, 1200, B)
+        pos = (lens - 1)[:, None]
+        return make_case(B, 4, 1, 1, 1200, 128, "bf16", lens.tolist(), pos.tolist(), seed=9)
     if name == "late_first_key":
         B, Hq, Hkv, Tq, Tmax = 2, 8, 2, 3, 2000
         bias = torch.zeros(B, 1, Tq, Tmax)
@@ -479,7 +487,7 @@ def tc_case(name):
 
 
 TC_CASES = ["fewer_tiles_than_ctas", "many_units", "units_over_many_ctas", "two_row_groups", "rows32",
-            "rising_scores", "late_first_key"]
+            "rising_scores", "late_first_key", "many_tiles_long", "many_tiles_many_units"]
 
 
 @pytest.mark.parametrize("case", TC_CASES)
@@ -528,7 +536,8 @@ def test_tc_decode_counters_are_left_clean_between_shapes():
     """Units spanning several CTAs are folded by the last CTA to arrive (a
     per-unit counter that every launch must leave at zero): interleaved shapes
     with different unit counts give the same results as when run alone."""
-    cases = [tc_case("units_over_many_ctas"), tc_case("rows32"), tc_case("many_units")]
+    cases = [tc_case("units_over_many_ctas"), tc_case("rows32"), tc_case("many_tiles_many_units"),
+             tc_case("many_units"), tc_case("many_tiles_long")]
     first = [run_gpu(c)[2:] for c in cases]
     for _ in range(2):
         for c, (o0, l0) in zip(reversed(cases), reversed(first)):
