@@ -420,6 +420,7 @@ def main():
     clocks = clk.summary()
     step_ms = max_over_ranks(sum(total) / len(total), world)
     main_avg = max_over_ranks(sum(main_ms) / len(main_ms), world)
+    spread = {"min": min(total), "median": sorted(total)[len(total) // 2], "max": max(total)}
     value = kv * world / (step_ms * 1e-3) / 1e9
     if s.name == "prefill":
         value = causal_flops(s, r.cpu) * world / (step_ms * 1e-3) / 1e12
@@ -445,6 +446,7 @@ def main():
                    "plan": plan, "parallelism": f"weak: {world} rank(s), own batch each",
                    "enqueue": "timed steps queued behind a 5 ms device sleep (host launch gaps untimed)"},
         "us_per_call": step_ms * 1e3,
+        "step_ms_spread": spread,
         "main_kernel_us": main_avg * 1e3,
         "frac_of_hbm_peak": (total_bytes / (step_ms * 1e-3) / 1e9) / peaks["hbm_gbs"],
         "roofline": roof,

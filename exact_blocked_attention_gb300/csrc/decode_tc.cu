@@ -203,6 +203,38 @@ __device__ __forceinline__ void st_cols(uint32_t taddr, const float (&x)[N]) {
   }
 }
 
+// Reduce NH values per lane across the 32 lanes of a warp (NH = 8, 16, 24):
+// three reduce-scatter steps (xor 16, 8, 4) halve the values a lane keeps,
+// two full steps (xor 2, 1) finish them.  Afterwards lane l holds the
+// results for rows base + i, i < NH / 8, base = (l >> 4 & 1) NH / 2 +
+// (l >> 3 & 1) NH / 4 + (l >> 2 & 1) NH / 8, in v[0 .. NH / 8).  The
+// shuffles of one step are independent (27 in all for NH = 24).
+template <int NH, bool kMax>
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[NH], int lane) {
+  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+#pragma unroll
+  for (int step = 0; step < 3; ++step) {
+    const int off = 16 >> step;
+    const int half = NH >> (step + 1);  // values kept after this step
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, off));
+    }
+  }
+#pragma unroll
+  for (int off = 2; off >= 1; off >>= 1)
+#pragma unroll
+    for (int i = 0; i < NH / 8; ++i) v[i] = op(v[i], __shfl_xor_sync(0xffffffffu, v[i], off));
+}
+
+template <int NH>
+__device__ __forceinline__ int scatter_base(int lane) {
+  return ((lane >> 4) & 1) * (NH / 2) + ((lane >> 3) & 1) * (NH / 4) + ((lane >> 2) & 1) * (NH / 8);
+}
+
 template <int NR>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmk,
@@ -804,12 +836,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (bar_or(kBarRows, kKeyThreads, trig)) {
         if (misc[2] != 0) { ok = false; break; }  // read after the barrier: same answer everywhere
         // ---- raise the reference maxima: tile maxima over the 128 keys ----
+        {
+          float v[NH];
 #pragma unroll
-        for (int r = 0; r < NH; ++r) {
-          float v = x[r];
+          for (int r = 0; r < NH; ++r) v[r] = x[r];
+          warp_reduce_scatter<NH, true>(v, lane);
+          if ((lane & 3) == 0) {
+            const int base = scatter_base<NH>(lane);
 #pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-          if (lane == (r & 31)) red[quarter * NR + c0 + r] = v;
+            for (int i = 0; i < NH / 8; ++i) red[quarter * NR + c0 + base + i] = v[i];
+          }
         }
         bar_sync(kBarRows, kKeyThreads);
         if (half == 0 && k < NR) {
@@ -904,14 +940,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (last) {
         // ---- close the unit (or this CTA's part of it): l over the keys ----
+        warp_reduce_scatter<NH, false>(lp, lane);
+        if ((lane & 3) == 0) {
+          const int base = scatter_base<NH>(lane);
 #pragma unroll
-        for (int r = 0; r < NH; ++r) {
-          float v = lp[r];
-#pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-          if (lane == (r & 31)) red[quarter * NR + c0 + r] = v;
-          lp[r] = 0.f;
+          for (int i = 0; i < NH / 8; ++i) red[quarter * NR + c0 + base + i] = lp[i];
         }
+#pragma unroll
+        for (int r = 0; r < NH; ++r) lp[r] = 0.f;
         bar_sync(kBarRows, kKeyThreads);
         if (half == 0 && k < NR) {
           const float l = (red[k] + red[NR + k]) + (red[2 * NR + k] + red[3 * NR + k]);
