@@ -9,15 +9,16 @@
 //
 //   S^T_j  = K_j Q^T       M = 128 keys, N = NR rows, K = 16 x 8
 //                          (A = K tile, B = Q rows; both K-major in smem)
-//   U^T   += V_j^T P_j^T   M = 128 value dims, N = 64 + NR, K = 16 x 8
+//   U^T   += V_j^T P_j^T   M = 128 value dims, N = 2 NR or 64 + NR, K = 16 x 8
 //                          (A = the V tile read MN-major, B = P^T in smem)
 //
 // so a tile of 128 keys costs 16 MMAs whatever the row count.  P is not an
-// input: each P^T row is written as bf16 P_hi (columns [0, NR) of the first
-// 64-column atom) and P_lo = bf16(P - P_hi) (the same columns of a second
-// atom), P_hi the truncated upper half of P; one product with N = 64 + NR
-// gives U_hi and U_lo side by side and U = U_hi + U_lo keeps ~2^-17 relative
-// accuracy of P while V stays bf16 and is read once.
+// input: each P^T row is written as bf16 P_hi (columns [0, NR)) and
+// P_lo = bf16(P - P_hi) (columns [NR, 2 NR) of the same 64-column atom for up
+// to 32 rows, else the same columns of a second atom), P_hi the truncated
+// upper half of P; one product gives U_hi and U_lo side by side and
+// U = U_hi + U_lo keeps ~2^-17 relative accuracy of P while V stays bf16 and
+// is read once.
 //
 // Work split: the key tiles of all units, in the order (sequence, KV head,
 // row group, tile), are cut into P = min(gridDim.x, tiles) equal contiguous
@@ -38,7 +39,7 @@
 //    bias with -inf = masked), and writes its part of the P^T row; per unit
 //    it then owns value dim k of its rows for the epilogue.
 //  * warp 8: producer: K and V tiles of 128 keys x 128 dims by tiled TMA
-//    into a ring of 4 slots of 32 KB (K_j and V_j alternate).
+//    into a ring of 5 slots of 32 KB (4 with 48 rows; K_j and V_j alternate).
 //  * warp 10: unit loader: per unit, the query rows (16-byte loads into the
 //    128-byte swizzled K-major layout) and the rows' integer facts, into one
 //    of two buffers, ahead of the unit's first product.
@@ -81,7 +82,6 @@ constexpr float kLazyRescale = 8.f;
 
 constexpr int BK = 128;               // keys per tile (TMEM lanes of S^T)
 constexpr int D = 128;                // head dim (TMEM lanes of U^T)
-constexpr int kSlots = 4;             // ring slots of one K or V tile
 constexpr int kBox = BK * 128;        // 128 rows x 64 dims, bf16: 16 KB
 constexpr int kSlotBytes = 2 * kBox;  // 128 rows x 128 dims
 constexpr int kKeyWarps = 8;   // two warps per TMEM lane quarter, each with half of the rows
@@ -94,8 +94,7 @@ constexpr int kBarRows = 1;  // named barrier of the key threads
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // S^T of tiles with even / odd index: +0 / +64
 constexpr uint32_t kColU = 128;  // U^T of units with even / odd index: +0 / +128;
-                                 // the P_hi part in columns [0, NR), P_lo in [64, 64 + NR)
-constexpr int kPBytes = 2 * kBox;  // one P^T buffer: P_hi box, then P_lo box
+                                 // the P_hi part in columns [0, NR), P_lo from column kLo
 
 // Integer facts of the rows of one unit (written by the producer).
 template <int NR>
@@ -111,6 +110,14 @@ struct RowFacts {
 
 template <int NR>
 struct TcLayout {
+  // Up to 32 rows, P_hi and P_lo share one 64-column atom (P_lo from column
+  // NR, the product's N = 2 NR), which leaves room for a fifth ring slot;
+  // 48 rows take two atoms (P_lo from column 64, N = 64 + NR) and four slots.
+  static constexpr bool kPacked = NR <= 32;
+  static constexpr int kSlots = kPacked ? 5 : 4;
+  static constexpr int kLo = kPacked ? NR : 64;          // column of P_lo / U_lo
+  static constexpr int kPVN = kPacked ? 2 * NR : 64 + NR;  // N of the PV product
+  static constexpr int kPBytes = kPacked ? kBox : 2 * kBox;  // one P^T buffer
   static constexpr int kQBox = NR * 128;  // NR rows x 64 dims
   static constexpr int kQBytes = 2 * kQBox;
   static constexpr int kOffRing = 0;
@@ -242,7 +249,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = TcLayout<NR>;
   constexpr uint32_t kIdescQK = tc::idesc_bf16(128, NR, 0, 0);  // K, Q both K-major
   // V^T, P^T both MN-major; N spans the P_hi atom (NR used of 64) and the P_lo atom
-  constexpr uint32_t kIdescPV = tc::idesc_bf16(128, 64 + NR, 1, 1);
+  constexpr uint32_t kIdescPV = tc::idesc_bf16(128, L::kPVN, 1, 1);
+  constexpr int kSlots = L::kSlots;
+  constexpr int kPBytes = L::kPBytes;
+  constexpr uint32_t kLo = L::kLo;
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -605,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ks = 0; ks < BK / 16; ++ks) {
           // A = V^T: 128 dims (two 64-dim boxes 16 KB apart) x keys [16 ks, 16 ks + 16)
           const uint64_t adesc = tc::smem_desc(vb + ks * 2048, kBox, 1024);
-          // B = P^T: keys [16 ks, +16) x (P_hi atom, P_lo atom 16 KB further)
+          // B = P^T: keys [16 ks, +16) x [P_hi | P_lo] (one atom, or two 16 KB apart)
           const uint64_t bdesc = tc::smem_desc(pb + ks * 2048, kBox, 1024);
           tc::mma_ss(ucol, adesc, bdesc, kIdescPV, (!first || ks > 0) ? 1u : 0u);
         }
@@ -663,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float ulo[NH];
         const uint32_t ua = tl + kColU + 128u * (uint32_t)pb + c0;
         ld_cols<NH>(ua, u);
-        ld_cols<NH>(ua + 64u, ulo);
+        ld_cols<NH>(ua + kLo, ulo);
 #pragma unroll
         for (int r = 0; r < NH; ++r) u[r] += ulo[r];  // U = P_hi V + P_lo V
       }
@@ -880,10 +890,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
           for (int part = 0; part < 2; ++part) {
             float u[NH];
-            ld_cols<NH>(ua + 64u * part, u);
+            ld_cols<NH>(ua + kLo * part, u);
 #pragma unroll
             for (int r = 0; r < NH; ++r) u[r] *= s_alpha[c0 + r];
-            st_cols<NH>(ua + 64u * part, u);
+            st_cols<NH>(ua + kLo * part, u);
           }
           resc = true;
         }
@@ -909,9 +919,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float rb = pb - __uint_as_float(__float_as_uint(pb) & 0xffff0000u);
             lo[e2] = pack_bf16(ra, rb);
           }
-          const int off = (((c0 / 8 + c8) ^ (k & 7)) << 4);
+          const int c = c0 / 8 + c8;  // 16-byte chunk of the row's P_hi
+          const int off = ((c ^ (k & 7)) << 4);
+          const int off_lo = L::kPacked ? (((c + NR / 8) ^ (k & 7)) << 4) : kBox + off;
           *reinterpret_cast<uint4*>(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(ph + kBox + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          *reinterpret_cast<uint4*>(ph + off_lo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
       if (cur.j == cur.n - 1 && key0 + BK > rf.unit_end) {
