@@ -810,16 +810,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int key = key0 + k;
       float x[NH];
       if (has_bias) {
-        // this tile's bias (prefetched into L1 one tile ahead), then the
-        // next tile's of the same unit into L1
+        // this tile's bias (rows of one sequence share lines: L1 hits); a
+        // per-row prefetch of the next tile measured slower (memory-pipe
+        // instructions, not bytes, are the cost here)
         const bool kin = key < p.Tmax;
-        const bool kin2 = cur.j + 1 < cur.n && key + BK < p.Tmax;
 #pragma unroll
-        for (int r = 0; r < NH; ++r) {
-          const float* bp = p.bias + rf.boff[c0 + r] + (int64_t)key * p.bi_sj;
-          x[r] = kin ? __ldg(bp) : 0.f;
-          if (kin2) asm volatile("prefetch.global.L1 [%0];" ::"l"(bp + (int64_t)BK * p.bi_sj));
-        }
+        for (int r = 0; r < NH; ++r)
+          x[r] = kin ? __ldg(p.bias + rf.boff[c0 + r] + (int64_t)key * p.bi_sj) : 0.f;
       }
       const bool sok = wait_all(&s_full[g & 1], (uint32_t)((g >> 1) & 1));
       bool trig = !sok;
