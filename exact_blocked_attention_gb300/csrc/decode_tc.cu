@@ -177,8 +177,12 @@ struct Cursor {
 };
 
 // CTA whose range [c W / P, (c + 1) W / P) holds global tile t.
+// (32-bit arithmetic: the host keeps the tile count below 2^24 and
+// P <= 255, so (t + 1) P < 2^32; a 64-bit division is a long software
+// sequence on the GPU.)
 __device__ __forceinline__ int64_t cta_of(int64_t t, int64_t W, int64_t P) {
-  return ((t + 1) * P + W - 1) / W - 1;
+  const uint32_t w = (uint32_t)W;
+  return (int64_t)((((uint32_t)t + 1u) * (uint32_t)P + w - 1u) / w) - 1;
 }
 
 // N consecutive TMEM columns of this thread's lane (N = 8, 16 or 24; the
@@ -371,8 +375,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // working CTA has a tile and the CTAs holding one unit are consecutive
       const long long P = W < (long long)gridDim.x ? W : (long long)gridDim.x;
       const bool works = (long long)blockIdx.x < P;
-      const long long t0 = works ? (long long)blockIdx.x * W / P : W;
-      const long long t1 = works ? ((long long)blockIdx.x + 1) * W / P : W;
+      // c W / P in 32 bits: W = q P + r, c W / P = c q + c r / P (c r < 2^16)
+      const uint32_t q = (uint32_t)W / (uint32_t)(P > 0 ? P : 1), r = (uint32_t)W - q * (uint32_t)P;
+      const uint32_t c = blockIdx.x;
+      const long long t0 = works ? (long long)(c * q + c * r / (uint32_t)P) : W;
+      const long long t1 = works ? (long long)((c + 1) * q + (c + 1) * r / (uint32_t)P) : W;
       const long long excl = incl - s;
       const unsigned own = __ballot_sync(0xffffffffu, t0 < t1 && excl <= t0 && t0 < incl);
       if (lane == 0) {
@@ -389,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++b;
         }
         const long long o = t0 - pre;
-        const int kvh = (int)(o / nb[b]);
+        const int kvh = (int)((uint32_t)o / (uint32_t)nb[b]);
         long long o2 = o - (long long)kvh * nb[b];
         long long su = pre + (long long)kvh * nb[b];
         int rg = 0;
