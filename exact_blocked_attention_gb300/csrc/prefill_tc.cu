@@ -335,13 +335,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 128; ++c) xs[c] = (key0 + c < my_end) ? xs[c] : kNegInf;
         }
         // block maximum on the raw scores (scale > 0), a tree of short chains
+        // (three-input max: 8 chains of 8 steps over 16 values each)
         float mx8[8];
 #pragma unroll
         for (int c = 0; c < 8; ++c) mx8[c] = xs[c];
 #pragma unroll
-        for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], xs[c]);
-        const float mraw = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int c = 8; c < 128; c += 2) mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], xs[c], xs[c + 1]);
+        const float mraw = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
         const float mt = (mraw == kNegInf) ? kNegInf : mraw * p.scale_log2;
         float alpha = 1.f;
         bool resc = false;
