@@ -109,7 +109,7 @@ Plan make_plan(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tmax, int
     const int64_t R = (rows + rg - 1) / rg;
     // (the kernel's schedule uses 32-bit arithmetic: fewer than 2^24 key
     // tiles in all, at most 255 CTAs)
-    const int64_t max_tiles = B * Hkv * rg * ((Tmax + 127) / 128);
+    const int64_t max_tiles = B * Hkv * rg * ((Tmax + 127) / 128 + 2);  // + the per-unit weight
     if (q_vec_ok && elt == Elt::BF16 && d == 128 && !force_mma && !force_cudacore && rows >= 1 &&
         B * rg <= blkattn::kDecodeTcMaxEntries && Tmax <= 65535LL * 128 && max_tiles < (1LL << 24) &&
         (sms > 0 ? sms : 148) <= 255) {

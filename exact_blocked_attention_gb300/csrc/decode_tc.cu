@@ -148,13 +148,16 @@ struct Start {
 };
 
 // Position in the tile order: global tile t of unit (b, kvh, rg), local tile
-// j of n, the unit's first global tile su.
+// j of n, the unit's first global tile su.  Each unit spans n real tiles and
+// `extra` weight-only tiles after them (the partition charges a unit for its
+// set-up and readout, so CTAs holding many short units get fewer tiles).
 struct Cursor {
   int64_t t, su;
   int b, kvh, rg, j, n;
+  int extra;
   // to the first tile of the next unit
   __device__ __forceinline__ void step_unit(const uint16_t* ntab, int RG, int Hkv, int B) {
-    su += n;
+    su += n + extra;
     t = su;
     j = 0;
     if (++rg == RG) {
@@ -255,6 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // V^T, P^T both MN-major; N spans the P_hi atom (NR used of 64) and the P_lo atom
   constexpr uint32_t kIdescPV = tc::idesc_bf16(128, L::kPVN, 1, 1);
   constexpr int kSlots = L::kSlots;
+  // weight-only tiles per unit in the partition (its set-up and readout)
+  constexpr int kUnitExtra = NR >= 48 ? 2 : 1;
   constexpr int kPBytes = L::kPBytes;
   constexpr uint32_t kLo = L::kLo;
 
@@ -353,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     for (int b = threadIdx.x; b < B; b += kThreads) {
       int s = 0;
-      for (int rg = 0; rg < RG; ++rg) s += ntab[b * RG + rg];
+      for (int rg = 0; rg < RG; ++rg) s += ntab[b * RG + rg] + kUnitExtra;
       nb[b] = s;
     }
     __syncthreads();
@@ -400,9 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         long long o2 = o - (long long)kvh * nb[b];
         long long su = pre + (long long)kvh * nb[b];
         int rg = 0;
-        while (o2 >= ntab[b * RG + rg]) {
-          o2 -= ntab[b * RG + rg];
-          su += ntab[b * RG + rg];
+        while (o2 >= ntab[b * RG + rg] + kUnitExtra) {
+          o2 -= ntab[b * RG + rg] + kUnitExtra;
+          su += ntab[b * RG + rg] + kUnitExtra;
           ++rg;
         }
         start->b = b;
@@ -432,6 +437,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   cur.rg = start->rg;
   cur.j = start->j;
   cur.n = (t0 < t1) ? (int)ntab[cur.b * RG + cur.rg] : 1;
+  cur.extra = kUnitExtra;
+  // a range may start among a unit's weight-only tiles: begin at the next unit
+  if (t0 < t1 && cur.j >= cur.n) cur.step_unit(ntab, RG, Hkv, B);
 
   if (warp == kTmaWarp) {
     // ---------------- producer: K and V tiles ----------------
@@ -441,8 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
       int64_t issued = 0;
       bool ok = true;
-      for (; ok && cur.t < t1; cur.next(ntab, RG, Hkv, B)) {
-        const int64_t g = cur.t - t0;
+      // g counts this CTA's tiles (positions skip the weight-only tiles)
+      for (int64_t g = 0; ok && cur.t < t1; cur.next(ntab, RG, Hkv, B), ++g) {
 #pragma unroll
         for (int kv = 0; kv < 2; ++kv) {
           const int64_t seq = 2 * g + kv;
@@ -576,7 +584,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Order S_0, S_1, U += P_0 V_0, S_2, U += P_1 V_1, ...: the products of
     // the next tile's scores run while the key threads work on this tile.
     if (lane == 0) {
-      const int64_t n_t = t1 - t0;
       Cursor cq = cur;  // tile of the next S product
       int uq = 0, up = 0;  // unit counters of the S and the U sides
       auto issue_qk = [&](int64_t gq) -> bool {
@@ -605,11 +612,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         cq.next(ntab, RG, Hkv, B);
         return true;
       };
-      bool ok = n_t == 0 || issue_qk(0);
-      for (int64_t g = 0; ok && g < n_t; cur.next(ntab, RG, Hkv, B), ++g) {
+      bool ok = !(cq.t < t1) || issue_qk(0);
+      for (int64_t g = 0; ok && cur.t < t1; cur.next(ntab, RG, Hkv, B), ++g) {
         const bool first = cur.t == t0 || cur.j == 0;
         const bool last = cur.t == t1 - 1 || cur.j == cur.n - 1;
-        if (g + 1 < n_t && !issue_qk(g + 1)) { ok = false; break; }
+        if (cq.t < t1 && !issue_qk(g + 1)) { ok = false; break; }
         // U^T += V_j^T [P_hi | P_lo]^T once the key threads wrote P^T
         const int64_t sv = 2 * g + 1;
         if (!mbar_wait(&p_full[g & 1], (uint32_t)((g >> 1) & 1))) { ok = false; break; }
@@ -802,11 +809,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (threadIdx.x == 0) mbar_arrive(&q_empty[pb]);
       return true;
     };
-    for (; cur.t < t1; cur.next(ntab, RG, Hkv, B)) {
+    for (int64_t g = 0; cur.t < t1; cur.next(ntab, RG, Hkv, B), ++g) {
       const bool first = cur.t == t0 || cur.j == 0;
       const bool last = cur.t == t1 - 1 || cur.j == cur.n - 1;
       const int ub = uidx & 1;
-      const int64_t g = cur.t - t0;
       const RowFacts<NR>& rf = facts0[ub];
       if (first) {
         // the row facts come with the query rows
