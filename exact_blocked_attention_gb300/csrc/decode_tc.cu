@@ -509,6 +509,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         qrow[h2] = static_cast<const __nv_bfloat16*>(p.q) + (int64_t)b * p.q_sb + (int64_t)hrow[h2] * p.q_sh +
                    (int64_t)irow[h2] * p.q_si;
         if (real[h2]) pos[h2] = p.qpos[b * p.qp_sb + irow[h2] * p.qp_si];
+        if (real[h2] && p.bias != nullptr) {
+          // the bias of the unit's first tile into L2 now (new rows miss)
+          const int64_t bo = (int64_t)b * p.bi_sb + (int64_t)hrow[h2] * p.bi_sh + (int64_t)irow[h2] * p.bi_si;
+          const int j0 = cur.j * BK;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int key = j0 + 32 * q4;
+            if (key < p.Tmax) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.bias + bo + (int64_t)key * p.bi_sj));
+          }
+        }
       }
       uint4 val[NR / 2];
 #pragma unroll
@@ -545,16 +555,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           oo = (int64_t)b * p.o_sb + (int64_t)h * p.o_sh + (int64_t)i * p.o_si;
           lo = (int64_t)b * p.l_sb + (int64_t)h * p.l_sh + (int64_t)i * p.l_si;
           umin = min(umin, e);
-          if (p.bias != nullptr) {
-            // the bias of the unit's first tile here into L2 (new rows miss)
-            const int j0 = cur.j * BK;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const int key = j0 + 32 * q4;
-              if (key < p.Tmax)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(p.bias + bo + (int64_t)key * p.bi_sj));
-            }
-          }
         }
         umax = max(umax, e);
         rf.end[r] = e;
