@@ -838,11 +838,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         float sc[NH];
         ld_cols<NH>(tl + kColS + 64u * (uint32_t)(g & 1) + c0, sc);
         const bool tail = key0 + BK > rf.min_end;
+        // pairs of rows in packed fp32 (f32x2) arithmetic
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+        if (has_bias) {
+          const float2 l2e = make_float2(kLog2e, kLog2e);
 #pragma unroll
-        for (int r = 0; r < NH; ++r) {
-          float v = has_bias ? fmaf(sc[r], p.scale_log2, x[r] * kLog2e) : sc[r] * p.scale_log2;
-          if (tail && key >= rf.end[c0 + r]) v = kNegInf;
-          x[r] = v;
+          for (int r = 0; r < NH; r += 2) {
+            const float2 v = __ffma2_rn(make_float2(sc[r], sc[r + 1]), sc2,
+                                        __fmul2_rn(make_float2(x[r], x[r + 1]), l2e));
+            x[r] = v.x;
+            x[r + 1] = v.y;
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < NH; r += 2) {
+            const float2 v = __fmul2_rn(make_float2(sc[r], sc[r + 1]), sc2);
+            x[r] = v.x;
+            x[r + 1] = v.y;
+          }
+        }
+        if (tail) {
+#pragma unroll
+          for (int r = 0; r < NH; ++r)
+            if (key >= rf.end[c0 + r]) x[r] = kNegInf;
         }
 #pragma unroll
         for (int r4 = 0; r4 < NH / 4; ++r4) {
@@ -920,14 +938,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2) {
             const int r = 8 * c8 + 2 * e2;
-            const float pa = fast_exp2(x[r] - mu[2 * e2]);  // masked: 2^-inf = 0
-            const float pb = fast_exp2(x[r + 1] - mu[2 * e2 + 1]);
-            lp[r] += pa;
-            lp[r + 1] += pb;
-            asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi[e2]) : "r"(__float_as_uint(pa)), "r"(__float_as_uint(pb)));
-            const float ra = pa - __uint_as_float(__float_as_uint(pa) & 0xffff0000u);
-            const float rb = pb - __uint_as_float(__float_as_uint(pb) & 0xffff0000u);
-            lo[e2] = pack_bf16(ra, rb);
+            const float2 e = __ffma2_rn(make_float2(mu[2 * e2], mu[2 * e2 + 1]), make_float2(-1.f, -1.f),
+                                        make_float2(x[r], x[r + 1]));
+            const float2 pp = make_float2(fast_exp2(e.x), fast_exp2(e.y));  // masked: 2^-inf = 0
+            const float2 l2 = __fadd2_rn(make_float2(lp[r], lp[r + 1]), pp);
+            lp[r] = l2.x;
+            lp[r + 1] = l2.y;
+            asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi[e2]) : "r"(__float_as_uint(pp.x)), "r"(__float_as_uint(pp.y)));
+            const float2 rem = __ffma2_rn(make_float2(__uint_as_float(__float_as_uint(pp.x) & 0xffff0000u),
+                                                      __uint_as_float(__float_as_uint(pp.y) & 0xffff0000u)),
+                                          make_float2(-1.f, -1.f), pp);
+            lo[e2] = pack_bf16(rem.x, rem.y);
           }
           const int c = c0 / 8 + c8;  // 16-byte chunk of the row's P_hi
           const int off = ((c ^ (k & 7)) << 4);
