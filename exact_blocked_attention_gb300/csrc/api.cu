@@ -213,13 +213,15 @@ int get_encoder() {
 
 struct MapKey {
   int dev;
+  int dtype;
+  int box_cols;
   int box_rows;
   const void* ptr;
   int64_t sizes[4];
   int64_t strides[3];
   bool operator==(const MapKey& o) const {
-    return dev == o.dev && box_rows == o.box_rows && ptr == o.ptr && std::memcmp(sizes, o.sizes, sizeof sizes) == 0 &&
-           std::memcmp(strides, o.strides, sizeof strides) == 0;
+    return dev == o.dev && dtype == o.dtype && box_cols == o.box_cols && box_rows == o.box_rows && ptr == o.ptr &&
+           std::memcmp(sizes, o.sizes, sizeof sizes) == 0 && std::memcmp(strides, o.strides, sizeof strides) == 0;
   }
 };
 struct MapEntry {
@@ -231,13 +233,15 @@ constexpr int kMapCache = 32;
 MapEntry g_maps[kMapCache];
 int g_map_next = 0;
 
-// 4-D map over a bf16 view [B, H, T, d] (element strides, last = 1):
-// dims {d, T, H, B}, box {64, box_rows, 1, 1}, 128-byte swizzle, zero fill
-// past T.  Used for the K/V cache (64-row boxes) and for Q (128-row boxes).
-int kv_tensor_map(int dev, const blkattn_tensor* t, int box_rows, const CUtensorMap** out) {
+// 4-D map over a view [B, H, T, d] (element strides, last = 1): dims
+// {d, T, H, B}, box {box_cols, box_rows, 1, 1}, 128-byte swizzle (box_cols *
+// element size = 128 bytes), zero fill past T.
+int tensor_map(int dev, const blkattn_tensor* t, int box_cols, int box_rows, const CUtensorMap** out) {
   MapKey key;
   std::memset(&key, 0, sizeof key);
   key.dev = dev;
+  key.dtype = t->dtype;
+  key.box_cols = box_cols;
   key.box_rows = box_rows;
   key.ptr = t->data;
   for (int i = 0; i < 4; ++i) key.sizes[i] = t->sizes[i];
@@ -251,15 +255,18 @@ int kv_tensor_map(int dev, const blkattn_tensor* t, int box_rows, const CUtensor
   if (st != BLKATTN_OK) return st;
   MapEntry& e = g_maps[g_map_next];
   g_map_next = (g_map_next + 1) % kMapCache;
+  const bool f32 = t->dtype == BLKATTN_F32;
+  const cuuint64_t eb = f32 ? 4 : 2;
   const cuuint64_t dims[4] = {(cuuint64_t)t->sizes[3], (cuuint64_t)t->sizes[2], (cuuint64_t)t->sizes[1],
                               (cuuint64_t)t->sizes[0]};
-  const cuuint64_t strides[3] = {(cuuint64_t)t->strides[2] * 2, (cuuint64_t)t->strides[1] * 2,
-                                 (cuuint64_t)t->strides[0] * 2};
-  const cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
+  const cuuint64_t strides[3] = {(cuuint64_t)t->strides[2] * eb, (cuuint64_t)t->strides[1] * eb,
+                                 (cuuint64_t)t->strides[0] * eb};
+  const cuuint32_t box[4] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUresult r = g_encode(&e.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = g_encode(&e.map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                              t->data, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     e.used = false;
     return cuda_fail(cudaErrorInvalidValue);  // the tensor map was refused
@@ -268,6 +275,21 @@ int kv_tensor_map(int dev, const blkattn_tensor* t, int box_rows, const CUtensor
   e.used = true;
   *out = &e.map;
   return BLKATTN_OK;
+}
+
+// bf16 K/V cache or Q: boxes of 64 dims (128 bytes) x box_rows rows.
+int kv_tensor_map(int dev, const blkattn_tensor* t, int box_rows, const CUtensorMap** out) {
+  return tensor_map(dev, t, 64, box_rows, out);
+}
+
+// Whether the output can be stored by tiled TMA from the prefill kernel:
+// fp32, unit dim stride, 16-byte aligned base and strides.
+bool out_tma_ok(const blkattn_tensor* out) {
+  if (out->dtype != BLKATTN_F32 || out->strides[3] != 1) return false;
+  if ((reinterpret_cast<uintptr_t>(out->data) % 16) != 0) return false;
+  for (int i = 0; i < 3; ++i)
+    if ((out->strides[i] * 4) % 16 != 0 || out->strides[i] <= 0) return false;
+  return true;
 }
 
 // Grow-only per-device scratch.  Growing while the stream is being captured
@@ -460,7 +482,8 @@ FwdParams fill_params(const blkattn_tensor* q, const blkattn_tensor* k, const bl
 
 // Enqueue the split-KV kernel and, with more than one split, the merge.
 int launch_fwd(const FwdParams& p, const Checked& c, const Plan& pl, const blkattn_tensor* q,
-               const blkattn_tensor* k, const blkattn_tensor* v, cudaStream_t stream) {
+               const blkattn_tensor* k, const blkattn_tensor* v, const blkattn_tensor* out,
+               cudaStream_t stream) {
   cudaError_t le;
   if (pl.cfg.kernel == blkattn::Kernel::DecodeTc) {
     int dev = 0;
@@ -487,7 +510,16 @@ int launch_fwd(const FwdParams& p, const Checked& c, const Plan& pl, const blkat
       const CUtensorMap* mq = nullptr;
       st = kv_tensor_map(dev, q, 128, &mq);
       if (st != BLKATTN_OK) return st;
-      le = blkattn::launch_prefill_tc(p, pl.cfg.row_groups, *mq, *mk, *mv, stream);
+      // whole output tiles by TMA where the output layout allows it
+      FwdParams pp = p;
+      const CUtensorMap* mo = mq;  // not read unless pp.o_tma
+      pp.o_tma = 0;
+      if (out_tma_ok(out)) {
+        st = tensor_map(dev, out, 32, 32, &mo);
+        if (st != BLKATTN_OK) return st;
+        pp.o_tma = 1;
+      }
+      le = blkattn::launch_prefill_tc(pp, pl.cfg.row_groups, *mq, *mk, *mv, *mo, stream);
     } else {
       le = blkattn::launch_decode_mma(p, (int)c.d, pl.cfg, *mk, *mv, stream);
     }
@@ -545,7 +577,7 @@ int fwd_with_scratch(const blkattn_tensor* q, const blkattn_tensor* k, const blk
   unsigned* counters = reinterpret_cast<unsigned*>(static_cast<char*>(scratch) + usable);
   const FwdParams p = fill_params(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, c, pl,
                                   scratch, ds->err, counters);
-  return launch_fwd(p, c, pl, q, k, v, stream);
+  return launch_fwd(p, c, pl, q, k, v, out, stream);
 }
 
 }  // namespace blkattn
@@ -612,7 +644,7 @@ int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_
   }
   const FwdParams p = fill_params(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, c, pl,
                                   ds->ws, ds->err, ds->cnt);
-  return launch_fwd(p, c, pl, q, k, v, stream);
+  return launch_fwd(p, c, pl, q, k, v, out, stream);
 }
 
 int blkattn_merge(const blkattn_states* a, const blkattn_states* b, const blkattn_states* out,

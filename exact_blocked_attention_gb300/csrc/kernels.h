@@ -58,6 +58,9 @@ struct FwdParams {
   // wrote theirs (zero before the launch, left zero after it)
   int rows_cta;
   unsigned* unit_cnt;
+  // prefill: 1 when the output tensor map (fp32, boxes {32, 32}, 128-byte
+  // swizzle) is valid and the kernel stores whole output tiles with TMA
+  int o_tma;
 };
 
 // Split-KV kernel configuration chosen by the planner.
@@ -96,9 +99,10 @@ size_t decode_mma_smem_bytes(int d, int mt);
 
 // Causal prefill on tcgen05 (bf16, d = 128, no bias): one CTA per 256 query
 // rows of one head (two 128-row query tiles); maps: Q and K/V boxes {64, 128},
-// all 128-byte swizzle.
+// all 128-byte swizzle; tmo (read only when p.o_tma) the fp32 output with
+// boxes {32, 32}, 128-byte swizzle.
 cudaError_t launch_prefill_tc(const FwdParams& p, int n_pairs, const CUtensorMap& tmq, const CUtensorMap& tmk,
-                              const CUtensorMap& tmv, cudaStream_t stream);
+                              const CUtensorMap& tmv, const CUtensorMap& tmo, cudaStream_t stream);
 int prefill_tc_smem_bytes();
 
 // Decode / verify on tcgen05 (bf16, d = 128, 16-byte aligned query rows, at

@@ -21,6 +21,11 @@
 // although P is not an input), and S_{j+1} is issued right after U += P_j V_j
 // (products execute in issue order).  The two query tiles ping-pong: while
 // one tile's rows compute P, the tensor core runs the other tile's products.
+// Each tile's chain S_j -> P_j -> products -> S_{j+1} passes through the
+// MMA thread, so its issue path is kept short: shared-memory descriptors are
+// formed once per operand buffer and only their address word moves.
+// The epilogue (o = u / l) stages fp32 rows in the freed K / V ring and
+// stores them with tiled TMA when the output layout allows it.
 //
 // Online rescaling is lazy: a row keeps its reference maximum m until a tile
 // raises the row maximum by more than 8 (base-2 units); only then is its U
@@ -80,7 +85,8 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmq,
-                      const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+                      const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                      const __grid_constant__ CUtensorMap tmo) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
@@ -229,26 +235,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(q_full, 0);
       // S_jj = Q_t K_jj^T into query tile t's S buffer
       auto issue_qk = [&](int t, int jj) {
-        const uint32_t kbase = sK + (jj % STAGES) * kTileBytes;
-        const uint32_t qbase = sQ + t * kTileBytes;
+        // descriptors: only the start address moves (split-word form)
+        const uint32_t klo = tc::desc_lo(sK + (jj % STAGES) * kTileBytes, 16);
+        const uint32_t qlo = tc::desc_lo(sQ + t * kTileBytes, 16);
+        constexpr uint32_t kHi = tc::desc_hi(1024);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t adesc = tc::smem_desc(qbase + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024);
-          const uint64_t bdesc = tc::smem_desc(kbase + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024);
+          const uint32_t off = (uint32_t)(((ks >> 2) * kBox + (ks & 3) * 32) >> 4);
+          const uint64_t adesc = tc::desc_join(qlo + off, kHi);
+          const uint64_t bdesc = tc::desc_join(klo + off, kHi);
           tc::mma_ss(tb + t * kTileCols + kColS, adesc, bdesc, kIdescQK, ks > 0 ? 1u : 0u);
         }
         tc::commit(&s_full[t]);
       };
       // U_t += P_jj V_jj (P_hi, then P_lo)
       auto issue_pv = [&](int t, int jj) {
-        const uint32_t vbase = sV + (jj % STAGES) * kTileBytes;
+        const uint32_t vlo = tc::desc_lo(sV + (jj % STAGES) * kTileBytes, kBox);
+        constexpr uint32_t kHi = tc::desc_hi(1024);
         const uint32_t tcol = tb + t * kTileCols;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
 #pragma unroll
           for (int ks = 0; ks < BN / 16; ++ks) {
             // B = V rows [16ks, 16ks+16) (keys, K) x 128 dims (N, two 64-dim boxes 16 KB apart)
-            const uint64_t bdesc = tc::smem_desc(vbase + ks * 16 * 128, kBox, 1024);
+            const uint64_t bdesc = tc::desc_join(vlo + (uint32_t)(ks * 16 * 128 >> 4), kHi);
             const uint32_t acol = tcol + kColS + part * kColPlo + 8 * ks;
             tc::mma_ts(tcol + kColO, acol, bdesc, kIdescPV, (jj > 0 || part > 0 || ks > 0) ? 1u : 0u);
           }
@@ -434,53 +444,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         tc::fence_after();
         const float inv = (m_ref == kNegInf) ? 0.f : 1.f / l;
-        // Every MMA has completed (drain), so the K (query tile 0) or V
-        // (query tile 1) ring is free: stage the 128 x 128 fp32 rows there and
-        // store whole rows with coalesced 16-byte writes.  Row r's 16-byte
-        // chunk c sits at chunk c ^ (r mod 32) (conflict-free both ways).
-        const bool staged = p.o_sd == 1 && !p.out_bf16 && (p.o_si % 4) == 0 &&
-                            (reinterpret_cast<uintptr_t>(p.out) % 16) == 0 && (p.o_sb % 4) == 0 &&
-                            (p.o_sh % 4) == 0;
-        float4* stage = reinterpret_cast<float4*>(sm + (x == 0 ? kOffK : kOffV));
-        const int rr = (int)(threadIdx.x & 127);
-#pragma unroll 1
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t r[32];
-          tc::ld32(tl + kColO + 32 * q4, r);
+        if (p.o_tma) {
+          // Every MMA has completed (drain), so the K (query tile 0) or V
+          // (query tile 1) ring is free.  Each warp stages its 32 rows x 128
+          // dims there as four 4 KB boxes of 32 dims in the 128-byte swizzled
+          // layout of the output map (16-byte chunk c of row r at c ^ (r mod
+          // 8): conflict-free) and one lane stores them with tiled TMA.
+          unsigned char* stage = sm + (x == 0 ? kOffK : kOffV) + (warp & 3) * 4 * 4096;
+          uint32_t r0[32], r1[32], r2[32], r3[32];
+          tc::ld32(tl + kColO, r0);
+          tc::ld32(tl + kColO + 32, r1);
+          tc::ld32(tl + kColO + 64, r2);
+          tc::ld32(tl + kColO + 96, r3);
           tc::wait_ld();
-          if (staged) {
+          auto put = [&](int q4, const uint32_t(&r)[32]) {
+            float4* box = reinterpret_cast<float4*>(stage + q4 * 4096);
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-              const int c = q4 * 8 + c4;
-              stage[rr * 32 + (c ^ (rr & 31))] =
-                  make_float4(__uint_as_float(r[4 * c4]) * inv, __uint_as_float(r[4 * c4 + 1]) * inv,
-                              __uint_as_float(r[4 * c4 + 2]) * inv, __uint_as_float(r[4 * c4 + 3]) * inv);
-            }
-          } else if (my_row) {
+            for (int c = 0; c < 8; ++c)
+              box[lane * 8 + (c ^ (lane & 7))] =
+                  make_float4(__uint_as_float(r[4 * c]) * inv, __uint_as_float(r[4 * c + 1]) * inv,
+                              __uint_as_float(r[4 * c + 2]) * inv, __uint_as_float(r[4 * c + 3]) * inv);
+          };
+          put(0, r0);
+          put(1, r1);
+          put(2, r2);
+          put(3, r3);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // staged rows -> TMA
+          __syncwarp();
+          const int row_w = (2 * pair + x) * BM + 32 * (warp & 3);
+          if (lane == 0 && row_w < p.Tq) {
+            // rows past Tq are clipped by the map
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const float o = __uint_as_float(r[c]) * inv;
-              const int64_t oi = out_row + (int64_t)(32 * q4 + c) * p.o_sd;
-              if (p.out_bf16)
-                static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
-              else
-                static_cast<float*>(p.out)[oi] = o;
-            }
+            for (int q4 = 0; q4 < 4; ++q4) tma_store_4d(&tmo, stage + q4 * 4096, 32 * q4, row_w, h, b);
+            bulk_commit();
           }
-        }
-        if (staged) {
-          asm volatile("bar.sync %0, 128;" ::"r"(1 + x) : "memory");  // this query tile's 4 warps
-          const int w4 = warp & 3;
-          const int row0 = (2 * pair + x) * BM;
-          for (int r2 = w4; r2 < BM; r2 += 4) {
-            if (row0 + r2 >= p.Tq) break;
-            const float4 v4 = stage[r2 * 32 + (lane ^ (r2 & 31))];
-            float* dst = static_cast<float*>(p.out) + (int64_t)b * p.o_sb + (int64_t)h * p.o_sh +
-                         (int64_t)(row0 + r2) * p.o_si;
-            reinterpret_cast<float4*>(dst)[lane] = v4;
+        } else {
+          // the tensor-memory loads are warp-collective: every lane takes
+          // part, rows past Tq store nothing
+#pragma unroll 1
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t r[32];
+            tc::ld32(tl + kColO + 32 * q4, r);
+            tc::wait_ld();
+            if (my_row) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const float o = __uint_as_float(r[c]) * inv;
+                const int64_t oi = out_row + (int64_t)(32 * q4 + c) * p.o_sd;
+                if (p.out_bf16)
+                  static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+                else
+                  static_cast<float*>(p.out)[oi] = o;
+              }
+            }
           }
         }
         if (my_row) p.lse[lse_idx] = (m_ref == kNegInf) ? kNegInf : (m_ref + __log2f(l)) * kLn2;
+        // the staging buffer is released with the CTA: the stores must have
+        // read it (no-op for a lane without stores)
+        if (p.o_tma && lane == 0) bulk_wait_read();
       }
     }
   }
@@ -496,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 int prefill_tc_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_prefill_tc(const FwdParams& p, int n_pairs, const CUtensorMap& tmq, const CUtensorMap& tmk,
-                              const CUtensorMap& tmv, cudaStream_t stream) {
+                              const CUtensorMap& tmv, const CUtensorMap& tmo, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -510,7 +532,7 @@ cudaError_t launch_prefill_tc(const FwdParams& p, int n_pairs, const CUtensorMap
   const int64_t groups = (heads + p.head_group - 1) / p.head_group;
   const int64_t blocks = groups * p.head_group * n_pairs;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  prefill_tc_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmk, tmv);
+  prefill_tc_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmk, tmv, tmo);
   return cudaGetLastError();
 }
 

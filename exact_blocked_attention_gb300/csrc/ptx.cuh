@@ -96,6 +96,21 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const void* map, int c0, 
       : "memory");
 }
 
+// Tiled TMA store of one box of a 4-D tensor map from shared memory (bulk
+// group completion).  Coordinates must be non-negative; c0 * element size must
+// be a multiple of 16 bytes; elements past the tensor's extent are not written.
+// The shared-memory source must be made visible to the async proxy first
+// (fence.proxy.async) and stay unchanged until bulk_wait_read() returns.
+__device__ __forceinline__ void tma_store_4d(const void* map, const void* src, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk store of this thread has read its source.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 // Named barrier `id` over `count` threads that also ANDs a predicate across
 // them: every thread gets the same answer.
 __device__ __forceinline__ bool bar_and(int id, int count, bool pred) {

@@ -39,7 +39,7 @@ __device__ __forceinline__ void fence_after() {
 // ---- descriptors ----
 // Shared-memory matrix descriptor: start address, leading/stride byte offsets
 // (>> 4), fixed version 0b001 at bit 46, 128-byte swizzle (mode 2 at 61-63).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+__host__ __device__ constexpr uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
   d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
@@ -48,6 +48,25 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   d |= (uint64_t)2 << 61;
   return d;
 }
+
+// The same descriptor as two 32-bit halves: the low word holds the start
+// address (>> 4) and the leading byte offset, the high word the stride byte
+// offset, the version and the swizzle mode.  Operands that differ only in
+// their start address share the high word, and moving the start by a
+// multiple of 16 bytes adds (bytes >> 4) to the low word: shared-memory
+// addresses stay below 2^18, so the 14-bit address field never carries.
+__host__ __device__ constexpr uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t desc_hi(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__host__ __device__ constexpr uint64_t desc_join(uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; }
+static_assert(desc_join(desc_lo(0x9400, 16) + (0x4020 >> 4), desc_hi(1024)) == smem_desc(0x9400 + 0x4020, 16, 1024),
+              "split descriptor");
+static_assert(desc_join(desc_lo(0x20000, 16384) + (7 * 2048 >> 4), desc_hi(1024)) ==
+                  smem_desc(0x20000 + 7 * 2048, 16384, 1024),
+              "split descriptor");
 
 // Instruction descriptor for kind::f16 with bf16 A and B, fp32 accumulator.
 // a_mn / b_mn: operand stored MN-major (1) or K-major (0).

@@ -396,6 +396,41 @@ def test_prefill_kernel_cases(case):
     assert_parity(ob, lb, ref, BF16_TOL_O, BF16_TOL_L, out_raw=raw, bf16_out=True)
 
 
+@pytest.mark.parametrize("layout", ["padded_rows", "seq_major", "odd_row_stride"])
+def test_prefill_output_layouts(layout):
+    """Output views into larger buffers: whole tiles go out by TMA where the
+    layout allows it (fp32, 16-byte strides), row by row otherwise; memory of
+    the buffer outside the view is never written (the tail tile is clipped)."""
+    B, Hq, Hkv, Tq, Tmax = 2, 3, 1, 161, 161
+    inp = make_case(B, Hq, Hkv, Tq, Tmax, 128, "bf16", [161, 150], [list(range(Tq))] * B, seed=11)
+    assert plan_of(inp)["kernel"] == 2
+    g = to_dev(inp)
+    sentinel = 12345.0
+    if layout == "padded_rows":  # rows past T_q in the buffer
+        buf = torch.full((B, Hq, Tq + 40, 128), sentinel, device="cuda")
+        out = buf[:, :, :Tq]
+    elif layout == "seq_major":  # [B, T, H, d] storage seen as [B, H, T, d]
+        buf = torch.full((B, Tq + 8, Hq, 128), sentinel, device="cuda")
+        out = buf[:, :Tq].permute(0, 2, 1, 3)
+    else:  # row stride of 130 floats: not a multiple of 16 bytes
+        buf = torch.full((B, Hq, Tq, 130), sentinel, device="cuda")
+        out = buf[..., :128]
+    lse = torch.empty(B, Hq, Tq, device="cuda")
+    blkattn.fwd(g["q"], g["k"], g["v"], g["seqlens"], g["qpos"], None, g["scale"], out, lse)
+    torch.cuda.synchronize()
+    assert blkattn.check_device_error() == 0
+    o = out.double().cpu().numpy().reshape(-1, 128)
+    assert_parity(o, lse.double().cpu().numpy().reshape(-1), run_oracle(inp), BF16_TOL_O, BF16_TOL_L)
+    outside = torch.ones_like(buf, dtype=torch.bool)
+    if layout == "padded_rows":
+        outside[:, :, :Tq] = False
+    elif layout == "seq_major":
+        outside[:, :Tq] = False
+    else:
+        outside[..., :128] = False
+    assert torch.all(buf[outside] == sentinel)
+
+
 def test_prefill_kernel_poisoned_padding():
     B, Hq, Hkv, Tq, Tmax = 1, 2, 2, 200, 512
     qpos = [list(range(100, 300))]
