@@ -586,25 +586,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       Cursor cq = cur;  // tile of the next S product
       int uq = 0, up = 0;  // unit counters of the S and the U sides
+      // Ring positions of the next K (even entries) and V (odd entries)
+      // tiles: slot and phase advance by two entries per tile, without
+      // divisions on this thread's path.
+      struct RingPos {
+        uint32_t slot, phase;
+        __device__ void adv2() {
+          slot += 2;
+          if (slot >= (uint32_t)kSlots) {
+            slot -= (uint32_t)kSlots;
+            phase ^= 1u;
+          }
+        }
+      };
+      RingPos kpos{0u, 0u}, vpos{1u, 0u};
+      constexpr uint32_t kHi = tc::desc_hi(1024);
+      // shared-memory descriptors: only the address word moves per MMA
+      const uint32_t qlo0 = tc::desc_lo(sQ, 16);
       auto issue_qk = [&](int64_t gq) -> bool {
         const bool first = cq.t == t0 || cq.j == 0;
         const bool last = cq.t == t1 - 1 || cq.j == cq.n - 1;
         const int qb = uq & 1;
         if (first && !mbar_wait(&q_full[qb], (uint32_t)((uq >> 1) & 1))) return false;
-        const int64_t sk = 2 * gq;
-        if (!mbar_wait(&full[sk % kSlots], (uint32_t)((sk / kSlots) & 1))) return false;
+        const uint32_t ks_slot = kpos.slot;
+        if (!mbar_wait(&full[ks_slot], kpos.phase)) return false;
+        kpos.adv2();
         tc::fence_after();
         // S^T = K_j Q^T into the S buffer of the tile's parity
-        const uint32_t kb = sRing + (uint32_t)(sk % kSlots) * kSlotBytes;
-        const uint32_t qbase = sQ + qb * L::kQBytes;
+        const uint32_t klo = tc::desc_lo(sRing + ks_slot * kSlotBytes, 16);
+        const uint32_t qlo = qlo0 + (uint32_t)(qb * L::kQBytes >> 4);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t adesc = tc::smem_desc(kb + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024);
-          const uint64_t bdesc = tc::smem_desc(qbase + (ks >> 2) * L::kQBox + (ks & 3) * 32, 16, 1024);
+          const uint64_t adesc = tc::desc_join(klo + (uint32_t)(((ks >> 2) * kBox + (ks & 3) * 32) >> 4), kHi);
+          const uint64_t bdesc = tc::desc_join(qlo + (uint32_t)(((ks >> 2) * L::kQBox + (ks & 3) * 32) >> 4), kHi);
           tc::mma_ss(tb + kColS + 64u * (uint32_t)(gq & 1), adesc, bdesc, kIdescQK, ks > 0 ? 1u : 0u);
         }
         tc::commit(&s_full[gq & 1]);
-        tc::commit(&empty[sk % kSlots]);
+        tc::commit(&empty[ks_slot]);
         if (last) {
           tc::commit(&q_empty[qb]);
           ++uq;
@@ -618,22 +636,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool last = cur.t == t1 - 1 || cur.j == cur.n - 1;
         if (cq.t < t1 && !issue_qk(g + 1)) { ok = false; break; }
         // U^T += V_j^T [P_hi | P_lo]^T once the key threads wrote P^T
-        const int64_t sv = 2 * g + 1;
+        const uint32_t vs_slot = vpos.slot;
         if (!mbar_wait(&p_full[g & 1], (uint32_t)((g >> 1) & 1))) { ok = false; break; }
-        if (!mbar_wait(&full[sv % kSlots], (uint32_t)((sv / kSlots) & 1))) { ok = false; break; }
+        if (!mbar_wait(&full[vs_slot], vpos.phase)) { ok = false; break; }
+        vpos.adv2();
         tc::fence_after();
-        const uint32_t vb = sRing + (uint32_t)(sv % kSlots) * kSlotBytes;
-        const uint32_t pb = sP + (uint32_t)(g & 1) * kPBytes;
+        const uint32_t vlo = tc::desc_lo(sRing + vs_slot * kSlotBytes, kBox);
+        const uint32_t plo = tc::desc_lo(sP + (uint32_t)(g & 1) * kPBytes, kBox);
         const uint32_t ucol = tb + kColU + 128u * (uint32_t)(up & 1);
 #pragma unroll
         for (int ks = 0; ks < BK / 16; ++ks) {
           // A = V^T: 128 dims (two 64-dim boxes 16 KB apart) x keys [16 ks, 16 ks + 16)
-          const uint64_t adesc = tc::smem_desc(vb + ks * 2048, kBox, 1024);
+          const uint64_t adesc = tc::desc_join(vlo + (uint32_t)(ks * 2048 >> 4), kHi);
           // B = P^T: keys [16 ks, +16) x [P_hi | P_lo] (one atom, or two 16 KB apart)
-          const uint64_t bdesc = tc::smem_desc(pb + ks * 2048, kBox, 1024);
+          const uint64_t bdesc = tc::desc_join(plo + (uint32_t)(ks * 2048 >> 4), kHi);
           tc::mma_ss(ucol, adesc, bdesc, kIdescPV, (!first || ks > 0) ? 1u : 0u);
         }
-        tc::commit(&empty[sv % kSlots]);
+        tc::commit(&empty[vs_slot]);
         tc::commit(pv_done);
         if (last) {
           tc::commit(&u_full[up & 1]);
