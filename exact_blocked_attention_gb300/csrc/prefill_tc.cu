@@ -121,15 +121,54 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int x = warp >> 2;  // query tile of a row warp (0 or 1)
   const int i0 = (2 * pair + (warp < 8 ? x : 0)) * BM;
 
-  // ---- visibility of the rows (integers) ----
-  int len = p.seqlens[b * p.sl_s];
-  len = len < 0 ? 0 : (len > p.Tmax ? p.Tmax : len);
+  const uint64_t pol_q = policy_evict_first();
+  const uint64_t pol_kv = policy_evict_last();  // K/V tiles are re-read by the other query tiles
+  // Barriers and tensor memory first: the producer then starts both Q tiles
+  // and the first K/V tile (always inside the cache, T_max >= 1) while the
+  // rows read their positions.
   if (threadIdx.x == 0) {
     misc[1] = 0; misc[2] = 0x7fffffff;
     misc[3] = 0; misc[4] = 0x7fffffff;
     misc[5] = 0;
+    mbar_init(q_full, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int t = 0; t < QT; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 4);  // one arrival per row warp of the query tile
+    }
+    mbar_init(drain, 1);
+    fence_barrier_init();
   }
+  if (warp == kMmaWarp) {
+    tc::alloc(reinterpret_cast<uint32_t*>(&misc[0]), kTmemCols);
+    tc::relinquish();
+  }
+  tc::fence_before();
   __syncthreads();
+  tc::fence_after();
+  if (warp == kTmaWarp && lane == 0) {
+    const int q0 = 2 * pair * BM;
+    mbar_arrive_expect_tx(q_full, QT * kTileBytes);
+    for (int t = 0; t < QT; ++t) {
+      tma_load_4d(sm + kOffQ + t * kTileBytes, &tmq, 0, q0 + t * BM, h, b, q_full, pol_q);
+      tma_load_4d(sm + kOffQ + t * kTileBytes + kBox, &tmq, 64, q0 + t * BM, h, b, q_full, pol_q);
+    }
+    mbar_arrive_expect_tx(&k_full[0], kTileBytes);
+    tma_load_4d(sm + kOffK, &tmk, 0, 0, hk, b, &k_full[0], pol_kv);
+    tma_load_4d(sm + kOffK + kBox, &tmk, 64, 0, hk, b, &k_full[0], pol_kv);
+    mbar_arrive_expect_tx(&v_full[0], kTileBytes);
+    tma_load_4d(sm + kOffV, &tmv, 0, 0, hk, b, &v_full[0], pol_kv);
+    tma_load_4d(sm + kOffV + kBox, &tmv, 64, 0, hk, b, &v_full[0], pol_kv);
+  }
+
+  // ---- visibility of the rows (integers) ----
+  int len = p.seqlens[b * p.sl_s];
+  len = len < 0 ? 0 : (len > p.Tmax ? p.Tmax : len);
   int my_end = 0;
   bool my_row = false;
   const int row_i = i0 + (int)(threadIdx.x & 127);
@@ -157,52 +196,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     p.lse[lse_idx] = kNegInf;
   };
-  if (n_max == 0) {
-    if (my_row) write_empty_row();
-    return;
-  }
-
-  if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_empty[s], 1);
-    }
-    for (int t = 0; t < QT; ++t) {
-      mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], 4);  // one arrival per row warp of the query tile
-    }
-    mbar_init(drain, 1);
-    fence_barrier_init();
-  }
-  if (warp == kMmaWarp) {
-    tc::alloc(reinterpret_cast<uint32_t*>(&misc[0]), kTmemCols);
-    tc::relinquish();
-  }
-  tc::fence_before();
-  __syncthreads();
-  tc::fence_after();
   const uint32_t tb = static_cast<uint32_t>(misc[0]);
   const uint32_t sQ = smem_u32(sm + kOffQ);
   const uint32_t sK = smem_u32(sm + kOffK);
   const uint32_t sV = smem_u32(sm + kOffV);
 
-  if (warp == kTmaWarp) {
+  if (n_max == 0) {
+    // no row of the CTA sees a key: the defined empty output; the first
+    // copies must still land before the CTA exits
+    if (my_row) write_empty_row();
+    if (warp == kTmaWarp && lane == 0) {
+      bool landed = mbar_wait(q_full, 0);
+      landed = mbar_wait(&k_full[0], 0) && landed;
+      landed = mbar_wait(&v_full[0], 0) && landed;
+      if (!landed) record_error(p.err, kErrTimeout);
+    }
+  } else if (warp == kTmaWarp) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      const uint64_t pol_q = policy_evict_first();
-      const uint64_t pol_kv = policy_evict_last();  // K/V tiles are re-read by the other query tiles
-      const int q0 = 2 * pair * BM;
-      mbar_arrive_expect_tx(q_full, QT * kTileBytes);
-      for (int t = 0; t < QT; ++t) {
-        tma_load_4d(sm + kOffQ + t * kTileBytes, &tmq, 0, q0 + t * BM, h, b, q_full, pol_q);
-        tma_load_4d(sm + kOffQ + t * kTileBytes + kBox, &tmq, 64, q0 + t * BM, h, b, q_full, pol_q);
-      }
-      int k_issued = 0, v_issued = 0;
+      // Q and K/V tile 0 are in flight already
+      int k_issued = 1, v_issued = 1;
       bool ok = true;
-      for (int j = 0; j < n_max && ok; ++j) {
+      for (int j = 1; j < n_max && ok; ++j) {
         const int s = j % STAGES;
         const int key0 = j * BN;
         if (j >= STAGES && !mbar_wait(&k_empty[s], ((j / STAGES) - 1) & 1)) { ok = false; break; }
