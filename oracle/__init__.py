@@ -67,6 +67,17 @@ def _load():
                 P, ctypes.c_int64,            # rows, nrows
                 P, P, P, P, P,                # out lse n_vis first last
                 I]                            # nthreads
+            lib.oracle_attention_tree.restype = I
+            lib.oracle_attention_tree.argtypes = [
+                I, I, I, I, I, I, I,          # B Hq Hkv Tq Tmax dh dv
+                P, I, P, I, P, I,             # q k v (+types)
+                P, P,                         # seqlens qpos
+                P, I, P,                      # bias, type, strides
+                P,                            # tree masks int64 [B, T_q]
+                ctypes.c_double,              # scale
+                P, ctypes.c_int64,            # rows, nrows
+                P, P, P, P, P,                # out lse n_vis first last
+                I]                            # nthreads
             lib.oracle_max_threads.restype = I
             _lib = lib
     return _lib
@@ -106,7 +117,7 @@ def _as_array(x):
 
 
 def attention(q, k, v, seqlens, qpos, scale, bias=None, rows=None,
-              nthreads: int = 0):
+              nthreads: int = 0, tree=None):
     """Explicit exact attention (eq. 33.2), one row at a time, in fp64.
 
     q [B,H_q,T_q,d_h], k [B,H_kv,T_max,d_h], v [B,H_kv,T_max,d_v] (float64,
@@ -114,6 +125,9 @@ def attention(q, k, v, seqlens, qpos, scale, bias=None, rows=None,
     int32 [B,T_q] (logical position of each query row), bias None or any
     array/tensor broadcastable to [B,H_q,T_q,T_max] (values finite or -inf).
     rows: None for all rows, or flattened row ids (b*H_q + h)*T_q + i.
+    tree: None, or int64 [B,T_q] node masks of a candidate token tree whose
+    nodes' keys are the last T_q cache entries of each sequence (bit k of
+    tree[b,i] set = row i sees tree node k; T_q <= 64).
 
     Returns dict(out [n,d_v] f64, lse [n] f64, n_visible, first, last int32 [n]).
     """
@@ -160,12 +174,17 @@ def attention(q, k, v, seqlens, qpos, scale, bias=None, rows=None,
     nvis = np.zeros(n, dtype=np.int32)
     first = np.zeros(n, dtype=np.int32)
     last = np.zeros(n, dtype=np.int32)
+    tr = None
+    if tree is not None:
+        tr = np.asarray(tree.detach().cpu().numpy() if hasattr(tree, "detach") else tree)
+        tr = np.ascontiguousarray(tr.astype(np.int64, copy=False)).reshape(B, Tq)
     P = lambda a: None if a is None else a.ctypes.data
-    rc = lib.oracle_attention(
+    rc = lib.oracle_attention_tree(
         B, Hq, Hkv, Tq, Tmax, dh, dv,
         P(qa), qt, P(ka), kt, P(va), vt,
         P(sl), P(qp),
         bias_ptr, bias_type, P(strides),
+        P(tr),
         float(scale),
         P(rows_arr), int(n),
         P(out), P(lse), P(nvis), P(first), P(last),

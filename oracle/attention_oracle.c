@@ -29,6 +29,16 @@
  *   - a row with no valid key (the empty set of §33.2, the last paragraph
  *     before Example 25.1) gets the defined output out = 0, lse = -inf.
  *   - lse is the natural logarithm of sum_j e^{z_j}.
+ *   - token-tree verification ("推理加速算法" (inference acceleration
+ *     algorithms) §7.2.2 Medusa, tree attention verification and its figure
+ *     of a candidate tree): when a tree is given, the T_q query rows of a
+ *     sequence are the nodes of a candidate tree and the last T_q cache
+ *     entries [len - T_q, len) hold those nodes' keys, node k at key
+ *     len - T_q + k.  A node sees the whole earlier cache and, inside the
+ *     tree, only the nodes named in its mask (its ancestors and itself): bit k
+ *     of tree[b, i] set = node i sees node k.  The plainest reading of
+ *     "verify every candidate path in one pass": no node sees a sibling
+ *     branch.  This is one more condition on top of the three above.
  *   - grouped-query heads: query head h reads KV head floor(h / (H_q/H_kv)).
  *
  * Inputs may be float64, float32 or bfloat16 (raw 16-bit patterns); every
@@ -66,6 +76,7 @@ typedef struct {
   const int32_t* qpos;
   const void* bias; int bias_type;  /* may be NULL */
   int64_t bias_stride[4];
+  const int64_t* tree;              /* may be NULL: [B, T_q] node masks, T_q <= 64 */
   double scale;
 } oracle_problem;
 
@@ -93,6 +104,13 @@ static int one_row(const oracle_problem* P, int64_t row, double* zbuf,
   for (int64_t j = 0; j < P->Tmax; ++j) {
     zbuf[j] = -INFINITY;
     if (!(j < len && j <= pos)) continue;
+    if (P->tree) {
+      const int64_t base = len - P->Tq; /* key of tree node 0 */
+      if (j >= base) {
+        const int64_t node = j - base;  /* 0 <= node < T_q because j < len */
+        if (!((((uint64_t)P->tree[b * P->Tq + i]) >> node) & 1u)) continue;
+      }
+    }
     double bias = 0.0;
     if (P->bias) {
       const int64_t bi = b * P->bias_stride[0] + h * P->bias_stride[1] +
@@ -141,23 +159,23 @@ static int one_row(const oracle_problem* P, int64_t row, double* zbuf,
  * key index (-1 when none).  nthreads <= 0 uses the OpenMP default.
  * Returns 0, -1 on bad sizes, -2 on an out-of-contract bias, -3 on no memory.
  */
-int oracle_attention(int B, int Hq, int Hkv, int Tq, int Tmax, int dh, int dv,
-                     const void* q, int q_type, const void* k, int k_type,
-                     const void* v, int v_type, const int32_t* seqlens,
-                     const int32_t* qpos, const void* bias, int bias_type,
-                     const int64_t* bias_stride, double scale,
-                     const int64_t* rows, int64_t nrows, double* out,
-                     double* lse, int32_t* n_vis, int32_t* first,
-                     int32_t* last, int nthreads) {
+int oracle_attention_tree(int B, int Hq, int Hkv, int Tq, int Tmax, int dh, int dv,
+                          const void* q, int q_type, const void* k, int k_type,
+                          const void* v, int v_type, const int32_t* seqlens,
+                          const int32_t* qpos, const void* bias, int bias_type,
+                          const int64_t* bias_stride, const int64_t* tree,
+                          double scale, const int64_t* rows, int64_t nrows,
+                          double* out, double* lse, int32_t* n_vis,
+                          int32_t* first, int32_t* last, int nthreads) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Tq < 0 || Tmax < 0 || dh <= 0 ||
-      dv <= 0 || Hq % Hkv != 0)
+      dv <= 0 || Hq % Hkv != 0 || (tree && Tq > 64))
     return -1;
   oracle_problem P;
   memset(&P, 0, sizeof P);
   P.B = B; P.Hq = Hq; P.Hkv = Hkv; P.Tq = Tq; P.Tmax = Tmax; P.dh = dh;
   P.dv = dv; P.q = q; P.q_type = q_type; P.k = k; P.k_type = k_type;
   P.v = v; P.v_type = v_type; P.seqlens = seqlens; P.qpos = qpos;
-  P.bias = bias; P.bias_type = bias_type; P.scale = scale;
+  P.bias = bias; P.bias_type = bias_type; P.scale = scale; P.tree = tree;
   if (bias)
     for (int s = 0; s < 4; ++s) P.bias_stride[s] = bias_stride[s];
   const int64_t total = (int64_t)B * Hq * Tq;
@@ -195,6 +213,20 @@ int oracle_attention(int B, int Hq, int Hkv, int Tq, int Tmax, int dh, int dv,
     free(zbuf);
   }
   return status;
+}
+
+/* The same without a tree. */
+int oracle_attention(int B, int Hq, int Hkv, int Tq, int Tmax, int dh, int dv,
+                     const void* q, int q_type, const void* k, int k_type,
+                     const void* v, int v_type, const int32_t* seqlens,
+                     const int32_t* qpos, const void* bias, int bias_type,
+                     const int64_t* bias_stride, double scale,
+                     const int64_t* rows, int64_t nrows, double* out,
+                     double* lse, int32_t* n_vis, int32_t* first,
+                     int32_t* last, int nthreads) {
+  return oracle_attention_tree(B, Hq, Hkv, Tq, Tmax, dh, dv, q, q_type, k, k_type, v, v_type,
+                               seqlens, qpos, bias, bias_type, bias_stride, NULL, scale, rows,
+                               nrows, out, lse, n_vis, first, last, nthreads);
 }
 
 /* Threads the OpenMP runtime would use (1 without OpenMP). */

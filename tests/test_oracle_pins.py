@@ -356,3 +356,139 @@ def test_row_subset_matches_full_run():
     sub = run(q, k, v, [30, 17], [[5, 10, 29], [0, 16, 40]], 0.4, rows=rows)
     np.testing.assert_array_equal(sub["out"], full["out"][rows])
     np.testing.assert_array_equal(sub["lse"], full["lse"][rows])
+
+
+# ---------------------------------------------------------------- token-tree verification
+# "推理加速算法" (inference acceleration algorithms) §7.2.2 Medusa, tree
+# attention verification: the T_q rows of a sequence are the nodes of a
+# candidate tree; the last T_q cache entries hold their keys (node k at key
+# len - T_q + k); a node sees the earlier cache and, in the tree, only its
+# ancestors and itself.  The pins below take the ancestry from parent arrays
+# (never from the bit masks the oracle reads).
+
+def _ancestor_masks(parents):
+    """Bit masks (int64) from a parent array: bit k of mask[i] = node k is i or
+    an ancestor of i.  parents[0] = -1 (root); parents[k] < k."""
+    masks = []
+    for i in range(len(parents)):
+        m, node = 0, i
+        while node >= 0:
+            m |= 1 << node
+            node = parents[node]
+        masks.append(m - (1 << 64) if m >= 1 << 63 else m)
+    return np.array(masks, dtype=np.int64)
+
+
+def _random_parents(rng, n):
+    return [-1] + [int(rng.integers(0, k)) for k in range(1, n)]
+
+
+def _is_ancestor_or_self(parents, k, i):
+    node = i
+    while node >= 0:
+        if node == k:
+            return True
+        node = parents[node]
+    return False
+
+
+def run_tree(q, k, v, seqlens, qpos, scale, tree, bias=None):
+    return oracle.attention(np.asarray(q, np.float64), np.asarray(k, np.float64),
+                            np.asarray(v, np.float64), np.asarray(seqlens, np.int32),
+                            np.asarray(qpos, np.int32), scale, bias=bias, tree=tree)
+
+
+def test_tree_brute_force_exact_rationals():
+    rng = np.random.default_rng(21)
+    B, Hq, Hkv, Tq, Tmax, dv = 2, 4, 2, 5, 9, 3
+    for trial in range(8):
+        with_bias = trial % 2 == 1
+        q, k, vals, r, sfrac, bias, scale = _rational_problem(rng, B, Hq, Hkv, Tq, Tmax, dv, with_bias)
+        parents = [_random_parents(rng, Tq) for _ in range(B)]
+        tree = np.stack([_ancestor_masks(p) for p in parents])
+        # lengths include ones shorter than the tree (its first nodes then
+        # have no cache entry) and positions that cut into the tree
+        seqlens = rng.integers(2, Tmax + 2, size=B).astype(np.int32)
+        qpos = np.where(rng.random((B, Tq)) < 0.7, Tmax + 5,
+                        rng.integers(-1, Tmax, size=(B, Tq))).astype(np.int32)
+        res = run_tree(q, k, vals, seqlens, qpos, scale, tree, bias=bias)
+        G = Hq // Hkv
+        for b, h, i in itertools.product(range(B), range(Hq), range(Tq)):
+            row = (b * Hq + h) * Tq + i
+            hk = h // G
+            length = min(int(seqlens[b]), Tmax)
+            num = [Fraction(0)] * dv
+            den = Fraction(0)
+            seen = []
+            for j in range(Tmax):
+                if not (j < length and j <= qpos[b, i]):
+                    continue
+                node = j - (length - Tq)
+                if node >= 0 and not _is_ancestor_or_self(parents[b], node, i):
+                    continue
+                w = r[b][hk][j]
+                if with_bias:
+                    s = sfrac[b][h][i][j]
+                    if s is None:
+                        continue
+                    w = w * s
+                seen.append(j)
+                den += w
+                for t in range(dv):
+                    num[t] += w * Fraction(vals[b, hk, j, t])
+            assert res["n_visible"][row] == len(seen)
+            assert res["first"][row] == (seen[0] if seen else -1)
+            assert res["last"][row] == (seen[-1] if seen else -1)
+            if not seen:
+                assert res["lse"][row] == -math.inf
+                assert np.all(res["out"][row] == 0.0)
+                continue
+            exact = np.array([float(x / den) for x in num])
+            np.testing.assert_allclose(res["out"][row], exact, rtol=1e-13, atol=1e-13)
+            assert res["lse"][row] == pytest.approx(math.log(den), abs=1e-13)
+
+
+def test_tree_chain_equals_causal_positions():
+    """A chain (every node the child of the one before) is ordinary causal
+    verification: node i at logical position len - T_q + i."""
+    rng = np.random.default_rng(22)
+    B, Hq, Hkv, Tq, Tmax, d = 3, 4, 2, 7, 40, 8
+    q = rng.normal(size=(B, Hq, Tq, d)); k = rng.normal(size=(B, Hkv, Tmax, d)); v = rng.normal(size=(B, Hkv, Tmax, d))
+    seqlens = np.array([40, 23, 7], dtype=np.int32)
+    chain = np.stack([_ancestor_masks([-1] + list(range(Tq - 1)))] * B)
+    full = np.broadcast_to((seqlens - 1)[:, None], (B, Tq)).astype(np.int32)
+    causal = (seqlens[:, None] - Tq + np.arange(Tq)[None, :]).astype(np.int32)
+    a = run_tree(q, k, v, seqlens, full, 0.3, chain)
+    b = run(q, k, v, seqlens, causal, 0.3)
+    np.testing.assert_array_equal(a["out"], b["out"])
+    np.testing.assert_array_equal(a["lse"], b["lse"])
+    np.testing.assert_array_equal(a["n_visible"], b["n_visible"])
+
+
+def test_tree_of_the_figure_one_hot():
+    """The pages' candidate tree (t+1; t+2a, t+2b, t+2c below it; t+3a below
+    t+2a) with V = I: a node's output is exactly 0 on every key of another
+    branch and positive on the prefix, its ancestors and itself."""
+    parents = [-1, 0, 0, 0, 1]  # t+1, t+2a, t+2b, t+2c, t+3a
+    Tq, L = 5, 6
+    Tmax = L + Tq
+    rng = np.random.default_rng(23)
+    q = rng.normal(size=(1, 1, Tq, 8)); k = rng.normal(size=(1, 1, Tmax, 8))
+    v = np.eye(Tmax).reshape(1, 1, Tmax, Tmax)
+    res = run_tree(q, k, v, [Tmax], [[Tmax - 1] * Tq], 0.5, _ancestor_masks(parents)[None])
+    sees = {0: {0}, 1: {0, 1}, 2: {0, 2}, 3: {0, 3}, 4: {0, 1, 4}}
+    for i in range(Tq):
+        for j in range(Tmax):
+            visible = j < L or (j - L) in sees[i]
+            if visible:
+                assert res["out"][i, j] > 0.0
+            else:
+                assert res["out"][i, j] == 0.0
+        assert res["n_visible"][i] == L + len(sees[i])
+        assert res["out"][i].sum() == pytest.approx(1.0, abs=1e-14)
+
+
+def test_tree_needs_at_most_64_nodes():
+    q = np.zeros((1, 1, 65, 2)); k = np.zeros((1, 1, 70, 2)); v = np.zeros((1, 1, 70, 2))
+    with pytest.raises(ValueError):
+        run_tree(q, k, v, [70], [[69] * 65], 1.0, np.zeros((1, 65), dtype=np.int64))
