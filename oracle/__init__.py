@@ -14,7 +14,9 @@ Contents
                    integer facts per row: visible-key count, first and last
                    visible key.  Pinned by tests/test_oracle_pins.py against
                    Example 25.1, exact rational brute force, closed forms and
-                   the cache-alignment example.
+                   the cache-alignment example.  Optional token-tree
+                   visibility ("推理加速算法" §7.2.2 Medusa, tree attention
+                   verification), pinned by brute force over random trees.
   states           the sufficient statistics (m, l, u) of eq. 33.3, the merge
                    rule of eqs. 33.4–33.5 and Algorithm 33.1, in numpy fp64.
 """
