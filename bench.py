@@ -84,12 +84,14 @@ def describe(s):
 
 
 def algorithmic_bytes(s, inp):
-    """K+V of the visible cache rows (once per KV head) + Q + O (+ lse)."""
+    """K+V of the visible cache rows (once per KV head) + Q + O (+ lse), and
+    the token-tree masks of a tree workload."""
     kv = workloads.kv_bytes(s, inp["seqlens"].numpy())
     elt = 2 if s.dtype == "bf16" else 4
     q = s.B * s.Hq * s.Tq * s.d * elt
     o = s.B * s.Hq * s.Tq * (s.d * 4 + 4)  # fp32 out + lse
-    return kv, kv + q + o
+    tr = 0 if inp.get("tree") is None else inp["tree"].numel() * 8  # token-tree node masks
+    return kv, kv + q + o + tr
 
 
 def causal_flops(s, inp):
@@ -220,7 +222,7 @@ class Runner:
     def call(self):
         g = self.dev
         self.blkattn.fwd(g["q"], g["k"], g["v"], g["seqlens"], g["qpos"], g["bias"], g["scale"],
-                         self.out, self.lse)
+                         self.out, self.lse, tree=g.get("tree"))
 
     def free(self):
         del self.dev, self.out, self.lse
@@ -273,8 +275,9 @@ def time_e2e(r: Runner, steps: int, warmup: int):
     -> pinned host, every step (device-timed with events)."""
     g = r.dev
     host = {k: r.cpu[k].pin_memory() for k in ("q", "k", "v", "seqlens", "qpos")}
-    if r.cpu["bias"] is not None:
-        host["bias"] = r.cpu["bias"].pin_memory()
+    for opt in ("bias", "tree"):
+        if r.cpu.get(opt) is not None:
+            host[opt] = r.cpu[opt].pin_memory()
     out_h = torch.empty(r.out.shape, dtype=r.out.dtype).pin_memory()
     lse_h = torch.empty(r.lse.shape, dtype=r.lse.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -327,7 +330,7 @@ def oracle_rate(s, inp, budget_s: float, threads: int = 0):
         rows = rng.choice(total_rows, size=n, replace=False)
         t0 = time.perf_counter()
         oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"], inp["qpos"], inp["scale"],
-                         bias=inp["bias"], rows=rows, nthreads=threads)
+                         bias=inp["bias"], rows=rows, nthreads=threads, tree=inp.get("tree"))
         spent += time.perf_counter() - t0
         done += n
         if spent >= budget_s or done >= total_rows:

@@ -25,12 +25,12 @@ ERR_NO_WORKSPACE = -5
 ERR_SCRATCH_LIMIT = -6
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
-BF16, F32, I32 = 1, 2, 3
-_DTYPES = {torch.bfloat16: BF16, torch.float32: F32, torch.int32: I32}
+BF16, F32, I32, I64 = 1, 2, 3, 4
+_DTYPES = {torch.bfloat16: BF16, torch.float32: F32, torch.int32: I32, torch.int64: I64}
 
 EXPORTED = ("blkattn_fwd", "blkattn_merge", "blkattn_status_string",
             "blkattn_check_device_error", "blkattn_debug_plan", "blkattn_debug_set_split_event",
-            "blkattn_fwd_static_scratch", "blkattn_last_cuda_error")
+            "blkattn_fwd_static_scratch", "blkattn_last_cuda_error", "blkattn_fwd_tree")
 
 
 class Tensor(ctypes.Structure):
@@ -74,6 +74,8 @@ def load(path: str = LIB_PATH):
             P = ctypes.c_void_p
             lib.blkattn_fwd.restype = ctypes.c_int
             lib.blkattn_fwd.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P]
+            lib.blkattn_fwd_tree.restype = ctypes.c_int
+            lib.blkattn_fwd_tree.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, P, P, P]
             lib.blkattn_fwd_static_scratch.restype = ctypes.c_int
             lib.blkattn_fwd_static_scratch.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P]
             lib.blkattn_merge.restype = ctypes.c_int
@@ -135,9 +137,16 @@ def _ref(x):
     return None if x is None else ctypes.byref(x)
 
 
-def fwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale: float, out, lse, stream=None):
-    """blkattn_fwd on torch CUDA tensors; out and lse are written in place."""
+def fwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale: float, out, lse, stream=None, tree=None):
+    """blkattn_fwd on torch CUDA tensors; out and lse are written in place.
+    tree: None, or int64 [B, T_q] token-tree node masks (blkattn_fwd_tree)."""
     lib = load()
+    if tree is not None:
+        descs = [describe(t) for t in (q, k, v, seqlens_k, q_logical_pos, tree, mask_bias, out, lse)]
+        st = lib.blkattn_fwd_tree(*[_ref(x) for x in descs[:7]], ctypes.c_float(scale),
+                                  _ref(descs[7]), _ref(descs[8]), _stream_handle(stream) if q.is_cuda else None)
+        _check(st)
+        return out, lse
     descs = [describe(t) for t in (q, k, v, seqlens_k, q_logical_pos, mask_bias, out, lse)]
     st = lib.blkattn_fwd(_ref(descs[0]), _ref(descs[1]), _ref(descs[2]), _ref(descs[3]),
                          _ref(descs[4]), _ref(descs[5]), ctypes.c_float(scale),
@@ -164,14 +173,15 @@ def fwd_static_scratch(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale: floa
 
 
 def attention(q, k, v, seqlens_k, q_logical_pos, mask_bias=None, scale=None,
-              out_dtype=torch.float32, stream=None):
-    """Allocate out/lse with torch and run blkattn_fwd."""
+              out_dtype=torch.float32, stream=None, tree=None):
+    """Allocate out/lse with torch and run blkattn_fwd (blkattn_fwd_tree with
+    a token tree)."""
     B, Hq, Tq, d = q.shape
     if scale is None:
         scale = d ** -0.5
     out = torch.empty((B, Hq, Tq, v.shape[3]), dtype=out_dtype, device=q.device)
     lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
-    return fwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, stream)
+    return fwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, stream, tree=tree)
 
 
 def _states(m, l, u) -> States:

@@ -342,12 +342,14 @@ struct Checked {
 };
 
 int validate_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
-                 const blkattn_tensor* sl, const blkattn_tensor* qp, const blkattn_tensor* bias,
-                 const blkattn_tensor* out, const blkattn_tensor* lse, Checked* c) {
+                 const blkattn_tensor* sl, const blkattn_tensor* qp, const blkattn_tensor* tree,
+                 const blkattn_tensor* bias, const blkattn_tensor* out, const blkattn_tensor* lse,
+                 Checked* c) {
   if (!dims_ok(q, 4) || !dims_ok(k, 4) || !dims_ok(v, 4) || !dims_ok(sl, 1) ||
       !dims_ok(qp, 2) || !dims_ok(out, 4) || !dims_ok(lse, 3))
     return BLKATTN_ERR_INVALID_ARG;
   if (bias && !dims_ok(bias, 4)) return BLKATTN_ERR_INVALID_ARG;
+  if (tree && (!dims_ok(tree, 2) || tree->dtype != BLKATTN_I64)) return BLKATTN_ERR_INVALID_ARG;
   if (!is_float_dtype(q->dtype) || k->dtype != q->dtype || v->dtype != q->dtype)
     return BLKATTN_ERR_INVALID_ARG;
   if (sl->dtype != BLKATTN_I32 || qp->dtype != BLKATTN_I32) return BLKATTN_ERR_INVALID_ARG;
@@ -371,6 +373,8 @@ int validate_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn
     return BLKATTN_ERR_INVALID_ARG;
   if (Tmax < 1 || v->sizes[2] != Tmax) return BLKATTN_ERR_INVALID_ARG;
   if (k->sizes[3] != d || v->sizes[3] != d || out->sizes[3] != d) return BLKATTN_ERR_INVALID_ARG;
+  // a token tree: one 64-bit node mask per (sequence, query row)
+  if (tree && (tree->sizes[0] != B || tree->sizes[1] != Tq || Tq > 64)) return BLKATTN_ERR_INVALID_ARG;
   if (bias) {  // each dim is full-size or 1 (a size-1 dim broadcasts)
     const int64_t full[4] = {B, Hq, Tq, Tmax};
     for (int i = 0; i < 4; ++i)
@@ -388,6 +392,7 @@ int validate_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn
     for (const blkattn_tensor* t : {q, k, v, sl, qp, out, lse})
       if (t->data == nullptr) return BLKATTN_ERR_INVALID_ARG;
     if (bias && bias->data == nullptr) return BLKATTN_ERR_INVALID_ARG;
+    if (tree && tree->data == nullptr) return BLKATTN_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(k->data) | reinterpret_cast<uintptr_t>(v->data)) % 16 != 0)
       return BLKATTN_ERR_INVALID_ARG;
   }
@@ -399,7 +404,7 @@ int validate_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn
   c->q_vec_ok = q->strides[3] == 1 && (reinterpret_cast<uintptr_t>(q->data) % 16) == 0 &&
                 (q->strides[0] * 2) % 16 == 0 && (q->strides[1] * 2) % 16 == 0 &&
                 (q->strides[2] * 2) % 16 == 0;
-  c->prefill_ok = bias == nullptr && c->q_vec_ok;
+  c->prefill_ok = bias == nullptr && tree == nullptr && c->q_vec_ok;
   return BLKATTN_OK;
 }
 
@@ -407,7 +412,8 @@ int validate_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn
 // when the plan has more than one split (m, l, u in 256-byte aligned parts).
 FwdParams fill_params(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
                       const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos,
-                      const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out,
+                      const blkattn_tensor* tree, const blkattn_tensor* mask_bias, float scale,
+                      const blkattn_tensor* out,
                       const blkattn_tensor* lse, const Checked& c, const Plan& pl, void* ws, int* err,
                       unsigned* counters) {
   const int eb = elt_bytes(q->dtype);
@@ -428,6 +434,11 @@ FwdParams fill_params(const blkattn_tensor* q, const blkattn_tensor* k, const bl
     int64_t bs[4];
     for (int i = 0; i < 4; ++i) bs[i] = mask_bias->sizes[i] == 1 ? 0 : mask_bias->strides[i];
     p.bi_sb = bs[0]; p.bi_sh = bs[1]; p.bi_si = bs[2]; p.bi_sj = bs[3];
+  }
+  if (tree) {
+    p.tree = static_cast<const int64_t*>(tree->data);
+    p.tr_sb = tree->strides[0];
+    p.tr_si = tree->strides[1];
   }
   p.scale_log2 = scale * 1.4426950408889634f;
   p.out = out->data;
@@ -544,18 +555,18 @@ int validate_fwd_args(const blkattn_tensor* q, const blkattn_tensor* k, const bl
                       const blkattn_tensor* mask_bias, const blkattn_tensor* out,
                       const blkattn_tensor* lse) {
   Checked c;
-  return validate_fwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, out, lse, &c);
+  return validate_fwd(q, k, v, seqlens_k, q_logical_pos, nullptr, mask_bias, out, lse, &c);
 }
 
 // blkattn_fwd with caller-provided scratch for the per-split states instead
 // of the library's grow-only workspace.  Never allocates device memory.
 int fwd_with_scratch(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
                      const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos,
-                     const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out,
-                     const blkattn_tensor* lse, blkattn_stream_t stream_, void* scratch,
-                     size_t scratch_bytes) {
+                     const blkattn_tensor* tree, const blkattn_tensor* mask_bias, float scale,
+                     const blkattn_tensor* out, const blkattn_tensor* lse, blkattn_stream_t stream_,
+                     void* scratch, size_t scratch_bytes) {
   Checked c;
-  int st = validate_fwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, out, lse, &c);
+  int st = validate_fwd(q, k, v, seqlens_k, q_logical_pos, tree, mask_bias, out, lse, &c);
   if (st != BLKATTN_OK) return st;
   if (c.B == 0 || c.Tq == 0) return BLKATTN_OK;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -575,8 +586,42 @@ int fwd_with_scratch(const blkattn_tensor* q, const blkattn_tensor* k, const blk
   if ((size_t)pl.ws_bytes > usable) return BLKATTN_ERR_SCRATCH_LIMIT;
   if ((size_t)pl.units * sizeof(unsigned) > blkattn::kStaticCounterBytes) return BLKATTN_ERR_SCRATCH_LIMIT;
   unsigned* counters = reinterpret_cast<unsigned*>(static_cast<char*>(scratch) + usable);
-  const FwdParams p = fill_params(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, c, pl,
-                                  scratch, ds->err, counters);
+  const FwdParams p = fill_params(q, k, v, seqlens_k, q_logical_pos, tree, mask_bias, scale, out, lse, c,
+                                  pl, scratch, ds->err, counters);
+  return launch_fwd(p, c, pl, q, k, v, out, stream);
+}
+
+// blkattn_fwd and blkattn_fwd_tree: the library's grow-only workspace and
+// per-unit counters.
+int fwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
+             const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos, const blkattn_tensor* tree,
+             const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out, const blkattn_tensor* lse,
+             blkattn_stream_t stream_) {
+  Checked c;
+  int st = validate_fwd(q, k, v, seqlens_k, q_logical_pos, tree, mask_bias, out, lse, &c);
+  if (st != BLKATTN_OK) return st;
+  if (c.B == 0 || c.Tq == 0) return BLKATTN_OK;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != BLKATTN_OK) return st;
+  const Plan pl = make_plan(c.B, c.Hq, c.Hkv, c.Tq, c.Tmax, (int)c.d, c.elt, ds->sms,
+                            c.prefill_ok && scale > 0.f, c.q_vec_ok);
+  if ((pl.cfg.kernel == blkattn::Kernel::TensorCore || pl.cfg.kernel == blkattn::Kernel::CudaCore) &&
+      c.B * pl.cfg.row_groups > 65535)
+    return BLKATTN_ERR_UNSUPPORTED;  // grid z of the split-KV kernels
+  if (pl.ws_bytes > 0) {
+    st = ensure_workspace(ds, (size_t)pl.ws_bytes, stream);
+    if (st != BLKATTN_OK) return st;
+  }
+  if (pl.units > 0) {
+    st = ensure_counters(ds, pl.units, stream);
+    if (st != BLKATTN_OK) return st;
+  }
+  const FwdParams p = fill_params(q, k, v, seqlens_k, q_logical_pos, tree, mask_bias, scale, out, lse, c, pl,
+                                  ds->ws, ds->err, ds->cnt);
   return launch_fwd(p, c, pl, q, k, v, out, stream);
 }
 
@@ -619,32 +664,15 @@ int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_
                 const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos,
                 const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out,
                 const blkattn_tensor* lse, blkattn_stream_t stream_) {
-  Checked c;
-  int st = validate_fwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, out, lse, &c);
-  if (st != BLKATTN_OK) return st;
-  if (c.B == 0 || c.Tq == 0) return BLKATTN_OK;
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  return blkattn::fwd_impl(q, k, v, seqlens_k, q_logical_pos, nullptr, mask_bias, scale, out, lse, stream_);
+}
 
-  std::lock_guard<std::mutex> lock(g_mu);
-  DeviceState* ds = nullptr;
-  st = device_state(&ds);
-  if (st != BLKATTN_OK) return st;
-  const Plan pl = make_plan(c.B, c.Hq, c.Hkv, c.Tq, c.Tmax, (int)c.d, c.elt, ds->sms,
-                            c.prefill_ok && scale > 0.f, c.q_vec_ok);
-  if ((pl.cfg.kernel == blkattn::Kernel::TensorCore || pl.cfg.kernel == blkattn::Kernel::CudaCore) &&
-      c.B * pl.cfg.row_groups > 65535)
-    return BLKATTN_ERR_UNSUPPORTED;  // grid z of the split-KV kernels
-  if (pl.ws_bytes > 0) {
-    st = ensure_workspace(ds, (size_t)pl.ws_bytes, stream);
-    if (st != BLKATTN_OK) return st;
-  }
-  if (pl.units > 0) {
-    st = ensure_counters(ds, pl.units, stream);
-    if (st != BLKATTN_OK) return st;
-  }
-  const FwdParams p = fill_params(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, c, pl,
-                                  ds->ws, ds->err, ds->cnt);
-  return launch_fwd(p, c, pl, q, k, v, out, stream);
+int blkattn_fwd_tree(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
+                     const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos,
+                     const blkattn_tensor* tree_mask, const blkattn_tensor* mask_bias, float scale,
+                     const blkattn_tensor* out, const blkattn_tensor* lse, blkattn_stream_t stream_) {
+  if (tree_mask == nullptr) return BLKATTN_ERR_INVALID_ARG;
+  return blkattn::fwd_impl(q, k, v, seqlens_k, q_logical_pos, tree_mask, mask_bias, scale, out, lse, stream_);
 }
 
 int blkattn_merge(const blkattn_states* a, const blkattn_states* b, const blkattn_states* out,

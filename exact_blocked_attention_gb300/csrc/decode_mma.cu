@@ -217,6 +217,10 @@ __global__ void __maxnreg__((mma_max_regs<MT, NWK>()))
     const int r1 = r0 + 8;
     const int hi0 = min(row_end_s[r0], k0 + p.chunk);
     const int hi1 = min(row_end_s[r1], k0 + p.chunk);
+    // token tree: keys from tbase on are seen only where the row's mask says
+    const int tbase = p.tree != nullptr ? len - p.Tq : 0x7fffffff;
+    const uint64_t tr0 = p.tree != nullptr ? (uint64_t)p.tree[(int64_t)b * p.tr_sb + (int64_t)row_i_s[r0] * p.tr_si] : ~0ull;
+    const uint64_t tr1 = p.tree != nullptr ? (uint64_t)p.tree[(int64_t)b * p.tr_sb + (int64_t)row_i_s[r1] * p.tr_si] : ~0ull;
     const float* bias0 = nullptr;
     const float* bias1 = nullptr;
     if (p.bias != nullptr) {
@@ -271,6 +275,11 @@ __global__ void __maxnreg__((mma_max_regs<MT, NWK>()))
         for (int e = 0; e < 2; ++e) {
           const int key = key_base + nt * 8 + 2 * t + e;
           bool v0 = key < hi0, v1 = key < hi1;
+          if (key >= tbase) {
+            const int node = key - tbase;
+            v0 = v0 && node < 64 && ((tr0 >> (node & 63)) & 1ull);
+            v1 = v1 && node < 64 && ((tr1 >> (node & 63)) & 1ull);
+          }
           float bb0 = 0.f, bb1 = 0.f;
           if (bias0 != nullptr) {
             if (v0) { bb0 = bias0[(int64_t)key * p.bi_sj]; v0 = bb0 != kNegInf; }

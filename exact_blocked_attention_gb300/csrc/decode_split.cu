@@ -234,6 +234,12 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     int row_hi[R];               // split-local end of the visible range per row
 #pragma unroll
     for (int r = 0; r < R; ++r) row_hi[r] = min(row_end[r], k0 + p.chunk);
+    // token tree: keys from tbase on are seen only where the row's mask says
+    const int tbase = p.tree != nullptr ? len - p.Tq : 0x7fffffff;
+    uint64_t row_tree[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      row_tree[r] = p.tree != nullptr ? (uint64_t)p.tree[(int64_t)b * p.tr_sb + (int64_t)row_i[r] * p.tr_si] : ~0ull;
 
     for (int t = 0; t < n_tiles; ++t) {
       const int st = t % STAGES;
@@ -275,6 +281,10 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       for (int r = 0; r < R; ++r) {
         acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], 16);
         bool vis = key < row_hi[r];
+        if (key >= tbase) {
+          const int node = key - tbase;
+          vis = vis && node < 64 && ((row_tree[r] >> (node & 63)) & 1ull);
+        }
         float bias = 0.f;
         if (p.bias != nullptr && vis) {
           bias = p.bias[(int64_t)b * p.bi_sb + (int64_t)row_h[r] * p.bi_sh +

@@ -102,10 +102,12 @@ struct RowFacts {
   int64_t boff[NR];  // bias row offsets (elements)
   int64_t ooff[NR];  // output row offsets
   int64_t loff[NR];  // lse offsets
+  uint64_t tree[NR]; // token tree: bit k = the row sees key tree_base + k (all ones without a tree)
   int end[NR];       // visible keys are [0, end): min(len, pos + 1), 0 for padding rows
   int unit_end;      // max over the rows
   int min_end;       // min over the real rows
-  int pad[2];
+  int tree_base;     // first key of the token tree (len - T_q); INT_MAX without a tree
+  int pad;
 };
 
 template <int NR>
@@ -548,9 +550,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (r >= NR) break;
         int e = 0;
         int64_t bo = 0, oo = 0, lo = 0;
+        uint64_t tr = ~0ull;
         if (real[h2]) {
           const int h = hrow[h2], i = irow[h2];
           e = pos[h2] < 0 ? 0 : min(pos[h2] + 1, len);
+          if (p.tree != nullptr) tr = (uint64_t)p.tree[(int64_t)b * p.tr_sb + (int64_t)i * p.tr_si];
           bo = (int64_t)b * p.bi_sb + (int64_t)h * p.bi_sh + (int64_t)i * p.bi_si;
           oo = (int64_t)b * p.o_sb + (int64_t)h * p.o_sh + (int64_t)i * p.o_si;
           lo = (int64_t)b * p.l_sb + (int64_t)h * p.l_sh + (int64_t)i * p.l_si;
@@ -558,6 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umax = max(umax, e);
         rf.end[r] = e;
+        rf.tree[r] = tr;
         rf.boff[r] = bo;
         rf.ooff[r] = oo;
         rf.loff[r] = lo;
@@ -570,6 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         rf.unit_end = umax;
         rf.min_end = umin;
+        rf.tree_base = p.tree != nullptr ? len - p.Tq : 0x7fffffff;
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q rows -> tensor core
       __syncwarp();
@@ -880,6 +886,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int r = 0; r < NH; ++r)
             if (key >= rf.end[c0 + r]) x[r] = kNegInf;
+        }
+        if (key0 + BK > rf.tree_base) {
+          // token tree: inside it a row sees only the nodes of its mask
+          const int node = key - rf.tree_base;
+          if (node >= 0 && node < 64) {
+#pragma unroll
+            for (int r = 0; r < NH; ++r)
+              if (!((rf.tree[c0 + r] >> node) & 1ull)) x[r] = kNegInf;
+          }
         }
 #pragma unroll
         for (int r4 = 0; r4 < NH / 4; ++r4) {

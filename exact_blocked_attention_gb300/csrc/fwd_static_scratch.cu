@@ -73,6 +73,6 @@ extern "C" int blkattn_fwd_static_scratch(const blkattn_tensor* q, const blkattn
   void* scratch = nullptr;
   st = scratch_address(&scratch);
   if (st != BLKATTN_OK) return st;
-  return blkattn::fwd_with_scratch(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, stream,
-                                   scratch, kScratchBytes);
+  return blkattn::fwd_with_scratch(q, k, v, seqlens_k, q_logical_pos, nullptr, mask_bias, scale, out, lse,
+                                   stream, scratch, kScratchBytes);
 }

@@ -32,6 +32,11 @@ struct FwdParams {
   // optional additive bias (device f32), 0-strides broadcast
   const float* bias;
   int64_t bi_sb, bi_sh, bi_si, bi_sj;
+  // optional token tree (device int64 [B, T_q], T_q <= 64): bit k of
+  // tree[b, i] lets row i see key len_b - T_q + k; keys before len_b - T_q
+  // are not affected
+  const int64_t* tree;
+  int64_t tr_sb, tr_si;
   float scale_log2;  // scale * log2(e): scores are kept in base-2 units
   // results
   void* out;
@@ -129,8 +134,13 @@ int validate_fwd_args(const blkattn_tensor* q, const blkattn_tensor* k, const bl
                       const blkattn_tensor* lse);
 int fwd_with_scratch(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
                      const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos,
-                     const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out,
-                     const blkattn_tensor* lse, blkattn_stream_t stream, void* scratch,
-                     size_t scratch_bytes);
+                     const blkattn_tensor* tree, const blkattn_tensor* mask_bias, float scale,
+                     const blkattn_tensor* out, const blkattn_tensor* lse, blkattn_stream_t stream,
+                     void* scratch, size_t scratch_bytes);
+// blkattn_fwd / blkattn_fwd_tree (tree may be NULL) on the library's workspace.
+int fwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
+             const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos, const blkattn_tensor* tree,
+             const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out, const blkattn_tensor* lse,
+             blkattn_stream_t stream);
 
 }  // namespace blkattn

@@ -22,6 +22,11 @@ additive bias M_j, grouped heads, and the cached-decoding positions of
                 random 128-key blocks of 10% of the sequences and every key of
                 1% of the (sequence, row) pairs, bf16
   prefill       batch 2, 32 heads (MHA), d=128, T_q=T_k=8192, row i at i, bf16
+  tree_verify   spec_verify's batch, heads, cache lengths and values with a
+                token tree of T_q=6 draft nodes per sequence ("推理加速算法"
+                §7.2.2 Medusa, tree attention verification): seeded random
+                parents, every row at len-1 and the tree region shaped by
+                ancestor masks, no bias
 
 Each has a reduced twin (``small=True``) that the fp64 oracle finishes in
 seconds while still spanning several key tiles and a ragged tail.
@@ -58,6 +63,7 @@ class Spec:
     bias_block: int = 128
     bias_block_frac: float = 0.0
     masked_row_frac: float = 0.0
+    tree: str = "none"           # "none" | "random" (token tree of T_q nodes per sequence)
     notes: str = field(default="", compare=False)
 
     @property
@@ -78,6 +84,10 @@ SPECS = {
                         bias="verify_blocks", bias_seq_frac=0.10, bias_block=128, bias_block_frac=0.10,
                         masked_row_frac=0.01),
     "prefill": Spec("prefill", 2, 32, 32, 8192, 8192, 128, "bf16", ("fixed", 8192), "causal", 5),
+    # spec_verify's seed: the same cache lengths and values, a 6-node tree in
+    # place of the 5-row chain and the bias
+    "tree_verify": Spec("tree_verify", 8, 64, 8, 6, 32774, 128, "bf16", ("verify", 1024, 32768), "tree", 3,
+                        tree="random"),
 }
 
 # Reduced twins: same structure, sizes the fp64 oracle covers in seconds, still
@@ -89,6 +99,7 @@ SMALL = {
     "spec_verify": replace(SPECS["spec_verify"], B=3, Hq=16, Hkv=2, Tmax=1290,
                            lens=("verify", 300, 1285), bias_seq_frac=0.34, masked_row_frac=0.07),
     "prefill": replace(SPECS["prefill"], B=1, Hq=2, Hkv=2, Tq=333, Tmax=333, lens=("fixed", 333)),
+    "tree_verify": replace(SPECS["tree_verify"], B=3, Hq=16, Hkv=2, Tmax=1290, lens=("verify", 300, 1284)),
 }
 
 
@@ -121,7 +132,8 @@ def generate(s: Spec, poison_padding: float | None = None) -> dict:
     """Draw one batch of inputs for workload ``s`` on the CPU.
 
     Returns q, k, v (torch, bf16 or f32), seqlens int32 [B], qpos int32 [B,T_q],
-    bias (float32 [B,1,T_q,T_max] or None), scale, and the spec.  Cache rows
+    bias (float32 [B,1,T_q,T_max] or None), tree (int64 [B,T_q] node masks or
+    None), scale, and the spec.  Cache rows
     at or beyond a sequence's length are drawn like the rest unless
     ``poison_padding`` is given (e.g. float('nan')), in which case they hold it.
     """
@@ -145,6 +157,8 @@ def generate(s: Spec, poison_padding: float | None = None) -> dict:
         qpos = (lens - s.Tq)[:, None] + np.arange(s.Tq)[None, :]
     elif s.pos == "causal":
         qpos = np.broadcast_to(np.arange(s.Tq)[None, :], (s.B, s.Tq)).copy()
+    elif s.pos == "tree":  # the whole cache; the tree masks shape the tree region
+        qpos = (lens - 1)[:, None] + np.zeros((1, s.Tq), dtype=np.int64)
     else:
         raise ValueError(s.pos)
 
@@ -173,6 +187,23 @@ def generate(s: Spec, poison_padding: float | None = None) -> dict:
         for flat in rng.choice(s.B * s.Tq, size=n_rows, replace=False):
             bias[flat // s.Tq, 0, flat % s.Tq, :] = -np.inf
 
+    tree = None
+    if s.tree == "random":
+        # per sequence a tree of T_q nodes: node 0 the root, node k's parent
+        # uniform over the earlier nodes; bit k of a row's mask = node k is
+        # the row's node or one of its ancestors
+        tree = np.zeros((s.B, s.Tq), dtype=np.int64)
+        for b in range(s.B):
+            parent = [-1] + [int(rng.integers(0, k)) for k in range(1, s.Tq)]
+            for i in range(s.Tq):
+                m, node = 0, i
+                while node >= 0:
+                    m |= 1 << node
+                    node = parent[node]
+                tree[b, i] = m - (1 << 64) if m >= 1 << 63 else m
+    elif s.tree != "none":
+        raise ValueError(s.tree)
+
     return {
         "q": _cast(q, s.dtype),
         "k": _cast(k, s.dtype),
@@ -180,6 +211,7 @@ def generate(s: Spec, poison_padding: float | None = None) -> dict:
         "seqlens": torch.from_numpy(lens.astype(np.int32)),
         "qpos": torch.from_numpy(qpos.astype(np.int32)),
         "bias": None if bias is None else torch.from_numpy(bias),
+        "tree": None if tree is None else torch.from_numpy(tree),
         "scale": s.scale,
         "spec": s,
     }

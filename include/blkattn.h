@@ -63,7 +63,8 @@ enum {
 enum {
   BLKATTN_BF16 = 1,  /* bfloat16 */
   BLKATTN_F32 = 2,   /* IEEE binary32 */
-  BLKATTN_I32 = 3    /* int32 */
+  BLKATTN_I32 = 3,   /* int32 */
+  BLKATTN_I64 = 4    /* int64 (token-tree node masks) */
 };
 
 /*
@@ -72,7 +73,7 @@ enum {
  */
 typedef struct {
   void* data;
-  int32_t dtype;      /* BLKATTN_BF16 | BLKATTN_F32 | BLKATTN_I32 */
+  int32_t dtype;      /* BLKATTN_BF16 | BLKATTN_F32 | BLKATTN_I32 | BLKATTN_I64 */
   int32_t ndim;
   int64_t sizes[4];
   int64_t strides[4];
@@ -114,6 +115,37 @@ int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k,
                 const blkattn_tensor* mask_bias, float scale,
                 const blkattn_tensor* out, const blkattn_tensor* lse,
                 blkattn_stream_t stream);
+
+/*
+ * blkattn_fwd_tree — blkattn_fwd for a token tree of draft rows.
+ *
+ * "推理加速算法" (inference acceleration algorithms) §7.2.2 Medusa, tree
+ * attention verification: a tree of candidate continuations is verified in
+ * one pass, every node attending to the cached prefix and to its own
+ * ancestors, never to another branch.
+ *
+ * Arguments as blkattn_fwd, plus
+ * tree_mask     int64 [B, T_q], any strides, device (required; T_q <= 64).
+ *               The T_q query rows of sequence b are the tree's nodes and
+ *               the last T_q cache entries [len_b - T_q, len_b) hold their
+ *               keys, node k at key len_b - T_q + k.  Bit k of
+ *               tree_mask[b, i] set = row i sees node k (normally its
+ *               ancestors and itself).
+ * Visibility of key j for row (b, h, i): j < len_b, j <= q_logical_pos[b, i]
+ * (pass len_b - 1 to leave the tree region to the mask), the bias is not
+ * -inf, and either j < len_b - T_q or bit (j - len_b + T_q) of
+ * tree_mask[b, i] is set.  Bits for nodes at or past len_b are ignored.
+ * Served by the decode/verify kernels (never the prefill kernel).
+ * Returns as blkattn_fwd; BLKATTN_ERR_INVALID_ARG also for a NULL tree_mask,
+ * a dtype other than BLKATTN_I64, sizes other than [B, T_q] or T_q > 64.
+ */
+int blkattn_fwd_tree(const blkattn_tensor* q, const blkattn_tensor* k,
+                     const blkattn_tensor* v, const blkattn_tensor* seqlens_k,
+                     const blkattn_tensor* q_logical_pos,
+                     const blkattn_tensor* tree_mask,
+                     const blkattn_tensor* mask_bias, float scale,
+                     const blkattn_tensor* out, const blkattn_tensor* lse,
+                     blkattn_stream_t stream);
 
 /*
  * blkattn_fwd_static_scratch — blkattn_fwd that allocates no device memory.

@@ -58,7 +58,7 @@ class FakeTensor:
     def desc(self):
         d = blkattn.Tensor()
         d.data = self.addr
-        d.dtype = {torch.bfloat16: 1, torch.float32: 2, torch.int32: 3}[self.dtype]
+        d.dtype = {torch.bfloat16: 1, torch.float32: 2, torch.int32: 3, torch.int64: 4}[self.dtype]
         d.ndim = len(self.shape)
         for i, (s, st) in enumerate(zip(self.shape, self.strides)):
             d.sizes[i] = s
@@ -108,6 +108,37 @@ def test_invalid_requests_are_rejected_before_cuda(lib, mutate, expect):
     a = good_args()
     mutate(a)
     assert call_fwd(lib, a["q"], a["k"], a["v"], a["sl"], a["qp"], a["bias"], a["out"], a["lse"]) == expect
+
+
+def call_fwd_tree(lib, q, k, v, sl, qp, tree, bias, out, lse):
+    ds = [None if t is None else t.desc() for t in (q, k, v, sl, qp, tree, bias, out, lse)]
+    ref = lambda d: None if d is None else ctypes.byref(d)
+    return lib.blkattn_fwd_tree(*[ref(x) for x in ds[:7]], ctypes.c_float(0.1), ref(ds[7]), ref(ds[8]), None)
+
+
+@pytest.mark.parametrize("tree,expect", [
+    (None, -1),                                                  # the tree is required
+    (FakeTensor((2, 3), torch.int32), -1),                       # masks are int64
+    (FakeTensor((2, 4), torch.int64), -1),                       # [B, T_q]
+    (FakeTensor((3, 3), torch.int64), -1),
+    (FakeTensor((2, 3, 1), torch.int64), -1),
+    (FakeTensor((2, 3), torch.int64, addr=0), -1),               # NULL data
+], ids=["missing", "int32", "tq", "batch", "ndim", "null-data"])
+def test_tree_requests_are_validated_before_cuda(lib, tree, expect):
+    a = good_args()
+    assert call_fwd_tree(lib, a["q"], a["k"], a["v"], a["sl"], a["qp"], tree, None, a["out"], a["lse"]) == expect
+
+
+def test_tree_needs_at_most_64_rows(lib):
+    a = good_args(Tq=65)
+    tree = FakeTensor((2, 65), torch.int64)
+    assert call_fwd_tree(lib, a["q"], a["k"], a["v"], a["sl"], a["qp"], tree, None, a["out"], a["lse"]) == -1
+    e = good_args(B=0)
+    for t in e.values():
+        if t is not None:
+            t.addr = 0
+    empty_tree = FakeTensor((0, 3), torch.int64, addr=0)
+    assert call_fwd_tree(lib, e["q"], e["k"], e["v"], e["sl"], e["qp"], empty_tree, None, e["out"], e["lse"]) == 0
 
 
 def test_empty_problem_is_a_no_op(lib):

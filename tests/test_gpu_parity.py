@@ -39,7 +39,7 @@ def to_dev(inp):
 def run_gpu(inp, out_dtype=torch.float32):
     g = to_dev(inp)
     out, lse = blkattn.attention(g["q"], g["k"], g["v"], g["seqlens"], g["qpos"], g["bias"],
-                                 g["scale"], out_dtype=out_dtype)
+                                 g["scale"], out_dtype=out_dtype, tree=g.get("tree"))
     torch.cuda.synchronize()
     assert blkattn.check_device_error() == 0
     d = out.shape[-1]
@@ -48,7 +48,7 @@ def run_gpu(inp, out_dtype=torch.float32):
 
 def run_oracle(inp, rows=None):
     return oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"], inp["qpos"], inp["scale"],
-                            bias=inp["bias"], rows=rows)
+                            bias=inp["bias"], rows=rows, tree=inp.get("tree"))
 
 
 def assert_parity(o, l, ref, tol_o, tol_l, out_raw=None, bf16_out=False):
@@ -125,7 +125,7 @@ def sample_rows(s, inp, n_random=160, seed=0):
     return np.array(sorted(rows), dtype=np.int64)
 
 
-@pytest.mark.parametrize("name", ["decode_gqa", "long_decode", "spec_verify", "prefill"])
+@pytest.mark.parametrize("name", ["decode_gqa", "long_decode", "spec_verify", "prefill", "tree_verify"])
 def test_full_size_workload_sampled_rows(name):
     s = workloads.spec(name)
     inp = workloads.generate(s)
@@ -348,6 +348,90 @@ def test_empty_calls_are_no_ops():
     blkattn.fwd(z(inp["q"]), z(inp["k"]), z(inp["v"]), z(inp["seqlens"]), z(inp["qpos"]), None, 0.1, out, lse)
     torch.cuda.synchronize()
     assert blkattn.check_device_error() == 0
+
+
+# ------------------------------------------------------------ token-tree verification
+# "推理加速算法" (inference acceleration algorithms) §7.2.2 Medusa, tree
+# attention verification: rows are tree nodes whose keys are the last T_q
+# cache entries; each sees the prefix and its ancestors (blkattn_fwd_tree).
+
+def _tree_masks(parents_per_seq):
+    out = []
+    for parents in parents_per_seq:
+        row = []
+        for i in range(len(parents)):
+            m, node = 0, i
+            while node >= 0:
+                m |= 1 << node
+                node = parents[node]
+            row.append(m - (1 << 64) if m >= 1 << 63 else m)
+        out.append(row)
+    return torch.tensor(out, dtype=torch.int64)
+
+
+def tree_case(name):
+    rng = np.random.default_rng(["nr48", "nr32_two_groups", "nr16", "d64_mma", "fp32_split",
+                                 "short_cache", "with_bias", "deep64"].index(name) + 40)
+    dtype, d, bias = "bf16", 128, None
+    if name == "nr48":              # 8 heads x 6 nodes = 48 rows per KV head
+        B, Hq, Hkv, Tq, lens = 3, 16, 2, 6, [700, 1290, 301]
+    elif name == "nr32_two_groups":  # 64 nodes, G = 1: two row groups of 32
+        B, Hq, Hkv, Tq, lens = 2, 2, 2, 64, [900, 640]
+    elif name == "nr16":             # 2 heads x 8 nodes = 16 rows
+        B, Hq, Hkv, Tq, lens = 2, 4, 2, 8, [333, 1024]
+    elif name == "d64_mma":          # head dim 64: the mma.sync split kernel
+        B, Hq, Hkv, Tq, lens, d = 2, 8, 2, 10, [512, 777], 64
+    elif name == "fp32_split":       # fp32: the CUDA-core split kernel
+        B, Hq, Hkv, Tq, lens, dtype, d = 2, 4, 2, 7, [260, 515], "f32", 64
+    elif name == "short_cache":      # cache shorter than the tree: early nodes have no key
+        B, Hq, Hkv, Tq, lens = 2, 8, 2, 12, [5, 12]
+    elif name == "with_bias":        # tree and an additive -inf bias together
+        B, Hq, Hkv, Tq, lens = 2, 8, 2, 6, [400, 130]
+    else:                            # deep64: a 64-node chain-heavy tree over 3 row groups
+        B, Hq, Hkv, Tq, lens = 1, 4, 2, 64, [3000]
+    Tmax = max(lens) + 3
+    parents = [[-1] + [int(rng.integers(max(0, k - 3) if name == "deep64" else 0, k)) for k in range(1, Tq)]
+               for _ in range(B)]
+    qpos = [[ln - 1] * Tq for ln in lens]
+    if name == "with_bias":
+        bias = torch.zeros(B, 1, Tq, Tmax)
+        bias[0, 0, :, 100:230] = -math.inf
+        bias[1, 0, 2, :] = -math.inf  # one node sees nothing
+    inp = make_case(B, Hq, Hkv, Tq, Tmax, d, dtype, lens, qpos, bias=bias, seed=int(rng.integers(1 << 30)))
+    inp["tree"] = _tree_masks(parents)
+    return inp
+
+
+TREE_CASES = ["nr48", "nr32_two_groups", "nr16", "d64_mma", "fp32_split", "short_cache", "with_bias", "deep64"]
+
+
+@pytest.mark.parametrize("name", TREE_CASES)
+def test_tree_verify_cases(name):
+    inp = tree_case(name)
+    expect = {"d64_mma": 1, "fp32_split": 0}.get(name, 3)  # the kernel each case is for
+    if inp["q"].shape[2] < 64:  # (the debug plan has no tree flag: with 64 rows it names prefill,
+        assert plan_of(inp)["kernel"] == expect  # which tree calls never take)
+    _, _, o, l = run_gpu(inp)
+    ref = run_oracle(inp)
+    tol = (F32_TOL, F32_TOL) if inp["q"].dtype == torch.float32 else (BF16_TOL_O, BF16_TOL_L)
+    assert_parity(o, l, ref, *tol)
+
+
+def test_tree_chain_equals_causal_verify_bitwise():
+    """A chain tree with every row at len-1 masks exactly the keys causal
+    verification (row i at len - T_q + i) masks: same plan, same bits."""
+    B, Hq, Hkv, Tq = 3, 16, 2, 6
+    lens = [800, 1290, 1030]
+    Tmax = 1290
+    chain = [[-1] + list(range(Tq - 1))] * B
+    full = make_case(B, Hq, Hkv, Tq, Tmax, 128, "bf16", lens, [[ln - 1] * Tq for ln in lens], seed=77)
+    causal = dict(full)
+    causal["qpos"] = torch.tensor([[ln - Tq + i for i in range(Tq)] for ln in lens], dtype=torch.int32)
+    full["tree"] = _tree_masks(chain)
+    raw_t, lse_t, _, _ = run_gpu(full)
+    raw_c, lse_c, _, _ = run_gpu(causal)
+    assert torch.equal(raw_t, raw_c)
+    assert torch.equal(lse_t, lse_c)
 
 
 # ------------------------------------------------------------ tcgen05 prefill kernel
