@@ -19,6 +19,10 @@ Contents
                    verification), pinned by brute force over random trees.
   states           the sufficient statistics (m, l, u) of eq. 33.3, the merge
                    rule of eqs. 33.4–33.5 and Algorithm 33.1, in numpy fp64.
+  spec_sampling    speculative-sampling acceptance and residual sampling
+                   (§33.5 eqs. 33.10–33.13, the in-order rule of §33.6),
+                   pinned by tests/test_spec_sampling_pins.py against
+                   Example 25.2 and Exercises 33.7 and 33.9.
 """
 from __future__ import annotations
 

@@ -1,0 +1,109 @@
+"""Speculative-sampling acceptance and residual sampling — TEST INFRASTRUCTURE ONLY.
+
+Plain numpy statement of "Chapter 33: inference compute optimisation" §33.5
+(eqs. 33.10–33.13) and the in-order rule of §33.6.  Only ``tests/``,
+``__graft_entry__.smoke()`` and ``bench.py``'s CPU legs may import it; it
+shares no code with the CUDA library.
+
+Distributions (fp64, the formulas as printed):
+  a(x)  = min(1, p(x)/q(x))                      eq. 33.10 (q(x) > 0)
+  A     = sum_x min(p(x), q(x)) = 1 - TV(p, q)   eq. 33.11
+  r(x)  = [p(x) - q(x)]_+ / Z,  Z = 1 - A        eq. 33.12 (not formed when Z = 0)
+  out   = min(p, q) + Z r = p                    eq. 33.13
+
+One verification step (the integer decisions the kernel must reproduce):
+  candidates x_1..x_k are taken in order; x_i is accepted iff
+  u_i * q_i(x_i) < p_i(x_i), evaluated in fp64 (exact for fp32 inputs:
+  a 24-bit by 24-bit product), which is u_i < a(x_i) for u_i in [0, 1).
+  At the first rejection the emitted token is drawn from the residual of
+  that position; if every candidate is accepted it is drawn from the next
+  target distribution p_{k+1}.  The draw is an inverse CDF in fixed point:
+  weights w(x) = floor(m(x) * 2^40) of the mass m (the positive difference
+  p - q computed in fp64, or p itself), integer prefix sums C, Z_int = C(V-1),
+  threshold T = floor(s * Z_int / 2^32) for the 32-bit uniform integer s, and
+  the token is the smallest x with C(x) > T.  Integer sums make the choice
+  independent of summation order.  When a rejection meets a zero residual
+  (Z_int = 0, which eq. 33.12 leaves unformed: rejection then has probability
+  zero) the candidate is accepted instead.  A candidate with q_i(x_i) = 0
+  cannot have been proposed; it is rejected.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+FIX_BITS = 40  # fractional bits of the fixed-point weights
+
+
+def acceptance(p, q):
+    """Eqs. 33.10–33.13 for one pair of distributions (1-D arrays, fp64).
+    Returns dict(a, accepted_mass, A, Z, residual (None when Z == 0), out)."""
+    p = np.asarray(p, dtype=np.float64)
+    q = np.asarray(q, dtype=np.float64)
+    a = np.where(q > 0, np.minimum(1.0, np.divide(p, q, out=np.zeros_like(p), where=q > 0)), 0.0)
+    accepted = np.minimum(p, q)                  # q(x) a(x)
+    A = float(accepted.sum())                    # eq. 33.11, first form
+    pos = np.maximum(p - q, 0.0)
+    Z = float(pos.sum())                         # equals 1 - A when both sum to 1
+    residual = None if Z == 0.0 else pos / Z     # eq. 33.12
+    out = accepted + (0.0 if residual is None else Z * residual)  # eq. 33.13
+    return {"a": a, "accepted_mass": accepted, "A": A, "Z": Z, "residual": residual, "out": out}
+
+
+def weights(mass_row) -> np.ndarray:
+    """Fixed-point weights floor(m * 2^40) (int64) of a non-negative fp64 row."""
+    m = np.asarray(mass_row, dtype=np.float64)
+    return np.floor(m * float(1 << FIX_BITS)).astype(np.int64)
+
+
+def inverse_cdf(w: np.ndarray, s: int) -> int:
+    """Smallest x with C(x) > floor(s * Z / 2^32), C the prefix sums of w."""
+    Z = int(w.sum())
+    T = (int(s) * Z) >> 32
+    c = 0
+    for x, wx in enumerate(w.tolist()):
+        c += int(wx)
+        if c > T:
+            return x
+    raise ValueError("empty distribution")
+
+
+def verify_step(p, q, draft, u_accept, u_sample):
+    """One speculative verification step per row.
+
+    p float32 [B, k+1, V] target probabilities, q float32 [B, k, V] draft
+    probabilities, draft int32 [B, k] candidates, u_accept float32 [B, k] in
+    [0, 1), u_sample uint32 [B].  Returns (n_accepted int32 [B], token
+    int32 [B]): the number of candidates kept and the token emitted after them.
+    """
+    p = np.asarray(p, dtype=np.float32)
+    q = np.asarray(q, dtype=np.float32)
+    draft = np.asarray(draft, dtype=np.int64)
+    u_accept = np.asarray(u_accept, dtype=np.float32)
+    u_sample = np.asarray(u_sample, dtype=np.uint64)
+    B, k1, V = p.shape
+    k = k1 - 1
+    n_acc = np.zeros(B, dtype=np.int32)
+    token = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        chosen = None
+        i = 0
+        while i < k:
+            x = int(draft[b, i])
+            px = float(p[b, i, x])
+            qx = float(q[b, i, x])
+            if qx > 0.0 and float(u_accept[b, i]) * qx < px:
+                i += 1
+                continue
+            # rejected: the residual of position i
+            m = np.maximum(p[b, i].astype(np.float64) - q[b, i].astype(np.float64), 0.0)
+            w = weights(m)
+            if int(w.sum()) == 0:  # rejection has probability zero here: keep the candidate
+                i += 1
+                continue
+            chosen = inverse_cdf(w, int(u_sample[b]))
+            break
+        if chosen is None:  # every candidate kept: the next target distribution
+            chosen = inverse_cdf(weights(p[b, k].astype(np.float64)), int(u_sample[b]))
+        n_acc[b] = i
+        token[b] = chosen
+    return n_acc, token
