@@ -18,14 +18,20 @@ One verification step (the integer decisions the kernel must reproduce):
   At the first rejection the emitted token is drawn from the residual of
   that position; if every candidate is accepted it is drawn from the next
   target distribution p_{k+1}.  The draw is an inverse CDF in fixed point:
-  weights w(x) = floor(m(x) * 2^40) of the mass m (the positive difference
-  p - q computed in fp64, or p itself), integer prefix sums C, Z_int = C(V-1),
+  the mass of x is m = p(x) - q(x) for a residual, taken in fp32 like its
+  operands (one correctly rounded subtraction), or p(x) for a target; it is
+  clamped to [0, 2] and becomes the weight F(m) = floor(m * 2^40) (exact:
+  scaling an fp32 by a power of two only moves its exponent); integer prefix
+  sums C, Z_int = C(V-1),
   threshold T = floor(s * Z_int / 2^32) for the 32-bit uniform integer s, and
   the token is the smallest x with C(x) > T.  Integer sums make the choice
   independent of summation order.  When a rejection meets a zero residual
   (Z_int = 0, which eq. 33.12 leaves unformed: rejection then has probability
-  zero) the candidate is accepted instead.  A candidate with q_i(x_i) = 0
-  cannot have been proposed; it is rejected.
+  zero) the candidate is accepted instead.  A candidate with q_i(x_i) = 0, or
+  outside the vocabulary, cannot have been proposed; it is rejected, and if
+  its position has no residual mass either the token is drawn from p_i
+  itself (p = q there).  A distribution with no mass at 2^-40 resolution
+  (not a distribution) gives token 0.
 """
 from __future__ import annotations
 
@@ -49,10 +55,19 @@ def acceptance(p, q):
     return {"a": a, "accepted_mass": accepted, "A": A, "Z": Z, "residual": residual, "out": out}
 
 
-def weights(mass_row) -> np.ndarray:
-    """Fixed-point weights floor(m * 2^40) (int64) of a non-negative fp64 row."""
-    m = np.asarray(mass_row, dtype=np.float64)
-    return np.floor(m * float(1 << FIX_BITS)).astype(np.int64)
+def fixed(m) -> np.ndarray:
+    """F(m) = floor(clamp(m, 0, 2) * 2^40) (int64) of fp32 masses, exact
+    (NaN counts as 0, like the fp32 min/max that skip NaN)."""
+    m = np.fmin(np.fmax(np.asarray(m, dtype=np.float32), np.float32(0.0)), np.float32(2.0))
+    return np.floor(m.astype(np.float64) * float(1 << FIX_BITS)).astype(np.int64)
+
+
+def weights(p_row, q_row=None) -> np.ndarray:
+    """Fixed-point weights of the residual p - q (fp32 subtraction) or of p."""
+    p_row = np.asarray(p_row, dtype=np.float32)
+    if q_row is None:
+        return fixed(p_row)
+    return fixed(p_row - np.asarray(q_row, dtype=np.float32))
 
 
 def inverse_cdf(w: np.ndarray, s: int) -> int:
@@ -89,21 +104,31 @@ def verify_step(p, q, draft, u_accept, u_sample):
         i = 0
         while i < k:
             x = int(draft[b, i])
-            px = float(p[b, i, x])
-            qx = float(q[b, i, x])
-            if qx > 0.0 and float(u_accept[b, i]) * qx < px:
+            if x < 0 or x >= V:  # cannot have been proposed
+                px = qx = 0.0
+            else:
+                px = float(p[b, i, x])
+                qx = float(q[b, i, x])
+            valid = qx > 0.0
+            if valid and float(u_accept[b, i]) * qx < px:
                 i += 1
                 continue
             # rejected: the residual of position i
-            m = np.maximum(p[b, i].astype(np.float64) - q[b, i].astype(np.float64), 0.0)
-            w = weights(m)
-            if int(w.sum()) == 0:  # rejection has probability zero here: keep the candidate
-                i += 1
-                continue
+            w = weights(p[b, i], q[b, i])
+            if int(w.sum()) == 0:
+                if valid:  # rejection has probability zero here: keep the candidate
+                    i += 1
+                    continue
+                # an impossible candidate and no residual (p = q here): the target itself
+                w = weights(p[b, i])
+                chosen = inverse_cdf(w, int(u_sample[b])) if int(w.sum()) > 0 else 0
+                break
             chosen = inverse_cdf(w, int(u_sample[b]))
             break
         if chosen is None:  # every candidate kept: the next target distribution
-            chosen = inverse_cdf(weights(p[b, k].astype(np.float64)), int(u_sample[b]))
+            w = weights(p[b, k])
+            # no mass at 2^-40 resolution (not a distribution): token 0 by definition
+            chosen = inverse_cdf(w, int(u_sample[b])) if int(w.sum()) > 0 else 0
         n_acc[b] = i
         token[b] = chosen
     return n_acc, token
