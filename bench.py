@@ -398,6 +398,50 @@ def measure_other(name, peaks):
     return entry
 
 
+def measure_spec_sample(peaks, steps=10, warmup=3):
+    """The speculative-sampling step (blkattn_spec_sample) on its full-size
+    workload: device time per call with L2 cleared by a read of twice its size
+    before each call (the rows a call reads fit in L2), and the bytes of the
+    rows each sequence draws from (p_i and q_i of the first rejected position,
+    or p_{k+1})."""
+    from exact_blocked_attention_gb300 import blkattn
+    s = workloads.sample_spec("spec_sample")
+    cpu = workloads.generate_sampling(s)
+    dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in cpu.items()}
+    n_acc = torch.empty(s.B, dtype=torch.int32, device="cuda")
+    tok = torch.empty(s.B, dtype=torch.int32, device="cuda")
+    call = lambda: blkattn.spec_sample(dev["p"], dev["q"], dev["draft"], dev["u_accept"], dev["u_sample"],
+                                       n_acc, tok)
+    call()
+    torch.cuda.synchronize()
+    n = n_acc.cpu().numpy()
+    row = s.V * 4
+    drawn = int(sum(2 * row if int(x) < s.k else row for x in n))
+    small = int(sum((int(x) + 1) * 12 for x in n)) + s.B * 12  # candidate p, q, u; s; outputs
+    total = drawn + small
+    # evict the rows by READING a buffer twice the L2 size: a written flush
+    # buffer would leave dirty lines whose write-back lands in the timed call
+    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    times = []
+    for it in range(warmup + steps):
+        flush.sum()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        if it >= warmup:
+            times.append(e0.elapsed_time(e1))
+    t_ms = sum(times) / len(times)
+    achieved = total / (t_ms * 1e-3) / 1e9
+    return {"workload": f"spec_sample: B={s.B} k={s.k} V={s.V} f32 probabilities",
+            "us_per_call": t_ms * 1e3, "l2": "evicted between steps by reading 2x its size",
+            "kept_candidates_histogram": np.bincount(n, minlength=s.k + 1).tolist(),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": measured_traffic("spec_sample"),
+                         "algorithmic_bytes": total, "peak_note": f"HBM copy bandwidth, {peaks['source']}"}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -482,6 +526,10 @@ def main():
             except Exception as exc:  # report, keep the headline line
                 others[name] = {"error": f"{type(exc).__name__}: {exc}"}
             torch.cuda.empty_cache()
+        try:
+            others["spec_sample"] = measure_spec_sample(peaks)
+        except Exception as exc:  # reported, not fatal
+            others["spec_sample"] = {"error": f"{type(exc).__name__}: {exc}"}
         line["workloads"] = others
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1 only) ----

@@ -30,7 +30,8 @@ _DTYPES = {torch.bfloat16: BF16, torch.float32: F32, torch.int32: I32, torch.int
 
 EXPORTED = ("blkattn_fwd", "blkattn_merge", "blkattn_status_string",
             "blkattn_check_device_error", "blkattn_debug_plan", "blkattn_debug_set_split_event",
-            "blkattn_fwd_static_scratch", "blkattn_last_cuda_error", "blkattn_fwd_tree")
+            "blkattn_fwd_static_scratch", "blkattn_last_cuda_error", "blkattn_fwd_tree",
+            "blkattn_spec_sample")
 
 
 class Tensor(ctypes.Structure):
@@ -76,6 +77,8 @@ def load(path: str = LIB_PATH):
             lib.blkattn_fwd.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P]
             lib.blkattn_fwd_tree.restype = ctypes.c_int
             lib.blkattn_fwd_tree.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, P, P, P]
+            lib.blkattn_spec_sample.restype = ctypes.c_int
+            lib.blkattn_spec_sample.argtypes = [P] * 8
             lib.blkattn_fwd_static_scratch.restype = ctypes.c_int
             lib.blkattn_fwd_static_scratch.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P]
             lib.blkattn_merge.restype = ctypes.c_int
@@ -182,6 +185,21 @@ def attention(q, k, v, seqlens_k, q_logical_pos, mask_bias=None, scale=None,
     out = torch.empty((B, Hq, Tq, v.shape[3]), dtype=out_dtype, device=q.device)
     lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
     return fwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, stream, tree=tree)
+
+
+def spec_sample(p, q, draft, u_accept, u_sample, n_accepted=None, token=None, stream=None):
+    """blkattn_spec_sample: one speculative verification step per sequence.
+    p f32 [B,k+1,V], q f32 [B,k,V], draft int32 [B,k], u_accept f32 [B,k],
+    u_sample int32 [B] (32 random bits).  Returns (n_accepted, token), int32 [B]."""
+    lib = load()
+    B = p.shape[0]
+    if n_accepted is None:
+        n_accepted = torch.empty(B, dtype=torch.int32, device=p.device)
+    if token is None:
+        token = torch.empty(B, dtype=torch.int32, device=p.device)
+    descs = [describe(t) for t in (p, q, draft, u_accept, u_sample, n_accepted, token)]
+    _check(lib.blkattn_spec_sample(*[_ref(d) for d in descs], _stream_handle(stream) if p.is_cuda else None))
+    return n_accepted, token
 
 
 def _states(m, l, u) -> States:

@@ -625,6 +625,10 @@ int fwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_ten
   return launch_fwd(p, c, pl, q, k, v, out, stream);
 }
 
+// CUDA failures of entry points outside this file: recorded for
+// blkattn_last_cuda_error like the ones here.
+int report_cuda_failure(cudaError_t e) { return cuda_fail(e); }
+
 }  // namespace blkattn
 
 extern "C" {

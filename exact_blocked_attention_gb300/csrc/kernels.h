@@ -137,6 +137,8 @@ int fwd_with_scratch(const blkattn_tensor* q, const blkattn_tensor* k, const blk
                      const blkattn_tensor* tree, const blkattn_tensor* mask_bias, float scale,
                      const blkattn_tensor* out, const blkattn_tensor* lse, blkattn_stream_t stream,
                      void* scratch, size_t scratch_bytes);
+// Records a CUDA failure for blkattn_last_cuda_error; returns BLKATTN_ERR_CUDA.
+int report_cuda_failure(cudaError_t e);
 // blkattn_fwd / blkattn_fwd_tree (tree may be NULL) on the library's workspace.
 int fwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
              const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos, const blkattn_tensor* tree,

@@ -223,3 +223,59 @@ def kv_bytes(s: Spec, seqlens) -> int:
     elt = 2 if s.dtype == "bf16" else 4
     lens = np.minimum(np.asarray(seqlens, dtype=np.int64), s.Tmax)
     return int(lens.sum()) * s.Hkv * s.d * elt * 2
+
+
+# ---------------------------------------------------------------- speculative sampling
+# One verification step ("Chapter 33: inference compute optimisation" §33.5,
+# eqs. 33.10-33.13): target and draft distributions over a vocabulary, the
+# draft's candidates, and the random numbers of the step.  The draft's logits
+# are the target's plus Gaussian noise, so that acceptance is neither certain
+# nor rare.
+
+@dataclass(frozen=True)
+class SampleSpec:
+    name: str
+    B: int          # sequences
+    k: int          # candidates per sequence
+    V: int          # vocabulary
+    seed: int
+    noise: float    # std of the draft's logit perturbation
+    temp: float = 1.0
+
+
+SAMPLE_SPECS = {
+    "spec_sample": SampleSpec("spec_sample", 64, 4, 128256, 7, 1.0),
+}
+SAMPLE_SMALL = {
+    "spec_sample": SampleSpec("spec_sample", 16, 3, 1000, 7, 1.0),
+}
+
+
+def sample_spec(name: str, small: bool = False) -> SampleSpec:
+    return (SAMPLE_SMALL if small else SAMPLE_SPECS)[name]
+
+
+def generate_sampling(s: SampleSpec) -> dict:
+    """p f32 [B,k+1,V], q f32 [B,k,V] (softmax rows), draft int32 [B,k] drawn
+    from q, u_accept f32 [B,k] in [0,1), u_sample int32 [B] (32 random bits)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([s.seed, 98])))
+    z = _normal((s.B, s.k + 1, s.V), s.seed, 11) * 3.0
+    zq = z[:, :s.k] + _normal((s.B, s.k, s.V), s.seed, 12) * s.noise
+
+    def softmax(a):
+        a = a / s.temp
+        a = a - a.max(axis=-1, keepdims=True)
+        e = np.exp(a.astype(np.float64))
+        return (e / e.sum(axis=-1, keepdims=True)).astype(np.float32)
+
+    p = softmax(z)
+    q = softmax(zq)
+    draft = np.zeros((s.B, s.k), dtype=np.int32)
+    for b in range(s.B):
+        for i in range(s.k):
+            c = np.cumsum(q[b, i].astype(np.float64))
+            draft[b, i] = min(int(np.searchsorted(c, rng.random() * c[-1], side="right")), s.V - 1)
+    u_accept = rng.random((s.B, s.k), dtype=np.float32)
+    u_sample = rng.integers(0, 2**32, size=s.B, dtype=np.uint64).astype(np.uint32).view(np.int32)
+    return {"p": torch.from_numpy(p), "q": torch.from_numpy(q), "draft": torch.from_numpy(draft),
+            "u_accept": torch.from_numpy(u_accept), "u_sample": torch.from_numpy(u_sample.copy()), "spec": s}

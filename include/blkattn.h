@@ -148,6 +148,42 @@ int blkattn_fwd_tree(const blkattn_tensor* q, const blkattn_tensor* k,
                      blkattn_stream_t stream);
 
 /*
+ * blkattn_spec_sample — one speculative-decoding verification step per
+ * sequence ("Chapter 33: inference compute optimisation" §33.5,
+ * eqs. 33.10–33.13; §33.6 for the in-order rule).
+ *
+ * p           f32 [B, k+1, V]: target probabilities after the confirmed
+ *             prefix and after each candidate (row k: past all of them);
+ *             vocabulary stride 1.
+ * q           f32 [B, k, V]: the draft probabilities the candidates were
+ *             drawn from; vocabulary stride 1.
+ * draft       int32 [B, k]: the candidates x_1..x_k.
+ * u_accept    f32 [B, k]: uniforms in [0, 1), one per candidate.
+ * u_sample    int32 [B]: one 32-bit uniform integer per sequence (the bits
+ *             are read as unsigned).
+ * n_accepted  int32 [B], written: candidates kept (0..k).
+ * token       int32 [B], written: the token emitted after them.
+ * Candidate x_i is kept iff u_i * q_i(x_i) < p_i(x_i) (computed in fp64,
+ * exact for fp32 operands), in order, up to the first rejection; then the
+ * token is drawn from the residual [p_i - q_i]_+ of that position, or from
+ * p_{k+1} when all are kept, by inverse CDF in fixed point (mass p - q in
+ * fp32, or p, clamped to [0, 2]; weight floor(mass * 2^40); integer prefix
+ * sums; threshold floor(s * Z / 2^32); the smallest token whose prefix sum
+ * exceeds it).  A rejection meeting a zero
+ * residual keeps the candidate; a candidate outside [0, V) or with q = 0 is
+ * rejected (its position having no residual mass, the token is drawn from
+ * p_i); a distribution with no mass at 2^-40 resolution gives token 0.
+ * k = 0 is allowed (q, draft, u_accept may then be empty).  The caller owns
+ * every buffer; the call enqueues one kernel on the stream and never reads
+ * device data on the host.  Returns BLKATTN_OK, BLKATTN_ERR_INVALID_ARG
+ * (shapes, dtypes, strides, NULL data) or BLKATTN_ERR_CUDA (launch).
+ */
+int blkattn_spec_sample(const blkattn_tensor* p, const blkattn_tensor* q,
+                        const blkattn_tensor* draft, const blkattn_tensor* u_accept,
+                        const blkattn_tensor* u_sample, const blkattn_tensor* n_accepted,
+                        const blkattn_tensor* token, blkattn_stream_t stream);
+
+/*
  * blkattn_fwd_static_scratch — blkattn_fwd that allocates no device memory.
  *
  * No counterpart on the pages: this is a deployment variant of blkattn_fwd.

@@ -141,6 +141,45 @@ def test_tree_needs_at_most_64_rows(lib):
     assert call_fwd_tree(lib, e["q"], e["k"], e["v"], e["sl"], e["qp"], empty_tree, None, e["out"], e["lse"]) == 0
 
 
+def call_spec(lib, p, q, draft, ua, us, n, tok):
+    ds = [None if t is None else t.desc() for t in (p, q, draft, ua, us, n, tok)]
+    ref = lambda d: None if d is None else ctypes.byref(d)
+    return lib.blkattn_spec_sample(*[ref(x) for x in ds], None)
+
+
+def good_spec(B=4, k=3, V=1000):
+    return dict(p=FakeTensor((B, k + 1, V), torch.float32), q=FakeTensor((B, k, V), torch.float32),
+                draft=FakeTensor((B, k), torch.int32), ua=FakeTensor((B, k), torch.float32),
+                us=FakeTensor((B,), torch.int32), n=FakeTensor((B,), torch.int32),
+                tok=FakeTensor((B,), torch.int32))
+
+
+@pytest.mark.parametrize("mutate", [
+    lambda a: a.update(p=FakeTensor((4, 4, 1000), torch.bfloat16)),
+    lambda a: a.update(q=FakeTensor((4, 4, 1000), torch.float32)),          # k must match
+    lambda a: a.update(q=FakeTensor((4, 3, 999), torch.float32)),
+    lambda a: a.update(draft=FakeTensor((4, 3), torch.int64)),
+    lambda a: a.update(ua=FakeTensor((4, 2), torch.float32)),
+    lambda a: a.update(us=FakeTensor((5,), torch.int32)),
+    lambda a: a.update(tok=FakeTensor((4,), torch.float32)),
+    lambda a: a.update(p=FakeTensor((4, 4, 1000), torch.float32, strides=(8000, 2000, 2))),  # vocab stride
+    lambda a: a.update(p=FakeTensor((4, 4, 1000), torch.float32, addr=0)),
+    lambda a: a.update(p=None),
+], ids=["p-dtype", "k-mismatch", "vocab", "draft-dtype", "uacc-shape", "usmp-shape", "tok-dtype",
+        "vocab-stride", "null-p", "missing-p"])
+def test_spec_sample_rejects_bad_requests(lib, mutate):
+    a = good_spec()
+    mutate(a)
+    assert call_spec(lib, a["p"], a["q"], a["draft"], a["ua"], a["us"], a["n"], a["tok"]) == -1
+
+
+def test_spec_sample_empty_batch(lib):
+    a = good_spec(B=0)
+    for t in a.values():
+        t.addr = 0
+    assert call_spec(lib, a["p"], a["q"], a["draft"], a["ua"], a["us"], a["n"], a["tok"]) == 0
+
+
 def test_empty_problem_is_a_no_op(lib):
     a = good_args(B=0)
     for t in a.values():

@@ -1,0 +1,98 @@
+"""The speculative-sampling step (blkattn_spec_sample) against the oracle
+(oracle/spec_sampling.py, pinned to Chapter 33 §33.5): the kept-candidate
+counts and the emitted tokens are integers decided the same way on both
+sides, so they must match exactly."""
+import numpy as np
+import pytest
+import torch
+
+from exact_blocked_attention_gb300 import blkattn, workloads
+from exact_blocked_attention_gb300 import build as libbuild
+from oracle import spec_sampling as ss
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    libbuild.build()
+    blkattn.load()
+
+
+def run_both(p, q, draft, u_acc, u_smp):
+    dev = [t.cuda() for t in (p, q, draft, u_acc, u_smp)]
+    n, tok = blkattn.spec_sample(*dev)
+    torch.cuda.synchronize()
+    on, ot = ss.verify_step(p.numpy(), q.numpy(), draft.numpy(), u_acc.numpy(),
+                            u_smp.numpy().view(np.uint32))
+    return n.cpu().numpy(), tok.cpu().numpy(), on, ot
+
+
+@pytest.mark.parametrize("small", [True, False])
+def test_workload_matches_oracle(small):
+    g = workloads.generate_sampling(workloads.sample_spec("spec_sample", small))
+    n, tok, on, ot = run_both(g["p"], g["q"], g["draft"], g["u_accept"], g["u_sample"])
+    np.testing.assert_array_equal(n, on)
+    np.testing.assert_array_equal(tok, ot)
+    assert len(set(n.tolist())) > 1  # the workload exercises several outcomes
+
+
+def random_case(B, k, V, seed):
+    rng = np.random.default_rng(seed)
+    p = rng.dirichlet(np.ones(V) * 0.5, size=(B, k + 1)).astype(np.float32)
+    q = rng.dirichlet(np.ones(V) * 0.5, size=(B, k)).astype(np.float32)
+    draft = rng.integers(0, V, size=(B, k)).astype(np.int32)
+    u = rng.random((B, k), dtype=np.float32)
+    s = rng.integers(0, 2**32, size=B, dtype=np.uint64).astype(np.uint32).view(np.int32)
+    return [torch.from_numpy(np.ascontiguousarray(a)) for a in (p, q, draft, u, s)]
+
+
+@pytest.mark.parametrize("B,k,V", [(9, 0, 37), (33, 1, 5), (17, 2, 33), (5, 6, 65537), (64, 3, 1)])
+def test_random_shapes(B, k, V):
+    n, tok, on, ot = run_both(*random_case(B, k, V, seed=B * 1000 + k * 10 + V))
+    np.testing.assert_array_equal(n, on)
+    np.testing.assert_array_equal(tok, ot)
+
+
+def test_degenerate_cases():
+    V = 40
+    B, k = 5, 2
+    p = np.full((B, k + 1, V), 1.0 / V, dtype=np.float32)
+    q = np.full((B, k, V), 1.0 / V, dtype=np.float32)
+    draft = np.full((B, k), 3, dtype=np.int32)
+    u = np.full((B, k), 0.75, dtype=np.float32)
+    # row 0: a rejection that meets a zero residual (mass below 2^-40 only):
+    # the candidate is kept, so both are kept
+    q[0, 0, 3] = 2.0**-30; p[0, 0, 3] = 2.0**-31
+    q[0, 0, 7] = 2.0**-45; p[0, 0, 7] = 2.0**-45 + 2.0**-50
+    # row 1: a candidate outside the vocabulary is rejected
+    draft[1, 0] = V
+    # row 2: a candidate the draft gives no probability is rejected
+    q[2, 0, 3] = 0.0
+    # row 3: every candidate kept and the next target has no mass: token 0
+    p[3, k] = 0.0
+    # row 4: a negative candidate is rejected
+    draft[4, 1] = -1
+    t = [torch.from_numpy(a) for a in (p, q, draft, u)]
+    s = torch.from_numpy(np.array([1, 2**31 - 1, -5, 7, 123456], dtype=np.int32))
+    n, tok, on, ot = run_both(*t, s)
+    np.testing.assert_array_equal(n, on)
+    np.testing.assert_array_equal(tok, ot)
+    assert n[0] == 2 and n[1] == 0 and n[2] == 0 and n[3] == 2 and tok[3] == 0 and n[4] == 1
+
+
+def test_strided_views():
+    p, q, draft, u, s = random_case(7, 3, 300, seed=5)
+    big_p = torch.zeros(7, 6, 300); big_p[:, 1:5] = p      # non-contiguous along k
+    big_q = torch.zeros(9, 3, 300); big_q[1:8] = q
+    n, tok = blkattn.spec_sample(big_p[:, 1:5].cuda(), big_q[1:8].cuda(), draft.cuda(), u.cuda(), s.cuda())
+    pv = big_p.cuda()[:, 1:5]
+    qv = big_q.cuda()[1:8]
+    n2, tok2 = blkattn.spec_sample(pv, qv, draft.cuda(), u.cuda(), s.cuda())
+    torch.cuda.synchronize()
+    on, ot = ss.verify_step(p.numpy(), q.numpy(), draft.numpy(), u.numpy(), s.numpy().view(np.uint32))
+    for a, b_ in ((n, tok), (n2, tok2)):
+        np.testing.assert_array_equal(a.cpu().numpy(), on)
+        np.testing.assert_array_equal(b_.cpu().numpy(), ot)
