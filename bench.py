@@ -451,6 +451,8 @@ def main():
     ap.add_argument("--workload", default=HEADLINE, choices=list(workloads.SPECS))
     ap.add_argument("--no-others", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-sampling", action="store_true",
+                    help="time only the speculative-sampling step and print its entry")
     ap.add_argument("--ref-budget-s", type=float, default=60.0,
                     help="--impl reference: seconds of oracle work over all steps")
     args = ap.parse_args()
@@ -466,6 +468,12 @@ def main():
         libbuild.build()
     barrier(world)
     peaks = measured_peaks()
+    if args.only_sampling:
+        from exact_blocked_attention_gb300 import blkattn
+        blkattn.load()
+        if rank == 0:
+            print(json.dumps(measure_spec_sample(peaks, steps=args.steps, warmup=args.warmup)), flush=True)
+        return
 
     # ---- headline workload: every rank runs its own batch (weak scaling) ----
     r = Runner(args.workload, seed_offset=rank)
