@@ -16,7 +16,9 @@ Contents
                    Example 25.1, exact rational brute force, closed forms and
                    the cache-alignment example.  Optional token-tree
                    visibility ("推理加速算法" §7.2.2 Medusa, tree attention
-                   verification), pinned by brute force over random trees.
+                   verification), pinned by brute force over random trees;
+                   optional sliding window (§33.7), pinned by the bound of
+                   eq. 33.16 and by brute force.
   states           the sufficient statistics (m, l, u) of eq. 33.3, the merge
                    rule of eqs. 33.4–33.5 and Algorithm 33.1, in numpy fp64.
   spec_sampling    speculative-sampling acceptance and residual sampling
@@ -73,6 +75,17 @@ def _load():
                 P, ctypes.c_int64,            # rows, nrows
                 P, P, P, P, P,                # out lse n_vis first last
                 I]                            # nthreads
+            lib.oracle_attention_masks.restype = I
+            lib.oracle_attention_masks.argtypes = [
+                I, I, I, I, I, I, I,          # B Hq Hkv Tq Tmax dh dv
+                P, I, P, I, P, I,             # q k v (+types)
+                P, P,                         # seqlens qpos
+                P, I, P,                      # bias, type, strides
+                P, ctypes.c_int64,            # tree masks, window
+                ctypes.c_double,              # scale
+                P, ctypes.c_int64,            # rows, nrows
+                P, P, P, P, P,                # out lse n_vis first last
+                I]                            # nthreads
             lib.oracle_attention_tree.restype = I
             lib.oracle_attention_tree.argtypes = [
                 I, I, I, I, I, I, I,          # B Hq Hkv Tq Tmax dh dv
@@ -123,7 +136,7 @@ def _as_array(x):
 
 
 def attention(q, k, v, seqlens, qpos, scale, bias=None, rows=None,
-              nthreads: int = 0, tree=None):
+              nthreads: int = 0, tree=None, window: int = 0):
     """Explicit exact attention (eq. 33.2), one row at a time, in fp64.
 
     q [B,H_q,T_q,d_h], k [B,H_kv,T_max,d_h], v [B,H_kv,T_max,d_v] (float64,
@@ -134,6 +147,8 @@ def attention(q, k, v, seqlens, qpos, scale, bias=None, rows=None,
     tree: None, or int64 [B,T_q] node masks of a candidate token tree whose
     nodes' keys are the last T_q cache entries of each sequence (bit k of
     tree[b,i] set = row i sees tree node k; T_q <= 64).
+    window: 0, or W > 0 for sliding-window attention (a row at position pos
+    sees only keys j > pos - W).
 
     Returns dict(out [n,d_v] f64, lse [n] f64, n_visible, first, last int32 [n]).
     """
@@ -185,12 +200,12 @@ def attention(q, k, v, seqlens, qpos, scale, bias=None, rows=None,
         tr = np.asarray(tree.detach().cpu().numpy() if hasattr(tree, "detach") else tree)
         tr = np.ascontiguousarray(tr.astype(np.int64, copy=False)).reshape(B, Tq)
     P = lambda a: None if a is None else a.ctypes.data
-    rc = lib.oracle_attention_tree(
+    rc = lib.oracle_attention_masks(
         B, Hq, Hkv, Tq, Tmax, dh, dv,
         P(qa), qt, P(ka), kt, P(va), vt,
         P(sl), P(qp),
         bias_ptr, bias_type, P(strides),
-        P(tr),
+        P(tr), int(window),
         float(scale),
         P(rows_arr), int(n),
         P(out), P(lse), P(nvis), P(first), P(last),

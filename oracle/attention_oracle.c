@@ -39,6 +39,12 @@
  *     of tree[b, i] set = node i sees node k.  The plainest reading of
  *     "verify every candidate path in one pass": no node sees a sibling
  *     branch.  This is one more condition on top of the three above.
+ *   - sliding-window attention ("Chapter 33: inference compute
+ *     optimisation" §33.7, the paragraph of eq. 33.16: only the keys of
+ *     the prescribed range stay visible): with a window of W keys a row at
+ *     logical position pos sees only keys j > pos - W, i.e. the W most
+ *     recent positions up to its own; another condition on top of the
+ *     others.  W = 0 means no window.
  *   - grouped-query heads: query head h reads KV head floor(h / (H_q/H_kv)).
  *
  * Inputs may be float64, float32 or bfloat16 (raw 16-bit patterns); every
@@ -77,6 +83,7 @@ typedef struct {
   const void* bias; int bias_type;  /* may be NULL */
   int64_t bias_stride[4];
   const int64_t* tree;              /* may be NULL: [B, T_q] node masks, T_q <= 64 */
+  int64_t window;                   /* 0: none; else keys j > pos - window */
   double scale;
 } oracle_problem;
 
@@ -104,6 +111,7 @@ static int one_row(const oracle_problem* P, int64_t row, double* zbuf,
   for (int64_t j = 0; j < P->Tmax; ++j) {
     zbuf[j] = -INFINITY;
     if (!(j < len && j <= pos)) continue;
+    if (P->window > 0 && j <= pos - P->window) continue; /* outside the window */
     if (P->tree) {
       const int64_t base = len - P->Tq; /* key of tree node 0 */
       if (j >= base) {
@@ -159,16 +167,17 @@ static int one_row(const oracle_problem* P, int64_t row, double* zbuf,
  * key index (-1 when none).  nthreads <= 0 uses the OpenMP default.
  * Returns 0, -1 on bad sizes, -2 on an out-of-contract bias, -3 on no memory.
  */
-int oracle_attention_tree(int B, int Hq, int Hkv, int Tq, int Tmax, int dh, int dv,
-                          const void* q, int q_type, const void* k, int k_type,
-                          const void* v, int v_type, const int32_t* seqlens,
-                          const int32_t* qpos, const void* bias, int bias_type,
-                          const int64_t* bias_stride, const int64_t* tree,
-                          double scale, const int64_t* rows, int64_t nrows,
-                          double* out, double* lse, int32_t* n_vis,
-                          int32_t* first, int32_t* last, int nthreads) {
+int oracle_attention_masks(int B, int Hq, int Hkv, int Tq, int Tmax, int dh, int dv,
+                           const void* q, int q_type, const void* k, int k_type,
+                           const void* v, int v_type, const int32_t* seqlens,
+                           const int32_t* qpos, const void* bias, int bias_type,
+                           const int64_t* bias_stride, const int64_t* tree,
+                           int64_t window, double scale, const int64_t* rows,
+                           int64_t nrows, double* out, double* lse,
+                           int32_t* n_vis, int32_t* first, int32_t* last,
+                           int nthreads) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Tq < 0 || Tmax < 0 || dh <= 0 ||
-      dv <= 0 || Hq % Hkv != 0 || (tree && Tq > 64))
+      dv <= 0 || Hq % Hkv != 0 || (tree && Tq > 64) || window < 0)
     return -1;
   oracle_problem P;
   memset(&P, 0, sizeof P);
@@ -176,6 +185,7 @@ int oracle_attention_tree(int B, int Hq, int Hkv, int Tq, int Tmax, int dh, int 
   P.dv = dv; P.q = q; P.q_type = q_type; P.k = k; P.k_type = k_type;
   P.v = v; P.v_type = v_type; P.seqlens = seqlens; P.qpos = qpos;
   P.bias = bias; P.bias_type = bias_type; P.scale = scale; P.tree = tree;
+  P.window = window;
   if (bias)
     for (int s = 0; s < 4; ++s) P.bias_stride[s] = bias_stride[s];
   const int64_t total = (int64_t)B * Hq * Tq;
@@ -213,6 +223,20 @@ int oracle_attention_tree(int B, int Hq, int Hkv, int Tq, int Tmax, int dh, int 
     free(zbuf);
   }
   return status;
+}
+
+/* The same with a tree and no window. */
+int oracle_attention_tree(int B, int Hq, int Hkv, int Tq, int Tmax, int dh, int dv,
+                          const void* q, int q_type, const void* k, int k_type,
+                          const void* v, int v_type, const int32_t* seqlens,
+                          const int32_t* qpos, const void* bias, int bias_type,
+                          const int64_t* bias_stride, const int64_t* tree,
+                          double scale, const int64_t* rows, int64_t nrows,
+                          double* out, double* lse, int32_t* n_vis,
+                          int32_t* first, int32_t* last, int nthreads) {
+  return oracle_attention_masks(B, Hq, Hkv, Tq, Tmax, dh, dv, q, q_type, k, k_type, v, v_type,
+                                seqlens, qpos, bias, bias_type, bias_stride, tree, 0, scale,
+                                rows, nrows, out, lse, n_vis, first, last, nthreads);
 }
 
 /* The same without a tree. */

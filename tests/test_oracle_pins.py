@@ -492,3 +492,95 @@ def test_tree_needs_at_most_64_nodes():
     q = np.zeros((1, 1, 65, 2)); k = np.zeros((1, 1, 70, 2)); v = np.zeros((1, 1, 70, 2))
     with pytest.raises(ValueError):
         run_tree(q, k, v, [70], [[69] * 65], 1.0, np.zeros((1, 65), dtype=np.int64))
+
+
+# ---------------------------------------------------------------- sliding window
+# "Chapter 33: inference compute optimisation" §33.7, the paragraph of
+# eq. 33.16: a window keeps only the keys of the prescribed range (here the
+# W most recent positions up to the row's own); dropping the original mass
+# delta moves the output by at most 2 delta M (M bounds the value norms).
+
+def run_window(q, k, v, seqlens, qpos, scale, window, bias=None):
+    return oracle.attention(np.asarray(q, np.float64), np.asarray(k, np.float64),
+                            np.asarray(v, np.float64), np.asarray(seqlens, np.int32),
+                            np.asarray(qpos, np.int32), scale, bias=bias, window=window)
+
+
+def test_window_bound_of_eq_33_16():
+    rng = np.random.default_rng(31)
+    B, Hq, Hkv, Tq, Tmax, d = 2, 4, 2, 5, 60, 8
+    q = rng.normal(size=(B, Hq, Tq, d)); k = rng.normal(size=(B, Hkv, Tmax, d))
+    v = rng.normal(size=(B, Hkv, Tmax, d)) * rng.uniform(0.1, 3.0, size=(B, Hkv, Tmax, 1))
+    seqlens = np.array([60, 41], dtype=np.int32)
+    qpos = np.stack([np.arange(55, 60), np.arange(36, 41)]).astype(np.int32)
+    scale = 0.7
+    full = run(q, k, v, seqlens, qpos, scale)
+    G = Hq // Hkv
+    for W in (1, 3, 10, 40):
+        win = run_window(q, k, v, seqlens, qpos, scale, W)
+        for b, h, i in itertools.product(range(B), range(Hq), range(Tq)):
+            row = (b * Hq + h) * Tq + i
+            pos, hk = int(qpos[b, i]), h // G
+            z = scale * (k[b, hk, :pos + 1] @ q[b, h, i])
+            w = np.exp(z - full["lse"][row])            # the original attention probabilities
+            delta = w[:max(0, pos + 1 - W)].sum()        # the mass the window drops
+            M = np.linalg.norm(v[b, hk, :pos + 1], axis=1).max()
+            err = np.linalg.norm(full["out"][row] - win["out"][row])
+            if delta < 1:
+                assert err <= 2 * delta * M + 1e-12
+            assert win["n_visible"][row] == min(W, pos + 1)
+
+
+def test_window_brute_force_exact_rationals():
+    rng = np.random.default_rng(32)
+    B, Hq, Hkv, Tq, Tmax, dv = 2, 4, 2, 3, 9, 3
+    for trial in range(6):
+        with_bias = trial % 2 == 1
+        q, k, vals, r, sfrac, bias, scale = _rational_problem(rng, B, Hq, Hkv, Tq, Tmax, dv, with_bias)
+        seqlens = rng.integers(0, Tmax + 2, size=B).astype(np.int32)
+        qpos = rng.integers(-2, Tmax + 3, size=(B, Tq)).astype(np.int32)
+        W = int(rng.integers(1, 6))
+        res = run_window(q, k, vals, seqlens, qpos, scale, W, bias=bias)
+        G = Hq // Hkv
+        for b, h, i in itertools.product(range(B), range(Hq), range(Tq)):
+            row = (b * Hq + h) * Tq + i
+            hk = h // G
+            num = [Fraction(0)] * dv
+            den = Fraction(0)
+            seen = []
+            for j in range(Tmax):
+                if not (j < seqlens[b] and j <= qpos[b, i] and qpos[b, i] - j < W):
+                    continue
+                wt = r[b][hk][j]
+                if with_bias:
+                    s = sfrac[b][h][i][j]
+                    if s is None:
+                        continue
+                    wt = wt * s
+                seen.append(j)
+                den += wt
+                for t in range(dv):
+                    num[t] += wt * Fraction(vals[b, hk, j, t])
+            assert res["n_visible"][row] == len(seen)
+            if not seen:
+                assert res["lse"][row] == -math.inf and np.all(res["out"][row] == 0.0)
+                continue
+            np.testing.assert_allclose(res["out"][row], [float(x / den) for x in num], rtol=1e-13, atol=1e-13)
+
+
+def test_window_special_cases():
+    rng = np.random.default_rng(33)
+    q = rng.normal(size=(1, 2, 3, 8)); k = rng.normal(size=(1, 1, 30, 8)); v = rng.normal(size=(1, 1, 30, 4))
+    sl, pos = [25], [[10, 24, 29]]
+    # a window at least as long as every visible range changes nothing
+    a = run_window(q, k, v, sl, pos, 0.4, 30)
+    b = run(q, k, v, sl, pos, 0.4)
+    np.testing.assert_array_equal(a["out"], b["out"])
+    np.testing.assert_array_equal(a["lse"], b["lse"])
+    # a window of one key returns that key's value exactly
+    c = run_window(q, k, v, sl, pos, 0.4, 1)
+    for h in range(2):
+        np.testing.assert_array_equal(c["out"][h * 3 + 0], v[0, 0, 10])
+        np.testing.assert_array_equal(c["out"][h * 3 + 1], v[0, 0, 24])
+        # position 29 is past the cache (length 25): its one-key window is empty
+        assert c["lse"][h * 3 + 2] == -math.inf and np.all(c["out"][h * 3 + 2] == 0.0)
