@@ -222,7 +222,7 @@ class Runner:
     def call(self):
         g = self.dev
         self.blkattn.fwd(g["q"], g["k"], g["v"], g["seqlens"], g["qpos"], g["bias"], g["scale"],
-                         self.out, self.lse, tree=g.get("tree"))
+                         self.out, self.lse, tree=g.get("tree"), window=g.get("window", 0))
 
     def free(self):
         del self.dev, self.out, self.lse
@@ -330,7 +330,8 @@ def oracle_rate(s, inp, budget_s: float, threads: int = 0):
         rows = rng.choice(total_rows, size=n, replace=False)
         t0 = time.perf_counter()
         oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"], inp["qpos"], inp["scale"],
-                         bias=inp["bias"], rows=rows, nthreads=threads, tree=inp.get("tree"))
+                         bias=inp["bias"], rows=rows, nthreads=threads, tree=inp.get("tree"),
+                         window=inp.get("window", 0))
         spent += time.perf_counter() - t0
         done += n
         if spent >= budget_s or done >= total_rows:

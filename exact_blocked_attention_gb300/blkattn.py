@@ -31,7 +31,7 @@ _DTYPES = {torch.bfloat16: BF16, torch.float32: F32, torch.int32: I32, torch.int
 EXPORTED = ("blkattn_fwd", "blkattn_merge", "blkattn_status_string",
             "blkattn_check_device_error", "blkattn_debug_plan", "blkattn_debug_set_split_event",
             "blkattn_fwd_static_scratch", "blkattn_last_cuda_error", "blkattn_fwd_tree",
-            "blkattn_spec_sample")
+            "blkattn_spec_sample", "blkattn_fwd_window")
 
 
 class Tensor(ctypes.Structure):
@@ -77,6 +77,8 @@ def load(path: str = LIB_PATH):
             lib.blkattn_fwd.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P]
             lib.blkattn_fwd_tree.restype = ctypes.c_int
             lib.blkattn_fwd_tree.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, P, P, P]
+            lib.blkattn_fwd_window.restype = ctypes.c_int
+            lib.blkattn_fwd_window.argtypes = [P, P, P, P, P, ctypes.c_int64, P, ctypes.c_float, P, P, P]
             lib.blkattn_spec_sample.restype = ctypes.c_int
             lib.blkattn_spec_sample.argtypes = [P] * 8
             lib.blkattn_fwd_static_scratch.restype = ctypes.c_int
@@ -140,10 +142,21 @@ def _ref(x):
     return None if x is None else ctypes.byref(x)
 
 
-def fwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale: float, out, lse, stream=None, tree=None):
+def fwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale: float, out, lse, stream=None, tree=None,
+        window: int = 0):
     """blkattn_fwd on torch CUDA tensors; out and lse are written in place.
-    tree: None, or int64 [B, T_q] token-tree node masks (blkattn_fwd_tree)."""
+    tree: None, or int64 [B, T_q] token-tree node masks (blkattn_fwd_tree).
+    window: 0, or a sliding window of that many keys (blkattn_fwd_window)."""
     lib = load()
+    if window:
+        if tree is not None:
+            raise ValueError("blkattn: a call takes a tree or a window, not both")
+        descs = [describe(t) for t in (q, k, v, seqlens_k, q_logical_pos, mask_bias, out, lse)]
+        st = lib.blkattn_fwd_window(*[_ref(x) for x in descs[:5]], ctypes.c_int64(int(window)), _ref(descs[5]),
+                                    ctypes.c_float(scale), _ref(descs[6]), _ref(descs[7]),
+                                    _stream_handle(stream) if q.is_cuda else None)
+        _check(st)
+        return out, lse
     if tree is not None:
         descs = [describe(t) for t in (q, k, v, seqlens_k, q_logical_pos, tree, mask_bias, out, lse)]
         st = lib.blkattn_fwd_tree(*[_ref(x) for x in descs[:7]], ctypes.c_float(scale),
@@ -176,7 +189,7 @@ def fwd_static_scratch(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale: floa
 
 
 def attention(q, k, v, seqlens_k, q_logical_pos, mask_bias=None, scale=None,
-              out_dtype=torch.float32, stream=None, tree=None):
+              out_dtype=torch.float32, stream=None, tree=None, window: int = 0):
     """Allocate out/lse with torch and run blkattn_fwd (blkattn_fwd_tree with
     a token tree)."""
     B, Hq, Tq, d = q.shape
@@ -184,7 +197,7 @@ def attention(q, k, v, seqlens_k, q_logical_pos, mask_bias=None, scale=None,
         scale = d ** -0.5
     out = torch.empty((B, Hq, Tq, v.shape[3]), dtype=out_dtype, device=q.device)
     lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
-    return fwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, stream, tree=tree)
+    return fwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, stream, tree=tree, window=window)
 
 
 def spec_sample(p, q, draft, u_accept, u_sample, n_accepted=None, token=None, stream=None):

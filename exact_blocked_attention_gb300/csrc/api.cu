@@ -80,8 +80,10 @@ int resident_ctas_per_sm(size_t smem_bytes) {
 // d = 128, no bias, 16-byte aligned query rows) if it also has T_q >= 64.
 // q_vec_ok: the query rows are contiguous and 16-byte aligned (the tcgen05
 // decode kernel loads them with 16-byte vector loads).
+// windowed: a sliding-window call (the tcgen05 decode kernel then keeps its
+// per-unit start tiles in half of its unit table).
 Plan make_plan(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tmax, int d, Elt elt,
-               int sms, bool prefill_ok, bool q_vec_ok) {
+               int sms, bool prefill_ok, bool q_vec_ok, bool windowed = false) {
   Plan pl;
   const int64_t rows = (Hq / Hkv) * Tq;  // query rows that read one KV head
   const char* force = std::getenv("BLKATTN_KERNEL");  // comparison runs only
@@ -111,7 +113,8 @@ Plan make_plan(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tmax, int
     // tiles in all, at most 255 CTAs)
     const int64_t max_tiles = B * Hkv * rg * ((Tmax + 127) / 128 + 2);  // + the per-unit weight
     if (q_vec_ok && elt == Elt::BF16 && d == 128 && !force_mma && !force_cudacore && rows >= 1 &&
-        B * rg <= blkattn::kDecodeTcMaxEntries && Tmax <= 65535LL * 128 && max_tiles < (1LL << 24) &&
+        B * rg <= (windowed ? blkattn::kDecodeTcMaxEntries / 2 : blkattn::kDecodeTcMaxEntries) &&
+        Tmax <= 65535LL * 128 && max_tiles < (1LL << 24) &&
         (sms > 0 ? sms : 148) <= 255) {
       const int64_t P = sms > 0 ? sms : 148;
       const int64_t U = B * Hkv * rg;
@@ -336,6 +339,7 @@ int ensure_counters(DeviceState* s, int64_t n, cudaStream_t stream) {
 
 struct Checked {
   int64_t B, Hq, Hkv, Tq, Tmax, d;
+  int64_t window = 0;  // sliding window (0: none)
   Elt elt;
   bool prefill_ok;  // no bias and q rows movable by TMA (see make_plan)
   bool q_vec_ok;    // query rows contiguous and 16-byte aligned
@@ -404,7 +408,7 @@ int validate_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn
   c->q_vec_ok = q->strides[3] == 1 && (reinterpret_cast<uintptr_t>(q->data) % 16) == 0 &&
                 (q->strides[0] * 2) % 16 == 0 && (q->strides[1] * 2) % 16 == 0 &&
                 (q->strides[2] * 2) % 16 == 0;
-  c->prefill_ok = bias == nullptr && tree == nullptr && c->q_vec_ok;
+  c->prefill_ok = bias == nullptr && tree == nullptr && c->q_vec_ok;  // (and no window: fwd_impl)
   return BLKATTN_OK;
 }
 
@@ -440,6 +444,7 @@ FwdParams fill_params(const blkattn_tensor* q, const blkattn_tensor* k, const bl
     p.tr_sb = tree->strides[0];
     p.tr_si = tree->strides[1];
   }
+  p.window = (int)c.window;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.out = out->data;
   p.out_bf16 = out->dtype == BLKATTN_BF16;
@@ -595,11 +600,14 @@ int fwd_with_scratch(const blkattn_tensor* q, const blkattn_tensor* k, const blk
 // per-unit counters.
 int fwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
              const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos, const blkattn_tensor* tree,
-             const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out, const blkattn_tensor* lse,
-             blkattn_stream_t stream_) {
+             int64_t window, const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out,
+             const blkattn_tensor* lse, blkattn_stream_t stream_) {
   Checked c;
   int st = validate_fwd(q, k, v, seqlens_k, q_logical_pos, tree, mask_bias, out, lse, &c);
   if (st != BLKATTN_OK) return st;
+  if (window < 0 || window > 0x7fffffff || (window > 0 && tree != nullptr)) return BLKATTN_ERR_INVALID_ARG;
+  c.window = window;
+  if (window > 0) c.prefill_ok = false;
   if (c.B == 0 || c.Tq == 0) return BLKATTN_OK;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
@@ -608,7 +616,7 @@ int fwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_ten
   st = device_state(&ds);
   if (st != BLKATTN_OK) return st;
   const Plan pl = make_plan(c.B, c.Hq, c.Hkv, c.Tq, c.Tmax, (int)c.d, c.elt, ds->sms,
-                            c.prefill_ok && scale > 0.f, c.q_vec_ok);
+                            c.prefill_ok && scale > 0.f, c.q_vec_ok, c.window > 0);
   if ((pl.cfg.kernel == blkattn::Kernel::TensorCore || pl.cfg.kernel == blkattn::Kernel::CudaCore) &&
       c.B * pl.cfg.row_groups > 65535)
     return BLKATTN_ERR_UNSUPPORTED;  // grid z of the split-KV kernels
@@ -668,7 +676,7 @@ int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_
                 const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos,
                 const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out,
                 const blkattn_tensor* lse, blkattn_stream_t stream_) {
-  return blkattn::fwd_impl(q, k, v, seqlens_k, q_logical_pos, nullptr, mask_bias, scale, out, lse, stream_);
+  return blkattn::fwd_impl(q, k, v, seqlens_k, q_logical_pos, nullptr, 0, mask_bias, scale, out, lse, stream_);
 }
 
 int blkattn_fwd_tree(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
@@ -676,7 +684,15 @@ int blkattn_fwd_tree(const blkattn_tensor* q, const blkattn_tensor* k, const blk
                      const blkattn_tensor* tree_mask, const blkattn_tensor* mask_bias, float scale,
                      const blkattn_tensor* out, const blkattn_tensor* lse, blkattn_stream_t stream_) {
   if (tree_mask == nullptr) return BLKATTN_ERR_INVALID_ARG;
-  return blkattn::fwd_impl(q, k, v, seqlens_k, q_logical_pos, tree_mask, mask_bias, scale, out, lse, stream_);
+  return blkattn::fwd_impl(q, k, v, seqlens_k, q_logical_pos, tree_mask, 0, mask_bias, scale, out, lse, stream_);
+}
+
+int blkattn_fwd_window(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
+                       const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos, int64_t window,
+                       const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out,
+                       const blkattn_tensor* lse, blkattn_stream_t stream_) {
+  if (window < 1) return BLKATTN_ERR_INVALID_ARG;
+  return blkattn::fwd_impl(q, k, v, seqlens_k, q_logical_pos, nullptr, window, mask_bias, scale, out, lse, stream_);
 }
 
 int blkattn_merge(const blkattn_states* a, const blkattn_states* b, const blkattn_states* out,

@@ -221,6 +221,15 @@ __global__ void __maxnreg__((mma_max_regs<MT, NWK>()))
     const int tbase = p.tree != nullptr ? len - p.Tq : 0x7fffffff;
     const uint64_t tr0 = p.tree != nullptr ? (uint64_t)p.tree[(int64_t)b * p.tr_sb + (int64_t)row_i_s[r0] * p.tr_si] : ~0ull;
     const uint64_t tr1 = p.tree != nullptr ? (uint64_t)p.tree[(int64_t)b * p.tr_sb + (int64_t)row_i_s[r1] * p.tr_si] : ~0ull;
+    // sliding window: each row's first visible key (pos >= 0 first, so the
+    // difference cannot overflow)
+    int ws0 = 0, ws1 = 0;
+    if (p.window > 0) {
+      const int q0 = p.qpos[b * p.qp_sb + row_i_s[r0] * p.qp_si];
+      const int q1 = p.qpos[b * p.qp_sb + row_i_s[r1] * p.qp_si];
+      ws0 = q0 < 0 ? 0 : max(0, q0 - p.window + 1);
+      ws1 = q1 < 0 ? 0 : max(0, q1 - p.window + 1);
+    }
     const float* bias0 = nullptr;
     const float* bias1 = nullptr;
     if (p.bias != nullptr) {
@@ -274,7 +283,7 @@ __global__ void __maxnreg__((mma_max_regs<MT, NWK>()))
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int key = key_base + nt * 8 + 2 * t + e;
-          bool v0 = key < hi0, v1 = key < hi1;
+          bool v0 = key < hi0 && key >= ws0, v1 = key < hi1 && key >= ws1;
           if (key >= tbase) {
             const int node = key - tbase;
             v0 = v0 && node < 64 && ((tr0 >> (node & 63)) & 1ull);

@@ -237,9 +237,16 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     // token tree: keys from tbase on are seen only where the row's mask says
     const int tbase = p.tree != nullptr ? len - p.Tq : 0x7fffffff;
     uint64_t row_tree[R];
+    int row_lo[R];  // sliding window: each row's first visible key
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+    for (int r = 0; r < R; ++r) {
       row_tree[r] = p.tree != nullptr ? (uint64_t)p.tree[(int64_t)b * p.tr_sb + (int64_t)row_i[r] * p.tr_si] : ~0ull;
+      row_lo[r] = 0;
+      if (p.window > 0) {  // (pos >= 0 first: the difference cannot overflow)
+        const int ps = p.qpos[b * p.qp_sb + row_i[r] * p.qp_si];
+        row_lo[r] = ps < 0 ? 0 : max(0, ps - p.window + 1);
+      }
+    }
 
     for (int t = 0; t < n_tiles; ++t) {
       const int st = t % STAGES;
@@ -280,7 +287,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], 16);
-        bool vis = key < row_hi[r];
+        bool vis = key < row_hi[r] && key >= row_lo[r];
         if (key >= tbase) {
           const int node = key - tbase;
           vis = vis && node < 64 && ((row_tree[r] >> (node & 63)) & 1ull);

@@ -102,12 +102,13 @@ struct RowFacts {
   int64_t boff[NR];  // bias row offsets (elements)
   int64_t ooff[NR];  // output row offsets
   int64_t loff[NR];  // lse offsets
-  uint64_t tree[NR]; // token tree: bit k = the row sees key tree_base + k (all ones without a tree)
+  uint64_t tree[NR]; // token tree: bit k = the row sees key tree_base + k (all ones without a tree);
+                     // with a sliding window instead: the row's first visible key
   int end[NR];       // visible keys are [0, end): min(len, pos + 1), 0 for padding rows
   int unit_end;      // max over the rows
   int min_end;       // min over the real rows
   int tree_base;     // first key of the token tree (len - T_q); INT_MAX without a tree
-  int pad;
+  int win_max;       // sliding window: the largest first visible key of the rows (0 without)
 };
 
 template <int NR>
@@ -157,6 +158,9 @@ struct Cursor {
   int64_t t, su;
   int b, kvh, rg, j, n;
   int extra;
+  int s0;               // the unit's first tile (sliding window; 0 otherwise)
+  const uint16_t* st;   // per-unit first tiles, or nullptr
+  __device__ __forceinline__ int key0() const { return (s0 + j) * BK; }
   // to the first tile of the next unit
   __device__ __forceinline__ void step_unit(const uint16_t* ntab, int RG, int Hkv, int B) {
     su += n + extra;
@@ -170,6 +174,7 @@ struct Cursor {
       }
     }
     n = (b < B) ? (int)ntab[b * RG + rg] : 1;
+    s0 = (b < B && st != nullptr) ? (int)st[b * RG + rg] : 0;
   }
   __device__ __forceinline__ void next(const uint16_t* ntab, int RG, int Hkv, int B) {
     if (j + 1 == n) {
@@ -269,6 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   RowFacts<NR>* facts0 = reinterpret_cast<RowFacts<NR>*>(sm + L::kOffRows);
   uint16_t* ntab = reinterpret_cast<uint16_t*>(sm + L::kOffNTab);
+  // sliding window: the units' first tiles in the upper half of the table
+  // (window calls have at most kDecodeTcMaxEntries / 2 units)
+  uint16_t* stab = ntab + kDecodeTcMaxEntries / 2;
   float* red = reinterpret_cast<float*>(sm + L::kOffRed);
   float* s_m = reinterpret_cast<float*>(sm + L::kOffStat);  // reference maximum, -inf = none yet
   float* s_muse = s_m + NR;                                  // m, or 0 when none yet
@@ -313,18 +321,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int len_raw = p.seqlens[b * p.sl_s];
       const int pk0 = rg * R;
       const int pk1 = min(pk0 + R, p.rows_per_head);
-      int maxpos = -1;
+      int maxpos = -1, minpos = 0x7fffffff;  // minpos over the rows that see keys
       if (pk1 - pk0 >= p.Tq) {
 #pragma unroll 4
-        for (int i = 0; i < p.Tq; ++i) maxpos = max(maxpos, p.qpos[b * p.qp_sb + i * p.qp_si]);
+        for (int i = 0; i < p.Tq; ++i) {
+          const int ps = p.qpos[b * p.qp_sb + i * p.qp_si];
+          maxpos = max(maxpos, ps);
+          if (ps >= 0) minpos = min(minpos, ps);
+        }
       } else {
 #pragma unroll 4
-        for (int pk = pk0; pk < pk1; ++pk) maxpos = max(maxpos, p.qpos[b * p.qp_sb + (pk % p.Tq) * p.qp_si]);
+        for (int pk = pk0; pk < pk1; ++pk) {
+          const int ps = p.qpos[b * p.qp_sb + (pk % p.Tq) * p.qp_si];
+          maxpos = max(maxpos, ps);
+          if (ps >= 0) minpos = min(minpos, ps);
+        }
       }
       const int len = len_raw < 0 ? 0 : (len_raw > p.Tmax ? p.Tmax : len_raw);
       const int uend = maxpos < 0 ? 0 : min(maxpos + 1, len);
-      const int n = (uend + BK - 1) / BK;
+      // sliding window: the unit starts at the tile of its earliest visible key
+      const int s0 = (p.window > 0 && minpos != 0x7fffffff) ? max(0, minpos - p.window + 1) / BK : 0;
+      const int n = (uend + BK - 1) / BK - s0;
       ntab[e] = (uint16_t)(n < 1 ? 1 : n);  // an all-empty unit still takes one (masked) tile
+      if (p.window > 0) stab[e] = (uint16_t)s0;
     }
     if (threadIdx.x == 0) {
       misc[1] = 0;
@@ -440,6 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   cur.j = start->j;
   cur.n = (t0 < t1) ? (int)ntab[cur.b * RG + cur.rg] : 1;
   cur.extra = kUnitExtra;
+  cur.st = p.window > 0 ? stab : nullptr;
+  cur.s0 = (t0 < t1 && cur.st != nullptr) ? (int)stab[cur.b * RG + cur.rg] : 0;
   // a range may start among a unit's weight-only tiles: begin at the next unit
   if (t0 < t1 && cur.j >= cur.n) cur.step_unit(ntab, RG, Hkv, B);
 
@@ -464,8 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           unsigned char* dst = sm + L::kOffRing + s * kSlotBytes;
           const void* map = kv ? static_cast<const void*>(&tmv) : static_cast<const void*>(&tmk);
           mbar_arrive_expect_tx(&full[s], kSlotBytes);
-          tma_load_4d(dst, map, 0, cur.j * BK, cur.kvh, cur.b, &full[s], pol);
-          tma_load_4d(dst + kBox, map, 64, cur.j * BK, cur.kvh, cur.b, &full[s], pol);
+          tma_load_4d(dst, map, 0, cur.key0(), cur.kvh, cur.b, &full[s], pol);
+          tma_load_4d(dst + kBox, map, 64, cur.key0(), cur.kvh, cur.b, &full[s], pol);
           issued = seq + 1;
         }
         // after the first tile, let the first unit's query rows land before
@@ -514,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (real[h2] && p.bias != nullptr) {
           // the bias of the unit's first tile into L2 now (new rows miss)
           const int64_t bo = (int64_t)b * p.bi_sb + (int64_t)hrow[h2] * p.bi_sh + (int64_t)irow[h2] * p.bi_si;
-          const int j0 = cur.j * BK;
+          const int j0 = cur.key0();
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             const int key = j0 + 32 * q4;
@@ -543,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // integer facts of the rows
       const int len = len_raw < 0 ? 0 : (len_raw > p.Tmax ? p.Tmax : len_raw);
       RowFacts<NR>& rf = facts0[qb];
-      int umax = 0, umin = 0x7fffffff;
+      int umax = 0, umin = 0x7fffffff, wmax = 0;
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         const int r = lane + 32 * h2;
@@ -555,6 +576,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int h = hrow[h2], i = irow[h2];
           e = pos[h2] < 0 ? 0 : min(pos[h2] + 1, len);
           if (p.tree != nullptr) tr = (uint64_t)p.tree[(int64_t)b * p.tr_sb + (int64_t)i * p.tr_si];
+          if (p.window > 0) {  // the row's first visible key (no overflow: pos >= 0 first)
+            tr = (uint64_t)(pos[h2] < 0 ? 0 : max(0, pos[h2] - p.window + 1));
+            wmax = max(wmax, (int)tr);
+          }
           bo = (int64_t)b * p.bi_sb + (int64_t)h * p.bi_sh + (int64_t)i * p.bi_si;
           oo = (int64_t)b * p.o_sb + (int64_t)h * p.o_sh + (int64_t)i * p.o_si;
           lo = (int64_t)b * p.l_sb + (int64_t)h * p.l_sh + (int64_t)i * p.l_si;
@@ -571,11 +596,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int off = 16; off >= 1; off >>= 1) {
         umax = max(umax, __shfl_xor_sync(0xffffffffu, umax, off));
         umin = min(umin, __shfl_xor_sync(0xffffffffu, umin, off));
+        wmax = max(wmax, __shfl_xor_sync(0xffffffffu, wmax, off));
       }
       if (lane == 0) {
         rf.unit_end = umax;
         rf.min_end = umin;
         rf.tree_base = p.tree != nullptr ? len - p.Tq : 0x7fffffff;
+        rf.win_max = wmax;
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q rows -> tensor core
       __syncwarp();
@@ -844,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool w = bar_and(kBarRows, kKeyThreads, wait_all(&q_full[ub], (uint32_t)((uidx >> 1) & 1)));
         if (!w) { ok = false; break; }
       }
-      const int key0 = cur.j * BK;
+      const int key0 = cur.key0();
       const int key = key0 + k;
       float x[NH];
       if (has_bias) {
@@ -886,6 +913,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int r = 0; r < NH; ++r)
             if (key >= rf.end[c0 + r]) x[r] = kNegInf;
+        }
+        if (key0 < rf.win_max) {
+          // sliding window: keys before a row's first visible key
+#pragma unroll
+          for (int r = 0; r < NH; ++r)
+            if (key < (int)rf.tree[c0 + r]) x[r] = kNegInf;
         }
         if (key0 + BK > rf.tree_base) {
           // token tree: inside it a row sees only the nodes of its mask
@@ -1087,7 +1120,8 @@ size_t decode_tc_smem_bytes(int nr) {
 
 cudaError_t launch_decode_tc(const FwdParams& p, int ctas, const CUtensorMap& tmk, const CUtensorMap& tmv,
                              cudaStream_t stream) {
-  if (p.rows_cta < 1 || p.rows_cta > 48 || ctas < 1 || p.B * p.row_groups > kDecodeTcMaxEntries)
+  if (p.rows_cta < 1 || p.rows_cta > 48 || ctas < 1 ||
+      p.B * p.row_groups > (p.window > 0 ? kDecodeTcMaxEntries / 2 : kDecodeTcMaxEntries))
     return cudaErrorInvalidValue;
   if (p.rows_cta <= 16) return launch_nr<16>(p, ctas, tmk, tmv, stream);
   if (p.rows_cta <= 32) return launch_nr<32>(p, ctas, tmk, tmv, stream);

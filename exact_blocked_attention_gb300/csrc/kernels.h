@@ -37,6 +37,8 @@ struct FwdParams {
   // are not affected
   const int64_t* tree;
   int64_t tr_sb, tr_si;
+  // optional sliding window: > 0 keeps only keys j > pos - window
+  int window;
   float scale_log2;  // scale * log2(e): scores are kept in base-2 units
   // results
   void* out;
@@ -139,10 +141,11 @@ int fwd_with_scratch(const blkattn_tensor* q, const blkattn_tensor* k, const blk
                      void* scratch, size_t scratch_bytes);
 // Records a CUDA failure for blkattn_last_cuda_error; returns BLKATTN_ERR_CUDA.
 int report_cuda_failure(cudaError_t e);
-// blkattn_fwd / blkattn_fwd_tree (tree may be NULL) on the library's workspace.
+// blkattn_fwd / _tree / _window (tree may be NULL, window 0 = none) on the
+// library's workspace.
 int fwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
              const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos, const blkattn_tensor* tree,
-             const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out, const blkattn_tensor* lse,
-             blkattn_stream_t stream);
+             int64_t window, const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out,
+             const blkattn_tensor* lse, blkattn_stream_t stream);
 
 }  // namespace blkattn

@@ -22,6 +22,9 @@ additive bias M_j, grouped heads, and the cached-decoding positions of
                 random 128-key blocks of 10% of the sequences and every key of
                 1% of the (sequence, row) pairs, bf16
   prefill       batch 2, 32 heads (MHA), d=128, T_q=T_k=8192, row i at i, bf16
+  window_decode batch 16, 32/8 heads, d=128, T_q=1 at len-1, cache lengths
+                uniform in [8192, 16384], a sliding window of 4096 keys
+                ("Chapter 33" §33.7, the paragraph of eq. 33.16), bf16
   tree_verify   spec_verify's batch, heads, cache lengths and values with a
                 token tree of T_q=6 draft nodes per sequence ("推理加速算法"
                 §7.2.2 Medusa, tree attention verification): seeded random
@@ -64,6 +67,7 @@ class Spec:
     bias_block_frac: float = 0.0
     masked_row_frac: float = 0.0
     tree: str = "none"           # "none" | "random" (token tree of T_q nodes per sequence)
+    window: int = 0              # sliding window of keys (0: none)
     notes: str = field(default="", compare=False)
 
     @property
@@ -88,6 +92,8 @@ SPECS = {
     # place of the 5-row chain and the bias
     "tree_verify": Spec("tree_verify", 8, 64, 8, 6, 32774, 128, "bf16", ("verify", 1024, 32768), "tree", 3,
                         tree="random"),
+    "window_decode": Spec("window_decode", 16, 32, 8, 1, 16384, 128, "bf16", ("uniform", 8192, 16384), "last", 8,
+                          window=4096),
 }
 
 # Reduced twins: same structure, sizes the fp64 oracle covers in seconds, still
@@ -100,6 +106,8 @@ SMALL = {
                            lens=("verify", 300, 1285), bias_seq_frac=0.34, masked_row_frac=0.07),
     "prefill": replace(SPECS["prefill"], B=1, Hq=2, Hkv=2, Tq=333, Tmax=333, lens=("fixed", 333)),
     "tree_verify": replace(SPECS["tree_verify"], B=3, Hq=16, Hkv=2, Tmax=1290, lens=("verify", 300, 1284)),
+    "window_decode": replace(SPECS["window_decode"], B=3, Hq=8, Hkv=2, Tmax=1500, lens=("uniform", 200, 1500),
+                             window=333),
 }
 
 
@@ -212,6 +220,7 @@ def generate(s: Spec, poison_padding: float | None = None) -> dict:
         "qpos": torch.from_numpy(qpos.astype(np.int32)),
         "bias": None if bias is None else torch.from_numpy(bias),
         "tree": None if tree is None else torch.from_numpy(tree),
+        "window": s.window,
         "scale": s.scale,
         "spec": s,
     }
@@ -222,6 +231,8 @@ def kv_bytes(s: Spec, seqlens) -> int:
     (sequence, KV head), each read once."""
     elt = 2 if s.dtype == "bf16" else 4
     lens = np.minimum(np.asarray(seqlens, dtype=np.int64), s.Tmax)
+    if s.window:  # rows at len - 1 see only the last `window` keys
+        lens = np.minimum(lens, s.window)
     return int(lens.sum()) * s.Hkv * s.d * elt * 2
 
 

@@ -148,6 +148,27 @@ int blkattn_fwd_tree(const blkattn_tensor* q, const blkattn_tensor* k,
                      blkattn_stream_t stream);
 
 /*
+ * blkattn_fwd_window — blkattn_fwd with sliding-window attention.
+ *
+ * "Chapter 33: inference compute optimisation" §33.7 (the paragraph of
+ * eq. 33.16): only the keys of the prescribed range stay visible.
+ * Arguments as blkattn_fwd, plus window >= 1: a row at logical position pos
+ * sees only keys j with pos - window < j <= pos (the window most recent
+ * positions up to its own), on top of the length, position and bias
+ * conditions.  The decode/verify kernels skip the key tiles before a unit's
+ * earliest visible key; window calls never take the prefill kernel, and the
+ * tcgen05 decode kernel takes at most 512 (sequence x row group) units of
+ * them (more go to the split kernels).  Returns as blkattn_fwd;
+ * BLKATTN_ERR_INVALID_ARG also for window < 1 or window > 2^31 - 1.
+ */
+int blkattn_fwd_window(const blkattn_tensor* q, const blkattn_tensor* k,
+                       const blkattn_tensor* v, const blkattn_tensor* seqlens_k,
+                       const blkattn_tensor* q_logical_pos, int64_t window,
+                       const blkattn_tensor* mask_bias, float scale,
+                       const blkattn_tensor* out, const blkattn_tensor* lse,
+                       blkattn_stream_t stream);
+
+/*
  * blkattn_spec_sample — one speculative-decoding verification step per
  * sequence ("Chapter 33: inference compute optimisation" §33.5,
  * eqs. 33.10–33.13; §33.6 for the in-order rule).

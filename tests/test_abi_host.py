@@ -141,6 +141,39 @@ def test_tree_needs_at_most_64_rows(lib):
     assert call_fwd_tree(lib, e["q"], e["k"], e["v"], e["sl"], e["qp"], empty_tree, None, e["out"], e["lse"]) == 0
 
 
+def call_fwd_window(lib, a, window):
+    ds = [None if a[n] is None else a[n].desc() for n in ("q", "k", "v", "sl", "qp", "bias", "out", "lse")]
+    ref = lambda d: None if d is None else ctypes.byref(d)
+    return lib.blkattn_fwd_window(*[ref(x) for x in ds[:5]], ctypes.c_int64(window), ref(ds[5]),
+                                  ctypes.c_float(0.1), ref(ds[6]), ref(ds[7]), None)
+
+
+@pytest.mark.parametrize("window", [0, -1, -(1 << 40), 1 << 31, 1 << 40],
+                         ids=["zero", "negative", "very-negative", "above-int32", "huge"])
+def test_window_must_be_a_positive_int32(lib, window):
+    a = good_args()
+    assert call_fwd_window(lib, a, window) == -1
+
+
+def test_window_requests_share_the_tensor_checks(lib):
+    a = good_args()
+    a["qp"] = FakeTensor((2, 4), torch.int32)
+    assert call_fwd_window(lib, a, 100) == -1
+    a = good_args(d=96)
+    assert call_fwd_window(lib, a, 100) == -2
+    e = good_args(B=0)
+    for t in e.values():
+        if t is not None:
+            t.addr = 0
+    assert call_fwd_window(lib, e, 1) == 0            # empty problem: nothing to do
+    assert call_fwd_window(lib, e, (1 << 31) - 1) == 0
+
+
+def test_window_and_tree_are_exclusive_in_the_binding():
+    with pytest.raises(ValueError):
+        blkattn.fwd(*([None] * 6), 0.1, None, None, tree=object(), window=4)
+
+
 def call_spec(lib, p, q, draft, ua, us, n, tok):
     ds = [None if t is None else t.desc() for t in (p, q, draft, ua, us, n, tok)]
     ref = lambda d: None if d is None else ctypes.byref(d)

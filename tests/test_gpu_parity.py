@@ -39,7 +39,7 @@ def to_dev(inp):
 def run_gpu(inp, out_dtype=torch.float32):
     g = to_dev(inp)
     out, lse = blkattn.attention(g["q"], g["k"], g["v"], g["seqlens"], g["qpos"], g["bias"],
-                                 g["scale"], out_dtype=out_dtype, tree=g.get("tree"))
+                                 g["scale"], out_dtype=out_dtype, tree=g.get("tree"), window=g.get("window", 0))
     torch.cuda.synchronize()
     assert blkattn.check_device_error() == 0
     d = out.shape[-1]
@@ -48,7 +48,7 @@ def run_gpu(inp, out_dtype=torch.float32):
 
 def run_oracle(inp, rows=None):
     return oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"], inp["qpos"], inp["scale"],
-                            bias=inp["bias"], rows=rows, tree=inp.get("tree"))
+                            bias=inp["bias"], rows=rows, tree=inp.get("tree"), window=inp.get("window", 0))
 
 
 def assert_parity(o, l, ref, tol_o, tol_l, out_raw=None, bf16_out=False):
@@ -125,7 +125,8 @@ def sample_rows(s, inp, n_random=160, seed=0):
     return np.array(sorted(rows), dtype=np.int64)
 
 
-@pytest.mark.parametrize("name", ["decode_gqa", "long_decode", "spec_verify", "prefill", "tree_verify"])
+@pytest.mark.parametrize("name", ["decode_gqa", "long_decode", "spec_verify", "prefill", "tree_verify",
+                                  "window_decode"])
 def test_full_size_workload_sampled_rows(name):
     s = workloads.spec(name)
     inp = workloads.generate(s)
@@ -432,6 +433,111 @@ def test_tree_chain_equals_causal_verify_bitwise():
     raw_c, lse_c, _, _ = run_gpu(causal)
     assert torch.equal(raw_t, raw_c)
     assert torch.equal(lse_t, lse_c)
+
+
+# "Chapter 33: inference compute optimisation" §33.7 (the paragraph of
+# eq. 33.16): sliding-window attention, each row at position pos sees the keys
+# pos - W < j <= pos (blkattn_fwd_window).
+
+def window_case(name):
+    rng = np.random.default_rng(WINDOW_CASES.index(name) + 60)
+    dtype, d, bias = "bf16", 128, None
+    if name == "tc_nr16":            # decode, 16 rows per KV head
+        B, Hq, Hkv, lens, W = 3, 32, 2, [3000, 1290, 17], 500
+        qpos = [[ln - 1] for ln in lens]
+    elif name == "tc_verify_nr48":   # causal verification rows: a different start per row
+        B, Hq, Hkv, lens, W = 3, 16, 2, [2000, 700, 300], 333
+        qpos = [[ln - 6 + i for i in range(6)] for ln in lens]
+    elif name == "tc_two_groups":    # 64 rows of one head: two row groups of 32 (never prefill)
+        B, Hq, Hkv, lens, W = 2, 2, 2, [1900, 640], 100
+        qpos = [[ln - 64 + i for i in range(64)] for ln in lens]
+    elif name == "tc_window_one":    # each row sees exactly its own key
+        B, Hq, Hkv, lens, W = 2, 16, 2, [900, 5], 1
+        qpos = [[ln - 3 + i for i in range(3)] for ln in lens]
+    elif name == "tc_tile_edges":    # windows that start on and next to key-tile edges
+        B, Hq, Hkv, lens, W = 4, 16, 2, [4097, 4096, 129, 256], 128
+        qpos = [[ln - 1, ln - 2] for ln in lens]
+    elif name == "tc_mixed_positions":  # pos < 0, 0, beyond the length and far apart in one unit
+        B, Hq, Hkv, lens, W = 3, 16, 2, [3000, 1500, 10], 50
+        qpos = [[-1, 0, 2999, 1000], [5000, 1499, 1400, 60], [-3, 9, 20, 4]]
+    elif name == "tc_bias":          # the window and an additive bias with -inf entries
+        B, Hq, Hkv, lens, W = 2, 8, 2, [1500, 800], 400
+        qpos = [[ln - 2, ln - 1] for ln in lens]
+        g = torch.Generator().manual_seed(9)
+        bias = torch.randn(B, Hq, 2, max(lens) + 3, generator=g)
+        bias[torch.rand(B, Hq, 2, max(lens) + 3, generator=g) < 0.25] = -math.inf
+        bias[0, 1, 0, 1099:] = -math.inf  # the whole window masked: an empty row
+    elif name == "many_units":       # more units than the tcgen05 kernel takes with a window
+        B, Hq, Hkv, W = 600, 4, 1, 100
+        lens = rng.integers(1, 700, B).tolist()
+        qpos = [[ln - 1] for ln in lens]
+    elif name == "d64_mma":          # head dim 64: the mma.sync split kernel
+        B, Hq, Hkv, lens, W, d = 2, 8, 2, [2000, 777], 300, 64
+        qpos = [[ln - 4 + i for i in range(4)] for ln in lens]
+    else:                            # fp32_split: the CUDA-core split kernel
+        B, Hq, Hkv, lens, W, dtype, d = 2, 4, 2, [1300, 515], 77, "f32", 64
+        qpos = [[ln - 3 + i for i in range(3)] for ln in lens]
+    Tmax = max(lens) + 3
+    Tq = len(qpos[0])
+    inp = make_case(B, Hq, Hkv, Tq, Tmax, d, dtype, lens, qpos, bias=bias, seed=int(rng.integers(1 << 30)))
+    inp["window"] = W
+    return inp
+
+
+WINDOW_CASES = ["tc_nr16", "tc_verify_nr48", "tc_two_groups", "tc_window_one", "tc_tile_edges",
+                "tc_mixed_positions", "tc_bias", "many_units", "d64_mma", "fp32_split"]
+
+
+@pytest.mark.parametrize("name", WINDOW_CASES)
+def test_window_cases(name):
+    inp = window_case(name)
+    if name.startswith("tc_") and name != "tc_two_groups":  # (the debug plan has no window flag)
+        assert plan_of(inp)["kernel"] == 3
+    raw, _, o, l = run_gpu(inp)
+    ref = run_oracle(inp)
+    tol = (F32_TOL, F32_TOL) if inp["q"].dtype == torch.float32 else (BF16_TOL_O, BF16_TOL_L)
+    assert_parity(o, l, ref, *tol)
+    if name == "tc_window_one":  # one visible key: the output is that key's value row
+        B, Hq, Tq = inp["q"].shape[:3]
+        G = Hq // inp["k"].shape[1]
+        for b in range(B):
+            for h in range(Hq):
+                for i in range(Tq):
+                    pos = int(inp["qpos"][b, i])
+                    if 0 <= pos < int(inp["seqlens"][b]):
+                        want = inp["v"][b, h // G, pos].float()
+                        assert torch.allclose(raw[b, h, i], want, rtol=2.0 ** -8, atol=1e-6)
+
+
+@pytest.mark.parametrize("name", ["tc_verify_nr48", "d64_mma", "fp32_split"])
+def test_window_covering_the_cache_changes_no_bit(name):
+    """A window at least as long as every row's key range masks nothing: the
+    same kernel, the same bits as the call without a window."""
+    inp = window_case(name)
+    plain = dict(inp)
+    plain["window"] = 0
+    wide = dict(inp)
+    wide["window"] = int(inp["seqlens"].max()) + 1
+    raw_p, lse_p, _, _ = run_gpu(plain)
+    raw_w, lse_w, _, _ = run_gpu(wide)
+    assert torch.equal(raw_p, raw_w)
+    assert torch.equal(lse_p, lse_w)
+
+
+def test_window_error_bound_of_eq_33_16():
+    """Eq. 33.16 on the kernel's own outputs: with delta the softmax mass the
+    full row puts outside the window (1 - exp(lse_W - lse_full)) and M the
+    largest value norm, |o_full - o_W| <= 2 delta M."""
+    inp = window_case("tc_nr16")
+    _, lse_w, o_w, l_w = run_gpu(inp)
+    full = dict(inp)
+    full["window"] = 0
+    _, _, o_f, l_f = run_gpu(full)
+    delta = 1.0 - np.exp(l_w.astype(np.float64) - l_f.astype(np.float64))
+    M = float(inp["v"].float().norm(dim=-1).max())
+    gap = np.linalg.norm(o_f.astype(np.float64) - o_w.astype(np.float64), axis=-1)
+    assert np.all(gap <= 2.0 * delta * M + 1e-2)
+    assert np.any(delta > 0.1)  # the window really drops mass here
 
 
 # ------------------------------------------------------------ tcgen05 prefill kernel
