@@ -25,6 +25,11 @@ Contents
                    (§33.5 eqs. 33.10–33.13, the in-order rule of §33.6),
                    pinned by tests/test_spec_sampling_pins.py against
                    Example 25.2 and Exercises 33.7 and 33.9.
+  backward         the gradients of eqs. 33.6–33.8 (§33.3) in numpy fp64,
+                   pinned by tests/test_backward_pins.py against finite
+                   differences of attention(), fp64 autograd of a separate
+                   dense formulation, Exercise 33.4's row-sum identity and
+                   closed forms.
 """
 from __future__ import annotations
 
