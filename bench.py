@@ -443,6 +443,46 @@ def measure_spec_sample(peaks, steps=10, warmup=3):
                          "algorithmic_bytes": total, "peak_note": f"HBM copy bandwidth, {peaks['source']}"}}
 
 
+def measure_backward(peaks, steps=5, warmup=3):
+    """The backward pass (blkattn_bwd: row facts, dQ, dK/dV) on the causal
+    prefill workload with an upstream gradient; inputs come from the
+    library's own forward.  Algorithmic work: the five products of eqs.
+    33.6-33.8, 10 * d flops per (row, visible key) (2.5x the forward's 4 * d);
+    the kernels form S and G_P twice, 7 products in all."""
+    from exact_blocked_attention_gb300 import blkattn
+    s = workloads.backward_spec()
+    cpu = workloads.generate_backward(s)
+    dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in cpu.items()}
+    out, lse = blkattn.attention(dev["q"], dev["k"], dev["v"], dev["seqlens"], dev["qpos"], None, cpu["scale"])
+    dq = torch.empty(dev["q"].shape, dtype=torch.float32, device="cuda")
+    dk = torch.empty(dev["k"].shape, dtype=torch.float32, device="cuda")
+    dv = torch.empty(dev["v"].shape, dtype=torch.float32, device="cuda")
+    call = lambda: blkattn.bwd(dev["q"], dev["k"], dev["v"], dev["seqlens"], dev["qpos"], None, cpu["scale"],
+                               out, lse, dev["go"], dq, dk, dv)
+    in_bytes = sum(t.numel() * t.element_size() for t in (dev["q"], dev["k"], dev["v"], dev["go"], out, lse))
+    times = []
+    for it in range(warmup + steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        if it >= warmup:
+            times.append(e0.elapsed_time(e1))
+    assert blkattn.check_device_error() == 0
+    t_ms = sum(times) / len(times)
+    flops = causal_flops(s, cpu) * 2.5
+    achieved = flops / (t_ms * 1e-3) / 1e12
+    return {"workload": f"prefill_backward: {describe(s)} + g_o bf16; dq, dk, dv f32",
+            "us_per_call": t_ms * 1e3, "l2": f"inputs ({in_bytes / 1e6:.0f} MB) larger than L2",
+            "kernels": "row facts, dQ (3 products per tile pair), dK/dV (4 products per tile pair)",
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": achieved / peaks["bf16_tflops"], "traffic": measured_traffic("prefill_backward"),
+                         "algorithmic_flops": flops,
+                         "peak_note": f"dense bf16 burst, {peaks['source']}"},
+            "frac_of_bf16_sustained": achieved / peaks["bf16_tflops_sustained"]}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -454,6 +494,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-sampling", action="store_true",
                     help="time only the speculative-sampling step and print its entry")
+    ap.add_argument("--only-backward", action="store_true",
+                    help="time only the backward pass and print its entry")
     ap.add_argument("--ref-budget-s", type=float, default=60.0,
                     help="--impl reference: seconds of oracle work over all steps")
     args = ap.parse_args()
@@ -474,6 +516,12 @@ def main():
         blkattn.load()
         if rank == 0:
             print(json.dumps(measure_spec_sample(peaks, steps=args.steps, warmup=args.warmup)), flush=True)
+        return
+    if args.only_backward:
+        from exact_blocked_attention_gb300 import blkattn
+        blkattn.load()
+        if rank == 0:
+            print(json.dumps(measure_backward(peaks, steps=args.steps, warmup=args.warmup)), flush=True)
         return
 
     # ---- headline workload: every rank runs its own batch (weak scaling) ----
@@ -535,6 +583,11 @@ def main():
             except Exception as exc:  # report, keep the headline line
                 others[name] = {"error": f"{type(exc).__name__}: {exc}"}
             torch.cuda.empty_cache()
+        try:
+            others["prefill_backward"] = measure_backward(peaks)
+        except Exception as exc:  # reported, not fatal
+            others["prefill_backward"] = {"error": f"{type(exc).__name__}: {exc}"}
+        torch.cuda.empty_cache()
         try:
             others["spec_sample"] = measure_spec_sample(peaks)
         except Exception as exc:  # reported, not fatal

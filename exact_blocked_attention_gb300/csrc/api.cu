@@ -637,6 +637,117 @@ int fwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_ten
 // blkattn_last_cuda_error like the ones here.
 int report_cuda_failure(cudaError_t e) { return cuda_fail(e); }
 
+namespace {
+
+// fp32 gradient rows written with 16-byte vector stores: unit dim stride,
+// 16-byte aligned base and strides.
+bool grad_rows_ok(const blkattn_tensor* t) {
+  if (t->dtype != BLKATTN_F32 || t->strides[3] != 1) return false;
+  if ((reinterpret_cast<uintptr_t>(t->data) % 16) != 0) return false;
+  for (int i = 0; i < 3; ++i)
+    if ((t->strides[i] * 4) % 16 != 0) return false;
+  return true;
+}
+
+// bf16 rows moved by tiled TMA: unit dim stride, 16-byte aligned base and strides.
+bool tma_rows_ok(const blkattn_tensor* t) {
+  if (t->dtype != BLKATTN_BF16 || t->strides[3] != 1) return false;
+  if ((reinterpret_cast<uintptr_t>(t->data) % 16) != 0) return false;
+  for (int i = 0; i < 3; ++i)
+    if ((t->strides[i] * 2) % 16 != 0) return false;
+  return true;
+}
+
+}  // namespace
+
+int bwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
+             const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos,
+             const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out,
+             const blkattn_tensor* lse, const blkattn_tensor* dout, const blkattn_tensor* dq,
+             const blkattn_tensor* dk, const blkattn_tensor* dv, blkattn_stream_t stream_) {
+  Checked c;
+  int st = validate_fwd(q, k, v, seqlens_k, q_logical_pos, nullptr, mask_bias, out, lse, &c);
+  if (st != BLKATTN_OK) return st;
+  if (!dims_ok(dout, 4) || !dims_ok(dq, 4) || !dims_ok(dk, 4) || !dims_ok(dv, 4)) return BLKATTN_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i) {
+    if (dout->sizes[i] != q->sizes[i] || dq->sizes[i] != q->sizes[i]) return BLKATTN_ERR_INVALID_ARG;
+    if (dk->sizes[i] != k->sizes[i] || dv->sizes[i] != k->sizes[i]) return BLKATTN_ERR_INVALID_ARG;
+  }
+  if (dout->dtype != q->dtype || dq->dtype != BLKATTN_F32 || dk->dtype != BLKATTN_F32 || dv->dtype != BLKATTN_F32)
+    return BLKATTN_ERR_INVALID_ARG;
+  if (!(scale == scale) || scale == __builtin_huge_valf() || scale == -__builtin_huge_valf())
+    return BLKATTN_ERR_INVALID_ARG;
+  if (c.B == 0) return BLKATTN_OK;
+  const bool rows = c.Tq > 0;
+  if (dk->data == nullptr || dv->data == nullptr) return BLKATTN_ERR_INVALID_ARG;
+  if (rows && (dout->data == nullptr || dq->data == nullptr)) return BLKATTN_ERR_INVALID_ARG;
+  if (!grad_rows_ok(dk) || !grad_rows_ok(dv) || (rows && !grad_rows_ok(dq))) return BLKATTN_ERR_INVALID_ARG;
+  // the tensor-core backward: bf16 operands, d = 128, TMA-movable Q and g_o rows
+  if (c.elt != Elt::BF16 || c.d != 128) return BLKATTN_ERR_UNSUPPORTED;
+  if (rows && (!tma_rows_ok(q) || !tma_rows_ok(dout))) return BLKATTN_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != BLKATTN_OK) return st;
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return cuda_fail(e);
+  const int64_t n_qt = (c.Tq + 127) / 128;
+  const int64_t n_kt = (c.Tmax + 127) / 128;
+  const int64_t nrows = c.B * c.Hq * c.Tq;
+  auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
+  const int64_t ws = 2 * al(nrows * 4) + al(c.B * n_qt * 4);
+  st = ensure_workspace(ds, (size_t)(ws > 0 ? ws : 256), stream);
+  if (st != BLKATTN_OK) return st;
+  const CUtensorMap *tmk = nullptr, *tmv = nullptr, *tmq = nullptr, *tmg = nullptr;
+  if ((st = kv_tensor_map(dev, k, 128, &tmk)) != BLKATTN_OK) return st;
+  if ((st = kv_tensor_map(dev, v, 128, &tmv)) != BLKATTN_OK) return st;
+  if (rows) {
+    if ((st = kv_tensor_map(dev, q, 128, &tmq)) != BLKATTN_OK) return st;
+    if ((st = kv_tensor_map(dev, dout, 128, &tmg)) != BLKATTN_OK) return st;
+  } else {
+    tmq = tmk;  // no query rows: the dK/dV kernel writes zeros and reads no query tile
+    tmg = tmk;
+  }
+  BwdParams p{};
+  p.out = out->data;
+  p.out_bf16 = out->dtype == BLKATTN_BF16;
+  p.o_sb = out->strides[0]; p.o_sh = out->strides[1]; p.o_si = out->strides[2]; p.o_sd = out->strides[3];
+  p.lse = static_cast<const float*>(lse->data);
+  p.l_sb = lse->strides[0]; p.l_sh = lse->strides[1]; p.l_si = lse->strides[2];
+  p.dout = dout->data;
+  p.g_sb = dout->strides[0]; p.g_sh = dout->strides[1]; p.g_si = dout->strides[2];
+  p.seqlens = static_cast<const int*>(seqlens_k->data);
+  p.sl_s = seqlens_k->strides[0];
+  p.qpos = static_cast<const int*>(q_logical_pos->data);
+  p.qp_sb = q_logical_pos->strides[0]; p.qp_si = q_logical_pos->strides[1];
+  p.bias = mask_bias ? static_cast<const float*>(mask_bias->data) : nullptr;
+  if (mask_bias) {  // size-1 dims broadcast
+    p.bi_sb = mask_bias->sizes[0] == 1 ? 0 : mask_bias->strides[0];
+    p.bi_sh = mask_bias->sizes[1] == 1 ? 0 : mask_bias->strides[1];
+    p.bi_si = mask_bias->sizes[2] == 1 ? 0 : mask_bias->strides[2];
+    p.bi_sj = mask_bias->sizes[3] == 1 ? 0 : mask_bias->strides[3];
+  }
+  p.dq = static_cast<float*>(dq->data);
+  p.dq_sb = dq->strides[0]; p.dq_sh = dq->strides[1]; p.dq_si = dq->strides[2];
+  p.dk = static_cast<float*>(dk->data);
+  p.dk_sb = dk->strides[0]; p.dk_sh = dk->strides[1]; p.dk_sj = dk->strides[2];
+  p.dv = static_cast<float*>(dv->data);
+  p.dv_sb = dv->strides[0]; p.dv_sh = dv->strides[1]; p.dv_sj = dv->strides[2];
+  char* base = static_cast<char*>(ds->ws);
+  p.ws_D = reinterpret_cast<float*>(base);
+  p.ws_L = reinterpret_cast<float*>(base + al(nrows * 4));
+  p.ws_end = reinterpret_cast<int*>(base + 2 * al(nrows * 4));
+  p.B = (int)c.B; p.Hq = (int)c.Hq; p.Hkv = (int)c.Hkv; p.G = (int)(c.Hq / c.Hkv);
+  p.Tq = (int)c.Tq; p.Tmax = (int)c.Tmax; p.n_qt = (int)n_qt; p.n_kt = (int)n_kt;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.err = ds->err;
+  if (cudaError_t e = launch_backward(p, *tmq, *tmg, *tmk, *tmv, stream); e != cudaSuccess) return cuda_fail(e);
+  return BLKATTN_OK;
+}
+
 }  // namespace blkattn
 
 extern "C" {
@@ -693,6 +804,17 @@ int blkattn_fwd_window(const blkattn_tensor* q, const blkattn_tensor* k, const b
                        const blkattn_tensor* lse, blkattn_stream_t stream_) {
   if (window < 1) return BLKATTN_ERR_INVALID_ARG;
   return blkattn::fwd_impl(q, k, v, seqlens_k, q_logical_pos, nullptr, window, mask_bias, scale, out, lse, stream_);
+}
+
+int blkattn_bwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
+                const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos,
+                const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out,
+                const blkattn_tensor* lse, const blkattn_tensor* dout, const blkattn_tensor* dq,
+                const blkattn_tensor* dk, const blkattn_tensor* dv, blkattn_stream_t stream) {
+  if (!q || !k || !v || !seqlens_k || !q_logical_pos || !out || !lse || !dout || !dq || !dk || !dv)
+    return BLKATTN_ERR_INVALID_ARG;
+  return blkattn::bwd_impl(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, dout, dq, dk, dv,
+                           stream);
 }
 
 int blkattn_merge(const blkattn_states* a, const blkattn_states* b, const blkattn_states* out,

@@ -127,6 +127,40 @@ cudaError_t launch_decode_tc(const FwdParams& p, int ctas, const CUtensorMap& tm
                              cudaStream_t stream);
 size_t decode_tc_smem_bytes(int rows_cta);
 
+// ---- backward pass (eqs. 33.6-33.8), tcgen05, bf16, d = 128 ----
+struct BwdParams {
+  const void* out;  // forward output o [B, H_q, T_q, d] (bf16 or fp32), read for D = g_o . o
+  int out_bf16;
+  int64_t o_sb, o_sh, o_si, o_sd;
+  const float* lse;  // forward lse [B, H_q, T_q] (natural log, -inf = empty row)
+  int64_t l_sb, l_sh, l_si;
+  const void* dout;  // upstream gradient g_o, bf16 [B, H_q, T_q, d] (unit dim stride)
+  int64_t g_sb, g_sh, g_si;
+  const int* seqlens;
+  int64_t sl_s;
+  const int* qpos;
+  int64_t qp_sb, qp_si;
+  const float* bias;  // nullptr or [B, H_q, T_q, T_max] view
+  int64_t bi_sb, bi_sh, bi_si, bi_sj;
+  float* dq;  // fp32 [B, H_q, T_q, d], unit dim stride, 16-byte aligned rows
+  int64_t dq_sb, dq_sh, dq_si;
+  float* dk;  // fp32 [B, H_kv, T_max, d], likewise
+  int64_t dk_sb, dk_sh, dk_sj;
+  float* dv;
+  int64_t dv_sb, dv_sh, dv_sj;
+  float* ws_D;    // [B * H_q * T_q] row sums g_o . o
+  float* ws_L;    // [B * H_q * T_q] lse in base-2 units (+inf for an empty row)
+  int* ws_end;    // [B * n_qt] largest row end min(pos + 1, len) of each 128-row query tile
+  int B, Hq, Hkv, G, Tq, Tmax, n_qt, n_kt;
+  float scale, scale_log2;
+  int* err;
+};
+// Row facts, then dQ (one CTA per 128-row query tile), then dK/dV (one CTA
+// per 128-key tile); maps: Q, g_o, K, V, boxes {64, 128}, 128-byte swizzle.
+cudaError_t launch_backward(const BwdParams& p, const CUtensorMap& tmq, const CUtensorMap& tmg,
+                            const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t stream);
+int backward_smem_bytes();
+
 // Validation only (no CUDA call), and blkattn_fwd with caller-given scratch
 // for the per-split states (no allocation; BLKATTN_ERR_SCRATCH_LIMIT when the
 // plan needs more than scratch_bytes).  Both live in api.cu.

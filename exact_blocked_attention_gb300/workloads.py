@@ -33,6 +33,9 @@ additive bias M_j, grouped heads, and the cached-decoding positions of
 
 Each has a reduced twin (``small=True``) that the fp64 oracle finishes in
 seconds while still spanning several key tiles and a ragged tail.
+
+The backward workload (§33.3, eqs. 33.6-33.8) is prefill's inputs plus an
+upstream gradient g_o drawn like q (N(0, 1), cast to bf16).
 """
 from __future__ import annotations
 
@@ -237,6 +240,18 @@ def kv_bytes(s: Spec, seqlens) -> int:
 
 
 # ---------------------------------------------------------------- speculative sampling
+def backward_spec(small: bool = False) -> Spec:
+    """Shapes of the backward workload: the causal prefill's."""
+    return spec("prefill", small)
+
+
+def generate_backward(s: Spec) -> dict:
+    """generate(s) plus the upstream gradient "go" [B, H_q, T_q, d]."""
+    inp = generate(s)
+    inp["go"] = _cast(_normal((s.B, s.Hq, s.Tq, s.d), s.seed, 21), s.dtype)
+    return inp
+
+
 # One verification step ("Chapter 33: inference compute optimisation" §33.5,
 # eqs. 33.10-33.13): target and draft distributions over a vocabulary, the
 # draft's candidates, and the random numbers of the step.  The draft's logits

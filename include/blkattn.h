@@ -243,6 +243,44 @@ int blkattn_fwd_static_scratch(const blkattn_tensor* q, const blkattn_tensor* k,
                                blkattn_stream_t stream);
 
 /*
+ * blkattn_bwd — gradients of blkattn_fwd with respect to q, k and v.
+ *
+ * "Chapter 33: inference compute optimisation" §33.3, eqs. 33.6–33.8: the
+ * probabilities are recomputed block by block from the scores and the saved
+ * lse (P = exp(S - lse)), never stored; with the upstream gradient g_o,
+ *   dv = P^T g_o,  dP = g_o v^T,  dS = P (dP - D),  D_i = g_o,i . o_i,
+ *   dq = scale dS k,  dk = scale dS^T q,
+ * where `scale` takes the place of eq. 33.8's 1/sqrt(d_h) and D is eq.
+ * 33.7's row sum in the form of Exercise 33.4.  Visibility is blkattn_fwd's
+ * (length, position, bias); invisible keys and empty rows get no gradient.
+ * With grouped heads, dk and dv of a KV head sum over its G query heads.
+ *
+ *   q, k, v, seqlens_k, q_logical_pos, mask_bias, scale: as for the
+ *        blkattn_fwd call whose gradients are wanted (bf16, d_h = 128; q rows
+ *        as k/v rows: unit dim stride, 16-byte aligned base and strides)
+ *   out  the forward output o [B,H_q,T_q,d] (bf16 or f32, any strides)
+ *   lse  the forward lse [B,H_q,T_q] (f32, natural log, -inf = empty row)
+ *   dout g_o [B,H_q,T_q,d], bf16, laid out like q
+ *   dq   f32 [B,H_q,T_q,d]; dk, dv f32 [B,H_kv,T_max,d]: unit dim stride,
+ *        16-byte aligned base and strides.  Every element is written (0 for
+ *        cache rows no query sees, including [len, T_max)).
+ * The products take P and dS as bf16 operands with fp32 accumulation; the
+ * result does not depend on the schedule (no atomics: deterministic).
+ * Uses the library's grow-only workspace (D and the base-2 lse per row).
+ * Returns as blkattn_fwd; BLKATTN_ERR_UNSUPPORTED for f32 or d_h != 128;
+ * BLKATTN_ERR_INVALID_ARG also for a non-finite scale or mismatched
+ * gradient shapes, dtypes or layouts.
+ */
+int blkattn_bwd(const blkattn_tensor* q, const blkattn_tensor* k,
+                const blkattn_tensor* v, const blkattn_tensor* seqlens_k,
+                const blkattn_tensor* q_logical_pos,
+                const blkattn_tensor* mask_bias, float scale,
+                const blkattn_tensor* out, const blkattn_tensor* lse,
+                const blkattn_tensor* dout, const blkattn_tensor* dq,
+                const blkattn_tensor* dk, const blkattn_tensor* dv,
+                blkattn_stream_t stream);
+
+/*
  * Attention states of rows, in the sufficient statistics of eq. 33.3:
  *   m [rows]           f32, the maximum score (natural-log units); -inf = empty
  *   l [rows]           f32, sum e^{z_j - m}; NULL means "normalised": l = 1 and

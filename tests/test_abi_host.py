@@ -174,6 +174,53 @@ def test_window_and_tree_are_exclusive_in_the_binding():
         blkattn.fwd(*([None] * 6), 0.1, None, None, tree=object(), window=4)
 
 
+def bwd_args(B=2, Hq=8, Hkv=2, Tq=3, Tmax=100, d=128, dt=torch.bfloat16):
+    a = good_args(B, Hq, Hkv, Tq, Tmax, d, dt)
+    a.update(dout=FakeTensor((B, Hq, Tq, d), dt), dq=FakeTensor((B, Hq, Tq, d), torch.float32),
+             dk=FakeTensor((B, Hkv, Tmax, d), torch.float32), dv=FakeTensor((B, Hkv, Tmax, d), torch.float32))
+    return a
+
+
+def call_bwd(lib, a, scale=0.1):
+    names = ("q", "k", "v", "sl", "qp", "bias", "out", "lse", "dout", "dq", "dk", "dv")
+    ds = [None if a[n] is None else a[n].desc() for n in names]
+    ref = lambda d: None if d is None else ctypes.byref(d)
+    return lib.blkattn_bwd(*[ref(x) for x in ds[:6]], ctypes.c_float(scale), *[ref(x) for x in ds[6:]], None)
+
+
+@pytest.mark.parametrize("mutate,expect", [
+    (lambda a: a.update(dout=FakeTensor((2, 8, 3, 128), torch.float32)), -1),      # g_o dtype = q dtype
+    (lambda a: a.update(dout=FakeTensor((2, 8, 4, 128), torch.bfloat16)), -1),     # g_o shape
+    (lambda a: a.update(dq=FakeTensor((2, 8, 3, 128), torch.bfloat16)), -1),       # gradients are f32
+    (lambda a: a.update(dk=FakeTensor((2, 2, 99, 128), torch.float32)), -1),       # dk shape
+    (lambda a: a.update(dv=FakeTensor((2, 8, 100, 128), torch.float32)), -1),      # dv heads
+    (lambda a: a.update(dq=FakeTensor((2, 8, 3, 128), torch.float32, addr=0x10008)), -1),  # not 16-B aligned
+    (lambda a: a.update(dk=FakeTensor((2, 2, 100, 128), torch.float32, strides=(25600, 12800, 129, 1))), -1),
+    (lambda a: a.update(q=FakeTensor((2, 8, 3, 128), torch.bfloat16, strides=(3072, 384, 130, 1))), -1),
+    (lambda a: a.update(dout=None), -1),
+    (lambda a: a.update(**bwd_args(d=64)), -2),                                     # d = 64: no backward kernel
+    (lambda a: a.update(**bwd_args(dt=torch.float32)), -2),                         # f32: no backward kernel
+], ids=["dout-dtype", "dout-shape", "dq-dtype", "dk-shape", "dv-heads", "dq-misaligned", "dk-row-stride",
+        "q-row-stride", "missing-dout", "d64", "f32"])
+def test_backward_requests_are_validated_before_cuda(lib, mutate, expect):
+    a = bwd_args()
+    mutate(a)
+    assert call_bwd(lib, a) == expect
+
+
+@pytest.mark.parametrize("scale", [float("nan"), float("inf"), -float("inf")])
+def test_backward_needs_a_finite_scale(lib, scale):
+    assert call_bwd(lib, bwd_args(), scale) == -1
+
+
+def test_backward_empty_batch_is_a_no_op(lib):
+    a = bwd_args(B=0)
+    for t in a.values():
+        if t is not None:
+            t.addr = 0
+    assert call_bwd(lib, a) == 0
+
+
 def call_spec(lib, p, q, draft, ua, us, n, tok):
     ds = [None if t is None else t.desc() for t in (p, q, draft, ua, us, n, tok)]
     ref = lambda d: None if d is None else ctypes.byref(d)
