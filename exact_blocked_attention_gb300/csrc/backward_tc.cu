@@ -15,21 +15,26 @@
 //     min(pos + 1, len) of each 128-row query tile.
 //  2. dQ: one CTA per 128-row query tile of one head, walking the key tiles
 //     its rows see.  Per tile: S = Q K^T and G_P = G_O V^T (smem x smem ->
-//     TMEM), then the rows form G_S in bf16 over G_P's columns, then
+//     TMEM), the rows form G_S in bf16 over G_P's columns, then
 //     G_Q += G_S K (A from TMEM, K as an N-major B operand).
 //  3. dK/dV: one CTA per 128-key tile of one KV head, walking the query
 //     tiles of its G query heads that see any of its keys.  Per tile:
 //     S^T = K Q^T and G_P^T = V G_O^T; the key rows form P^T and G_S^T in
-//     bf16 over their columns; then G_V += P^T G_O and G_K += G_S^T Q.
+//     bf16 over those columns; then G_V += P^T G_O and G_K += G_S^T Q.
 // Both products into one accumulator stay in one CTA, so no atomics and a
 // fixed summation order: the results are deterministic.  The price is that
 // S and G_P are formed twice (7 products of 128 x 128 x 128 per tile pair
 // instead of 5).
 //
-// Roles in kernels 2 and 3 (192 threads): warps 0-3 one thread per TMEM lane
-// (a query row in 2, a key in 3), warp 4 the TMA producer, warp 5 TMEM
-// allocation and the single MMA-issuing thread.  Products execute in issue
-// order, so the next tile's S may overwrite the columns the previous tile's
+// Roles in kernels 2 and 3 (320 threads): warps 0-7 one thread per TMEM lane
+// and half tile: group g = warp / 4 owns columns [64 g, 64 g + 64) of every
+// tile (keys in 2, query rows in 3), lane quarter warp % 4; warp 8 the TMA
+// producer; warp 9 TMEM allocation and the single MMA-issuing thread.  The
+// products of a tile are issued by half (N = 64 for S and G_P, K = 64 for
+// the accumulating ones), each half with its own barriers, so one group's
+// exponentials overlap the tensor core's work on the other half, and the
+// next tile's first half starts as soon as its columns are free.  Products
+// execute in issue order, so a new S may overwrite the columns the previous
 // products read.  Every wait is bounded (error flag, then an orderly exit).
 //
 // Visibility is the forward's (length, position, bias; select, not add):
@@ -47,16 +52,17 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int BT = 128;  // rows of a query tile, keys of a key tile (TMEM lanes)
+constexpr int HT = 64;   // half tile: the columns of one group
 constexpr int D = 128;   // head dim
 constexpr int STAGES = 2;
 constexpr int kBox = 128 * 128;       // one 64-dim (128-byte) box of 128 rows: 16 KB
 constexpr int kTileBytes = 2 * kBox;  // 128 rows x 128 dims, bf16
-constexpr int kThreads = 192;
-constexpr int kTmaWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 320;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kIdescKK = tc::idesc_bf16(128, 128, 0, 0);  // both operands K-major
-constexpr uint32_t kIdescTN = tc::idesc_bf16(128, 128, 0, 1);  // A in TMEM, B N-major
+constexpr uint32_t kIdescHalf = tc::idesc_bf16(128, HT, 0, 0);  // S half: both K-major, N = 64
+constexpr uint32_t kIdescTN = tc::idesc_bf16(128, 128, 0, 1);   // A in TMEM, B N-major, N = 128
 
 // Shared memory: two stationary tiles, two 2-stage rings, barriers, facts.
 constexpr int kOffA0 = 0;                             // dQ: Q    | dK/dV: K
@@ -66,32 +72,34 @@ constexpr int kOffR1 = kOffR0 + STAGES * kTileBytes;  // dQ: V ring | dK/dV: G_O
 constexpr int kOffBar = kOffR1 + STAGES * kTileBytes;
 constexpr int kNumBars = 16;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kOffFacts = kOffMisc + 64;                   // dK/dV: [2][3][128] (L, D, end)
-constexpr int kSmemBytes = kOffFacts + 2 * 3 * 128 * 4 + 1024;  // + slack to align to 1024
+constexpr int kOffFacts = kOffMisc + 64;                      // dK/dV: float4 [2][128] (L, D, end, -)
+constexpr int kSmemBytes = kOffFacts + 2 * 128 * 16 + 1024;  // + slack to align to 1024
 
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
-// S (or S^T) = A B^T over d = 128: both operands K-major, 128-byte swizzled.
-__device__ __forceinline__ void issue_kk(uint32_t dcol, uint32_t sa, uint32_t sb) {
+// Half g of S = A B^T over d = 128: A = 128 rows (all), B = rows [64 g, 64 g
+// + 64) of a 128-row tile; both K-major, 128-byte swizzled (rows 64.. start
+// 8 KB into each 64-dim box, a whole number of 8-row atoms).
+__device__ __forceinline__ void issue_half(uint32_t dcol, uint32_t sa, uint32_t sb, int g) {
   const uint32_t alo = tc::desc_lo(sa, 16);
-  const uint32_t blo = tc::desc_lo(sb, 16);
+  const uint32_t blo = tc::desc_lo(sb + (uint32_t)(g * HT * 128), 16);
   constexpr uint32_t kHi = tc::desc_hi(1024);
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
     const uint32_t off = (uint32_t)(((ks >> 2) * kBox + (ks & 3) * 32) >> 4);
-    tc::mma_ss(dcol, tc::desc_join(alo + off, kHi), tc::desc_join(blo + off, kHi), kIdescKK, ks > 0 ? 1u : 0u);
+    tc::mma_ss(dcol, tc::desc_join(alo + off, kHi), tc::desc_join(blo + off, kHi), kIdescHalf, ks > 0 ? 1u : 0u);
   }
 }
 
-// C += A B with A = 128 lanes x 128 bf16 (packed pairs in 64 TMEM columns
-// from acol) and B = a [128 rows (the contraction) x 128 dims] tile in shared
-// memory (N-major: two 64-dim boxes 16 KB apart).
-__device__ __forceinline__ void issue_tn(uint32_t dcol, uint32_t acol, uint32_t sb, bool accumulate) {
+// C += A B over the contraction rows [64 g, 64 g + 64): A = 128 lanes x 64
+// bf16 (packed pairs in 32 TMEM columns from acol), B = those rows of a
+// [128 x 128 dims] tile in shared memory (N-major: two 64-dim boxes 16 KB apart).
+__device__ __forceinline__ void issue_acc(uint32_t dcol, uint32_t acol, uint32_t sb, int g, bool accumulate) {
   const uint32_t blo = tc::desc_lo(sb, kBox);
   constexpr uint32_t kHi = tc::desc_hi(1024);
 #pragma unroll
-  for (int ks = 0; ks < BT / 16; ++ks) {
-    const uint64_t bdesc = tc::desc_join(blo + (uint32_t)(ks * 16 * 128 >> 4), kHi);
+  for (int ks = 0; ks < HT / 16; ++ks) {
+    const uint64_t bdesc = tc::desc_join(blo + (uint32_t)((g * 4 + ks) * 16 * 128 >> 4), kHi);
     tc::mma_ts(dcol, acol + 8 * ks, bdesc, kIdescTN, (accumulate || ks > 0) ? 1u : 0u);
   }
 }
@@ -148,7 +156,21 @@ __global__ void __launch_bounds__(256) bwd_facts_kernel(const BwdParams p) {
   }
 }
 
+// TMEM set-up shared by the two tensor-core kernels (after thread 0 has
+// initialised the barriers): warp 9 allocates, everyone reads the base.
+__device__ __forceinline__ uint32_t setup_tmem(int* misc, int warp) {
+  if (warp == kMmaWarp) {
+    tc::alloc(reinterpret_cast<uint32_t*>(&misc[0]), kTmemCols);
+    tc::relinquish();
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  return static_cast<uint32_t>(misc[0]);
+}
+
 // ---------------------------------------------------------------- dQ
+template <bool BIAS>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmg,
                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
@@ -160,9 +182,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* v_full = bars + 3;        // [STAGES]
   uint64_t* k_empty = bars + 5;       // [STAGES]
   uint64_t* v_empty = bars + 7;       // [STAGES]
-  uint64_t* sp_full = bars + 9;       // S and G_P of the tile are in TMEM
-  uint64_t* ds_full = bars + 10;      // G_S of the tile is in TMEM (4 row warps)
-  uint64_t* drain = bars + 11;        // every product has completed
+  uint64_t* sp_full = bars + 9;       // [2] half g of S and G_P is in TMEM
+  uint64_t* p_full = bars + 11;       // [2] half g of G_S is in TMEM (4 warps of group g)
+  uint64_t* drain = bars + 13;        // every product has completed
   int* misc = reinterpret_cast<int*>(sm + kOffMisc);  // [0] TMEM base, [1] CTA end
 
   // longest query tiles first (causal: the last tiles see the most keys)
@@ -185,51 +207,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    mbar_init(sp_full, 1);
-    mbar_init(ds_full, 4);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&sp_full[g], 1);
+      mbar_init(&p_full[g], 4);
+    }
     mbar_init(drain, 1);
     fence_barrier_init();
   }
-  if (warp == kMmaWarp) {
-    tc::alloc(reinterpret_cast<uint32_t*>(&misc[0]), kTmemCols);
-    tc::relinquish();
-  }
-  tc::fence_before();
-  __syncthreads();
-  tc::fence_after();
-  const uint64_t pol_q = policy_evict_first();
+  const uint32_t tb = setup_tmem(misc, warp);
+  const uint64_t pol = policy_evict_first();
   if (warp == kTmaWarp && lane == 0) {
     // the query-side tiles and the first key tile (T_max >= 1) right away
     mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
-    tma_load_4d(sm + kOffA0, &tmq, 0, i0, h, b, q_full, pol_q);
-    tma_load_4d(sm + kOffA0 + kBox, &tmq, 64, i0, h, b, q_full, pol_q);
-    tma_load_4d(sm + kOffA1, &tmg, 0, i0, h, b, q_full, pol_q);
-    tma_load_4d(sm + kOffA1 + kBox, &tmg, 64, i0, h, b, q_full, pol_q);
+    tma_load_4d(sm + kOffA0, &tmq, 0, i0, h, b, q_full, pol);
+    tma_load_4d(sm + kOffA0 + kBox, &tmq, 64, i0, h, b, q_full, pol);
+    tma_load_4d(sm + kOffA1, &tmg, 0, i0, h, b, q_full, pol);
+    tma_load_4d(sm + kOffA1 + kBox, &tmg, 64, i0, h, b, q_full, pol);
     mbar_arrive_expect_tx(&k_full[0], kTileBytes);
-    tma_load_4d(sm + kOffR0, &tmk, 0, 0, hk, b, &k_full[0], pol_q);
-    tma_load_4d(sm + kOffR0 + kBox, &tmk, 64, 0, hk, b, &k_full[0], pol_q);
+    tma_load_4d(sm + kOffR0, &tmk, 0, 0, hk, b, &k_full[0], pol);
+    tma_load_4d(sm + kOffR0 + kBox, &tmk, 64, 0, hk, b, &k_full[0], pol);
     mbar_arrive_expect_tx(&v_full[0], kTileBytes);
-    tma_load_4d(sm + kOffR1, &tmv, 0, 0, hk, b, &v_full[0], pol_q);
-    tma_load_4d(sm + kOffR1 + kBox, &tmv, 64, 0, hk, b, &v_full[0], pol_q);
+    tma_load_4d(sm + kOffR1, &tmv, 0, 0, hk, b, &v_full[0], pol);
+    tma_load_4d(sm + kOffR1 + kBox, &tmv, 64, 0, hk, b, &v_full[0], pol);
   }
 
   const int len = seq_len(p, b);
   const int row_i = i0 + (int)(threadIdx.x & 127);
-  const bool my_row = warp < 4 && row_i < p.Tq;
+  const bool my_row = warp < 8 && row_i < p.Tq;
   const int my_end = my_row ? row_end(p, b, row_i, len) : 0;
-  if (my_row) atomicMax(&misc[1], my_end);
+  if (my_row && warp < 4) atomicMax(&misc[1], my_end);
   __syncthreads();
   const int cta_end = misc[1];
   const int n = (cta_end + BT - 1) / BT;
-  const uint32_t tb = static_cast<uint32_t>(misc[0]);
   const uint32_t sQ = smem_u32(sm + kOffA0), sG = smem_u32(sm + kOffA1);
   const uint32_t sK = smem_u32(sm + kOffR0), sV = smem_u32(sm + kOffR1);
-  float* dq_row = p.dq + (int64_t)b * p.dq_sb + (int64_t)h * p.dq_sh + (int64_t)row_i * p.dq_si;
+  const int grp = (warp >> 2) & 1;  // column half of a compute warp
+  float* dq_row = p.dq + (int64_t)b * p.dq_sb + (int64_t)h * p.dq_sh + (int64_t)row_i * p.dq_si + grp * HT;
 
   if (n == 0) {
     // no row of the tile sees a key: G_Q = 0; the first copies must land
     if (my_row)
-      for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(dq_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c = 0; c < HT; c += 4) *reinterpret_cast<float4*>(dq_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
     if (warp == kTmaWarp && lane == 0) {
       bool landed = mbar_wait(q_full, 0);
       landed = mbar_wait(&k_full[0], 0) && landed;
@@ -246,13 +264,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = ((j / STAGES) - 1) & 1;
         if (j >= STAGES && !mbar_wait(&k_empty[s], ph)) { ok = false; break; }
         mbar_arrive_expect_tx(&k_full[s], kTileBytes);
-        tma_load_4d(sm + kOffR0 + s * kTileBytes, &tmk, 0, j * BT, hk, b, &k_full[s], pol_q);
-        tma_load_4d(sm + kOffR0 + s * kTileBytes + kBox, &tmk, 64, j * BT, hk, b, &k_full[s], pol_q);
+        tma_load_4d(sm + kOffR0 + s * kTileBytes, &tmk, 0, j * BT, hk, b, &k_full[s], pol);
+        tma_load_4d(sm + kOffR0 + s * kTileBytes + kBox, &tmk, 64, j * BT, hk, b, &k_full[s], pol);
         k_issued = j + 1;
         if (j >= STAGES && !mbar_wait(&v_empty[s], ph)) { ok = false; break; }
         mbar_arrive_expect_tx(&v_full[s], kTileBytes);
-        tma_load_4d(sm + kOffR1 + s * kTileBytes, &tmv, 0, j * BT, hk, b, &v_full[s], pol_q);
-        tma_load_4d(sm + kOffR1 + s * kTileBytes + kBox, &tmv, 64, j * BT, hk, b, &v_full[s], pol_q);
+        tma_load_4d(sm + kOffR1 + s * kTileBytes, &tmv, 0, j * BT, hk, b, &v_full[s], pol);
+        tma_load_4d(sm + kOffR1 + s * kTileBytes + kBox, &tmv, 64, j * BT, hk, b, &v_full[s], pol);
         v_issued = j + 1;
       }
       // every issued copy lands before the CTA exits
@@ -265,78 +283,104 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      bool ok = mbar_wait(q_full, 0);
-      for (int j = 0; ok && j < n; ++j) {
+      // S and G_P of half g of key tile j (S at columns 64 g, G_P at 128 + 64 g)
+      auto half = [&](int j, int g) {
+        const int s = j % STAGES;
+        issue_half(tb + HT * g, sQ, sK + s * kTileBytes, g);
+        issue_half(tb + 128 + HT * g, sG, sV + s * kTileBytes, g);
+        tc::commit(&sp_full[g]);
+      };
+      auto tile_ready = [&](int j) -> bool {
         const int s = j % STAGES;
         const uint32_t ph = (j / STAGES) & 1;
-        if (!mbar_wait(&k_full[s], ph)) { ok = false; break; }
+        const bool r = mbar_wait(&k_full[s], ph) && mbar_wait(&v_full[s], ph);
         tc::fence_after();
-        issue_kk(tb + 0, sQ, sK + s * kTileBytes);          // S = Q K^T
-        if (!mbar_wait(&v_full[s], ph)) { ok = false; break; }
+        return r;
+      };
+      bool ok = mbar_wait(q_full, 0) && tile_ready(0);
+      if (ok) {
+        half(0, 0);
+        half(0, 1);
+        tc::commit(&v_empty[0]);
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        const int s = j % STAGES;
+        const bool next = j + 1 < n;
+        // G_Q += G_S K over the keys of half 0, then half 0 of the next tile
+        if (!mbar_wait(&p_full[0], j & 1)) { ok = false; break; }
         tc::fence_after();
-        issue_kk(tb + 128, sG, sV + s * kTileBytes);        // G_P = G_O V^T
-        tc::commit(sp_full);
-        tc::commit(&v_empty[s]);
-        if (!mbar_wait(ds_full, j & 1)) { ok = false; break; }
+        issue_acc(tb + 256, tb + 128, sK + s * kTileBytes, 0, j > 0);
+        if (next) {
+          if (!tile_ready(j + 1)) { ok = false; break; }
+          half(j + 1, 0);
+        }
+        // half 1 likewise; K_j is then free, and V_{j+1} once its halves are done
+        if (!mbar_wait(&p_full[1], j & 1)) { ok = false; break; }
         tc::fence_after();
-        issue_tn(tb + 256, tb + 128, sK + s * kTileBytes, j > 0);  // G_Q += G_S K
+        issue_acc(tb + 256, tb + 128 + HT, sK + s * kTileBytes, 1, true);
         tc::commit(&k_empty[s]);
+        if (next) {
+          half(j + 1, 1);
+          tc::commit(&v_empty[(j + 1) % STAGES]);
+        }
       }
       if (!ok) record_error(p.err, kErrTimeout);
       tc::commit(drain);
       if (!mbar_wait(drain, 0)) record_error(p.err, kErrTimeout);
     }
   } else {
-    // ---------------- rows: P, G_S ----------------
-    const uint32_t tl = tb + ((uint32_t)(32 * warp) << 16);  // this warp's lane quarter
+    // ---------------- rows x half tile: P, G_S ----------------
+    const uint32_t tl = tb + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's lane quarter
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity));
     };
     const int64_t fact = ((int64_t)b * p.Hq + h) * p.Tq + (my_row ? row_i : 0);
     const float Lrow = my_row ? p.ws_L[fact] : __builtin_huge_valf();
     const float Drow = my_row ? p.ws_D[fact] : 0.f;
-    const float* brow = (p.bias != nullptr && my_row)
-                            ? p.bias + (int64_t)b * p.bi_sb + (int64_t)h * p.bi_sh + (int64_t)row_i * p.bi_si
-                            : nullptr;
+    const float* brow = nullptr;
+    if constexpr (BIAS)
+      brow = p.bias + (int64_t)b * p.bi_sb + (int64_t)h * p.bi_sh + (int64_t)(my_row ? row_i : 0) * p.bi_si;
+    const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
+    const float2 nl2 = make_float2(-Lrow, -Lrow);
+    const float2 nd2 = make_float2(-Drow, -Drow);
     bool ok = true;
     for (int j = 0; j < n; ++j) {
-      if (!wait_all(sp_full, j & 1)) { ok = false; break; }
+      if (!wait_all(&sp_full[grp], j & 1)) { ok = false; break; }
       tc::fence_after();
-      const int key0 = j * BT;
-#pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
+      const int key0 = j * BT + grp * HT;  // first key of this half
+#pragma unroll
+      for (int q2 = 0; q2 < 2; ++q2) {
         uint32_t rs[32], rp[32], ds[16];
-        tc::ld32(tl + 32 * q4, rs);
-        tc::ld32(tl + 128 + 32 * q4, rp);
+        tc::ld32(tl + HT * grp + 32 * q2, rs);
+        tc::ld32(tl + 128 + HT * grp + 32 * q2, rp);
         tc::wait_ld();
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          float g2[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int key = key0 + 32 * q4 + c + e;
-            float x = __uint_as_float(rs[c + e]) * p.scale_log2;
-            bool vis = key < my_end;
-            if (brow != nullptr) {
-              const float m = key < p.Tmax ? brow[(int64_t)key * p.bi_sj] : 0.f;
-              vis = vis && m != -__builtin_huge_valf();
-              x = fmaf(m, kLog2e, x);
-            }
-            const float pr = fast_exp2(x - Lrow);
-            g2[e] = vis ? pr * (__uint_as_float(rp[c + e]) - Drow) : 0.f;
+          const int key = key0 + 32 * q2 + c;
+          float2 x = __ffma2_rn(make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])), c2, nl2);
+          bool v0 = key < my_end, v1 = key + 1 < my_end;
+          if constexpr (BIAS) {
+            const float m0 = key < p.Tmax ? brow[(int64_t)key * p.bi_sj] : 0.f;
+            const float m1 = key + 1 < p.Tmax ? brow[(int64_t)(key + 1) * p.bi_sj] : 0.f;
+            v0 = v0 && m0 != -__builtin_huge_valf();
+            v1 = v1 && m1 != -__builtin_huge_valf();
+            x = __ffma2_rn(make_float2(m0, m1), make_float2(kLog2e, kLog2e), x);
           }
-          ds[c >> 1] = pack_bf16(g2[0], g2[1]);
+          const float2 gp = __fadd2_rn(make_float2(__uint_as_float(rp[c]), __uint_as_float(rp[c + 1])), nd2);
+          const float2 g = __fmul2_rn(make_float2(fast_exp2(x.x), fast_exp2(x.y)), gp);
+          ds[c >> 1] = pack_bf16(v0 ? g.x : 0.f, v1 ? g.y : 0.f);
         }
-        tc::st16(tl + 128 + 16 * q4, ds);  // G_S over G_P's first 64 columns
+        tc::st16(tl + 128 + HT * grp + 16 * q2, ds);  // G_S over G_P's first 32 columns of the half
       }
-      if (key0 + BT > cta_end) {
-        // last tile: K rows past every visible key of the CTA are zeroed
-        // before G_S K reads them (they may hold anything)
+      if (j * BT + BT > cta_end) {
+        // last tile: the K rows of this half past every visible key of the
+        // CTA are zeroed before G_S K reads them (they may hold anything)
         const int s = j % STAGES;
         if (!wait_all(&k_full[s], (j / STAGES) & 1)) { ok = false; break; }
         unsigned char* kt = sm + kOffR0 + s * kTileBytes;
-        const int z0 = cta_end - key0;
-        for (int idx = (int)threadIdx.x; idx < (BT - z0) * 16; idx += 128) {
+        const int z0 = max(cta_end - j * BT, grp * HT);
+        const int t = (int)(threadIdx.x & 127);
+        for (int idx = t; idx < (grp * HT + HT - z0) * 16; idx += 128) {
           const int r = z0 + (idx >> 4);
           const int c = idx & 15;
           *reinterpret_cast<uint4*>(kt + (c >> 3) * kBox + r * 128 + (((c & 7) ^ (r & 7)) << 4)) =
@@ -347,22 +391,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full);
+      if (lane == 0) mbar_arrive(&p_full[grp]);
     }
     if (ok && !wait_all(drain, 0)) ok = false;
     if (!ok) {
       if (lane == 0) record_error(p.err, kErrTimeout);
     } else {
+      // G_Q: this group stores dims [64 g, 64 g + 64)
       tc::fence_after();
 #pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q2 = 0; q2 < 2; ++q2) {
         uint32_t r[32];
-        tc::ld32(tl + 256 + 32 * q4, r);
+        tc::ld32(tl + 256 + HT * grp + 32 * q2, r);
         tc::wait_ld();
         if (my_row) {
 #pragma unroll
           for (int c = 0; c < 32; c += 4)
-            *reinterpret_cast<float4*>(dq_row + 32 * q4 + c) =
+            *reinterpret_cast<float4*>(dq_row + 32 * q2 + c) =
                 make_float4(__uint_as_float(r[c]) * p.scale, __uint_as_float(r[c + 1]) * p.scale,
                             __uint_as_float(r[c + 2]) * p.scale, __uint_as_float(r[c + 3]) * p.scale);
         }
@@ -403,6 +448,7 @@ __device__ __forceinline__ bool next_visit(const BwdParams& p, const int* ends, 
   return false;
 }
 
+template <bool BIAS>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkv_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmg,
                    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
@@ -412,11 +458,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kv_full = bars;          // K and V tiles
   uint64_t* qg_full = bars + 1;      // [STAGES] Q and G_O tiles
   uint64_t* qg_empty = bars + 3;     // [STAGES]
-  uint64_t* sp_full = bars + 5;      // S^T and G_P^T in TMEM
-  uint64_t* p_full = bars + 6;       // P^T and G_S^T in TMEM (4 key warps)
-  uint64_t* drain = bars + 7;
+  uint64_t* sp_full = bars + 5;      // [2] half g of S^T and G_P^T in TMEM
+  uint64_t* p_full = bars + 7;       // [2] half g of P^T and G_S^T in TMEM (4 warps of group g)
+  uint64_t* drain = bars + 9;
   int* misc = reinterpret_cast<int*>(sm + kOffMisc);
-  float* facts = reinterpret_cast<float*>(sm + kOffFacts);  // [2][3][128]: L, D, end (int bits)
+  float4* facts = reinterpret_cast<float4*>(sm + kOffFacts);  // [2][128]: L, D, end (int bits), -
 
   // longest key tiles first (causal: the first tiles are seen by the most rows)
   const int per = p.B * p.Hkv;
@@ -435,19 +481,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&qg_full[s], 1);
       mbar_init(&qg_empty[s], 1);
     }
-    mbar_init(sp_full, 1);
-    mbar_init(p_full, 4);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&sp_full[g], 1);
+      mbar_init(&p_full[g], 4);
+    }
     mbar_init(drain, 1);
     fence_barrier_init();
   }
-  if (warp == kMmaWarp) {
-    tc::alloc(reinterpret_cast<uint32_t*>(&misc[0]), kTmemCols);
-    tc::relinquish();
-  }
-  tc::fence_before();
-  __syncthreads();
-  tc::fence_after();
-  const uint32_t tb = static_cast<uint32_t>(misc[0]);
+  const uint32_t tb = setup_tmem(misc, warp);
   const uint32_t sK = smem_u32(sm + kOffA0), sV = smem_u32(sm + kOffA1);
   const uint32_t sQ = smem_u32(sm + kOffR0), sG = smem_u32(sm + kOffR1);
   const uint64_t pol = policy_evict_first();
@@ -483,135 +524,153 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0 && any) {
-      bool ok = mbar_wait(kv_full, 0);
-      Visit v = first;
-      int t = 0;
-      while (ok) {
+      // S^T and G_P^T of the query rows [64 g, 64 g + 64) of visit t
+      auto half = [&](int t, int g) {
         const int s = t % STAGES;
-        if (!mbar_wait(&qg_full[s], (t / STAGES) & 1)) { ok = false; break; }
+        issue_half(tb + HT * g, sK, sQ + s * kTileBytes, g);
+        issue_half(tb + 128 + HT * g, sV, sG + s * kTileBytes, g);
+        tc::commit(&sp_full[g]);
+      };
+      auto visit_ready = [&](int t) -> bool {
+        const bool r = mbar_wait(&qg_full[t % STAGES], (t / STAGES) & 1);
         tc::fence_after();
-        issue_kk(tb + 0, sK, sQ + s * kTileBytes);    // S^T = K Q^T
-        issue_kk(tb + 128, sV, sG + s * kTileBytes);  // G_P^T = V G_O^T
-        tc::commit(sp_full);
-        if (!mbar_wait(p_full, t & 1)) { ok = false; break; }
+        return r;
+      };
+      bool ok = mbar_wait(kv_full, 0) && visit_ready(0);
+      if (ok) {
+        half(0, 0);
+        half(0, 1);
+      }
+      Visit v = first;
+      for (int t = 0; ok; ++t) {
+        const int s = t % STAGES;
+        const bool next = next_visit(p, ends, k0, v);
+        // G_V += P^T G_O and G_K += G_S^T Q over the rows of half 0, then
+        // half 0 of the next visit
+        if (!mbar_wait(&p_full[0], t & 1)) { ok = false; break; }
         tc::fence_after();
-        issue_tn(tb + 256, tb + 0, sG + s * kTileBytes, t > 0);    // G_V += P^T G_O
-        issue_tn(tb + 384, tb + 128, sQ + s * kTileBytes, t > 0);  // G_K += G_S^T Q
+        issue_acc(tb + 256, tb + 0, sG + s * kTileBytes, 0, t > 0);
+        issue_acc(tb + 384, tb + 128, sQ + s * kTileBytes, 0, t > 0);
+        if (next) {
+          if (!visit_ready(t + 1)) { ok = false; break; }
+          half(t + 1, 0);
+        }
+        if (!mbar_wait(&p_full[1], t & 1)) { ok = false; break; }
+        tc::fence_after();
+        issue_acc(tb + 256, tb + HT, sG + s * kTileBytes, 1, true);
+        issue_acc(tb + 384, tb + 128 + HT, sQ + s * kTileBytes, 1, true);
         tc::commit(&qg_empty[s]);
-        ++t;
-        if (!next_visit(p, ends, k0, v)) break;
+        if (!next) break;
+        half(t + 1, 1);
       }
       if (!ok) record_error(p.err, kErrTimeout);
       tc::commit(drain);
       if (!mbar_wait(drain, 0)) record_error(p.err, kErrTimeout);
     }
   } else {
-    // ---------------- keys: P^T, G_S^T ----------------
-    const int key = k0 + (int)threadIdx.x;
-    const uint32_t tl = tb + ((uint32_t)(32 * warp) << 16);
+    // ---------------- keys x half tile: P^T, G_S^T ----------------
+    const int grp = warp >> 2;
+    const int key = k0 + 32 * (warp & 3) + lane;
+    const uint32_t tl = tb + ((uint32_t)(32 * (warp & 3)) << 16);
     const int len = seq_len(p, b);
+    const int t128 = (int)(threadIdx.x & 127);  // thread within the group
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity));
     };
+    const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
     bool ok = true;
     if (any) {
       Visit v = first;
-      int t = 0;
-      while (true) {
+      for (int t = 0;; ++t) {
         const int h = hk * p.G + v.g;
-        float* f = facts + (t & 1) * 3 * 128;
-        {
-          // this tile's row facts, one row per thread
-          const int i = v.qt * BT + (int)threadIdx.x;
-          float L = __builtin_huge_valf(), Dv = 0.f;
-          int e = 0;
+        float4* f = facts + (t & 1) * 128 + grp * HT;
+        if (t128 < HT) {
+          // the facts of this half's query rows, one row per thread
+          const int i = v.qt * BT + grp * HT + t128;
+          float4 e = make_float4(__builtin_huge_valf(), 0.f, __int_as_float(0), 0.f);
           if (i < p.Tq) {
             const int64_t r = ((int64_t)b * p.Hq + h) * p.Tq + i;
-            L = p.ws_L[r];
-            Dv = p.ws_D[r];
-            e = row_end(p, b, i, len);
+            e = make_float4(p.ws_L[r], p.ws_D[r], __int_as_float(row_end(p, b, i, len)), 0.f);
           }
-          f[threadIdx.x] = L;
-          f[128 + threadIdx.x] = Dv;
-          f[256 + threadIdx.x] = __int_as_float(e);
+          f[t128] = e;
         }
-        // (the barrier also publishes the facts; the verdict is the same
-        // for all 128 key threads, so none is left at a later barrier)
-        if (!bar_and(1, 128, wait_all(sp_full, t & 1))) { ok = false; break; }
+        // (the barrier also publishes the facts; the verdict is the same for
+        // the group's 128 threads, so none is left at a later barrier)
+        if (!bar_and(1 + grp, 128, wait_all(&sp_full[grp], t & 1))) { ok = false; break; }
         tc::fence_after();
-        const float* brow = p.bias != nullptr
-                                ? p.bias + (int64_t)b * p.bi_sb + (int64_t)h * p.bi_sh +
-                                      (int64_t)(v.qt * BT) * p.bi_si + (int64_t)key * p.bi_sj
-                                : nullptr;
-#pragma unroll 1
-        for (int q4 = 0; q4 < 4; ++q4) {
+        const float* bcol = nullptr;
+        if constexpr (BIAS)
+          bcol = p.bias + (int64_t)b * p.bi_sb + (int64_t)h * p.bi_sh +
+                 (int64_t)(v.qt * BT + grp * HT) * p.bi_si + (int64_t)key * p.bi_sj;
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
           uint32_t rs[32], rp[32], pp[16], ds[16];
-          tc::ld32(tl + 32 * q4, rs);
-          tc::ld32(tl + 128 + 32 * q4, rp);
+          tc::ld32(tl + HT * grp + 32 * q2, rs);
+          tc::ld32(tl + 128 + HT * grp + 32 * q2, rp);
           tc::wait_ld();
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            float pv[2], gv[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int col = 32 * q4 + c + e;  // query row within the tile
-              float x = __uint_as_float(rs[c + e]) * p.scale_log2;
-              bool vis = key < __float_as_int(f[256 + col]);
-              if (brow != nullptr) {
-                const int i = v.qt * BT + col;
-                const float m = (i < p.Tq && key < p.Tmax) ? brow[(int64_t)col * p.bi_si] : 0.f;
-                vis = vis && m != -__builtin_huge_valf();
-                x = fmaf(m, kLog2e, x);
-              }
-              const float pr = vis ? fast_exp2(x - f[col]) : 0.f;
-              pv[e] = pr;
-              gv[e] = vis ? pr * (__uint_as_float(rp[c + e]) - f[128 + col]) : 0.f;
+            const int col = 32 * q2 + c;  // query row within the half
+            const float4 f0 = f[col], f1 = f[col + 1];
+            float2 x = __ffma2_rn(make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])), c2,
+                                  make_float2(-f0.x, -f1.x));
+            bool v0 = key < __float_as_int(f0.z), v1 = key < __float_as_int(f1.z);
+            if constexpr (BIAS) {
+              const int i = v.qt * BT + grp * HT + col;
+              const bool kin = key < p.Tmax;
+              const float m0 = (kin && i < p.Tq) ? bcol[(int64_t)col * p.bi_si] : 0.f;
+              const float m1 = (kin && i + 1 < p.Tq) ? bcol[(int64_t)(col + 1) * p.bi_si] : 0.f;
+              v0 = v0 && m0 != -__builtin_huge_valf();
+              v1 = v1 && m1 != -__builtin_huge_valf();
+              x = __ffma2_rn(make_float2(m0, m1), make_float2(kLog2e, kLog2e), x);
             }
-            pp[c >> 1] = pack_bf16(pv[0], pv[1]);
-            ds[c >> 1] = pack_bf16(gv[0], gv[1]);
+            const float p0 = v0 ? fast_exp2(x.x) : 0.f;
+            const float p1 = v1 ? fast_exp2(x.y) : 0.f;
+            const float2 g = __fmul2_rn(make_float2(p0, p1),
+                                        __fadd2_rn(make_float2(__uint_as_float(rp[c]), __uint_as_float(rp[c + 1])),
+                                                   make_float2(-f0.y, -f1.y)));
+            pp[c >> 1] = pack_bf16(p0, p1);
+            // G_S^T by select: a masked G_P may be NaN (cache padding)
+            ds[c >> 1] = pack_bf16(v0 ? g.x : 0.f, v1 ? g.y : 0.f);
           }
-          tc::st16(tl + 16 * q4, pp);         // P^T over S^T's first 64 columns
-          tc::st16(tl + 128 + 16 * q4, ds);   // G_S^T over G_P^T's first 64 columns
+          tc::st16(tl + HT * grp + 16 * q2, pp);        // P^T over S^T's first 32 columns of the half
+          tc::st16(tl + 128 + HT * grp + 16 * q2, ds);  // G_S^T likewise over G_P^T
         }
         tc::wait_st();
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
-        ++t;
+        if (lane == 0) mbar_arrive(&p_full[grp]);
         if (!next_visit(p, ends, k0, v)) break;
       }
       if (ok && !wait_all(drain, 0)) ok = false;
     }
+    float* dv_row = p.dv + (int64_t)b * p.dv_sb + (int64_t)hk * p.dv_sh + (int64_t)key * p.dv_sj + grp * HT;
+    float* dk_row = p.dk + (int64_t)b * p.dk_sb + (int64_t)hk * p.dk_sh + (int64_t)key * p.dk_sj + grp * HT;
     if (!ok) {
       if (lane == 0) record_error(p.err, kErrTimeout);
-    } else if (key < p.Tmax) {
-      float* dv_row = p.dv + (int64_t)b * p.dv_sb + (int64_t)hk * p.dv_sh + (int64_t)key * p.dv_sj;
-      float* dk_row = p.dk + (int64_t)b * p.dk_sb + (int64_t)hk * p.dk_sh + (int64_t)key * p.dk_sj;
-      if (!any) {
-        for (int c = 0; c < D; c += 4) {
+    } else if (!any) {
+      if (key < p.Tmax)
+        for (int c = 0; c < HT; c += 4) {
           *reinterpret_cast<float4*>(dv_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
           *reinterpret_cast<float4*>(dk_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-      }
-    }
-    if (ok && any) {
-      // the tensor-memory loads are warp-collective: every lane takes part
+    } else {
+      // this group stores dims [64 g, 64 g + 64) of G_V and G_K (the
+      // tensor-memory loads are warp-collective: every lane takes part)
       tc::fence_after();
-      float* dv_row = p.dv + (int64_t)b * p.dv_sb + (int64_t)hk * p.dv_sh + (int64_t)key * p.dv_sj;
-      float* dk_row = p.dk + (int64_t)b * p.dk_sb + (int64_t)hk * p.dk_sh + (int64_t)key * p.dk_sj;
 #pragma unroll 1
       for (int part = 0; part < 2; ++part) {
         float* dst = part == 0 ? dv_row : dk_row;
         const float mul = part == 0 ? 1.f : p.scale;
 #pragma unroll 1
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q2 = 0; q2 < 2; ++q2) {
           uint32_t r[32];
-          tc::ld32(tl + 256 + 128 * part + 32 * q4, r);
+          tc::ld32(tl + 256 + 128 * part + HT * grp + 32 * q2, r);
           tc::wait_ld();
           if (key < p.Tmax) {
 #pragma unroll
             for (int c = 0; c < 32; c += 4)
-              *reinterpret_cast<float4*>(dst + 32 * q4 + c) =
+              *reinterpret_cast<float4*>(dst + 32 * q2 + c) =
                   make_float4(__uint_as_float(r[c]) * mul, __uint_as_float(r[c + 1]) * mul,
                               __uint_as_float(r[c + 2]) * mul, __uint_as_float(r[c + 3]) * mul);
           }
@@ -626,35 +685,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tc::dealloc(tb, kTmemCols);
 }
 
+template <bool BIAS>
+cudaError_t launch_pair(const BwdParams& p, const CUtensorMap& tmq, const CUtensorMap& tmg, const CUtensorMap& tmk,
+                        const CUtensorMap& tmv, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    for (const void* f : {(const void*)bwd_dq_kernel<BIAS>, (const void*)bwd_dkv_kernel<BIAS>}) {
+      cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      if (e != cudaSuccess) return e;
+    }
+    attr_set = true;
+  }
+  const int64_t dq_blocks = (int64_t)p.B * p.Hq * p.n_qt;
+  const int64_t dkv_blocks = (int64_t)p.B * p.Hkv * p.n_kt;
+  if (dq_blocks > 0x7fffffff || dkv_blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  if (dq_blocks > 0) {
+    bwd_dq_kernel<BIAS><<<(unsigned)dq_blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmg, tmk, tmv);
+    if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
+  }
+  bwd_dkv_kernel<BIAS><<<(unsigned)dkv_blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmg, tmk, tmv);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 int backward_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_backward(const BwdParams& p, const CUtensorMap& tmq, const CUtensorMap& tmg,
                             const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    for (const void* f : {(const void*)bwd_dq_kernel, (const void*)bwd_dkv_kernel}) {
-      cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-      if (e != cudaSuccess) return e;
-    }
-    attr_set = true;
-  }
   const int64_t rows = (int64_t)p.B * p.Hq * p.Tq;
   int64_t fb = (rows + 7) / 8;
   if (fb < 1) fb = 1;
   if (fb > 4096) fb = 4096;
   bwd_facts_kernel<<<(unsigned)fb, 256, 0, stream>>>(p);
   if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
-  const int64_t dq_blocks = (int64_t)p.B * p.Hq * p.n_qt;
-  const int64_t dkv_blocks = (int64_t)p.B * p.Hkv * p.n_kt;
-  if (dq_blocks > 0x7fffffff || dkv_blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  if (dq_blocks > 0) {
-    bwd_dq_kernel<<<(unsigned)dq_blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmg, tmk, tmv);
-    if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
-  }
-  bwd_dkv_kernel<<<(unsigned)dkv_blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmg, tmk, tmv);
-  return cudaGetLastError();
+  return p.bias != nullptr ? launch_pair<true>(p, tmq, tmg, tmk, tmv, stream)
+                           : launch_pair<false>(p, tmq, tmg, tmk, tmv, stream);
 }
 
 }  // namespace blkattn
