@@ -744,6 +744,16 @@ int bwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_ten
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.err = ds->err;
+  {
+    // L2-sized dispatch groups: half the L2 for the operands a group streams
+    int l2 = 0;
+    if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || l2 <= 0) l2 = 64 << 20;
+    const int64_t kv_head = 2 * c.Tmax * 128 * 2;              // K and V of one (sequence, KV head)
+    const int64_t q_unit = 2 * (c.Hq / c.Hkv) * c.Tq * 128 * 2;  // Q and g_o of its G query heads
+    auto clamp = [](int64_t x, int64_t hi) { return x < 1 ? 1 : (x > hi ? hi : x); };
+    p.hg_q = (int)clamp((l2 / 2) / kv_head, c.B * c.Hq);
+    p.hg_kv = (int)clamp((l2 / 2) / (q_unit > 0 ? q_unit : 1), c.B * c.Hkv);
+  }
   if (cudaError_t e = launch_backward(p, *tmq, *tmg, *tmk, *tmv, stream); e != cudaSuccess) return cuda_fail(e);
   return BLKATTN_OK;
 }

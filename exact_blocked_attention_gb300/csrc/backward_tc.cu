@@ -115,9 +115,10 @@ __device__ __forceinline__ int seq_len(const BwdParams& p, int b) {
 }
 
 // ---------------------------------------------------------------- row facts
-// One warp per row (b, h, i): D = g_o . o (fp32), L = lse * log2 e (+inf for
-// an empty row, so that 2^(x - L) = 0).  Then one thread per (b, query tile):
-// the largest row end of the tile.
+// One warp per row (b, h, i): -D = -(g_o . o) (fp32) and -L = -lse log2 e
+// (-inf for an empty row, so that 2^(x - L) = 0), negated for the fused
+// multiply-adds that use them.  Then one thread per (b, query tile): the
+// largest row end of the tile.
 __global__ void __launch_bounds__(256) bwd_facts_kernel(const BwdParams p) {
   const int64_t rows = (int64_t)p.B * p.Hq * p.Tq;
   const int64_t warps = (int64_t)gridDim.x * 8;
@@ -141,8 +142,8 @@ __global__ void __launch_bounds__(256) bwd_facts_kernel(const BwdParams p) {
     for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
       const float l = p.lse[b * p.l_sb + h * p.l_sh + i * p.l_si];
-      p.ws_D[r] = acc;
-      p.ws_L[r] = (l == -__builtin_huge_valf()) ? __builtin_huge_valf() : l * kLog2e;
+      p.ws_D[r] = -acc;
+      p.ws_L[r] = (l == -__builtin_huge_valf()) ? -__builtin_huge_valf() : -l * kLog2e;
     }
   }
   const int64_t tiles = (int64_t)p.B * p.n_qt;
@@ -169,11 +170,84 @@ __device__ __forceinline__ uint32_t setup_tmem(int* misc, int warp) {
   return static_cast<uint32_t>(misc[0]);
 }
 
+// 32 entries of one row (dQ: a query row over 32 keys) from the scores s and
+// G_P in TMEM: G_S = 2^(s scale log2 e + m log2 e - L) (G_P - D), by select
+// where the key is invisible, packed to bf16 pairs.  MASK = false: every
+// entry is visible (no bias, the whole half tile before the row end).
+template <bool BIAS, bool MASK>
+__device__ __forceinline__ void dq_chunk(const uint32_t (&rs)[32], const uint32_t (&rp)[32], int key, int my_end,
+                                         float2 c2, float2 nl2, float2 nd2, const float* brow, int64_t bi_sj,
+                                         int Tmax, uint32_t (&ds)[16]) {
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    float2 x = __ffma2_rn(make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])), c2, nl2);
+    bool v0 = true, v1 = true;
+    if constexpr (MASK) {
+      v0 = key + c < my_end;
+      v1 = key + c + 1 < my_end;
+    }
+    if constexpr (BIAS) {
+      const float m0 = key + c < Tmax ? brow[(int64_t)(key + c) * bi_sj] : 0.f;
+      const float m1 = key + c + 1 < Tmax ? brow[(int64_t)(key + c + 1) * bi_sj] : 0.f;
+      v0 = v0 && m0 != -__builtin_huge_valf();
+      v1 = v1 && m1 != -__builtin_huge_valf();
+      x = __ffma2_rn(make_float2(m0, m1), make_float2(kLog2e, kLog2e), x);
+    }
+    const float2 gp = __fadd2_rn(make_float2(__uint_as_float(rp[c]), __uint_as_float(rp[c + 1])), nd2);
+    const float2 g = __fmul2_rn(make_float2(fast_exp2(x.x), fast_exp2(x.y)), gp);
+    if constexpr (MASK || BIAS)
+      ds[c >> 1] = pack_bf16(v0 ? g.x : 0.f, v1 ? g.y : 0.f);
+    else
+      ds[c >> 1] = pack_bf16(g.x, g.y);
+  }
+}
+
+// 32 entries of one key's row (dK/dV: a key over 32 query rows) from S^T and
+// G_P^T in TMEM and the rows' facts f (-L, -D, end): P^T and G_S^T packed to
+// bf16 pairs, by select where the row does not see the key.  MASK = false:
+// the key is visible to every row of the half (no bias, before every end).
+template <bool BIAS, bool MASK>
+__device__ __forceinline__ void dkv_chunk(const uint32_t (&rs)[32], const uint32_t (&rp)[32], const float4* f,
+                                          int key, float2 c2, const float* bcol, int64_t bi_si, int rows_left,
+                                          bool kin, uint32_t (&pp)[16], uint32_t (&ds)[16]) {
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    const float4 f0 = f[c], f1 = f[c + 1];
+    float2 x = __ffma2_rn(make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])), c2,
+                          make_float2(f0.x, f1.x));
+    bool v0 = true, v1 = true;
+    if constexpr (MASK) {
+      v0 = key < __float_as_int(f0.z);
+      v1 = key < __float_as_int(f1.z);
+    }
+    if constexpr (BIAS) {
+      const float m0 = (kin && c < rows_left) ? bcol[(int64_t)c * bi_si] : 0.f;
+      const float m1 = (kin && c + 1 < rows_left) ? bcol[(int64_t)(c + 1) * bi_si] : 0.f;
+      v0 = v0 && m0 != -__builtin_huge_valf();
+      v1 = v1 && m1 != -__builtin_huge_valf();
+      x = __ffma2_rn(make_float2(m0, m1), make_float2(kLog2e, kLog2e), x);
+    }
+    float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+    if constexpr (MASK || BIAS) {
+      p0 = v0 ? p0 : 0.f;
+      p1 = v1 ? p1 : 0.f;
+    }
+    const float2 g = __fmul2_rn(make_float2(p0, p1), __fadd2_rn(make_float2(__uint_as_float(rp[c]),
+                                                                             __uint_as_float(rp[c + 1])),
+                                                                 make_float2(f0.y, f1.y)));
+    pp[c >> 1] = pack_bf16(p0, p1);
+    // G_S^T by select: a masked G_P may be NaN (cache padding)
+    if constexpr (MASK || BIAS)
+      ds[c >> 1] = pack_bf16(v0 ? g.x : 0.f, v1 ? g.y : 0.f);
+    else
+      ds[c >> 1] = pack_bf16(g.x, g.y);
+  }
+}
+
 // ---------------------------------------------------------------- dQ
 template <bool BIAS>
-__global__ void __launch_bounds__(kThreads, 1)
-    bwd_dq_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmg,
-                  const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+__device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& tmq, const CUtensorMap& tmg,
+                                        const CUtensorMap& tmk, const CUtensorMap& tmv, int blk) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
@@ -187,10 +261,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = bars + 13;        // every product has completed
   int* misc = reinterpret_cast<int*>(sm + kOffMisc);  // [0] TMEM base, [1] CTA end
 
-  // longest query tiles first (causal: the last tiles see the most keys)
-  const int per = p.B * p.Hq;
-  const int qt = p.n_qt - 1 - (int)(blockIdx.x / per);
-  const int bh = (int)(blockIdx.x % per);
+  // Groups of p.hg_q (sequence, head) pairs whose K/V fit in L2 together;
+  // within a group the longest query tiles first (causal: the last tiles see
+  // the most keys), the group's heads side by side.
+  const int per_group = p.n_qt * p.hg_q;
+  const int r_in = blk % per_group;
+  const int qt = p.n_qt - 1 - r_in / p.hg_q;
+  const int bh = (blk / per_group) * p.hg_q + r_in % p.hg_q;
+  if (bh >= p.B * p.Hq) return;  // padding of the last group (the whole CTA)
   const int h = bh % p.Hq;
   const int b = bh / p.Hq;
   const int hk = h / p.G;
@@ -335,41 +413,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __all_sync(0xffffffffu, mbar_wait(bar, parity));
     };
     const int64_t fact = ((int64_t)b * p.Hq + h) * p.Tq + (my_row ? row_i : 0);
-    const float Lrow = my_row ? p.ws_L[fact] : __builtin_huge_valf();
-    const float Drow = my_row ? p.ws_D[fact] : 0.f;
+    const float nLrow = my_row ? p.ws_L[fact] : -__builtin_huge_valf();  // -L (base 2)
+    const float nDrow = my_row ? p.ws_D[fact] : 0.f;                     // -D
     const float* brow = nullptr;
     if constexpr (BIAS)
       brow = p.bias + (int64_t)b * p.bi_sb + (int64_t)h * p.bi_sh + (int64_t)(my_row ? row_i : 0) * p.bi_si;
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
-    const float2 nl2 = make_float2(-Lrow, -Lrow);
-    const float2 nd2 = make_float2(-Drow, -Drow);
+    const float2 nl2 = make_float2(nLrow, nLrow);
+    const float2 nd2 = make_float2(nDrow, nDrow);
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       if (!wait_all(&sp_full[grp], j & 1)) { ok = false; break; }
       tc::fence_after();
       const int key0 = j * BT + grp * HT;  // first key of this half
+      // (warp-uniform) every row of the warp sees every key of the half
+      const bool whole = !BIAS && __all_sync(0xffffffffu, key0 + HT <= my_end);
 #pragma unroll
       for (int q2 = 0; q2 < 2; ++q2) {
         uint32_t rs[32], rp[32], ds[16];
         tc::ld32(tl + HT * grp + 32 * q2, rs);
         tc::ld32(tl + 128 + HT * grp + 32 * q2, rp);
         tc::wait_ld();
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const int key = key0 + 32 * q2 + c;
-          float2 x = __ffma2_rn(make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])), c2, nl2);
-          bool v0 = key < my_end, v1 = key + 1 < my_end;
-          if constexpr (BIAS) {
-            const float m0 = key < p.Tmax ? brow[(int64_t)key * p.bi_sj] : 0.f;
-            const float m1 = key + 1 < p.Tmax ? brow[(int64_t)(key + 1) * p.bi_sj] : 0.f;
-            v0 = v0 && m0 != -__builtin_huge_valf();
-            v1 = v1 && m1 != -__builtin_huge_valf();
-            x = __ffma2_rn(make_float2(m0, m1), make_float2(kLog2e, kLog2e), x);
-          }
-          const float2 gp = __fadd2_rn(make_float2(__uint_as_float(rp[c]), __uint_as_float(rp[c + 1])), nd2);
-          const float2 g = __fmul2_rn(make_float2(fast_exp2(x.x), fast_exp2(x.y)), gp);
-          ds[c >> 1] = pack_bf16(v0 ? g.x : 0.f, v1 ? g.y : 0.f);
-        }
+        const int key = key0 + 32 * q2;
+        if (whole)
+          dq_chunk<BIAS, false>(rs, rp, key, my_end, c2, nl2, nd2, brow, p.bi_sj, p.Tmax, ds);
+        else
+          dq_chunk<BIAS, true>(rs, rp, key, my_end, c2, nl2, nd2, brow, p.bi_sj, p.Tmax, ds);
         tc::st16(tl + 128 + HT * grp + 16 * q2, ds);  // G_S over G_P's first 32 columns of the half
       }
       if (j * BT + BT > cta_end) {
@@ -449,9 +518,8 @@ __device__ __forceinline__ bool next_visit(const BwdParams& p, const int* ends, 
 }
 
 template <bool BIAS>
-__global__ void __launch_bounds__(kThreads, 1)
-    bwd_dkv_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmg,
-                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+__device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& tmq, const CUtensorMap& tmg,
+                                         const CUtensorMap& tmk, const CUtensorMap& tmv, int blk) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
@@ -464,12 +532,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* misc = reinterpret_cast<int*>(sm + kOffMisc);
   float4* facts = reinterpret_cast<float4*>(sm + kOffFacts);  // [2][128]: L, D, end (int bits), -
 
-  // longest key tiles first (causal: the first tiles are seen by the most rows)
-  const int per = p.B * p.Hkv;
-  const int kt = (int)(blockIdx.x / per);
-  const int r_in = (int)(blockIdx.x % per);
-  const int b = r_in / p.Hkv;
-  const int hk = r_in % p.Hkv;
+  // Groups of p.hg_kv (sequence, KV head) pairs whose query-side tiles fit in
+  // L2 together; within a group the longest key tiles first (causal: the
+  // first tiles are seen by the most rows), the group's heads side by side.
+  const int per_group = p.n_kt * p.hg_kv;
+  const int r_in = blk % per_group;
+  const int kt = r_in / p.hg_kv;
+  const int bk = (blk / per_group) * p.hg_kv + r_in % p.hg_kv;
+  if (bk >= p.B * p.Hkv) return;  // padding of the last group (the whole CTA)
+  const int b = bk / p.Hkv;
+  const int hk = bk % p.Hkv;
   const int k0 = kt * BT;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -587,12 +659,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t128 < HT) {
           // the facts of this half's query rows, one row per thread
           const int i = v.qt * BT + grp * HT + t128;
-          float4 e = make_float4(__builtin_huge_valf(), 0.f, __int_as_float(0), 0.f);
+          float4 e = make_float4(-__builtin_huge_valf(), 0.f, __int_as_float(0), 0.f);
           if (i < p.Tq) {
             const int64_t r = ((int64_t)b * p.Hq + h) * p.Tq + i;
             e = make_float4(p.ws_L[r], p.ws_D[r], __int_as_float(row_end(p, b, i, len)), 0.f);
           }
           f[t128] = e;
+          // the smallest row end of the half (two warps of 32 rows)
+          const int mn = __reduce_min_sync(0xffffffffu, __float_as_int(e.z));
+          if (lane == 0) misc[4 + (t & 1) * 4 + grp * 2 + (t128 >> 5)] = mn;
         }
         // (the barrier also publishes the facts; the verdict is the same for
         // the group's 128 threads, so none is left at a later barrier)
@@ -602,37 +677,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (BIAS)
           bcol = p.bias + (int64_t)b * p.bi_sb + (int64_t)h * p.bi_sh +
                  (int64_t)(v.qt * BT + grp * HT) * p.bi_si + (int64_t)key * p.bi_sj;
+        // (warp-uniform) every row of the half sees every key of the warp
+        const int* mn = misc + 4 + (t & 1) * 4 + grp * 2;
+        const bool whole = !BIAS && __all_sync(0xffffffffu, key < min(mn[0], mn[1]));
+        const int rows_left = p.Tq - (v.qt * BT + grp * HT);  // rows of the half inside T_q
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {
           uint32_t rs[32], rp[32], pp[16], ds[16];
           tc::ld32(tl + HT * grp + 32 * q2, rs);
           tc::ld32(tl + 128 + HT * grp + 32 * q2, rp);
           tc::wait_ld();
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const int col = 32 * q2 + c;  // query row within the half
-            const float4 f0 = f[col], f1 = f[col + 1];
-            float2 x = __ffma2_rn(make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])), c2,
-                                  make_float2(-f0.x, -f1.x));
-            bool v0 = key < __float_as_int(f0.z), v1 = key < __float_as_int(f1.z);
-            if constexpr (BIAS) {
-              const int i = v.qt * BT + grp * HT + col;
-              const bool kin = key < p.Tmax;
-              const float m0 = (kin && i < p.Tq) ? bcol[(int64_t)col * p.bi_si] : 0.f;
-              const float m1 = (kin && i + 1 < p.Tq) ? bcol[(int64_t)(col + 1) * p.bi_si] : 0.f;
-              v0 = v0 && m0 != -__builtin_huge_valf();
-              v1 = v1 && m1 != -__builtin_huge_valf();
-              x = __ffma2_rn(make_float2(m0, m1), make_float2(kLog2e, kLog2e), x);
-            }
-            const float p0 = v0 ? fast_exp2(x.x) : 0.f;
-            const float p1 = v1 ? fast_exp2(x.y) : 0.f;
-            const float2 g = __fmul2_rn(make_float2(p0, p1),
-                                        __fadd2_rn(make_float2(__uint_as_float(rp[c]), __uint_as_float(rp[c + 1])),
-                                                   make_float2(-f0.y, -f1.y)));
-            pp[c >> 1] = pack_bf16(p0, p1);
-            // G_S^T by select: a masked G_P may be NaN (cache padding)
-            ds[c >> 1] = pack_bf16(v0 ? g.x : 0.f, v1 ? g.y : 0.f);
-          }
+          const float* bq = BIAS ? bcol + (int64_t)(32 * q2) * p.bi_si : nullptr;
+          if (whole)
+            dkv_chunk<BIAS, false>(rs, rp, f + 32 * q2, key, c2, bq, p.bi_si, rows_left - 32 * q2,
+                                   key < p.Tmax, pp, ds);
+          else
+            dkv_chunk<BIAS, true>(rs, rp, f + 32 * q2, key, c2, bq, p.bi_si, rows_left - 32 * q2,
+                                  key < p.Tmax, pp, ds);
           tc::st16(tl + HT * grp + 16 * q2, pp);        // P^T over S^T's first 32 columns of the half
           tc::st16(tl + 128 + HT * grp + 16 * q2, ds);  // G_S^T likewise over G_P^T
         }
@@ -686,24 +747,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool BIAS>
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmg,
+              const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+  dq_body<BIAS>(p, tmq, tmg, tmk, tmv, (int)blockIdx.x);
+}
+template <bool BIAS>
+__global__ void __launch_bounds__(kThreads, 1)
+    dkv_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmg,
+               const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+  dkv_body<BIAS>(p, tmq, tmg, tmk, tmv, (int)blockIdx.x);
+}
+template <bool BIAS>
 cudaError_t launch_pair(const BwdParams& p, const CUtensorMap& tmq, const CUtensorMap& tmg, const CUtensorMap& tmk,
                         const CUtensorMap& tmv, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    for (const void* f : {(const void*)bwd_dq_kernel<BIAS>, (const void*)bwd_dkv_kernel<BIAS>}) {
+    for (const void* f : {(const void*)dq_kernel<BIAS>, (const void*)dkv_kernel<BIAS>}) {
       cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
       if (e != cudaSuccess) return e;
     }
     attr_set = true;
   }
-  const int64_t dq_blocks = (int64_t)p.B * p.Hq * p.n_qt;
-  const int64_t dkv_blocks = (int64_t)p.B * p.Hkv * p.n_kt;
+  if (p.hg_q < 1 || p.hg_kv < 1) return cudaErrorInvalidValue;
+  const int64_t dq_blocks = ((int64_t)p.B * p.Hq + p.hg_q - 1) / p.hg_q * p.hg_q * p.n_qt;
+  const int64_t dkv_blocks = ((int64_t)p.B * p.Hkv + p.hg_kv - 1) / p.hg_kv * p.hg_kv * p.n_kt;
   if (dq_blocks > 0x7fffffff || dkv_blocks > 0x7fffffff) return cudaErrorInvalidValue;
   if (dq_blocks > 0) {
-    bwd_dq_kernel<BIAS><<<(unsigned)dq_blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmg, tmk, tmv);
+    dq_kernel<BIAS><<<(unsigned)dq_blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmg, tmk, tmv);
     if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
   }
-  bwd_dkv_kernel<BIAS><<<(unsigned)dkv_blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmg, tmk, tmv);
+  dkv_kernel<BIAS><<<(unsigned)dkv_blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmg, tmk, tmv);
   return cudaGetLastError();
 }
 

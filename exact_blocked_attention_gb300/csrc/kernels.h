@@ -152,6 +152,8 @@ struct BwdParams {
   float* ws_L;    // [B * H_q * T_q] lse in base-2 units (+inf for an empty row)
   int* ws_end;    // [B * n_qt] largest row end min(pos + 1, len) of each 128-row query tile
   int B, Hq, Hkv, G, Tq, Tmax, n_qt, n_kt;
+  int hg_q;   // dQ: (sequence, head) pairs dispatched together (their K/V fit in L2)
+  int hg_kv;  // dK/dV: (sequence, KV head) pairs dispatched together (their Q, g_o fit in L2)
   float scale, scale_log2;
   int* err;
 };
