@@ -713,6 +713,7 @@ int bwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_ten
   BwdParams p{};
   p.out = out->data;
   p.out_bf16 = out->dtype == BLKATTN_BF16;
+  p.out_vec = rows && out_tma_ok(out);  // fp32, unit dim stride, 16-byte aligned rows
   p.o_sb = out->strides[0]; p.o_sh = out->strides[1]; p.o_si = out->strides[2]; p.o_sd = out->strides[3];
   p.lse = static_cast<const float*>(lse->data);
   p.l_sb = lse->strides[0]; p.l_sh = lse->strides[1]; p.l_si = lse->strides[2];

@@ -130,14 +130,24 @@ __global__ void __launch_bounds__(256) bwd_facts_kernel(const BwdParams p) {
     const int b = (int)(bh / p.Hq);
     const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(p.dout) + b * p.g_sb + h * p.g_sh + i * p.g_si;
     const int64_t ob = b * p.o_sb + h * p.o_sh + i * p.o_si;
-    float acc = 0.f;
+    // lane: dims [4 lane, 4 lane + 4) (g_o rows are 16-byte aligned: one 8-byte load)
+    const uint2 gw = *reinterpret_cast<const uint2*>(g + 4 * lane);
+    float o[4];
+    if (p.out_vec) {  // fp32 rows, unit dim stride, 16-byte aligned: one 16-byte load
+      const float4 v = *reinterpret_cast<const float4*>(static_cast<const float*>(p.out) + ob + 4 * lane);
+      o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+    } else {
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      const int t = lane + 32 * c;
-      const float o = p.out_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.out)[ob + t * p.o_sd])
-                                 : static_cast<const float*>(p.out)[ob + t * p.o_sd];
-      acc = fmaf(__bfloat162float(g[t]), o, acc);
+      for (int c = 0; c < 4; ++c) {
+        const int64_t t = ob + (int64_t)(4 * lane + c) * p.o_sd;
+        o[c] = p.out_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.out)[t])
+                          : static_cast<const float*>(p.out)[t];
+      }
     }
+    float acc = bf16lo(gw.x) * o[0];
+    acc = fmaf(bf16hi(gw.x), o[1], acc);
+    acc = fmaf(bf16lo(gw.y), o[2], acc);
+    acc = fmaf(bf16hi(gw.y), o[3], acc);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {

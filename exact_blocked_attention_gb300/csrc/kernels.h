@@ -131,6 +131,7 @@ size_t decode_tc_smem_bytes(int rows_cta);
 struct BwdParams {
   const void* out;  // forward output o [B, H_q, T_q, d] (bf16 or fp32), read for D = g_o . o
   int out_bf16;
+  int out_vec;  // fp32 rows with unit dim stride, 16-byte aligned (vector loads)
   int64_t o_sb, o_sh, o_si, o_sd;
   const float* lse;  // forward lse [B, H_q, T_q] (natural log, -inf = empty row)
   int64_t l_sb, l_sh, l_si;
