@@ -682,8 +682,9 @@ int bwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_ten
   if (dk->data == nullptr || dv->data == nullptr) return BLKATTN_ERR_INVALID_ARG;
   if (rows && (dout->data == nullptr || dq->data == nullptr)) return BLKATTN_ERR_INVALID_ARG;
   if (!grad_rows_ok(dk) || !grad_rows_ok(dv) || (rows && !grad_rows_ok(dq))) return BLKATTN_ERR_INVALID_ARG;
-  // the tensor-core backward: bf16 operands, d = 128, TMA-movable Q and g_o rows
-  if (c.elt != Elt::BF16 || c.d != 128) return BLKATTN_ERR_UNSUPPORTED;
+  // the tensor-core backward: bf16 operands, d = 128, TMA-movable Q and g_o
+  // rows, at most 1024 query tiles of 128 rows per sequence
+  if (c.elt != Elt::BF16 || c.d != 128 || c.Tq > 131072) return BLKATTN_ERR_UNSUPPORTED;
   if (rows && (!tma_rows_ok(q) || !tma_rows_ok(dout))) return BLKATTN_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 

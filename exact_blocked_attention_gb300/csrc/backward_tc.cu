@@ -73,7 +73,9 @@ constexpr int kOffBar = kOffR1 + STAGES * kTileBytes;
 constexpr int kNumBars = 16;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kOffFacts = kOffMisc + 64;                      // dK/dV: float4 [2][128] (L, D, end, -)
-constexpr int kSmemBytes = kOffFacts + 2 * 128 * 16 + 1024;  // + slack to align to 1024
+constexpr int kMaxQTiles = 1024;                              // query tiles per sequence (T_q <= 131072)
+constexpr int kOffEnds = kOffFacts + 2 * 128 * 16;            // dK/dV: int [kMaxQTiles] row ends per query tile
+constexpr int kSmemBytes = kOffEnds + kMaxQTiles * 4 + 1024;  // + slack to align to 1024
 
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
@@ -541,6 +543,7 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
   uint64_t* drain = bars + 9;
   int* misc = reinterpret_cast<int*>(sm + kOffMisc);
   float4* facts = reinterpret_cast<float4*>(sm + kOffFacts);  // [2][128]: L, D, end (int bits), -
+  int* ends = reinterpret_cast<int*>(sm + kOffEnds);          // this sequence's row end per query tile
 
   // Groups of p.hg_kv (sequence, KV head) pairs whose query-side tiles fit in
   // L2 together; within a group the longest key tiles first (causal: the
@@ -555,7 +558,10 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
   const int k0 = kt * BT;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int* ends = p.ws_end + (int64_t)b * p.n_qt;
+  // the visit sequence is walked from shared memory (a global load per step
+  // sat on the MMA thread's path between visits); published by the barrier
+  // in setup_tmem
+  for (int i = threadIdx.x; i < p.n_qt; i += kThreads) ends[i] = p.ws_end[(int64_t)b * p.n_qt + i];
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -779,7 +785,7 @@ cudaError_t launch_pair(const BwdParams& p, const CUtensorMap& tmq, const CUtens
     }
     attr_set = true;
   }
-  if (p.hg_q < 1 || p.hg_kv < 1) return cudaErrorInvalidValue;
+  if (p.hg_q < 1 || p.hg_kv < 1 || p.n_qt > kMaxQTiles) return cudaErrorInvalidValue;
   const int64_t dq_blocks = ((int64_t)p.B * p.Hq + p.hg_q - 1) / p.hg_q * p.hg_q * p.n_qt;
   const int64_t dkv_blocks = ((int64_t)p.B * p.Hkv + p.hg_kv - 1) / p.hg_kv * p.hg_kv * p.n_kt;
   if (dq_blocks > 0x7fffffff || dkv_blocks > 0x7fffffff) return cudaErrorInvalidValue;

@@ -267,7 +267,8 @@ int blkattn_fwd_static_scratch(const blkattn_tensor* q, const blkattn_tensor* k,
  * The products take P and dS as bf16 operands with fp32 accumulation; the
  * result does not depend on the schedule (no atomics: deterministic).
  * Uses the library's grow-only workspace (D and the base-2 lse per row).
- * Returns as blkattn_fwd; BLKATTN_ERR_UNSUPPORTED for f32 or d_h != 128;
+ * Returns as blkattn_fwd; BLKATTN_ERR_UNSUPPORTED for f32, d_h != 128 or
+ * T_q > 131072;
  * BLKATTN_ERR_INVALID_ARG also for a non-finite scale or mismatched
  * gradient shapes, dtypes or layouts.
  */

@@ -200,8 +200,9 @@ def call_bwd(lib, a, scale=0.1):
     (lambda a: a.update(dout=None), -1),
     (lambda a: a.update(**bwd_args(d=64)), -2),                                     # d = 64: no backward kernel
     (lambda a: a.update(**bwd_args(dt=torch.float32)), -2),                         # f32: no backward kernel
+    (lambda a: a.update(**bwd_args(B=1, Tq=131073)), -2),                           # > 1024 query tiles
 ], ids=["dout-dtype", "dout-shape", "dq-dtype", "dk-shape", "dv-heads", "dq-misaligned", "dk-row-stride",
-        "q-row-stride", "missing-dout", "d64", "f32"])
+        "q-row-stride", "missing-dout", "d64", "f32", "too-many-rows"])
 def test_backward_requests_are_validated_before_cuda(lib, mutate, expect):
     a = bwd_args()
     mutate(a)
