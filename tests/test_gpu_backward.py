@@ -206,3 +206,38 @@ def test_full_size_backward_sampled_heads():
     ref = obwd.attention_backward(inp["q"], inp["k"], inp["v"], inp["seqlens"], inp["qpos"], inp["scale"],
                                   inp["go"], units=units)
     assert_grads((dq.cpu(), dk.cpu(), dv.cpu()), ref, units=units)
+
+
+def test_backward_into_strided_gradient_views():
+    """dq, dk, dv written into views of larger buffers (padded rows): the
+    same bits as contiguous outputs, and nothing outside the views changes."""
+    c = case("decode_rows")
+    ref = reference(c)
+    o, lse = oracle_forward_state(ref)
+    a = run(c, o, lse)
+    cu = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in c.items()}
+    views = []
+    for t in (c["q"], c["k"], c["v"]):
+        shape = tuple(t.shape)
+        big = torch.full(shape[:-1] + (shape[-1] + 8,), 7.0, device="cuda")
+        views.append((big, big[..., 4:4 + shape[-1]]))
+    blkattn.bwd(cu["q"], cu["k"], cu["v"], cu["seqlens"], cu["qpos"], None, c["scale"], o.cuda(), lse.cuda(),
+                cu["go"], views[0][1], views[1][1], views[2][1])
+    torch.cuda.synchronize()
+    assert blkattn.check_device_error() == 0
+    for (big, view), want in zip(views, a):
+        assert torch.equal(view.cpu(), want)
+        assert bool((big[..., :4] == 7.0).all()) and bool((big[..., -4:] == 7.0).all())
+
+
+def test_backward_bias_broadcast_over_heads_with_groups():
+    """A [B, 1, T_q, T_max] bias (stride 0 over heads) with grouped heads."""
+    B, Hq, Hkv, T = 2, 8, 2, 190
+    g = torch.Generator().manual_seed(12)
+    bias = torch.randn(B, 1, T, T + 30, generator=g)
+    bias[torch.rand(B, 1, T, T + 30, generator=g) < 0.15] = -math.inf
+    bias[0, 0, 50, :] = -math.inf
+    c = make(B, Hq, Hkv, T, T + 30, [T + 30, 120], [list(range(T))] * 2, bias=bias, seed=13)
+    ref = reference(c)
+    o, lse = oracle_forward_state(ref)
+    assert_grads(run(c, o, lse), ref)
