@@ -685,7 +685,7 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
           const int mn = __reduce_min_sync(0xffffffffu, __float_as_int(e.z));
           if (lane == 0) misc[4 + (t & 1) * 4 + grp * 2 + (t128 >> 5)] = mn;
         }
-        // (the barrier also publishes the facts; the verdict is the same for
+        // (the barrier also publishes the facts; the answer is the same for
         // the group's 128 threads, so none is left at a later barrier)
         if (!bar_and(1 + grp, 128, wait_all(&sp_full[grp], t & 1))) { ok = false; break; }
         tc::fence_after();

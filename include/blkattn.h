@@ -52,7 +52,7 @@ typedef struct CUstream_st* blkattn_stream_t;
 enum {
   BLKATTN_OK = 0,
   BLKATTN_ERR_INVALID_ARG = -1,   /* bad shape, dtype, stride, alignment, H_q % H_kv, NULL */
-  BLKATTN_ERR_UNSUPPORTED = -2,   /* a valid request this build has no kernel for (e.g. d not in {64,128}) */
+  BLKATTN_ERR_UNSUPPORTED = -2,   /* a valid request the library has no kernel for (e.g. d not in {64,128}) */
   BLKATTN_ERR_CUDA = -3,          /* a CUDA runtime call or kernel launch failed */
   BLKATTN_ERR_DEVICE_TIMEOUT = -4,/* a kernel's bounded wait ran out (reported by blkattn_check_device_error) */
   BLKATTN_ERR_NO_WORKSPACE = -5,  /* the workspace must grow while the stream is being captured */
