@@ -95,11 +95,19 @@ def algorithmic_bytes(s, inp):
 
 
 def causal_flops(s, inp):
-    """4 * d per (row, visible key): QK^T and PV, 2 flops per multiply-add."""
+    """4 * d per (row, visible key): QK^T and PV, 2 flops per multiply-add
+    (a sliding window keeps the keys pos - W < j <= pos)."""
     lens = inp["seqlens"].numpy().astype(np.int64)
     pos = inp["qpos"].numpy().astype(np.int64)
-    vis = np.clip(np.minimum(lens[:, None], pos + 1), 0, None)  # [B, Tq]
+    end = np.clip(np.minimum(lens[:, None], pos + 1), 0, None)  # [B, Tq]
+    start = np.maximum(pos - s.window + 1, 0) if s.window else np.zeros_like(pos)
+    vis = np.clip(end - start, 0, None)
     return float(vis.sum()) * s.Hq * 4 * s.d
+
+
+def tensor_bound(s):
+    """Workloads measured in FLOP/s (many query rows per head on tcgen05)."""
+    return s.name in ("prefill", "window_prefill")
 
 
 class ClockSampler:
@@ -306,7 +314,7 @@ def time_e2e(r: Runner, steps: int, warmup: int):
 def roofline_entry(r: Runner, main_ms, peaks, flops=None):
     s = r.s
     kv, total_bytes = algorithmic_bytes(s, r.cpu)
-    if s.name == "prefill":
+    if tensor_bound(s):
         achieved = flops / (main_ms * 1e-3) / 1e12
         return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"], "traffic": measured_traffic(s.name),
@@ -375,7 +383,7 @@ def run_reference(args, rank, world):
 
 def measure_other(name, peaks):
     ro = Runner(name)
-    fl = ro.s.name == "prefill"
+    fl = tensor_bound(ro.s)
     steps_o = 10 if not fl else 5
     # inputs larger than L2 need no flush (writing a flush buffer between
     # steps would leave dirty lines whose write-back lands in the timed step)
@@ -537,7 +545,7 @@ def main():
     main_avg = max_over_ranks(sum(main_ms) / len(main_ms), world)
     spread = {"min": min(total), "median": sorted(total)[len(total) // 2], "max": max(total)}
     value = kv * world / (step_ms * 1e-3) / 1e9
-    if s.name == "prefill":
+    if tensor_bound(s):
         value = causal_flops(s, r.cpu) * world / (step_ms * 1e-3) / 1e12
     e2e_ms, h2d, d2h = time_e2e(r, max(3, args.steps // 4), 2)
     e2e_ms = max_over_ranks(e2e_ms, world)
@@ -552,7 +560,7 @@ def main():
     line = {
         "metric": METRIC if s.name == HEADLINE else f"{s.name} throughput",
         "value": value,
-        "unit": "GB/s" if s.name != "prefill" else "TFLOP/s",
+        "unit": "GB/s" if not tensor_bound(s) else "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": s.dtype,
         "data": "synthetic",

@@ -410,7 +410,7 @@ int validate_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn
   c->q_vec_ok = q->strides[3] == 1 && (reinterpret_cast<uintptr_t>(q->data) % 16) == 0 &&
                 (q->strides[0] * 2) % 16 == 0 && (q->strides[1] * 2) % 16 == 0 &&
                 (q->strides[2] * 2) % 16 == 0;
-  c->prefill_ok = bias == nullptr && tree == nullptr && c->q_vec_ok;  // (and no window: fwd_impl)
+  c->prefill_ok = bias == nullptr && tree == nullptr && c->q_vec_ok;
   return BLKATTN_OK;
 }
 
@@ -608,8 +608,7 @@ int fwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_ten
   int st = validate_fwd(q, k, v, seqlens_k, q_logical_pos, tree, mask_bias, out, lse, &c);
   if (st != BLKATTN_OK) return st;
   if (window < 0 || window > 0x7fffffff || (window > 0 && tree != nullptr)) return BLKATTN_ERR_INVALID_ARG;
-  c.window = window;
-  if (window > 0) c.prefill_ok = false;
+  c.window = window;  // (the prefill kernel takes windows too: a first key tile per CTA and a window mask)
   if (c.B == 0 || c.Tq == 0) return BLKATTN_OK;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 

@@ -83,6 +83,7 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return pol;
 }
 
+template <bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmq,
                       const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -98,7 +99,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_full = v_empty + STAGES;  // [QT]
   uint64_t* p_full = s_full + QT;       // [QT]
   uint64_t* drain = p_full + QT;
-  // misc: [0] tmem base, [1 + 2x] end of query tile x, [2 + 2x] min end of x, [5] timeout
+  // misc: [0] tmem base, [1 + 2x] end of query tile x, [2 + 2x] min end of x, [5] timeout,
+  // (sliding window) [6 + 2x] smallest and [7 + 2x] largest first visible key of x's rows
   int* misc = reinterpret_cast<int*>(sm + kOffMisc);
 
   // Linear grid in dispatch order: groups of p.head_group (sequence, head)
@@ -130,6 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc[1] = 0; misc[2] = 0x7fffffff;
     misc[3] = 0; misc[4] = 0x7fffffff;
     misc[5] = 0;
+    misc[6] = 0x7fffffff; misc[7] = 0;
+    misc[8] = 0x7fffffff; misc[9] = 0;
     mbar_init(q_full, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&k_full[s], 1);
@@ -158,18 +162,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_4d(sm + kOffQ + t * kTileBytes, &tmq, 0, q0 + t * BM, h, b, q_full, pol_q);
       tma_load_4d(sm + kOffQ + t * kTileBytes + kBox, &tmq, 64, q0 + t * BM, h, b, q_full, pol_q);
     }
-    mbar_arrive_expect_tx(&k_full[0], kTileBytes);
-    tma_load_4d(sm + kOffK, &tmk, 0, 0, hk, b, &k_full[0], pol_kv);
-    tma_load_4d(sm + kOffK + kBox, &tmk, 64, 0, hk, b, &k_full[0], pol_kv);
-    mbar_arrive_expect_tx(&v_full[0], kTileBytes);
-    tma_load_4d(sm + kOffV, &tmv, 0, 0, hk, b, &v_full[0], pol_kv);
-    tma_load_4d(sm + kOffV + kBox, &tmv, 64, 0, hk, b, &v_full[0], pol_kv);
+    if constexpr (!WIN) {  // (with a window the first key tile is known only from the positions)
+      mbar_arrive_expect_tx(&k_full[0], kTileBytes);
+      tma_load_4d(sm + kOffK, &tmk, 0, 0, hk, b, &k_full[0], pol_kv);
+      tma_load_4d(sm + kOffK + kBox, &tmk, 64, 0, hk, b, &k_full[0], pol_kv);
+      mbar_arrive_expect_tx(&v_full[0], kTileBytes);
+      tma_load_4d(sm + kOffV, &tmv, 0, 0, hk, b, &v_full[0], pol_kv);
+      tma_load_4d(sm + kOffV + kBox, &tmv, 64, 0, hk, b, &v_full[0], pol_kv);
+    }
   }
 
   // ---- visibility of the rows (integers) ----
   int len = p.seqlens[b * p.sl_s];
   len = len < 0 ? 0 : (len > p.Tmax ? p.Tmax : len);
-  int my_end = 0;
+  int my_end = 0, my_start = 0;
   bool my_row = false;
   const int row_i = i0 + (int)(threadIdx.x & 127);
   if (warp < 8 && row_i < p.Tq) {
@@ -178,12 +184,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     my_row = true;
     atomicMax(&misc[1 + 2 * x], my_end);
     atomicMin(&misc[2 + 2 * x], my_end);
+    if constexpr (WIN) {
+      // sliding window: keys pos - W < j <= pos (pos >= 0 first: no overflow)
+      my_start = pos < 0 ? 0 : max(0, pos - p.window + 1);
+      if (my_end > my_start) {
+        atomicMin(&misc[6 + 2 * x], my_start);
+        atomicMax(&misc[7 + 2 * x], my_start);
+      }
+    }
   }
   __syncthreads();
-  const int n_t0 = (misc[1] + BN - 1) / BN;
-  const int n_t1 = (misc[3] + BN - 1) / BN;
-  const int n_max = max(n_t0, n_t1);
-  const int cta_end = max(misc[1], misc[3]);
+  // key tiles [f_x, e_x) of query tile x (f_x = 0 without a window), and the
+  // CTA's range [j_lo, j_hi) over the query tiles that see any key; ring
+  // slots and phases count from j_lo
+  int e_t0 = (misc[1] + BN - 1) / BN;
+  int e_t1 = (misc[3] + BN - 1) / BN;
+  int f_t0 = 0, f_t1 = 0;
+  if constexpr (WIN) {
+    f_t0 = misc[6] == 0x7fffffff ? e_t0 : misc[6] / BN;
+    f_t1 = misc[8] == 0x7fffffff ? e_t1 : misc[8] / BN;
+    if (f_t0 >= e_t0) f_t0 = e_t0 = 0;  // no row of the tile sees a key
+    if (f_t1 >= e_t1) f_t1 = e_t1 = 0;
+  }
+  const int n_t0 = e_t0 - f_t0;  // key tiles per query tile
+  const int n_t1 = e_t1 - f_t1;
+  const int j_lo = !WIN ? 0 : (n_t0 == 0 ? f_t1 : (n_t1 == 0 ? f_t0 : min(f_t0, f_t1)));
+  const int j_hi = max(e_t0, e_t1);
+  const int n_max = j_hi - j_lo;  // key tiles the CTA loads
+  const int cta_end = max(n_t0 > 0 ? misc[1] : 0, n_t1 > 0 ? misc[3] : 0);
   const int64_t out_row = (int64_t)b * p.o_sb + (int64_t)h * p.o_sh + (int64_t)row_i * p.o_si;
   const int64_t lse_idx = (int64_t)b * p.l_sb + (int64_t)h * p.l_sh + (int64_t)row_i * p.l_si;
 
@@ -207,19 +235,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (my_row) write_empty_row();
     if (warp == kTmaWarp && lane == 0) {
       bool landed = mbar_wait(q_full, 0);
-      landed = mbar_wait(&k_full[0], 0) && landed;
-      landed = mbar_wait(&v_full[0], 0) && landed;
+      if constexpr (!WIN) {
+        landed = mbar_wait(&k_full[0], 0) && landed;
+        landed = mbar_wait(&v_full[0], 0) && landed;
+      }
       if (!landed) record_error(p.err, kErrTimeout);
     }
   } else if (warp == kTmaWarp) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      // Q and K/V tile 0 are in flight already
-      int k_issued = 1, v_issued = 1;
+      // Q (and, without a window, K/V tile 0) are in flight already; u
+      // counts the CTA's key tiles from j_lo
+      int k_issued = WIN ? 0 : 1, v_issued = WIN ? 0 : 1;
       bool ok = true;
-      for (int j = 1; j < n_max && ok; ++j) {
+      for (int j = WIN ? 0 : 1; j < n_max && ok; ++j) {
         const int s = j % STAGES;
-        const int key0 = j * BN;
+        const int key0 = (j_lo + j) * BN;
         if (j >= STAGES && !mbar_wait(&k_empty[s], ((j / STAGES) - 1) & 1)) { ok = false; break; }
         unsigned char* kd = sm + kOffK + s * kTileBytes;
         mbar_arrive_expect_tx(&k_full[s], kTileBytes);
@@ -263,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::commit(&s_full[t]);
       };
-      // U_t += P_jj V_jj (P_hi, then P_lo)
-      auto issue_pv = [&](int t, int jj) {
+      // U_t += P_jj V_jj (P_hi, then P_lo); `more`: U_t already holds a tile
+      auto issue_pv = [&](int t, int jj, bool more) {
         const uint32_t vlo = tc::desc_lo(sV + (jj % STAGES) * kTileBytes, kBox);
         constexpr uint32_t kHi = tc::desc_hi(1024);
         const uint32_t tcol = tb + t * kTileCols;
@@ -275,16 +306,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             // B = V rows [16ks, 16ks+16) (keys, K) x 128 dims (N, two 64-dim boxes 16 KB apart)
             const uint64_t bdesc = tc::desc_join(vlo + (uint32_t)(ks * 16 * 128 >> 4), kHi);
             const uint32_t acol = tcol + kColS + part * kColPlo + 8 * ks;
-            tc::mma_ts(tcol + kColO, acol, bdesc, kIdescPV, (jj > 0 || part > 0 || ks > 0) ? 1u : 0u);
+            tc::mma_ts(tcol + kColO, acol, bdesc, kIdescPV, (more || part > 0 || ks > 0) ? 1u : 0u);
           }
         }
       };
-      // prologue: S_0 for both query tiles
+      // (j counts the CTA's key tiles from j_lo; query tile t covers
+      // [a_t, a_t + n_t) of them, a_t = 0 without a window)
+      const int a_t0 = f_t0 - j_lo, a_t1 = f_t1 - j_lo;
+      // prologue: the first scores of the query tiles that start at j_lo
       if (ok && !mbar_wait(&k_full[0], 0)) ok = false;
       if (ok) {
         tc::fence_after();
-        if (n_t0 > 0) issue_qk(0, 0);
-        if (n_t1 > 0) issue_qk(1, 0);
+        if (n_t0 > 0 && a_t0 == 0) issue_qk(0, 0);
+        if (n_t1 > 0 && a_t1 == 0) issue_qk(1, 0);
         tc::commit(&k_empty[0]);
       }
       for (int j = 0; ok && j < n_max; ++j) {
@@ -294,13 +328,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (next && !mbar_wait(&k_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1)) { ok = false; break; }
         for (int t = 0; t < QT && ok; ++t) {
           const int nt = t == 0 ? n_t0 : n_t1;
-          if (j >= nt) continue;
+          const int at = t == 0 ? a_t0 : a_t1;
+          if (j < at || j >= at + nt) {
+            // a query tile whose range starts at the next key tile: its first scores
+            if (WIN && nt > 0 && j + 1 == at) issue_qk(t, j + 1);
+            continue;
+          }
           // U += P_j V_j as soon as this query tile's P_j is ready, then
           // S_{j+1} into the same TMEM columns (issue order = execution order)
-          if (!mbar_wait(&p_full[t], j & 1)) { ok = false; break; }
+          if (!mbar_wait(&p_full[t], (j - at) & 1)) { ok = false; break; }
           tc::fence_after();
-          issue_pv(t, j);
-          if (j + 1 < nt) issue_qk(t, j + 1);
+          issue_pv(t, j, j > at);
+          if (j + 1 < at + nt) issue_qk(t, j + 1);
         }
         if (!ok) break;
         tc::commit(&v_empty[s]);                           // V_j free once these products complete
@@ -321,6 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- rows: online softmax statistics (query tile x) ----------------
     const int n_mine = x == 0 ? n_t0 : n_t1;
     const int my_min = misc[2 + 2 * x];
+    const int f_mine = x == 0 ? f_t0 : f_t1;            // first key tile (0 without a window)
+    const int win_max = WIN ? misc[7 + 2 * x] : 0;     // keys below it are masked for some row
     if (n_mine == 0) {
       if (my_row) write_empty_row();
     } else {
@@ -353,11 +394,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             xs[96 + c] = __uint_as_float(r3[c]);
           }
         }
-        const int key0 = j * BN;
+        const int key0 = (f_mine + j) * BN;
         // the mask (select, diagonal tiles only) before any arithmetic
         if (key0 + BN > my_min) {
 #pragma unroll
           for (int c = 0; c < 128; ++c) xs[c] = (key0 + c < my_end) ? xs[c] : kNegInf;
+        }
+        if constexpr (WIN) {
+          // sliding window: keys before the row's first visible key
+          if (key0 < win_max) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c) xs[c] = (key0 + c >= my_start) ? xs[c] : kNegInf;
+          }
         }
         // block maximum on the raw scores (scale > 0), a tree of short chains
         // (three-input max: 8 chains of 8 steps over 16 values each)
@@ -431,8 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (key0 + BN > cta_end) {
           // last tile of the CTA: zero the V rows past every visible key of
           // both query tiles (both may do it; the values are the same)
-          const int s = j % STAGES;
-          if (!wait_all(&v_full[s], (j / STAGES) & 1)) { ok = false; break; }
+          const int u = f_mine - j_lo + j;  // the CTA's key-tile count (ring position)
+          const int s = u % STAGES;
+          if (!wait_all(&v_full[s], (u / STAGES) & 1)) { ok = false; break; }
           unsigned char* vt = sm + kOffV + s * kTileBytes;
           const int z0 = cta_end - key0;
           for (int idx = (int)(threadIdx.x & 127); idx < (BN - z0) * 16; idx += 128) {
@@ -536,10 +585,12 @@ cudaError_t launch_prefill_tc(const FwdParams& p, int n_pairs, const CUtensorMap
                               const CUtensorMap& tmv, const CUtensorMap& tmo, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
+    for (const void* f : {(const void*)prefill_tc_kernel<false>, (const void*)prefill_tc_kernel<true>}) {
+      cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      if (e != cudaSuccess) return e;
+    }
     attr_set = true;
   }
   const int64_t heads = (int64_t)p.Hq * p.B;
@@ -547,7 +598,10 @@ cudaError_t launch_prefill_tc(const FwdParams& p, int n_pairs, const CUtensorMap
   const int64_t groups = (heads + p.head_group - 1) / p.head_group;
   const int64_t blocks = groups * p.head_group * n_pairs;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  prefill_tc_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmk, tmv, tmo);
+  if (p.window > 0)
+    prefill_tc_kernel<true><<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmk, tmv, tmo);
+  else
+    prefill_tc_kernel<false><<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmk, tmv, tmo);
   return cudaGetLastError();
 }
 

@@ -25,6 +25,8 @@ additive bias M_j, grouped heads, and the cached-decoding positions of
   window_decode batch 16, 32/8 heads, d=128, T_q=1 at len-1, cache lengths
                 uniform in [8192, 16384], a sliding window of 4096 keys
                 ("Chapter 33" §33.7, the paragraph of eq. 33.16), bf16
+  window_prefill prefill's shapes (B=2, 32 heads, T=8192, causal) with a sliding
+                window of 1024 keys, bf16
   tree_verify   spec_verify's batch, heads, cache lengths and values with a
                 token tree of T_q=6 draft nodes per sequence ("推理加速算法"
                 §7.2.2 Medusa, tree attention verification): seeded random
@@ -97,6 +99,8 @@ SPECS = {
                         tree="random"),
     "window_decode": Spec("window_decode", 16, 32, 8, 1, 16384, 128, "bf16", ("uniform", 8192, 16384), "last", 8,
                           window=4096),
+    "window_prefill": Spec("window_prefill", 2, 32, 32, 8192, 8192, 128, "bf16", ("fixed", 8192), "causal", 9,
+                           window=1024),
 }
 
 # Reduced twins: same structure, sizes the fp64 oracle covers in seconds, still
@@ -111,6 +115,8 @@ SMALL = {
     "tree_verify": replace(SPECS["tree_verify"], B=3, Hq=16, Hkv=2, Tmax=1290, lens=("verify", 300, 1284)),
     "window_decode": replace(SPECS["window_decode"], B=3, Hq=8, Hkv=2, Tmax=1500, lens=("uniform", 200, 1500),
                              window=333),
+    "window_prefill": replace(SPECS["window_prefill"], B=1, Hq=2, Hkv=2, Tq=333, Tmax=333, lens=("fixed", 333),
+                              window=100),
 }
 
 
@@ -234,7 +240,7 @@ def kv_bytes(s: Spec, seqlens) -> int:
     (sequence, KV head), each read once."""
     elt = 2 if s.dtype == "bf16" else 4
     lens = np.minimum(np.asarray(seqlens, dtype=np.int64), s.Tmax)
-    if s.window:  # rows at len - 1 see only the last `window` keys
+    if s.window and s.pos == "last":  # rows at len - 1 see only the last `window` keys
         lens = np.minimum(lens, s.window)
     return int(lens.sum()) * s.Hkv * s.d * elt * 2
 

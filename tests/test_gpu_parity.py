@@ -126,7 +126,7 @@ def sample_rows(s, inp, n_random=160, seed=0):
 
 
 @pytest.mark.parametrize("name", ["decode_gqa", "long_decode", "spec_verify", "prefill", "tree_verify",
-                                  "window_decode"])
+                                  "window_decode", "window_prefill"])
 def test_full_size_workload_sampled_rows(name):
     s = workloads.spec(name)
     inp = workloads.generate(s)
@@ -448,7 +448,7 @@ def window_case(name):
     elif name == "tc_verify_nr48":   # causal verification rows: a different start per row
         B, Hq, Hkv, lens, W = 3, 16, 2, [2000, 700, 300], 333
         qpos = [[ln - 6 + i for i in range(6)] for ln in lens]
-    elif name == "tc_two_groups":    # 64 rows of one head: two row groups of 32 (never prefill)
+    elif name == "tc_two_groups":    # 64 rows of one head (a prefill shape: the windowed prefill kernel)
         B, Hq, Hkv, lens, W = 2, 2, 2, [1900, 640], 100
         qpos = [[ln - 64 + i for i in range(64)] for ln in lens]
     elif name == "tc_window_one":    # each row sees exactly its own key
@@ -518,6 +518,59 @@ def test_window_covering_the_cache_changes_no_bit(name):
     plain["window"] = 0
     wide = dict(inp)
     wide["window"] = int(inp["seqlens"].max()) + 1
+    raw_p, lse_p, _, _ = run_gpu(plain)
+    raw_w, lse_w, _, _ = run_gpu(wide)
+    assert torch.equal(raw_p, raw_w)
+    assert torch.equal(lse_p, lse_w)
+
+
+def window_prefill_case(name):
+    """Prefill shapes (many query rows per head) with a sliding window: the
+    tcgen05 prefill kernel with a first key tile per CTA and a window mask."""
+    rng = np.random.default_rng(WINDOW_PREFILL_CASES.index(name) + 80)
+    if name == "causal_w100":        # window shorter than a key tile, ragged T
+        B, Hq, Hkv, T, lens, W = 2, 4, 4, 700, [700, 451], 100
+        qpos = [list(range(T))] * B
+    elif name == "causal_w128_gqa":  # window of exactly one key tile, grouped heads
+        B, Hq, Hkv, T, lens, W = 1, 8, 2, 1030, [1030], 128
+        qpos = [list(range(T))]
+    elif name == "causal_w1":        # every row sees only its own key
+        B, Hq, Hkv, T, lens, W = 1, 2, 2, 300, [300], 1
+        qpos = [list(range(T))]
+    elif name == "causal_w1000":     # window longer than most rows' history
+        B, Hq, Hkv, T, lens, W = 1, 2, 2, 1500, [1500], 1000
+        qpos = [list(range(T))]
+    elif name == "last_rows":        # non-causal rows: every row sees the last W keys
+        B, Hq, Hkv, T, lens, W = 2, 2, 1, 200, [900, 333], 257
+        qpos = [[899] * T, [332] * T]
+    else:                            # random positions, including negative and beyond the length
+        B, Hq, Hkv, T, lens, W = 2, 4, 2, 260, [800, 190], 90
+        qpos = [rng.integers(-5, ln + 40, size=T).tolist() for ln in lens]
+    Tmax = max(max(lens), T)
+    inp = make_case(B, Hq, Hkv, T, Tmax, 128, "bf16", lens, qpos, seed=int(rng.integers(1 << 30)))
+    inp["window"] = W
+    return inp
+
+
+WINDOW_PREFILL_CASES = ["causal_w100", "causal_w128_gqa", "causal_w1", "causal_w1000", "last_rows", "random_pos"]
+
+
+@pytest.mark.parametrize("name", WINDOW_PREFILL_CASES)
+def test_window_prefill_cases(name):
+    inp = window_prefill_case(name)
+    assert plan_of(inp)["kernel"] == 2  # the tcgen05 prefill kernel
+    raw, _, o, l = run_gpu(inp)
+    assert_parity(o, l, run_oracle(inp), BF16_TOL_O, BF16_TOL_L, out_raw=raw)
+
+
+def test_window_prefill_covering_the_cache_changes_no_bit():
+    """A window longer than every row's history: the windowed prefill kernel
+    gives the same bits as the unwindowed one."""
+    inp = window_prefill_case("causal_w100")
+    plain = dict(inp)
+    plain["window"] = 0
+    wide = dict(inp)
+    wide["window"] = 100000
     raw_p, lse_p, _, _ = run_gpu(plain)
     raw_w, lse_w, _, _ = run_gpu(wide)
     assert torch.equal(raw_p, raw_w)
