@@ -16,7 +16,8 @@ gradient G_O:
 S_ij = scale * q_i . k_j + M_ij on the visible keys; the pages write 1/sqrt(d_h)
 where the interface takes `scale`, and eq. 33.8's 1/sqrt(d_h) is the same
 factor.  Visibility is the forward's: key j is visible to row (b, h, i) iff
-j < len_b, j <= pos[b, i] and M[b, h, i, j] != -inf.  Invisible keys have
+j < len_b, j <= pos[b, i] and M[b, h, i, j] != -inf, and, with a sliding
+window of W keys (§33.7, the paragraph of eq. 33.16), j > pos[b, i] - W.  Invisible keys have
 P = 0 and take no gradient; a row with no visible key has P = 0 everywhere
 (its forward output is the defined 0) and contributes nothing.  Grouped
 query attention: query head h reads KV head h // G, so G_K and G_V of a KV
@@ -55,13 +56,14 @@ def _f64(x):
 
 
 def attention_backward(q, k, v, seqlens, qpos, scale, dout, bias=None, units=None,
-                       with_abs: bool = True):
+                       with_abs: bool = True, window: int = 0):
     """Gradients of exact attention (eqs. 33.6–33.8) in fp64.
 
     q [B,H_q,T_q,d], k, v [B,H_kv,T_max,d], seqlens int [B], qpos int [B,T_q],
     dout [B,H_q,T_q,d] (the upstream gradient G_O), bias None or broadcastable
     to [B,H_q,T_q,T_max] (finite or -inf).  units: None for every (b, kv head),
     else a list of (b, kv_head) pairs to compute (the others stay zero).
+    window: 0, or W > 0 for sliding-window visibility.
 
     Returns dict(dq [B,H_q,T_q,d], dk, dv [B,H_kv,T_max,d], o [B,H_q,T_q,d],
     lse [B,H_q,T_q] (natural log, -inf for rows with no visible key),
@@ -93,6 +95,8 @@ def attention_backward(q, k, v, seqlens, qpos, scale, dout, bias=None, units=Non
                 Qh, GOh = Q[b, h, r0:r1], GO[b, h, r0:r1]
                 # visibility (the forward's rule)
                 vis = (keys[None, :] < length) & (keys[None, :] <= qp[b, r0:r1, None])
+                if window > 0:
+                    vis &= keys[None, :] > qp[b, r0:r1, None] - window
                 S = scale * (Qh @ Kb.T)
                 if Mb is not None:
                     Mh = Mb[b, h, r0:r1]

@@ -37,15 +37,16 @@ def loss(c, q=None, k=None, v=None):
     q = c["q"] if q is None else q
     k = c["k"] if k is None else k
     v = c["v"] if v is None else v
-    r = oracle.attention(q, k, v, c["seqlens"], c["qpos"], c["scale"], bias=c["bias"])
+    r = oracle.attention(q, k, v, c["seqlens"], c["qpos"], c["scale"], bias=c["bias"], window=c.get("window", 0))
     return float((r["out"].reshape(c["go"].shape) * c["go"]).sum())
 
 
-@pytest.mark.parametrize("G,bias", [(1, False), (2, True), (3, True)])
-def test_gradients_match_finite_differences_of_the_forward_oracle(G, bias):
-    c = tiny_case(seed=G, G=G, bias=bias)
+@pytest.mark.parametrize("G,bias,window", [(1, False, 0), (2, True, 0), (3, True, 0), (2, False, 2), (1, True, 3)])
+def test_gradients_match_finite_differences_of_the_forward_oracle(G, bias, window):
+    c = tiny_case(seed=G + 7 * window, G=G, bias=bias)
+    c["window"] = window
     g = bwd.attention_backward(c["q"], c["k"], c["v"], c["seqlens"], c["qpos"], c["scale"], c["go"],
-                               bias=c["bias"])
+                               bias=c["bias"], window=window)
     h = 1e-6
     for name, key in (("dq", "q"), ("dk", "k"), ("dv", "v")):
         x = c[key]
@@ -183,3 +184,24 @@ def test_error_scales_dominate_the_gradients():
     for name in ("dq", "dk", "dv"):
         assert np.all(g[name + "_abs"] >= 0)
         assert np.all(np.abs(g[name]) <= g[name + "_abs"] + 1e-12)
+
+
+def test_window_gradients_match_fp64_autograd():
+    """Sliding window (keys pos - W < j <= pos): the dense autograd
+    formulation with the window folded into its bias as -inf."""
+    c = tiny_case(seed=31, G=2, bias=False)
+    W = 2
+    B, Hq, Tq, d = c["q"].shape
+    Tmax = c["k"].shape[2]
+    j = np.arange(Tmax)
+    M = np.where(j[None, None, :] > c["qpos"][:, :, None] - W, 0.0, -np.inf)[:, None].repeat(Hq, axis=1)
+    dense = dict(c, bias=M)
+    dq, dk, dv = dense_autograd(dense)
+    g = bwd.attention_backward(c["q"], c["k"], c["v"], c["seqlens"], c["qpos"], c["scale"], c["go"], window=W)
+    np.testing.assert_allclose(g["dq"], dq, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(g["dk"], dk, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(g["dv"], dv, rtol=1e-12, atol=1e-13)
+    # W = 1: one visible key per row, so no score gradient at all
+    g1 = bwd.attention_backward(c["q"], c["k"], c["v"], c["seqlens"], c["qpos"], c["scale"], c["go"], window=1)
+    np.testing.assert_array_equal(g1["dq"], 0.0)
+    np.testing.assert_array_equal(g1["dk"], 0.0)
