@@ -451,22 +451,24 @@ def measure_spec_sample(peaks, steps=10, warmup=3):
                          "algorithmic_bytes": total, "peak_note": f"HBM copy bandwidth, {peaks['source']}"}}
 
 
-def measure_backward(peaks, steps=5, warmup=3):
+def measure_backward(peaks, steps=5, warmup=3, name="prefill"):
     """The backward pass (blkattn_bwd: row facts, dQ, dK/dV) on the causal
     prefill workload with an upstream gradient; inputs come from the
     library's own forward.  Algorithmic work: the five products of eqs.
     33.6-33.8, 10 * d flops per (row, visible key) (2.5x the forward's 4 * d);
     the kernels form S and G_P twice, 7 products in all."""
     from exact_blocked_attention_gb300 import blkattn
-    s = workloads.backward_spec()
+    s = workloads.spec(name)
     cpu = workloads.generate_backward(s)
     dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in cpu.items()}
-    out, lse = blkattn.attention(dev["q"], dev["k"], dev["v"], dev["seqlens"], dev["qpos"], None, cpu["scale"])
+    W = cpu.get("window", 0)
+    out, lse = blkattn.attention(dev["q"], dev["k"], dev["v"], dev["seqlens"], dev["qpos"], None, cpu["scale"],
+                                 window=W)
     dq = torch.empty(dev["q"].shape, dtype=torch.float32, device="cuda")
     dk = torch.empty(dev["k"].shape, dtype=torch.float32, device="cuda")
     dv = torch.empty(dev["v"].shape, dtype=torch.float32, device="cuda")
     call = lambda: blkattn.bwd(dev["q"], dev["k"], dev["v"], dev["seqlens"], dev["qpos"], None, cpu["scale"],
-                               out, lse, dev["go"], dq, dk, dv)
+                               out, lse, dev["go"], dq, dk, dv, window=W)
     in_bytes = sum(t.numel() * t.element_size() for t in (dev["q"], dev["k"], dev["v"], dev["go"], out, lse))
     times = []
     for it in range(warmup + steps):
@@ -481,11 +483,11 @@ def measure_backward(peaks, steps=5, warmup=3):
     t_ms = sum(times) / len(times)
     flops = causal_flops(s, cpu) * 2.5
     achieved = flops / (t_ms * 1e-3) / 1e12
-    return {"workload": f"prefill_backward: {describe(s)} + g_o bf16; dq, dk, dv f32",
+    return {"workload": f"{name}_backward: {describe(s)}" + (f" window={W}" if W else "") + " + g_o bf16; dq, dk, dv f32",
             "us_per_call": t_ms * 1e3, "l2": f"inputs ({in_bytes / 1e6:.0f} MB) larger than L2",
             "kernels": "row facts, dQ (3 products per tile pair), dK/dV (4 products per tile pair)",
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": achieved / peaks["bf16_tflops"], "traffic": measured_traffic("prefill_backward"),
+                         "frac": achieved / peaks["bf16_tflops"], "traffic": measured_traffic(f"{name}_backward"),
                          "algorithmic_flops": flops,
                          "peak_note": f"dense bf16 burst, {peaks['source']}"},
             "frac_of_bf16_sustained": achieved / peaks["bf16_tflops_sustained"]}
@@ -530,6 +532,8 @@ def main():
         blkattn.load()
         if rank == 0:
             print(json.dumps(measure_backward(peaks, steps=args.steps, warmup=args.warmup)), flush=True)
+            print(json.dumps(measure_backward(peaks, steps=args.steps, warmup=args.warmup, name="window_prefill")),
+                  flush=True)
         return
 
     # ---- headline workload: every rank runs its own batch (weak scaling) ----
@@ -591,11 +595,12 @@ def main():
             except Exception as exc:  # report, keep the headline line
                 others[name] = {"error": f"{type(exc).__name__}: {exc}"}
             torch.cuda.empty_cache()
-        try:
-            others["prefill_backward"] = measure_backward(peaks)
-        except Exception as exc:  # reported, not fatal
-            others["prefill_backward"] = {"error": f"{type(exc).__name__}: {exc}"}
-        torch.cuda.empty_cache()
+        for bname in ("prefill", "window_prefill"):
+            try:
+                others[f"{bname}_backward"] = measure_backward(peaks, name=bname)
+            except Exception as exc:  # reported, not fatal
+                others[f"{bname}_backward"] = {"error": f"{type(exc).__name__}: {exc}"}
+            torch.cuda.empty_cache()
         try:
             others["spec_sample"] = measure_spec_sample(peaks)
         except Exception as exc:  # reported, not fatal

@@ -31,7 +31,7 @@ _DTYPES = {torch.bfloat16: BF16, torch.float32: F32, torch.int32: I32, torch.int
 EXPORTED = ("blkattn_fwd", "blkattn_merge", "blkattn_status_string",
             "blkattn_check_device_error", "blkattn_debug_plan", "blkattn_debug_set_split_event",
             "blkattn_fwd_static_scratch", "blkattn_last_cuda_error", "blkattn_fwd_tree",
-            "blkattn_spec_sample", "blkattn_fwd_window", "blkattn_bwd")
+            "blkattn_spec_sample", "blkattn_fwd_window", "blkattn_bwd", "blkattn_bwd_window")
 
 
 class Tensor(ctypes.Structure):
@@ -79,6 +79,8 @@ def load(path: str = LIB_PATH):
             lib.blkattn_fwd_tree.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, P, P, P]
             lib.blkattn_bwd.restype = ctypes.c_int
             lib.blkattn_bwd.argtypes = [P] * 6 + [ctypes.c_float] + [P] * 7
+            lib.blkattn_bwd_window.restype = ctypes.c_int
+            lib.blkattn_bwd_window.argtypes = [P] * 5 + [ctypes.c_int64, P, ctypes.c_float] + [P] * 7
             lib.blkattn_fwd_window.restype = ctypes.c_int
             lib.blkattn_fwd_window.argtypes = [P, P, P, P, P, ctypes.c_int64, P, ctypes.c_float, P, P, P]
             lib.blkattn_spec_sample.restype = ctypes.c_int
@@ -173,25 +175,32 @@ def fwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale: float, out, lse, st
     return out, lse
 
 
-def bwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale: float, out, lse, dout, dq, dk, dv, stream=None):
-    """blkattn_bwd on torch CUDA tensors; dq, dk, dv are written in place."""
+def bwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale: float, out, lse, dout, dq, dk, dv, stream=None,
+        window: int = 0):
+    """blkattn_bwd (blkattn_bwd_window when window > 0) on torch CUDA tensors;
+    dq, dk, dv are written in place."""
     lib = load()
     descs = [describe(t) for t in (q, k, v, seqlens_k, q_logical_pos, mask_bias, out, lse, dout, dq, dk, dv)]
-    st = lib.blkattn_bwd(*[_ref(x) for x in descs[:6]], ctypes.c_float(scale),
-                         *[_ref(x) for x in descs[6:]], _stream_handle(stream) if q.is_cuda else None)
+    sh = _stream_handle(stream) if q.is_cuda else None
+    if window:
+        st = lib.blkattn_bwd_window(*[_ref(x) for x in descs[:5]], ctypes.c_int64(int(window)), _ref(descs[5]),
+                                    ctypes.c_float(scale), *[_ref(x) for x in descs[6:]], sh)
+    else:
+        st = lib.blkattn_bwd(*[_ref(x) for x in descs[:6]], ctypes.c_float(scale),
+                             *[_ref(x) for x in descs[6:]], sh)
     _check(st)
     return dq, dk, dv
 
 
 def attention_backward(q, k, v, seqlens_k, q_logical_pos, out, lse, dout, mask_bias=None, scale=None,
-                       stream=None):
+                       stream=None, window: int = 0):
     """Allocate fp32 dq, dk, dv and call bwd (scale defaults to 1/sqrt(d))."""
     if scale is None:
         scale = q.shape[-1] ** -0.5
     dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
     dk = torch.empty(k.shape, dtype=torch.float32, device=k.device)
     dv = torch.empty(v.shape, dtype=torch.float32, device=v.device)
-    return bwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, dout, dq, dk, dv, stream)
+    return bwd(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, dout, dq, dk, dv, stream, window=window)
 
 
 def fwd_static_scratch(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale: float, out, lse,

@@ -665,7 +665,8 @@ int bwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_ten
              const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos,
              const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out,
              const blkattn_tensor* lse, const blkattn_tensor* dout, const blkattn_tensor* dq,
-             const blkattn_tensor* dk, const blkattn_tensor* dv, blkattn_stream_t stream_) {
+             const blkattn_tensor* dk, const blkattn_tensor* dv, int64_t window, blkattn_stream_t stream_) {
+  if (window < 0 || window > 0x7fffffff) return BLKATTN_ERR_INVALID_ARG;
   Checked c;
   int st = validate_fwd(q, k, v, seqlens_k, q_logical_pos, nullptr, mask_bias, out, lse, &c);
   if (st != BLKATTN_OK) return st;
@@ -699,7 +700,7 @@ int bwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_ten
   const int64_t n_kt = (c.Tmax + 127) / 128;
   const int64_t nrows = c.B * c.Hq * c.Tq;
   auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
-  const int64_t ws = 2 * al(nrows * 4) + al(c.B * n_qt * 4);
+  const int64_t ws = 2 * al(nrows * 4) + 2 * al(c.B * n_qt * 4);
   st = ensure_workspace(ds, (size_t)(ws > 0 ? ws : 256), stream);
   if (st != BLKATTN_OK) return st;
   const CUtensorMap *tmk = nullptr, *tmv = nullptr, *tmq = nullptr, *tmg = nullptr;
@@ -742,6 +743,8 @@ int bwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_ten
   p.ws_D = reinterpret_cast<float*>(base);
   p.ws_L = reinterpret_cast<float*>(base + al(nrows * 4));
   p.ws_end = reinterpret_cast<int*>(base + 2 * al(nrows * 4));
+  p.ws_start = reinterpret_cast<int*>(base + 2 * al(nrows * 4) + al(c.B * n_qt * 4));
+  p.window = (int)window;
   p.B = (int)c.B; p.Hq = (int)c.Hq; p.Hkv = (int)c.Hkv; p.G = (int)(c.Hq / c.Hkv);
   p.Tq = (int)c.Tq; p.Tmax = (int)c.Tmax; p.n_qt = (int)n_qt; p.n_kt = (int)n_kt;
   p.scale = scale;
@@ -826,8 +829,20 @@ int blkattn_bwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_
                 const blkattn_tensor* dk, const blkattn_tensor* dv, blkattn_stream_t stream) {
   if (!q || !k || !v || !seqlens_k || !q_logical_pos || !out || !lse || !dout || !dq || !dk || !dv)
     return BLKATTN_ERR_INVALID_ARG;
-  return blkattn::bwd_impl(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, dout, dq, dk, dv,
+  return blkattn::bwd_impl(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, dout, dq, dk, dv, 0,
                            stream);
+}
+
+int blkattn_bwd_window(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,
+                       const blkattn_tensor* seqlens_k, const blkattn_tensor* q_logical_pos, int64_t window,
+                       const blkattn_tensor* mask_bias, float scale, const blkattn_tensor* out,
+                       const blkattn_tensor* lse, const blkattn_tensor* dout, const blkattn_tensor* dq,
+                       const blkattn_tensor* dk, const blkattn_tensor* dv, blkattn_stream_t stream) {
+  if (!q || !k || !v || !seqlens_k || !q_logical_pos || !out || !lse || !dout || !dq || !dk || !dv)
+    return BLKATTN_ERR_INVALID_ARG;
+  if (window < 1) return BLKATTN_ERR_INVALID_ARG;
+  return blkattn::bwd_impl(q, k, v, seqlens_k, q_logical_pos, mask_bias, scale, out, lse, dout, dq, dk, dv,
+                           window, stream);
 }
 
 int blkattn_merge(const blkattn_states* a, const blkattn_states* b, const blkattn_states* out,

@@ -72,10 +72,11 @@ constexpr int kOffR1 = kOffR0 + STAGES * kTileBytes;  // dQ: V ring | dK/dV: G_O
 constexpr int kOffBar = kOffR1 + STAGES * kTileBytes;
 constexpr int kNumBars = 16;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kOffFacts = kOffMisc + 64;                      // dK/dV: float4 [2][128] (L, D, end, -)
+constexpr int kOffFacts = kOffMisc + 128;                     // dK/dV: float4 [2][128] (-L, -D, end, start)
 constexpr int kMaxQTiles = 1024;                              // query tiles per sequence (T_q <= 131072)
 constexpr int kOffEnds = kOffFacts + 2 * 128 * 16;            // dK/dV: int [kMaxQTiles] row ends per query tile
-constexpr int kSmemBytes = kOffEnds + kMaxQTiles * 4 + 1024;  // + slack to align to 1024
+constexpr int kOffStarts = kOffEnds + kMaxQTiles * 4;         // dK/dV (window): smallest row start per query tile
+constexpr int kSmemBytes = kOffStarts + kMaxQTiles * 4 + 1024;  // + slack to align to 1024
 
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
@@ -109,6 +110,14 @@ __device__ __forceinline__ void issue_acc(uint32_t dcol, uint32_t acol, uint32_t
 __device__ __forceinline__ int row_end(const BwdParams& p, int b, int i, int len) {
   const int pos = p.qpos[b * p.qp_sb + (int64_t)i * p.qp_si];
   return pos < 0 ? 0 : (pos >= len ? len : pos + 1);
+}
+
+// first visible key of row i under the sliding window (0 without one, and
+// for pos < 0: such a row sees nothing anyway); pos >= 0 first, no overflow
+__device__ __forceinline__ int row_start(const BwdParams& p, int b, int i) {
+  if (p.window <= 0) return 0;
+  const int pos = p.qpos[b * p.qp_sb + (int64_t)i * p.qp_si];
+  return pos < 0 ? 0 : max(0, pos - p.window + 1);
 }
 
 __device__ __forceinline__ int seq_len(const BwdParams& p, int b) {
@@ -163,9 +172,14 @@ __global__ void __launch_bounds__(256) bwd_facts_kernel(const BwdParams p) {
     const int b = (int)(e / p.n_qt);
     const int qt = (int)(e % p.n_qt);
     const int len = seq_len(p, b);
-    int mx = 0;
-    for (int i = qt * BT; i < min(qt * BT + BT, p.Tq); ++i) mx = max(mx, row_end(p, b, i, len));
+    int mx = 0, mn = 0x7fffffff;
+    for (int i = qt * BT; i < min(qt * BT + BT, p.Tq); ++i) {
+      const int e_i = row_end(p, b, i, len), s_i = row_start(p, b, i);
+      mx = max(mx, e_i);
+      if (e_i > s_i) mn = min(mn, s_i);
+    }
     p.ws_end[e] = mx;
+    p.ws_start[e] = mn;
   }
 }
 
@@ -186,10 +200,10 @@ __device__ __forceinline__ uint32_t setup_tmem(int* misc, int warp) {
 // G_P in TMEM: G_S = 2^(s scale log2 e + m log2 e - L) (G_P - D), by select
 // where the key is invisible, packed to bf16 pairs.  MASK = false: every
 // entry is visible (no bias, the whole half tile before the row end).
-template <bool BIAS, bool MASK>
+template <bool BIAS, bool MASK, bool WIN = false>
 __device__ __forceinline__ void dq_chunk(const uint32_t (&rs)[32], const uint32_t (&rp)[32], int key, int my_end,
                                          float2 c2, float2 nl2, float2 nd2, const float* brow, int64_t bi_sj,
-                                         int Tmax, uint32_t (&ds)[16]) {
+                                         int Tmax, uint32_t (&ds)[16], int my_start = 0) {
 #pragma unroll
   for (int c = 0; c < 32; c += 2) {
     float2 x = __ffma2_rn(make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])), c2, nl2);
@@ -197,6 +211,10 @@ __device__ __forceinline__ void dq_chunk(const uint32_t (&rs)[32], const uint32_
     if constexpr (MASK) {
       v0 = key + c < my_end;
       v1 = key + c + 1 < my_end;
+      if constexpr (WIN) {  // sliding window: keys before the row's first visible key
+        v0 = v0 && key + c >= my_start;
+        v1 = v1 && key + c + 1 >= my_start;
+      }
     }
     if constexpr (BIAS) {
       const float m0 = key + c < Tmax ? brow[(int64_t)(key + c) * bi_sj] : 0.f;
@@ -218,7 +236,7 @@ __device__ __forceinline__ void dq_chunk(const uint32_t (&rs)[32], const uint32_
 // G_P^T in TMEM and the rows' facts f (-L, -D, end): P^T and G_S^T packed to
 // bf16 pairs, by select where the row does not see the key.  MASK = false:
 // the key is visible to every row of the half (no bias, before every end).
-template <bool BIAS, bool MASK>
+template <bool BIAS, bool MASK, bool WIN = false>
 __device__ __forceinline__ void dkv_chunk(const uint32_t (&rs)[32], const uint32_t (&rp)[32], const float4* f,
                                           int key, float2 c2, const float* bcol, int64_t bi_si, int rows_left,
                                           bool kin, uint32_t (&pp)[16], uint32_t (&ds)[16]) {
@@ -231,6 +249,10 @@ __device__ __forceinline__ void dkv_chunk(const uint32_t (&rs)[32], const uint32
     if constexpr (MASK) {
       v0 = key < __float_as_int(f0.z);
       v1 = key < __float_as_int(f1.z);
+      if constexpr (WIN) {  // sliding window: the row's first visible key in .w
+        v0 = v0 && key >= __float_as_int(f0.w);
+        v1 = v1 && key >= __float_as_int(f1.w);
+      }
     }
     if constexpr (BIAS) {
       const float m0 = (kin && c < rows_left) ? bcol[(int64_t)c * bi_si] : 0.f;
@@ -257,7 +279,7 @@ __device__ __forceinline__ void dkv_chunk(const uint32_t (&rs)[32], const uint32
 }
 
 // ---------------------------------------------------------------- dQ
-template <bool BIAS>
+template <bool BIAS, bool WIN>
 __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& tmq, const CUtensorMap& tmg,
                                         const CUtensorMap& tmk, const CUtensorMap& tmv, int blk) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -290,6 +312,7 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
 
   if (threadIdx.x == 0) {
     misc[1] = 0;
+    if constexpr (WIN) misc[2] = 0x7fffffff;
     mbar_init(q_full, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&k_full[s], 1);
@@ -313,22 +336,39 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
     tma_load_4d(sm + kOffA0 + kBox, &tmq, 64, i0, h, b, q_full, pol);
     tma_load_4d(sm + kOffA1, &tmg, 0, i0, h, b, q_full, pol);
     tma_load_4d(sm + kOffA1 + kBox, &tmg, 64, i0, h, b, q_full, pol);
-    mbar_arrive_expect_tx(&k_full[0], kTileBytes);
-    tma_load_4d(sm + kOffR0, &tmk, 0, 0, hk, b, &k_full[0], pol);
-    tma_load_4d(sm + kOffR0 + kBox, &tmk, 64, 0, hk, b, &k_full[0], pol);
-    mbar_arrive_expect_tx(&v_full[0], kTileBytes);
-    tma_load_4d(sm + kOffR1, &tmv, 0, 0, hk, b, &v_full[0], pol);
-    tma_load_4d(sm + kOffR1 + kBox, &tmv, 64, 0, hk, b, &v_full[0], pol);
+    if constexpr (!WIN) {  // (with a window the first key tile is known only from the positions)
+      mbar_arrive_expect_tx(&k_full[0], kTileBytes);
+      tma_load_4d(sm + kOffR0, &tmk, 0, 0, hk, b, &k_full[0], pol);
+      tma_load_4d(sm + kOffR0 + kBox, &tmk, 64, 0, hk, b, &k_full[0], pol);
+      mbar_arrive_expect_tx(&v_full[0], kTileBytes);
+      tma_load_4d(sm + kOffR1, &tmv, 0, 0, hk, b, &v_full[0], pol);
+      tma_load_4d(sm + kOffR1 + kBox, &tmv, 64, 0, hk, b, &v_full[0], pol);
+    }
   }
 
   const int len = seq_len(p, b);
   const int row_i = i0 + (int)(threadIdx.x & 127);
   const bool my_row = warp < 8 && row_i < p.Tq;
   const int my_end = my_row ? row_end(p, b, row_i, len) : 0;
-  if (my_row && warp < 4) atomicMax(&misc[1], my_end);
+  int my_start = 0;
+  if constexpr (WIN) {
+    my_start = my_row ? row_start(p, b, row_i) : 0;
+    if (my_row && warp < 4 && my_end > my_start) {
+      atomicMax(&misc[1], my_end);
+      atomicMin(&misc[2], my_start);
+    }
+  } else {
+    if (my_row && warp < 4) atomicMax(&misc[1], my_end);
+  }
   __syncthreads();
+  // key tiles [j_lo, j_lo + n) (j_lo = 0 without a window); ring slots and
+  // phases count from j_lo
   const int cta_end = misc[1];
-  const int n = (cta_end + BT - 1) / BT;
+  int j_lo = 0, n = (cta_end + BT - 1) / BT;
+  if constexpr (WIN) {
+    j_lo = misc[2] != 0x7fffffff ? misc[2] / BT : 0;
+    n = max(0, n - j_lo);
+  }
   const uint32_t sQ = smem_u32(sm + kOffA0), sG = smem_u32(sm + kOffA1);
   const uint32_t sK = smem_u32(sm + kOffR0), sV = smem_u32(sm + kOffR1);
   const int grp = (warp >> 2) & 1;  // column half of a compute warp
@@ -340,27 +380,30 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
       for (int c = 0; c < HT; c += 4) *reinterpret_cast<float4*>(dq_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
     if (warp == kTmaWarp && lane == 0) {
       bool landed = mbar_wait(q_full, 0);
-      landed = mbar_wait(&k_full[0], 0) && landed;
-      landed = mbar_wait(&v_full[0], 0) && landed;
+      if constexpr (!WIN) {
+        landed = mbar_wait(&k_full[0], 0) && landed;
+        landed = mbar_wait(&v_full[0], 0) && landed;
+      }
       if (!landed) record_error(p.err, kErrTimeout);
     }
   } else if (warp == kTmaWarp) {
     if (lane == 0) {
-      // Q, G_O and K/V tile 0 are in flight already
-      int k_issued = 1, v_issued = 1;
+      // Q, G_O (and, without a window, K/V tile 0) are in flight already
+      int k_issued = WIN ? 0 : 1, v_issued = WIN ? 0 : 1;
       bool ok = true;
-      for (int j = 1; j < n && ok; ++j) {
+      for (int j = WIN ? 0 : 1; j < n && ok; ++j) {
         const int s = j % STAGES;
         const uint32_t ph = ((j / STAGES) - 1) & 1;
+        const int key0 = (j_lo + j) * BT;
         if (j >= STAGES && !mbar_wait(&k_empty[s], ph)) { ok = false; break; }
         mbar_arrive_expect_tx(&k_full[s], kTileBytes);
-        tma_load_4d(sm + kOffR0 + s * kTileBytes, &tmk, 0, j * BT, hk, b, &k_full[s], pol);
-        tma_load_4d(sm + kOffR0 + s * kTileBytes + kBox, &tmk, 64, j * BT, hk, b, &k_full[s], pol);
+        tma_load_4d(sm + kOffR0 + s * kTileBytes, &tmk, 0, key0, hk, b, &k_full[s], pol);
+        tma_load_4d(sm + kOffR0 + s * kTileBytes + kBox, &tmk, 64, key0, hk, b, &k_full[s], pol);
         k_issued = j + 1;
         if (j >= STAGES && !mbar_wait(&v_empty[s], ph)) { ok = false; break; }
         mbar_arrive_expect_tx(&v_full[s], kTileBytes);
-        tma_load_4d(sm + kOffR1 + s * kTileBytes, &tmv, 0, j * BT, hk, b, &v_full[s], pol);
-        tma_load_4d(sm + kOffR1 + s * kTileBytes + kBox, &tmv, 64, j * BT, hk, b, &v_full[s], pol);
+        tma_load_4d(sm + kOffR1 + s * kTileBytes, &tmv, 0, key0, hk, b, &v_full[s], pol);
+        tma_load_4d(sm + kOffR1 + s * kTileBytes + kBox, &tmv, 64, key0, hk, b, &v_full[s], pol);
         v_issued = j + 1;
       }
       // every issued copy lands before the CTA exits
@@ -437,9 +480,9 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
     for (int j = 0; j < n; ++j) {
       if (!wait_all(&sp_full[grp], j & 1)) { ok = false; break; }
       tc::fence_after();
-      const int key0 = j * BT + grp * HT;  // first key of this half
+      const int key0 = (j_lo + j) * BT + grp * HT;  // first key of this half
       // (warp-uniform) every row of the warp sees every key of the half
-      const bool whole = !BIAS && __all_sync(0xffffffffu, key0 + HT <= my_end);
+      const bool whole = !BIAS && __all_sync(0xffffffffu, key0 + HT <= my_end && (!WIN || key0 >= my_start));
 #pragma unroll
       for (int q2 = 0; q2 < 2; ++q2) {
         uint32_t rs[32], rp[32], ds[16];
@@ -448,18 +491,18 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
         tc::wait_ld();
         const int key = key0 + 32 * q2;
         if (whole)
-          dq_chunk<BIAS, false>(rs, rp, key, my_end, c2, nl2, nd2, brow, p.bi_sj, p.Tmax, ds);
+          dq_chunk<BIAS, false, WIN>(rs, rp, key, my_end, c2, nl2, nd2, brow, p.bi_sj, p.Tmax, ds, my_start);
         else
-          dq_chunk<BIAS, true>(rs, rp, key, my_end, c2, nl2, nd2, brow, p.bi_sj, p.Tmax, ds);
+          dq_chunk<BIAS, true, WIN>(rs, rp, key, my_end, c2, nl2, nd2, brow, p.bi_sj, p.Tmax, ds, my_start);
         tc::st16(tl + 128 + HT * grp + 16 * q2, ds);  // G_S over G_P's first 32 columns of the half
       }
-      if (j * BT + BT > cta_end) {
+      if ((j_lo + j) * BT + BT > cta_end) {
         // last tile: the K rows of this half past every visible key of the
         // CTA are zeroed before G_S K reads them (they may hold anything)
         const int s = j % STAGES;
         if (!wait_all(&k_full[s], (j / STAGES) & 1)) { ok = false; break; }
         unsigned char* kt = sm + kOffR0 + s * kTileBytes;
-        const int z0 = max(cta_end - j * BT, grp * HT);
+        const int z0 = max(cta_end - (j_lo + j) * BT, grp * HT);
         const int t = (int)(threadIdx.x & 127);
         for (int idx = t; idx < (grp * HT + HT - z0) * 16; idx += 128) {
           const int r = z0 + (idx >> 4);
@@ -505,11 +548,14 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
 // ---------------------------------------------------------------- dK / dV
 // The (query head, query tile) pairs a key tile visits: for each of the G
 // heads of its KV head, the query tiles whose largest row end passes the
-// tile's first key.  Every role walks the same sequence.
+// tile's first key (and, with a sliding window, whose smallest row start
+// comes before its last key).  Every role walks the same sequence.
 struct Visit {
   int g, qt;
 };
-__device__ __forceinline__ bool next_visit(const BwdParams& p, const int* ends, int k0, Visit& v) {
+template <bool WIN>
+__device__ __forceinline__ bool next_visit(const BwdParams& p, const int* ends, const int* starts, int k0,
+                                           Visit& v) {
   // advance from v (exclusive); v.g = -1 starts
   int g = v.g, qt = v.qt + 1;
   if (g < 0) {
@@ -517,7 +563,7 @@ __device__ __forceinline__ bool next_visit(const BwdParams& p, const int* ends, 
     qt = 0;
   }
   while (g < p.G) {
-    while (qt < p.n_qt && ends[qt] <= k0) ++qt;
+    while (qt < p.n_qt && (ends[qt] <= k0 || (WIN && starts[qt] >= k0 + BT))) ++qt;
     if (qt < p.n_qt) {
       v.g = g;
       v.qt = qt;
@@ -529,7 +575,7 @@ __device__ __forceinline__ bool next_visit(const BwdParams& p, const int* ends, 
   return false;
 }
 
-template <bool BIAS>
+template <bool BIAS, bool WIN>
 __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& tmq, const CUtensorMap& tmg,
                                          const CUtensorMap& tmk, const CUtensorMap& tmv, int blk) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -544,6 +590,7 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
   int* misc = reinterpret_cast<int*>(sm + kOffMisc);
   float4* facts = reinterpret_cast<float4*>(sm + kOffFacts);  // [2][128]: L, D, end (int bits), -
   int* ends = reinterpret_cast<int*>(sm + kOffEnds);          // this sequence's row end per query tile
+  int* starts = reinterpret_cast<int*>(sm + kOffStarts);      // (window) smallest row start per query tile
 
   // Groups of p.hg_kv (sequence, KV head) pairs whose query-side tiles fit in
   // L2 together; within a group the longest key tiles first (causal: the
@@ -561,7 +608,10 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
   // the visit sequence is walked from shared memory (a global load per step
   // sat on the MMA thread's path between visits); published by the barrier
   // in setup_tmem
-  for (int i = threadIdx.x; i < p.n_qt; i += kThreads) ends[i] = p.ws_end[(int64_t)b * p.n_qt + i];
+  for (int i = threadIdx.x; i < p.n_qt; i += kThreads) {
+    ends[i] = p.ws_end[(int64_t)b * p.n_qt + i];
+    if constexpr (WIN) starts[i] = p.ws_start[(int64_t)b * p.n_qt + i];
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -581,7 +631,7 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
   const uint32_t sQ = smem_u32(sm + kOffR0), sG = smem_u32(sm + kOffR1);
   const uint64_t pol = policy_evict_first();
   Visit first{-1, -1};
-  const bool any = next_visit(p, ends, k0, first);
+  const bool any = next_visit<WIN>(p, ends, starts, k0, first);
 
   if (warp == kTmaWarp) {
     if (lane == 0 && any) {
@@ -604,7 +654,7 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
         tma_load_4d(sm + kOffR1 + s * kTileBytes, &tmg, 0, row, h, b, &qg_full[s], pol);
         tma_load_4d(sm + kOffR1 + s * kTileBytes + kBox, &tmg, 64, row, h, b, &qg_full[s], pol);
         ++t;
-      } while (next_visit(p, ends, k0, v));
+      } while (next_visit<WIN>(p, ends, starts, k0, v));
       if (!mbar_wait(kv_full, 0)) ok = false;
       for (int u = t - STAGES < 0 ? 0 : t - STAGES; u < t; ++u)
         if (!mbar_wait(&qg_full[u % STAGES], (u / STAGES) & 1)) ok = false;
@@ -632,7 +682,7 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
       Visit v = first;
       for (int t = 0; ok; ++t) {
         const int s = t % STAGES;
-        const bool next = next_visit(p, ends, k0, v);
+        const bool next = next_visit<WIN>(p, ends, starts, k0, v);
         // G_V += P^T G_O and G_K += G_S^T Q over the rows of half 0, then
         // half 0 of the next visit
         if (!mbar_wait(&p_full[0], t & 1)) { ok = false; break; }
@@ -675,15 +725,20 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
         if (t128 < HT) {
           // the facts of this half's query rows, one row per thread
           const int i = v.qt * BT + grp * HT + t128;
-          float4 e = make_float4(-__builtin_huge_valf(), 0.f, __int_as_float(0), 0.f);
+          float4 e = make_float4(-__builtin_huge_valf(), 0.f, __int_as_float(0), __int_as_float(0));
           if (i < p.Tq) {
             const int64_t r = ((int64_t)b * p.Hq + h) * p.Tq + i;
-            e = make_float4(p.ws_L[r], p.ws_D[r], __int_as_float(row_end(p, b, i, len)), 0.f);
+            e = make_float4(p.ws_L[r], p.ws_D[r], __int_as_float(row_end(p, b, i, len)),
+                            __int_as_float(WIN ? row_start(p, b, i) : 0));
           }
           f[t128] = e;
-          // the smallest row end of the half (two warps of 32 rows)
+          // the smallest row end (and largest row start) of the half (two warps of 32 rows)
           const int mn = __reduce_min_sync(0xffffffffu, __float_as_int(e.z));
           if (lane == 0) misc[4 + (t & 1) * 4 + grp * 2 + (t128 >> 5)] = mn;
+          if constexpr (WIN) {
+            const int mx = __reduce_max_sync(0xffffffffu, __float_as_int(e.w));
+            if (lane == 0) misc[12 + (t & 1) * 4 + grp * 2 + (t128 >> 5)] = mx;
+          }
         }
         // (the barrier also publishes the facts; the answer is the same for
         // the group's 128 threads, so none is left at a later barrier)
@@ -695,7 +750,9 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
                  (int64_t)(v.qt * BT + grp * HT) * p.bi_si + (int64_t)key * p.bi_sj;
         // (warp-uniform) every row of the half sees every key of the warp
         const int* mn = misc + 4 + (t & 1) * 4 + grp * 2;
-        const bool whole = !BIAS && __all_sync(0xffffffffu, key < min(mn[0], mn[1]));
+        const int* mx = misc + 12 + (t & 1) * 4 + grp * 2;
+        const bool whole =
+            !BIAS && __all_sync(0xffffffffu, key < min(mn[0], mn[1]) && (!WIN || key >= max(mx[0], mx[1])));
         const int rows_left = p.Tq - (v.qt * BT + grp * HT);  // rows of the half inside T_q
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {
@@ -705,11 +762,11 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
           tc::wait_ld();
           const float* bq = BIAS ? bcol + (int64_t)(32 * q2) * p.bi_si : nullptr;
           if (whole)
-            dkv_chunk<BIAS, false>(rs, rp, f + 32 * q2, key, c2, bq, p.bi_si, rows_left - 32 * q2,
-                                   key < p.Tmax, pp, ds);
+            dkv_chunk<BIAS, false, WIN>(rs, rp, f + 32 * q2, key, c2, bq, p.bi_si, rows_left - 32 * q2,
+                                        key < p.Tmax, pp, ds);
           else
-            dkv_chunk<BIAS, true>(rs, rp, f + 32 * q2, key, c2, bq, p.bi_si, rows_left - 32 * q2,
-                                  key < p.Tmax, pp, ds);
+            dkv_chunk<BIAS, true, WIN>(rs, rp, f + 32 * q2, key, c2, bq, p.bi_si, rows_left - 32 * q2,
+                                       key < p.Tmax, pp, ds);
           tc::st16(tl + HT * grp + 16 * q2, pp);        // P^T over S^T's first 32 columns of the half
           tc::st16(tl + 128 + HT * grp + 16 * q2, ds);  // G_S^T likewise over G_P^T
         }
@@ -717,7 +774,7 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[grp]);
-        if (!next_visit(p, ends, k0, v)) break;
+        if (!next_visit<WIN>(p, ends, starts, k0, v)) break;
       }
       if (ok && !wait_all(drain, 0)) ok = false;
     }
@@ -762,24 +819,24 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
   if (warp == kMmaWarp) tc::dealloc(tb, kTmemCols);
 }
 
-template <bool BIAS>
+template <bool BIAS, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmg,
               const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
-  dq_body<BIAS>(p, tmq, tmg, tmk, tmv, (int)blockIdx.x);
+  dq_body<BIAS, WIN>(p, tmq, tmg, tmk, tmv, (int)blockIdx.x);
 }
-template <bool BIAS>
+template <bool BIAS, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     dkv_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmg,
                const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
-  dkv_body<BIAS>(p, tmq, tmg, tmk, tmv, (int)blockIdx.x);
+  dkv_body<BIAS, WIN>(p, tmq, tmg, tmk, tmv, (int)blockIdx.x);
 }
-template <bool BIAS>
+template <bool BIAS, bool WIN>
 cudaError_t launch_pair(const BwdParams& p, const CUtensorMap& tmq, const CUtensorMap& tmg, const CUtensorMap& tmk,
                         const CUtensorMap& tmv, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    for (const void* f : {(const void*)dq_kernel<BIAS>, (const void*)dkv_kernel<BIAS>}) {
+    for (const void* f : {(const void*)dq_kernel<BIAS, WIN>, (const void*)dkv_kernel<BIAS, WIN>}) {
       cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
       if (e != cudaSuccess) return e;
     }
@@ -790,10 +847,10 @@ cudaError_t launch_pair(const BwdParams& p, const CUtensorMap& tmq, const CUtens
   const int64_t dkv_blocks = ((int64_t)p.B * p.Hkv + p.hg_kv - 1) / p.hg_kv * p.hg_kv * p.n_kt;
   if (dq_blocks > 0x7fffffff || dkv_blocks > 0x7fffffff) return cudaErrorInvalidValue;
   if (dq_blocks > 0) {
-    dq_kernel<BIAS><<<(unsigned)dq_blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmg, tmk, tmv);
+    dq_kernel<BIAS, WIN><<<(unsigned)dq_blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmg, tmk, tmv);
     if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
   }
-  dkv_kernel<BIAS><<<(unsigned)dkv_blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmg, tmk, tmv);
+  dkv_kernel<BIAS, WIN><<<(unsigned)dkv_blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmg, tmk, tmv);
   return cudaGetLastError();
 }
 
@@ -809,8 +866,11 @@ cudaError_t launch_backward(const BwdParams& p, const CUtensorMap& tmq, const CU
   if (fb > 4096) fb = 4096;
   bwd_facts_kernel<<<(unsigned)fb, 256, 0, stream>>>(p);
   if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
-  return p.bias != nullptr ? launch_pair<true>(p, tmq, tmg, tmk, tmv, stream)
-                           : launch_pair<false>(p, tmq, tmg, tmk, tmv, stream);
+  if (p.window > 0)
+    return p.bias != nullptr ? launch_pair<true, true>(p, tmq, tmg, tmk, tmv, stream)
+                             : launch_pair<false, true>(p, tmq, tmg, tmk, tmv, stream);
+  return p.bias != nullptr ? launch_pair<true, false>(p, tmq, tmg, tmk, tmv, stream)
+                           : launch_pair<false, false>(p, tmq, tmg, tmk, tmv, stream);
 }
 
 }  // namespace blkattn

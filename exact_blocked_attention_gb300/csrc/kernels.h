@@ -152,6 +152,8 @@ struct BwdParams {
   float* ws_D;    // [B * H_q * T_q] row sums g_o . o
   float* ws_L;    // [B * H_q * T_q] lse in base-2 units (+inf for an empty row)
   int* ws_end;    // [B * n_qt] largest row end min(pos + 1, len) of each 128-row query tile
+  int* ws_start;  // [B * n_qt] smallest first visible key of the tile's rows that see a key (INT_MAX: none)
+  int window;     // sliding window (0: none): a row sees keys pos - window < j <= pos
   int B, Hq, Hkv, G, Tq, Tmax, n_qt, n_kt;
   int hg_q;   // dQ: (sequence, head) pairs dispatched together (their K/V fit in L2)
   int hg_kv;  // dK/dV: (sequence, KV head) pairs dispatched together (their Q, g_o fit in L2)

@@ -282,6 +282,23 @@ int blkattn_bwd(const blkattn_tensor* q, const blkattn_tensor* k,
                 blkattn_stream_t stream);
 
 /*
+ * blkattn_bwd_window — blkattn_bwd for a blkattn_fwd_window call: the same
+ * arguments plus window >= 1 (keys pos - window < j <= pos, "Chapter 33"
+ * §33.7, the paragraph of eq. 33.16).  Each dQ block starts at the key tile
+ * of its rows' earliest visible key and each dK/dV block visits only the
+ * query tiles whose windows reach it.  Returns as blkattn_bwd;
+ * BLKATTN_ERR_INVALID_ARG also for window < 1 or window > 2^31 - 1.
+ */
+int blkattn_bwd_window(const blkattn_tensor* q, const blkattn_tensor* k,
+                       const blkattn_tensor* v, const blkattn_tensor* seqlens_k,
+                       const blkattn_tensor* q_logical_pos, int64_t window,
+                       const blkattn_tensor* mask_bias, float scale,
+                       const blkattn_tensor* out, const blkattn_tensor* lse,
+                       const blkattn_tensor* dout, const blkattn_tensor* dq,
+                       const blkattn_tensor* dk, const blkattn_tensor* dv,
+                       blkattn_stream_t stream);
+
+/*
  * Attention states of rows, in the sufficient statistics of eq. 33.3:
  *   m [rows]           f32, the maximum score (natural-log units); -inf = empty
  *   l [rows]           f32, sum e^{z_j - m}; NULL means "normalised": l = 1 and

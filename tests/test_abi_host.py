@@ -214,6 +214,17 @@ def test_backward_needs_a_finite_scale(lib, scale):
     assert call_bwd(lib, bwd_args(), scale) == -1
 
 
+@pytest.mark.parametrize("window", [0, -3, 1 << 31])
+def test_backward_window_must_be_a_positive_int32(lib, window):
+    a = bwd_args()
+    names = ("q", "k", "v", "sl", "qp", "bias", "out", "lse", "dout", "dq", "dk", "dv")
+    ds = [None if a[n] is None else a[n].desc() for n in names]
+    ref = lambda d: None if d is None else ctypes.byref(d)
+    st = lib.blkattn_bwd_window(*[ref(x) for x in ds[:5]], ctypes.c_int64(window), ref(ds[5]), ctypes.c_float(0.1),
+                                *[ref(x) for x in ds[6:]], None)
+    assert st == -1
+
+
 def test_backward_empty_batch_is_a_no_op(lib):
     a = bwd_args(B=0)
     for t in a.values():

@@ -40,7 +40,7 @@ def make(B, Hq, Hkv, Tq, Tmax, seqlens, qpos, bias=None, seed=0, d=128):
 
 def reference(c, units=None):
     return obwd.attention_backward(c["q"], c["k"], c["v"], c["seqlens"], c["qpos"], c["scale"], c["go"],
-                                   bias=c["bias"], units=units)
+                                   bias=c["bias"], units=units, window=c.get("window", 0))
 
 
 def run(c, o, lse):
@@ -48,7 +48,7 @@ def run(c, o, lse):
     dev = lambda t: None if t is None else t.cuda()
     dq, dk, dv = blkattn.attention_backward(dev(c["q"]), dev(c["k"]), dev(c["v"]), dev(c["seqlens"]),
                                             dev(c["qpos"]), dev(o), dev(lse), dev(c["go"]),
-                                            mask_bias=dev(c["bias"]), scale=c["scale"])
+                                            mask_bias=dev(c["bias"]), scale=c["scale"], window=c.get("window", 0))
     torch.cuda.synchronize()
     assert blkattn.check_device_error() == 0
     return dq.cpu(), dk.cpu(), dv.cpu()
@@ -241,3 +241,71 @@ def test_backward_bias_broadcast_over_heads_with_groups():
     ref = reference(c)
     o, lse = oracle_forward_state(ref)
     assert_grads(run(c, o, lse), ref)
+
+
+# sliding window ("Chapter 33" §33.7, the paragraph of eq. 33.16): keys
+# pos - W < j <= pos; the dQ blocks start at their rows' earliest visible key
+# tile and the dK/dV blocks visit only the query tiles whose windows reach them
+
+def window_case(name):
+    if name == "causal_w100":
+        T = 300
+        c = make(2, 4, 4, T, T, [T, 251], [list(range(T))] * 2, seed=21)
+        c["window"] = 100
+    elif name == "causal_w128_gqa":
+        T = 520
+        c = make(1, 8, 2, T, T, [T], [list(range(T))], seed=22)
+        c["window"] = 128
+    elif name == "w1":
+        T = 200
+        c = make(1, 2, 2, T, T, [T], [list(range(T))], seed=23)
+        c["window"] = 1
+    elif name == "decode_rows":
+        c = case("decode_rows")
+        c["window"] = 77
+    elif name == "bias_broadcast":
+        B, T = 2, 260
+        g = torch.Generator().manual_seed(24)
+        bias = torch.randn(B, 1, T, T, generator=g)
+        bias[torch.rand(B, 1, T, T, generator=g) < 0.2] = -math.inf
+        c = make(B, 4, 2, T, T, [T, 190], [list(range(T))] * 2, bias=bias, seed=25)
+        c["window"] = 60
+    else:  # random positions, some beyond the length or negative
+        rng = np.random.default_rng(26)
+        B, T = 2, 270
+        c = make(B, 4, 2, T, 700, [700, 300], [rng.integers(-4, 740, T).tolist(), rng.integers(-4, 330, T).tolist()],
+                 seed=27)
+        c["window"] = 150
+    return c
+
+
+WINDOW_CASES = ["causal_w100", "causal_w128_gqa", "w1", "decode_rows", "bias_broadcast", "random_pos"]
+
+
+@pytest.mark.parametrize("name", WINDOW_CASES)
+def test_window_backward_matches_the_oracle(name):
+    c = window_case(name)
+    ref = reference(c)
+    o, lse = oracle_forward_state(ref)
+    assert_grads(run(c, o, lse), ref)
+
+
+def test_window_backward_after_the_library_windowed_forward():
+    c = window_case("causal_w128_gqa")
+    dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in c.items()}
+    out, lse = blkattn.attention(dev["q"], dev["k"], dev["v"], dev["seqlens"], dev["qpos"], None, c["scale"],
+                                 window=c["window"])
+    torch.cuda.synchronize()
+    assert_grads(run(c, out.cpu(), lse.cpu()), reference(c))
+
+
+def test_window_covering_everything_changes_no_bit():
+    """A window longer than every row's history: the windowed kernels give the
+    same bits as the unwindowed ones."""
+    c = window_case("causal_w100")
+    ref = reference(dict(c, window=0))
+    o, lse = oracle_forward_state(ref)
+    a = run(dict(c, window=0), o, lse)
+    b = run(dict(c, window=100000), o, lse)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)

@@ -136,6 +136,7 @@ def random_bwd_case(seed):
         bias = torch.randn(B, 1, Tq, Tmax, generator=g)
         bias[torch.rand(B, 1, Tq, Tmax, generator=g) < 0.2] = -math.inf
         c["bias"] = bias
+    c["window"] = int(rng.integers(1, Tmax + 20)) if rng.random() < 0.35 else 0
     return c
 
 
@@ -143,13 +144,13 @@ def random_bwd_case(seed):
 def test_random_backward(seed):
     c = random_bwd_case(seed)
     ref = obwd.attention_backward(c["q"], c["k"], c["v"], c["seqlens"], c["qpos"], c["scale"], c["go"],
-                                  bias=c["bias"])
+                                  bias=c["bias"], window=c["window"])
     dev = lambda t: None if t is None else t.cuda()
     o = torch.from_numpy(ref["o"]).float()
     lse = torch.from_numpy(ref["lse"]).float()
     dq, dk, dv = blkattn.attention_backward(dev(c["q"]), dev(c["k"]), dev(c["v"]), dev(c["seqlens"]),
                                             dev(c["qpos"]), dev(o), dev(lse), dev(c["go"]),
-                                            mask_bias=dev(c["bias"]), scale=c["scale"])
+                                            mask_bias=dev(c["bias"]), scale=c["scale"], window=c["window"])
     torch.cuda.synchronize()
     assert blkattn.check_device_error() == 0
     for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
