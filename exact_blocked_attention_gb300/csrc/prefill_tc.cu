@@ -34,6 +34,12 @@
 // the state (m, l, u) still represents the same set (eqs. 33.4-33.5 hold for
 // any common reference), and P <= 2^8.
 //
+// With a sliding window ("Chapter 33" §33.7, the paragraph of eq. 33.16;
+// the WIN instantiation) a row at position pos sees keys pos - W < j <= pos:
+// each query tile gets a first key tile (its rows' earliest visible key), the
+// CTA loads from the smaller of the two, and the leading tiles are masked per
+// row.  The unwindowed instantiation is unchanged by this.
+//
 // Rows with no visible key keep the empty state and get out = 0,
 // lse = -inf.  V rows of the last tile past the CTA's last visible key (cache
 // padding, possibly NaN) are zero-filled in shared memory before the PV

@@ -155,10 +155,10 @@ int blkattn_fwd_tree(const blkattn_tensor* q, const blkattn_tensor* k,
  * Arguments as blkattn_fwd, plus window >= 1: a row at logical position pos
  * sees only keys j with pos - window < j <= pos (the window most recent
  * positions up to its own), on top of the length, position and bias
- * conditions.  The decode/verify kernels skip the key tiles before a unit's
- * earliest visible key; window calls never take the prefill kernel, and the
- * tcgen05 decode kernel takes at most 512 (sequence x row group) units of
- * them (more go to the split kernels).  Returns as blkattn_fwd;
+ * conditions.  The kernels skip the key tiles before their rows' earliest
+ * visible key (the tcgen05 decode kernel per unit, the prefill kernel per
+ * CTA); the tcgen05 decode kernel takes at most 512 (sequence x row group)
+ * units of window calls (more go to the split kernels).  Returns as blkattn_fwd;
  * BLKATTN_ERR_INVALID_ARG also for window < 1 or window > 2^31 - 1.
  */
 int blkattn_fwd_window(const blkattn_tensor* q, const blkattn_tensor* k,
