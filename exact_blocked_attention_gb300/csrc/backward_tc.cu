@@ -37,8 +37,11 @@
 // execute in issue order, so a new S may overwrite the columns the previous
 // products read.  Every wait is bounded (error flag, then an orderly exit).
 //
-// Visibility is the forward's (length, position, bias; select, not add):
-// invisible entries get P = 0 and G_S = 0 exactly.  Cache rows past the last
+// Visibility is the forward's (length, position, bias, and with the WIN
+// instantiations a sliding window; select, not add): invisible entries get
+// P = 0 and G_S = 0 exactly.  With a window, dQ blocks start at their rows'
+// earliest visible key tile and dK/dV blocks skip the query tiles whose
+// windows end before them.  Cache rows past the last
 // key a CTA's rows see may hold anything (NaN): the dQ kernel zeroes those K
 // rows in shared memory before G_S K reads them.
 #include <cuda_bf16.h>
