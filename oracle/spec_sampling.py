@@ -18,11 +18,10 @@ One verification step (the integer decisions the kernel must reproduce):
   At the first rejection the emitted token is drawn from the residual of
   that position; if every candidate is accepted it is drawn from the next
   target distribution p_{k+1}.  The draw is an inverse CDF in fixed point:
-  the mass of x is m = p(x) - q(x) for a residual, taken in fp32 like its
-  operands (one correctly rounded subtraction), or p(x) for a target; it is
-  clamped to [0, 2] and becomes the weight F(m) = floor(m * 2^40) (exact:
-  scaling an fp32 by a power of two only moves its exponent); integer prefix
-  sums C, Z_int = C(V-1),
+  the mass of x is m = p(x) - q(x) for a residual, the EXACT difference of
+  the two fp32 values as eq. 33.12 writes it (no rounding), or p(x) for a
+  target; it is clamped to [0, 2] and becomes the weight
+  F(m) = floor(m * 2^40); integer prefix sums C, Z_int = C(V-1),
   threshold T = floor(s * Z_int / 2^32) for the 32-bit uniform integer s, and
   the token is the smallest x with C(x) > T.  Integer sums make the choice
   independent of summation order.  When a rejection meets a zero residual
@@ -34,6 +33,9 @@ One verification step (the integer decisions the kernel must reproduce):
   (not a distribution) gives token 0.
 """
 from __future__ import annotations
+
+import math
+from fractions import Fraction
 
 import numpy as np
 
@@ -56,18 +58,39 @@ def acceptance(p, q):
 
 
 def fixed(m) -> np.ndarray:
-    """F(m) = floor(clamp(m, 0, 2) * 2^40) (int64) of fp32 masses, exact
-    (NaN counts as 0, like the fp32 min/max that skip NaN)."""
-    m = np.fmin(np.fmax(np.asarray(m, dtype=np.float32), np.float32(0.0)), np.float32(2.0))
-    return np.floor(m.astype(np.float64) * float(1 << FIX_BITS)).astype(np.int64)
+    """F(m) = floor(clamp(m, 0, 2) * 2^40) (int64) of fp64 masses, exact:
+    scaling by a power of two only moves the exponent (NaN counts as 0, like
+    a min/max that skips NaN)."""
+    m = np.fmin(np.fmax(np.asarray(m, dtype=np.float64), 0.0), 2.0)
+    return np.floor(m * float(1 << FIX_BITS)).astype(np.int64)
+
+
+def fixed_exact(m: Fraction) -> int:
+    """F(m) for an exact rational mass."""
+    m = min(max(m, Fraction(0)), Fraction(2))
+    return math.floor(m * (1 << FIX_BITS))
 
 
 def weights(p_row, q_row=None) -> np.ndarray:
-    """Fixed-point weights of the residual p - q (fp32 subtraction) or of p."""
-    p_row = np.asarray(p_row, dtype=np.float32)
+    """Fixed-point weights F([p - q]_+) of eq. 33.12's residual, with p - q
+    the exact difference of the fp32 values, or F(p) of a target row.
+
+    A nonzero fp32 value has all its bits between 2^(e-24) and 2^(e-1), e its
+    binary exponent (np.frexp), so the difference of two finite fp32 values
+    needs at most |e_p - e_q| + 25 bits: an fp64 subtraction is exact when the
+    exponents are at most 28 apart (or either value is 0).  The other entries
+    are subtracted as rationals."""
+    p = np.asarray(p_row, dtype=np.float32).astype(np.float64)
     if q_row is None:
-        return fixed(p_row)
-    return fixed(p_row - np.asarray(q_row, dtype=np.float32))
+        return fixed(p)
+    q = np.asarray(q_row, dtype=np.float32).astype(np.float64)
+    w = fixed(p - q)
+    _, ep = np.frexp(p)
+    _, eq = np.frexp(q)
+    wide = np.isfinite(p) & np.isfinite(q) & (p != 0) & (q != 0) & (np.abs(ep - eq) > 28)
+    for x in np.flatnonzero(wide):
+        w.flat[x] = fixed_exact(Fraction(float(p.flat[x])) - Fraction(float(q.flat[x])))
+    return w
 
 
 def inverse_cdf(w: np.ndarray, s: int) -> int:

@@ -159,3 +159,73 @@ def test_sampled_output_follows_the_target():
     emitted = np.where(n == 1, x, tok)
     freq = np.bincount(emitted, minlength=V) / N
     assert np.all(np.abs(freq - p) < 5 * np.sqrt(p * (1 - p) / N) + 1e-3)
+
+
+# ---- eq. 33.12's residual [p - q]_+ is the EXACT difference of the fp32 values
+
+EXACT_RESIDUAL_CASES = [
+    # (p, q, F(p - q)) worked out by hand: F(m) = floor(m 2^40)
+    (1 - 2.0**-24, 2.0**-30, 2**40 - 2**16 - 2**10),  # an fp32 subtraction returns p
+    (1 - 2.0**-24, 2.0**-80, 2**40 - 2**16 - 1),      # 80 significant bits: an fp64 subtraction rounds too
+    (0.75, 3 * 2.0**-40, 3 * 2**38 - 3),
+    (0.5, 3 * 2.0**-27, 2**39 - 3 * 2**13),            # fp32 rounds 0.5 - 0.75 ulp to 0.5 - 1 ulp
+    (2.0**-10 + 2.0**-33, 2.0**-10, 2**7),             # cancellation (exact in any precision)
+    (2.0**-17, 2.0**-60, 2**23 - 1),                   # just below an integer weight
+    (0.25, 0.25, 0), (0.1, 0.2, 0),                    # [.]_+ clips
+    (2.0**-41, 0.0, 0), (2.0**-40, 0.0, 1), (3 * 2.0**-41, 2.0**-149, 1),
+]
+
+
+@pytest.mark.parametrize("p,q,want", EXACT_RESIDUAL_CASES)
+def test_residual_weight_is_the_exact_difference(p, q, want):
+    assert np.float32(p) == p and np.float32(q) == q  # the operands are fp32 values
+    assert int(ss.weights(np.array([p], np.float32), np.array([q], np.float32))[0]) == want
+
+
+def test_exact_residual_cases_discriminate_rounding():
+    """The first cases are ones where a rounded subtraction gives another weight
+    (a planted fp32 or fp64 residual would fail the pins above)."""
+    for p, q, want in EXACT_RESIDUAL_CASES[:4]:
+        m32 = float(np.float32(p) - np.float32(q))
+        assert math.floor(m32 * 2**40) != want
+    p, q, want = EXACT_RESIDUAL_CASES[1]
+    assert math.floor((p - q) * 2**40) != want
+
+
+def test_residual_weights_brute_force_wide_exponents():
+    """Random fp32 pairs whose exponents lie up to 60 binades apart, against
+    the exact rational difference formed from integer numerators (every
+    exponent gap, so the rule for where fp64 is exact is pinned too)."""
+    rng = np.random.default_rng(11)
+    n = 4000
+    p = (rng.random(n) * 2.0 ** -rng.integers(0, 30, n)).astype(np.float32)
+    q = (rng.random(n) * 2.0 ** -rng.integers(0, 60, n)).astype(np.float32)
+    q[::7] = p[::7]
+    q[1::7] = np.nextafter(p[1::7], np.float32(0))
+    w = ss.weights(p, q)
+    for x in range(n):
+        a, da = float(p[x]).as_integer_ratio()
+        b, db = float(q[x]).as_integer_ratio()
+        num, den = a * db - b * da, da * db  # p - q = num / den exactly
+        want = 0 if num <= 0 else min((num << 40) // den, 2**41)
+        assert int(w[x]) == want, (x, float(p[x]), float(q[x]))
+    gaps = np.abs(np.frexp(p.astype(np.float64))[1] - np.frexp(q.astype(np.float64))[1])
+    assert (gaps > 28).sum() > 500 and (gaps <= 28).sum() > 500
+
+
+def test_token_follows_the_exact_residual():
+    """A draw on the boundary that the exact residual moves: V = 3, the
+    candidate (token 2, p = 0) is rejected, the residual weights are
+    w = (2^39 - 3 2^13, 2^38, 0) (by hand, as above), and the first draw s
+    with floor(s Z / 2^32) >= w_0 emits token 1 while s - 1 emits token 0.
+    With the residual rounded to fp32 (w_0 = 2^39 - 2^14) both give token 0."""
+    p = np.array([[[0.5, 0.25, 0.0], [1.0, 0.0, 0.0]]], np.float32)
+    q = np.array([[[3 * 2.0**-27, 0.0, 0.5]]], np.float32)
+    w0, w1 = 2**39 - 3 * 2**13, 2**38
+    Z = w0 + w1
+    s = -(-(w0 << 32) // Z)  # ceil(w0 2^32 / Z)
+    assert (s * Z) >> 32 == w0 and ((s - 1) * Z) >> 32 < w0
+    assert tuple(x[0] for x in ss.verify_step(p, q, [[2]], [[0.5]], [s])) == (0, 1)
+    assert tuple(x[0] for x in ss.verify_step(p, q, [[2]], [[0.5]], [s - 1])) == (0, 0)
+    w0r = 2**39 - 2**14  # the rounded residual would put s below its boundary
+    assert (s * (w0r + w1)) >> 32 < w0r
