@@ -188,16 +188,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pos = p.qpos[b * p.qp_sb + row_i * p.qp_si];
     my_end = pos < 0 ? 0 : (pos >= len ? len : pos + 1);
     my_row = true;
-    atomicMax(&misc[1 + 2 * x], my_end);
-    atomicMin(&misc[2 + 2 * x], my_end);
     if constexpr (WIN) {
       // sliding window: keys pos - W < j <= pos (pos >= 0 first: no overflow)
       my_start = pos < 0 ? 0 : max(0, pos - p.window + 1);
       if (my_end > my_start) {
         atomicMin(&misc[6 + 2 * x], my_start);
         atomicMax(&misc[7 + 2 * x], my_start);
+      } else {
+        // a window that starts at or past the cache length holds no key: the
+        // row is masked by its end on every tile, like a row at pos < 0
+        my_end = 0;
       }
     }
+    atomicMax(&misc[1 + 2 * x], my_end);
+    atomicMin(&misc[2 + 2 * x], my_end);
   }
   __syncthreads();
   // key tiles [f_x, e_x) of query tile x (f_x = 0 without a window), and the

@@ -270,6 +270,11 @@ def window_case(name):
         bias[torch.rand(B, 1, T, T, generator=g) < 0.2] = -math.inf
         c = make(B, 4, 2, T, T, [T, 190], [list(range(T))] * 2, bias=bias, seed=25)
         c["window"] = 60
+    elif name == "beyond_window":  # rows whose window starts at or past the length, next to live rows
+        T = 300
+        c = make(2, 2, 1, T, 800, [800, 700], [[100] * 127 + [1000] + [300, 888, 889, 5000] * 43,
+                                               [650] * 128 + [789, 788, 2000] * 57 + [1]], seed=28)
+        c["window"] = 90
     else:  # random positions, some beyond the length or negative
         rng = np.random.default_rng(26)
         B, T = 2, 270
@@ -279,7 +284,7 @@ def window_case(name):
     return c
 
 
-WINDOW_CASES = ["causal_w100", "causal_w128_gqa", "w1", "decode_rows", "bias_broadcast", "random_pos"]
+WINDOW_CASES = ["causal_w100", "causal_w128_gqa", "w1", "decode_rows", "bias_broadcast", "random_pos", "beyond_window"]
 
 
 @pytest.mark.parametrize("name", WINDOW_CASES)

@@ -543,6 +543,10 @@ def window_prefill_case(name):
     elif name == "last_rows":        # non-causal rows: every row sees the last W keys
         B, Hq, Hkv, T, lens, W = 2, 2, 1, 200, [900, 333], 257
         qpos = [[899] * T, [332] * T]
+    elif name == "beyond_window":    # rows whose window starts at or past the length, next to live rows
+        # (len 800, W 90: pos >= 889 sees nothing, pos 888 sees key 799 only)
+        B, Hq, Hkv, T, lens, W = 2, 2, 1, 300, [800, 700], 90
+        qpos = [[100] * 127 + [1000] + [300, 888, 889, 5000] * 43, [650] * 128 + [789, 788, 2000] * 57 + [1]]
     else:                            # random positions, including negative and beyond the length
         B, Hq, Hkv, T, lens, W = 2, 4, 2, 260, [800, 190], 90
         qpos = [rng.integers(-5, ln + 40, size=T).tolist() for ln in lens]
@@ -552,7 +556,8 @@ def window_prefill_case(name):
     return inp
 
 
-WINDOW_PREFILL_CASES = ["causal_w100", "causal_w128_gqa", "causal_w1", "causal_w1000", "last_rows", "random_pos"]
+WINDOW_PREFILL_CASES = ["causal_w100", "causal_w128_gqa", "causal_w1", "causal_w1000", "last_rows", "random_pos",
+                        "beyond_window"]
 
 
 @pytest.mark.parametrize("name", WINDOW_PREFILL_CASES)
@@ -560,7 +565,10 @@ def test_window_prefill_cases(name):
     inp = window_prefill_case(name)
     assert plan_of(inp)["kernel"] == 2  # the tcgen05 prefill kernel
     raw, _, o, l = run_gpu(inp)
-    assert_parity(o, l, run_oracle(inp), BF16_TOL_O, BF16_TOL_L, out_raw=raw)
+    ref = run_oracle(inp)
+    assert_parity(o, l, ref, BF16_TOL_O, BF16_TOL_L, out_raw=raw)
+    if name == "beyond_window":  # the empty rows share query tiles with rows that see keys
+        assert (ref["n_visible"] == 0).sum() >= 2 * 43 * 2 and (ref["n_visible"] > 0).any()
 
 
 def test_window_prefill_covering_the_cache_changes_no_bit():
