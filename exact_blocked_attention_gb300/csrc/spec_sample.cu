@@ -8,11 +8,16 @@
 //   at the first rejection, draw from [p_i - q_i]_+ / Z     (eq. 33.12)
 //   if all k are kept, draw from p_{k+1}
 //
-// The draw is an inverse CDF in fixed point: the mass of token x is
-// p(x) - q(x) in fp32 (one rounded subtraction) for a residual or p(x) for a
-// target, clamped to [0, 2]; its weight is F(m) = floor(m * 2^40), formed as
-// two exact 20-bit halves with fp32 floors (no fp64 and no 64-bit
-// conversion: both run at a small fraction of the fp32 rate here); integer
+// The draw is an inverse CDF in fixed point: the mass of token x is the
+// exact difference p(x) - q(x) for a residual (eq. 33.12 does not round it)
+// or p(x) for a target, clamped to [0, 2]; its weight is F(m) = floor(m *
+// 2^40).  The difference is kept as an unevaluated pair hi + lo with Knuth's
+// TwoSum (TAOCP vol. 2, §4.2.2: hi = fl(p - q) and lo = (p - q) - hi, both
+// exact fp32 values), F(hi) is formed as two exact 20-bit halves with fp32
+// floors, and lo moves the weight only when hi * 2^40 is an integer (then
+// by floor(lo * 2^40); otherwise |lo| 2^40 is below the distance from
+// hi * 2^40 to either neighbouring integer).  No fp64 and no 64-bit
+// conversion: both run at a small fraction of the fp32 rate here.  Integer
 // prefix sums (order-independent, so every reduction shape gives the same
 // token), threshold floor(s * Z / 2^32) for
 // the row's 32-bit uniform s, and the token is the smallest index whose
@@ -47,30 +52,48 @@ constexpr int kCluster = 2;                 // CTAs per sequence
 constexpr int kParts = kCluster * kWarps;   // first-level slices
 constexpr float kTwo20 = 1048576.0f;         // 2^20
 constexpr float kTwo40 = 1099511627776.0f;   // 2^40
-constexpr float kMagic = 12582912.0f;        // 1.5 * 2^23: x + kMagic holds integer x < 2^22 in its low bits
+constexpr float kMagic = 12582912.0f;        // 1.5 * 2^23: x + kMagic holds integer |x| < 2^22 in its low bits
 constexpr int kMagicBits = 0x4B400000;
 
-// mass of one entry: p - q (fp32) for a residual, p for a target; [0, 2]
-__device__ __forceinline__ float mass_of(float pv, float qv, bool has_q) {
-  const float m = has_q ? __fsub_rn(pv, qv) : pv;
-  return fminf(fmaxf(m, 0.f), 2.f);
-}
-
-// F(m) = floor(m 2^40) = h 2^20 + l with h = floor(m 2^20) <= 2^21 and
-// l = floor(m 2^40 - h 2^20) < 2^20, each exact in fp32; they are added to
-// the 32-bit counters (sh, sl) as integers
-__device__ __forceinline__ void add_fixed(float m, int& sh, int& sl) {
-  const float h = floorf(m * kTwo20);
-  const float l = floorf(fmaf(h, -kTwo20, m * kTwo40));
+// Weight F(m) = floor(m 2^40) of one entry, m = clamp(p - q, 0, 2) with the
+// exact difference (has_q) or m = clamp(p, 0, 2), added to the lane's 32-bit
+// counters as F = sh 2^20 + sl:
+//   hi = fl(p - q), lo = (p - q) - hi         (TwoSum: exact for finite p, q)
+//   h = floor(c 2^20) <= 2^21, r = c 2^40 - h 2^20 (exact), l = floor(r) < 2^20
+//   for c = clamp(hi, 0, 2), and F = h 2^20 + l + e with
+//   e = floor(lo 2^40) when 0 < hi <= 2 and r == l (c 2^40 is an integer,
+//   so F = c 2^40 + floor(lo 2^40)); e <= 0 when hi == 2 (m above 2 clamps);
+//   e = 0 otherwise: hi <= 0 means m <= 0 (|lo| < |hi|), hi > 2 means m > 2,
+//   and for a non-integer c 2^40, |lo| 2^40 <= ulp(c 2^40) / 2 keeps it
+//   between the same integers.  |e| <= 2^17 (|lo| <= ulp(hi) / 2 <= 2^-23).
+// NaN masses count as 0 (fmaxf skips NaN), +inf as 2.
+__device__ __forceinline__ void add_entry(float pv, float qv, bool has_q, int& sh, int& sl) {
+  float hi = pv, e = 0.f;
+  if (has_q) {
+    hi = __fsub_rn(pv, qv);
+    const float bb = __fsub_rn(hi, pv);  // the part of hi that came from -q
+    const float lo = __fadd_rn(__fsub_rn(pv, __fsub_rn(hi, bb)), __fsub_rn(-qv, bb));
+    e = floorf(lo * kTwo40);
+    if (hi >= 2.f) e = fminf(e, 0.f);
+    if (!(hi > 0.f && hi <= 2.f)) e = 0.f;
+  }
+  const float c = fminf(fmaxf(hi, 0.f), 2.f);
+  const float h = floorf(c * kTwo20);
+  const float r = fmaf(h, -kTwo20, c * kTwo40);
+  const float l = floorf(r);
+  if (r != l) e = 0.f;
   sh += __float_as_int(h + kMagic) - kMagicBits;
-  sl += __float_as_int(l + kMagic) - kMagicBits;
+  sl += __float_as_int((l + e) + kMagic) - kMagicBits;  // l + e exact: |l + e| < 2^21
 }
-__device__ __forceinline__ uint64_t combine(int sh, int sl) { return ((uint64_t)(uint32_t)sh << 20) + (uint32_t)sl; }
+// (sl may be negative: l + e < 0 when l = 0 and lo < 0)
+__device__ __forceinline__ uint64_t combine(int sh, int sl) {
+  return (uint64_t)((int64_t)sh * (1 << 20) + (int64_t)sl);
+}
 
 // weight of entry x of the residual of (p, q) (q == nullptr: of p itself)
 __device__ __forceinline__ uint64_t weight(const float* p, const float* q, int64_t x) {
   int sh = 0, sl = 0;
-  add_fixed(mass_of(__ldg(p + x), q != nullptr ? __ldg(q + x) : 0.f, q != nullptr), sh, sl);
+  add_entry(__ldg(p + x), q != nullptr ? __ldg(q + x) : 0.f, q != nullptr, sh, sl);
   return combine(sh, sl);
 }
 
@@ -82,7 +105,7 @@ __device__ __forceinline__ int64_t cut(int64_t L0, int64_t n, int w, int parts =
 
 // sum of the weights of [lo, hi) by one warp.  A lane's 32-bit counters
 // take at most 2^9 entries between folds into its 64-bit sum (2^9 (2^21 +
-// 2^20) < 2^31).
+// 2^20 + 2^17) < 2^31).
 __device__ __forceinline__ uint64_t warp_sum(const float* p, const float* q, int64_t lo, int64_t hi, int lane,
                                              bool vec) {
   uint64_t s = 0;
@@ -97,10 +120,10 @@ __device__ __forceinline__ uint64_t warp_sum(const float* p, const float* q, int
       for (int64_t x0 = xb + 4 * lane; x0 < xe; x0 += 128) {
         const float4 a = __ldg(reinterpret_cast<const float4*>(p + x0));
         const float4 c = hq ? __ldg(reinterpret_cast<const float4*>(q + x0)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        add_fixed(mass_of(a.x, c.x, hq), sh, sl);
-        add_fixed(mass_of(a.y, c.y, hq), sh, sl);
-        add_fixed(mass_of(a.z, c.z, hq), sh, sl);
-        add_fixed(mass_of(a.w, c.w, hq), sh, sl);
+        add_entry(a.x, c.x, hq, sh, sl);
+        add_entry(a.y, c.y, hq, sh, sl);
+        add_entry(a.z, c.z, hq, sh, sl);
+        add_entry(a.w, c.w, hq, sh, sl);
       }
       s += combine(sh, sl);
     }
@@ -109,7 +132,7 @@ __device__ __forceinline__ uint64_t warp_sum(const float* p, const float* q, int
   {
     int sh = 0, sl = 0, n = 0;
     for (int64_t y = x + lane; y < hi; y += 32) {
-      add_fixed(mass_of(__ldg(p + y), hq ? __ldg(q + y) : 0.f, hq), sh, sl);
+      add_entry(__ldg(p + y), hq ? __ldg(q + y) : 0.f, hq, sh, sl);
       if (++n == 256) {
         s += combine(sh, sl);
         sh = sl = n = 0;

@@ -84,7 +84,8 @@ def weights(p_row, q_row=None) -> np.ndarray:
     if q_row is None:
         return fixed(p)
     q = np.asarray(q_row, dtype=np.float32).astype(np.float64)
-    w = fixed(p - q)
+    with np.errstate(invalid="ignore"):  # inf - inf is NaN, which F counts as 0
+        w = fixed(p - q)
     _, ep = np.frexp(p)
     _, eq = np.frexp(q)
     wide = np.isfinite(p) & np.isfinite(q) & (p != 0) & (q != 0) & (np.abs(ep - eq) > 28)

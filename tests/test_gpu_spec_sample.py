@@ -96,3 +96,48 @@ def test_strided_views():
     for a, b_ in ((n, tok), (n2, tok2)):
         np.testing.assert_array_equal(a.cpu().numpy(), on)
         np.testing.assert_array_equal(b_.cpu().numpy(), ot)
+
+
+def rounded_residual_token(p_row, q_row, s):
+    """The token a residual rounded to fp32 before F would give (a planted
+    mistake, used only to show that the rows below discriminate)."""
+    m = (np.asarray(p_row, np.float32) - np.asarray(q_row, np.float32)).astype(np.float64)
+    return ss.inverse_cdf(ss.fixed(m), s)
+
+
+def adversarial_rows(B, k, V, seed):
+    """Rows whose first candidate is rejected (its p is 0) and whose 32-bit
+    draw sits where the exact residual of eq. 33.12 and the fp32-rounded one
+    emit different tokens."""
+    rng = np.random.default_rng(seed)
+    p = rng.dirichlet(np.ones(V) * 0.5, size=(B, k + 1)).astype(np.float32)
+    q = rng.dirichlet(np.ones(V) * 0.5, size=(B, k)).astype(np.float32)
+    draft = rng.integers(0, V, size=(B, k)).astype(np.int32)
+    u = rng.random((B, k), dtype=np.float32)
+    s = np.zeros(B, dtype=np.uint64)
+    for b in range(B):
+        x = int(draft[b, 0])
+        p[b, 0, x] = 0.0
+        q[b, 0, x] = max(q[b, 0, x], np.float32(1e-3))
+        w = ss.weights(p[b, 0], q[b, 0])
+        wr = ss.fixed((p[b, 0] - q[b, 0]).astype(np.float64))
+        Z, Zr = int(w.sum()), int(wr.sum())
+        C, Cr = np.cumsum(w), np.cumsum(wr)
+        # first draw past each token boundary, exact and rounded
+        first = [-(-(int(c) << 32) // Z) for c in C[:-1]]
+        first_r = [-(-(int(c) << 32) // Zr) for c in Cr[:-1]]
+        cand = [min(a, c) for a, c in zip(first, first_r) if a != c and min(a, c) < 2**32]
+        assert cand, "no discriminating draw in this row"
+        s[b] = cand[int(rng.integers(len(cand)))]
+        assert ss.inverse_cdf(w, int(s[b])) != rounded_residual_token(p[b, 0], q[b, 0], int(s[b]))
+    return [torch.from_numpy(np.ascontiguousarray(a)) for a in (p, q, draft, u, s.astype(np.uint32).view(np.int32))]
+
+
+@pytest.mark.parametrize("B,k,V", [(32, 2, 5000), (8, 4, 128256)])
+def test_residual_is_drawn_from_the_exact_difference(B, k, V):
+    """Eq. 33.12's [p - q]_+ is the exact difference: on rows where rounding
+    it changes the token, the kernel emits the exact residual's token."""
+    n, tok, on, ot = run_both(*adversarial_rows(B, k, V, seed=V + k))
+    np.testing.assert_array_equal(n, on)
+    np.testing.assert_array_equal(tok, ot)
+    assert np.all(n == 0)
