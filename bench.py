@@ -58,20 +58,30 @@ def measured_peaks():
                 "source": "fallback"}
 
 
+def code_digest(sources):
+    """sha256 (first 16 hex digits) over the given C/CUDA sources with their
+    comments and blank space removed: a comment-only edit keeps the digest."""
+    import hashlib
+    import re
+    m = hashlib.sha256()
+    for src in sources:
+        with open(os.path.join(ROOT, src)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        m.update(" ".join(text.split()).encode())
+    return m.hexdigest()[:16]
+
+
 def measured_traffic(workload):
     """DRAM bytes per launch of the workload's main kernel from the committed
-    ncu capture (profiles/traffic.json), or None when the kernel's sources
+    ncu capture (profiles/traffic.json), or None when the kernel's code
     changed since that capture."""
-    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             entry = json.load(f)["workloads"][workload]
-        m = hashlib.sha256()
-        for src in entry["sources"]:
-            with open(os.path.join(ROOT, src), "rb") as f:
-                m.update(f.read())
-        if m.hexdigest()[:16] != entry["sources_sha256_16"]:
+        if code_digest(entry["sources"]) != entry["code_sha256_16"]:
             return None
         return entry["dram_bytes_per_launch"]
     except (OSError, KeyError, ValueError):
@@ -316,12 +326,13 @@ def roofline_entry(r: Runner, main_ms, peaks, flops=None):
     kv, total_bytes = algorithmic_bytes(s, r.cpu)
     if tensor_bound(s):
         achieved = flops / (main_ms * 1e-3) / 1e12
-        return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"], "traffic": measured_traffic(s.name),
-                "algorithmic_bytes": total_bytes, "peak_note": f"dense bf16 burst, {peaks['source']}"}
+        return {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": measured_traffic(s.name),
+                "algorithmic_flops": flops, "algorithmic_bytes": total_bytes,
+                "peak_note": f"dense bf16 burst, {peaks['source']}"}
     achieved = total_bytes / (main_ms * 1e-3) / 1e9
-    return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"], "traffic": measured_traffic(s.name),
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": measured_traffic(s.name),
             "algorithmic_bytes": total_bytes, "peak_note": f"HBM copy bandwidth, {peaks['source']}"}
 
 
@@ -348,11 +359,21 @@ def oracle_rate(s, inp, budget_s: float, threads: int = 0):
     return spent / done * total_rows, done, cores
 
 
+def line_config(s, inp, world):
+    """The `config` of the JSON line: the workload, its per-step work and how
+    L2 is kept out of the timing (the same dict on both arms)."""
+    kv, total_bytes = algorithmic_bytes(s, inp)
+    in_bytes = sum(t.numel() * t.element_size() for t in inp.values() if torch.is_tensor(t))
+    return {"workload": describe(s), "kv_bytes_per_step": kv, "algorithmic_bytes_per_step": total_bytes,
+            "l2": "flushed between steps" if in_bytes < 2 * L2_BYTES else f"inputs ({in_bytes / 1e6:.0f} MB) larger than L2",
+            "parallelism": f"weak: {world} rank(s), own batch each"}
+
+
 def run_reference(args, rank, world):
     """--impl reference: the fp64 CPU oracle on the host cores (rank 0 only)."""
     if rank != 0:
         return
-    s = workloads.spec(HEADLINE)
+    s = workloads.spec(args.workload)
     inp = workloads.generate(s)
     kv, _ = algorithmic_bytes(s, inp)
     budget = max(0.25, args.ref_budget_s / max(1, args.steps + args.warmup))
@@ -372,7 +393,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": describe(s), "l2": "n/a (CPU)"},
+        "config": line_config(s, inp, world),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"{rows_total} random query rows over {args.steps} steps, "
                                    f"scaled to all {s.B * s.Hq * s.Tq} rows"},
@@ -391,23 +412,35 @@ def measure_other(name, peaks):
     tot, mn, _ = time_steps(ro, steps_o, 3, 1, flush=in_bytes < 2 * L2_BYTES)
     t_ms = sum(tot) / len(tot)
     m_ms = sum(mn) / len(mn)
-    kvo, tb = algorithmic_bytes(ro.s, ro.cpu)
-    entry = {"workload": describe(ro.s), "us_per_call": t_ms * 1e3, "main_kernel_us": m_ms * 1e3,
-             "l2": "flushed between steps" if in_bytes < 2 * L2_BYTES else f"inputs ({in_bytes / 1e6:.0f} MB) larger than L2",
-             "kv_gbs": kvo / (t_ms * 1e-3) / 1e9, "plan": ro.plan,
-             "roofline": roofline_entry(ro, m_ms, peaks, causal_flops(ro.s, ro.cpu) if fl else None)}
-    if fl:
-        f = causal_flops(ro.s, ro.cpu)
-        entry["tflops"] = f / (t_ms * 1e-3) / 1e12
-        entry["frac_of_bf16_peak"] = entry["tflops"] / peaks["bf16_tflops"]
-        entry["frac_of_bf16_sustained"] = entry["tflops"] / peaks["bf16_tflops_sustained"]
-    else:
-        entry["frac_of_hbm_peak"] = (tb / (t_ms * 1e-3) / 1e9) / peaks["hbm_gbs"]
+    roof = roofline_entry(ro, m_ms, peaks, causal_flops(ro.s, ro.cpu) if fl else None)
     ro.free()
-    return entry
+    # whole call (us) against the roofline; the main kernel's own figures are in `roofline`
+    work = roof.get("algorithmic_flops", roof.get("algorithmic_bytes"))
+    per_s = work / (t_ms * 1e-3) / (1e12 if fl else 1e9)
+    return compact(name, t_ms * 1e3, per_s, roof, m_ms * 1e3)
 
 
-def measure_spec_sample(peaks, steps=10, warmup=3):
+# workloads that are BASELINE configurations (the others are "next" rows)
+CONFIG_OF = {"tiny_fp32": 1, "decode_gqa": 2, "long_decode": 3, "spec_verify": 4, "prefill": 5}
+
+
+def compact(name, us, achieved, roof, main_us=None):
+    """One short entry per workload: whole-call time and throughput, its
+    fraction of the roofline's peak, and DRAM traffic over algorithmic bytes
+    (from the committed ncu record; null when the kernel changed since)."""
+    e = {}
+    if name in CONFIG_OF:
+        e["config"] = CONFIG_OF[name]
+    e.update({"us": round(us, 2), "achieved": round(achieved, 1), "unit": roof["unit"],
+              "frac": round(achieved / roof["peak"], 4), "bound": roof["bound"]})
+    if main_us is not None:
+        e["main_us"] = round(main_us, 2)
+    t, ab = roof.get("traffic"), roof.get("algorithmic_bytes")
+    e["traffic_ratio"] = round(t / ab, 3) if (t and ab) else None
+    return e
+
+
+def measure_spec_sample(peaks, steps=10, warmup=3, full=False):
     """The speculative-sampling step (blkattn_spec_sample) on its full-size
     workload: device time per call with L2 cleared by a read of twice its size
     before each call (the rows a call reads fit in L2), and the bytes of the
@@ -443,15 +476,17 @@ def measure_spec_sample(peaks, steps=10, warmup=3):
             times.append(e0.elapsed_time(e1))
     t_ms = sum(times) / len(times)
     achieved = total / (t_ms * 1e-3) / 1e9
-    return {"workload": f"spec_sample: B={s.B} k={s.k} V={s.V} f32 probabilities",
-            "us_per_call": t_ms * 1e3, "l2": "evicted between steps by reading 2x its size",
-            "kept_candidates_histogram": np.bincount(n, minlength=s.k + 1).tolist(),
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved / peaks["hbm_gbs"], "traffic": measured_traffic("spec_sample"),
-                         "algorithmic_bytes": total, "peak_note": f"HBM copy bandwidth, {peaks['source']}"}}
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": measured_traffic("spec_sample"),
+            "algorithmic_bytes": total}
+    if full:
+        return {"workload": f"spec_sample: B={s.B} k={s.k} V={s.V} f32 probabilities",
+                "us_per_call": t_ms * 1e3, "l2": "evicted between steps by reading 2x its size",
+                "kept_candidates_histogram": np.bincount(n, minlength=s.k + 1).tolist(), "roofline": roof}
+    return compact("spec_sample", t_ms * 1e3, achieved, roof)
 
 
-def measure_backward(peaks, steps=5, warmup=3, name="prefill"):
+def measure_backward(peaks, steps=5, warmup=3, name="prefill", full=False):
     """The backward pass (blkattn_bwd: row facts, dQ, dK/dV) on the causal
     prefill workload with an upstream gradient; inputs come from the
     library's own forward.  Algorithmic work: the five products of eqs.
@@ -483,14 +518,18 @@ def measure_backward(peaks, steps=5, warmup=3, name="prefill"):
     t_ms = sum(times) / len(times)
     flops = causal_flops(s, cpu) * 2.5
     achieved = flops / (t_ms * 1e-3) / 1e12
-    return {"workload": f"{name}_backward: {describe(s)}" + (f" window={W}" if W else "") + " + g_o bf16; dq, dk, dv f32",
-            "us_per_call": t_ms * 1e3, "l2": f"inputs ({in_bytes / 1e6:.0f} MB) larger than L2",
-            "kernels": "row facts, dQ (3 products per tile pair), dK/dV (4 products per tile pair)",
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": achieved / peaks["bf16_tflops"], "traffic": measured_traffic(f"{name}_backward"),
-                         "algorithmic_flops": flops,
-                         "peak_note": f"dense bf16 burst, {peaks['source']}"},
-            "frac_of_bf16_sustained": achieved / peaks["bf16_tflops_sustained"]}
+    # bytes every call must move at least once: q, k, v, g_o, o, lse in; dq, dk, dv out
+    moved = sum(t.numel() * t.element_size() for t in (dev["q"], dev["k"], dev["v"], dev["go"], out, lse, dq, dk, dv))
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16_tflops"], "traffic": measured_traffic(f"{name}_backward"),
+            "algorithmic_flops": flops, "algorithmic_bytes": moved}
+    if full:
+        return {"workload": f"{name}_backward: {describe(s)}" + (f" window={W}" if W else "") +
+                            " + g_o bf16; dq, dk, dv f32",
+                "us_per_call": t_ms * 1e3, "l2": f"inputs ({in_bytes / 1e6:.0f} MB) larger than L2",
+                "kernels": "row facts, dQ (3 products per tile pair), dK/dV (4 products per tile pair)",
+                "roofline": roof, "frac_of_bf16_sustained": achieved / peaks["bf16_tflops_sustained"]}
+    return compact(f"{name}_backward", t_ms * 1e3, achieved, roof)
 
 
 def main():
@@ -525,15 +564,15 @@ def main():
         from exact_blocked_attention_gb300 import blkattn
         blkattn.load()
         if rank == 0:
-            print(json.dumps(measure_spec_sample(peaks, steps=args.steps, warmup=args.warmup)), flush=True)
+            print(json.dumps(measure_spec_sample(peaks, steps=args.steps, warmup=args.warmup, full=True)), flush=True)
         return
     if args.only_backward:
         from exact_blocked_attention_gb300 import blkattn
         blkattn.load()
         if rank == 0:
-            print(json.dumps(measure_backward(peaks, steps=args.steps, warmup=args.warmup)), flush=True)
-            print(json.dumps(measure_backward(peaks, steps=args.steps, warmup=args.warmup, name="window_prefill")),
-                  flush=True)
+            print(json.dumps(measure_backward(peaks, steps=args.steps, warmup=args.warmup, full=True)), flush=True)
+            print(json.dumps(measure_backward(peaks, steps=args.steps, warmup=args.warmup, name="window_prefill",
+                                              full=True)), flush=True)
         return
 
     # ---- headline workload: every rank runs its own batch (weak scaling) ----
@@ -568,44 +607,17 @@ def main():
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": s.dtype,
         "data": "synthetic",
-        "config": {"workload": describe(s), "kv_bytes_per_step": kv, "algorithmic_bytes_per_step": total_bytes,
-                   "l2": "flushed between steps" if flush else f"inputs ({in_bytes / 1e6:.0f} MB) larger than L2",
-                   "plan": plan, "parallelism": f"weak: {world} rank(s), own batch each",
-                   "enqueue": "timed steps queued behind a 5 ms device sleep (host launch gaps untimed)"},
-        "us_per_call": step_ms * 1e3,
-        "step_ms_spread": spread,
-        "main_kernel_us": main_avg * 1e3,
-        "frac_of_hbm_peak": (total_bytes / (step_ms * 1e-3) / 1e9) / peaks["hbm_gbs"],
+        "config": line_config(s, cpu_inp, world),
+        "plan": {k: plan[k] for k in ("kernel", "rows_per_cta", "n_splits", "ctas", "workspace_bytes")},
+        "us_per_call": round(step_ms * 1e3, 2),
+        "step_us_spread": [round(min(total) * 1e3, 2), round(spread["median"] * 1e3, 2), round(max(total) * 1e3, 2)],
+        "main_kernel_us": round(main_avg * 1e3, 2),
+        "frac_of_hbm_peak": round((total_bytes / (step_ms * 1e-3) / 1e9) / peaks["hbm_gbs"], 4),
         "roofline": roof,
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clocks,
-        "wall_s_timed": wall,
     }
-
-    # ---- the other workloads (rank 0 only), each with its own roofline ----
-    if rank == 0 and not args.no_others:
-        others = {}
-        for name in workloads.SPECS:
-            if name == s.name:
-                continue
-            try:
-                others[name] = measure_other(name, peaks)
-            except Exception as exc:  # report, keep the headline line
-                others[name] = {"error": f"{type(exc).__name__}: {exc}"}
-            torch.cuda.empty_cache()
-        for bname in ("prefill", "window_prefill"):
-            try:
-                others[f"{bname}_backward"] = measure_backward(peaks, name=bname)
-            except Exception as exc:  # reported, not fatal
-                others[f"{bname}_backward"] = {"error": f"{type(exc).__name__}: {exc}"}
-            torch.cuda.empty_cache()
-        try:
-            others["spec_sample"] = measure_spec_sample(peaks)
-        except Exception as exc:  # reported, not fatal
-            others["spec_sample"] = {"error": f"{type(exc).__name__}: {exc}"}
-        line["workloads"] = others
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1 only) ----
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -613,6 +625,27 @@ def main():
         line["cpu_baseline"] = {"value": kv / sec / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
                                 "sample": f"{rows} random query rows of the same batch, fp64, "
                                           f"scaled to all {s.B * s.Hq * s.Tq} rows"}
+    # ---- the other workloads (rank 0 only), each with its own roofline ----
+    if rank == 0 and not args.no_others:
+        # (the configurations last: the end of the line is what a short log tail shows)
+        order = ["tree_verify", "window_decode", "window_prefill", "prefill_backward", "window_prefill_backward",
+                 "spec_sample", "tiny_fp32", "long_decode", "spec_verify", "prefill", "decode_gqa"]
+        others = {}
+        for name in order:
+            if name == s.name:
+                continue
+            try:
+                if name.endswith("_backward"):
+                    others[name] = measure_backward(peaks, name=name[: -len("_backward")])
+                elif name == "spec_sample":
+                    others[name] = measure_spec_sample(peaks)
+                else:
+                    others[name] = measure_other(name, peaks)
+            except Exception as exc:  # report, keep the headline line
+                others[name] = {"error": f"{type(exc).__name__}: {exc}"}
+            torch.cuda.empty_cache()
+        line["workloads"] = others
+
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
