@@ -31,12 +31,13 @@ _DTYPES = {torch.bfloat16: BF16, torch.float32: F32, torch.int32: I32, torch.int
 EXPORTED = ("blkattn_fwd", "blkattn_merge", "blkattn_status_string",
             "blkattn_check_device_error", "blkattn_debug_plan", "blkattn_debug_set_split_event",
             "blkattn_fwd_static_scratch", "blkattn_last_cuda_error", "blkattn_fwd_tree",
-            "blkattn_spec_sample", "blkattn_fwd_window", "blkattn_bwd", "blkattn_bwd_window")
+            "blkattn_spec_sample", "blkattn_fwd_window", "blkattn_bwd", "blkattn_bwd_window",
+            "blkattn_debug_stall_next_decode")
 
 
 class Tensor(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
-                ("sizes", ctypes.c_int64 * 4), ("strides", ctypes.c_int64 * 4)]
+                ("sizes", ctypes.c_int64 * 4), ("strides", ctypes.c_int64 * 4), ("device", ctypes.c_int32)]
 
 
 class States(ctypes.Structure):
@@ -95,6 +96,8 @@ def load(path: str = LIB_PATH):
             lib.blkattn_check_device_error.argtypes = [P]
             lib.blkattn_debug_plan.restype = ctypes.c_int
             lib.blkattn_debug_plan.argtypes = [ctypes.c_int64] * 6 + [ctypes.c_int32, ctypes.c_int32, P]
+            lib.blkattn_debug_stall_next_decode.restype = None
+            lib.blkattn_debug_stall_next_decode.argtypes = [ctypes.c_int32]
             lib.blkattn_debug_set_split_event.restype = None
             lib.blkattn_debug_set_split_event.argtypes = [P]
             lib.blkattn_last_cuda_error.restype = ctypes.c_char_p
@@ -130,6 +133,7 @@ def describe(t: torch.Tensor | None) -> Tensor | None:
     d.data = t.data_ptr() if t.numel() > 0 else None
     d.dtype = _DTYPES[t.dtype]
     d.ndim = t.dim()
+    d.device = t.device.index if t.is_cuda else -1  # host memory: refused by the library
     for i, (s, st) in enumerate(zip(t.shape, t.stride())):
         d.sizes[i] = s
         d.strides[i] = st
@@ -274,6 +278,13 @@ def merge(a, b, out, stream=None):
 def check_device_error(stream=None) -> int:
     """Synchronise and read/clear the device error word (test hook)."""
     return int(load().blkattn_check_device_error(_stream_handle(stream)))
+
+
+def stall_next_decode(cta: int) -> None:
+    """Test hook: the next tcgen05 decode launch stops CTA ``cta`` (mod the
+    CTA count) at a wait nothing completes; its bounded waits run out and
+    check_device_error() then reports ERR_DEVICE_TIMEOUT."""
+    load().blkattn_debug_stall_next_decode(int(cta))
 
 
 def set_split_event(event) -> None:

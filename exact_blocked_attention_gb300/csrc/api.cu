@@ -10,6 +10,7 @@
 
 #include <cstdlib>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include "blkattn.h"
@@ -40,6 +41,7 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 cudaEvent_t g_split_event = nullptr;  // measurement hook (blkattn_debug_set_split_event)
+int g_stall_next = -1;                // test hook (blkattn_debug_stall_next_decode)
 
 // The CUDA error behind the last BLKATTN_ERR_CUDA (blkattn_last_cuda_error).
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
@@ -57,6 +59,22 @@ bool dims_ok(const blkattn_tensor* t, int ndim) {
   for (int i = 0; i < ndim; ++i)
     if (t->sizes[i] < 0 || t->strides[i] < 0) return false;
   return true;
+}
+
+// Every tensor given (NULL entries skipped) names the same device ordinal
+// as `first`, and that ordinal is a device (not host memory).
+bool same_device(const blkattn_tensor* first, std::initializer_list<const blkattn_tensor*> ts) {
+  if (first->device < 0) return false;
+  for (const blkattn_tensor* t : ts)
+    if (t != nullptr && t->device != first->device) return false;
+  return true;
+}
+
+// The call's device must be the current one (the library never switches it).
+int check_current_device(int32_t device) {
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return cuda_fail(e);
+  return dev == device ? BLKATTN_OK : BLKATTN_ERR_INVALID_ARG;
 }
 
 
@@ -297,49 +315,57 @@ bool out_tma_ok(const blkattn_tensor* out) {
   return true;
 }
 
-// Grow-only per-device scratch.  Growing while the stream is being captured
-// is refused (a capture may not allocate).
-int ensure_workspace(DeviceState* s, size_t bytes, cudaStream_t stream) {
-  if (bytes <= s->ws_bytes) return BLKATTN_OK;
+// Grow-only per-device scratch, grown stream-ordered on the call's stream:
+// the old buffer is released after the work already queued there
+// (cudaFreeAsync) and the new one is allocated from the device's memory pool
+// in stream order (cudaMallocAsync), so no call synchronises the device.
+// Work on other streams that used the old buffer must be ordered before this
+// call by the caller (calls on different streams must not overlap).  Growing
+// while the stream is being captured is refused (a capture may not allocate).
+int grow_stream_ordered(void** buf, size_t* have, size_t bytes, cudaStream_t stream) {
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   if (cudaError_t e = cudaStreamIsCapturing(stream, &cs); e != cudaSuccess) return cuda_fail(e);
   if (cs != cudaStreamCaptureStatusNone) return BLKATTN_ERR_NO_WORKSPACE;
-  if (s->ws) {
-    if (cudaError_t e = cudaFree(s->ws); e != cudaSuccess) return cuda_fail(e);  // waits for users of the old one
-    s->ws = nullptr;
-    s->ws_bytes = 0;
+  if (*buf) {
+    if (cudaError_t e = cudaFreeAsync(*buf, stream); e != cudaSuccess) return cuda_fail(e);
+    *buf = nullptr;
+    *have = 0;
   }
-  if (cudaError_t e = cudaMalloc(&s->ws, bytes); e != cudaSuccess) {
-    s->ws = nullptr;
+  if (cudaError_t e = cudaMallocAsync(buf, bytes, stream); e != cudaSuccess) {
+    *buf = nullptr;
     return cuda_fail(e);
   }
-  s->ws_bytes = bytes;
+  *have = bytes;
   return BLKATTN_OK;
 }
 
-// Grow-only per-device counters (zeroed on allocation, on the call's stream;
-// the kernel leaves them zero).  Growing while the stream is being captured
-// is refused.
+int ensure_workspace(DeviceState* s, size_t bytes, cudaStream_t stream) {
+  if (bytes <= s->ws_bytes) return BLKATTN_OK;
+  return grow_stream_ordered(&s->ws, &s->ws_bytes, bytes, stream);
+}
+
+// Grow-only per-device counters, zeroed on the call's stream when they grow
+// (the kernel leaves them zero).
 int ensure_counters(DeviceState* s, int64_t n, cudaStream_t stream) {
   if ((size_t)n <= s->cnt_n) return BLKATTN_OK;
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaError_t e = cudaStreamIsCapturing(stream, &cs); e != cudaSuccess) return cuda_fail(e);
-  if (cs != cudaStreamCaptureStatusNone) return BLKATTN_ERR_NO_WORKSPACE;
-  if (s->cnt) {
-    if (cudaError_t e = cudaFree(s->cnt); e != cudaSuccess) return cuda_fail(e);
+  void* buf = s->cnt;
+  size_t bytes = s->cnt_n * sizeof(unsigned);
+  const int st = grow_stream_ordered(&buf, &bytes, (size_t)n * sizeof(unsigned), stream);
+  s->cnt = static_cast<unsigned*>(buf);
+  s->cnt_n = bytes / sizeof(unsigned);
+  if (st != BLKATTN_OK) return st;
+  if (cudaError_t e = cudaMemsetAsync(s->cnt, 0, (size_t)n * sizeof(unsigned), stream); e != cudaSuccess) {
+    // the counters cannot be trusted: drop them so the next call reallocates
+    cudaFreeAsync(s->cnt, stream);
     s->cnt = nullptr;
     s->cnt_n = 0;
-  }
-  if (cudaError_t e = cudaMalloc(&s->cnt, (size_t)n * sizeof(unsigned)); e != cudaSuccess) {
-    s->cnt = nullptr;
     return cuda_fail(e);
   }
-  if (cudaError_t e = cudaMemsetAsync(s->cnt, 0, (size_t)n * sizeof(unsigned), stream); e != cudaSuccess) return cuda_fail(e);
-  s->cnt_n = (size_t)n;
   return BLKATTN_OK;
 }
 
 struct Checked {
+  int32_t device;  // the ordinal every tensor of the call names
   int64_t B, Hq, Hkv, Tq, Tmax, d;
   int64_t window = 0;  // sliding window (0: none)
   Elt elt;
@@ -361,6 +387,8 @@ int validate_fwd(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn
   if (sl->dtype != BLKATTN_I32 || qp->dtype != BLKATTN_I32) return BLKATTN_ERR_INVALID_ARG;
   if (!is_float_dtype(out->dtype) || lse->dtype != BLKATTN_F32) return BLKATTN_ERR_INVALID_ARG;
   if (bias && bias->dtype != BLKATTN_F32) return BLKATTN_ERR_INVALID_ARG;
+  if (!same_device(q, {k, v, sl, qp, tree, bias, out, lse})) return BLKATTN_ERR_INVALID_ARG;
+  c->device = q->device;
 
   c->B = q->sizes[0];
   c->Hq = q->sizes[1];
@@ -477,6 +505,7 @@ FwdParams fill_params(const blkattn_tensor* q, const blkattn_tensor* k, const bl
     p.ws_u = reinterpret_cast<float*>(base + 2 * ((n * 4 + 255) / 256) * 256);
   }
   p.err = err;
+  p.test_stall_cta = -1;
   // prefill dispatch groups: (sequence, head) pairs whose K and V take about
   // half of the L2 cache together (129 MB on GB300; queried once per device)
   {
@@ -512,7 +541,12 @@ int launch_fwd(const FwdParams& p, const Checked& c, const Plan& pl, const blkat
     if (st != BLKATTN_OK) return st;
     st = kv_tensor_map(dev, v, 128, &mv);
     if (st != BLKATTN_OK) return st;
-    le = blkattn::launch_decode_tc(p, (int)pl.ctas, *mk, *mv, stream);
+    FwdParams pt = p;
+    if (g_stall_next >= 0) {  // test hook: one launch only
+      pt.test_stall_cta = (int)(g_stall_next % pl.ctas);
+      g_stall_next = -1;
+    }
+    le = blkattn::launch_decode_tc(pt, (int)pl.ctas, *mk, *mv, stream);
   } else if (pl.cfg.kernel == blkattn::Kernel::TensorCore || pl.cfg.kernel == blkattn::Kernel::Prefill) {
     int dev = 0;
     if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return cuda_fail(e);
@@ -576,6 +610,7 @@ int fwd_with_scratch(const blkattn_tensor* q, const blkattn_tensor* k, const blk
   int st = validate_fwd(q, k, v, seqlens_k, q_logical_pos, tree, mask_bias, out, lse, &c);
   if (st != BLKATTN_OK) return st;
   if (c.B == 0 || c.Tq == 0) return BLKATTN_OK;
+  if ((st = check_current_device(c.device)) != BLKATTN_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* ds = nullptr;
@@ -610,6 +645,7 @@ int fwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_ten
   if (window < 0 || window > 0x7fffffff || (window > 0 && tree != nullptr)) return BLKATTN_ERR_INVALID_ARG;
   c.window = window;  // (the prefill kernel takes windows too: a first key tile per CTA and a window mask)
   if (c.B == 0 || c.Tq == 0) return BLKATTN_OK;
+  if ((st = check_current_device(c.device)) != BLKATTN_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
   std::lock_guard<std::mutex> lock(g_mu);
@@ -677,6 +713,7 @@ int bwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_ten
   }
   if (dout->dtype != q->dtype || dq->dtype != BLKATTN_F32 || dk->dtype != BLKATTN_F32 || dv->dtype != BLKATTN_F32)
     return BLKATTN_ERR_INVALID_ARG;
+  if (!same_device(q, {dout, dq, dk, dv})) return BLKATTN_ERR_INVALID_ARG;
   if (!(scale == scale) || scale == __builtin_huge_valf() || scale == -__builtin_huge_valf())
     return BLKATTN_ERR_INVALID_ARG;
   if (c.B == 0) return BLKATTN_OK;
@@ -688,6 +725,7 @@ int bwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_ten
   // rows, at most 1024 query tiles of 128 rows per sequence
   if (c.elt != Elt::BF16 || c.d != 128 || c.Tq > 131072) return BLKATTN_ERR_UNSUPPORTED;
   if (rows && (!tma_rows_ok(q) || !tma_rows_ok(dout))) return BLKATTN_ERR_INVALID_ARG;
+  if ((st = check_current_device(c.device)) != BLKATTN_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
   std::lock_guard<std::mutex> lock(g_mu);
@@ -865,6 +903,11 @@ int blkattn_merge(const blkattn_states* a, const blkattn_states* b, const blkatt
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (cudaError_t e = blkattn::launch_state_merge(p, stream); e != cudaSuccess) return cuda_fail(e);
   return BLKATTN_OK;
+}
+
+void blkattn_debug_stall_next_decode(int32_t cta) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_stall_next = cta < 0 ? -1 : cta;
 }
 
 void blkattn_debug_set_split_event(void* ev) {

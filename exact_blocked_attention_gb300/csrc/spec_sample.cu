@@ -337,11 +337,20 @@ extern "C" int blkattn_spec_sample(const blkattn_tensor* p, const blkattn_tensor
     return BLKATTN_ERR_INVALID_ARG;
   // vocabulary contiguous (an empty q, or a vocabulary of one, has no such stride)
   if ((V > 1 && p->strides[2] != 1) || (k > 0 && V > 1 && q->strides[2] != 1)) return BLKATTN_ERR_INVALID_ARG;
+  // one device, the current one
+  for (const blkattn_tensor* t : {q, draft, u_accept, u_sample, n_accepted, token})
+    if (t->device != p->device) return BLKATTN_ERR_INVALID_ARG;
+  if (p->device < 0) return BLKATTN_ERR_INVALID_ARG;
   if (B == 0) return BLKATTN_OK;
   if (B > 0x3fffffff || k > 0x7fffffff || V > 0x7fffffff) return BLKATTN_ERR_UNSUPPORTED;  // grid: two CTAs a row
   for (const blkattn_tensor* t : {p, q, draft, u_accept, u_sample, n_accepted, token})
     if (t->data == nullptr && !(t == q && k == 0) && !(t == draft && k == 0) && !(t == u_accept && k == 0))
       return BLKATTN_ERR_INVALID_ARG;
+  {
+    int dev = 0;
+    if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return blkattn::report_cuda_failure(e);
+    if (dev != p->device) return BLKATTN_ERR_INVALID_ARG;
+  }
   blkattn::spec_sample_kernel<<<(unsigned)(B * blkattn::kCluster), blkattn::kThreads, 0,
                                  reinterpret_cast<cudaStream_t>(stream)>>>(
       static_cast<const float*>(p->data), p->strides[0], p->strides[1], static_cast<const float*>(q->data),

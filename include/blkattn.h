@@ -69,7 +69,15 @@ enum {
 
 /*
  * A strided view.  sizes/strides are in ELEMENTS; a stride of 0 broadcasts.
- * Only the first ndim entries are read.
+ * Only the first ndim entries are read.  `device` is the CUDA device ordinal
+ * of the memory `data` points to.  Every tensor of one call must name the
+ * same device and that device must be current when the call is made;
+ * otherwise the call returns BLKATTN_ERR_INVALID_ARG ("Generation and
+ * Caching with the Same Model", the cache-reuse forward: cached K/V and the
+ * new tokens must be on one device; Chapter 33 §33.3, interface, backend
+ * and correctness conditions: the backend follows the device).  A negative
+ * ordinal (host memory) is refused the same way.  The library never switches
+ * the current device.
  */
 typedef struct {
   void* data;
@@ -77,6 +85,7 @@ typedef struct {
   int32_t ndim;
   int64_t sizes[4];
   int64_t strides[4];
+  int32_t device;     /* CUDA device ordinal holding `data` */
 } blkattn_tensor;
 
 /*
@@ -105,9 +114,12 @@ typedef struct {
  * Returns BLKATTN_OK after enqueuing the work (asynchronous), or a negative
  * status without enqueuing anything.  Library-owned scratch (per-split
  * partial states, and per-unit counters that every call leaves at zero)
- * comes from per-device, grow-only buffers, allocated (counters zeroed on
- * the stream) before the first call that needs them; calls on different
- * streams of one device must not overlap in time.
+ * comes from per-device, grow-only buffers.  They grow stream-ordered on the
+ * call's stream (cudaFreeAsync of the old buffer, cudaMallocAsync of the
+ * new one, counters zeroed by cudaMemsetAsync), so a call never synchronises
+ * the device; growth during stream capture is refused with
+ * BLKATTN_ERR_NO_WORKSPACE.  Calls on different streams of one device must
+ * not overlap in time (they share the buffers): order them with events.
  */
 int blkattn_fwd(const blkattn_tensor* q, const blkattn_tensor* k,
                 const blkattn_tensor* v, const blkattn_tensor* seqlens_k,
@@ -187,9 +199,10 @@ int blkattn_fwd_window(const blkattn_tensor* q, const blkattn_tensor* k,
  * Candidate x_i is kept iff u_i * q_i(x_i) < p_i(x_i) (computed in fp64,
  * exact for fp32 operands), in order, up to the first rejection; then the
  * token is drawn from the residual [p_i - q_i]_+ of that position, or from
- * p_{k+1} when all are kept, by inverse CDF in fixed point (mass p - q in
- * fp32, or p, clamped to [0, 2]; weight floor(mass * 2^40); integer prefix
- * sums; threshold floor(s * Z / 2^32); the smallest token whose prefix sum
+ * p_{k+1} when all are kept, by inverse CDF in fixed point (mass: the exact
+ * difference p - q of the fp32 values, as eq. 33.12 writes it, or p,
+ * clamped to [0, 2]; weight floor(mass * 2^40); integer prefix sums;
+ * threshold floor(s * Z / 2^32); the smallest token whose prefix sum
  * exceeds it).  A rejection meeting a zero
  * residual keeps the candidate; a candidate outside [0, V) or with q = 0 is
  * rejected (its position having no residual mass, the token is drawn from
@@ -197,7 +210,8 @@ int blkattn_fwd_window(const blkattn_tensor* q, const blkattn_tensor* k,
  * k = 0 is allowed (q, draft, u_accept may then be empty).  The caller owns
  * every buffer; the call enqueues one kernel on the stream and never reads
  * device data on the host.  Returns BLKATTN_OK, BLKATTN_ERR_INVALID_ARG
- * (shapes, dtypes, strides, NULL data) or BLKATTN_ERR_CUDA (launch).
+ * (shapes, dtypes, strides, NULL data, tensors on another device than the
+ * current one) or BLKATTN_ERR_CUDA (launch).
  */
 int blkattn_spec_sample(const blkattn_tensor* p, const blkattn_tensor* q,
                         const blkattn_tensor* draft, const blkattn_tensor* u_accept,
@@ -379,6 +393,23 @@ int blkattn_debug_plan(int64_t B, int64_t H_q, int64_t H_kv, int64_t T_q,
  * switches it off.  Process-wide; not for concurrent callers.
  */
 void blkattn_debug_set_split_event(void* ev);
+
+/*
+ * Test hook of the bounded waits (no counterpart on the pages; it exercises
+ * the rule of Chapter 33 §33.2 that undefined values must not propagate, here
+ * for a kernel that cannot finish).  After this call, the NEXT launch of the
+ * tcgen05 decode kernel (a blkattn_fwd call that blkattn_debug_plan reports
+ * as kernel 3) makes the MMA-issuing thread of CTA (cta mod the launch's CTA
+ * count) wait on a barrier that nothing completes.  That wait gives up after
+ * 1 ms; the thread then issues no product, and the CTA's other roles give up
+ * their own bounded waits (2 s each), let the copies they issued land, free
+ * tensor memory and return.  The call's output is undefined;
+ * blkattn_check_device_error then reports BLKATTN_ERR_DEVICE_TIMEOUT and
+ * resets the per-unit counters the stopped CTA left behind, so the next call
+ * is correct.  No fault and no unbounded wait is involved.  cta < 0 cancels a
+ * pending request.  Process-wide; not for concurrent callers.
+ */
+void blkattn_debug_stall_next_decode(int32_t cta);
 
 #ifdef __cplusplus
 }

@@ -44,7 +44,8 @@ def test_status_strings(lib):
 class FakeTensor:
     """Descriptor with a fake (never dereferenced) device address."""
 
-    def __init__(self, shape, dtype, strides=None, addr=0x10000):
+    def __init__(self, shape, dtype, strides=None, addr=0x10000, device=0):
+        self.device = device
         self.shape = tuple(shape)
         self.dtype = dtype
         if strides is None:
@@ -60,6 +61,7 @@ class FakeTensor:
         d.data = self.addr
         d.dtype = {torch.bfloat16: 1, torch.float32: 2, torch.int32: 3, torch.int64: 4}[self.dtype]
         d.ndim = len(self.shape)
+        d.device = self.device
         for i, (s, st) in enumerate(zip(self.shape, self.strides)):
             d.sizes[i] = s
             d.strides[i] = st
@@ -101,9 +103,15 @@ def good_args(B=2, Hq=8, Hkv=2, Tq=3, Tmax=100, d=128, dt=torch.bfloat16):
     (lambda a: a.update(q=FakeTensor((2, 8, 3, 128), torch.bfloat16, addr=0)), -1),  # NULL data
     (lambda a: a.update(**good_args(d=96)), -2),  # head dim without a kernel
     (lambda a: a.update(q=None), -1),
+    (lambda a: a.update(k=FakeTensor((2, 2, 100, 128), torch.bfloat16, device=1)), -1),  # device mismatch
+    (lambda a: a.update(lse=FakeTensor((2, 8, 3), torch.float32, device=3)), -1),
+    (lambda a: a.update(bias=FakeTensor((2, 8, 3, 100), torch.float32, device=1)), -1),
+    (lambda a: a.update(**{n: FakeTensor(t.shape, t.dtype, t.strides, device=-1)
+                           for n, t in good_args().items() if t is not None}), -1),  # host memory
 ], ids=["q-int", "mixed-dtype", "hq-not-multiple", "v-len", "qpos-shape", "seqlens-shape",
         "seqlens-dtype", "lse-dtype", "out-dim", "k-inner-stride", "k-row-misaligned",
-        "k-base-misaligned", "bias-shape", "bias-heads", "bias-dtype", "null-data", "d96", "missing-q"])
+        "k-base-misaligned", "bias-shape", "bias-heads", "bias-dtype", "null-data", "d96", "missing-q",
+        "k-other-device", "lse-other-device", "bias-other-device", "host-memory"])
 def test_invalid_requests_are_rejected_before_cuda(lib, mutate, expect):
     a = good_args()
     mutate(a)
@@ -201,8 +209,10 @@ def call_bwd(lib, a, scale=0.1):
     (lambda a: a.update(**bwd_args(d=64)), -2),                                     # d = 64: no backward kernel
     (lambda a: a.update(**bwd_args(dt=torch.float32)), -2),                         # f32: no backward kernel
     (lambda a: a.update(**bwd_args(B=1, Tq=131073)), -2),                           # > 1024 query tiles
+    (lambda a: a.update(dk=FakeTensor((2, 2, 100, 128), torch.float32, device=1)), -1),   # device mismatch
+    (lambda a: a.update(dout=FakeTensor((2, 8, 3, 128), torch.bfloat16, device=2)), -1),
 ], ids=["dout-dtype", "dout-shape", "dq-dtype", "dk-shape", "dv-heads", "dq-misaligned", "dk-row-stride",
-        "q-row-stride", "missing-dout", "d64", "f32", "too-many-rows"])
+        "q-row-stride", "missing-dout", "d64", "f32", "too-many-rows", "dk-other-device", "dout-other-device"])
 def test_backward_requests_are_validated_before_cuda(lib, mutate, expect):
     a = bwd_args()
     mutate(a)
@@ -257,8 +267,10 @@ def good_spec(B=4, k=3, V=1000):
     lambda a: a.update(p=FakeTensor((4, 4, 1000), torch.float32, strides=(8000, 2000, 2))),  # vocab stride
     lambda a: a.update(p=FakeTensor((4, 4, 1000), torch.float32, addr=0)),
     lambda a: a.update(p=None),
+    lambda a: a.update(tok=FakeTensor((4,), torch.int32, device=1)),                   # device mismatch
+    lambda a: a.update(**{n: FakeTensor(t.shape, t.dtype, t.strides, device=-1) for n, t in good_spec().items()}),
 ], ids=["p-dtype", "k-mismatch", "vocab", "draft-dtype", "uacc-shape", "usmp-shape", "tok-dtype",
-        "vocab-stride", "null-p", "missing-p"])
+        "vocab-stride", "null-p", "missing-p", "tok-other-device", "host-memory"])
 def test_spec_sample_rejects_bad_requests(lib, mutate):
     a = good_spec()
     mutate(a)
