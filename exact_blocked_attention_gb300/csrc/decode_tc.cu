@@ -663,7 +663,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         cq.next(ntab, RG, Hkv, B);
         return true;
       };
-      bool ok = !(cq.t < t1) || issue_qk(0);
+      // (test hook: `drain` has no arrival before the thread's own commit
+      // below, so this wait runs out)
+      bool ok = blockIdx.x != (unsigned)p.test_stall_cta || mbar_wait_ns(drain, 0, 1000000ull);
+      ok = ok && (!(cq.t < t1) || issue_qk(0));
       for (int64_t g = 0; ok && cur.t < t1; cur.next(ntab, RG, Hkv, B), ++g) {
         const bool first = cur.t == t0 || cur.j == 0;
         const bool last = cur.t == t1 - 1 || cur.j == cur.n - 1;

@@ -68,6 +68,11 @@ struct FwdParams {
   // prefill: 1 when the output tensor map (fp32, boxes {32, 32}, 128-byte
   // swizzle) is valid and the kernel stores whole output tiles with TMA
   int o_tma;
+  // test hook of the tcgen05 decode kernel (-1: none): the MMA-issuing thread
+  // of this CTA waits on a barrier nothing completes, gives up after 1 ms
+  // and issues no product, so the CTA's other roles run out their bounded
+  // waits (blkattn_debug_stall_next_decode)
+  int test_stall_cta;
 };
 
 // Split-KV kernel configuration chosen by the planner.
