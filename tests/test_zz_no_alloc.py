@@ -20,6 +20,8 @@ from exact_blocked_attention_gb300 import build as libbuild
 pytestmark = pytest.mark.gpu
 
 TOL_O, TOL_L = 2e-3, 1e-3  # the bf16 parity tolerances of the other GPU tests
+# the array's last 256 KiB hold the per-unit counters; plans get the rest
+PLAN_BYTES = blkattn.STATIC_SCRATCH_BYTES - 256 * 1024
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -40,7 +42,7 @@ def both_paths(s, g):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     plan = blkattn.debug_plan(s.B, s.Hq, s.Hkv, s.Tq, s.Tmax, s.d, torch.bfloat16, sms)
     assert plan["n_splits"] > 1, "the case must use the split scratch"
-    assert 0 < plan["workspace_bytes"] <= blkattn.STATIC_SCRATCH_BYTES
+    assert 0 < plan["workspace_bytes"] <= PLAN_BYTES
     ref_o, ref_l = blkattn.attention(g["q"], g["k"], g["v"], g["seqlens"], g["qpos"], g["bias"], g["scale"])
     out = torch.full_like(ref_o, float("nan"))
     lse = torch.full_like(ref_l, float("nan"))
@@ -97,3 +99,32 @@ def test_static_scratch_refuses_problems_beyond_its_size():
     blkattn.fwd(q, k, v, sl, qp, None, d ** -0.5, out, lse)
     torch.cuda.synchronize()
     assert torch.isfinite(out).all()
+
+
+def test_static_scratch_refuses_plans_in_the_counter_region():
+    """A plan larger than the 15.75 MiB the split states may use, though not
+    larger than the whole 16 MiB array, is refused too (the last 256 KiB hold
+    the unit counters).  (The 65536-unit counter limit is never the binding
+    one: that many units need more than 16 MiB of split states.)"""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    Hq, Hkv, Tq, d, Tmax = 32, 8, 1, 128, 256
+    for B in range(1, 1025):
+        plan = blkattn.debug_plan(B, Hq, Hkv, Tq, Tmax, d, torch.bfloat16, sms)
+        if PLAN_BYTES < plan["workspace_bytes"] <= blkattn.STATIC_SCRATCH_BYTES:
+            break
+    else:
+        pytest.fail("no plan between 15.75 and 16 MiB")
+    assert plan["kernel"] == 3 and plan["n_splits"] > 1
+    g = torch.Generator().manual_seed(1)
+    q = torch.randn(B, Hq, Tq, d, generator=g).to(torch.bfloat16).cuda()
+    k = torch.randn(B, Hkv, Tmax, d, generator=g).to(torch.bfloat16).cuda()
+    v = torch.randn(B, Hkv, Tmax, d, generator=g).to(torch.bfloat16).cuda()
+    sl = torch.full((B,), Tmax, dtype=torch.int32).cuda()
+    qp = torch.full((B, Tq), Tmax - 1, dtype=torch.int32).cuda()
+    out = torch.full((B, Hq, Tq, d), 7.0, device="cuda")
+    lse = torch.full((B, Hq, Tq), 7.0, device="cuda")
+    with pytest.raises(blkattn.BlkattnError) as e:
+        blkattn.fwd_static_scratch(q, k, v, sl, qp, None, d ** -0.5, out, lse)
+    assert e.value.status == blkattn.ERR_SCRATCH_LIMIT
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0) and torch.all(lse == 7.0)  # nothing was enqueued
