@@ -9,17 +9,24 @@
 // the CTA loads; key tiles beyond the CTA's last visible key are never loaded.
 //
 //   S_j  = Q K_j^T     tcgen05.mma M=128 N=128 K=16 x 8      (smem x smem -> TMEM)
-//   U   += P_j V_j     tcgen05.mma M=128 N=128 K=16 x 8 x 2  (P from TMEM, V smem)
+//   U   += P_j V_j     tcgen05.mma M=128 N=128 K=16 x 8 (x 2 on split tiles; P from TMEM, V smem)
 //
 // Roles (320 threads): warps 0-3 and 4-7 = one thread per query row of the
 // first / second query tile (a TMEM lane each): scores, mask by select,
 // online statistics, P; warp 8 = TMA producer (both Q tiles once, K and V
 // tiles into 2-stage rings released separately); warp 9 = TMEM allocation
 // and the single thread that issues every MMA.  Each query tile has one S
-// buffer in TMEM; P_j is written over it as bf16 P_hi and P_lo (P = P_hi +
-// P_lo to ~16 bits, so the PV product keeps ~2^-17 relative accuracy
-// although P is not an input), and S_{j+1} is issued right after U += P_j V_j
-// (products execute in issue order).  The two query tiles ping-pong: while
+// buffer in TMEM and P_j is written over it.  On a key tile that some row of
+// the query tile does not see in full (the diagonal, a window's leading
+// edge: where the rows with few keys get most of their weight) P_j goes in
+// as bf16 P_hi and P_lo (P = P_hi + P_lo to ~16 bits, two PV products, ~2^-17
+// relative accuracy although P is not an input); on the other tiles as one
+// bf16 P rounded to nearest, with l summing the rounded values so that u / l
+// stays a convex combination of the values (rows that see those tiles see
+// at least 128 keys in each, and the rounding errors average out: measured
+// well inside the output bar).  The MMA thread tells the two kinds of tile
+// apart by the same rule as the rows.  S_{j+1} is issued right after U +=
+// P_j V_j (products execute in issue order).  The two query tiles ping-pong: while
 // one tile's rows compute P, the tensor core runs the other tile's products.
 // Each tile's chain S_j -> P_j -> products -> S_{j+1} passes through the
 // MMA thread, so its issue path is kept short: shared-memory descriptors are
@@ -304,13 +311,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::commit(&s_full[t]);
       };
-      // U_t += P_jj V_jj (P_hi, then P_lo); `more`: U_t already holds a tile
+      // U_t += P_jj V_jj (P_hi, then P_lo on the tiles that split P);
+      // `more`: U_t already holds a tile
+      const int min_end[QT] = {misc[2], misc[4]};
+      const int win_max[QT] = {WIN ? misc[7] : 0, WIN ? misc[9] : 0};
       auto issue_pv = [&](int t, int jj, bool more) {
         const uint32_t vlo = tc::desc_lo(sV + (jj % STAGES) * kTileBytes, kBox);
         constexpr uint32_t kHi = tc::desc_hi(1024);
         const uint32_t tcol = tb + t * kTileCols;
+        const int k0 = (j_lo + jj) * BN;
+        const bool split = k0 + BN > min_end[t] || (WIN && k0 < win_max[t]);
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
+          if (part == 1 && !split) break;
 #pragma unroll
           for (int ks = 0; ks < BN / 16; ++ks) {
             // B = V rows [16ks, 16ks+16) (keys, K) x 128 dims (N, two 64-dim boxes 16 KB apart)
@@ -372,6 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int my_min = misc[2 + 2 * x];
     const int f_mine = x == 0 ? f_t0 : f_t1;            // first key tile (0 without a window)
     const int win_max = WIN ? misc[7 + 2 * x] : 0;     // keys below it are masked for some row
+    // a key tile some row of the query tile does not see in full (the
+    // diagonal, a window's leading edge): P goes to the product as P_hi +
+    // P_lo (the few-key rows live here); elsewhere as one bf16 P
+    auto split_tile = [&](int k0) { return k0 + BN > my_min || (WIN && k0 < win_max); };
     if (n_mine == 0) {
       if (my_row) write_empty_row();
     } else {
@@ -460,25 +477,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 neg1 = make_float2(-1.f, -1.f);
         float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                         make_float2(0.f, 0.f)};
+        if (split_tile(key0)) {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {  // 32 keys -> 16 columns of P_hi and of P_lo
-          uint32_t hi[16], lo[16];
+          for (int q4 = 0; q4 < 4; ++q4) {  // 32 keys -> 16 columns of P_hi and of P_lo
+            uint32_t hi[16], lo[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int k2 = 32 * q4 + 2 * c;
-            const float2 e = __ffma2_rn(make_float2(xs[k2], xs[k2 + 1]), sc2, nm2);
-            const float2 pp = make_float2(fast_exp2(e.x), fast_exp2(e.y));
-            ls[c & 3] = __fadd2_rn(ls[c & 3], pp);
-            // P = P_hi + P_lo: P_hi = the upper halves (truncation, exact),
-            // P_lo = bf16(P - P_hi) (P - P_hi exact in fp32, below 2^-7 P)
-            asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi[c]) : "r"(__float_as_uint(pp.x)), "r"(__float_as_uint(pp.y)));
-            const float2 th = make_float2(__uint_as_float(__float_as_uint(pp.x) & 0xffff0000u),
-                                          __uint_as_float(__float_as_uint(pp.y) & 0xffff0000u));
-            const float2 rem = __ffma2_rn(th, neg1, pp);
-            lo[c] = pack_bf16(rem.x, rem.y);
+            for (int c = 0; c < 16; ++c) {
+              const int k2 = 32 * q4 + 2 * c;
+              const float2 e = __ffma2_rn(make_float2(xs[k2], xs[k2 + 1]), sc2, nm2);
+              const float2 pp = make_float2(fast_exp2(e.x), fast_exp2(e.y));
+              ls[c & 3] = __fadd2_rn(ls[c & 3], pp);
+              // P = P_hi + P_lo: P_hi = the upper halves (truncation, exact),
+              // P_lo = bf16(P - P_hi) (P - P_hi exact in fp32, below 2^-7 P)
+              asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi[c]) : "r"(__float_as_uint(pp.x)), "r"(__float_as_uint(pp.y)));
+              const float2 th = make_float2(__uint_as_float(__float_as_uint(pp.x) & 0xffff0000u),
+                                            __uint_as_float(__float_as_uint(pp.y) & 0xffff0000u));
+              const float2 rem = __ffma2_rn(th, neg1, pp);
+              lo[c] = pack_bf16(rem.x, rem.y);
+            }
+            tc::st16(tl + kColS + 16 * q4, hi);
+            tc::st16(tl + kColPlo + 16 * q4, lo);
           }
-          tc::st16(tl + kColS + 16 * q4, hi);
-          tc::st16(tl + kColPlo + 16 * q4, lo);
+        } else {
+          // every row sees every key of the tile: P rounded to bf16 (to
+          // nearest) is the product's operand, and l sums the rounded values,
+          // so u / l stays a convex combination of the values
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {  // 32 keys -> 16 columns of P
+            uint32_t pb[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int k2 = 32 * q4 + 2 * c;
+              const float2 e = __ffma2_rn(make_float2(xs[k2], xs[k2 + 1]), sc2, nm2);
+              pb[c] = pack_bf16(fast_exp2(e.x), fast_exp2(e.y));
+              ls[c & 3] = __fadd2_rn(ls[c & 3], make_float2(__uint_as_float(pb[c] << 16),
+                                                            __uint_as_float(pb[c] & 0xffff0000u)));
+            }
+            tc::st16(tl + kColS + 16 * q4, pb);
+          }
         }
         {
           const float2 a = __fadd2_rn(ls[0], ls[1]);

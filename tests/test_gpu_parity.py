@@ -71,6 +71,7 @@ def assert_parity(o, l, ref, tol_o, tol_l, out_raw=None, bf16_out=False):
     assert np.all(np.isfinite(l[live]))
     lerr = np.abs(l[live] - ref["lse"][live])
     assert lerr.max() <= tol_l, f"lse err {lerr.max():.3e}"
+    return float((err / bound).max())  # the worst row's share of the bar
 
 
 def tols(s):
@@ -160,7 +161,12 @@ def test_full_size_workload(name):
     if s.Tq >= 64:
         rows = prefill_rows(s)
         ref = run_oracle(inp, rows=rows)
-        assert_parity(o[rows], l[rows], ref, *tols(s))
+        share = assert_parity(o[rows], l[rows], ref, *tols(s))
+        # P goes to the PV product as one bf16 value on key tiles every row
+        # of the query tile sees in full (P_hi + P_lo elsewhere): a numpy
+        # study put the worst row at 0.37 of the bar; keep a clear margin
+        print(f"{name}: worst row at {share:.3f} of the output bar")
+        assert share <= 0.75
     else:
         ref = run_oracle(inp)
         assert_parity(o, l, ref, *tols(s))
