@@ -26,16 +26,21 @@
 // S and G_P are formed twice (7 products of 128 x 128 x 128 per tile pair
 // instead of 5).
 //
-// Roles in kernels 2 and 3 (320 threads): warps 0-7 one thread per TMEM lane
+// Roles in kernels 2 and 3 (352 threads): warps 0-7 one thread per TMEM lane
 // and half tile: group g = warp / 4 owns columns [64 g, 64 g + 64) of every
 // tile (keys in 2, query rows in 3), lane quarter warp % 4; warp 8 the TMA
-// producer; warp 9 TMEM allocation and the single MMA-issuing thread.  The
-// products of a tile are issued by half (N = 64 for S and G_P, K = 64 for
-// the accumulating ones), each half with its own barriers, so one group's
-// exponentials overlap the tensor core's work on the other half, and the
-// next tile's first half starts as soon as its columns are free.  Products
-// execute in issue order, so a new S may overwrite the columns the previous
-// products read.  Every wait is bounded (error flag, then an orderly exit).
+// producer; warp 9 TMEM allocation and the thread that issues the
+// accumulating products; warp 10 the thread that issues the S and G_P
+// products.  (One thread issues a product every ~75 cycles; an N = 64
+// product's math takes ~32, and two issuing threads get one every ~49.)
+// The products of a tile are issued by half (N = 64 for S and G_P, K = 64
+// for the accumulating ones), each half with its own barriers, so one
+// group's exponentials overlap the tensor core's work on the other half.
+// The next tile's half g overwrites the columns the accumulating products of
+// half g read, so its S and G_P wait until those products have completed
+// (a barrier per half).  The accumulating products come from one thread in
+// a fixed order, so the sums stay deterministic.  Every wait is bounded
+// (error flag, then an orderly exit).
 //
 // Visibility is the forward's (length, position, bias, and with the WIN
 // instantiations a sliding window; select, not add): invisible entries get
@@ -60,9 +65,10 @@ constexpr int D = 128;   // head dim
 constexpr int STAGES = 2;
 constexpr int kBox = 128 * 128;       // one 64-dim (128-byte) box of 128 rows: 16 KB
 constexpr int kTileBytes = 2 * kBox;  // 128 rows x 128 dims, bf16
-constexpr int kThreads = 320;
 constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;    // the accumulating products (and TMEM allocation)
+constexpr int kScoreWarp = 10; // the S and G_P products
+constexpr int kThreads = 352;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescHalf = tc::idesc_bf16(128, HT, 0, 0);  // S half: both K-major, N = 64
 constexpr uint32_t kIdescTN = tc::idesc_bf16(128, 128, 0, 1);   // A in TMEM, B N-major, N = 128
@@ -295,7 +301,8 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
   uint64_t* v_empty = bars + 7;       // [STAGES]
   uint64_t* sp_full = bars + 9;       // [2] half g of S and G_P is in TMEM
   uint64_t* p_full = bars + 11;       // [2] half g of G_S is in TMEM (4 warps of group g)
-  uint64_t* drain = bars + 13;        // every product has completed
+  uint64_t* drain = bars + 13;        // every product has completed (both issuing threads)
+  uint64_t* acc_done = bars + 14;     // [2] G_Q += G_S K over half g has completed
   int* misc = reinterpret_cast<int*>(sm + kOffMisc);  // [0] TMEM base, [1] CTA end
 
   // Groups of p.hg_q (sequence, head) pairs whose K/V fit in L2 together;
@@ -326,8 +333,9 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
     for (int g = 0; g < 2; ++g) {
       mbar_init(&sp_full[g], 1);
       mbar_init(&p_full[g], 4);
+      mbar_init(&acc_done[g], 1);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);
     fence_barrier_init();
   }
   const uint32_t tb = setup_tmem(misc, warp);
@@ -417,7 +425,8 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
         if (!mbar_wait(&v_full[j % STAGES], (j / STAGES) & 1)) ok = false;
       if (!ok) record_error(p.err, kErrTimeout);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kScoreWarp) {
+    // ---------------- S and G_P products (one thread) ----------------
     if (lane == 0) {
       // S and G_P of half g of key tile j (S at columns 64 g, G_P at 128 + 64 g)
       auto half = [&](int j, int g) {
@@ -439,26 +448,37 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
         half(0, 1);
         tc::commit(&v_empty[0]);
       }
+      for (int j = 0; ok && j + 1 < n; ++j) {
+        // half g of tile j + 1 overwrites the columns G_Q += G_S K of tile j
+        // reads: it waits until that product has completed
+        if (!tile_ready(j + 1)) { ok = false; break; }
+        if (!mbar_wait(&acc_done[0], j & 1)) { ok = false; break; }
+        tc::fence_after();
+        half(j + 1, 0);
+        if (!mbar_wait(&acc_done[1], j & 1)) { ok = false; break; }
+        tc::fence_after();
+        half(j + 1, 1);
+        tc::commit(&v_empty[(j + 1) % STAGES]);  // V_{j+1} once its halves are done
+      }
+      if (!ok) record_error(p.err, kErrTimeout);
+      tc::commit(drain);
+      if (!mbar_wait(drain, 0)) record_error(p.err, kErrTimeout);
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------- G_Q += G_S K (one thread; a fixed order) ----------------
+    if (lane == 0) {
+      bool ok = true;
       for (int j = 0; ok && j < n; ++j) {
         const int s = j % STAGES;
-        const bool next = j + 1 < n;
-        // G_Q += G_S K over the keys of half 0, then half 0 of the next tile
         if (!mbar_wait(&p_full[0], j & 1)) { ok = false; break; }
         tc::fence_after();
         issue_acc(tb + 256, tb + 128, sK + s * kTileBytes, 0, j > 0);
-        if (next) {
-          if (!tile_ready(j + 1)) { ok = false; break; }
-          half(j + 1, 0);
-        }
-        // half 1 likewise; K_j is then free, and V_{j+1} once its halves are done
+        tc::commit(&acc_done[0]);
         if (!mbar_wait(&p_full[1], j & 1)) { ok = false; break; }
         tc::fence_after();
         issue_acc(tb + 256, tb + 128 + HT, sK + s * kTileBytes, 1, true);
-        tc::commit(&k_empty[s]);
-        if (next) {
-          half(j + 1, 1);
-          tc::commit(&v_empty[(j + 1) % STAGES]);
-        }
+        tc::commit(&acc_done[1]);
+        tc::commit(&k_empty[s]);  // K_j is free: tile j's halves completed before its G_S was written
       }
       if (!ok) record_error(p.err, kErrTimeout);
       tc::commit(drain);
@@ -589,7 +609,8 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
   uint64_t* qg_empty = bars + 3;     // [STAGES]
   uint64_t* sp_full = bars + 5;      // [2] half g of S^T and G_P^T in TMEM
   uint64_t* p_full = bars + 7;       // [2] half g of P^T and G_S^T in TMEM (4 warps of group g)
-  uint64_t* drain = bars + 9;
+  uint64_t* drain = bars + 9;        // every product has completed (both issuing threads)
+  uint64_t* acc_done = bars + 10;    // [2] G_V and G_K over half g have completed
   int* misc = reinterpret_cast<int*>(sm + kOffMisc);
   float4* facts = reinterpret_cast<float4*>(sm + kOffFacts);  // [2][128]: L, D, end (int bits), -
   int* ends = reinterpret_cast<int*>(sm + kOffEnds);          // this sequence's row end per query tile
@@ -625,8 +646,9 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
     for (int g = 0; g < 2; ++g) {
       mbar_init(&sp_full[g], 1);
       mbar_init(&p_full[g], 4);
+      mbar_init(&acc_done[g], 1);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);
     fence_barrier_init();
   }
   const uint32_t tb = setup_tmem(misc, warp);
@@ -663,7 +685,8 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
         if (!mbar_wait(&qg_full[u % STAGES], (u / STAGES) & 1)) ok = false;
       if (!ok) record_error(p.err, kErrTimeout);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kScoreWarp) {
+    // ---------------- S^T and G_P^T products (one thread) ----------------
     if (lane == 0 && any) {
       // S^T and G_P^T of the query rows [64 g, 64 g + 64) of visit t
       auto half = [&](int t, int g) {
@@ -683,26 +706,42 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
         half(0, 1);
       }
       Visit v = first;
+      for (int t = 0; ok && next_visit<WIN>(p, ends, starts, k0, v); ++t) {
+        // half g of visit t + 1 overwrites the columns G_V and G_K of visit
+        // t read: it waits until those products have completed
+        if (!visit_ready(t + 1)) { ok = false; break; }
+        if (!mbar_wait(&acc_done[0], t & 1)) { ok = false; break; }
+        tc::fence_after();
+        half(t + 1, 0);
+        if (!mbar_wait(&acc_done[1], t & 1)) { ok = false; break; }
+        tc::fence_after();
+        half(t + 1, 1);
+      }
+      if (!ok) record_error(p.err, kErrTimeout);
+      tc::commit(drain);
+      if (!mbar_wait(drain, 0)) record_error(p.err, kErrTimeout);
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------- G_V += P^T G_O, G_K += G_S^T Q (one thread; a fixed order) ----------------
+    if (lane == 0 && any) {
+      bool ok = true;
+      Visit v = first;
       for (int t = 0; ok; ++t) {
         const int s = t % STAGES;
         const bool next = next_visit<WIN>(p, ends, starts, k0, v);
-        // G_V += P^T G_O and G_K += G_S^T Q over the rows of half 0, then
-        // half 0 of the next visit
         if (!mbar_wait(&p_full[0], t & 1)) { ok = false; break; }
         tc::fence_after();
         issue_acc(tb + 256, tb + 0, sG + s * kTileBytes, 0, t > 0);
         issue_acc(tb + 384, tb + 128, sQ + s * kTileBytes, 0, t > 0);
-        if (next) {
-          if (!visit_ready(t + 1)) { ok = false; break; }
-          half(t + 1, 0);
-        }
+        tc::commit(&acc_done[0]);
         if (!mbar_wait(&p_full[1], t & 1)) { ok = false; break; }
         tc::fence_after();
         issue_acc(tb + 256, tb + HT, sG + s * kTileBytes, 1, true);
         issue_acc(tb + 384, tb + 128 + HT, sQ + s * kTileBytes, 1, true);
+        tc::commit(&acc_done[1]);
+        // the visit's Q and G_O slot is free: its halves completed before its P^T was written
         tc::commit(&qg_empty[s]);
         if (!next) break;
-        half(t + 1, 1);
       }
       if (!ok) record_error(p.err, kErrTimeout);
       tc::commit(drain);
