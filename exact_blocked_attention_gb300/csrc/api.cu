@@ -674,6 +674,14 @@ int fwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_ten
 // blkattn_last_cuda_error like the ones here.
 int report_cuda_failure(cudaError_t e) { return cuda_fail(e); }
 
+int device_error_word(int** out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  const int st = device_state(&ds);
+  if (st == BLKATTN_OK) *out = ds->err;
+  return st;
+}
+
 namespace {
 
 // fp32 gradient rows written with 16-byte vector stores: unit dim stride,

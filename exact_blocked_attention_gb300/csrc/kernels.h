@@ -185,6 +185,9 @@ int fwd_with_scratch(const blkattn_tensor* q, const blkattn_tensor* k, const blk
                      void* scratch, size_t scratch_bytes);
 // Records a CUDA failure for blkattn_last_cuda_error; returns BLKATTN_ERR_CUDA.
 int report_cuda_failure(cudaError_t e);
+// The current device's error word (kernels record a bounded wait that ran
+// out there; blkattn_check_device_error reads and clears it).
+int device_error_word(int** out);
 // blkattn_fwd / _tree / _window (tree may be NULL, window 0 = none) on the
 // library's workspace.
 int fwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_tensor* v,

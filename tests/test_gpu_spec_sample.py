@@ -141,3 +141,29 @@ def test_residual_is_drawn_from_the_exact_difference(B, k, V):
     np.testing.assert_array_equal(n, on)
     np.testing.assert_array_equal(tok, ot)
     assert np.all(n == 0)
+
+
+def test_unaligned_rows_take_plain_loads():
+    """Rows that do not start on a 16-byte boundary are read with plain loads
+    (no bulk copies); the results are the same integers."""
+    p, q, draft, u, s = random_case(6, 2, 5003, seed=9)
+    bp = torch.zeros(6 * 3 * 5003 + 1)
+    bp[1:] = p.reshape(-1)
+    bq = torch.zeros(6 * 2 * 5003 + 3)
+    bq[3:] = q.reshape(-1)
+    pv = bp.cuda()[1:].view(6, 3, 5003)  # 4-byte offsets: not 16-byte aligned
+    qv = bq.cuda()[3:].view(6, 2, 5003)
+    n, tok = blkattn.spec_sample(pv, qv, draft.cuda(), u.cuda(), s.cuda())
+    torch.cuda.synchronize()
+    on, ot = ss.verify_step(p.numpy(), q.numpy(), draft.numpy(), u.numpy(), s.numpy().view(np.uint32))
+    np.testing.assert_array_equal(n.cpu().numpy(), on)
+    np.testing.assert_array_equal(tok.cpu().numpy(), ot)
+
+
+def test_vocabulary_beyond_the_recorded_chunks():
+    """A vocabulary of 1.3 M entries: each CTA's half spans more ring slots
+    than it records sums for, so chunks hold several slots and the last
+    scan covers a whole chunk."""
+    n, tok, on, ot = run_both(*random_case(3, 1, 1300003, seed=77))
+    np.testing.assert_array_equal(n, on)
+    np.testing.assert_array_equal(tok, ot)
