@@ -38,7 +38,10 @@
 // group's exponentials overlap the tensor core's work on the other half.
 // The next tile's half g overwrites the columns the accumulating products of
 // half g read, so its S and G_P wait until those products have completed
-// (a barrier per half).  The accumulating products come from one thread in
+// (a barrier per half).  In dK/dV the stages are split further: the key rows
+// form P^T as soon as S^T is in (G_P^T may still be in the pipe) and G_V's
+// products start on it while the rows form G_S^T; the next S^T waits only
+// for G_V, the next G_P^T for G_K.  The accumulating products come from one thread in
 // a fixed order, so the sums stay deterministic.  Every wait is bounded
 // (error flag, then an orderly exit).
 //
@@ -79,7 +82,7 @@ constexpr int kOffA1 = kTileBytes;                    // dQ: G_O  | dK/dV: V
 constexpr int kOffR0 = 2 * kTileBytes;                // dQ: K ring | dK/dV: Q ring
 constexpr int kOffR1 = kOffR0 + STAGES * kTileBytes;  // dQ: V ring | dK/dV: G_O ring
 constexpr int kOffBar = kOffR1 + STAGES * kTileBytes;
-constexpr int kNumBars = 16;
+constexpr int kNumBars = 24;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kOffFacts = kOffMisc + 128;                     // dK/dV: float4 [2][128] (-L, -D, end, start)
 constexpr int kMaxQTiles = 1024;                              // query tiles per sequence (T_q <= 131072)
@@ -241,14 +244,18 @@ __device__ __forceinline__ void dq_chunk(const uint32_t (&rs)[32], const uint32_
   }
 }
 
-// 32 entries of one key's row (dK/dV: a key over 32 query rows) from S^T and
-// G_P^T in TMEM and the rows' facts f (-L, -D, end): P^T and G_S^T packed to
-// bf16 pairs, by select where the row does not see the key.  MASK = false:
-// the key is visible to every row of the half (no bias, before every end).
+// dK/dV: 32 entries of one key's row (a key over 32 query rows) in two
+// steps, so that P^T can go to its products before G_P^T has arrived.
+// Step 1: P^T of 32 rows from S^T and the rows' facts f (-L, -D, end,
+// start), packed to bf16 pairs, by select where the row does not see the
+// key; returns the visibility bits of the 32 rows (bit c: row c sees the
+// key).  MASK = false: the key is visible to every row of the half (no bias,
+// before every end).
 template <bool BIAS, bool MASK, bool WIN = false>
-__device__ __forceinline__ void dkv_chunk(const uint32_t (&rs)[32], const uint32_t (&rp)[32], const float4* f,
-                                          int key, float2 c2, const float* bcol, int64_t bi_si, int rows_left,
-                                          bool kin, uint32_t (&pp)[16], uint32_t (&ds)[16]) {
+__device__ __forceinline__ uint32_t dkv_p(const uint32_t (&rs)[32], const float4* f, int key, float2 c2,
+                                          const float* bcol, int64_t bi_si, int rows_left, bool kin,
+                                          uint32_t (&pp)[16]) {
+  uint32_t vis = 0xffffffffu;
 #pragma unroll
   for (int c = 0; c < 32; c += 2) {
     const float4 f0 = f[c], f1 = f[c + 1];
@@ -274,14 +281,26 @@ __device__ __forceinline__ void dkv_chunk(const uint32_t (&rs)[32], const uint32
     if constexpr (MASK || BIAS) {
       p0 = v0 ? p0 : 0.f;
       p1 = v1 ? p1 : 0.f;
+      vis &= ~((v0 ? 0u : 1u) << c) & ~((v1 ? 0u : 1u) << (c + 1));
     }
-    const float2 g = __fmul2_rn(make_float2(p0, p1), __fadd2_rn(make_float2(__uint_as_float(rp[c]),
-                                                                             __uint_as_float(rp[c + 1])),
-                                                                 make_float2(f0.y, f1.y)));
     pp[c >> 1] = pack_bf16(p0, p1);
-    // G_S^T by select: a masked G_P may be NaN (cache padding)
-    if constexpr (MASK || BIAS)
-      ds[c >> 1] = pack_bf16(v0 ? g.x : 0.f, v1 ? g.y : 0.f);
+  }
+  return vis;
+}
+
+// Step 2: G_S^T = P (G_P - D) of the 32 rows from G_P^T and step 1's P (the
+// bf16 pairs: G_S^T is rounded to bf16 for its product anyway), by select
+// where the row does not see the key (a masked G_P may be NaN).
+template <bool SEL>
+__device__ __forceinline__ void dkv_ds(const uint32_t (&rp)[32], const uint32_t (&pp)[16], uint32_t vis,
+                                       const float4* f, uint32_t (&ds)[16]) {
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    const float2 pv = make_float2(__uint_as_float(pp[c >> 1] << 16), __uint_as_float(pp[c >> 1] & 0xffff0000u));
+    const float2 g = __fmul2_rn(pv, __fadd2_rn(make_float2(__uint_as_float(rp[c]), __uint_as_float(rp[c + 1])),
+                                               make_float2(f[c].y, f[c + 1].y)));
+    if constexpr (SEL)
+      ds[c >> 1] = pack_bf16(((vis >> c) & 1u) ? g.x : 0.f, ((vis >> (c + 1)) & 1u) ? g.y : 0.f);
     else
       ds[c >> 1] = pack_bf16(g.x, g.y);
   }
@@ -607,10 +626,13 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
   uint64_t* kv_full = bars;          // K and V tiles
   uint64_t* qg_full = bars + 1;      // [STAGES] Q and G_O tiles
   uint64_t* qg_empty = bars + 3;     // [STAGES]
-  uint64_t* sp_full = bars + 5;      // [2] half g of S^T and G_P^T in TMEM
-  uint64_t* p_full = bars + 7;       // [2] half g of P^T and G_S^T in TMEM (4 warps of group g)
-  uint64_t* drain = bars + 9;        // every product has completed (both issuing threads)
-  uint64_t* acc_done = bars + 10;    // [2] G_V and G_K over half g have completed
+  uint64_t* s_full = bars + 5;       // [2] half g of S^T in TMEM
+  uint64_t* gp_full = bars + 7;      // [2] half g of G_P^T in TMEM
+  uint64_t* pt_full = bars + 9;      // [2] half g of P^T in TMEM (4 warps of group g)
+  uint64_t* ds_full = bars + 11;     // [2] half g of G_S^T in TMEM (4 warps of group g)
+  uint64_t* dv_done = bars + 13;     // [2] G_V += P^T G_O over half g has completed
+  uint64_t* dk_done = bars + 15;     // [2] G_K += G_S^T Q over half g has completed
+  uint64_t* drain = bars + 17;       // every product has completed (both issuing threads)
   int* misc = reinterpret_cast<int*>(sm + kOffMisc);
   float4* facts = reinterpret_cast<float4*>(sm + kOffFacts);  // [2][128]: L, D, end (int bits), -
   int* ends = reinterpret_cast<int*>(sm + kOffEnds);          // this sequence's row end per query tile
@@ -644,9 +666,12 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
       mbar_init(&qg_empty[s], 1);
     }
     for (int g = 0; g < 2; ++g) {
-      mbar_init(&sp_full[g], 1);
-      mbar_init(&p_full[g], 4);
-      mbar_init(&acc_done[g], 1);
+      mbar_init(&s_full[g], 1);
+      mbar_init(&gp_full[g], 1);
+      mbar_init(&pt_full[g], 4);
+      mbar_init(&ds_full[g], 4);
+      mbar_init(&dv_done[g], 1);
+      mbar_init(&dk_done[g], 1);
     }
     mbar_init(drain, 2);
     fence_barrier_init();
@@ -688,12 +713,14 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
   } else if (warp == kScoreWarp) {
     // ---------------- S^T and G_P^T products (one thread) ----------------
     if (lane == 0 && any) {
-      // S^T and G_P^T of the query rows [64 g, 64 g + 64) of visit t
-      auto half = [&](int t, int g) {
-        const int s = t % STAGES;
-        issue_half(tb + HT * g, sK, sQ + s * kTileBytes, g);
-        issue_half(tb + 128 + HT * g, sV, sG + s * kTileBytes, g);
-        tc::commit(&sp_full[g]);
+      // S^T (G_P^T) of the query rows [64 g, 64 g + 64) of visit t
+      auto half_s = [&](int t, int g) {
+        issue_half(tb + HT * g, sK, sQ + (t % STAGES) * kTileBytes, g);
+        tc::commit(&s_full[g]);
+      };
+      auto half_gp = [&](int t, int g) {
+        issue_half(tb + 128 + HT * g, sV, sG + (t % STAGES) * kTileBytes, g);
+        tc::commit(&gp_full[g]);
       };
       auto visit_ready = [&](int t) -> bool {
         const bool r = mbar_wait(&qg_full[t % STAGES], (t / STAGES) & 1);
@@ -702,20 +729,29 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
       };
       bool ok = mbar_wait(kv_full, 0) && visit_ready(0);
       if (ok) {
-        half(0, 0);
-        half(0, 1);
+        half_s(0, 0);
+        half_gp(0, 0);
+        half_s(0, 1);
+        half_gp(0, 1);
       }
       Visit v = first;
       for (int t = 0; ok && next_visit<WIN>(p, ends, starts, k0, v); ++t) {
-        // half g of visit t + 1 overwrites the columns G_V and G_K of visit
-        // t read: it waits until those products have completed
+        // S^T of visit t + 1 overwrites the P^T columns G_V of visit t read,
+        // G_P^T the G_S^T columns G_K read: each waits for those products
         if (!visit_ready(t + 1)) { ok = false; break; }
-        if (!mbar_wait(&acc_done[0], t & 1)) { ok = false; break; }
+        const uint32_t ph = t & 1;
+        if (!mbar_wait(&dv_done[0], ph)) { ok = false; break; }
         tc::fence_after();
-        half(t + 1, 0);
-        if (!mbar_wait(&acc_done[1], t & 1)) { ok = false; break; }
+        half_s(t + 1, 0);
+        if (!mbar_wait(&dk_done[0], ph)) { ok = false; break; }
         tc::fence_after();
-        half(t + 1, 1);
+        half_gp(t + 1, 0);
+        if (!mbar_wait(&dv_done[1], ph)) { ok = false; break; }
+        tc::fence_after();
+        half_s(t + 1, 1);
+        if (!mbar_wait(&dk_done[1], ph)) { ok = false; break; }
+        tc::fence_after();
+        half_gp(t + 1, 1);
       }
       if (!ok) record_error(p.err, kErrTimeout);
       tc::commit(drain);
@@ -729,16 +765,25 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
       for (int t = 0; ok; ++t) {
         const int s = t % STAGES;
         const bool next = next_visit<WIN>(p, ends, starts, k0, v);
-        if (!mbar_wait(&p_full[0], t & 1)) { ok = false; break; }
+        const uint32_t ph = t & 1;
+        // G_V over half 0 as soon as its P^T is in, G_K once its G_S^T is,
+        // then half 1 (this order every visit)
+        if (!mbar_wait(&pt_full[0], ph)) { ok = false; break; }
         tc::fence_after();
         issue_acc(tb + 256, tb + 0, sG + s * kTileBytes, 0, t > 0);
+        tc::commit(&dv_done[0]);
+        if (!mbar_wait(&ds_full[0], ph)) { ok = false; break; }
+        tc::fence_after();
         issue_acc(tb + 384, tb + 128, sQ + s * kTileBytes, 0, t > 0);
-        tc::commit(&acc_done[0]);
-        if (!mbar_wait(&p_full[1], t & 1)) { ok = false; break; }
+        tc::commit(&dk_done[0]);
+        if (!mbar_wait(&pt_full[1], ph)) { ok = false; break; }
         tc::fence_after();
         issue_acc(tb + 256, tb + HT, sG + s * kTileBytes, 1, true);
+        tc::commit(&dv_done[1]);
+        if (!mbar_wait(&ds_full[1], ph)) { ok = false; break; }
+        tc::fence_after();
         issue_acc(tb + 384, tb + 128 + HT, sQ + s * kTileBytes, 1, true);
-        tc::commit(&acc_done[1]);
+        tc::commit(&dk_done[1]);
         // the visit's Q and G_O slot is free: its halves completed before its P^T was written
         tc::commit(&qg_empty[s]);
         if (!next) break;
@@ -784,7 +829,7 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
         }
         // (the barrier also publishes the facts; the answer is the same for
         // the group's 128 threads, so none is left at a later barrier)
-        if (!bar_and(1 + grp, 128, wait_all(&sp_full[grp], t & 1))) { ok = false; break; }
+        if (!bar_and(1 + grp, 128, wait_all(&s_full[grp], t & 1))) { ok = false; break; }
         tc::fence_after();
         const float* bcol = nullptr;
         if constexpr (BIAS)
@@ -796,26 +841,44 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
         const bool whole =
             !BIAS && __all_sync(0xffffffffu, key < min(mn[0], mn[1]) && (!WIN || key >= max(mx[0], mx[1])));
         const int rows_left = p.Tq - (v.qt * BT + grp * HT);  // rows of the half inside T_q
+        // step 1: P^T from S^T (G_P^T may still be in the tensor pipe)
+        uint32_t pk[2][16], vis[2];
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {
-          uint32_t rs[32], rp[32], pp[16], ds[16];
+          uint32_t rs[32];
           tc::ld32(tl + HT * grp + 32 * q2, rs);
-          tc::ld32(tl + 128 + HT * grp + 32 * q2, rp);
           tc::wait_ld();
           const float* bq = BIAS ? bcol + (int64_t)(32 * q2) * p.bi_si : nullptr;
           if (whole)
-            dkv_chunk<BIAS, false, WIN>(rs, rp, f + 32 * q2, key, c2, bq, p.bi_si, rows_left - 32 * q2,
-                                        key < p.Tmax, pp, ds);
+            vis[q2] = dkv_p<BIAS, false, WIN>(rs, f + 32 * q2, key, c2, bq, p.bi_si, rows_left - 32 * q2,
+                                              key < p.Tmax, pk[q2]);
           else
-            dkv_chunk<BIAS, true, WIN>(rs, rp, f + 32 * q2, key, c2, bq, p.bi_si, rows_left - 32 * q2,
-                                       key < p.Tmax, pp, ds);
-          tc::st16(tl + HT * grp + 16 * q2, pp);        // P^T over S^T's first 32 columns of the half
-          tc::st16(tl + 128 + HT * grp + 16 * q2, ds);  // G_S^T likewise over G_P^T
+            vis[q2] = dkv_p<BIAS, true, WIN>(rs, f + 32 * q2, key, c2, bq, p.bi_si, rows_left - 32 * q2,
+                                             key < p.Tmax, pk[q2]);
+          tc::st16(tl + HT * grp + 16 * q2, pk[q2]);  // P^T over S^T's first 32 columns of the half
         }
         tc::wait_st();
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[grp]);
+        if (lane == 0) mbar_arrive(&pt_full[grp]);
+        // step 2: G_S^T from G_P^T and P
+        if (!bar_and(1 + grp, 128, wait_all(&gp_full[grp], t & 1))) { ok = false; break; }
+        tc::fence_after();
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+          uint32_t rp[32], ds[16];
+          tc::ld32(tl + 128 + HT * grp + 32 * q2, rp);
+          tc::wait_ld();
+          if (whole)
+            dkv_ds<false>(rp, pk[q2], vis[q2], f + 32 * q2, ds);
+          else
+            dkv_ds<true>(rp, pk[q2], vis[q2], f + 32 * q2, ds);
+          tc::st16(tl + 128 + HT * grp + 16 * q2, ds);  // G_S^T over G_P^T's first 32 columns
+        }
+        tc::wait_st();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ds_full[grp]);
         if (!next_visit<WIN>(p, ends, starts, k0, v)) break;
       }
       if (ok && !wait_all(drain, 0)) ok = false;
