@@ -167,3 +167,18 @@ def test_vocabulary_beyond_the_recorded_chunks():
     n, tok, on, ot = run_both(*random_case(3, 1, 1300003, seed=77))
     np.testing.assert_array_equal(n, on)
     np.testing.assert_array_equal(tok, ot)
+
+
+def test_more_candidates_than_a_warp_tests_at_once():
+    """k = 40 candidates: the first 35 positions have p = q (always kept for
+    u < 1), so the in-order test runs past the first 32 candidates."""
+    B, k, V = 4, 40, 777
+    p, q, draft, u, s = [t.numpy().copy() for t in random_case(B, k, V, seed=41)]
+    for b in range(B):
+        for i in range(35):
+            q[b, i] = p[b, i]
+            draft[b, i] = int(np.argmax(q[b, i]))  # a proposable candidate (q > 0)
+    n, tok, on, ot = run_both(*[torch.from_numpy(np.ascontiguousarray(a)) for a in (p, q, draft, u, s)])
+    np.testing.assert_array_equal(n, on)
+    np.testing.assert_array_equal(tok, ot)
+    assert np.all(n >= 35)
