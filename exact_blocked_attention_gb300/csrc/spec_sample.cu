@@ -17,7 +17,11 @@
 // floors, and lo moves the weight only when hi * 2^40 is an integer (then
 // by floor(lo * 2^40); otherwise |lo| 2^40 is below the distance from
 // hi * 2^40 to either neighbouring integer).  No fp64 and no 64-bit
-// conversion: both run at a small fraction of the fp32 rate here.  Integer
+// conversion: both run at a small fraction of the fp32 rate here.  When
+// every mass of a warp's share of a slot lies in [0, 1] (as for any real
+// distribution) a shorter exact form without the pair and the clamps gives
+// the same weights; the warp checks that and takes the full form otherwise.
+// Integer
 // prefix sums (order-independent, so every reduction shape gives the same
 // token), threshold floor(s * Z / 2^32) for
 // the row's 32-bit uniform s, and the token is the smallest index whose
@@ -61,6 +65,7 @@ constexpr int kRingBytes = kStages * kSlot * 4 * 2;
 constexpr int kSmemBytes = kRingBytes + kMaxChunks * kWarps * 8 + 64;
 constexpr float kTwo20 = 1048576.0f;         // 2^20
 constexpr float kTwo40 = 1099511627776.0f;   // 2^40
+constexpr float kTwoM20 = 1.0f / 1048576.0f;  // 2^-20
 constexpr float kMagic = 12582912.0f;        // 1.5 * 2^23: x + kMagic holds integer |x| < 2^22 in its low bits
 constexpr int kMagicBits = 0x4B400000;
 
@@ -100,6 +105,37 @@ __device__ __forceinline__ void add_entry(float pv, float qv, int& sh, int& sl) 
   sh += __float_as_int(mh) - kMagicBits;
   sl += __float_as_int(ml) - kMagicBits + e;
 }
+// The same weight for masses already in [0, 1], where no clamp acts, in
+// seven fp32 operations and no select.  With qs = min(q, p) (m = 0 when
+// q >= p) and v = p - qs >= 0:
+//   y  = rd(v)                       floor(y 2^20) = floor(v 2^20): that floor
+//                                    times 2^-20 is an fp32 value <= v
+//   mh = rd(y 2^20 + 1.5 2^23)       one fused rounding: 1.5 2^23 + h, h = floor(v 2^20)
+//   D  = p - h 2^-20                 exact: a multiple of ulp(p) in [0, p]
+//   t  = rd(D - qs)                  D - qs = v - h 2^-20 lies in [0, 2^-20)
+//   ml = rd(t 2^40 + 1.5 2^23)       1.5 2^23 + l, l = floor((v - h 2^-20) 2^40)
+// and F = h 2^20 + l.  (rd: rounding toward -inf; the floor of a value whose
+// floor is an fp32 number equals the floor of its round-down.)  in_range
+// collects the bit patterns: all of them <= 0x3F800000 (1.0f) means every
+// mass was a non-negative number <= 1 (-0, NaN, inf and negatives fail).
+template <bool HQ>
+__device__ __forceinline__ void add_entry_unit(float pv, float qv, int& sh, int& sl, unsigned& bits) {
+  bits = max(bits, __float_as_uint(pv));
+  float qs = 0.f, y = pv;
+  if constexpr (HQ) {
+    bits = max(bits, __float_as_uint(qv));
+    qs = fminf(qv, pv);
+    y = __fadd_rd(pv, -qs);
+  }
+  const float mh = __fmaf_rd(y, kTwo20, kMagic);
+  const float d = __fmaf_rn(-__fsub_rn(mh, kMagic), kTwoM20, pv);
+  const float t = HQ ? __fadd_rd(d, -qs) : d;
+  const float ml = __fmaf_rd(t, kTwo40, kMagic);
+  sh += __float_as_int(mh) - kMagicBits;
+  sl += __float_as_int(ml) - kMagicBits;
+}
+constexpr unsigned kOneBits = 0x3F800000u;
+
 // (sl may be negative: l + e < 0 when l = 0 and lo < 0)
 __device__ __forceinline__ uint64_t combine(int sh, int sl) {
   return (uint64_t)((int64_t)sh * (1 << 20) + (int64_t)sl);
@@ -123,15 +159,33 @@ template <bool HQ>
 __device__ __forceinline__ void slot_sum(const float* sp, const float* sq, const float* gp, const float* gq,
                                          int nw, int copied_here, int lane, int& sh, int& sl) {
   if (copied_here >= kPerWarp) {
+    int fh = 0, fl = 0;
+    unsigned bits = 0;
 #pragma unroll
     for (int v4 = 0; v4 < kPerWarp / 128; ++v4) {
       const float4 a = reinterpret_cast<const float4*>(sp)[v4 * 32 + lane];
       const float4 c = HQ ? reinterpret_cast<const float4*>(sq)[v4 * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-      add_entry<HQ>(a.x, c.x, sh, sl);
-      add_entry<HQ>(a.y, c.y, sh, sl);
-      add_entry<HQ>(a.z, c.z, sh, sl);
-      add_entry<HQ>(a.w, c.w, sh, sl);
+      add_entry_unit<HQ>(a.x, c.x, fh, fl, bits);
+      add_entry_unit<HQ>(a.y, c.y, fh, fl, bits);
+      add_entry_unit<HQ>(a.z, c.z, fh, fl, bits);
+      add_entry_unit<HQ>(a.w, c.w, fh, fl, bits);
     }
+    if (__any_sync(0xffffffffu, bits > kOneBits)) {
+      // a mass outside [0, 1] in the warp's 512 entries: all of them again
+      // with the clamps
+      fh = fl = 0;
+#pragma unroll 1
+      for (int v4 = 0; v4 < kPerWarp / 128; ++v4) {
+        const float4 a = reinterpret_cast<const float4*>(sp)[v4 * 32 + lane];
+        const float4 c = HQ ? reinterpret_cast<const float4*>(sq)[v4 * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+        add_entry<HQ>(a.x, c.x, fh, fl);
+        add_entry<HQ>(a.y, c.y, fh, fl);
+        add_entry<HQ>(a.z, c.z, fh, fl);
+        add_entry<HQ>(a.w, c.w, fh, fl);
+      }
+    }
+    sh += fh;
+    sl += fl;
   } else {
     for (int e = lane; e < nw; e += 32) {
       const float pv = e < copied_here ? sp[e] : __ldg(gp + e);
@@ -160,15 +214,22 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* csum = reinterpret_cast<uint64_t*>(smem_raw + kRingBytes);  // [chunk][warp]
   __shared__ uint64_t full[kStages], empty[kStages];
   __shared__ uint64_t part[kWarps];   // each consumer warp's total over this CTA's half
-  __shared__ uint64_t halves[kCluster];
-  __shared__ uint64_t wtot[kWarps + 1];  // warp totals of the final scan (every warp takes part)
-  __shared__ int state[2];            // [0] first position not kept, [1] its candidate is possible
+  // the two halves' totals of a row sum, by the parity of the sum's round:
+  // each CTA writes its total into both CTAs' copy, so one cluster barrier
+  // makes both visible (a copy is written again two rounds later, after the
+  // next round's barrier, which both CTAs reach only after reading it)
+  __shared__ uint64_t halves[2][kCluster];
+  __shared__ uint64_t wtot[2][kWarps + 1];  // warp totals of the final scan (every warp takes part)
+  __shared__ uint64_t pick_c;  // the draw's prefix before the warp range it lies in
+  __shared__ int pick_w;
+  // [0] first position not kept, [1] its candidate is possible, [2] the
+  // row's 32 random bits (loaded with the candidates, not at the draw)
+  __shared__ int state[3];
   cg::cluster_group cl = cg::this_cluster();
   const unsigned rank = cl.block_rank();
   const int b = blockIdx.x / kCluster;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t s = (uint32_t)u_smp[(int64_t)b * s_sb];
   if (threadIdx.x == 0) {
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&full[st], 1);
@@ -177,12 +238,19 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   __syncthreads();
+  // this CTA has started; the matching wait precedes the first write into
+  // the peer's shared memory
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
   // this CTA's half of the row: slots of kSlot entries, chunks of m slots
   const int64_t c_lo = half_cut(V, rank), c_hi = half_cut(V, rank + 1);
-  const int64_t n_slots = (c_hi - c_lo + kSlot - 1) / kSlot;
-  const int64_t m = (n_slots + kMaxChunks - 1) / kMaxChunks < 1 ? 1 : (n_slots + kMaxChunks - 1) / kMaxChunks;
-  int64_t ring_pos = 0;  // slots streamed so far (ring slot and phase)
+  // (32-bit slot counts: a half has at most 2^18 slots, and the rows a call
+  // streams, at most k + 2 of them, fit in device memory)
+  const int n_slots = (int)((c_hi - c_lo + kSlot - 1) / kSlot);
+  const int m = max(1, (n_slots + kMaxChunks - 1) / kMaxChunks);
+  uint32_t ring_pos = 0;  // slots streamed so far (ring slot and phase)
+  int round = 0;          // row sums done
+  uint64_t h_first = 0;   // the first half's total in the last row sum
   bool ok = true;
 
   // Z of one row: each CTA sums its half through the ring, the pair
@@ -192,11 +260,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == kProducer) {
       if (lane == 0 && vec_) {
         const uint64_t pol = policy_evict_first();  // the rows are read once
-        for (int64_t u = 0; u < n_slots; ++u) {
-          const int64_t g = ring_pos + u;
+        for (int u = 0; u < n_slots; ++u) {
+          const uint32_t g = ring_pos + (uint32_t)u;
           const int st = (int)(g % kStages);
-          if (g >= kStages && !mbar_wait(&empty[st], (uint32_t)(((g / kStages) - 1) & 1))) { ok = false; break; }
-          const int64_t x0 = c_lo + u * kSlot;
+          if (g >= kStages && !mbar_wait(&empty[st], ((g / kStages) - 1) & 1)) { ok = false; break; }
+          const int64_t x0 = c_lo + (int64_t)u * kSlot;
           const uint32_t bytes = (uint32_t)((min((int64_t)kSlot, c_hi - x0) & ~(int64_t)3) * 4);
           mbar_arrive_expect_tx(&full[st], hq ? 2 * bytes : bytes);
           if (bytes > 0) {
@@ -208,14 +276,15 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     } else {
       uint64_t tot = 0;
       int sh = 0, sl = 0;
-      for (int64_t u = 0; u < n_slots; ++u) {
-        const int64_t g = ring_pos + u;
+      int ch = 0, in_ch = 0;  // chunk of the slot, slots of the chunk done
+      for (int u = 0; u < n_slots; ++u) {
+        const uint32_t g = ring_pos + (uint32_t)u;
         const int st = (int)(g % kStages);
-        const int64_t x0 = c_lo + u * kSlot;
+        const int64_t x0 = c_lo + (int64_t)u * kSlot;
         const int64_t xw = x0 + warp * kPerWarp;  // this warp's 512 entries
         const int64_t nw = min((int64_t)kPerWarp, c_hi - xw);  // (<= 0: none)
         if (vec_) {
-          if (!__all_sync(0xffffffffu, ok && mbar_wait(&full[st], (uint32_t)((g / kStages) & 1)))) ok = false;
+          if (!__all_sync(0xffffffffu, ok && mbar_wait(&full[st], (g / kStages) & 1))) ok = false;
           // slot entries [0, copied) came by copy; a ragged end of <= 3 by plain loads
           const int copied = (int)(min((int64_t)kSlot, c_hi - x0) & ~(int64_t)3);
           const int here = (int)max((int64_t)0, min((int64_t)kPerWarp, (int64_t)copied - warp * kPerWarp));
@@ -237,37 +306,46 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         }
         // fold the lane counters (16 entries per slot: every 32 slots at
         // least) and record the warp's running total at each chunk's end
-        const bool chunk_end = (u + 1) % m == 0 || u + 1 == n_slots;
+        const bool chunk_end = ++in_ch == m || u + 1 == n_slots;
         if (chunk_end || ((u + 1) & 31) == 0) {
           uint64_t cs = combine(sh, sl);
           sh = sl = 0;
 #pragma unroll
           for (int off = 16; off >= 1; off >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, off);
           tot += cs;
-          if (chunk_end && lane == 0) csum[(u / m) * kWarps + warp] = tot;
+          if (chunk_end && lane == 0) csum[ch * kWarps + warp] = tot;
+        }
+        if (chunk_end) {
+          ++ch;
+          in_ch = 0;
         }
       }
       if (lane == 0) part[warp] = tot;
     }
     if (warp == kProducer && lane == 0 && vec_) {
       // the copies this thread issued have landed before anything moves on
-      for (int64_t g = max(ring_pos, ring_pos + n_slots - kStages); g < ring_pos + n_slots; ++g)
-        if (!mbar_wait(&full[g % kStages], (uint32_t)((g / kStages) & 1))) ok = false;
+      const uint32_t end = ring_pos + (uint32_t)n_slots;
+      for (uint32_t g = n_slots > kStages ? end - kStages : ring_pos; g < end; ++g)
+        if (!mbar_wait(&full[g % kStages], (g / kStages) & 1)) ok = false;
     }
-    if (vec_) ring_pos += n_slots;  // (the barriers' phases advance only on this path)
+    if (vec_) ring_pos += (uint32_t)n_slots;  // (the barriers' phases advance only on this path)
     __syncthreads();
+    uint64_t* hv = halves[round & 1];
+    if (round == 0) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // the peer has started
     if (threadIdx.x == 0) {
       uint64_t h = 0;
       for (int w = 0; w < kWarps; ++w) h += part[w];
-      halves[rank] = h;
+      hv[rank] = h;
+      *cl.map_shared_rank(&hv[rank], rank ^ 1u) = h;
     }
-    cl.sync();  // both halves' totals are written
-    if (threadIdx.x == 0) halves[rank ^ 1u] = cl.map_shared_rank(halves, rank ^ 1u)[rank ^ 1u];
-    cl.sync();  // the remote read is done before either CTA rewrites halves[] or exits
-    return halves[0] + halves[1];
+    cl.sync();  // both totals are in both CTAs
+    ++round;
+    h_first = hv[0];
+    return hv[0] + hv[1];
   };
 
   int i = 0;
+  uint32_t s = 0;
   const float* pr = nullptr;
   const float* qr = nullptr;
   bool vec = false;
@@ -276,6 +354,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     // ---- in-order acceptance, up to the first rejection: warp 0 tests 32
     // candidates at once (their loads in parallel), the lowest failing lane wins
     if (warp == 0) {
+      const int sv = lane == 0 ? u_smp[(int64_t)b * s_sb] : 0;
       int j = k, valid = 0;
       for (int j0 = i; j0 < k; j0 += 32) {
         const int jj = j0 + lane;
@@ -302,11 +381,13 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         state[0] = j;
         state[1] = valid;
+        state[2] = sv;
       }
     }
     __syncthreads();
     i = state[0];
     const bool valid = state[1] != 0;
+    s = (uint32_t)state[2];
     // the distribution to draw from: the residual at the rejected position,
     // or the target one past the candidates
     pr = p + (int64_t)b * p_sb + (int64_t)i * p_si;
@@ -336,69 +417,89 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
   const uint64_t T = __umul64hi((uint64_t)s << 32, Z);  // floor(s Z / 2^32) < Z
 
   // ---- the half holding T; its CTA finishes the draw from its own sums ----
-  const unsigned owner = T < halves[0] ? 0u : 1u;
+  const unsigned owner = T < h_first ? 0u : 1u;
   if (rank != owner) return;
-  uint64_t c = owner == 0 ? 0 : halves[0];
-  // the chunk, then (one-slot chunks) the warp's 512 entries holding T; the
-  // chunk sums are differences of the warps' running totals
-  const int64_t n_ch = (n_slots + m - 1) / m;
-  int64_t ch = 0;
-  uint64_t prev[kWarps];
+  uint64_t c = owner == 0 ? 0 : h_first;
+  // the chunk holding T: the half's running total at a chunk's end is the
+  // sum of the warps' running totals there, and these grow along the
+  // vocabulary, so the chunk is the number of chunk ends at or below T (one
+  // thread per chunk end; the last chunk holds T if no earlier one does)
+  const int n_ch = (n_slots + m - 1) / m;
+  auto chunk_end = [&](int x) -> uint64_t {  // (x < 0: before the first chunk)
+    uint64_t t = 0;
+    if (x >= 0) {
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) prev[w] = 0;
-  for (; ch < n_ch - 1; ++ch) {
-    uint64_t cs = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) cs += csum[ch * kWarps + w] - prev[w];
-    if (c + cs > T) break;
-    c += cs;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) prev[w] = csum[ch * kWarps + w];
-  }
-  int64_t L0 = c_lo + ch * m * kSlot;
-  int64_t L1 = min(c_hi, L0 + m * kSlot);
-  if (m == 1) {
-    int w = 0;
-    for (; w < kWarps - 1; ++w) {
-      const uint64_t ws = csum[ch * kWarps + w] - prev[w];
-      if (c + ws > T) break;
-      c += ws;
+      for (int w = 0; w < kWarps; ++w) t += csum[x * kWarps + w];
     }
-    L0 = min(c_hi, L0 + (int64_t)w * kPerWarp);
+    return t;
+  };
+  const int ch = __syncthreads_count((int)threadIdx.x < n_ch - 1 && c + chunk_end((int)threadIdx.x) <= T);
+  int64_t L0 = c_lo + (int64_t)ch * m * kSlot;
+  int64_t L1 = min(c_hi, L0 + (int64_t)m * kSlot);
+  if (m > 1) {
+    c += chunk_end(ch - 1);
+  } else {
+    // one-slot chunks: the warp whose 512 entries hold T.  Warp 0, lane w:
+    // warp w's running totals before and at the chunk's end; their sum over
+    // the lanes is the chunk's base, their differences the warps' amounts,
+    // whose inclusive prefix passes T - base first at the warp sought
+    if (warp == 0) {
+      uint64_t before = 0, amount = 0;
+      if (lane < kWarps) {
+        before = ch > 0 ? csum[(ch - 1) * kWarps + lane] : 0;
+        amount = csum[ch * kWarps + lane] - before;
+      }
+      uint64_t base = before;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) base += __shfl_xor_sync(0xffffffffu, base, off);
+      base += c;
+#pragma unroll
+      for (int off = 1; off < kWarps; off <<= 1) {
+        const uint64_t y = __shfl_up_sync(0xffffffffu, amount, off);
+        if (lane >= off) amount += y;
+      }
+      const int w = __popc(__ballot_sync(0xffffffffu, lane < kWarps - 1 && base + amount <= T));
+      const uint64_t below = __shfl_sync(0xffffffffu, amount, w > 0 ? w - 1 : 0);
+      if (lane == 0) {
+        pick_w = w;
+        pick_c = base + (w > 0 ? below : 0);
+      }
+    }
+    __syncthreads();
+    c = pick_c;
+    L0 = min(c_hi, L0 + (int64_t)pick_w * kPerWarp);
     L1 = min(c_hi, L0 + kPerWarp);
   }
-  // ---- one scan of [L0, L1) over the whole CTA, kThreads entries at a time
-  // (prefix sums grow along the vocabulary, so the entries past T are a
-  // suffix: the first of them is the count of those before it) ----
-  int64_t found = -1;
-  for (int64_t x0 = L0; x0 < L1; x0 += kThreads) {
+  // ---- one scan of [L0, L1), kThreads entries a round: an inclusive prefix
+  // over each warp's lanes, then over the warps' totals.  T lies in the round
+  // whose total passes it, in the one warp whose range holds it, at the lowest
+  // lane whose prefix passes it; that lane writes the result ----
+  for (int64_t x0 = L0, r = 0; x0 < L1; x0 += kThreads, ++r) {
     const int64_t x = x0 + threadIdx.x;
     uint64_t v = x < L1 ? weight(pr, qr, x) : 0;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {  // inclusive prefix sum over the lanes
+    for (int off = 1; off < 32; off <<= 1) {
       const uint64_t y = __shfl_up_sync(0xffffffffu, v, off);
       if (lane >= off) v += y;
     }
-    if (lane == 31) wtot[warp] = v;
+    // (two buffers: a round's totals are rewritten two rounds later, after
+    // the next round's barrier, which follows every read of them)
+    uint64_t* wt = wtot[r & 1];
+    if (lane == 31) wt[warp] = v;
     __syncthreads();
-    uint64_t before = c, chunk = 0;
+    uint64_t before = c, total = 0;
 #pragma unroll
     for (int w2 = 0; w2 < kWarps + 1; ++w2) {
-      before += w2 < warp ? wtot[w2] : 0;
-      chunk += wtot[w2];
+      before += w2 < warp ? wt[w2] : 0;
+      total += wt[w2];
     }
-    const int nvalid = (int)min((int64_t)kThreads, L1 - x0);
-    // (the barrier also ends every thread's reads of wtot)
-    const int ahead = __syncthreads_count(x < L1 && before + v <= T);
-    if (ahead < nvalid) {
-      found = x0 + ahead;
-      break;
+    const unsigned past = __ballot_sync(0xffffffffu, before + v > T);
+    if (before <= T && T < before + wt[warp] && lane == __ffs(past) - 1) {
+      n_out[(int64_t)b * n_sb] = i;
+      tok_out[(int64_t)b * t_sb] = (int32_t)x;  // T < Z: some round holds it
     }
-    c += chunk;
-  }
-  if (threadIdx.x == 0) {
-    n_out[(int64_t)b * n_sb] = i;
-    tok_out[(int64_t)b * t_sb] = (int32_t)found;  // found >= 0: T < Z
+    if (c + total > T) break;
+    c += total;
   }
 }
 

@@ -945,3 +945,32 @@ def test_a_wait_that_runs_out_is_reported_and_the_next_call_is_correct():
         o = out.double().cpu().numpy().reshape(-1, s.d)
         l = lse.double().cpu().numpy().reshape(-1)
         assert_parity(o, l, run_oracle(inp), BF16_TOL_O, BF16_TOL_L)
+
+
+# ------------------------------------------------------------ guard bands
+
+@pytest.mark.parametrize("name", list(workloads.SMALL))
+def test_outputs_stay_inside_their_views(name):
+    """out and lse as views inside larger buffers filled with a sentinel
+    (padding on every dimension): every kernel path writes its view and
+    nothing around it."""
+    s = workloads.spec(name, small=True)
+    inp = workloads.generate(s)
+    g = to_dev(inp)
+    sentinel = -7777.0
+    obuf = torch.full((s.B + 1, s.Hq + 2, s.Tq + 3, s.d + 8), sentinel, device="cuda")
+    lbuf = torch.full((s.B + 1, s.Hq + 2, s.Tq + 5), sentinel, device="cuda")
+    out = obuf[1:, 1:-1, 2:-1, 4:-4]
+    lse = lbuf[:-1, 2:, 3:-2]
+    blkattn.fwd(g["q"], g["k"], g["v"], g["seqlens"], g["qpos"], g["bias"], g["scale"], out, lse,
+                tree=g.get("tree"), window=g.get("window", 0))
+    torch.cuda.synchronize()
+    assert blkattn.check_device_error() == 0
+    omask = torch.ones_like(obuf, dtype=torch.bool)
+    omask[1:, 1:-1, 2:-1, 4:-4] = False
+    lmask = torch.ones_like(lbuf, dtype=torch.bool)
+    lmask[:-1, 2:, 3:-2] = False
+    assert bool((obuf[omask] == sentinel).all()) and bool((lbuf[lmask] == sentinel).all())
+    o = out.double().cpu().numpy().reshape(-1, s.d)
+    l = lse.double().cpu().numpy().reshape(-1)
+    assert_parity(o, l, run_oracle(inp), *tols(s))

@@ -182,3 +182,38 @@ def test_more_candidates_than_a_warp_tests_at_once():
     np.testing.assert_array_equal(n, on)
     np.testing.assert_array_equal(tok, ot)
     assert np.all(n >= 35)
+
+
+def test_masses_outside_the_unit_interval():
+    """Rows of a full-size vocabulary with a few masses outside [0, 1] (-0,
+    negatives, above 1 and 2, NaN, inf) among ordinary ones: the slots holding
+    them take the clamped form of the weights, the others the short form, and
+    the draw is the oracle's."""
+    B, k, V = 8, 2, 128256
+    rng = np.random.default_rng(11)
+    p = rng.dirichlet(np.ones(V) * 0.5, size=(B, k + 1)).astype(np.float32)
+    q = rng.dirichlet(np.ones(V) * 0.5, size=(B, k)).astype(np.float32)
+    draft = rng.integers(0, V, size=(B, k)).astype(np.int32)
+    u = rng.random((B, k), dtype=np.float32)
+    odd = np.array([-0.0, -1e-3, 1.5, 3.0, np.nan, np.inf, -np.inf, 2.0, 1.0000001], dtype=np.float32)
+    for b in range(B):
+        if b >= 5:  # every candidate kept: the next target row is drawn from
+            u[b] = 0.0
+            for i in range(k):
+                p[b, i, draft[b, i]] = max(p[b, i, draft[b, i]], np.float32(1e-6))
+                q[b, i, draft[b, i]] = max(q[b, i, draft[b, i]], np.float32(1e-6))
+        else:  # the first candidate is rejected: its residual is drawn from
+            p[b, 0, draft[b, 0]] = 0.0
+            q[b, 0, draft[b, 0]] = max(q[b, 0, draft[b, 0]], np.float32(1e-3))
+        if b % 2 == 0:
+            continue  # even rows stay in range
+        for j, x in enumerate(rng.choice(V, size=6, replace=False)):
+            if x != draft[b, 0]:
+                (p if j % 2 == 0 else q)[b, 0, x] = odd[(b + j) % len(odd)]
+        p[b, k, rng.integers(V)] = odd[b % len(odd)]
+    s = rng.integers(0, 2**32, size=B, dtype=np.uint64).astype(np.uint32).view(np.int32)
+    t = [torch.from_numpy(np.ascontiguousarray(a)) for a in (p, q, draft, u, s)]
+    n, tok, on, ot = run_both(*t)
+    np.testing.assert_array_equal(n, on)
+    np.testing.assert_array_equal(tok, ot)
+    assert np.all(n[:5] == 0) and np.all(n[5:] == k)
