@@ -543,23 +543,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      uint4 val[NR / 2];
+      // query rows, 128-byte swizzled K-major (rows of 64 dims), by 16-byte
+      // asynchronous copies that bypass the registers: all of them are in
+      // flight at once whatever the row count (rows past the unit's end are
+      // zero-filled); they complete before the rows are announced below
 #pragma unroll
       for (int it = 0; it < NR / 2; ++it) {
         // chunk (lane & 15) of row 2 it + (lane >> 4), described by lane (row & 31)
         const int r = 2 * it + (lane >> 4);
+        const int c = lane & 15;
         const int set = (2 * it) >> 5;  // rows of this iteration are all < 32 or all >= 32
         const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(
             __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(qrow[set]), r & 31));
         const bool rr = __shfl_sync(0xffffffffu, real[set], r & 31);
-        val[it] = rr ? __ldg(reinterpret_cast<const uint4*>(src) + (lane & 15)) : make_uint4(0, 0, 0, 0);
-      }
-      // query rows, 128-byte swizzled K-major (rows of 64 dims)
-#pragma unroll
-      for (int it = 0; it < NR / 2; ++it) {
-        const int r = 2 * it + (lane >> 4);
-        const int c = lane & 15;
-        *reinterpret_cast<uint4*>(qs + (c >> 3) * L::kQBox + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = val[it];
+        cp_async_16(smem_u32(qs + (c >> 3) * L::kQBox + r * 128 + (((c & 7) ^ (r & 7)) << 4)),
+                    rr ? static_cast<const void*>(reinterpret_cast<const uint4*>(src) + c) : p.q, rr ? 16u : 0u);
       }
       // integer facts of the rows
       const int len = len_raw < 0 ? 0 : (len_raw > p.Tmax ? p.Tmax : len_raw);
@@ -604,6 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         rf.tree_base = p.tree != nullptr ? len - p.Tq : 0x7fffffff;
         rf.win_max = wmax;
       }
+      cp_async_wait_all();  // this lane's query-row copies have landed
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q rows -> tensor core
       __syncwarp();
       if (lane == 0) mbar_arrive(&q_full[qb]);
@@ -768,6 +767,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.lse[pf.loff[k]] = (m == kNegInf) ? kNegInf : (m + __log2f(s_lfin[k])) * kLn2;
         }
       } else {
+        // (kept in L2 until the fold reads it: the key stream passing through
+        // meanwhile is marked evict-first)
+        const uint64_t keep = policy_evict_last();
         // this CTA's partial state of the unit, then the last of the unit's
         // CTAs to get here folds all of them (eqs. 33.4-33.5, in CTA order)
         const int64_t slot = (int64_t)blockIdx.x + unit;
@@ -775,11 +777,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < NH; ++r) {
           const int row = c0 + r;
           if (row >= rr) break;
-          p.ws_u[((slot * R + row) * D) + k] = u[r];
+          st_global_hint(p.ws_u + ((slot * R + row) * D) + k, u[r], keep);
         }
         if (half == 0 && k < rr) {
-          p.ws_m[slot * R + k] = s_mfin[k];
-          p.ws_l[slot * R + k] = s_lfin[k];
+          st_global_hint(p.ws_m + slot * R + k, s_mfin[k], keep);
+          st_global_hint(p.ws_l + slot * R + k, s_lfin[k], keep);
         }
         __threadfence();  // the partial state is visible before the count says so
         bar_sync(kBarRows, kKeyThreads);

@@ -83,6 +83,19 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return pol;
 }
 
+// L2 policy: small data read again much later in the same launch (while a
+// stream marked evict-first passes through the cache) is evicted last.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// A global store with an L2 cache policy.
+__device__ __forceinline__ void st_global_hint(float* ptr, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(policy) : "memory");
+}
+
 // One bulk asynchronous global->shared copy, completion counted in bytes on
 // the mbarrier.  dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
@@ -93,6 +106,14 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+
+// 16-byte asynchronous global->shared copy that bypasses L1 and the
+// registers; src_bytes = 0 zero-fills the destination (src is not read).
+// Completion: cp_async_wait_all by the same thread.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Tiled TMA load of one box of a 4-D tensor map into shared memory.  The map
 // must be a __grid_constant__ kernel parameter; c0 * element size must be a
