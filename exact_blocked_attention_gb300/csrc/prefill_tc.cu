@@ -560,25 +560,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           // dims there as four 4 KB boxes of 32 dims in the 128-byte swizzled
           // layout of the output map (16-byte chunk c of row r at c ^ (r mod
           // 8): conflict-free) and one lane stores them with tiled TMA.
+          // One 32-dim box at a time (a short loop body for code that runs
+          // once per CTA).
           unsigned char* stage = sm + (x == 0 ? kOffK : kOffV) + (warp & 3) * 4 * 4096;
-          uint32_t r0[32], r1[32], r2[32], r3[32];
-          tc::ld32(tl + kColO, r0);
-          tc::ld32(tl + kColO + 32, r1);
-          tc::ld32(tl + kColO + 64, r2);
-          tc::ld32(tl + kColO + 96, r3);
-          tc::wait_ld();
-          auto put = [&](int q4, const uint32_t(&r)[32]) {
+#pragma unroll 1
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t r[32];
+            tc::ld32(tl + kColO + 32 * q4, r);
+            tc::wait_ld();
             float4* box = reinterpret_cast<float4*>(stage + q4 * 4096);
 #pragma unroll
             for (int c = 0; c < 8; ++c)
               box[lane * 8 + (c ^ (lane & 7))] =
                   make_float4(__uint_as_float(r[4 * c]) * inv, __uint_as_float(r[4 * c + 1]) * inv,
                               __uint_as_float(r[4 * c + 2]) * inv, __uint_as_float(r[4 * c + 3]) * inv);
-          };
-          put(0, r0);
-          put(1, r1);
-          put(2, r2);
-          put(3, r3);
+          }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // staged rows -> TMA
           __syncwarp();
           const int row_w = (2 * pair + x) * BM + 32 * (warp & 3);
