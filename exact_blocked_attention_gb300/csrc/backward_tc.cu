@@ -89,6 +89,40 @@ constexpr int kMaxQTiles = 1024;                              // query tiles per
 constexpr int kOffEnds = kOffFacts + 2 * 128 * 16;            // dK/dV: int [kMaxQTiles] row ends per query tile
 constexpr int kOffStarts = kOffEnds + kMaxQTiles * 4;         // dK/dV (window): smallest row start per query tile
 constexpr int kSmemBytes = kOffStarts + kMaxQTiles * 4 + 1024;  // + slack to align to 1024
+// Epilogue staging (in a ring the finished products no longer read): per
+// compute warp its 32 rows of one group's 64 columns, a row padded to 68
+// floats (conflict-free both ways); group g's warps in ring g.
+constexpr int kStageRow = HT + 4;
+constexpr int kStageWarp = 32 * kStageRow * 4;
+static_assert(4 * kStageWarp <= STAGES * kTileBytes, "staging fits a ring");
+
+// One compute warp's 32 rows x 64 columns of an fp32 accumulator (TMEM
+// columns col, col + 32) times mul, to rows dst0 + r * row_stride of global
+// memory, the first `rows` of them: staged through shared memory so that the
+// global stores are 16 lanes to a row, 256 contiguous bytes each.
+__device__ __forceinline__ void store_rows(uint32_t col, float mul, float* stg, float* dst0, int64_t row_stride,
+                                           int rows, int lane) {
+#pragma unroll 1
+  for (int q2 = 0; q2 < 2; ++q2) {
+    uint32_t r[32];
+    tc::ld32(col + 32 * q2, r);
+    tc::wait_ld();
+#pragma unroll
+    for (int c = 0; c < 32; c += 4)
+      *reinterpret_cast<float4*>(stg + lane * kStageRow + 32 * q2 + c) =
+          make_float4(__uint_as_float(r[c]) * mul, __uint_as_float(r[c + 1]) * mul, __uint_as_float(r[c + 2]) * mul,
+                      __uint_as_float(r[c + 3]) * mul);
+  }
+  __syncwarp();
+#pragma unroll 4
+  for (int it = 0; it < 16; ++it) {
+    const int r = 2 * it + (lane >> 4);
+    if (r < rows)
+      *reinterpret_cast<float4*>(dst0 + r * row_stride + 4 * (lane & 15)) =
+          *reinterpret_cast<const float4*>(stg + r * kStageRow + 4 * (lane & 15));
+  }
+  __syncwarp();  // the staging rows are read before they are written again
+}
 
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
@@ -563,21 +597,14 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
     if (!ok) {
       if (lane == 0) record_error(p.err, kErrTimeout);
     } else {
-      // G_Q: this group stores dims [64 g, 64 g + 64)
+      // G_Q: this group stores dims [64 g, 64 g + 64) of the warp's rows,
+      // staged in the K/V rings (every product has completed)
       tc::fence_after();
-#pragma unroll 1
-      for (int q2 = 0; q2 < 2; ++q2) {
-        uint32_t r[32];
-        tc::ld32(tl + 256 + HT * grp + 32 * q2, r);
-        tc::wait_ld();
-        if (my_row) {
-#pragma unroll
-          for (int c = 0; c < 32; c += 4)
-            *reinterpret_cast<float4*>(dq_row + 32 * q2 + c) =
-                make_float4(__uint_as_float(r[c]) * p.scale, __uint_as_float(r[c + 1]) * p.scale,
-                            __uint_as_float(r[c + 2]) * p.scale, __uint_as_float(r[c + 3]) * p.scale);
-        }
-      }
+      const int r0 = i0 + 32 * (warp & 3);
+      store_rows(tl + 256 + HT * grp, p.scale,
+                 reinterpret_cast<float*>(sm + (grp == 0 ? kOffR0 : kOffR1) + (warp & 3) * kStageWarp),
+                 p.dq + (int64_t)b * p.dq_sb + (int64_t)h * p.dq_sh + (int64_t)r0 * p.dq_si + grp * HT, p.dq_si,
+                 min(32, p.Tq - r0), lane);
     }
   }
 
@@ -894,27 +921,19 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
           *reinterpret_cast<float4*>(dk_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     } else {
-      // this group stores dims [64 g, 64 g + 64) of G_V and G_K (the
-      // tensor-memory loads are warp-collective: every lane takes part)
+      // this group stores dims [64 g, 64 g + 64) of G_V and G_K for the
+      // warp's keys, staged in the Q/G_O rings (every product has completed;
+      // the tensor-memory loads are warp-collective: every lane takes part)
       tc::fence_after();
-#pragma unroll 1
-      for (int part = 0; part < 2; ++part) {
-        float* dst = part == 0 ? dv_row : dk_row;
-        const float mul = part == 0 ? 1.f : p.scale;
-#pragma unroll 1
-        for (int q2 = 0; q2 < 2; ++q2) {
-          uint32_t r[32];
-          tc::ld32(tl + 256 + 128 * part + HT * grp + 32 * q2, r);
-          tc::wait_ld();
-          if (key < p.Tmax) {
-#pragma unroll
-            for (int c = 0; c < 32; c += 4)
-              *reinterpret_cast<float4*>(dst + 32 * q2 + c) =
-                  make_float4(__uint_as_float(r[c]) * mul, __uint_as_float(r[c + 1]) * mul,
-                              __uint_as_float(r[c + 2]) * mul, __uint_as_float(r[c + 3]) * mul);
-          }
-        }
-      }
+      const int key_w = k0 + 32 * (warp & 3);
+      float* stg = reinterpret_cast<float*>(sm + (grp == 0 ? kOffR0 : kOffR1) + (warp & 3) * kStageWarp);
+      const int rows = min(32, p.Tmax - key_w);
+      store_rows(tl + 256 + HT * grp, 1.f, stg,
+                 p.dv + (int64_t)b * p.dv_sb + (int64_t)hk * p.dv_sh + (int64_t)key_w * p.dv_sj + grp * HT, p.dv_sj,
+                 rows, lane);
+      store_rows(tl + 256 + 128 + HT * grp, p.scale, stg,
+                 p.dk + (int64_t)b * p.dk_sb + (int64_t)hk * p.dk_sh + (int64_t)key_w * p.dk_sj + grp * HT, p.dk_sj,
+                 rows, lane);
     }
   }
 
