@@ -554,7 +554,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         tc::fence_after();
         const float inv = (m_ref == kNegInf) ? 0.f : 1.f / l;
-        if (p.o_tma) {
+        if (p.o_tma && !WIN) {
+          // Every MMA has completed (drain), so the K (query tile 0) or V
+          // (query tile 1) ring is free.  Each warp stages its 32 rows, 64
+          // dims at a time (rows padded to 68 floats: conflict-free both
+          // ways), and stores them back 16 lanes to a row (256 contiguous
+          // bytes per row per store instruction).  (Measured against the
+          // tiled-TMA form below: faster for full causal tiles, slower for
+          // the short windowed CTAs, which keep TMA.)
+          constexpr int kRow = 68;
+          float* stg = reinterpret_cast<float*>(sm + (x == 0 ? kOffK : kOffV) + (warp & 3) * 32 * kRow * 4);
+          const int r0 = (2 * pair + x) * BM + 32 * (warp & 3);
+          const int rows = min(32, p.Tq - r0);
+          float* dst0 = static_cast<float*>(p.out) + (int64_t)b * p.o_sb + (int64_t)h * p.o_sh + (int64_t)r0 * p.o_si;
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+#pragma unroll 1
+            for (int q2 = 0; q2 < 2; ++q2) {
+              uint32_t r[32];
+              tc::ld32(tl + kColO + 64 * half + 32 * q2, r);
+              tc::wait_ld();
+#pragma unroll
+              for (int c = 0; c < 32; c += 4)
+                *reinterpret_cast<float4*>(stg + lane * kRow + 32 * q2 + c) =
+                    make_float4(__uint_as_float(r[c]) * inv, __uint_as_float(r[c + 1]) * inv,
+                                __uint_as_float(r[c + 2]) * inv, __uint_as_float(r[c + 3]) * inv);
+            }
+            __syncwarp();
+#pragma unroll 4
+            for (int it = 0; it < 16; ++it) {
+              const int rr = 2 * it + (lane >> 4);
+              if (rr < rows)
+                *reinterpret_cast<float4*>(dst0 + rr * p.o_si + 64 * half + 4 * (lane & 15)) =
+                    *reinterpret_cast<const float4*>(stg + rr * kRow + 4 * (lane & 15));
+            }
+            __syncwarp();
+          }
+        } else if (p.o_tma) {
           // Every MMA has completed (drain), so the K (query tile 0) or V
           // (query tile 1) ring is free.  Each warp stages its 32 rows x 128
           // dims there as four 4 KB boxes of 32 dims in the 128-byte swizzled
@@ -608,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (my_row) p.lse[lse_idx] = (m_ref == kNegInf) ? kNegInf : (m_ref + __log2f(l)) * kLn2;
         // the staging buffer is released with the CTA: the stores must have
         // read it (no-op for a lane without stores)
-        if (p.o_tma && lane == 0) bulk_wait_read();
+        if (WIN && p.o_tma && lane == 0) bulk_wait_read();
       }
     }
   }
