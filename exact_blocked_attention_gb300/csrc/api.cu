@@ -259,7 +259,10 @@ int g_map_next = 0;
 // 4-D map over a view [B, H, T, d] (element strides, last = 1): dims
 // {d, T, H, B}, box {box_cols, box_rows, 1, 1}, 128-byte swizzle (box_cols *
 // element size = 128 bytes), zero fill past T.
-int tensor_map(int dev, const blkattn_tensor* t, int box_cols, int box_rows, const CUtensorMap** out) {
+// The map is copied into *out: a cache entry may be replaced by the next
+// lookup of the same call (a hit followed by a miss landing on that entry),
+// so no caller keeps a pointer into the cache.
+int tensor_map(int dev, const blkattn_tensor* t, int box_cols, int box_rows, CUtensorMap* out) {
   MapKey key;
   std::memset(&key, 0, sizeof key);
   key.dev = dev;
@@ -271,7 +274,7 @@ int tensor_map(int dev, const blkattn_tensor* t, int box_cols, int box_rows, con
   for (int i = 0; i < 3; ++i) key.strides[i] = t->strides[i];
   for (int i = 0; i < kMapCache; ++i)
     if (g_maps[i].used && g_maps[i].key == key) {
-      *out = &g_maps[i].map;
+      *out = g_maps[i].map;
       return BLKATTN_OK;
     }
   int st = get_encoder();
@@ -296,12 +299,12 @@ int tensor_map(int dev, const blkattn_tensor* t, int box_cols, int box_rows, con
   }
   e.key = key;
   e.used = true;
-  *out = &e.map;
+  *out = e.map;
   return BLKATTN_OK;
 }
 
 // bf16 K/V cache or Q: boxes of 64 dims (128 bytes) x box_rows rows.
-int kv_tensor_map(int dev, const blkattn_tensor* t, int box_rows, const CUtensorMap** out) {
+int kv_tensor_map(int dev, const blkattn_tensor* t, int box_rows, CUtensorMap* out) {
   return tensor_map(dev, t, 64, box_rows, out);
 }
 
@@ -537,8 +540,7 @@ int launch_fwd(const FwdParams& p, const Checked& c, const Plan& pl, const blkat
   if (pl.cfg.kernel == blkattn::Kernel::DecodeTc) {
     int dev = 0;
     if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return cuda_fail(e);
-    const CUtensorMap* mk = nullptr;
-    const CUtensorMap* mv = nullptr;
+    CUtensorMap mk, mv;
     int st = kv_tensor_map(dev, k, 128, &mk);
     if (st != BLKATTN_OK) return st;
     st = kv_tensor_map(dev, v, 128, &mv);
@@ -548,12 +550,11 @@ int launch_fwd(const FwdParams& p, const Checked& c, const Plan& pl, const blkat
       pt.test_stall_cta = (int)(g_stall_next % pl.ctas);
       g_stall_next = -1;
     }
-    le = blkattn::launch_decode_tc(pt, (int)pl.ctas, *mk, *mv, stream);
+    le = blkattn::launch_decode_tc(pt, (int)pl.ctas, mk, mv, stream);
   } else if (pl.cfg.kernel == blkattn::Kernel::TensorCore || pl.cfg.kernel == blkattn::Kernel::Prefill) {
     int dev = 0;
     if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return cuda_fail(e);
-    const CUtensorMap* mk = nullptr;
-    const CUtensorMap* mv = nullptr;
+    CUtensorMap mk, mv;
     // K/V boxes: 64 keys for the split-KV kernel, 128 for the prefill kernel
     const int kv_rows = (pl.cfg.kernel == blkattn::Kernel::Prefill) ? 128 : 64;
     int st = kv_tensor_map(dev, k, kv_rows, &mk);
@@ -561,21 +562,21 @@ int launch_fwd(const FwdParams& p, const Checked& c, const Plan& pl, const blkat
     st = kv_tensor_map(dev, v, kv_rows, &mv);
     if (st != BLKATTN_OK) return st;
     if (pl.cfg.kernel == blkattn::Kernel::Prefill) {
-      const CUtensorMap* mq = nullptr;
+      CUtensorMap mq;
       st = kv_tensor_map(dev, q, 128, &mq);
       if (st != BLKATTN_OK) return st;
       // whole output tiles by TMA where the output layout allows it
       FwdParams pp = p;
-      const CUtensorMap* mo = mq;  // not read unless pp.o_tma
+      CUtensorMap mo = mq;  // not read unless pp.o_tma
       pp.o_tma = 0;
       if (out_tma_ok(out)) {
         st = tensor_map(dev, out, 32, 32, &mo);
         if (st != BLKATTN_OK) return st;
         pp.o_tma = 1;
       }
-      le = blkattn::launch_prefill_tc(pp, pl.cfg.row_groups, *mq, *mk, *mv, *mo, stream);
+      le = blkattn::launch_prefill_tc(pp, pl.cfg.row_groups, mq, mk, mv, mo, stream);
     } else {
-      le = blkattn::launch_decode_mma(p, (int)c.d, pl.cfg, *mk, *mv, stream);
+      le = blkattn::launch_decode_mma(p, (int)c.d, pl.cfg, mk, mv, stream);
     }
   } else {
     le = blkattn::launch_decode_split(p, c.elt, (int)c.d, pl.cfg, stream);
@@ -751,7 +752,7 @@ int bwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_ten
   const int64_t ws = 2 * al(nrows * 4) + 2 * al(c.B * n_qt * 4);
   st = ensure_workspace(ds, (size_t)(ws > 0 ? ws : 256), stream);
   if (st != BLKATTN_OK) return st;
-  const CUtensorMap *tmk = nullptr, *tmv = nullptr, *tmq = nullptr, *tmg = nullptr;
+  CUtensorMap tmk, tmv, tmq, tmg;
   if ((st = kv_tensor_map(dev, k, 128, &tmk)) != BLKATTN_OK) return st;
   if ((st = kv_tensor_map(dev, v, 128, &tmv)) != BLKATTN_OK) return st;
   if (rows) {
@@ -808,7 +809,7 @@ int bwd_impl(const blkattn_tensor* q, const blkattn_tensor* k, const blkattn_ten
     p.hg_q = (int)clamp((l2 / 2) / kv_head, c.B * c.Hq);
     p.hg_kv = (int)clamp((l2 / 2) / (q_unit > 0 ? q_unit : 1), c.B * c.Hkv);
   }
-  if (cudaError_t e = launch_backward(p, *tmq, *tmg, *tmk, *tmv, stream); e != cudaSuccess) return cuda_fail(e);
+  if (cudaError_t e = launch_backward(p, tmq, tmg, tmk, tmv, stream); e != cudaSuccess) return cuda_fail(e);
   return BLKATTN_OK;
 }
 

@@ -974,3 +974,30 @@ def test_outputs_stay_inside_their_views(name):
     o = out.double().cpu().numpy().reshape(-1, s.d)
     l = lse.double().cpu().numpy().reshape(-1)
     assert_parity(o, l, run_oracle(inp), *tols(s))
+
+
+# ------------------------------------------------------------ tensor-map cache
+
+def test_tensor_maps_stay_valid_when_the_cache_turns_over_inside_a_call():
+    """The library caches TMA descriptors per (tensor, box) in a small ring.
+    One K cache is reused across calls (a cache hit every time) while each
+    call brings a fresh V (a miss, written at the ring's next position); after
+    at most one turn of the ring that miss lands on the very entry K was found
+    in, during the same call.  Every call must still read its own K and V."""
+    g = torch.Generator().manual_seed(77)
+    B, Hq, Hkv, T, d = 2, 8, 2, 300, 128
+    q = torch.randn(B, Hq, 1, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, Hkv, T, d, generator=g).to(torch.bfloat16)
+    sl = torch.tensor([T, 211], dtype=torch.int32)
+    qp = (sl - 1).view(B, 1).to(torch.int32)
+    qd, kd, sld, qpd = q.cuda(), k.cuda(), sl.cuda(), qp.cuda()
+    keep = []  # every V stays alive: each call's V is at a new address
+    for it in range(40):
+        v = torch.randn(B, Hkv, T, d, generator=g).to(torch.bfloat16)
+        vd = v.cuda()
+        keep.append(vd)
+        out, lse = blkattn.attention(qd, kd, vd, sld, qpd, None, d ** -0.5)
+        torch.cuda.synchronize()
+        ref = oracle.attention(q, k, v, sl, qp, d ** -0.5)
+        assert_parity(out.double().cpu().numpy().reshape(-1, d), lse.double().cpu().numpy().reshape(-1), ref,
+                      BF16_TOL_O, BF16_TOL_L)
