@@ -314,3 +314,41 @@ def test_window_covering_everything_changes_no_bit():
     b = run(dict(c, window=100000), o, lse)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+def test_a_captured_backward_replays_on_new_data():
+    """blkattn_bwd captured once in a CUDA graph (after one uncaptured call)
+    and replayed on new Q, K, V and g_o written into the same buffers: each
+    replay's gradients are the oracle's for the data present at replay time."""
+    c = case("causal_gqa_short")
+    ref = reference(c)
+    o, lse = oracle_forward_state(ref)
+    dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in c.items()}
+    od, lsed = o.cuda(), lse.cuda()
+    dq = torch.empty(dev["q"].shape, dtype=torch.float32, device="cuda")
+    dk = torch.empty(dev["k"].shape, dtype=torch.float32, device="cuda")
+    dv = torch.empty(dev["v"].shape, dtype=torch.float32, device="cuda")
+    call = lambda: blkattn.bwd(dev["q"], dev["k"], dev["v"], dev["seqlens"], dev["qpos"], None, c["scale"],
+                               od, lsed, dev["go"], dq, dk, dv)
+    call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            call()
+    torch.cuda.current_stream().wait_stream(side)
+    for rep in range(2):
+        new = make(2, 8, 2, 257, 297, [297, 200], [list(range(257)), list(range(257))], seed=40 + rep)
+        ref = reference(new)
+        o, lse = oracle_forward_state(ref)
+        for key in ("q", "k", "v", "go"):
+            dev[key].copy_(new[key])
+        od.copy_(o)
+        lsed.copy_(lse)
+        dq.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert blkattn.check_device_error() == 0
+        assert_grads((dq.cpu(), dk.cpu(), dv.cpu()), ref)

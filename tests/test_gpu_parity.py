@@ -1001,3 +1001,44 @@ def test_tensor_maps_stay_valid_when_the_cache_turns_over_inside_a_call():
         ref = oracle.attention(q, k, v, sl, qp, d ** -0.5)
         assert_parity(out.double().cpu().numpy().reshape(-1, d), lse.double().cpu().numpy().reshape(-1), ref,
                       BF16_TOL_O, BF16_TOL_L)
+
+
+# ------------------------------------------------------------ CUDA graphs
+
+@pytest.mark.parametrize("name", ["decode_gqa", "spec_verify", "window_decode", "prefill"])
+def test_a_captured_call_replays_on_new_data(name):
+    """A serving loop captures the call once in a CUDA graph and replays it on
+    new inputs written into the same buffers: after one uncaptured call (which
+    grows the scratch, builds the tensor maps), the captured call allocates
+    nothing, and every replay gives the oracle's result for the data in the
+    buffers at replay time (the split-unit counters are left at zero by every
+    launch, so replays do not see each other's state)."""
+    s = workloads.spec(name, small=True)
+    inp = workloads.generate(s)
+    g = to_dev(inp)
+    out = torch.empty(s.B, s.Hq, s.Tq, s.d, device="cuda")
+    lse = torch.empty(s.B, s.Hq, s.Tq, device="cuda")
+    call = lambda: blkattn.fwd(g["q"], g["k"], g["v"], g["seqlens"], g["qpos"], g["bias"], g["scale"], out, lse,
+                               tree=g.get("tree"), window=g.get("window", 0))
+    call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            call()
+    torch.cuda.current_stream().wait_stream(side)
+    gen = torch.Generator().manual_seed(5)
+    for rep in range(3):
+        new = dict(inp)
+        for key in ("q", "k", "v"):
+            new[key] = torch.randn(inp[key].shape, generator=gen).to(inp[key].dtype)
+            g[key].copy_(new[key])
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert blkattn.check_device_error() == 0
+        o = out.double().cpu().numpy().reshape(-1, s.d)
+        l = lse.double().cpu().numpy().reshape(-1)
+        assert_parity(o, l, run_oracle(new), *tols(s))

@@ -217,3 +217,33 @@ def test_masses_outside_the_unit_interval():
     np.testing.assert_array_equal(n, on)
     np.testing.assert_array_equal(tok, ot)
     assert np.all(n[:5] == 0) and np.all(n[5:] == k)
+
+
+def test_a_captured_step_replays_on_new_data():
+    """The verification step captured once in a CUDA graph and replayed on new
+    distributions, candidates and random numbers written into the same
+    buffers: every replay decides as the oracle does on that data."""
+    B, k, V = 16, 3, 20000
+    t = [x.cuda() for x in random_case(B, k, V, seed=1)]
+    n = torch.empty(B, dtype=torch.int32, device="cuda")
+    tok = torch.empty(B, dtype=torch.int32, device="cuda")
+    call = lambda: blkattn.spec_sample(*t, n, tok)
+    call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            call()
+    torch.cuda.current_stream().wait_stream(side)
+    for rep in range(3):
+        new = random_case(B, k, V, seed=100 + rep)
+        for dst, src in zip(t, new):
+            dst.copy_(src)
+        graph.replay()
+        torch.cuda.synchronize()
+        on, ot = ss.verify_step(new[0].numpy(), new[1].numpy(), new[2].numpy(), new[3].numpy(),
+                                new[4].numpy().view(np.uint32))
+        np.testing.assert_array_equal(n.cpu().numpy(), on)
+        np.testing.assert_array_equal(tok.cpu().numpy(), ot)
