@@ -1042,3 +1042,34 @@ def test_a_captured_call_replays_on_new_data(name):
         o = out.double().cpu().numpy().reshape(-1, s.d)
         l = lse.double().cpu().numpy().reshape(-1)
         assert_parity(o, l, run_oracle(new), *tols(s))
+
+
+# ------------------------------------------------------------ large offsets
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.bfloat16, 64), (torch.float32, 64)])
+def test_caches_larger_than_2_gib_per_tensor(dtype, d):
+    """K and V of one call larger than 2^31 bytes each (4 KV heads of 2.2 to
+    4.4 M keys; the last head's last rows lie past 2 GiB): every kernel path (tcgen05
+    decode for bf16 d = 128, the mma.sync kernel for bf16 d = 64, CUDA cores
+    for fp32) addresses them with 64-bit offsets.  Checked on one row of the
+    first and one of the last KV head against the oracle."""
+    B, Hkv, G = 1, 4, 2
+    Hq = Hkv * G
+    elt = 2 if dtype == torch.bfloat16 else 4
+    T = int(2 ** 31 * 1.05) // (Hkv * d * elt)  # 5 % past 2 GiB per tensor
+    assert Hkv * T * d * elt > 2 ** 31
+    gen = torch.Generator(device="cuda").manual_seed(11)
+    k = torch.randn(B, Hkv, T, d, device="cuda", generator=gen, dtype=dtype)
+    v = torch.randn(B, Hkv, T, d, device="cuda", generator=gen, dtype=dtype)
+    q = torch.randn(B, Hq, 1, d, device="cuda", generator=gen, dtype=dtype)
+    sl = torch.tensor([T], dtype=torch.int32)
+    qp = torch.tensor([[T - 1]], dtype=torch.int32)
+    out, lse = blkattn.attention(q, k, v, sl.cuda(), qp.cuda(), None, d ** -0.5)
+    torch.cuda.synchronize()
+    assert blkattn.check_device_error() == 0
+    rows = np.array([0, Hq - 1])  # head 0 (KV head 0) and head Hq - 1 (KV head 3)
+    ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), sl, qp, d ** -0.5, rows=rows)
+    o = out.double().cpu().numpy().reshape(-1, d)[rows]
+    l = lse.double().cpu().numpy().reshape(-1)[rows]
+    tol = (BF16_TOL_O, BF16_TOL_L) if dtype == torch.bfloat16 else (F32_TOL, F32_TOL)
+    assert_parity(o, l, ref, *tol)
