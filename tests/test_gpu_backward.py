@@ -352,3 +352,18 @@ def test_a_captured_backward_replays_on_new_data():
         torch.cuda.synchronize()
         assert blkattn.check_device_error() == 0
         assert_grads((dq.cpu(), dk.cpu(), dv.cpu()), ref)
+
+
+def test_token_major_layouts():
+    """Q, K, V and g_o stored token-major ([B, T, H, d]) and passed as
+    [B, H, T, d] views: the backward's tensor maps follow the strides."""
+    c = case("causal_gqa_short")
+    ref = reference(c)
+    o, lse = oracle_forward_state(ref)
+    tm = lambda t: t.permute(0, 2, 1, 3).contiguous().cuda().permute(0, 2, 1, 3)  # token-major storage
+    dq, dk, dv = blkattn.attention_backward(tm(c["q"]), tm(c["k"]), tm(c["v"]), c["seqlens"].cuda(),
+                                            c["qpos"].cuda(), o.cuda(), lse.cuda(), tm(c["go"]),
+                                            mask_bias=None, scale=c["scale"])
+    torch.cuda.synchronize()
+    assert blkattn.check_device_error() == 0
+    assert_grads((dq.cpu(), dk.cpu(), dv.cpu()), ref)

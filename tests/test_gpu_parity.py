@@ -1073,3 +1073,34 @@ def test_caches_larger_than_2_gib_per_tensor(dtype, d):
     l = lse.double().cpu().numpy().reshape(-1)[rows]
     tol = (BF16_TOL_O, BF16_TOL_L) if dtype == torch.bfloat16 else (F32_TOL, F32_TOL)
     assert_parity(o, l, ref, *tol)
+
+
+# ------------------------------------------------------------ token-major caches
+
+@pytest.mark.parametrize("kind", ["decode_d128", "decode_d64", "verify_48_rows", "prefill"])
+def test_token_major_layouts(kind):
+    """Q, K and V stored token-major ([B, T, H, d], as many serving caches
+    keep them) and passed as [B, H, T, d] views with permuted strides: the
+    tensor maps and the row addressing follow the strides."""
+    g = torch.Generator().manual_seed(21)
+    d = 64 if kind == "decode_d64" else 128
+    if kind == "prefill":
+        B, Hq, Hkv, Tq, T = 2, 4, 2, 300, 300
+        sl = torch.tensor([300, 251], dtype=torch.int32)
+        qp = torch.stack([torch.arange(Tq), torch.arange(Tq) - 49]).to(torch.int32)
+    else:
+        B, Hq, Hkv, T = 3, 16 if kind == "verify_48_rows" else 8, 2, 900
+        Tq = 5 if kind == "verify_48_rows" else 1
+        sl = torch.tensor([900, 413, 37], dtype=torch.int32)
+        qp = (sl.view(B, 1) - Tq + torch.arange(Tq).view(1, Tq)).to(torch.int32)
+    kt = torch.randn(B, T, Hkv, d, generator=g).to(torch.bfloat16)
+    vt = torch.randn(B, T, Hkv, d, generator=g).to(torch.bfloat16)
+    qt = torch.randn(B, Tq, Hq, d, generator=g).to(torch.bfloat16)
+    k, v, q = kt.cuda().permute(0, 2, 1, 3), vt.cuda().permute(0, 2, 1, 3), qt.cuda().permute(0, 2, 1, 3)
+    out, lse = blkattn.attention(q, k, v, sl.cuda(), qp.cuda(), None, d ** -0.5)
+    torch.cuda.synchronize()
+    assert blkattn.check_device_error() == 0
+    ref = oracle.attention(qt.permute(0, 2, 1, 3).contiguous(), kt.permute(0, 2, 1, 3).contiguous(),
+                           vt.permute(0, 2, 1, 3).contiguous(), sl, qp, d ** -0.5)
+    assert_parity(out.double().cpu().numpy().reshape(-1, d), lse.double().cpu().numpy().reshape(-1), ref,
+                  BF16_TOL_O, BF16_TOL_L)
