@@ -1104,3 +1104,25 @@ def test_token_major_layouts(kind):
                            vt.permute(0, 2, 1, 3).contiguous(), sl, qp, d ** -0.5)
     assert_parity(out.double().cpu().numpy().reshape(-1, d), lse.double().cpu().numpy().reshape(-1), ref,
                   BF16_TOL_O, BF16_TOL_L)
+
+
+# ------------------------------------------------------------ unit-table limits
+
+@pytest.mark.parametrize("B,window", [(1024, 0), (1025, 0), (512, 40), (513, 40)])
+def test_unit_table_boundaries(B, window):
+    """The tcgen05 decode kernel keeps its (sequence, row group) table in
+    shared memory: at most 1024 entries, 512 with a sliding window (the other
+    half holds the units' first tiles).  Batches at the limit run on it, one
+    past it on the split-KV fallback; both give the oracle's results."""
+    rng = np.random.default_rng(B + window)
+    T = 96
+    lens = rng.integers(1, T + 1, B)
+    lens[:2] = [T, 1]
+    inp = make_case(B, 4, 1, 1, T, 128, "bf16", lens.tolist(), (lens - 1)[:, None].tolist(), seed=B)
+    if window:
+        inp["window"] = window
+    if not window:
+        assert (plan_of(inp)["kernel"] == 3) == (B <= 1024)
+    _, _, o, l = run_gpu(inp)
+    ref = run_oracle(inp)
+    assert_parity(o, l, ref, BF16_TOL_O, BF16_TOL_L)
