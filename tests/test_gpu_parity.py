@@ -1126,3 +1126,26 @@ def test_unit_table_boundaries(B, window):
     _, _, o, l = run_gpu(inp)
     ref = run_oracle(inp)
     assert_parity(o, l, ref, BF16_TOL_O, BF16_TOL_L)
+
+
+def test_prefill_at_the_longest_query_block():
+    """One head of a 131072-token causal prefill (512 CTAs of two query tiles,
+    the longest rows over 1024 key tiles) against the oracle on sampled rows,
+    the first and last rows included."""
+    T, d = 131072, 128
+    gen = torch.Generator(device="cuda").manual_seed(31)
+    q = torch.randn(1, 1, T, d, device="cuda", generator=gen, dtype=torch.bfloat16)
+    k = torch.randn(1, 1, T, d, device="cuda", generator=gen, dtype=torch.bfloat16)
+    v = torch.randn(1, 1, T, d, device="cuda", generator=gen, dtype=torch.bfloat16)
+    sl = torch.tensor([T], dtype=torch.int32)
+    qp = torch.arange(T, dtype=torch.int32).view(1, T)
+    assert plan_of({"q": q, "k": k})["kernel"] == 2
+    out, lse = blkattn.attention(q, k, v, sl.cuda(), qp.cuda(), None, d ** -0.5)
+    torch.cuda.synchronize()
+    assert blkattn.check_device_error() == 0
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, T - 257, T - 1],
+                                     np.random.default_rng(3).integers(0, T, 40)]))
+    ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), sl, qp, d ** -0.5, rows=rows)
+    o = out.double().cpu().numpy().reshape(-1, d)[rows]
+    l = lse.double().cpu().numpy().reshape(-1)[rows]
+    assert_parity(o, l, ref, BF16_TOL_O, BF16_TOL_L)
