@@ -15,8 +15,9 @@
 //     min(pos + 1, len) of each 128-row query tile.
 //  2. dQ: one CTA per 128-row query tile of one head, walking the key tiles
 //     its rows see.  Per tile: S = Q K^T and G_P = G_O V^T (smem x smem ->
-//     TMEM), the rows form G_S in bf16 over G_P's columns, then
-//     G_Q += G_S K (A from TMEM, K as an N-major B operand).
+//     TMEM), the rows form G_S in bf16 in columns of its own (two buffers by
+//     tile parity), then G_Q += G_S K (A from TMEM, K as an N-major B
+//     operand).
 //  3. dK/dV: one CTA per 128-key tile of one KV head, walking the query
 //     tiles of its G query heads that see any of its keys.  Per tile:
 //     S^T = K Q^T and G_P^T = V G_O^T; the key rows form P^T and G_S^T in
@@ -33,12 +34,21 @@
 // accumulating products; warp 10 the thread that issues the S and G_P
 // products.  (One thread issues a product every ~75 cycles; an N = 64
 // product's math takes ~32, and two issuing threads get one every ~49.)
-// The products of a tile are issued by half (N = 64 for S and G_P, K = 64
-// for the accumulating ones), each half with its own barriers, so one
-// group's exponentials overlap the tensor core's work on the other half.
-// The next tile's half g overwrites the columns the accumulating products of
-// half g read, so its S and G_P wait until those products have completed
-// (a barrier per half).  In dK/dV the stages are split further: the key rows
+// In dQ, S and G_P are whole-tile products (N = 128) and the rows read them
+// out of TMEM at once: the next tile's S (G_P) is issued as soon as every row
+// warp has read this tile's, so the tensor core works on tile j + 1 while
+// the rows form tile j's P and G_S; nothing waits for G_Q += G_S K but the
+// reuse of its G_S buffer two tiles later.  K_j is read by S_j and, one tile
+// later, by G_Q += G_S K_j, so the dQ kernel keeps three K slots (two for V):
+// with two, the copy of K_{j+2} could start only once G_Q's product of tile
+// j had completed, and the copies' latency set the kernel's pace.
+// In dK/dV (tensor memory full: S^T, G_P^T, G_V, G_K) the products of a tile
+// are issued by half (N = 64 for S^T and G_P^T, K = 64 for the accumulating
+// ones), each half with its own barriers, so one group's exponentials
+// overlap the tensor core's work on the other half.  The next tile's half g
+// overwrites the columns the accumulating products of half g read, so its
+// S^T and G_P^T wait until those products have completed (a barrier per
+// half).  The stages are split further: the key rows
 // form P^T as soon as S^T is in (G_P^T may still be in the pipe) and G_V's
 // products start on it while the rows form G_S^T; the next S^T waits only
 // for G_V, the next G_P^T for G_K.  The accumulating products come from one thread in
@@ -75,6 +85,8 @@ constexpr int kThreads = 352;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescHalf = tc::idesc_bf16(128, HT, 0, 0);  // S half: both K-major, N = 64
 constexpr uint32_t kIdescTN = tc::idesc_bf16(128, 128, 0, 1);   // A in TMEM, B N-major, N = 128
+constexpr uint32_t kIdescFull = tc::idesc_bf16(128, 128, 0, 0); // S whole: both K-major, N = 128
+constexpr uint32_t kColDS = 384;  // dQ: G_S of tiles with even / odd index at +0 / +64 (bf16 pairs)
 
 // Shared memory: two stationary tiles, two 2-stage rings, barriers, facts.
 constexpr int kOffA0 = 0;                             // dQ: Q    | dK/dV: K
@@ -89,6 +101,18 @@ constexpr int kMaxQTiles = 1024;                              // query tiles per
 constexpr int kOffEnds = kOffFacts + 2 * 128 * 16;            // dK/dV: int [kMaxQTiles] row ends per query tile
 constexpr int kOffStarts = kOffEnds + kMaxQTiles * 4;         // dK/dV (window): smallest row start per query tile
 constexpr int kSmemBytes = kOffStarts + kMaxQTiles * 4 + 1024;  // + slack to align to 1024
+// dQ kernel: Q and G_O, a 3-slot K ring (K_j is read by S_j and, a tile
+// later, by G_Q += G_S K_j, so its slot is held longer than V_j's), a 2-slot
+// V ring, barriers.  (No row facts: the rows read their own.)
+constexpr int KST = 3;
+constexpr int kDqOffQ = 0;
+constexpr int kDqOffG = kTileBytes;
+constexpr int kDqOffK = 2 * kTileBytes;
+constexpr int kDqOffV = kDqOffK + KST * kTileBytes;
+constexpr int kDqOffBar = kDqOffV + STAGES * kTileBytes;
+constexpr int kDqOffMisc = kDqOffBar + kNumBars * 8;
+constexpr int kDqSmemBytes = kDqOffMisc + 128 + 1024;  // + slack to align to 1024
+static_assert(kDqSmemBytes <= 227 * 1024, "dQ shared memory");
 // Epilogue staging (in a ring the finished products no longer read): per
 // compute warp its 32 rows of one group's 64 columns, a row padded to 68
 // floats (conflict-free both ways); group g's warps in ring g.
@@ -137,6 +161,19 @@ __device__ __forceinline__ void issue_half(uint32_t dcol, uint32_t sa, uint32_t 
   for (int ks = 0; ks < D / 16; ++ks) {
     const uint32_t off = (uint32_t)(((ks >> 2) * kBox + (ks & 3) * 32) >> 4);
     tc::mma_ss(dcol, tc::desc_join(alo + off, kHi), tc::desc_join(blo + off, kHi), kIdescHalf, ks > 0 ? 1u : 0u);
+  }
+}
+
+// S = A B^T over d = 128 for all 128 rows of both tiles (N = 128): the
+// dQ kernel's score products.
+__device__ __forceinline__ void issue_full(uint32_t dcol, uint32_t sa, uint32_t sb) {
+  const uint32_t alo = tc::desc_lo(sa, 16);
+  const uint32_t blo = tc::desc_lo(sb, 16);
+  constexpr uint32_t kHi = tc::desc_hi(1024);
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const uint32_t off = (uint32_t)(((ks >> 2) * kBox + (ks & 3) * 32) >> 4);
+    tc::mma_ss(dcol, tc::desc_join(alo + off, kHi), tc::desc_join(blo + off, kHi), kIdescFull, ks > 0 ? 1u : 0u);
   }
 }
 
@@ -242,14 +279,15 @@ __device__ __forceinline__ uint32_t setup_tmem(int* misc, int warp) {
   return static_cast<uint32_t>(misc[0]);
 }
 
-// 32 entries of one row (dQ: a query row over 32 keys) from the scores s and
-// G_P in TMEM: G_S = 2^(s scale log2 e + m log2 e - L) (G_P - D), by select
-// where the key is invisible, packed to bf16 pairs.  MASK = false: every
-// entry is visible (no bias, the whole half tile before the row end).
+// dQ, step 1: P of one row over 32 keys from its scores s in TMEM words:
+// P = 2^(s scale log2 e + m log2 e - L), 0 by select where the key is
+// invisible; P replaces s in place (fp32 bits).  Returns the visibility bits
+// (bit c: key + c is visible).  MASK = false: every key of the half is
+// visible (no bias, the whole half tile before the row end).
 template <bool BIAS, bool MASK, bool WIN = false>
-__device__ __forceinline__ void dq_chunk(const uint32_t (&rs)[32], const uint32_t (&rp)[32], int key, int my_end,
-                                         float2 c2, float2 nl2, float2 nd2, const float* brow, int64_t bi_sj,
-                                         int Tmax, uint32_t (&ds)[16], int my_start = 0) {
+__device__ __forceinline__ uint32_t dq_p(uint32_t (&rs)[32], int key, int my_end, float2 c2, float2 nl2,
+                                         const float* brow, int64_t bi_sj, int Tmax, int my_start) {
+  uint32_t vis = 0xffffffffu;
 #pragma unroll
   for (int c = 0; c < 32; c += 2) {
     float2 x = __ffma2_rn(make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])), c2, nl2);
@@ -269,10 +307,29 @@ __device__ __forceinline__ void dq_chunk(const uint32_t (&rs)[32], const uint32_
       v1 = v1 && m1 != -__builtin_huge_valf();
       x = __ffma2_rn(make_float2(m0, m1), make_float2(kLog2e, kLog2e), x);
     }
+    float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+    if constexpr (MASK || BIAS) {
+      p0 = v0 ? p0 : 0.f;
+      p1 = v1 ? p1 : 0.f;
+      vis &= ~((v0 ? 0u : 1u) << c) & ~((v1 ? 0u : 1u) << (c + 1));
+    }
+    rs[c] = __float_as_uint(p0);
+    rs[c + 1] = __float_as_uint(p1);
+  }
+  return vis;
+}
+
+// dQ, step 2: G_S = P (G_P - D) over the same 32 keys, packed to bf16 pairs,
+// by select where the key is invisible (a masked G_P may be NaN).
+template <bool SEL>
+__device__ __forceinline__ void dq_ds(const uint32_t (&pr)[32], const uint32_t (&rp)[32], uint32_t vis, float2 nd2,
+                                      uint32_t (&ds)[16]) {
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
     const float2 gp = __fadd2_rn(make_float2(__uint_as_float(rp[c]), __uint_as_float(rp[c + 1])), nd2);
-    const float2 g = __fmul2_rn(make_float2(fast_exp2(x.x), fast_exp2(x.y)), gp);
-    if constexpr (MASK || BIAS)
-      ds[c >> 1] = pack_bf16(v0 ? g.x : 0.f, v1 ? g.y : 0.f);
+    const float2 g = __fmul2_rn(make_float2(__uint_as_float(pr[c]), __uint_as_float(pr[c + 1])), gp);
+    if constexpr (SEL)
+      ds[c >> 1] = pack_bf16(((vis >> c) & 1u) ? g.x : 0.f, ((vis >> (c + 1)) & 1u) ? g.y : 0.f);
     else
       ds[c >> 1] = pack_bf16(g.x, g.y);
   }
@@ -346,17 +403,20 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
                                         const CUtensorMap& tmk, const CUtensorMap& tmv, int blk) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kDqOffBar);
   uint64_t* q_full = bars;            // Q and G_O tiles
-  uint64_t* k_full = bars + 1;        // [STAGES]
-  uint64_t* v_full = bars + 3;        // [STAGES]
-  uint64_t* k_empty = bars + 5;       // [STAGES]
-  uint64_t* v_empty = bars + 7;       // [STAGES]
-  uint64_t* sp_full = bars + 9;       // [2] half g of S and G_P is in TMEM
-  uint64_t* p_full = bars + 11;       // [2] half g of G_S is in TMEM (4 warps of group g)
-  uint64_t* drain = bars + 13;        // every product has completed (both issuing threads)
-  uint64_t* acc_done = bars + 14;     // [2] G_Q += G_S K over half g has completed
-  int* misc = reinterpret_cast<int*>(sm + kOffMisc);  // [0] TMEM base, [1] CTA end
+  uint64_t* k_full = bars + 1;        // [KST]
+  uint64_t* v_full = bars + 4;        // [STAGES]
+  uint64_t* k_empty = bars + 6;       // [KST]
+  uint64_t* v_empty = bars + 9;       // [STAGES]
+  uint64_t* s_full = bars + 11;       // S of the tile is in TMEM
+  uint64_t* gp_full = bars + 12;      // G_P of the tile is in TMEM
+  uint64_t* s_free = bars + 13;       // the 8 row warps have read S (its columns are free)
+  uint64_t* gp_free = bars + 14;      // the 8 row warps have read G_P
+  uint64_t* p_full = bars + 15;       // [2] G_S of tiles with even / odd index is in TMEM (8 warps)
+  uint64_t* acc_done = bars + 17;     // [2] G_Q += G_S K of tiles with even / odd index has completed
+  uint64_t* drain = bars + 19;        // every product has completed (both issuing threads)
+  int* misc = reinterpret_cast<int*>(sm + kDqOffMisc);  // [0] TMEM base, [1] CTA end
 
   // Groups of p.hg_q (sequence, head) pairs whose K/V fit in L2 together;
   // within a group the longest query tiles first (causal: the last tiles see
@@ -377,16 +437,21 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
     misc[1] = 0;
     if constexpr (WIN) misc[2] = 0x7fffffff;
     mbar_init(q_full, 1);
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < KST; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
       mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int g = 0; g < 2; ++g) {
-      mbar_init(&sp_full[g], 1);
-      mbar_init(&p_full[g], 4);
-      mbar_init(&acc_done[g], 1);
+    mbar_init(s_full, 1);
+    mbar_init(gp_full, 1);
+    mbar_init(s_free, 8);
+    mbar_init(gp_free, 8);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&p_full[x], 8);
+      mbar_init(&acc_done[x], 1);
     }
     mbar_init(drain, 2);
     fence_barrier_init();
@@ -396,17 +461,17 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
   if (warp == kTmaWarp && lane == 0) {
     // the query-side tiles and the first key tile (T_max >= 1) right away
     mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
-    tma_load_4d(sm + kOffA0, &tmq, 0, i0, h, b, q_full, pol);
-    tma_load_4d(sm + kOffA0 + kBox, &tmq, 64, i0, h, b, q_full, pol);
-    tma_load_4d(sm + kOffA1, &tmg, 0, i0, h, b, q_full, pol);
-    tma_load_4d(sm + kOffA1 + kBox, &tmg, 64, i0, h, b, q_full, pol);
+    tma_load_4d(sm + kDqOffQ, &tmq, 0, i0, h, b, q_full, pol);
+    tma_load_4d(sm + kDqOffQ + kBox, &tmq, 64, i0, h, b, q_full, pol);
+    tma_load_4d(sm + kDqOffG, &tmg, 0, i0, h, b, q_full, pol);
+    tma_load_4d(sm + kDqOffG + kBox, &tmg, 64, i0, h, b, q_full, pol);
     if constexpr (!WIN) {  // (with a window the first key tile is known only from the positions)
       mbar_arrive_expect_tx(&k_full[0], kTileBytes);
-      tma_load_4d(sm + kOffR0, &tmk, 0, 0, hk, b, &k_full[0], pol);
-      tma_load_4d(sm + kOffR0 + kBox, &tmk, 64, 0, hk, b, &k_full[0], pol);
+      tma_load_4d(sm + kDqOffK, &tmk, 0, 0, hk, b, &k_full[0], pol);
+      tma_load_4d(sm + kDqOffK + kBox, &tmk, 64, 0, hk, b, &k_full[0], pol);
       mbar_arrive_expect_tx(&v_full[0], kTileBytes);
-      tma_load_4d(sm + kOffR1, &tmv, 0, 0, hk, b, &v_full[0], pol);
-      tma_load_4d(sm + kOffR1 + kBox, &tmv, 64, 0, hk, b, &v_full[0], pol);
+      tma_load_4d(sm + kDqOffV, &tmv, 0, 0, hk, b, &v_full[0], pol);
+      tma_load_4d(sm + kDqOffV + kBox, &tmv, 64, 0, hk, b, &v_full[0], pol);
     }
   }
 
@@ -433,8 +498,8 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
     j_lo = misc[2] != 0x7fffffff ? misc[2] / BT : 0;
     n = max(0, n - j_lo);
   }
-  const uint32_t sQ = smem_u32(sm + kOffA0), sG = smem_u32(sm + kOffA1);
-  const uint32_t sK = smem_u32(sm + kOffR0), sV = smem_u32(sm + kOffR1);
+  const uint32_t sQ = smem_u32(sm + kDqOffQ), sG = smem_u32(sm + kDqOffG);
+  const uint32_t sK = smem_u32(sm + kDqOffK), sV = smem_u32(sm + kDqOffV);
   const int grp = (warp >> 2) & 1;  // column half of a compute warp
   float* dq_row = p.dq + (int64_t)b * p.dq_sb + (int64_t)h * p.dq_sh + (int64_t)row_i * p.dq_si + grp * HT;
 
@@ -456,24 +521,23 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
       int k_issued = WIN ? 0 : 1, v_issued = WIN ? 0 : 1;
       bool ok = true;
       for (int j = WIN ? 0 : 1; j < n && ok; ++j) {
-        const int s = j % STAGES;
-        const uint32_t ph = ((j / STAGES) - 1) & 1;
+        const int sk = j % KST, sv = j % STAGES;
         const int key0 = (j_lo + j) * BT;
-        if (j >= STAGES && !mbar_wait(&k_empty[s], ph)) { ok = false; break; }
-        mbar_arrive_expect_tx(&k_full[s], kTileBytes);
-        tma_load_4d(sm + kOffR0 + s * kTileBytes, &tmk, 0, key0, hk, b, &k_full[s], pol);
-        tma_load_4d(sm + kOffR0 + s * kTileBytes + kBox, &tmk, 64, key0, hk, b, &k_full[s], pol);
+        if (j >= KST && !mbar_wait(&k_empty[sk], ((j / KST) - 1) & 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(&k_full[sk], kTileBytes);
+        tma_load_4d(sm + kDqOffK + sk * kTileBytes, &tmk, 0, key0, hk, b, &k_full[sk], pol);
+        tma_load_4d(sm + kDqOffK + sk * kTileBytes + kBox, &tmk, 64, key0, hk, b, &k_full[sk], pol);
         k_issued = j + 1;
-        if (j >= STAGES && !mbar_wait(&v_empty[s], ph)) { ok = false; break; }
-        mbar_arrive_expect_tx(&v_full[s], kTileBytes);
-        tma_load_4d(sm + kOffR1 + s * kTileBytes, &tmv, 0, key0, hk, b, &v_full[s], pol);
-        tma_load_4d(sm + kOffR1 + s * kTileBytes + kBox, &tmv, 64, key0, hk, b, &v_full[s], pol);
+        if (j >= STAGES && !mbar_wait(&v_empty[sv], ((j / STAGES) - 1) & 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(&v_full[sv], kTileBytes);
+        tma_load_4d(sm + kDqOffV + sv * kTileBytes, &tmv, 0, key0, hk, b, &v_full[sv], pol);
+        tma_load_4d(sm + kDqOffV + sv * kTileBytes + kBox, &tmv, 64, key0, hk, b, &v_full[sv], pol);
         v_issued = j + 1;
       }
       // every issued copy lands before the CTA exits
       if (!mbar_wait(q_full, 0)) ok = false;
-      for (int j = k_issued - STAGES < 0 ? 0 : k_issued - STAGES; j < k_issued; ++j)
-        if (!mbar_wait(&k_full[j % STAGES], (j / STAGES) & 1)) ok = false;
+      for (int j = k_issued - KST < 0 ? 0 : k_issued - KST; j < k_issued; ++j)
+        if (!mbar_wait(&k_full[j % KST], (j / KST) & 1)) ok = false;
       for (int j = v_issued - STAGES < 0 ? 0 : v_issued - STAGES; j < v_issued; ++j)
         if (!mbar_wait(&v_full[j % STAGES], (j / STAGES) & 1)) ok = false;
       if (!ok) record_error(p.err, kErrTimeout);
@@ -481,37 +545,33 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
   } else if (warp == kScoreWarp) {
     // ---------------- S and G_P products (one thread) ----------------
     if (lane == 0) {
-      // S and G_P of half g of key tile j (S at columns 64 g, G_P at 128 + 64 g)
-      auto half = [&](int j, int g) {
-        const int s = j % STAGES;
-        issue_half(tb + HT * g, sQ, sK + s * kTileBytes, g);
-        issue_half(tb + 128 + HT * g, sG, sV + s * kTileBytes, g);
-        tc::commit(&sp_full[g]);
-      };
       auto tile_ready = [&](int j) -> bool {
-        const int s = j % STAGES;
-        const uint32_t ph = (j / STAGES) & 1;
-        const bool r = mbar_wait(&k_full[s], ph) && mbar_wait(&v_full[s], ph);
+        const bool r = mbar_wait(&k_full[j % KST], (j / KST) & 1) && mbar_wait(&v_full[j % STAGES], (j / STAGES) & 1);
         tc::fence_after();
         return r;
       };
       bool ok = mbar_wait(q_full, 0) && tile_ready(0);
       if (ok) {
-        half(0, 0);
-        half(0, 1);
+        issue_full(tb + 0, sQ, sK);
+        tc::commit(s_full);
+        issue_full(tb + 128, sG, sV);
+        tc::commit(gp_full);
         tc::commit(&v_empty[0]);
       }
       for (int j = 0; ok && j + 1 < n; ++j) {
-        // half g of tile j + 1 overwrites the columns G_Q += G_S K of tile j
-        // reads: it waits until that product has completed
+        // tile j + 1's S (G_P) overwrites tile j's as soon as the rows have
+        // read it; G_S has columns of its own
+        const int s1 = (j + 1) % STAGES;
         if (!tile_ready(j + 1)) { ok = false; break; }
-        if (!mbar_wait(&acc_done[0], j & 1)) { ok = false; break; }
+        if (!mbar_wait(s_free, j & 1)) { ok = false; break; }
         tc::fence_after();
-        half(j + 1, 0);
-        if (!mbar_wait(&acc_done[1], j & 1)) { ok = false; break; }
+        issue_full(tb + 0, sQ, sK + ((j + 1) % KST) * kTileBytes);
+        tc::commit(s_full);
+        if (!mbar_wait(gp_free, j & 1)) { ok = false; break; }
         tc::fence_after();
-        half(j + 1, 1);
-        tc::commit(&v_empty[(j + 1) % STAGES]);  // V_{j+1} once its halves are done
+        issue_full(tb + 128, sG, sV + s1 * kTileBytes);
+        tc::commit(gp_full);
+        tc::commit(&v_empty[s1]);  // V_{j+1} once its product is done
       }
       if (!ok) record_error(p.err, kErrTimeout);
       tc::commit(drain);
@@ -522,16 +582,14 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
     if (lane == 0) {
       bool ok = true;
       for (int j = 0; ok && j < n; ++j) {
-        const int s = j % STAGES;
-        if (!mbar_wait(&p_full[0], j & 1)) { ok = false; break; }
+        const int s = j % KST;
+        const int par = j & 1;
+        if (!mbar_wait(&p_full[par], (j >> 1) & 1)) { ok = false; break; }
         tc::fence_after();
-        issue_acc(tb + 256, tb + 128, sK + s * kTileBytes, 0, j > 0);
-        tc::commit(&acc_done[0]);
-        if (!mbar_wait(&p_full[1], j & 1)) { ok = false; break; }
-        tc::fence_after();
-        issue_acc(tb + 256, tb + 128 + HT, sK + s * kTileBytes, 1, true);
-        tc::commit(&acc_done[1]);
-        tc::commit(&k_empty[s]);  // K_j is free: tile j's halves completed before its G_S was written
+        issue_acc(tb + 256, tb + kColDS + 64 * par, sK + s * kTileBytes, 0, j > 0);
+        issue_acc(tb + 256, tb + kColDS + 64 * par + 32, sK + s * kTileBytes, 1, true);
+        tc::commit(&acc_done[par]);
+        tc::commit(&k_empty[s]);  // K_j is free: its S completed before its G_S was written
       }
       if (!ok) record_error(p.err, kErrTimeout);
       tc::commit(drain);
@@ -554,30 +612,69 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
     const float2 nd2 = make_float2(nDrow, nDrow);
     bool ok = true;
     for (int j = 0; j < n; ++j) {
-      if (!wait_all(&sp_full[grp], j & 1)) { ok = false; break; }
+      const int par = j & 1;
+      if (!wait_all(s_full, j & 1)) { ok = false; break; }
       tc::fence_after();
       const int key0 = (j_lo + j) * BT + grp * HT;  // first key of this half
       // (warp-uniform) every row of the warp sees every key of the half
       const bool whole = !BIAS && __all_sync(0xffffffffu, key0 + HT <= my_end && (!WIN || key0 >= my_start));
+      // This half of S, then its columns are free for the next tile's S, and
+      // P while G_P is in the pipe.  With a bias, S and P go chunk by chunk
+      // after G_P has arrived instead (the bias loads would hold too many
+      // registers across the wait).
+      uint32_t pr[2][32];
+      uint32_t vis[2] = {0u, 0u};
+      if constexpr (!BIAS) {
+        tc::ld32(tl + HT * grp, pr[0]);
+        tc::ld32(tl + HT * grp + 32, pr[1]);
+        tc::wait_ld();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free);
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+          if (whole)
+            vis[q2] = dq_p<false, false, WIN>(pr[q2], key0 + 32 * q2, my_end, c2, nl2, brow, p.bi_sj, p.Tmax, my_start);
+          else
+            vis[q2] = dq_p<false, true, WIN>(pr[q2], key0 + 32 * q2, my_end, c2, nl2, brow, p.bi_sj, p.Tmax, my_start);
+        }
+      }
+      if (!wait_all(gp_full, j & 1)) { ok = false; break; }
+      // G_S of tile j goes where tile j - 2's was: its product must have completed
+      if (j >= 2 && !wait_all(&acc_done[par], ((j >> 1) - 1) & 1)) { ok = false; break; }
+      tc::fence_after();
 #pragma unroll
       for (int q2 = 0; q2 < 2; ++q2) {
-        uint32_t rs[32], rp[32], ds[16];
-        tc::ld32(tl + HT * grp + 32 * q2, rs);
+        if constexpr (BIAS) {  // (whole is false with a bias)
+          tc::ld32(tl + HT * grp + 32 * q2, pr[q2]);
+          tc::wait_ld();
+          if (q2 == 1) {
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free);
+          }
+          vis[q2] = dq_p<true, true, WIN>(pr[q2], key0 + 32 * q2, my_end, c2, nl2, brow, p.bi_sj, p.Tmax, my_start);
+        }
+        uint32_t rp[32], ds[16];
         tc::ld32(tl + 128 + HT * grp + 32 * q2, rp);
         tc::wait_ld();
-        const int key = key0 + 32 * q2;
+        if (q2 == 1) {  // G_P's columns are free for the next tile's G_P
+          tc::fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(gp_free);
+        }
         if (whole)
-          dq_chunk<BIAS, false, WIN>(rs, rp, key, my_end, c2, nl2, nd2, brow, p.bi_sj, p.Tmax, ds, my_start);
+          dq_ds<false>(pr[q2], rp, vis[q2], nd2, ds);
         else
-          dq_chunk<BIAS, true, WIN>(rs, rp, key, my_end, c2, nl2, nd2, brow, p.bi_sj, p.Tmax, ds, my_start);
-        tc::st16(tl + 128 + HT * grp + 16 * q2, ds);  // G_S over G_P's first 32 columns of the half
+          dq_ds<true>(pr[q2], rp, vis[q2], nd2, ds);
+        tc::st16(tl + kColDS + 64 * par + 32 * grp + 16 * q2, ds);
       }
       if ((j_lo + j) * BT + BT > cta_end) {
         // last tile: the K rows of this half past every visible key of the
         // CTA are zeroed before G_S K reads them (they may hold anything)
-        const int s = j % STAGES;
-        if (!wait_all(&k_full[s], (j / STAGES) & 1)) { ok = false; break; }
-        unsigned char* kt = sm + kOffR0 + s * kTileBytes;
+        const int s = j % KST;
+        if (!wait_all(&k_full[s], (j / KST) & 1)) { ok = false; break; }
+        unsigned char* kt = sm + kDqOffK + s * kTileBytes;
         const int z0 = max(cta_end - (j_lo + j) * BT, grp * HT);
         const int t = (int)(threadIdx.x & 127);
         for (int idx = t; idx < (grp * HT + HT - z0) * 16; idx += 128) {
@@ -591,7 +688,7 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[grp]);
+      if (lane == 0) mbar_arrive(&p_full[par]);
     }
     if (ok && !wait_all(drain, 0)) ok = false;
     if (!ok) {
@@ -602,7 +699,7 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
       tc::fence_after();
       const int r0 = i0 + 32 * (warp & 3);
       store_rows(tl + 256 + HT * grp, p.scale,
-                 reinterpret_cast<float*>(sm + (grp == 0 ? kOffR0 : kOffR1) + (warp & 3) * kStageWarp),
+                 reinterpret_cast<float*>(sm + kDqOffK + (grp * 4 + (warp & 3)) * kStageWarp),
                  p.dq + (int64_t)b * p.dq_sb + (int64_t)h * p.dq_sh + (int64_t)r0 * p.dq_si + grp * HT, p.dq_si,
                  min(32, p.Tq - r0), lane);
     }
@@ -960,10 +1057,12 @@ cudaError_t launch_pair(const BwdParams& p, const CUtensorMap& tmq, const CUtens
                         const CUtensorMap& tmv, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    for (const void* f : {(const void*)dq_kernel<BIAS, WIN>, (const void*)dkv_kernel<BIAS, WIN>}) {
-      cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-      if (e != cudaSuccess) return e;
-    }
+    cudaError_t e = cudaFuncSetAttribute((const void*)dq_kernel<BIAS, WIN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute((const void*)dkv_kernel<BIAS, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
+    if (e != cudaSuccess) return e;
     attr_set = true;
   }
   if (p.hg_q < 1 || p.hg_kv < 1 || p.n_qt > kMaxQTiles) return cudaErrorInvalidValue;
@@ -971,7 +1070,7 @@ cudaError_t launch_pair(const BwdParams& p, const CUtensorMap& tmq, const CUtens
   const int64_t dkv_blocks = ((int64_t)p.B * p.Hkv + p.hg_kv - 1) / p.hg_kv * p.hg_kv * p.n_kt;
   if (dq_blocks > 0x7fffffff || dkv_blocks > 0x7fffffff) return cudaErrorInvalidValue;
   if (dq_blocks > 0) {
-    dq_kernel<BIAS, WIN><<<(unsigned)dq_blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmg, tmk, tmv);
+    dq_kernel<BIAS, WIN><<<(unsigned)dq_blocks, kThreads, kDqSmemBytes, stream>>>(p, tmq, tmg, tmk, tmv);
     if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
   }
   dkv_kernel<BIAS, WIN><<<(unsigned)dkv_blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmg, tmk, tmv);
@@ -980,7 +1079,7 @@ cudaError_t launch_pair(const BwdParams& p, const CUtensorMap& tmq, const CUtens
 
 }  // namespace
 
-int backward_smem_bytes() { return kSmemBytes; }
+int backward_smem_bytes() { return kDqSmemBytes > kSmemBytes ? kDqSmemBytes : kSmemBytes; }
 
 cudaError_t launch_backward(const BwdParams& p, const CUtensorMap& tmq, const CUtensorMap& tmg,
                             const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t stream) {
