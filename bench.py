@@ -214,6 +214,29 @@ def queue_ahead(ms: float = 5.0):
         torch.cuda._sleep(int(ms * 1e-3 * 2.0e9))
 
 
+def device_times(call, steps: int, warmup: int, before=None):
+    """Device time (ms) of each of `steps` calls, CUDA events around each on
+    the current stream, after `warmup` untimed calls.  All steps are enqueued
+    behind a device sleep (queue_ahead) with one synchronize at the end, so
+    the host's marshalling of a call never lands between its events.
+    `before` (an L2 eviction) runs ahead of every call, outside its events."""
+    for _ in range(warmup):
+        if before is not None:
+            before()
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    queue_ahead()
+    for e0, e1 in ev:
+        if before is not None:
+            before()
+        e0.record()
+        call()
+        e1.record()
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in ev]
+
+
 class Runner:
     """Inputs resident on the device plus the call the user makes."""
 
@@ -512,16 +535,7 @@ def measure_spec_sample(peaks, steps=10, warmup=3, full=False):
     # evict the rows by READING a buffer twice the L2 size: a written flush
     # buffer would leave dirty lines whose write-back lands in the timed call
     flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
-    times = []
-    for it in range(warmup + steps):
-        flush.sum()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        call()
-        e1.record()
-        torch.cuda.synchronize()
-        if it >= warmup:
-            times.append(e0.elapsed_time(e1))
+    times = device_times(call, steps, warmup, before=lambda: flush.sum())
     t_ms = sum(times) / len(times)
     achieved = total / (t_ms * 1e-3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -553,15 +567,7 @@ def measure_backward(peaks, steps=5, warmup=3, name="prefill", full=False):
     call = lambda: blkattn.bwd(dev["q"], dev["k"], dev["v"], dev["seqlens"], dev["qpos"], None, cpu["scale"],
                                out, lse, dev["go"], dq, dk, dv, window=W)
     in_bytes = sum(t.numel() * t.element_size() for t in (dev["q"], dev["k"], dev["v"], dev["go"], out, lse))
-    times = []
-    for it in range(warmup + steps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        call()
-        e1.record()
-        torch.cuda.synchronize()
-        if it >= warmup:
-            times.append(e0.elapsed_time(e1))
+    times = device_times(call, steps, warmup)
     assert blkattn.check_device_error() == 0
     t_ms = sum(times) / len(times)
     flops = causal_flops(s, cpu) * 2.5

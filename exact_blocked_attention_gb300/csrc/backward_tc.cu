@@ -209,61 +209,95 @@ __device__ __forceinline__ int seq_len(const BwdParams& p, int b) {
 }
 
 // ---------------------------------------------------------------- row facts
-// One warp per row (b, h, i): -D = -(g_o . o) (fp32) and -L = -lse log2 e
-// (-inf for an empty row, so that 2^(x - L) = 0), negated for the fused
-// multiply-adds that use them.  Then one thread per (b, query tile): the
-// largest row end of the tile.
+// One warp per (b, query tile): the largest row end of the tile (and the
+// smallest row start, for a sliding window).  Then one warp per row
+// (b, h, i): -D = -(g_o . o) (fp32) and -L = -lse log2 e (-inf for an empty
+// row, so that 2^(x - L) = 0), negated for the fused multiply-adds that use
+// them.
 __global__ void __launch_bounds__(256) bwd_facts_kernel(const BwdParams p) {
   const int64_t rows = (int64_t)p.B * p.Hq * p.Tq;
   const int64_t warps = (int64_t)gridDim.x * 8;
   const int lane = threadIdx.x & 31;
-  for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < rows; r += warps) {
-    const int i = (int)(r % p.Tq);
-    const int64_t bh = r / p.Tq;
-    const int h = (int)(bh % p.Hq);
-    const int b = (int)(bh / p.Hq);
-    const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(p.dout) + b * p.g_sb + h * p.g_sh + i * p.g_si;
-    const int64_t ob = b * p.o_sb + h * p.o_sh + i * p.o_si;
-    // lane: dims [4 lane, 4 lane + 4) (g_o rows are 16-byte aligned: one 8-byte load)
-    const uint2 gw = *reinterpret_cast<const uint2*>(g + 4 * lane);
-    float o[4];
-    if (p.out_vec) {  // fp32 rows, unit dim stride, 16-byte aligned: one 16-byte load
-      const float4 v = *reinterpret_cast<const float4*>(static_cast<const float*>(p.out) + ob + 4 * lane);
-      o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
-    } else {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int64_t t = ob + (int64_t)(4 * lane + c) * p.o_sd;
-        o[c] = p.out_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.out)[t])
-                          : static_cast<const float*>(p.out)[t];
-      }
-    }
-    float acc = bf16lo(gw.x) * o[0];
-    acc = fmaf(bf16hi(gw.x), o[1], acc);
-    acc = fmaf(bf16lo(gw.y), o[2], acc);
-    acc = fmaf(bf16hi(gw.y), o[3], acc);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-      const float l = p.lse[b * p.l_sb + h * p.l_sh + i * p.l_si];
-      p.ws_D[r] = -acc;
-      p.ws_L[r] = (l == -__builtin_huge_valf()) ? -__builtin_huge_valf() : -l * kLog2e;
-    }
-  }
+  // first, one warp per (sequence, query tile): the largest row end of the
+  // tile and, over the rows that see keys, the smallest row start
   const int64_t tiles = (int64_t)p.B * p.n_qt;
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < tiles; e += (int64_t)gridDim.x * blockDim.x) {
+  for (int64_t e = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); e < tiles; e += warps) {
     const int b = (int)(e / p.n_qt);
     const int qt = (int)(e % p.n_qt);
     const int len = seq_len(p, b);
     int mx = 0, mn = 0x7fffffff;
-    for (int i = qt * BT; i < min(qt * BT + BT, p.Tq); ++i) {
+    const int i1 = min(qt * BT + BT, p.Tq);
+    for (int i = qt * BT + lane; i < i1; i += 32) {
       const int e_i = row_end(p, b, i, len), s_i = row_start(p, b, i);
       mx = max(mx, e_i);
       if (e_i > s_i) mn = min(mn, s_i);
     }
-    p.ws_end[e] = mx;
-    p.ws_start[e] = mn;
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    if (lane == 0) {
+      p.ws_end[e] = mx;
+      p.ws_start[e] = mn;
+    }
   }
+  // two rows per warp and step, every load of both issued before either
+  // row's reduction (twice the bytes in flight per warp)
+  for (int64_t r0 = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r0 < rows; r0 += 2 * warps) {
+    uint2 gw[2];
+    float o[2][4], l[2];
+    int64_t rr[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int64_t r = r0 + u * warps;
+      rr[u] = r;
+      gw[u] = make_uint2(0u, 0u);
+      o[u][0] = o[u][1] = o[u][2] = o[u][3] = 0.f;
+      l[u] = 0.f;
+      if (r >= rows) continue;
+      const int i = (int)(r % p.Tq);
+      const int64_t bh = r / p.Tq;
+      const int h = (int)(bh % p.Hq);
+      const int b = (int)(bh / p.Hq);
+      const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(p.dout) + b * p.g_sb + h * p.g_sh + i * p.g_si;
+      const int64_t ob = b * p.o_sb + h * p.o_sh + i * p.o_si;
+      // lane: dims [4 lane, 4 lane + 4) (g_o rows are 16-byte aligned: one 8-byte load)
+      gw[u] = *reinterpret_cast<const uint2*>(g + 4 * lane);
+      if (p.out_vec) {  // fp32 rows, unit dim stride, 16-byte aligned: one 16-byte load
+        const float4 v = *reinterpret_cast<const float4*>(static_cast<const float*>(p.out) + ob + 4 * lane);
+        o[u][0] = v.x; o[u][1] = v.y; o[u][2] = v.z; o[u][3] = v.w;
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int64_t t = ob + (int64_t)(4 * lane + c) * p.o_sd;
+          o[u][c] = p.out_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.out)[t])
+                               : static_cast<const float*>(p.out)[t];
+        }
+      }
+      if (lane == 0) l[u] = p.lse[b * p.l_sb + h * p.l_sh + i * p.l_si];
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (rr[u] >= rows) break;
+      float acc = bf16lo(gw[u].x) * o[u][0];
+      acc = fmaf(bf16hi(gw[u].x), o[u][1], acc);
+      acc = fmaf(bf16lo(gw[u].y), o[u][2], acc);
+      acc = fmaf(bf16hi(gw[u].y), o[u][3], acc);
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (lane == 0) {
+        p.ws_D[rr[u]] = -acc;
+        p.ws_L[rr[u]] = (l[u] == -__builtin_huge_valf()) ? -__builtin_huge_valf() : -l[u] * kLog2e;
+      }
+    }
+  }
+}
+
+// L2 prefetch of one box of a 4-D tensor map (no shared memory, no
+// completion): the later tiled load of the same box then hits L2.
+__device__ __forceinline__ void tma_prefetch_l2_4d(const void* map, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
 }
 
 // TMEM set-up shared by the two tensor-core kernels (after thread 0 has
@@ -533,6 +567,13 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
         tma_load_4d(sm + kDqOffV + sv * kTileBytes, &tmv, 0, key0, hk, b, &v_full[sv], pol);
         tma_load_4d(sm + kDqOffV + sv * kTileBytes + kBox, &tmv, 64, key0, hk, b, &v_full[sv], pol);
         v_issued = j + 1;
+        if (j + 1 < n && j + 1 >= STAGES) {
+          // the next tile's copies wait for slots: bring it into L2 now
+          tma_prefetch_l2_4d(&tmk, 0, key0 + BT, hk, b);
+          tma_prefetch_l2_4d(&tmk, 64, key0 + BT, hk, b);
+          tma_prefetch_l2_4d(&tmv, 0, key0 + BT, hk, b);
+          tma_prefetch_l2_4d(&tmv, 64, key0 + BT, hk, b);
+        }
       }
       // every issued copy lands before the CTA exits
       if (!mbar_wait(q_full, 0)) ok = false;
@@ -828,6 +869,15 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
         tma_load_4d(sm + kOffR1 + s * kTileBytes, &tmg, 0, row, h, b, &qg_full[s], pol);
         tma_load_4d(sm + kOffR1 + s * kTileBytes + kBox, &tmg, 64, row, h, b, &qg_full[s], pol);
         ++t;
+        Visit vn = v;
+        if (t >= STAGES && next_visit<WIN>(p, ends, starts, k0, vn)) {
+          // the next visit's copies wait for a slot: bring its tiles into L2 now
+          const int hn = hk * p.G + vn.g, rn = vn.qt * BT;
+          tma_prefetch_l2_4d(&tmq, 0, rn, hn, b);
+          tma_prefetch_l2_4d(&tmq, 64, rn, hn, b);
+          tma_prefetch_l2_4d(&tmg, 0, rn, hn, b);
+          tma_prefetch_l2_4d(&tmg, 64, rn, hn, b);
+        }
       } while (next_visit<WIN>(p, ends, starts, k0, v));
       if (!mbar_wait(kv_full, 0)) ok = false;
       for (int u = t - STAGES < 0 ? 0 : t - STAGES; u < t; ++u)
