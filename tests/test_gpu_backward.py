@@ -304,6 +304,22 @@ def test_window_backward_after_the_library_windowed_forward():
     assert_grads(run(c, out.cpu(), lse.cpu()), reference(c))
 
 
+@pytest.mark.parametrize("window", [0, 300])
+def test_many_key_tiles_with_a_bias(window):
+    """Nine key tiles per head, with a bias that masks a fifth of the
+    entries: the dQ kernel's K ring (three slots) and V ring (two) wrap
+    several times, and its bias instantiations read S chunk by chunk."""
+    B, H, T = 1, 2, 1100
+    g = torch.Generator().manual_seed(31 + window)
+    bias = torch.randn(B, H, T, T, generator=g)
+    bias[torch.rand(B, H, T, T, generator=g) < 0.2] = -math.inf
+    c = make(B, H, 1, T, T, [T], [list(range(T))], bias=bias, seed=32 + window)
+    c["window"] = window
+    ref = reference(c)
+    o, lse = oracle_forward_state(ref)
+    assert_grads(run(c, o, lse), ref)
+
+
 def test_window_covering_everything_changes_no_bit():
     """A window longer than every row's history: the windowed kernels give the
     same bits as the unwindowed ones."""
