@@ -492,6 +492,7 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
   }
   const uint32_t tb = setup_tmem(misc, warp);
   const uint64_t pol = policy_evict_first();
+  const uint64_t pol_ring = policy_evict_last();  // K/V tiles: re-read by the head's other query tiles
   if (warp == kTmaWarp && lane == 0) {
     // the query-side tiles and the first key tile (T_max >= 1) right away
     mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
@@ -501,11 +502,11 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
     tma_load_4d(sm + kDqOffG + kBox, &tmg, 64, i0, h, b, q_full, pol);
     if constexpr (!WIN) {  // (with a window the first key tile is known only from the positions)
       mbar_arrive_expect_tx(&k_full[0], kTileBytes);
-      tma_load_4d(sm + kDqOffK, &tmk, 0, 0, hk, b, &k_full[0], pol);
-      tma_load_4d(sm + kDqOffK + kBox, &tmk, 64, 0, hk, b, &k_full[0], pol);
+      tma_load_4d(sm + kDqOffK, &tmk, 0, 0, hk, b, &k_full[0], pol_ring);
+      tma_load_4d(sm + kDqOffK + kBox, &tmk, 64, 0, hk, b, &k_full[0], pol_ring);
       mbar_arrive_expect_tx(&v_full[0], kTileBytes);
-      tma_load_4d(sm + kDqOffV, &tmv, 0, 0, hk, b, &v_full[0], pol);
-      tma_load_4d(sm + kDqOffV + kBox, &tmv, 64, 0, hk, b, &v_full[0], pol);
+      tma_load_4d(sm + kDqOffV, &tmv, 0, 0, hk, b, &v_full[0], pol_ring);
+      tma_load_4d(sm + kDqOffV + kBox, &tmv, 64, 0, hk, b, &v_full[0], pol_ring);
     }
   }
 
@@ -559,13 +560,13 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
         const int key0 = (j_lo + j) * BT;
         if (j >= KST && !mbar_wait(&k_empty[sk], ((j / KST) - 1) & 1)) { ok = false; break; }
         mbar_arrive_expect_tx(&k_full[sk], kTileBytes);
-        tma_load_4d(sm + kDqOffK + sk * kTileBytes, &tmk, 0, key0, hk, b, &k_full[sk], pol);
-        tma_load_4d(sm + kDqOffK + sk * kTileBytes + kBox, &tmk, 64, key0, hk, b, &k_full[sk], pol);
+        tma_load_4d(sm + kDqOffK + sk * kTileBytes, &tmk, 0, key0, hk, b, &k_full[sk], pol_ring);
+        tma_load_4d(sm + kDqOffK + sk * kTileBytes + kBox, &tmk, 64, key0, hk, b, &k_full[sk], pol_ring);
         k_issued = j + 1;
         if (j >= STAGES && !mbar_wait(&v_empty[sv], ((j / STAGES) - 1) & 1)) { ok = false; break; }
         mbar_arrive_expect_tx(&v_full[sv], kTileBytes);
-        tma_load_4d(sm + kDqOffV + sv * kTileBytes, &tmv, 0, key0, hk, b, &v_full[sv], pol);
-        tma_load_4d(sm + kDqOffV + sv * kTileBytes + kBox, &tmv, 64, key0, hk, b, &v_full[sv], pol);
+        tma_load_4d(sm + kDqOffV + sv * kTileBytes, &tmv, 0, key0, hk, b, &v_full[sv], pol_ring);
+        tma_load_4d(sm + kDqOffV + sv * kTileBytes + kBox, &tmv, 64, key0, hk, b, &v_full[sv], pol_ring);
         v_issued = j + 1;
         if (j + 1 < n && j + 1 >= STAGES) {
           // the next tile's copies wait for slots: bring it into L2 now
@@ -845,6 +846,7 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
   const uint32_t sK = smem_u32(sm + kOffA0), sV = smem_u32(sm + kOffA1);
   const uint32_t sQ = smem_u32(sm + kOffR0), sG = smem_u32(sm + kOffR1);
   const uint64_t pol = policy_evict_first();
+  const uint64_t pol_ring = policy_evict_last();  // Q/G_O tiles: re-read by the head's other key tiles
   Visit first{-1, -1};
   const bool any = next_visit<WIN>(p, ends, starts, k0, first);
 
@@ -864,10 +866,10 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
         const int h = hk * p.G + v.g;
         const int row = v.qt * BT;
         mbar_arrive_expect_tx(&qg_full[s], 2 * kTileBytes);
-        tma_load_4d(sm + kOffR0 + s * kTileBytes, &tmq, 0, row, h, b, &qg_full[s], pol);
-        tma_load_4d(sm + kOffR0 + s * kTileBytes + kBox, &tmq, 64, row, h, b, &qg_full[s], pol);
-        tma_load_4d(sm + kOffR1 + s * kTileBytes, &tmg, 0, row, h, b, &qg_full[s], pol);
-        tma_load_4d(sm + kOffR1 + s * kTileBytes + kBox, &tmg, 64, row, h, b, &qg_full[s], pol);
+        tma_load_4d(sm + kOffR0 + s * kTileBytes, &tmq, 0, row, h, b, &qg_full[s], pol_ring);
+        tma_load_4d(sm + kOffR0 + s * kTileBytes + kBox, &tmq, 64, row, h, b, &qg_full[s], pol_ring);
+        tma_load_4d(sm + kOffR1 + s * kTileBytes, &tmg, 0, row, h, b, &qg_full[s], pol_ring);
+        tma_load_4d(sm + kOffR1 + s * kTileBytes + kBox, &tmg, 64, row, h, b, &qg_full[s], pol_ring);
         ++t;
         Visit vn = v;
         if (t >= STAGES && next_visit<WIN>(p, ends, starts, k0, vn)) {
