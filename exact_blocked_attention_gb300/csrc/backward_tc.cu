@@ -27,12 +27,16 @@
 // S and G_P are formed twice (7 products of 128 x 128 x 128 per tile pair
 // instead of 5).
 //
-// Roles in kernels 2 and 3 (352 threads): warps 0-7 one thread per TMEM lane
-// and half tile: group g = warp / 4 owns columns [64 g, 64 g + 64) of every
-// tile (keys in 2, query rows in 3), lane quarter warp % 4; warp 8 the TMA
-// producer; warp 9 TMEM allocation and the thread that issues the
-// accumulating products; warp 10 the thread that issues the S and G_P
-// products.  (One thread issues a product every ~75 cycles; an N = 64
+// Roles in kernel 2 (352 threads): warps 0-7 one thread per TMEM lane and
+// half tile: group g = warp / 4 owns key columns [64 g, 64 g + 64) of every
+// tile, lane quarter warp % 4; warp 8 the TMA producer; warp 9 TMEM
+// allocation and the thread that issues the accumulating products; warp 10
+// the thread that issues the S and G_P products.  Kernel 3 (608 threads) has
+// 16 row warps: group g = warp / 4 owns query columns [32 g, 32 g + 32) (half
+// g / 2), then the producer (16), the accumulating thread (17) and the score
+// thread (18); each group writes its P^T and G_S^T into the first 16 of its
+// own 32 columns, so the A operand of half h is two 16-column pieces 32
+// columns apart.  (One thread issues a product every ~75 cycles; an N = 64
 // product's math takes ~32, and two issuing threads get one every ~49.)
 // In dQ, S and G_P are whole-tile products (N = 128) and the rows read them
 // out of TMEM at once: the next tile's S (G_P) is issued as soon as every row
@@ -44,7 +48,7 @@
 // j had completed, and the copies' latency set the kernel's pace.
 // In dK/dV (tensor memory full: S^T, G_P^T, G_V, G_K) the products of a tile
 // are issued by half (N = 64 for S^T and G_P^T, K = 64 for the accumulating
-// ones), each half with its own barriers, so one group's exponentials
+// ones), each half with its own barriers, so one half's exponentials
 // overlap the tensor core's work on the other half.  The next tile's half g
 // overwrites the columns the accumulating products of half g read, so its
 // S^T and G_P^T wait until those products have completed (a barrier per
@@ -82,6 +86,15 @@ constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;    // the accumulating products (and TMEM allocation)
 constexpr int kScoreWarp = 10; // the S and G_P products
 constexpr int kThreads = 352;
+// dK/dV kernel: 16 row warps (a lane quarter and 32 query columns each; the
+// four warps of a quarter-group g own columns [32 g, 32 g + 32), half g / 2),
+// then the producer, the accumulating thread (and TMEM allocation) and the
+// score thread
+constexpr int kKvRowWarps = 16;
+constexpr int kKvTmaWarp = 16;
+constexpr int kKvMmaWarp = 17;
+constexpr int kKvScoreWarp = 18;
+constexpr int kKvThreads = 32 * 19;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescHalf = tc::idesc_bf16(128, HT, 0, 0);  // S half: both K-major, N = 64
 constexpr uint32_t kIdescTN = tc::idesc_bf16(128, 128, 0, 1);   // A in TMEM, B N-major, N = 128
@@ -150,6 +163,36 @@ __device__ __forceinline__ void store_rows(uint32_t col, float mul, float* stg, 
 
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
+// One warp's 32 rows x 32 columns of an fp32 accumulator (TMEM columns
+// col..col + 31) times mul, to rows dst0 + r * row_stride, the first `rows`
+// of them: staged through shared memory (rows padded to 36 floats) so that
+// the global stores are 8 lanes to a row, 128 contiguous bytes each.
+constexpr int kStage32Row = 32 + 4;
+constexpr int kStage32Warp = 32 * kStage32Row;  // floats
+static_assert(kKvRowWarps * kStage32Warp * 4 <= 2 * STAGES * kTileBytes, "dK/dV staging fits the rings");
+__device__ __forceinline__ void store_rows32(uint32_t col, float mul, float* stg, float* dst0, int64_t row_stride,
+                                             int rows, int lane) {
+  uint32_t r[32];
+  tc::ld32(col, r);
+  tc::wait_ld();
+#pragma unroll
+  for (int c = 0; c < 32; c += 4)
+    *reinterpret_cast<float4*>(stg + lane * kStage32Row + c) =
+        make_float4(__uint_as_float(r[c]) * mul, __uint_as_float(r[c + 1]) * mul, __uint_as_float(r[c + 2]) * mul,
+                    __uint_as_float(r[c + 3]) * mul);
+  __syncwarp();
+#pragma unroll 4
+  for (int it = 0; it < 8; ++it) {
+    const int rr = 4 * it + (lane >> 3);
+    if (rr < rows)
+      *reinterpret_cast<float4*>(dst0 + rr * row_stride + 4 * (lane & 7)) =
+          *reinterpret_cast<const float4*>(stg + rr * kStage32Row + 4 * (lane & 7));
+  }
+  __syncwarp();  // the staging rows are read before they are written again
+}
+
+
+
 // Half g of S = A B^T over d = 128: A = 128 rows (all), B = rows [64 g, 64 g
 // + 64) of a 128-row tile; both K-major, 128-byte swizzled (rows 64.. start
 // 8 KB into each 64-dim box, a whole number of 8-row atoms).
@@ -187,6 +230,20 @@ __device__ __forceinline__ void issue_acc(uint32_t dcol, uint32_t acol, uint32_t
   for (int ks = 0; ks < HT / 16; ++ks) {
     const uint64_t bdesc = tc::desc_join(blo + (uint32_t)((g * 4 + ks) * 16 * 128 >> 4), kHi);
     tc::mma_ts(dcol, acol + 8 * ks, bdesc, kIdescTN, (accumulate || ks > 0) ? 1u : 0u);
+  }
+}
+
+// issue_acc for the dK/dV layout: the A operand of half g (64 contraction
+// rows, 32 bf16-pair columns) sits as two 16-column pieces 32 columns
+// apart (acol and acol + 32), one per row-warp group of the half.
+__device__ __forceinline__ void issue_acc_split(uint32_t dcol, uint32_t acol, uint32_t sb, int g, bool accumulate) {
+  const uint32_t blo = tc::desc_lo(sb, kBox);
+  constexpr uint32_t kHi = tc::desc_hi(1024);
+#pragma unroll
+  for (int ks = 0; ks < HT / 16; ++ks) {
+    const uint64_t bdesc = tc::desc_join(blo + (uint32_t)((g * 4 + ks) * 16 * 128 >> 4), kHi);
+    const uint32_t a = acol + (ks < 2 ? 8 * ks : 32 + 8 * (ks - 2));
+    tc::mma_ts(dcol, a, bdesc, kIdescTN, (accumulate || ks > 0) ? 1u : 0u);
   }
 }
 
@@ -302,8 +359,8 @@ __device__ __forceinline__ void tma_prefetch_l2_4d(const void* map, int c0, int 
 
 // TMEM set-up shared by the two tensor-core kernels (after thread 0 has
 // initialised the barriers): warp 9 allocates, everyone reads the base.
-__device__ __forceinline__ uint32_t setup_tmem(int* misc, int warp) {
-  if (warp == kMmaWarp) {
+__device__ __forceinline__ uint32_t setup_tmem(int* misc, int warp, int alloc_warp = kMmaWarp) {
+  if (warp == alloc_warp) {
     tc::alloc(reinterpret_cast<uint32_t*>(&misc[0]), kTmemCols);
     tc::relinquish();
   }
@@ -820,7 +877,7 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
   // the visit sequence is walked from shared memory (a global load per step
   // sat on the MMA thread's path between visits); published by the barrier
   // in setup_tmem
-  for (int i = threadIdx.x; i < p.n_qt; i += kThreads) {
+  for (int i = threadIdx.x; i < p.n_qt; i += kKvThreads) {
     ends[i] = p.ws_end[(int64_t)b * p.n_qt + i];
     if constexpr (WIN) starts[i] = p.ws_start[(int64_t)b * p.n_qt + i];
   }
@@ -834,15 +891,15 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
     for (int g = 0; g < 2; ++g) {
       mbar_init(&s_full[g], 1);
       mbar_init(&gp_full[g], 1);
-      mbar_init(&pt_full[g], 4);
-      mbar_init(&ds_full[g], 4);
+      mbar_init(&pt_full[g], 8);  // the 8 row warps of half g
+      mbar_init(&ds_full[g], 8);
       mbar_init(&dv_done[g], 1);
       mbar_init(&dk_done[g], 1);
     }
     mbar_init(drain, 2);
     fence_barrier_init();
   }
-  const uint32_t tb = setup_tmem(misc, warp);
+  const uint32_t tb = setup_tmem(misc, warp, kKvMmaWarp);
   const uint32_t sK = smem_u32(sm + kOffA0), sV = smem_u32(sm + kOffA1);
   const uint32_t sQ = smem_u32(sm + kOffR0), sG = smem_u32(sm + kOffR1);
   const uint64_t pol = policy_evict_first();
@@ -850,7 +907,7 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
   Visit first{-1, -1};
   const bool any = next_visit<WIN>(p, ends, starts, k0, first);
 
-  if (warp == kTmaWarp) {
+  if (warp == kKvTmaWarp) {
     if (lane == 0 && any) {
       bool ok = true;
       mbar_arrive_expect_tx(kv_full, 2 * kTileBytes);
@@ -886,7 +943,7 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
         if (!mbar_wait(&qg_full[u % STAGES], (u / STAGES) & 1)) ok = false;
       if (!ok) record_error(p.err, kErrTimeout);
     }
-  } else if (warp == kScoreWarp) {
+  } else if (warp == kKvScoreWarp) {
     // ---------------- S^T and G_P^T products (one thread) ----------------
     if (lane == 0 && any) {
       // S^T (G_P^T) of the query rows [64 g, 64 g + 64) of visit t
@@ -933,7 +990,7 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
       tc::commit(drain);
       if (!mbar_wait(drain, 0)) record_error(p.err, kErrTimeout);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kKvMmaWarp) {
     // ---------------- G_V += P^T G_O, G_K += G_S^T Q (one thread; a fixed order) ----------------
     if (lane == 0 && any) {
       bool ok = true;
@@ -946,19 +1003,19 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
         // then half 1 (this order every visit)
         if (!mbar_wait(&pt_full[0], ph)) { ok = false; break; }
         tc::fence_after();
-        issue_acc(tb + 256, tb + 0, sG + s * kTileBytes, 0, t > 0);
+        issue_acc_split(tb + 256, tb + 0, sG + s * kTileBytes, 0, t > 0);
         tc::commit(&dv_done[0]);
         if (!mbar_wait(&ds_full[0], ph)) { ok = false; break; }
         tc::fence_after();
-        issue_acc(tb + 384, tb + 128, sQ + s * kTileBytes, 0, t > 0);
+        issue_acc_split(tb + 384, tb + 128, sQ + s * kTileBytes, 0, t > 0);
         tc::commit(&dk_done[0]);
         if (!mbar_wait(&pt_full[1], ph)) { ok = false; break; }
         tc::fence_after();
-        issue_acc(tb + 256, tb + HT, sG + s * kTileBytes, 1, true);
+        issue_acc_split(tb + 256, tb + HT, sG + s * kTileBytes, 1, true);
         tc::commit(&dv_done[1]);
         if (!mbar_wait(&ds_full[1], ph)) { ok = false; break; }
         tc::fence_after();
-        issue_acc(tb + 384, tb + 128 + HT, sQ + s * kTileBytes, 1, true);
+        issue_acc_split(tb + 384, tb + 128 + HT, sQ + s * kTileBytes, 1, true);
         tc::commit(&dk_done[1]);
         // the visit's Q and G_O slot is free: its halves completed before its P^T was written
         tc::commit(&qg_empty[s]);
@@ -969,8 +1026,9 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
       if (!mbar_wait(drain, 0)) record_error(p.err, kErrTimeout);
     }
   } else {
-    // ---------------- keys x half tile: P^T, G_S^T ----------------
-    const int grp = warp >> 2;
+    // ---------------- keys x 32 query columns: P^T, G_S^T ----------------
+    const int grp = warp >> 2;  // columns [32 grp, 32 grp + 32): half hf = grp / 2
+    const int hf = grp >> 1;
     const int key = k0 + 32 * (warp & 3) + lane;
     const uint32_t tl = tb + ((uint32_t)(32 * (warp & 3)) << 16);
     const int len = seq_len(p, b);
@@ -984,10 +1042,10 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
       Visit v = first;
       for (int t = 0;; ++t) {
         const int h = hk * p.G + v.g;
-        float4* f = facts + (t & 1) * 128 + grp * HT;
-        if (t128 < HT) {
-          // the facts of this half's query rows, one row per thread
-          const int i = v.qt * BT + grp * HT + t128;
+        float4* f = facts + (t & 1) * 128 + grp * 32;
+        if (t128 < 32) {
+          // the facts of this group's query rows, one row per thread
+          const int i = v.qt * BT + grp * 32 + t128;
           float4 e = make_float4(-__builtin_huge_valf(), 0.f, __int_as_float(0), __int_as_float(0));
           if (i < p.Tq) {
             const int64_t r = ((int64_t)b * p.Hq + h) * p.Tq + i;
@@ -995,101 +1053,96 @@ __device__ __forceinline__ void dkv_body(const BwdParams& p, const CUtensorMap& 
                             __int_as_float(WIN ? row_start(p, b, i) : 0));
           }
           f[t128] = e;
-          // the smallest row end (and largest row start) of the half (two warps of 32 rows)
+          // the smallest row end (and largest row start) of the group's rows
           const int mn = __reduce_min_sync(0xffffffffu, __float_as_int(e.z));
-          if (lane == 0) misc[4 + (t & 1) * 4 + grp * 2 + (t128 >> 5)] = mn;
+          if (lane == 0) misc[4 + (t & 1) * 4 + grp] = mn;
           if constexpr (WIN) {
             const int mx = __reduce_max_sync(0xffffffffu, __float_as_int(e.w));
-            if (lane == 0) misc[12 + (t & 1) * 4 + grp * 2 + (t128 >> 5)] = mx;
+            if (lane == 0) misc[12 + (t & 1) * 4 + grp] = mx;
           }
         }
         // (the barrier also publishes the facts; the answer is the same for
         // the group's 128 threads, so none is left at a later barrier)
-        if (!bar_and(1 + grp, 128, wait_all(&s_full[grp], t & 1))) { ok = false; break; }
+        if (!bar_and(1 + grp, 128, wait_all(&s_full[hf], t & 1))) { ok = false; break; }
         tc::fence_after();
         const float* bcol = nullptr;
         if constexpr (BIAS)
           bcol = p.bias + (int64_t)b * p.bi_sb + (int64_t)h * p.bi_sh +
-                 (int64_t)(v.qt * BT + grp * HT) * p.bi_si + (int64_t)key * p.bi_sj;
-        // (warp-uniform) every row of the half sees every key of the warp
-        const int* mn = misc + 4 + (t & 1) * 4 + grp * 2;
-        const int* mx = misc + 12 + (t & 1) * 4 + grp * 2;
-        const bool whole =
-            !BIAS && __all_sync(0xffffffffu, key < min(mn[0], mn[1]) && (!WIN || key >= max(mx[0], mx[1])));
-        const int rows_left = p.Tq - (v.qt * BT + grp * HT);  // rows of the half inside T_q
-        // step 1: P^T from S^T (G_P^T may still be in the tensor pipe)
-        uint32_t pk[2][16], vis[2];
-#pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
+                 (int64_t)(v.qt * BT + grp * 32) * p.bi_si + (int64_t)key * p.bi_sj;
+        // (warp-uniform) every row of the group sees every key of the warp
+        const int mn = misc[4 + (t & 1) * 4 + grp];
+        const int mx = misc[12 + (t & 1) * 4 + grp];
+        const bool whole = !BIAS && __all_sync(0xffffffffu, key < mn && (!WIN || key >= mx));
+        const int rows_left = p.Tq - (v.qt * BT + grp * 32);  // rows of the group inside T_q
+        // step 1: P^T from S^T (G_P^T may still be in the tensor pipe), into
+        // the first 16 of this group's own 32 columns
+        uint32_t pk[16], vis;
+        {
           uint32_t rs[32];
-          tc::ld32(tl + HT * grp + 32 * q2, rs);
+          tc::ld32(tl + 32 * grp, rs);
           tc::wait_ld();
-          const float* bq = BIAS ? bcol + (int64_t)(32 * q2) * p.bi_si : nullptr;
           if (whole)
-            vis[q2] = dkv_p<BIAS, false, WIN>(rs, f + 32 * q2, key, c2, bq, p.bi_si, rows_left - 32 * q2,
-                                              key < p.Tmax, pk[q2]);
+            vis = dkv_p<BIAS, false, WIN>(rs, f, key, c2, bcol, p.bi_si, rows_left, key < p.Tmax, pk);
           else
-            vis[q2] = dkv_p<BIAS, true, WIN>(rs, f + 32 * q2, key, c2, bq, p.bi_si, rows_left - 32 * q2,
-                                             key < p.Tmax, pk[q2]);
-          tc::st16(tl + HT * grp + 16 * q2, pk[q2]);  // P^T over S^T's first 32 columns of the half
+            vis = dkv_p<BIAS, true, WIN>(rs, f, key, c2, bcol, p.bi_si, rows_left, key < p.Tmax, pk);
+          tc::st16(tl + 32 * grp, pk);
         }
         tc::wait_st();
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&pt_full[grp]);
-        // step 2: G_S^T from G_P^T and P
-        if (!bar_and(1 + grp, 128, wait_all(&gp_full[grp], t & 1))) { ok = false; break; }
+        if (lane == 0) mbar_arrive(&pt_full[hf]);
+        // step 2: G_S^T from G_P^T and P, likewise over G_P^T's columns
+        if (!bar_and(1 + grp, 128, wait_all(&gp_full[hf], t & 1))) { ok = false; break; }
         tc::fence_after();
-#pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
+        {
           uint32_t rp[32], ds[16];
-          tc::ld32(tl + 128 + HT * grp + 32 * q2, rp);
+          tc::ld32(tl + 128 + 32 * grp, rp);
           tc::wait_ld();
           if (whole)
-            dkv_ds<false>(rp, pk[q2], vis[q2], f + 32 * q2, ds);
+            dkv_ds<false>(rp, pk, vis, f, ds);
           else
-            dkv_ds<true>(rp, pk[q2], vis[q2], f + 32 * q2, ds);
-          tc::st16(tl + 128 + HT * grp + 16 * q2, ds);  // G_S^T over G_P^T's first 32 columns
+            dkv_ds<true>(rp, pk, vis, f, ds);
+          tc::st16(tl + 128 + 32 * grp, ds);
         }
         tc::wait_st();
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ds_full[grp]);
+        if (lane == 0) mbar_arrive(&ds_full[hf]);
         if (!next_visit<WIN>(p, ends, starts, k0, v)) break;
       }
       if (ok && !wait_all(drain, 0)) ok = false;
     }
-    float* dv_row = p.dv + (int64_t)b * p.dv_sb + (int64_t)hk * p.dv_sh + (int64_t)key * p.dv_sj + grp * HT;
-    float* dk_row = p.dk + (int64_t)b * p.dk_sb + (int64_t)hk * p.dk_sh + (int64_t)key * p.dk_sj + grp * HT;
+    float* dv_row = p.dv + (int64_t)b * p.dv_sb + (int64_t)hk * p.dv_sh + (int64_t)key * p.dv_sj + grp * 32;
+    float* dk_row = p.dk + (int64_t)b * p.dk_sb + (int64_t)hk * p.dk_sh + (int64_t)key * p.dk_sj + grp * 32;
     if (!ok) {
       if (lane == 0) record_error(p.err, kErrTimeout);
     } else if (!any) {
       if (key < p.Tmax)
-        for (int c = 0; c < HT; c += 4) {
+        for (int c = 0; c < 32; c += 4) {
           *reinterpret_cast<float4*>(dv_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
           *reinterpret_cast<float4*>(dk_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     } else {
-      // this group stores dims [64 g, 64 g + 64) of G_V and G_K for the
-      // warp's keys, staged in the Q/G_O rings (every product has completed;
-      // the tensor-memory loads are warp-collective: every lane takes part)
+      // this warp stores dims [32 grp, 32 grp + 32) of G_V and G_K for its
+      // keys, staged in the Q/G_O rings (every product has completed; the
+      // tensor-memory loads are warp-collective: every lane takes part)
       tc::fence_after();
       const int key_w = k0 + 32 * (warp & 3);
-      float* stg = reinterpret_cast<float*>(sm + (grp == 0 ? kOffR0 : kOffR1) + (warp & 3) * kStageWarp);
+      float* stg = reinterpret_cast<float*>(sm + kOffR0) + warp * kStage32Warp;
       const int rows = min(32, p.Tmax - key_w);
-      store_rows(tl + 256 + HT * grp, 1.f, stg,
-                 p.dv + (int64_t)b * p.dv_sb + (int64_t)hk * p.dv_sh + (int64_t)key_w * p.dv_sj + grp * HT, p.dv_sj,
-                 rows, lane);
-      store_rows(tl + 256 + 128 + HT * grp, p.scale, stg,
-                 p.dk + (int64_t)b * p.dk_sb + (int64_t)hk * p.dk_sh + (int64_t)key_w * p.dk_sj + grp * HT, p.dk_sj,
-                 rows, lane);
+      store_rows32(tl + 256 + 32 * grp, 1.f, stg,
+                   p.dv + (int64_t)b * p.dv_sb + (int64_t)hk * p.dv_sh + (int64_t)key_w * p.dv_sj + grp * 32, p.dv_sj,
+                   rows, lane);
+      store_rows32(tl + 384 + 32 * grp, p.scale, stg,
+                   p.dk + (int64_t)b * p.dk_sb + (int64_t)hk * p.dk_sh + (int64_t)key_w * p.dk_sj + grp * 32, p.dk_sj,
+                   rows, lane);
     }
   }
 
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  if (warp == kMmaWarp) tc::dealloc(tb, kTmemCols);
+  if (warp == kKvMmaWarp) tc::dealloc(tb, kTmemCols);
 }
 
 template <bool BIAS, bool WIN>
@@ -1099,7 +1152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   dq_body<BIAS, WIN>(p, tmq, tmg, tmk, tmv, (int)blockIdx.x);
 }
 template <bool BIAS, bool WIN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kKvThreads, 1)
     dkv_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmg,
                const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
   dkv_body<BIAS, WIN>(p, tmq, tmg, tmk, tmv, (int)blockIdx.x);
@@ -1125,7 +1178,7 @@ cudaError_t launch_pair(const BwdParams& p, const CUtensorMap& tmq, const CUtens
     dq_kernel<BIAS, WIN><<<(unsigned)dq_blocks, kThreads, kDqSmemBytes, stream>>>(p, tmq, tmg, tmk, tmv);
     if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
   }
-  dkv_kernel<BIAS, WIN><<<(unsigned)dkv_blocks, kThreads, kSmemBytes, stream>>>(p, tmq, tmg, tmk, tmv);
+  dkv_kernel<BIAS, WIN><<<(unsigned)dkv_blocks, kKvThreads, kSmemBytes, stream>>>(p, tmq, tmg, tmk, tmv);
   return cudaGetLastError();
 }
 
