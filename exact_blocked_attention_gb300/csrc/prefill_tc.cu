@@ -96,6 +96,13 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return pol;
 }
 
+// The first key tile of a CTA whose first row is at position q0 under a
+// sliding window (rows at their own index, the prefill layout).
+__device__ __forceinline__ int spec_first_tile(int q0, int window) {
+  const int64_t s0 = (int64_t)q0 - (int64_t)window + 1;
+  return s0 > 0 ? (int)(s0 / BN) : 0;
+}
+
 template <bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmq,
@@ -175,14 +182,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_4d(sm + kOffQ + t * kTileBytes, &tmq, 0, q0 + t * BM, h, b, q_full, pol_q);
       tma_load_4d(sm + kOffQ + t * kTileBytes + kBox, &tmq, 64, q0 + t * BM, h, b, q_full, pol_q);
     }
-    if constexpr (!WIN) {  // (with a window the first key tile is known only from the positions)
-      mbar_arrive_expect_tx(&k_full[0], kTileBytes);
-      tma_load_4d(sm + kOffK, &tmk, 0, 0, hk, b, &k_full[0], pol_kv);
-      tma_load_4d(sm + kOffK + kBox, &tmk, 64, 0, hk, b, &k_full[0], pol_kv);
-      mbar_arrive_expect_tx(&v_full[0], kTileBytes);
-      tma_load_4d(sm + kOffV, &tmv, 0, 0, hk, b, &v_full[0], pol_kv);
-      tma_load_4d(sm + kOffV + kBox, &tmv, 64, 0, hk, b, &v_full[0], pol_kv);
-    }
+    // K/V tile 0 of the CTA's range right away; with a window the range
+    // starts at the key tile of the CTA's earliest visible key, known only
+    // from the positions, so the copy goes to the tile that rows at positions
+    // q0 + r would start at (ring position 0; if the positions say otherwise,
+    // the CTA's tiles start at ring position 1 and this copy is dropped)
+    const int key_first = WIN ? spec_first_tile(2 * pair * BM, p.window) * BN : 0;
+    mbar_arrive_expect_tx(&k_full[0], kTileBytes);
+    tma_load_4d(sm + kOffK, &tmk, 0, key_first, hk, b, &k_full[0], pol_kv);
+    tma_load_4d(sm + kOffK + kBox, &tmk, 64, key_first, hk, b, &k_full[0], pol_kv);
+    mbar_arrive_expect_tx(&v_full[0], kTileBytes);
+    tma_load_4d(sm + kOffV, &tmv, 0, key_first, hk, b, &v_full[0], pol_kv);
+    tma_load_4d(sm + kOffV + kBox, &tmv, 64, key_first, hk, b, &v_full[0], pol_kv);
   }
 
   // ---- visibility of the rows (integers) ----
@@ -228,6 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int j_lo = !WIN ? 0 : (n_t0 == 0 ? f_t1 : (n_t1 == 0 ? f_t0 : min(f_t0, f_t1)));
   const int j_hi = max(e_t0, e_t1);
   const int n_max = j_hi - j_lo;  // key tiles the CTA loads
+  // ring position of the CTA's key tile j: j + ro (ro = 1 when the copy made
+  // before the positions were read holds another tile)
+  const int ro = (WIN && j_lo != spec_first_tile(2 * pair * BM, p.window)) ? 1 : 0;
   const int cta_end = max(n_t0 > 0 ? misc[1] : 0, n_t1 > 0 ? misc[3] : 0);
   const int64_t out_row = (int64_t)b * p.o_sb + (int64_t)h * p.o_sh + (int64_t)row_i * p.o_si;
   const int64_t lse_idx = (int64_t)b * p.l_sb + (int64_t)h * p.l_sh + (int64_t)row_i * p.l_si;
@@ -252,34 +266,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (my_row) write_empty_row();
     if (warp == kTmaWarp && lane == 0) {
       bool landed = mbar_wait(q_full, 0);
-      if constexpr (!WIN) {
-        landed = mbar_wait(&k_full[0], 0) && landed;
-        landed = mbar_wait(&v_full[0], 0) && landed;
-      }
+      landed = mbar_wait(&k_full[0], 0) && landed;
+      landed = mbar_wait(&v_full[0], 0) && landed;
       if (!landed) record_error(p.err, kErrTimeout);
     }
   } else if (warp == kTmaWarp) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      // Q (and, without a window, K/V tile 0) are in flight already; u
-      // counts the CTA's key tiles from j_lo
-      int k_issued = WIN ? 0 : 1, v_issued = WIN ? 0 : 1;
+      // Q and ring position 0 are in flight already; positions issued so far
+      int k_issued = 1, v_issued = 1;
       bool ok = true;
-      for (int j = WIN ? 0 : 1; j < n_max && ok; ++j) {
-        const int s = j % STAGES;
+      if (ro == 1) {
+        // position 0 holds another tile: it lands, then its slot is released
+        ok = mbar_wait(&k_full[0], 0) && mbar_wait(&v_full[0], 0);
+        mbar_arrive(&k_empty[0]);
+        mbar_arrive(&v_empty[0]);
+      }
+      for (int j = 1 - ro; j < n_max && ok; ++j) {
+        const int u = j + ro;
+        const int s = u % STAGES;
         const int key0 = (j_lo + j) * BN;
-        if (j >= STAGES && !mbar_wait(&k_empty[s], ((j / STAGES) - 1) & 1)) { ok = false; break; }
+        if (u >= STAGES && !mbar_wait(&k_empty[s], ((u / STAGES) - 1) & 1)) { ok = false; break; }
         unsigned char* kd = sm + kOffK + s * kTileBytes;
         mbar_arrive_expect_tx(&k_full[s], kTileBytes);
         tma_load_4d(kd, &tmk, 0, key0, hk, b, &k_full[s], pol_kv);
         tma_load_4d(kd + kBox, &tmk, 64, key0, hk, b, &k_full[s], pol_kv);
-        k_issued = j + 1;
-        if (j >= STAGES && !mbar_wait(&v_empty[s], ((j / STAGES) - 1) & 1)) { ok = false; break; }
+        k_issued = u + 1;
+        if (u >= STAGES && !mbar_wait(&v_empty[s], ((u / STAGES) - 1) & 1)) { ok = false; break; }
         unsigned char* vd = sm + kOffV + s * kTileBytes;
         mbar_arrive_expect_tx(&v_full[s], kTileBytes);
         tma_load_4d(vd, &tmv, 0, key0, hk, b, &v_full[s], pol_kv);
         tma_load_4d(vd + kBox, &tmv, 64, key0, hk, b, &v_full[s], pol_kv);
-        v_issued = j + 1;
+        v_issued = u + 1;
       }
       // every issued copy must land before the CTA can exit
       if (!mbar_wait(q_full, 0)) ok = false;
@@ -299,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S_jj = Q_t K_jj^T into query tile t's S buffer
       auto issue_qk = [&](int t, int jj) {
         // descriptors: only the start address moves (split-word form)
-        const uint32_t klo = tc::desc_lo(sK + (jj % STAGES) * kTileBytes, 16);
+        const uint32_t klo = tc::desc_lo(sK + ((jj + ro) % STAGES) * kTileBytes, 16);
         const uint32_t qlo = tc::desc_lo(sQ + t * kTileBytes, 16);
         constexpr uint32_t kHi = tc::desc_hi(1024);
 #pragma unroll
@@ -316,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int min_end[QT] = {misc[2], misc[4]};
       const int win_max[QT] = {WIN ? misc[7] : 0, WIN ? misc[9] : 0};
       auto issue_pv = [&](int t, int jj, bool more) {
-        const uint32_t vlo = tc::desc_lo(sV + (jj % STAGES) * kTileBytes, kBox);
+        const uint32_t vlo = tc::desc_lo(sV + ((jj + ro) % STAGES) * kTileBytes, kBox);
         constexpr uint32_t kHi = tc::desc_hi(1024);
         const uint32_t tcol = tb + t * kTileCols;
         const int k0 = (j_lo + jj) * BN;
@@ -337,18 +355,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       // [a_t, a_t + n_t) of them, a_t = 0 without a window)
       const int a_t0 = f_t0 - j_lo, a_t1 = f_t1 - j_lo;
       // prologue: the first scores of the query tiles that start at j_lo
-      if (ok && !mbar_wait(&k_full[0], 0)) ok = false;
+      if (ok && !mbar_wait(&k_full[ro], 0)) ok = false;  // ring position ro < STAGES: phase 0
       if (ok) {
         tc::fence_after();
         if (n_t0 > 0 && a_t0 == 0) issue_qk(0, 0);
         if (n_t1 > 0 && a_t1 == 0) issue_qk(1, 0);
-        tc::commit(&k_empty[0]);
+        tc::commit(&k_empty[ro]);
       }
       for (int j = 0; ok && j < n_max; ++j) {
-        const int s = j % STAGES;
+        const int u = j + ro;  // ring position
+        const int s = u % STAGES;
         const bool next = j + 1 < n_max;
-        if (!mbar_wait(&v_full[s], (j / STAGES) & 1)) { ok = false; break; }
-        if (next && !mbar_wait(&k_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1)) { ok = false; break; }
+        if (!mbar_wait(&v_full[s], (u / STAGES) & 1)) { ok = false; break; }
+        if (next && !mbar_wait(&k_full[(u + 1) % STAGES], ((u + 1) / STAGES) & 1)) { ok = false; break; }
         for (int t = 0; t < QT && ok; ++t) {
           const int nt = t == 0 ? n_t0 : n_t1;
           const int at = t == 0 ? a_t0 : a_t1;
@@ -366,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         tc::commit(&v_empty[s]);                           // V_j free once these products complete
-        if (next) tc::commit(&k_empty[(j + 1) % STAGES]);  // K_{j+1} likewise
+        if (next) tc::commit(&k_empty[(u + 1) % STAGES]);  // K_{j+1} likewise
       }
       if (!ok) {
         record_error(p.err, kErrTimeout);
@@ -525,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (key0 + BN > cta_end) {
           // last tile of the CTA: zero the V rows past every visible key of
           // both query tiles (both may do it; the values are the same)
-          const int u = f_mine - j_lo + j;  // the CTA's key-tile count (ring position)
+          const int u = f_mine - j_lo + j + ro;  // ring position of this key tile
           const int s = u % STAGES;
           if (!wait_all(&v_full[s], (u / STAGES) & 1)) { ok = false; break; }
           unsigned char* vt = sm + kOffV + s * kTileBytes;
