@@ -488,6 +488,13 @@ __device__ __forceinline__ void dkv_ds(const uint32_t (&rp)[32], const uint32_t 
   }
 }
 
+// The first key tile of a dQ block whose first row is at position q0 under
+// a sliding window (rows at their own index, the prefill layout).
+__device__ __forceinline__ int dq_spec_first_tile(int q0, int window) {
+  const int64_t s0 = (int64_t)q0 - (int64_t)window + 1;
+  return s0 > 0 ? (int)(s0 / BT) : 0;
+}
+
 // ---------------------------------------------------------------- dQ
 template <bool BIAS, bool WIN>
 __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& tmq, const CUtensorMap& tmg,
@@ -557,14 +564,16 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
     tma_load_4d(sm + kDqOffQ + kBox, &tmq, 64, i0, h, b, q_full, pol);
     tma_load_4d(sm + kDqOffG, &tmg, 0, i0, h, b, q_full, pol);
     tma_load_4d(sm + kDqOffG + kBox, &tmg, 64, i0, h, b, q_full, pol);
-    if constexpr (!WIN) {  // (with a window the first key tile is known only from the positions)
-      mbar_arrive_expect_tx(&k_full[0], kTileBytes);
-      tma_load_4d(sm + kDqOffK, &tmk, 0, 0, hk, b, &k_full[0], pol_ring);
-      tma_load_4d(sm + kDqOffK + kBox, &tmk, 64, 0, hk, b, &k_full[0], pol_ring);
-      mbar_arrive_expect_tx(&v_full[0], kTileBytes);
-      tma_load_4d(sm + kDqOffV, &tmv, 0, 0, hk, b, &v_full[0], pol_ring);
-      tma_load_4d(sm + kDqOffV + kBox, &tmv, 64, 0, hk, b, &v_full[0], pol_ring);
-    }
+    // with a window the first key tile follows from the positions: the copy
+    // goes to the tile rows at their own index start at (ring position 0;
+    // another first tile moves the block's tiles one ring position on)
+    const int key_first = WIN ? dq_spec_first_tile(i0, p.window) * BT : 0;
+    mbar_arrive_expect_tx(&k_full[0], kTileBytes);
+    tma_load_4d(sm + kDqOffK, &tmk, 0, key_first, hk, b, &k_full[0], pol_ring);
+    tma_load_4d(sm + kDqOffK + kBox, &tmk, 64, key_first, hk, b, &k_full[0], pol_ring);
+    mbar_arrive_expect_tx(&v_full[0], kTileBytes);
+    tma_load_4d(sm + kDqOffV, &tmv, 0, key_first, hk, b, &v_full[0], pol_ring);
+    tma_load_4d(sm + kDqOffV + kBox, &tmv, 64, key_first, hk, b, &v_full[0], pol_ring);
   }
 
   const int len = seq_len(p, b);
@@ -590,6 +599,8 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
     j_lo = misc[2] != 0x7fffffff ? misc[2] / BT : 0;
     n = max(0, n - j_lo);
   }
+  // ring position of key tile j: j + ro (ro = 1 when the early copy holds another tile)
+  const int ro = (WIN && j_lo != dq_spec_first_tile(i0, p.window)) ? 1 : 0;
   const uint32_t sQ = smem_u32(sm + kDqOffQ), sG = smem_u32(sm + kDqOffG);
   const uint32_t sK = smem_u32(sm + kDqOffK), sV = smem_u32(sm + kDqOffV);
   const int grp = (warp >> 2) & 1;  // column half of a compute warp
@@ -601,31 +612,36 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
       for (int c = 0; c < HT; c += 4) *reinterpret_cast<float4*>(dq_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
     if (warp == kTmaWarp && lane == 0) {
       bool landed = mbar_wait(q_full, 0);
-      if constexpr (!WIN) {
-        landed = mbar_wait(&k_full[0], 0) && landed;
-        landed = mbar_wait(&v_full[0], 0) && landed;
-      }
+      landed = mbar_wait(&k_full[0], 0) && landed;
+      landed = mbar_wait(&v_full[0], 0) && landed;
       if (!landed) record_error(p.err, kErrTimeout);
     }
   } else if (warp == kTmaWarp) {
     if (lane == 0) {
-      // Q, G_O (and, without a window, K/V tile 0) are in flight already
-      int k_issued = WIN ? 0 : 1, v_issued = WIN ? 0 : 1;
+      // Q, G_O and ring position 0 are in flight already; positions issued
+      int k_issued = 1, v_issued = 1;
       bool ok = true;
-      for (int j = WIN ? 0 : 1; j < n && ok; ++j) {
-        const int sk = j % KST, sv = j % STAGES;
+      if (ro == 1) {
+        // position 0 holds another tile: it lands, then its slots are released
+        ok = mbar_wait(&k_full[0], 0) && mbar_wait(&v_full[0], 0);
+        mbar_arrive(&k_empty[0]);
+        mbar_arrive(&v_empty[0]);
+      }
+      for (int j = 1 - ro; j < n && ok; ++j) {
+        const int u = j + ro;
+        const int sk = u % KST, sv = u % STAGES;
         const int key0 = (j_lo + j) * BT;
-        if (j >= KST && !mbar_wait(&k_empty[sk], ((j / KST) - 1) & 1)) { ok = false; break; }
+        if (u >= KST && !mbar_wait(&k_empty[sk], ((u / KST) - 1) & 1)) { ok = false; break; }
         mbar_arrive_expect_tx(&k_full[sk], kTileBytes);
         tma_load_4d(sm + kDqOffK + sk * kTileBytes, &tmk, 0, key0, hk, b, &k_full[sk], pol_ring);
         tma_load_4d(sm + kDqOffK + sk * kTileBytes + kBox, &tmk, 64, key0, hk, b, &k_full[sk], pol_ring);
-        k_issued = j + 1;
-        if (j >= STAGES && !mbar_wait(&v_empty[sv], ((j / STAGES) - 1) & 1)) { ok = false; break; }
+        k_issued = u + 1;
+        if (u >= STAGES && !mbar_wait(&v_empty[sv], ((u / STAGES) - 1) & 1)) { ok = false; break; }
         mbar_arrive_expect_tx(&v_full[sv], kTileBytes);
         tma_load_4d(sm + kDqOffV + sv * kTileBytes, &tmv, 0, key0, hk, b, &v_full[sv], pol_ring);
         tma_load_4d(sm + kDqOffV + sv * kTileBytes + kBox, &tmv, 64, key0, hk, b, &v_full[sv], pol_ring);
-        v_issued = j + 1;
-        if (j + 1 < n && j + 1 >= STAGES) {
+        v_issued = u + 1;
+        if (j + 1 < n && u + 1 >= STAGES) {
           // the next tile's copies wait for slots: bring it into L2 now
           tma_prefetch_l2_4d(&tmk, 0, key0 + BT, hk, b);
           tma_prefetch_l2_4d(&tmk, 64, key0 + BT, hk, b);
@@ -645,26 +661,27 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
     // ---------------- S and G_P products (one thread) ----------------
     if (lane == 0) {
       auto tile_ready = [&](int j) -> bool {
-        const bool r = mbar_wait(&k_full[j % KST], (j / KST) & 1) && mbar_wait(&v_full[j % STAGES], (j / STAGES) & 1);
+        const int u = j + ro;
+        const bool r = mbar_wait(&k_full[u % KST], (u / KST) & 1) && mbar_wait(&v_full[u % STAGES], (u / STAGES) & 1);
         tc::fence_after();
         return r;
       };
       bool ok = mbar_wait(q_full, 0) && tile_ready(0);
       if (ok) {
-        issue_full(tb + 0, sQ, sK);
+        issue_full(tb + 0, sQ, sK + (ro % KST) * kTileBytes);
         tc::commit(s_full);
-        issue_full(tb + 128, sG, sV);
+        issue_full(tb + 128, sG, sV + (ro % STAGES) * kTileBytes);
         tc::commit(gp_full);
-        tc::commit(&v_empty[0]);
+        tc::commit(&v_empty[ro % STAGES]);
       }
       for (int j = 0; ok && j + 1 < n; ++j) {
         // tile j + 1's S (G_P) overwrites tile j's as soon as the rows have
         // read it; G_S has columns of its own
-        const int s1 = (j + 1) % STAGES;
+        const int s1 = (j + 1 + ro) % STAGES;
         if (!tile_ready(j + 1)) { ok = false; break; }
         if (!mbar_wait(s_free, j & 1)) { ok = false; break; }
         tc::fence_after();
-        issue_full(tb + 0, sQ, sK + ((j + 1) % KST) * kTileBytes);
+        issue_full(tb + 0, sQ, sK + ((j + 1 + ro) % KST) * kTileBytes);
         tc::commit(s_full);
         if (!mbar_wait(gp_free, j & 1)) { ok = false; break; }
         tc::fence_after();
@@ -681,7 +698,7 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
     if (lane == 0) {
       bool ok = true;
       for (int j = 0; ok && j < n; ++j) {
-        const int s = j % KST;
+        const int s = (j + ro) % KST;
         const int par = j & 1;
         if (!mbar_wait(&p_full[par], (j >> 1) & 1)) { ok = false; break; }
         tc::fence_after();
@@ -771,8 +788,8 @@ __device__ __forceinline__ void dq_body(const BwdParams& p, const CUtensorMap& t
       if ((j_lo + j) * BT + BT > cta_end) {
         // last tile: the K rows of this half past every visible key of the
         // CTA are zeroed before G_S K reads them (they may hold anything)
-        const int s = j % KST;
-        if (!wait_all(&k_full[s], (j / KST) & 1)) { ok = false; break; }
+        const int s = (j + ro) % KST;
+        if (!wait_all(&k_full[s], ((j + ro) / KST) & 1)) { ok = false; break; }
         unsigned char* kt = sm + kDqOffK + s * kTileBytes;
         const int z0 = max(cta_end - (j_lo + j) * BT, grp * HT);
         const int t = (int)(threadIdx.x & 127);
